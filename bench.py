@@ -1,0 +1,427 @@
+#!/usr/bin/env python3
+"""Benchmark of DeltaLog recurrent-state decode on GB300.
+
+One bench step = one full decode run of the workload: `tokens` decode tokens
+for every slot, i.e. `tokens` x (ReplayPrep + AppendDecode) launches, all
+inputs pre-generated in HBM.  Default workload: GDN decode at serving batch,
+B=256 slots, H=32 heads, d_k=d_v=128, fp32 state (512 MiB, larger than L2),
+512 tokens, merge interval M=16; the M sweep {1,4,8,16,32} and the in-house
+eager kernel are measured beside it.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload gdn|kda|rwkv6] [--M 16] [--no-sweep] [--no-cpu]
+
+Multi-GPU (torchrun): slots are independent, so every rank decodes its own
+batch shard with no collective on the data path (weak scaling); the timing
+is the max over ranks and the value sums all ranks' tokens·heads.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOADS = {
+    # name: op, B, H, d, tokens, M (headline), seed
+    "gdn": dict(op=0, B=256, H=32, d=128, tokens=512, M=16, seed=1001,
+                desc="GDN decode B=256 H=32 d_k=d_v=128 fp32 state, 512 tokens"),
+    "kda": dict(op=1, B=128, H=32, d=128, tokens=512, M=16, seed=1002,
+                desc="KDA decode B=128 H=32 d_k=d_v=128 fp32 state, 512 tokens"),
+    "rwkv6": dict(op=2, B=128, H=40, d=64, tokens=512, M=16, seed=1003,
+                  desc="RWKV6 decode B=128 H=40 head 64 fp32 state, 512 tokens"),
+}
+METRIC = "state-update tokens·heads/s and achieved HBM GB/s vs ~8 TB/s; write bytes/step"
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ------------------------------------------------------------ traffic model --
+def algorithmic_bytes(op, d, M, n):
+    """Algorithmic HBM bytes of one token for one slot-head with log length n
+    before the step, split by kernel: returns (replay_prep, append_decode,
+    append_decode_writes).  Counts each byte the step must move once:
+    AppendDecode reads the dense base (d_v*d_k*4), the value-side log rows
+    (n*d_v*4, bf16 for RWKV6), v_t (and k_t, q_t for GDN) and the coefficient
+    block; it writes o_t (bf16) and appends u_t (delta-rule ops), or on a merge
+    step writes the dense base back (and reads the key log rows for GDN).
+    ReplayPrep reads k_t, q_t, g_t, beta_t and the key log (and log-decay) rows,
+    writes the coefficient block and appends k_t, Λ_t (and v_t for RWKV6)."""
+    dk = dv = d
+    merge = (n + 1 == M)
+    Mcap = max(M - 1, 1)
+    Mcap4 = (Mcap + 3) // 4 * 4
+    perkey = op != 0
+    delta = op != 2
+    P0 = 8 + 2 * Mcap4 + (2 * dk if perkey else 0)
+    CB = P0 + (dk + M * dk if perkey else (M + 3) // 4 * 4)
+    coef = (CB if merge else P0) * 4
+    lw = dk * 4 if perkey else 4
+    # ReplayPrep
+    rp_r = 2 * dk * 2 + (dk * 4 if perkey else 4) + (4 if delta else 0) + n * (dk * 2 + lw)
+    if op == 2:
+        rp_r += dk * 4          # bonus
+    rp_w = coef + (0 if merge else dk * 2 + lw + (dv * 2 if op == 2 else 0))
+    # AppendDecode
+    esa = 4 if delta else 2
+    ad_r = dv * dk * 4 + n * dv * esa + coef + (dv * 2) + (2 * dk * 2 if op == 0 else 0)
+    if op == 0 and merge:
+        ad_r += (n + 1) * dk * 2 - dk * 2     # key log rows (k_t already counted)
+    ad_w = dv * 2 + (dv * dk * 4 if merge else (dv * 4 if delta else 0))
+    return rp_r + rp_w, ad_r + ad_w, rp_w + ad_w
+
+
+def eager_bytes(op, d):
+    dk = dv = d
+    r = dv * dk * 4 + 2 * dk * 2 + dv * 2 + (dk * 4 if op != 0 else 4) + (4 if op != 2 else 0)
+    if op == 2:
+        r += dk * 4
+    w = dv * dk * 4 + dv * 2
+    return r + w, w
+
+
+# --------------------------------------------------------------- clocks ------
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4)
+                          if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(self.rows)}
+
+
+# ------------------------------------------------------------ distributed ----
+def dist_setup(want):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world <= 1:
+        return 0, 1, None
+    import torch.distributed as dist
+    backend = "nccl" if want == "cuda" else "gloo"
+    dist.init_process_group(backend=backend)
+    return dist.get_rank(), dist.get_world_size(), dist
+
+
+def reduce_max(dist, value, device):
+    """Max of a float over ranks (identity when not distributed)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+# ------------------------------------------------------------- reference -----
+def run_reference(args):
+    """Reference arm: the fp64 oracle (C, OpenMP) on the host cores, timed on a
+    bounded sample of the same workload, reported in the same unit."""
+    rank, world, dist = dist_setup("cpu")
+    if rank != 0:
+        return 0
+    import torch
+    import oracle
+    from linear_attention_recurrent_gdn_gb300 import inputs as gen
+    w = WORKLOADS[args.workload]
+    sample_sh = int(os.environ.get("DL_REF_SLOT_HEADS", "256"))
+    tokens = int(os.environ.get("DL_REF_TOKENS", "64"))
+    oracle.build()
+    res = cpu_baseline(w, sample_sh, tokens, args.steps, args.warmup)
+    out = {"metric": METRIC, "value": res["value"], "unit": "tokens·heads/s", "n_gpus": 0,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic", "impl": "reference",
+           "config": {"workload": w["desc"] + " (oracle sample)", "op": gen.OP_NAMES[w["op"]],
+                      "B": w["B"], "H": w["H"], "d_k": w["d"], "d_v": w["d"],
+                      "tokens": w["tokens"], "M": w["M"]},
+           "cpu_baseline": {"value": res["value"], "unit": "tokens·heads/s",
+                            "cores": res["cores"], "kind": "oracle", "sample": res["sample"]},
+           "e2e": {"value": res["value"], "unit": "tokens·heads/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+    return 0
+
+
+def cpu_baseline(w, sample_sh, tokens, steps=1, warmup=0):
+    """Time the fp64 eager oracle on `sample_sh` slot-heads x `tokens` tokens of
+    the workload's input distributions (drawn on the CPU)."""
+    import torch
+    import oracle
+    from linear_attention_recurrent_gdn_gb300 import inputs as gen
+    op, d = w["op"], w["d"]
+    H = min(w["H"], sample_sh)
+    B = max(1, sample_sh // H)
+    x = gen.make_inputs(op, tokens, B, H, d, d, w["seed"])
+    S0 = gen.initial_state(B, H, d, d, w["seed"]).reshape(B * H, d, d).double().numpy()
+    f = lambda t: t.reshape((tokens, B * H) + t.shape[3:]).double().numpy()
+    if op == 2:
+        bonus = gen.rwkv6_bonus(H, d, w["seed"]).double().numpy()
+        extra = [bonus[h] for b in range(B) for h in range(H)]
+        import numpy as np
+        extra = np.stack(extra)
+        fn = oracle.rwkv6_eager
+    else:
+        extra = f(x["beta"])
+        fn = oracle.gdn_eager if op == 0 else oracle.kda_eager
+    args = (S0, f(x["q"]), f(x["k"]), f(x["v"]), f(x["g"]), extra)
+    for _ in range(warmup):
+        fn(*args)
+    times = []
+    for _ in range(max(1, steps)):
+        t0 = time.perf_counter()
+        fn(*args)
+        times.append(time.perf_counter() - t0)
+    t = statistics.median(times)
+    return {"value": B * H * tokens / t, "ms_per_step": t * 1e3, "cores": oracle.num_threads(),
+            "sample": "%d slot-heads x %d tokens of the workload (fp64 eager, median of %d)"
+                      % (B * H, tokens, len(times))}
+
+
+# ------------------------------------------------------------------ ours -----
+def run_ours(args):
+    import torch
+    if not torch.cuda.is_available():
+        print(json.dumps({"metric": METRIC, "error": "no CUDA device"}))
+        return 1
+    rank, world, dist = dist_setup("cuda")
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    from linear_attention_recurrent_gdn_gb300 import build
+    if rank == 0:
+        build.build()
+    barrier(dist)
+    from linear_attention_recurrent_gdn_gb300 import deltalog as dl
+    from linear_attention_recurrent_gdn_gb300 import inputs as gen
+
+    w = WORKLOADS[args.workload]
+    op, B, H, d, T = w["op"], w["B"], w["H"], w["d"], w["tokens"]
+    M = args.M or w["M"]
+    seed = w["seed"] + 7919 * rank      # each rank decodes its own batch shard
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+
+    t0 = time.time()
+    x = gen.make_inputs(op, T, B, H, d, d, seed, device=dev)
+    S0 = gen.initial_state(B, H, d, d, seed, device=dev)
+    bonus = gen.rwkv6_bonus(H, d, seed, device=dev) if op == 2 else None
+    out = torch.empty((T, B, H, d), dtype=torch.bfloat16, device=dev)
+    slots = list(range(B))
+    torch.cuda.synchronize()
+    log("inputs generated in %.1fs" % (time.time() - t0))
+
+    def make_ctx(m):
+        c = dl.DeltaLog(op, B, H, d, d, m, out_bf16=True, stream=stream.cuda_stream)
+        c.set_state(slots, S0)
+        if bonus is not None:
+            c.set_bonus(bonus)
+        return c
+
+    def decode_run(c, eager=False):
+        fn = c.step_eager if eager else c.step
+        for t in range(T):
+            fn(slots, x["q"][t], x["k"][t], x["v"][t], x["g"][t],
+               x["beta"][t] if x["beta"] is not None else None, out[t])
+
+    def timed(c, steps, warmup, eager=False):
+        for _ in range(warmup):
+            decode_run(c, eager)
+        barrier(dist)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            decode_run(c, eager)
+        e1.record(stream)
+        e1.synchronize()
+        torch.cuda.synchronize()
+        barrier(dist)
+        return e0.elapsed_time(e1) / steps     # ms per bench step
+
+    units_per_step = T * B * H                    # token·heads per rank per bench step
+
+    # ---- headline: DeltaLog at M
+    ctx = make_ctx(M)
+    with ClockSampler(local) as clk:
+        ms = timed(ctx, args.steps, args.warmup)
+    ms_max = reduce_max(dist, ms, dev)
+    value = units_per_step * world / (ms_max / 1e3)
+    launches = 2 * T * args.steps * ((B + 1023) // 1024)
+
+    # ---- per-kernel times (instrumented pass: events around every launch)
+    ctx.set_timing(True)
+    decode_run(ctx)
+    kms, kcnt = ctx.get_timing()
+    ctx.set_timing(False)
+    n_seq = [t % M for t in range(T)]
+    rp_b = ad_b = wr_all = 0
+    for n in n_seq:
+        a, b_, c_ = algorithmic_bytes(op, d, M, n)
+        rp_b += a * B * H
+        ad_b += b_ * B * H
+        wr_all += c_ * B * H
+    ad_ms = kms[1] / max(kcnt[1], 1)
+    rp_ms = kms[0] / max(kcnt[0], 1)
+    ad_gbs = ad_b / T / (ad_ms * 1e-3) / 1e9
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        peak, peak_src = float(peaks["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        peak, peak_src = 6800.0, "fallback"
+    step_bytes = (rp_b + ad_b) / T
+    ctx.close()
+
+    result = {
+        "metric": METRIC, "value": value, "unit": "tokens·heads/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": w["desc"] + ", merge interval M=%d" % M,
+                   "op": gen.OP_NAMES[op], "B": B, "H": H, "d_k": d, "d_v": d, "tokens": T,
+                   "M": M, "inputs": "bf16 q/k/v, fp32 g/beta, bf16 o",
+                   "l2": "inputs larger than L2 (fp32 state %d MiB per rank)"
+                         % (B * H * d * d * 4 >> 20),
+                   "parallelism": "replicas/batch shards x%d" % world},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "roofline": {"bound": "hbm", "achieved": ad_gbs, "peak": peak, "unit": "GB/s",
+                     "frac": ad_gbs / peak, "traffic": None,
+                     "kernel": "AppendDecode", "peak_source": peak_src + " hbm_gbs",
+                     "bytes_per_launch": ad_b / T, "ms_per_launch": ad_ms},
+        "kernels_ms_per_token": {"ReplayPrep": rp_ms, "AppendDecode": ad_ms},
+        "step_gbs": step_bytes / (ms_max / T * 1e-3) / 1e9,
+        "write_bytes_per_token": {"deltalog": wr_all / T,
+                                  "deltalog_state_only": B * H * d * d * 4 / M},
+    }
+
+    # ---- M sweep and the eager kernel (informational)
+    if not args.no_sweep:
+        sweep = {}
+        for m in (1, 4, 8, 16, 32):
+            c = make_ctx(m)
+            sms = reduce_max(dist, timed(c, 2, 1), dev)
+            sweep[str(m)] = units_per_step * world / (sms / 1e3)
+            c.close()
+        c = make_ctx(1)
+        ems = reduce_max(dist, timed(c, 2, 1, eager=True), dev)
+        c.close()
+        eb, ew = eager_bytes(op, d)
+        sweep["eager_kernel"] = units_per_step * world / (ems / 1e3)
+        result["m_sweep"] = sweep
+        result["eager_kernel_gbs"] = eb * B * H / (ems / T * 1e-3) / 1e9
+        result["write_bytes_per_token"]["eager"] = ew * B * H
+        result["write_cut_vs_eager"] = ew * B * H / result["write_bytes_per_token"]["deltalog"]
+        result["note_writes"] = "algorithmic bytes; DRAM-measured writes are in profiles/"
+
+    # ---- end to end through the public API with host buffers
+    pin = {k: (v.cpu().pin_memory() if v is not None else None) for k, v in x.items()}
+    hout = torch.empty((T, B, H, d), dtype=torch.bfloat16).pin_memory()
+    c = make_ctx(M)
+
+    def host_run():
+        for t in range(T):
+            c.step_host(slots, pin["q"][t], pin["k"][t], pin["v"][t], pin["g"][t],
+                        pin["beta"][t] if pin["beta"] is not None else None, hout[t])
+    for _ in range(args.warmup):
+        host_run()
+    barrier(dist)
+    t0 = time.perf_counter()
+    e2e_steps = max(1, min(args.steps, 5))
+    for _ in range(e2e_steps):
+        host_run()
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(dist, (time.perf_counter() - t0) * 1e3 / e2e_steps, dev)
+    c.close()
+    h2d = sum(v[0].numel() * v.element_size() for v in pin.values() if v is not None) * T
+    d2h = hout[0].numel() * hout.element_size() * T
+    result["e2e"] = {"value": units_per_step * world / (e2e_ms / 1e3), "unit": "tokens·heads/s",
+                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                     "ms_per_step": e2e_ms, "api": "dl_step_host"}
+
+    # ---- CPU baseline (rank 0, N = 1 only)
+    if rank == 0 and world == 1 and not args.no_cpu:
+        import oracle
+        oracle.build()
+        result["cpu_baseline"] = cpu_baseline(w, int(os.environ.get("DL_REF_SLOT_HEADS", "256")),
+                                              int(os.environ.get("DL_REF_TOKENS", "64")))
+        result["cpu_baseline"].update({"unit": "tokens·heads/s", "kind": "oracle"})
+        result["cpu_baseline"].pop("ms_per_step", None)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="gdn", choices=sorted(WORKLOADS))
+    ap.add_argument("--M", type=int, default=0)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,217 @@
+/*
+ * deltalog.h — C ABI of libdeltalog: deferred materialisation of the recurrent
+ * state in linear-attention decoding (DeltaLog), for Gated DeltaNet (GDN),
+ * Kimi Delta Attention (KDA) and RWKV6, on one GB300 GPU (sm_103a).
+ *
+ * What it computes.  Each slot (a request or a branch) and head holds a
+ * recurrent state S in R^{d_v x d_k}, stored value-major: S[v][i], row = value
+ * index, contiguous along d_k.  One decode token updates it and reads it out:
+ *
+ *   GDN    u_t = beta_t (v_t - alpha_t S_{t-1} k_t)        alpha_t = exp(g_t), one per head
+ *          S_t = alpha_t S_{t-1} + u_t k_t^T,   o_t = scale * S_t q_t
+ *   KDA    S_t = S_{t-1} Diag(alpha_t) (I - beta_t k_t k_t^T) + beta_t v_t k_t^T
+ *          (alpha_t = exp(g_t) one per key channel),       o_t = scale * S_t q_t
+ *   RWKV6  S_t = S_{t-1} Diag(w_t) + v_t k_t^T              w_t = exp(g_t) per key channel
+ *          o_t = scale * (S_{t-1} r_t + (sum_i r_i bonus_i k_i) v_t)
+ *
+ * (The RWKV6 rule is the key-major rule Z_t = Diag(w_t) Z_{t-1} + k_t v_t^T,
+ * o_t = r_t^T (Z_{t-1} + Diag(bonus) k_t v_t^T) with S = Z^T.)  The operator
+ * traits follow the DeltaLog page ("DeltaLog: Deferred Materialization of
+ * Recurrent States for Linear Attention Decoding"), section "Kernel
+ * implementation": GDN has a head-scalar decay and the delta-rule correction,
+ * KDA a per-key decay and the delta rule, RWKV6 a per-key decay and raw-value
+ * updates.
+ *
+ * How.  Section "Methodology — Base + Log" of the same page: the state is a
+ * dense base S̄ (history up to the last merge) plus a bounded log of compressed
+ * update factors with cumulative log-decay metadata.  For M-1 tokens a step
+ * reads S̄ but does not rewrite it; it appends its factors (value side u_t,
+ * or v_t for RWKV6; key side k_t; log-decay Λ_t) to the log.  Every M-th token
+ * of a slot is a merge step: the same kernel also writes base + replayed log
+ * back into S̄ and clears the log.  M = 1 is eager decoding.  The results are
+ * those of the eager rules above, up to floating-point rounding order.
+ * Section "Kernel implementation — Staged execution": per step a ReplayPrep
+ * kernel computes the per slot-head coefficients once, and a value-tiled
+ * AppendDecode kernel streams S̄ in value-row tiles, each with its shard of
+ * the value-side log.
+ *
+ * Forking.  The Flide page ("같은 맥락에서 여러 판단을 빠르게 처리하는 Flide",
+ * section "Research method step by step", second step) runs a shared context
+ * once, saves the final recurrent state, and starts every question branch from
+ * its own request's saved state by indexing it.  dl_fork does this: a branch
+ * points at the source's dense base (no copy) and gets a copy of its log; the
+ * branch writes a private base at its first merge.  A slot whose base is
+ * indexed by another slot is frozen until every such branch has merged.
+ *
+ * Conventions for every call below.
+ *   - Slot ids (int32) are HOST arrays; each call validates them on the host
+ *     before anything is enqueued: every id in [0, num_slots), no id twice in
+ *     one call.  An invalid argument returns DL_EINVAL and changes nothing;
+ *     a frozen slot returns DL_EBUSY and changes nothing.
+ *   - Every tensor pointer is a DEVICE pointer on the context's device,
+ *     16-byte aligned, C-contiguous, owned by the caller, and must stay valid
+ *     until the work enqueued on the context's stream has run.  Rows of
+ *     per-token tensors follow the order of the slot list.
+ *   - Work is enqueued asynchronously on the context's CUDA stream; calls that
+ *     return host data (dl_get_meta, dl_get_timing, dl_sync) synchronise it.
+ *   - bf16 tensors are raw IEEE bfloat16 (uint16 storage).
+ *   - Errors: a CUDA error returns DL_ECUDA; a device-side error (a kernel
+ *     gave up a bounded wait) is recorded in a device status word and returned
+ *     as DL_EDEVICE by the next synchronising call.  Both are sticky for the
+ *     context.  dl_last_error() gives a one-line description.  No exception
+ *     crosses this interface.
+ *   - A context is not thread-safe; use one per host thread.
+ */
+#ifndef DELTALOG_H
+#define DELTALOG_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DL_ABI_VERSION 1
+
+typedef enum dl_status {
+    DL_OK = 0,
+    DL_EINVAL = 1,       /* bad argument (range, duplicate, shape, alignment, NULL) */
+    DL_ENOMEM = 2,       /* device or host allocation failed                        */
+    DL_ECUDA = 3,        /* a CUDA runtime call failed                              */
+    DL_EBUSY = 4,        /* slot frozen: its base is indexed by a forked branch     */
+    DL_EDEVICE = 5,      /* a kernel reported an error through the status word      */
+    DL_EUNSUPPORTED = 6  /* configuration this build has no kernel for              */
+} dl_status;
+
+typedef enum dl_op { DL_GDN = 0, DL_KDA = 1, DL_RWKV6 = 2 } dl_op;
+
+typedef struct dl_config {
+    int32_t op;              /* dl_op                                                   */
+    int32_t num_slots;       /* state slots (requests + branches), >= 1                 */
+    int32_t num_heads;       /* H, >= 1                                                 */
+    int32_t d_k;             /* key dimension: 64 or 128                                */
+    int32_t d_v;             /* value dimension: equal to d_k in this build             */
+    int32_t merge_interval;  /* M in [1, 32]; 1 = eager (every step merges)             */
+    int32_t out_bf16;        /* 1: o is bf16; 0: o is fp32                              */
+    float scale;             /* output scale (1.0 for the decode workloads)             */
+} dl_config;
+
+/* ------------------------------------------------------------------------ */
+/* Host bookkeeping (no GPU needed).  This is the slot table every context   */
+/* keeps: per slot the log length n (0 <= n < M), the slot whose dense base  */
+/* it reads (base_of), and how many other slots index its base (refs).       */
+/* The rules are those stated for dl_step / dl_fork / dl_set_state /          */
+/* dl_merge below; the table is exposed so that callers (and tests) can plan */
+/* and check them without a device.                                           */
+/* ------------------------------------------------------------------------ */
+typedef struct dl_table dl_table;
+
+/* Create a table of num_slots slots, all with n = 0 and base_of[s] = s. */
+dl_status dl_table_create(int32_t num_slots, int32_t merge_interval, dl_table **out);
+void dl_table_destroy(dl_table *t);
+/* Advance the listed slots by one token.  If plan != NULL it receives, per
+ * slot in argument order, 4 int32: slot, base read this step, n before the
+ * step, 1 if this step is the slot's merge step.  A merge step resets n to 0
+ * and makes the slot own its base (base_of[s] = s). */
+dl_status dl_table_step(dl_table *t, const int32_t *slots, int32_t n, int32_t *plan);
+/* Validate an eager step: each slot must own its base and have n == 0. */
+dl_status dl_table_step_eager(dl_table *t, const int32_t *slots, int32_t n);
+/* Fork: each dst releases whatever base it indexed, then indexes src's base and
+ * takes src's log length.  dst must not contain src nor a frozen slot. */
+dl_status dl_table_fork(dl_table *t, int32_t src, const int32_t *dsts, int32_t n);
+/* Re-seed or merge: each slot releases its base reference, owns its base, n = 0. */
+dl_status dl_table_reset(dl_table *t, const int32_t *slots, int32_t n);
+/* Validate a slot list (range, duplicates). */
+dl_status dl_table_check(const dl_table *t, const int32_t *slots, int32_t n);
+/* Copy out the table; any pointer may be NULL.  Arrays have num_slots entries. */
+dl_status dl_table_get(const dl_table *t, int32_t *n_log, int32_t *base_of, int32_t *refs);
+
+/* ------------------------------------------------------------------------ */
+/* Device context                                                            */
+/* ------------------------------------------------------------------------ */
+typedef struct dl_ctx dl_ctx;
+
+/* Allocate, on the current CUDA device, the dense bases S̄ [num_slots, H, d_v,
+ * d_k] fp32 (zeroed), the bounded log (value side [num_slots, H, M-1, d_v]
+ * fp32, or bf16 for RWKV6; keys [num_slots, H, M-1, d_k] bf16; cumulative
+ * log-decay [num_slots, H, M-1] or [num_slots, H, M-1, d_k] fp32), the slot
+ * table on host and device, and per-step scratch.  stream is a cudaStream_t
+ * (NULL = legacy default stream).  On failure *out is NULL. */
+dl_status dl_create(const dl_config *cfg, void *stream, dl_ctx **out);
+/* Synchronise the stream, free everything.  NULL is accepted. */
+dl_status dl_destroy(dl_ctx *ctx);
+/* Use another stream for subsequent calls (the caller orders the two). */
+dl_status dl_set_stream(dl_ctx *ctx, void *stream);
+
+/* Load initial states: S [n, H, d_v, d_k] fp32 device -> S̄ of the listed slots;
+ * their logs are emptied (n = 0) and they own their bases again. */
+dl_status dl_set_state(dl_ctx *ctx, const int32_t *slots, int32_t n, const float *S);
+
+/* RWKV6 only: the per-head bonus, [H, d_k] fp32 device (copied). */
+dl_status dl_set_bonus(dl_ctx *ctx, const float *bonus);
+
+/* Flide-style fork of src into each dst (see above): no dense state is copied;
+ * only src's log rows (n_src entries) are copied into each dst's log. */
+dl_status dl_fork(dl_ctx *ctx, int32_t src, const int32_t *dsts, int32_t n);
+
+/* One decode token for each listed slot (n slots, row i of every tensor is
+ * slot slots[i]):
+ *   q (r for RWKV6), k   [n, H, d_k] bf16
+ *   v                    [n, H, d_v] bf16
+ *   g                    [n, H] fp32 (GDN) or [n, H, d_k] fp32 (KDA, RWKV6): log-decay
+ *   beta                 [n, H] fp32 (GDN, KDA); ignored for RWKV6 (may be NULL)
+ *   o                    [n, H, d_v] bf16 or fp32 (dl_config.out_bf16), written
+ * Launches ReplayPrep then AppendDecode (merge fused for the slots whose log
+ * is full).  A frozen slot in the list returns DL_EBUSY. */
+dl_status dl_step(dl_ctx *ctx, const int32_t *slots, int32_t n,
+                  const void *q, const void *k, const void *v,
+                  const float *g, const float *beta, void *o);
+
+/* Same arguments and results as dl_step, but every tensor is in HOST memory
+ * (pinned memory gives full copy speed).  The call copies the inputs to
+ * device staging buffers owned by the context, runs dl_step, copies o back
+ * and synchronises the stream before returning. */
+dl_status dl_step_host(dl_ctx *ctx, const int32_t *slots, int32_t n,
+                       const void *q, const void *k, const void *v,
+                       const float *g, const float *beta, void *o);
+
+/* The eager dense step, one kernel that reads and rewrites the whole state of
+ * every listed slot-head (the "state-update tax" of the DeltaLog page, section
+ * "Problem").  Same arguments as dl_step; each slot must own its base and
+ * have an empty log (true for every slot of an M = 1 context), else DL_EINVAL. */
+dl_status dl_step_eager(dl_ctx *ctx, const int32_t *slots, int32_t n,
+                        const void *q, const void *k, const void *v,
+                        const float *g, const float *beta, void *o);
+
+/* Force a merge now: S̄[s] <- base + replayed log, log emptied, slot owns its base. */
+dl_status dl_merge(dl_ctx *ctx, const int32_t *slots, int32_t n);
+
+/* Materialise the logical state of each listed slot into S_out [n, H, d_v,
+ * d_k] fp32 device.  Does not change the context. */
+dl_status dl_read_state(dl_ctx *ctx, const int32_t *slots, int32_t n, float *S_out);
+
+/* Synchronise and copy the device slot table: n_log and base_of are host
+ * arrays of num_slots int32 (either may be NULL).  Returns DL_EDEVICE if the
+ * device table disagrees with the host table. */
+dl_status dl_get_meta(dl_ctx *ctx, int32_t *n_log, int32_t *base_of);
+
+/* Synchronise the stream and report any CUDA or device-side error. */
+dl_status dl_sync(dl_ctx *ctx);
+
+/* Kernel timing: when enabled, every launch is bracketed by CUDA events on the
+ * context's stream (this disables launch overlap between ReplayPrep and
+ * AppendDecode).  dl_get_timing synchronises and returns, per kernel kind
+ * (0 ReplayPrep, 1 AppendDecode, 2 EagerStep, 3 Merge/ReadState), the summed
+ * milliseconds and the number of launches since timing was enabled. */
+dl_status dl_set_timing(dl_ctx *ctx, int32_t enable);
+dl_status dl_get_timing(dl_ctx *ctx, double *ms, int64_t *launches);
+
+/* One-line text for the last error of ctx (never NULL). */
+const char *dl_last_error(const dl_ctx *ctx);
+const char *dl_status_str(dl_status s);
+int32_t dl_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DELTALOG_H */

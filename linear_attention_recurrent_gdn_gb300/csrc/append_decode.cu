@@ -1,0 +1,55 @@
+// AppendDecode instantiations and launcher (kernel body in pipeline.cuh).
+#include "pipeline.cuh"
+#include "launch.h"
+
+namespace dl {
+
+template <int OP, int DK>
+static cudaError_t launch_ad(const StepArgs& a, int grid, size_t smem, bool pdl, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(PIPE_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, pipe_kernel<OP, DK, DK, APPEND>, a);
+}
+
+cudaError_t launch_append_decode(int op, int dk, const StepArgs& a, int grid, size_t smem,
+                                 bool pdl, cudaStream_t s) {
+  if (a.rows <= 0) return cudaSuccess;
+  if (dk == 64) {
+    if (op == GDN) return launch_ad<GDN, 64>(a, grid, smem, pdl, s);
+    if (op == KDA) return launch_ad<KDA, 64>(a, grid, smem, pdl, s);
+    return launch_ad<RWKV6, 64>(a, grid, smem, pdl, s);
+  }
+  if (op == GDN) return launch_ad<GDN, 128>(a, grid, smem, pdl, s);
+  if (op == KDA) return launch_ad<KDA, 128>(a, grid, smem, pdl, s);
+  return launch_ad<RWKV6, 128>(a, grid, smem, pdl, s);
+}
+
+template <int OP, int DK>
+static cudaError_t cfg_one(size_t smem) {
+  cudaError_t e = cudaFuncSetAttribute(pipe_kernel<OP, DK, DK, APPEND>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(pipe_kernel<OP, DK, DK, EAGER>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+}
+
+cudaError_t configure_pipeline(int op, int dk, size_t smem) {
+  if (dk == 64) {
+    if (op == GDN) return cfg_one<GDN, 64>(smem);
+    if (op == KDA) return cfg_one<KDA, 64>(smem);
+    return cfg_one<RWKV6, 64>(smem);
+  }
+  if (op == GDN) return cfg_one<GDN, 128>(smem);
+  if (op == KDA) return cfg_one<KDA, 128>(smem);
+  return cfg_one<RWKV6, 128>(smem);
+}
+
+}  // namespace dl

@@ -1,0 +1,640 @@
+// C ABI of libdeltalog (declared and documented in include/deltalog.h).
+//
+// The context owns the dense bases S̄, the bounded logs, the device copy of the
+// slot table, the ReplayPrep coefficient scratch and a device status word.  The
+// host slot table (slot_table.cpp) validates every call and yields the per-row
+// step plan (slot, base read, log length) that is passed to the kernels as a
+// launch parameter, so that no host-device synchronisation is needed per step.
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <memory>
+#include <new>
+#include <string>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "../../include/deltalog.h"
+#include "dl_device.cuh"
+#include "launch.h"
+#include "layout.h"
+
+namespace {
+
+constexpr int NKIND = 4;   // timing kinds: ReplayPrep, AppendDecode, EagerStep, Merge/ReadState
+
+struct TimedPair {
+  cudaEvent_t a, b;
+};
+
+}  // namespace
+
+struct dl_ctx {
+  dl_config cfg{};
+  cudaStream_t stream = nullptr;
+  int device = 0, num_sms = 0, smem_optin = 0;
+  dl_table* table = nullptr;
+  dl::Layout L{};
+  float* Sbar = nullptr;
+  void* alog = nullptr;
+  uint16_t* klog = nullptr;
+  float* Llog = nullptr;
+  int32_t* nlog = nullptr;
+  int32_t* base_of = nullptr;
+  float* coef = nullptr;
+  float* bonus = nullptr;
+  int32_t* status = nullptr;
+  int32_t coef_rows = 0;
+  void* stage = nullptr;        // device staging for dl_step_host
+  size_t stage_bytes = 0;
+  std::vector<int32_t> plan;
+  std::unique_ptr<dl::StepArgs> step_args;
+  std::unique_ptr<dl::SlotListArgs> list_args;
+  std::string err = "no error";
+  dl_status sticky = DL_OK;
+  bool timing = false;
+  std::vector<TimedPair> timed[NKIND];
+  double timed_ms[NKIND] = {0, 0, 0, 0};
+  int64_t timed_n[NKIND] = {0, 0, 0, 0};
+};
+
+namespace {
+
+dl_status set_err(dl_ctx* c, dl_status s, const char* fmt, ...) {
+  if (c) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    c->err = buf;
+    if (s == DL_ECUDA || s == DL_EDEVICE) c->sticky = s;
+  }
+  return s;
+}
+
+dl_status cuda_err(dl_ctx* c, cudaError_t e, const char* what) {
+  return set_err(c, DL_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define DL_CUDA(call, what)                   \
+  do {                                        \
+    cudaError_t e_ = (call);                  \
+    if (e_ != cudaSuccess) return cuda_err(c, e_, what); \
+  } while (0)
+
+// Allocation with an optional countdown failure for tests (DL_TEST_FAIL_ALLOC=k
+// makes the k-th device allocation of dl_create fail).
+int g_fail_countdown = -1;
+
+cudaError_t dev_alloc(void** p, size_t bytes) {
+  if (g_fail_countdown > 0 && --g_fail_countdown == 0) {
+    *p = nullptr;
+    return cudaErrorMemoryAllocation;
+  }
+  return cudaMalloc(p, bytes < 16 ? 16 : bytes);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+void free_all(dl_ctx* c) {
+  void* ptrs[] = {c->Sbar, c->alog, c->klog, c->Llog, c->nlog, c->base_of,
+                  c->coef, c->bonus, c->status, c->stage};
+  for (void* p : ptrs)
+    if (p) cudaFree(p);
+  c->Sbar = nullptr;
+  c->alog = nullptr;
+  c->klog = nullptr;
+  c->Llog = nullptr;
+  c->nlog = nullptr;
+  c->base_of = nullptr;
+  c->coef = nullptr;
+  c->bonus = nullptr;
+  c->status = nullptr;
+  c->stage = nullptr;
+  for (auto& v : c->timed)
+    for (auto& p : v) {
+      cudaEventDestroy(p.a);
+      cudaEventDestroy(p.b);
+    }
+  if (c->table) dl_table_destroy(c->table);
+  c->table = nullptr;
+}
+
+// Pipeline shape for a launch with G tiles per unit: the most stages that fit
+// (up to 12), and enough aux slots to cover the units those stages span.
+struct PipeShape {
+  int ns, na;
+  size_t smem;
+};
+
+PipeShape pipe_shape(const dl_ctx* c, int G, bool append) {
+  const size_t tile = (size_t)dl::BV * c->cfg.d_k * 4;
+  const size_t aux = append ? c->L.aux_bytes : c->L.e_bytes;
+  const size_t budget = (size_t)c->smem_optin - dl::BAR_BYTES - 1024;
+  PipeShape best{1, 1, dl::BAR_BYTES + tile + aux};
+  for (int ns = 2; ns <= 12; ++ns) {
+    int na = (ns + G - 1) / G + 1;
+    if (na > ns + 1) na = ns + 1;
+    const size_t need = (size_t)ns * tile + (size_t)na * aux;
+    if (need <= budget) best = PipeShape{ns, na, dl::BAR_BYTES + need};
+  }
+  return best;
+}
+
+bool record(dl_ctx* c, int kind, cudaEvent_t* ev) {
+  if (!c->timing) return false;
+  cudaEventCreate(ev);
+  cudaEventRecord(*ev, c->stream);
+  (void)kind;
+  return true;
+}
+
+void record_end(dl_ctx* c, int kind, cudaEvent_t start) {
+  cudaEvent_t stop;
+  cudaEventCreate(&stop);
+  cudaEventRecord(stop, c->stream);
+  c->timed[kind].push_back(TimedPair{start, stop});
+}
+
+dl_status check_ctx(dl_ctx* c) {
+  if (!c) return DL_EINVAL;
+  if (c->sticky != DL_OK) return c->sticky;
+  return DL_OK;
+}
+
+dl_status check_step_ptrs(dl_ctx* c, int32_t n, const void* q, const void* k, const void* v,
+                          const float* g, const float* beta, const void* o) {
+  if (n == 0) return DL_OK;
+  if (!q || !k || !v || !g || !o || (c->cfg.op != DL_RWKV6 && !beta))
+    return set_err(c, DL_EINVAL, "NULL tensor pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(o) ||
+      (beta && !aligned16(beta)))
+    return set_err(c, DL_EINVAL, "tensor pointers must be 16-byte aligned");
+  if (c->cfg.op == DL_RWKV6 && !c->bonus)
+    return set_err(c, DL_EINVAL, "RWKV6 needs dl_set_bonus before stepping");
+  return DL_OK;
+}
+
+void fill_step_args(dl_ctx* c, dl::StepArgs& a, int32_t row0, int32_t rows, const void* q,
+                    const void* k, const void* v, const float* g, const float* beta, void* o) {
+  const dl_config& f = c->cfg;
+  const size_t H = f.num_heads;
+  const size_t gw = (f.op == DL_GDN) ? 1 : f.d_k;
+  a.q = static_cast<const uint16_t*>(q) + (size_t)row0 * H * f.d_k;
+  a.k = static_cast<const uint16_t*>(k) + (size_t)row0 * H * f.d_k;
+  a.v = static_cast<const uint16_t*>(v) + (size_t)row0 * H * f.d_v;
+  a.g = g + (size_t)row0 * H * gw;
+  a.beta = beta ? beta + (size_t)row0 * H : nullptr;
+  const size_t osz = f.out_bf16 ? 2 : 4;
+  a.o = static_cast<unsigned char*>(o) + (size_t)row0 * H * f.d_v * osz;
+  a.Sbar = c->Sbar;
+  a.alog = c->alog;
+  a.klog = c->klog;
+  a.Llog = c->Llog;
+  a.coef = c->coef;
+  a.bonus = c->bonus;
+  a.nlog = c->nlog;
+  a.base_of = c->base_of;
+  a.status = c->status;
+  a.rows = rows;
+  a.H = f.num_heads;
+  a.M = f.merge_interval;
+  a.Mcap = c->L.Mcap;
+  a.Mcap4 = c->L.Mcap4;
+  a.CB = c->L.CB;
+  a.P0 = c->L.P0;
+  a.out_bf16 = f.out_bf16;
+  a.scale = f.scale;
+  a.aux_bytes = c->L.aux_bytes;
+  for (int32_t i = 0; i < rows; ++i) {
+    const int32_t* p = &c->plan[4 * (size_t)(row0 + i)];
+    a.items[i].slot = p[0];
+    a.items[i].base = p[1];
+    a.items[i].n = p[2];
+  }
+}
+
+// Choose G (value tiles per work unit) and the grid for `rows` slot rows.
+void unit_shape(const dl_ctx* c, dl::StepArgs& a, int* grid) {
+  const int nvt = c->cfg.d_v / dl::BV;
+  const long n_sh = (long)a.rows * a.H;
+  if (n_sh >= 2L * c->num_sms) {
+    a.G = nvt;
+    a.NG = 1;
+  } else {
+    a.G = 1;
+    a.NG = nvt;
+  }
+  const long units = n_sh * a.NG;
+  *grid = (int)(units < c->num_sms ? units : c->num_sms);
+}
+
+dl_status run_step(dl_ctx* c, const int32_t* slots, int32_t n, const void* q, const void* k,
+                   const void* v, const float* g, const float* beta, void* o, bool eager) {
+  (void)slots;
+  const dl_config& f = c->cfg;
+  dl::StepArgs& a = *c->step_args;
+  for (int32_t row0 = 0; row0 < n; row0 += dl::MAX_ROWS) {
+    const int32_t rows = (n - row0) < dl::MAX_ROWS ? (n - row0) : dl::MAX_ROWS;
+    fill_step_args(c, a, row0, rows, q, k, v, g, beta, o);
+    int grid = 0;
+    unit_shape(c, a, &grid);
+    const PipeShape ps = pipe_shape(c, a.G, !eager);
+    a.ns = ps.ns;
+    a.na = ps.na;
+    cudaEvent_t e0;
+    if (eager) {
+      const bool t = record(c, 2, &e0);
+      DL_CUDA(dl::launch_eager_step(f.op, f.d_k, a, grid, ps.smem, c->stream), "EagerStep launch");
+      if (t) record_end(c, 2, e0);
+    } else {
+      bool t = record(c, 0, &e0);
+      DL_CUDA(dl::launch_replay_prep(f.op, f.d_k, a, c->stream), "ReplayPrep launch");
+      if (t) record_end(c, 0, e0);
+      t = record(c, 1, &e0);
+      DL_CUDA(dl::launch_append_decode(f.op, f.d_k, a, grid, ps.smem, !c->timing, c->stream),
+              "AppendDecode launch");
+      if (t) record_end(c, 1, e0);
+    }
+  }
+  return DL_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t dl_abi_version(void) { return DL_ABI_VERSION; }
+
+const char* dl_status_str(dl_status s) {
+  switch (s) {
+    case DL_OK: return "DL_OK";
+    case DL_EINVAL: return "DL_EINVAL";
+    case DL_ENOMEM: return "DL_ENOMEM";
+    case DL_ECUDA: return "DL_ECUDA";
+    case DL_EBUSY: return "DL_EBUSY";
+    case DL_EDEVICE: return "DL_EDEVICE";
+    case DL_EUNSUPPORTED: return "DL_EUNSUPPORTED";
+  }
+  return "DL_?";
+}
+
+const char* dl_last_error(const dl_ctx* c) { return c ? c->err.c_str() : "NULL context"; }
+
+dl_status dl_create(const dl_config* cfg, void* stream, dl_ctx** out) {
+  if (!out) return DL_EINVAL;
+  *out = nullptr;
+  if (!cfg) return DL_EINVAL;
+  const dl_config f = *cfg;
+  if (f.op < DL_GDN || f.op > DL_RWKV6 || f.num_slots < 1 || f.num_heads < 1 ||
+      f.merge_interval < 1 || (f.out_bf16 != 0 && f.out_bf16 != 1))
+    return DL_EINVAL;
+  if (f.merge_interval > 32) return DL_EUNSUPPORTED;
+  if ((f.d_k != 64 && f.d_k != 128) || f.d_v != f.d_k) return DL_EUNSUPPORTED;
+
+  dl_ctx* c = new (std::nothrow) dl_ctx;
+  if (!c) return DL_ENOMEM;
+  c->cfg = f;
+  c->stream = static_cast<cudaStream_t>(stream);
+  c->L = dl::make_layout(f.op, f.merge_interval, f.d_k, f.d_v);
+  c->plan.resize(4 * (size_t)f.num_slots);
+  c->step_args.reset(new (std::nothrow) dl::StepArgs());
+  c->list_args.reset(new (std::nothrow) dl::SlotListArgs());
+  if (const char* s = getenv("DL_TEST_FAIL_ALLOC")) g_fail_countdown = atoi(s);
+  dl_status rc = DL_OK;
+  do {
+    if (!c->step_args || !c->list_args) { rc = DL_ENOMEM; break; }
+    if (dl_table_create(f.num_slots, f.merge_interval, &c->table) != DL_OK) { rc = DL_ENOMEM; break; }
+    cudaError_t e = cudaGetDevice(&c->device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
+    if (e == cudaSuccess)
+      e = cudaDeviceGetAttribute(&c->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c->device);
+    if (e != cudaSuccess) { rc = cuda_err(c, e, "device query"); break; }
+    const size_t S = f.num_slots, H = f.num_heads, dk = f.d_k, dv = f.d_v, Mcap = c->L.Mcap;
+    const size_t esa = (f.op == DL_RWKV6) ? 2 : 4;
+    const size_t lw = (f.op == DL_GDN) ? 1 : dk;
+    c->coef_rows = f.num_slots < dl::MAX_ROWS ? f.num_slots : dl::MAX_ROWS;
+    struct { void** p; size_t bytes; } al[] = {
+        {reinterpret_cast<void**>(&c->Sbar), S * H * dv * dk * 4},
+        {&c->alog, S * H * Mcap * dv * esa},
+        {reinterpret_cast<void**>(&c->klog), S * H * Mcap * dk * 2},
+        {reinterpret_cast<void**>(&c->Llog), S * H * Mcap * lw * 4},
+        {reinterpret_cast<void**>(&c->nlog), S * 4},
+        {reinterpret_cast<void**>(&c->base_of), S * 4},
+        {reinterpret_cast<void**>(&c->coef), (size_t)c->coef_rows * H * c->L.CB * 4},
+        {reinterpret_cast<void**>(&c->status), 16},
+    };
+    for (auto& x : al) {
+      e = dev_alloc(x.p, x.bytes);
+      if (e != cudaSuccess) break;
+    }
+    if (e != cudaSuccess) { rc = set_err(c, DL_ENOMEM, "device allocation failed"); break; }
+    e = cudaMemsetAsync(c->Sbar, 0, S * H * dv * dk * 4, c->stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(c->alog, 0, S * H * Mcap * dv * esa, c->stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(c->klog, 0, S * H * Mcap * dk * 2, c->stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(c->Llog, 0, S * H * Mcap * lw * 4, c->stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(c->nlog, 0, S * 4, c->stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(c->status, 0, 16, c->stream);
+    if (e == cudaSuccess) {
+      std::vector<int32_t> iota(S);
+      for (size_t s = 0; s < S; ++s) iota[s] = (int32_t)s;
+      e = cudaMemcpyAsync(c->base_of, iota.data(), S * 4, cudaMemcpyHostToDevice, c->stream);
+      if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
+    }
+    if (e != cudaSuccess) { rc = cuda_err(c, e, "context initialisation"); break; }
+    const PipeShape big = pipe_shape(c, 1, true);
+    size_t smem = big.smem;
+    for (int G = 1; G <= 4; G *= 2) {
+      const PipeShape a = pipe_shape(c, G, true), b = pipe_shape(c, G, false);
+      if (a.smem > smem) smem = a.smem;
+      if (b.smem > smem) smem = b.smem;
+    }
+    e = dl::configure_pipeline(f.op, f.d_k, smem);
+    if (e != cudaSuccess) { rc = cuda_err(c, e, "kernel attribute"); break; }
+  } while (0);
+  g_fail_countdown = -1;
+  if (rc != DL_OK) {
+    free_all(c);
+    delete c;
+    return rc;
+  }
+  *out = c;
+  return DL_OK;
+}
+
+dl_status dl_destroy(dl_ctx* c) {
+  if (!c) return DL_OK;
+  cudaStreamSynchronize(c->stream);
+  free_all(c);
+  delete c;
+  return DL_OK;
+}
+
+dl_status dl_set_stream(dl_ctx* c, void* stream) {
+  if (!c) return DL_EINVAL;
+  c->stream = static_cast<cudaStream_t>(stream);
+  return DL_OK;
+}
+
+dl_status dl_set_state(dl_ctx* c, const int32_t* slots, int32_t n, const float* S) {
+  dl_status rc = check_ctx(c);
+  if (rc != DL_OK) return rc;
+  if (n < 0 || (n > 0 && (!S || !aligned16(S)))) return set_err(c, DL_EINVAL, "bad state pointer");
+  rc = dl_table_reset(c->table, slots, n);
+  if (rc != DL_OK) return set_err(c, rc, "dl_set_state: invalid or frozen slot list");
+  dl::SlotListArgs& a = *c->list_args;
+  const size_t per = (size_t)c->cfg.num_heads * c->cfg.d_v * c->cfg.d_k;
+  for (int32_t r0 = 0; r0 < n; r0 += dl::MAX_ROWS) {
+    const int32_t rows = (n - r0) < dl::MAX_ROWS ? (n - r0) : dl::MAX_ROWS;
+    a = dl::SlotListArgs{};
+    a.Sbar = c->Sbar;
+    a.nlog = c->nlog;
+    a.base_of = c->base_of;
+    a.S_in = S + (size_t)r0 * per;
+    a.rows = rows;
+    a.H = c->cfg.num_heads;
+    a.Mcap = c->L.Mcap;
+    for (int32_t i = 0; i < rows; ++i) a.items[i] = dl::StepItem{slots[r0 + i], slots[r0 + i], 0};
+    DL_CUDA(dl::launch_set_state(c->cfg.d_k, c->cfg.d_v, a, c->stream), "SetState launch");
+  }
+  return DL_OK;
+}
+
+dl_status dl_set_bonus(dl_ctx* c, const float* bonus) {
+  dl_status rc = check_ctx(c);
+  if (rc != DL_OK) return rc;
+  if (c->cfg.op != DL_RWKV6) return set_err(c, DL_EINVAL, "bonus applies to RWKV6 only");
+  if (!bonus) return set_err(c, DL_EINVAL, "NULL bonus");
+  const size_t bytes = (size_t)c->cfg.num_heads * c->cfg.d_k * 4;
+  if (!c->bonus) {
+    cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&c->bonus), bytes);
+    if (e != cudaSuccess) return set_err(c, DL_ENOMEM, "bonus allocation failed");
+  }
+  DL_CUDA(cudaMemcpyAsync(c->bonus, bonus, bytes, cudaMemcpyDeviceToDevice, c->stream), "bonus copy");
+  return DL_OK;
+}
+
+dl_status dl_fork(dl_ctx* c, int32_t src, const int32_t* dsts, int32_t n) {
+  dl_status rc = check_ctx(c);
+  if (rc != DL_OK) return rc;
+  if (n < 0) return set_err(c, DL_EINVAL, "negative count");
+  int32_t src_base = 0, src_n = 0;
+  if (src >= 0 && src < c->cfg.num_slots) {
+    std::vector<int32_t> nl(c->cfg.num_slots), bo(c->cfg.num_slots);
+    dl_table_get(c->table, nl.data(), bo.data(), nullptr);
+    src_base = bo[src];
+    src_n = nl[src];
+  }
+  rc = dl_table_fork(c->table, src, dsts, n);
+  if (rc != DL_OK) return set_err(c, rc, "dl_fork: invalid or frozen slots");
+  dl::SlotListArgs& a = *c->list_args;
+  for (int32_t r0 = 0; r0 < n; r0 += dl::MAX_ROWS) {
+    const int32_t rows = (n - r0) < dl::MAX_ROWS ? (n - r0) : dl::MAX_ROWS;
+    a = dl::SlotListArgs{};
+    a.alog = c->alog;
+    a.klog = c->klog;
+    a.Llog = c->Llog;
+    a.nlog = c->nlog;
+    a.base_of = c->base_of;
+    a.rows = rows;
+    a.H = c->cfg.num_heads;
+    a.Mcap = c->L.Mcap;
+    a.src_slot = src;
+    a.src_n = src_n;
+    a.src_base = src_base;
+    for (int32_t i = 0; i < rows; ++i) a.items[i] = dl::StepItem{dsts[r0 + i], src_base, src_n};
+    DL_CUDA(dl::launch_fork(c->cfg.op, c->cfg.d_k, a, c->stream), "Fork launch");
+  }
+  return DL_OK;
+}
+
+dl_status dl_step(dl_ctx* c, const int32_t* slots, int32_t n, const void* q, const void* k,
+                  const void* v, const float* g, const float* beta, void* o) {
+  dl_status rc = check_ctx(c);
+  if (rc != DL_OK) return rc;
+  if (n < 0) return set_err(c, DL_EINVAL, "negative count");
+  rc = check_step_ptrs(c, n, q, k, v, g, beta, o);
+  if (rc != DL_OK) return rc;
+  rc = dl_table_step(c->table, slots, n, c->plan.data());
+  if (rc != DL_OK) return set_err(c, rc, "dl_step: invalid or frozen slot list");
+  return run_step(c, slots, n, q, k, v, g, beta, o, false);
+}
+
+dl_status dl_step_eager(dl_ctx* c, const int32_t* slots, int32_t n, const void* q, const void* k,
+                        const void* v, const float* g, const float* beta, void* o) {
+  dl_status rc = check_ctx(c);
+  if (rc != DL_OK) return rc;
+  if (n < 0) return set_err(c, DL_EINVAL, "negative count");
+  rc = check_step_ptrs(c, n, q, k, v, g, beta, o);
+  if (rc != DL_OK) return rc;
+  rc = dl_table_step_eager(c->table, slots, n);
+  if (rc != DL_OK)
+    return set_err(c, rc, "dl_step_eager: slots must own their base and have an empty log");
+  for (int32_t i = 0; i < n; ++i) {
+    c->plan[4 * (size_t)i + 0] = slots[i];
+    c->plan[4 * (size_t)i + 1] = slots[i];
+    c->plan[4 * (size_t)i + 2] = 0;
+    c->plan[4 * (size_t)i + 3] = 1;
+  }
+  return run_step(c, slots, n, q, k, v, g, beta, o, true);
+}
+
+dl_status dl_step_host(dl_ctx* c, const int32_t* slots, int32_t n, const void* q, const void* k,
+                       const void* v, const float* g, const float* beta, void* o) {
+  dl_status rc = check_ctx(c);
+  if (rc != DL_OK) return rc;
+  if (n < 0) return set_err(c, DL_EINVAL, "negative count");
+  if (n == 0) return DL_OK;
+  if (!q || !k || !v || !g || !o || (c->cfg.op != DL_RWKV6 && !beta))
+    return set_err(c, DL_EINVAL, "NULL tensor pointer");
+  const dl_config& f = c->cfg;
+  const size_t H = f.num_heads;
+  const size_t bq = (size_t)n * H * f.d_k * 2, bv = (size_t)n * H * f.d_v * 2;
+  const size_t bg = (size_t)n * H * (f.op == DL_GDN ? 1 : f.d_k) * 4;
+  const size_t bb = (size_t)n * H * 4, bo = (size_t)n * H * f.d_v * (f.out_bf16 ? 2 : 4);
+  auto r16 = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  const size_t need = 2 * r16(bq) + r16(bv) + r16(bg) + r16(bb) + r16(bo);
+  if (need > c->stage_bytes) {
+    if (c->stage) cudaFree(c->stage);
+    c->stage = nullptr;
+    c->stage_bytes = 0;
+    // size for the largest batch the context can take, so that later calls do not reallocate
+    const size_t Sn = f.num_slots;
+    const size_t full = 2 * r16(Sn * H * f.d_k * 2) + r16(Sn * H * f.d_v * 2) +
+                        r16(Sn * H * (f.op == DL_GDN ? 1 : f.d_k) * 4) + r16(Sn * H * 4) +
+                        r16(Sn * H * f.d_v * 4);
+    if (cudaMalloc(&c->stage, full) != cudaSuccess) return set_err(c, DL_ENOMEM, "staging allocation");
+    c->stage_bytes = full;
+  }
+  unsigned char* p = static_cast<unsigned char*>(c->stage);
+  void* dq = p; p += r16(bq);
+  void* dk = p; p += r16(bq);
+  void* dv = p; p += r16(bv);
+  float* dg = reinterpret_cast<float*>(p); p += r16(bg);
+  float* db = reinterpret_cast<float*>(p); p += r16(bb);
+  void* dout = p;
+  // validate before any copy so that an error leaves nothing enqueued
+  rc = dl_table_check(c->table, slots, n);
+  if (rc != DL_OK) return set_err(c, rc, "dl_step_host: invalid slot list");
+  DL_CUDA(cudaMemcpyAsync(dq, q, bq, cudaMemcpyHostToDevice, c->stream), "H2D q");
+  DL_CUDA(cudaMemcpyAsync(dk, k, bq, cudaMemcpyHostToDevice, c->stream), "H2D k");
+  DL_CUDA(cudaMemcpyAsync(dv, v, bv, cudaMemcpyHostToDevice, c->stream), "H2D v");
+  DL_CUDA(cudaMemcpyAsync(dg, g, bg, cudaMemcpyHostToDevice, c->stream), "H2D g");
+  if (f.op != DL_RWKV6)
+    DL_CUDA(cudaMemcpyAsync(db, beta, bb, cudaMemcpyHostToDevice, c->stream), "H2D beta");
+  rc = dl_step(c, slots, n, dq, dk, dv, dg, f.op != DL_RWKV6 ? db : nullptr, dout);
+  if (rc != DL_OK) return rc;
+  DL_CUDA(cudaMemcpyAsync(o, dout, bo, cudaMemcpyDeviceToHost, c->stream), "D2H o");
+  DL_CUDA(cudaStreamSynchronize(c->stream), "stream sync");
+  return DL_OK;
+}
+
+static dl_status merge_or_read(dl_ctx* c, const int32_t* slots, int32_t n, float* S_out) {
+  std::vector<int32_t> nl(c->cfg.num_slots), bo(c->cfg.num_slots);
+  dl_table_get(c->table, nl.data(), bo.data(), nullptr);
+  std::vector<dl::StepItem> items(n);
+  for (int32_t i = 0; i < n; ++i) items[i] = dl::StepItem{slots[i], bo[slots[i]], nl[slots[i]]};
+  if (!S_out) {
+    dl_status rc = dl_table_reset(c->table, slots, n);
+    if (rc != DL_OK) return set_err(c, rc, "dl_merge: invalid or frozen slot list");
+  }
+  dl::SlotListArgs& a = *c->list_args;
+  const size_t per = (size_t)c->cfg.num_heads * c->cfg.d_v * c->cfg.d_k;
+  for (int32_t r0 = 0; r0 < n; r0 += dl::MAX_ROWS) {
+    const int32_t rows = (n - r0) < dl::MAX_ROWS ? (n - r0) : dl::MAX_ROWS;
+    a = dl::SlotListArgs{};
+    a.Sbar = c->Sbar;
+    a.alog = c->alog;
+    a.klog = c->klog;
+    a.Llog = c->Llog;
+    a.nlog = c->nlog;
+    a.base_of = c->base_of;
+    a.S_out = S_out ? S_out + (size_t)r0 * per : nullptr;
+    a.rows = rows;
+    a.H = c->cfg.num_heads;
+    a.Mcap = c->L.Mcap;
+    for (int32_t i = 0; i < rows; ++i) a.items[i] = items[r0 + i];
+    cudaEvent_t e0;
+    const bool t = record(c, 3, &e0);
+    DL_CUDA(dl::launch_merge(c->cfg.op, c->cfg.d_k, a, c->stream), "Merge launch");
+    if (t) record_end(c, 3, e0);
+  }
+  return DL_OK;
+}
+
+dl_status dl_merge(dl_ctx* c, const int32_t* slots, int32_t n) {
+  dl_status rc = check_ctx(c);
+  if (rc != DL_OK) return rc;
+  if (n < 0) return set_err(c, DL_EINVAL, "negative count");
+  rc = dl_table_check(c->table, slots, n);
+  if (rc != DL_OK) return set_err(c, rc, "dl_merge: invalid slot list");
+  return merge_or_read(c, slots, n, nullptr);
+}
+
+dl_status dl_read_state(dl_ctx* c, const int32_t* slots, int32_t n, float* S_out) {
+  dl_status rc = check_ctx(c);
+  if (rc != DL_OK) return rc;
+  if (n < 0) return set_err(c, DL_EINVAL, "negative count");
+  if (n > 0 && (!S_out || !aligned16(S_out))) return set_err(c, DL_EINVAL, "bad output pointer");
+  rc = dl_table_check(c->table, slots, n);
+  if (rc != DL_OK) return set_err(c, rc, "dl_read_state: invalid slot list");
+  return merge_or_read(c, slots, n, S_out);
+}
+
+dl_status dl_sync(dl_ctx* c) {
+  if (!c) return DL_EINVAL;
+  if (c->sticky != DL_OK) return c->sticky;
+  DL_CUDA(cudaStreamSynchronize(c->stream), "stream sync");
+  DL_CUDA(cudaGetLastError(), "pending CUDA error");
+  int32_t st = 0;
+  DL_CUDA(cudaMemcpy(&st, c->status, 4, cudaMemcpyDeviceToHost), "status read");
+  if (st != 0) return set_err(c, DL_EDEVICE, "kernel reported device status %d (bounded wait gave up)", st);
+  return DL_OK;
+}
+
+dl_status dl_get_meta(dl_ctx* c, int32_t* n_log, int32_t* base_of) {
+  dl_status rc = dl_sync(c);
+  if (rc != DL_OK) return rc;
+  const size_t S = c->cfg.num_slots;
+  std::vector<int32_t> dn(S), db(S), hn(S), hb(S);
+  DL_CUDA(cudaMemcpy(dn.data(), c->nlog, S * 4, cudaMemcpyDeviceToHost), "meta read");
+  DL_CUDA(cudaMemcpy(db.data(), c->base_of, S * 4, cudaMemcpyDeviceToHost), "meta read");
+  dl_table_get(c->table, hn.data(), hb.data(), nullptr);
+  if (n_log) memcpy(n_log, dn.data(), S * 4);
+  if (base_of) memcpy(base_of, db.data(), S * 4);
+  if (dn != hn || db != hb) return set_err(c, DL_EDEVICE, "device slot table disagrees with host table");
+  return DL_OK;
+}
+
+dl_status dl_set_timing(dl_ctx* c, int32_t enable) {
+  if (!c) return DL_EINVAL;
+  c->timing = enable != 0;
+  for (int k = 0; k < NKIND; ++k) {
+    c->timed_ms[k] = 0;
+    c->timed_n[k] = 0;
+  }
+  return DL_OK;
+}
+
+dl_status dl_get_timing(dl_ctx* c, double* ms, int64_t* launches) {
+  if (!c) return DL_EINVAL;
+  DL_CUDA(cudaStreamSynchronize(c->stream), "stream sync");
+  for (int k = 0; k < NKIND; ++k) {
+    for (auto& p : c->timed[k]) {
+      float t = 0.f;
+      if (cudaEventElapsedTime(&t, p.a, p.b) == cudaSuccess) c->timed_ms[k] += t;
+      c->timed_n[k] += 1;
+      cudaEventDestroy(p.a);
+      cudaEventDestroy(p.b);
+    }
+    c->timed[k].clear();
+    if (ms) ms[k] = c->timed_ms[k];
+    if (launches) launches[k] = c->timed_n[k];
+  }
+  return DL_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,29 @@
+// EagerStep instantiations and launcher (kernel body in pipeline.cuh): the
+// dense step that reads and rewrites every state row of every active
+// slot-head each token — the "state-update tax" the DeltaLog page describes
+// in its "Problem" section, kept as the in-house comparison kernel.
+#include "pipeline.cuh"
+#include "launch.h"
+
+namespace dl {
+
+template <int OP, int DK>
+static cudaError_t launch_ea(const StepArgs& a, int grid, size_t smem, cudaStream_t s) {
+  pipe_kernel<OP, DK, DK, EAGER><<<grid, PIPE_THREADS, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_eager_step(int op, int dk, const StepArgs& a, int grid, size_t smem,
+                              cudaStream_t s) {
+  if (a.rows <= 0) return cudaSuccess;
+  if (dk == 64) {
+    if (op == GDN) return launch_ea<GDN, 64>(a, grid, smem, s);
+    if (op == KDA) return launch_ea<KDA, 64>(a, grid, smem, s);
+    return launch_ea<RWKV6, 64>(a, grid, smem, s);
+  }
+  if (op == GDN) return launch_ea<GDN, 128>(a, grid, smem, s);
+  if (op == KDA) return launch_ea<KDA, 128>(a, grid, smem, s);
+  return launch_ea<RWKV6, 128>(a, grid, smem, s);
+}
+
+}  // namespace dl

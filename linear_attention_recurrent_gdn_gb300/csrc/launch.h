@@ -1,0 +1,30 @@
+// Host-side entry points of the kernel translation units (internal).
+#pragma once
+#include <cuda_runtime.h>
+#include "dl_device.cuh"
+
+namespace dl {
+
+// ReplayPrep: one CTA per slot row.
+cudaError_t launch_replay_prep(int op, int dk, const StepArgs& a, cudaStream_t s);
+
+// AppendDecode (pipelined; merge fused).  `pdl` launches it as a programmatic
+// dependent of the preceding ReplayPrep in the same stream.
+cudaError_t launch_append_decode(int op, int dk, const StepArgs& a, int grid, size_t smem,
+                                 bool pdl, cudaStream_t s);
+
+// EagerStep: the dense read-modify-write step (the comparison kernel).
+cudaError_t launch_eager_step(int op, int dk, const StepArgs& a, int grid, size_t smem,
+                              cudaStream_t s);
+
+// Allow the pipelined kernels of (op, dk) to use `smem` bytes of dynamic shared memory.
+cudaError_t configure_pipeline(int op, int dk, size_t smem);
+
+// Standalone merge / read-state (S_out == nullptr: write back into S̄ and reset the log).
+cudaError_t launch_merge(int op, int dk, const SlotListArgs& a, cudaStream_t s);
+// Copy initial states into S̄ and reset the listed slots' table entries.
+cudaError_t launch_set_state(int dk, int dv, const SlotListArgs& a, cudaStream_t s);
+// Copy the source's log rows into each destination and point it at the source's base.
+cudaError_t launch_fork(int op, int dk, const SlotListArgs& a, cudaStream_t s);
+
+}  // namespace dl

@@ -1,0 +1,455 @@
+// Pipelined value-tile kernels: AppendDecode (DeltaLog step with the merge
+// fused) and EagerStep (dense read-modify-write step).
+//
+// DeltaLog page, section "Kernel implementation": the state is split along the
+// value dimension d_v and each work item handles one slice of the dense base
+// together with the matching shard of the value-side log, while the key-side
+// factors and log-decay metadata (here: the ReplayPrep coefficient block) are
+// shared by all value tiles of a slot-head.
+//
+// Structure on sm_103a (one CTA per SM, persistent over work units):
+//   * work unit = (slot-head, group of G value tiles); tile = 32 value rows of
+//     the dense base (32 x d_k fp32, contiguous in HBM);
+//   * warp NCW is the producer: one lane issues 1-D bulk copies (TMA engine)
+//     of each tile into a ring of `ns` shared-memory stages, and of each unit's
+//     small inputs (coefficients, k/q/v, value-side log rows, key log rows on a
+//     merge) into a ring of `na` aux slots, completion tracked in bytes on
+//     mbarriers; the dense base is read with an L2 evict-first policy;
+//   * warps 0..NCW-1 are consumers: one warp owns one tile.  Lane l holds d_k/32
+//     consecutive key channels; a pass over the 32 rows accumulates per-row
+//     partial dot products, a transposed butterfly reduction (31 shuffles for
+//     32 rows) leaves row l's sums on lane l, which then finishes that row:
+//     log replay, output, the appended factor; on a merge step the warp then
+//     re-reads the tile from shared memory and writes the updated rows;
+//   * every wait is bounded (see mbar_wait); a consumer releases its stage and
+//     its share of the aux slot with one mbarrier arrive each.
+// AppendDecode launches as a programmatic dependent of ReplayPrep: its
+// producer streams the first ns tiles before it waits for ReplayPrep's
+// coefficient blocks.
+#pragma once
+#include "dl_device.cuh"
+#include "layout.h"
+
+namespace dl {
+
+enum Mode : int { APPEND = 0, EAGER = 1 };
+
+constexpr int MAX_NS = 24, MAX_NA = 24;
+
+struct Bars {
+  uint32_t b0;
+  int ns, na;
+  __device__ uint32_t full(int s) const { return b0 + 8u * s; }
+  __device__ uint32_t empty(int s) const { return b0 + 8u * (ns + s); }
+  __device__ uint32_t afull(int x) const { return b0 + 8u * (2 * ns + x); }
+  __device__ uint32_t aempty(int x) const { return b0 + 8u * (2 * ns + na + x); }
+};
+
+struct UnitPos {
+  int sh, row, h, grp;
+};
+
+__device__ __forceinline__ UnitPos unit_pos(const StepArgs& a, int u) {
+  UnitPos p;
+  p.sh = u / a.NG;
+  p.grp = u - p.sh * a.NG;
+  p.row = p.sh / a.H;
+  p.h = p.sh - p.row * a.H;
+  return p;
+}
+
+__device__ __forceinline__ void store_out(const StepArgs& a, size_t idx, float val) {
+  if (a.out_bf16) static_cast<uint16_t*>(a.o)[idx] = f2bf16(val);
+  else static_cast<float*>(a.o)[idx] = val;
+}
+
+// ---------------------------------------------------------------- producer --
+template <int OP, int DK, int DV, int MODE>
+__device__ __forceinline__ void issue_aux(const StepArgs& a, const Layout& Lay, const UnitPos& p,
+                                          unsigned char* ax, uint32_t bar, bool with_coef_now) {
+  constexpr bool DELTA = OP != RWKV6;
+  const StepItem it = a.items[p.row];
+  const size_t sh = p.sh;
+  if constexpr (MODE == APPEND) {
+    constexpr int ESA = DELTA ? 4 : 2;
+    const int n = it.n;
+    const bool merge = (n + 1 == a.M);
+    const size_t lh = (size_t)it.slot * a.H + p.h;
+    uint32_t bytes = (merge ? Lay.CB : Lay.P0) * 4u;
+    if (OP == GDN) bytes += 2u * DK * 2u;
+    if (DELTA) bytes += DV * 2u;
+    bytes += (uint32_t)n * DV * ESA;
+    if (OP == RWKV6) bytes += DV * 2u;
+    if (OP == GDN && merge) bytes += (uint32_t)(n + 1) * DK * 2u;
+    mbar_arrive_expect_tx(bar, bytes);
+    if (OP == GDN) {
+      bulk_g2s(smem_u32(ax + Lay.aux_kq), a.k + sh * DK, DK * 2, bar);
+      bulk_g2s(smem_u32(ax + Lay.aux_kq + DK * 2), a.q + sh * DK, DK * 2, bar);
+    }
+    if (DELTA) bulk_g2s(smem_u32(ax + Lay.aux_v), a.v + sh * DV, DV * 2, bar);
+    if (n > 0)
+      bulk_g2s(smem_u32(ax + Lay.aux_U),
+               static_cast<const unsigned char*>(a.alog) + lh * Lay.Mcap * DV * ESA,
+               (uint32_t)n * DV * ESA, bar);
+    if (OP == RWKV6) bulk_g2s(smem_u32(ax + Lay.aux_U + n * DV * 2), a.v + sh * DV, DV * 2, bar);
+    if (OP == GDN && merge) {
+      if (n > 0)
+        bulk_g2s(smem_u32(ax + Lay.aux_kl), a.klog + lh * Lay.Mcap * DK, (uint32_t)n * DK * 2,
+                 bar);
+      bulk_g2s(smem_u32(ax + Lay.aux_kl + n * DK * 2), a.k + sh * DK, DK * 2, bar);
+    }
+    if (with_coef_now)
+      bulk_g2s(smem_u32(ax + Lay.aux_coef), a.coef + sh * a.CB, (merge ? Lay.CB : Lay.P0) * 4u,
+               bar);
+  } else {
+    uint32_t bytes = 2u * DK * 2u + DV * 2u + (OP != GDN ? DK * 4u : 0u);
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_g2s(smem_u32(ax + Lay.e_kq), a.k + sh * DK, DK * 2, bar);
+    bulk_g2s(smem_u32(ax + Lay.e_kq + DK * 2), a.q + sh * DK, DK * 2, bar);
+    bulk_g2s(smem_u32(ax + Lay.e_v), a.v + sh * DV, DV * 2, bar);
+    if (OP != GDN) bulk_g2s(smem_u32(ax + Lay.e_g), a.g + sh * DK, DK * 4, bar);
+  }
+}
+
+template <int OP, int DK, int DV>
+__device__ __forceinline__ void issue_coef(const StepArgs& a, const Layout& Lay, const UnitPos& p,
+                                           unsigned char* ax, uint32_t bar) {
+  const StepItem it = a.items[p.row];
+  const bool merge = (it.n + 1 == a.M);
+  bulk_g2s(smem_u32(ax + Lay.aux_coef), a.coef + (size_t)p.sh * a.CB,
+           (merge ? Lay.CB : Lay.P0) * 4u, bar);
+}
+
+// ---------------------------------------------------------- AppendDecode ----
+template <int OP, int DK, int DV>
+__device__ __forceinline__ void consume_append(const StepArgs& a, const Layout& Lay,
+                                               const UnitPos& p, int vt, const float* T,
+                                               unsigned char* ax, int lane) {
+  constexpr int VEC = DK / 32;
+  constexpr bool DELTA = OP != RWKV6;
+  const StepItem it = a.items[p.row];
+  const int n = it.n;
+  const bool merge = (n + 1 == a.M);
+  const float* cf = reinterpret_cast<const float*>(ax + Lay.aux_coef);
+  const int vecA = HDR + 2 * Lay.Mcap4;
+
+  float kv[VEC], qv[VEC];
+  if constexpr (OP == GDN) {
+    const uint16_t* kq16 = reinterpret_cast<const uint16_t*>(ax + Lay.aux_kq);
+    ldvec_bf16<VEC>(kv, kq16 + lane * VEC);
+    ldvec_bf16<VEC>(qv, kq16 + DK + lane * VEC);
+  } else if constexpr (OP == KDA) {
+    ldvec<VEC>(kv, cf + vecA + lane * VEC);
+    ldvec<VEC>(qv, cf + vecA + DK + lane * VEC);
+  } else {
+    ldvec<VEC>(kv, cf + vecA + lane * VEC);   // r̂
+  }
+
+  // pass 1: per-row partial dot products over this lane's key channels
+  float pa[32], pb[32];
+#pragma unroll
+  for (int r = 0; r < 32; ++r) {
+    float t[VEC];
+    ldvec<VEC>(t, T + r * DK + lane * VEC);
+    float x = 0.f, y = 0.f;
+#pragma unroll
+    for (int c = 0; c < VEC; ++c) {
+      x += t[c] * kv[c];
+      if (DELTA) y += t[c] * qv[c];
+    }
+    pa[r] = x;
+    pb[r] = y;
+  }
+  const float A = reduce_scatter32(pa, lane);
+  float B = 0.f;
+  if constexpr (DELTA) B = reduce_scatter32(pb, lane);
+
+  // row epilogue on lane = row
+  const int col = vt * BV + lane;
+  const size_t oidx = (size_t)p.sh * DV + col;
+  if constexpr (DELTA) {
+    const float* U = reinterpret_cast<const float*>(ax + Lay.aux_U);
+    float x = (OP == GDN) ? cf[0] * A : A;
+    float ob = (OP == GDN) ? cf[0] * B : B;
+    for (int j = 0; j < n; ++j) {
+      const float uj = U[j * DV + col];
+      x += cf[HDR + j] * uj;
+      ob += cf[HDR + Lay.Mcap4 + j] * uj;
+    }
+    const float vv = bf16f(reinterpret_cast<const uint16_t*>(ax + Lay.aux_v)[col]);
+    const float u = cf[2] * (vv - x);
+    store_out(a, oidx, a.scale * (ob + cf[1] * u));
+    if (!merge) {
+      const size_t lh = (size_t)it.slot * a.H + p.h;
+      static_cast<float*>(a.alog)[(lh * Lay.Mcap + n) * DV + col] = u;
+    } else {
+      reinterpret_cast<float*>(ax + Lay.aux_U)[n * DV + col] = u;
+      __syncwarp();
+    }
+  } else {
+    const uint16_t* V = reinterpret_cast<const uint16_t*>(ax + Lay.aux_U);
+    float o = A;
+    for (int j = 0; j < n; ++j) o += cf[HDR + j] * bf16f(V[j * DV + col]);
+    o += cf[3] * bf16f(V[n * DV + col]);
+    store_out(a, oidx, a.scale * o);
+  }
+  if (!merge) return;
+
+  // merge: S̄[slot] rows = D ⊙ S̄[base] rows + Σ_{j<=n} a_j[row] K̃_j
+  float D[VEC];
+  if constexpr (OP == GDN) {
+#pragma unroll
+    for (int c = 0; c < VEC; ++c) D[c] = cf[0];
+  } else {
+    ldvec<VEC>(D, cf + Lay.P0 + lane * VEC);
+  }
+  float* dst = a.Sbar + (((size_t)it.slot * a.H + p.h) * DV + vt * BV) * DK + lane * VEC;
+#pragma unroll 1
+  for (int rb = 0; rb < 4; ++rb) {
+    float acc[8][VEC];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float t[VEC];
+      ldvec<VEC>(t, T + (rb * 8 + i) * DK + lane * VEC);
+#pragma unroll
+      for (int c = 0; c < VEC; ++c) acc[i][c] = D[c] * t[c];
+    }
+#pragma unroll 2
+    for (int j = 0; j <= n; ++j) {
+      float K[VEC];
+      if constexpr (OP == GDN) {
+        ldvec_bf16<VEC>(K, reinterpret_cast<const uint16_t*>(ax + Lay.aux_kl) + j * DK + lane * VEC);
+        const float w = cf[Lay.P0 + j];
+#pragma unroll
+        for (int c = 0; c < VEC; ++c) K[c] *= w;
+      } else {
+        ldvec<VEC>(K, cf + Lay.P0 + DK + j * DK + lane * VEC);
+      }
+      float uu[8];
+      if constexpr (DELTA) {
+        const float* U = reinterpret_cast<const float*>(ax + Lay.aux_U) + j * DV + vt * BV + rb * 8;
+        const float4 u0 = *reinterpret_cast<const float4*>(U);
+        const float4 u1 = *reinterpret_cast<const float4*>(U + 4);
+        uu[0] = u0.x; uu[1] = u0.y; uu[2] = u0.z; uu[3] = u0.w;
+        uu[4] = u1.x; uu[5] = u1.y; uu[6] = u1.z; uu[7] = u1.w;
+      } else {
+        const uint4 w = *reinterpret_cast<const uint4*>(
+            reinterpret_cast<const uint16_t*>(ax + Lay.aux_U) + j * DV + vt * BV + rb * 8);
+        uu[0] = bf16lo(w.x); uu[1] = bf16hi(w.x); uu[2] = bf16lo(w.y); uu[3] = bf16hi(w.y);
+        uu[4] = bf16lo(w.z); uu[5] = bf16hi(w.z); uu[6] = bf16lo(w.w); uu[7] = bf16hi(w.w);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int c = 0; c < VEC; ++c) acc[i][c] += uu[i] * K[c];
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) stvec_cs<VEC>(dst + (size_t)(rb * 8 + i) * DK, acc[i]);
+  }
+}
+
+// ------------------------------------------------------------- EagerStep ----
+template <int OP, int DK, int DV>
+__device__ __forceinline__ void consume_eager(const StepArgs& a, const Layout& Lay,
+                                              const UnitPos& p, int vt, const float* T,
+                                              unsigned char* ax, int lane, float g_s, float beta_s) {
+  constexpr int VEC = DK / 32;
+  const StepItem it = a.items[p.row];
+  float kv[VEC], qv[VEC], D[VEC], kh[VEC], qh[VEC];
+  const uint16_t* kq16 = reinterpret_cast<const uint16_t*>(ax + Lay.e_kq);
+  ldvec_bf16<VEC>(kv, kq16 + lane * VEC);
+  ldvec_bf16<VEC>(qv, kq16 + DK + lane * VEC);
+  float sc = 0.f;   // k·q (delta ops) or Σ r bonus k (RWKV6)
+  if constexpr (OP == GDN) {
+    const float al = expf(g_s);
+#pragma unroll
+    for (int c = 0; c < VEC; ++c) {
+      D[c] = al; kh[c] = kv[c]; qh[c] = qv[c];
+      sc += kv[c] * qv[c];
+    }
+  } else {
+    float gv[VEC];
+    ldvec<VEC>(gv, reinterpret_cast<const float*>(ax + Lay.e_g) + lane * VEC);
+    if constexpr (OP == KDA) {
+#pragma unroll
+      for (int c = 0; c < VEC; ++c) {
+        D[c] = expf(gv[c]);
+        kh[c] = D[c] * kv[c];
+        qh[c] = D[c] * qv[c];
+        sc += kv[c] * qv[c];
+      }
+    } else {
+      float bon[VEC];
+      ldvec<VEC>(bon, a.bonus + (size_t)p.h * DK + lane * VEC);
+#pragma unroll
+      for (int c = 0; c < VEC; ++c) {
+        D[c] = expf(gv[c]);
+        kh[c] = qv[c];
+        qh[c] = 0.f;
+        sc += qv[c] * bon[c] * kv[c];
+      }
+    }
+  }
+  sc = warp_sum(sc);
+
+  float pa[32], pb[32];
+#pragma unroll
+  for (int r = 0; r < 32; ++r) {
+    float t[VEC];
+    ldvec<VEC>(t, T + r * DK + lane * VEC);
+    float x = 0.f, y = 0.f;
+#pragma unroll
+    for (int c = 0; c < VEC; ++c) {
+      x += t[c] * kh[c];
+      if (OP != RWKV6) y += t[c] * qh[c];
+    }
+    pa[r] = x;
+    pb[r] = y;
+  }
+  const float A = reduce_scatter32(pa, lane);
+  float B = 0.f;
+  if constexpr (OP != RWKV6) B = reduce_scatter32(pb, lane);
+  const int col = vt * BV + lane;
+  const float vv = bf16f(reinterpret_cast<const uint16_t*>(ax + Lay.e_v)[col]);
+  float u;
+  if constexpr (OP == GDN) {
+    u = beta_s * (vv - D[0] * A);
+    store_out(a, (size_t)p.sh * DV + col, a.scale * (D[0] * B + sc * u));
+  } else if constexpr (OP == KDA) {
+    u = beta_s * (vv - A);
+    store_out(a, (size_t)p.sh * DV + col, a.scale * (B + sc * u));
+  } else {
+    u = vv;
+    store_out(a, (size_t)p.sh * DV + col, a.scale * (A + sc * vv));
+  }
+  float* dst = a.Sbar + (((size_t)it.slot * a.H + p.h) * DV + vt * BV) * DK + lane * VEC;
+#pragma unroll 4
+  for (int r = 0; r < 32; ++r) {
+    const float ur = __shfl_sync(0xffffffffu, u, r);
+    float t[VEC];
+    ldvec<VEC>(t, T + r * DK + lane * VEC);
+#pragma unroll
+    for (int c = 0; c < VEC; ++c) t[c] = D[c] * t[c] + ur * kv[c];
+    stvec_cs<VEC>(dst + (size_t)r * DK, t);
+  }
+}
+
+// ----------------------------------------------------------------- kernel ---
+template <int OP, int DK, int DV, int MODE>
+__global__ void __launch_bounds__(PIPE_THREADS, 1) pipe_kernel(const __grid_constant__ StepArgs a) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  constexpr uint32_t TILE_BYTES = BV * DK * 4;
+  const Layout Lay = make_layout(OP, a.M, DK, DV);
+  const int NS = a.ns, NA = a.na, G = a.G;
+  const uint32_t aux_bytes = (MODE == APPEND) ? Lay.aux_bytes : Lay.e_bytes;
+  const Bars bars{smem_u32(smem), NS, NA};
+  float* tiles = reinterpret_cast<float*>(smem + BAR_BYTES);
+  unsigned char* auxm = smem + BAR_BYTES + (size_t)NS * TILE_BYTES;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(bars.full(s), 1);
+      mbar_init(bars.empty(s), 1);
+    }
+    for (int x = 0; x < NA; ++x) {
+      mbar_init(bars.afull(x), 1);
+      mbar_init(bars.aempty(x), G);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  const int n_units = a.rows * a.H * a.NG;
+  const int my_units =
+      (int)blockIdx.x < n_units ? (n_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  const int my_tiles = my_units * G;
+
+  if (warp == NCW) {
+    // ------------------------------------------------------------ producer
+    if (lane != 0) return;
+    const uint64_t pol = policy_evict_first();
+    bool primary_done = (MODE != APPEND);
+    int pending_from = 0;   // units [pending_from, ka) still need their coefficient copy
+    int ti = 0, ka = 0;
+    bool ok = true;
+    while (ti < my_tiles) {
+      const int kt = ti / G;
+      if (!primary_done && (ti >= NS || (kt == ka && ka >= NA))) {
+        // the next wait needs consumers to make progress, and they need coefficients
+        pdl_wait_primary();
+        primary_done = true;
+        for (int u = pending_from; u < ka; ++u) {
+          const UnitPos p = unit_pos(a, (int)blockIdx.x + u * (int)gridDim.x);
+          issue_coef<OP, DK, DV>(a, Lay, p, auxm + (size_t)(u % NA) * aux_bytes,
+                                 bars.afull(u % NA));
+        }
+        pending_from = ka;
+      }
+      if (kt == ka) {
+        const int x = ka % NA;
+        if (!mbar_wait(bars.aempty(x), ((ka / NA) & 1) ^ 1, a.status, DEV_TIMEOUT_EMPTY)) {
+          ok = false;
+          break;
+        }
+        const UnitPos p = unit_pos(a, (int)blockIdx.x + ka * (int)gridDim.x);
+        issue_aux<OP, DK, DV, MODE>(a, Lay, p, auxm + (size_t)x * aux_bytes, bars.afull(x),
+                                    primary_done);
+        ++ka;
+      }
+      const int s = ti % NS;
+      if (!mbar_wait(bars.empty(s), ((ti / NS) & 1) ^ 1, a.status, DEV_TIMEOUT_EMPTY)) {
+        ok = false;
+        break;
+      }
+      const UnitPos p = unit_pos(a, (int)blockIdx.x + kt * (int)gridDim.x);
+      const int vt = p.grp * G + (ti - kt * G);
+      const int base = (MODE == APPEND) ? a.items[p.row].base : a.items[p.row].slot;
+      const float* src = a.Sbar + (((size_t)base * a.H + p.h) * DV + vt * BV) * DK;
+      mbar_arrive_expect_tx(bars.full(s), TILE_BYTES);
+      bulk_g2s_hint(smem_u32(tiles + (size_t)s * BV * DK), src, TILE_BYTES, bars.full(s), pol);
+      ++ti;
+    }
+    if (ok && !primary_done) {
+      pdl_wait_primary();
+      for (int u = pending_from; u < ka; ++u) {
+        const UnitPos p = unit_pos(a, (int)blockIdx.x + u * (int)gridDim.x);
+        issue_coef<OP, DK, DV>(a, Lay, p, auxm + (size_t)(u % NA) * aux_bytes,
+                               bars.afull(u % NA));
+      }
+    }
+    if (!ok) {
+      // an error was recorded: let the copies already in flight land before exiting
+      if (!primary_done) pdl_wait_primary();
+      for (int t = ti - NS > 0 ? ti - NS : 0; t < ti; ++t) mbar_drain(bars.full(t % NS), (t / NS) & 1);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  for (int i = warp; i < my_tiles; i += NCW) {
+    const int kk = i / G;
+    const UnitPos p = unit_pos(a, (int)blockIdx.x + kk * (int)gridDim.x);
+    const int vt = p.grp * G + (i - kk * G);
+    const int x = kk % NA, s = i % NS;
+    float g_s = 0.f, beta_s = 0.f;
+    if constexpr (MODE == EAGER) {
+      if (OP == GDN) g_s = a.g[p.sh];
+      if (OP != RWKV6) beta_s = a.beta[p.sh];
+    }
+    bool ok = mbar_wait(bars.afull(x), (kk / NA) & 1, a.status, DEV_TIMEOUT_AUX);
+    ok = ok && mbar_wait(bars.full(s), (i / NS) & 1, a.status, DEV_TIMEOUT_TILE);
+    if (!__all_sync(0xffffffffu, ok)) break;
+    const float* T = tiles + (size_t)s * BV * DK;
+    unsigned char* ax = auxm + (size_t)x * aux_bytes;
+    if constexpr (MODE == APPEND) consume_append<OP, DK, DV>(a, Lay, p, vt, T, ax, lane);
+    else consume_eager<OP, DK, DV>(a, Lay, p, vt, T, ax, lane, g_s, beta_s);
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(bars.empty(s));
+      mbar_arrive(bars.aempty(x));
+    }
+  }
+}
+
+}  // namespace dl

@@ -1,0 +1,174 @@
+// Slot-level kernels outside the per-token hot loop:
+//   * Merge / ReadState — materialise base + replayed log (DeltaLog page,
+//     "Methodology — Base + Log", merge phase) into S̄ (forced merge) or into a
+//     caller buffer (read-out; the context is unchanged);
+//   * SetState — load initial states into S̄;
+//   * Fork — Flide page, "Research method step by step", second step: a branch
+//     indexes the source's saved state; only the source's log rows are copied.
+#include "dl_device.cuh"
+#include "layout.h"
+#include "launch.h"
+
+namespace dl {
+
+// One CTA per (row, head, value tile), 8 warps x 4 rows.  The logical state of
+// slot s with n log entries and cumulative log-decay Λ_{n-1} is
+//   S = D ⊙ S̄[base] + Σ_{j<n} a_j K̃_j^T,  D = e^{Λ_{n-1}},  K̃_j = k_j ⊙ e^{Λ_{n-1} - Λ_j}
+// (scalar decay for GDN, per key channel for KDA and RWKV6).
+template <int OP, int DK, int DV>
+__global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ SlotListArgs a) {
+  constexpr int VEC = DK / 32, NVT = DV / BV;
+  constexpr bool PERKEY = OP != GDN;
+  extern __shared__ __align__(16) float sm[];
+  const int b = blockIdx.x;
+  const int vt = b % NVT, sh = b / NVT, h = sh % a.H, row = sh / a.H;
+  const StepItem it = a.items[row];
+  const int n = it.n, Mcap = a.Mcap;
+  const size_t lh = (size_t)it.slot * a.H + h;
+  float* Kt = sm;                    // [n][DK]
+  float* U = sm + n * DK;            // [n][BV]
+  float* sD = U + n * BV;            // [DK]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if constexpr (PERKEY) {
+    for (int i = tid; i < DK; i += 256) {
+      const float Lc = n > 0 ? a.Llog[(lh * Mcap + n - 1) * DK + i] : 0.f;
+      sD[i] = expf(Lc);
+    }
+    for (int idx = tid; idx < n * DK; idx += 256) {
+      const int j = idx / DK, i = idx - j * DK;
+      const float Lc = a.Llog[(lh * Mcap + n - 1) * DK + i];
+      Kt[idx] = bf16f(a.klog[(lh * Mcap + j) * DK + i]) * expf(Lc - a.Llog[(lh * Mcap + j) * DK + i]);
+    }
+  } else {
+    const float Lc = n > 0 ? a.Llog[lh * Mcap + n - 1] : 0.f;
+    for (int i = tid; i < DK; i += 256) sD[i] = expf(Lc);
+    for (int idx = tid; idx < n * DK; idx += 256) {
+      const int j = idx / DK, i = idx - j * DK;
+      Kt[idx] = bf16f(a.klog[(lh * Mcap + j) * DK + i]) * expf(Lc - a.Llog[lh * Mcap + j]);
+    }
+  }
+  for (int idx = tid; idx < n * BV; idx += 256) {
+    const int j = idx / BV, r = idx - j * BV;
+    const size_t src = (lh * Mcap + j) * DV + vt * BV + r;
+    U[idx] = (OP == RWKV6) ? bf16f(static_cast<const uint16_t*>(a.alog)[src])
+                           : static_cast<const float*>(a.alog)[src];
+  }
+  __syncthreads();
+
+  float D[VEC];
+  ldvec<VEC>(D, sD + lane * VEC);
+  for (int r = warp * 4; r < warp * 4 + 4; ++r) {
+    const int vrow = vt * BV + r;
+    float t[VEC];
+    ldvec<VEC>(t, a.Sbar + (((size_t)it.base * a.H + h) * DV + vrow) * DK + lane * VEC);
+#pragma unroll
+    for (int c = 0; c < VEC; ++c) t[c] *= D[c];
+    for (int j = 0; j < n; ++j) {
+      const float uj = U[j * BV + r];
+#pragma unroll
+      for (int c = 0; c < VEC; ++c) t[c] += uj * Kt[j * DK + lane * VEC + c];
+    }
+    float* dst = a.S_out ? a.S_out + (((size_t)row * a.H + h) * DV + vrow) * DK
+                         : a.Sbar + (((size_t)it.slot * a.H + h) * DV + vrow) * DK;
+    stvec_cs<VEC>(dst + lane * VEC, t);
+  }
+  if (!a.S_out && h == 0 && vt == 0 && tid == 0) {
+    a.nlog[it.slot] = 0;
+    a.base_of[it.slot] = it.slot;
+  }
+}
+
+// One CTA per (row, head): copy DV x DK floats of S_in into S̄[slot].
+template <int DK, int DV>
+__global__ void __launch_bounds__(256) set_state_kernel(const __grid_constant__ SlotListArgs a) {
+  const int sh = blockIdx.x, h = sh % a.H, row = sh / a.H;
+  const StepItem it = a.items[row];
+  const float4* src = reinterpret_cast<const float4*>(a.S_in + (size_t)sh * DV * DK);
+  float4* dst = reinterpret_cast<float4*>(a.Sbar + ((size_t)it.slot * a.H + h) * DV * DK);
+  for (int i = threadIdx.x; i < DV * DK / 4; i += 256) dst[i] = src[i];
+  if (h == 0 && threadIdx.x == 0) {
+    a.nlog[it.slot] = 0;
+    a.base_of[it.slot] = it.slot;
+  }
+}
+
+// One CTA per (destination, head): copy the source's log rows 0..src_n-1.
+template <int OP, int DK, int DV>
+__global__ void __launch_bounds__(128) fork_kernel(const __grid_constant__ SlotListArgs a) {
+  constexpr int ESA = (OP == RWKV6) ? 2 : 4;
+  constexpr int LW = (OP == GDN) ? 1 : DK;    // Λ floats per entry
+  const int b = blockIdx.x, h = b % a.H, row = b / a.H;
+  const int dst = a.items[row].slot;
+  const int n = a.src_n, Mcap = a.Mcap;
+  const size_t ls = (size_t)a.src_slot * a.H + h, ld = (size_t)dst * a.H + h;
+  {
+    const size_t words = (size_t)n * DV * ESA / 16;
+    const uint4* s = reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(a.alog) +
+                                                    ls * Mcap * DV * ESA);
+    uint4* d = reinterpret_cast<uint4*>(static_cast<unsigned char*>(a.alog) + ld * Mcap * DV * ESA);
+    for (size_t i = threadIdx.x; i < words; i += 128) d[i] = s[i];
+  }
+  {
+    const size_t words = (size_t)n * DK * 2 / 16;
+    const uint4* s = reinterpret_cast<const uint4*>(a.klog + ls * Mcap * DK);
+    uint4* d = reinterpret_cast<uint4*>(a.klog + ld * Mcap * DK);
+    for (size_t i = threadIdx.x; i < words; i += 128) d[i] = s[i];
+  }
+  for (int i = threadIdx.x; i < n * LW; i += 128)
+    a.Llog[ld * Mcap * LW + i] = a.Llog[ls * Mcap * LW + i];
+  if (h == 0 && threadIdx.x == 0) {
+    a.nlog[dst] = n;
+    a.base_of[dst] = a.src_base;
+  }
+}
+
+template <int OP, int DK>
+static cudaError_t merge_dispatch(const SlotListArgs& a, cudaStream_t s) {
+  constexpr int NVT = DK / BV;
+  int nmax = 0;
+  for (int i = 0; i < a.rows; ++i) nmax = a.items[i].n > nmax ? a.items[i].n : nmax;
+  const size_t smem = ((size_t)nmax * DK + (size_t)nmax * BV + DK) * sizeof(float);
+  merge_kernel<OP, DK, DK><<<a.rows * a.H * NVT, 256, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_merge(int op, int dk, const SlotListArgs& a, cudaStream_t s) {
+  if (a.rows <= 0) return cudaSuccess;
+  if (dk == 64) {
+    if (op == GDN) return merge_dispatch<GDN, 64>(a, s);
+    if (op == KDA) return merge_dispatch<KDA, 64>(a, s);
+    return merge_dispatch<RWKV6, 64>(a, s);
+  }
+  if (op == GDN) return merge_dispatch<GDN, 128>(a, s);
+  if (op == KDA) return merge_dispatch<KDA, 128>(a, s);
+  return merge_dispatch<RWKV6, 128>(a, s);
+}
+
+cudaError_t launch_set_state(int dk, int dv, const SlotListArgs& a, cudaStream_t s) {
+  if (a.rows <= 0) return cudaSuccess;
+  (void)dv;
+  if (dk == 64) set_state_kernel<64, 64><<<a.rows * a.H, 256, 0, s>>>(a);
+  else set_state_kernel<128, 128><<<a.rows * a.H, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <int OP, int DK>
+static cudaError_t fork_dispatch(const SlotListArgs& a, cudaStream_t s) {
+  fork_kernel<OP, DK, DK><<<a.rows * a.H, 128, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fork(int op, int dk, const SlotListArgs& a, cudaStream_t s) {
+  if (a.rows <= 0) return cudaSuccess;
+  if (dk == 64) {
+    if (op == GDN) return fork_dispatch<GDN, 64>(a, s);
+    if (op == KDA) return fork_dispatch<KDA, 64>(a, s);
+    return fork_dispatch<RWKV6, 64>(a, s);
+  }
+  if (op == GDN) return fork_dispatch<GDN, 128>(a, s);
+  if (op == KDA) return fork_dispatch<KDA, 128>(a, s);
+  return fork_dispatch<RWKV6, 128>(a, s);
+}
+
+}  // namespace dl
