@@ -35,6 +35,10 @@ WORKLOADS = {
                 desc="KDA decode B=128 H=32 d_k=d_v=128 fp32 state, 512 tokens"),
     "rwkv6": dict(op=2, B=128, H=40, d=64, tokens=512, M=16, seed=1003,
                   desc="RWKV6 decode B=128 H=40 head 64 fp32 state, 512 tokens"),
+    "fork": dict(op=0, B=512, H=16, d=128, tokens=256, M=16, seed=1004, requests=64,
+                 branches=8, ctx_tokens=2048,
+                 desc="forked GDN decode: 64 requests x 2048 context tokens, 8 branches each "
+                      "(512 branch slots) of U{16..256} tokens, H=16 d_k=d_v=128"),
 }
 METRIC = "state-update tokens·heads/s and achieved HBM GB/s vs ~8 TB/s; write bytes/step"
 
@@ -247,7 +251,13 @@ def run_ours(args):
     from linear_attention_recurrent_gdn_gb300 import deltalog as dl
     from linear_attention_recurrent_gdn_gb300 import inputs as gen
 
-    w = WORKLOADS[args.workload]
+    w = dict(WORKLOADS[args.workload])
+    if args.B:
+        w["B"] = args.B
+        w["desc"] += " [profiling override B=%d]" % args.B
+    if args.tokens:
+        w["tokens"] = args.tokens
+        w["desc"] += " [profiling override tokens=%d]" % args.tokens
     op, B, H, d, T = w["op"], w["B"], w["H"], w["d"], w["tokens"]
     M = args.M or w["M"]
     seed = w["seed"] + 7919 * rank      # each rank decodes its own batch shard
@@ -368,6 +378,10 @@ def run_ours(args):
         result["note_writes"] = "algorithmic bytes; DRAM-measured writes are in profiles/"
 
     # ---- end to end through the public API with host buffers
+    if args.no_e2e:
+        if rank == 0:
+            print(json.dumps(result), flush=True)
+        return 0
     pin = {k: (v.cpu().pin_memory() if v is not None else None) for k, v in x.items()}
     hout = torch.empty((T, B, H, d), dtype=torch.bfloat16).pin_memory()
     c = make_ctx(M)
@@ -407,6 +421,80 @@ def run_ours(args):
     return 0
 
 
+def run_fork(args):
+    """Forked decode: bases are built once (setup, untimed); one bench step =
+    fork every request into its branches (by index, no state copy) + the
+    ragged branch decode until the longest branch ends."""
+    import numpy as np
+    import torch
+    rank, world, dist = dist_setup("cuda")
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    from linear_attention_recurrent_gdn_gb300 import build
+    if rank == 0:
+        build.build()
+    barrier(dist)
+    from linear_attention_recurrent_gdn_gb300 import deltalog as dl
+    from linear_attention_recurrent_gdn_gb300 import inputs as gen
+    w = WORKLOADS["fork"]
+    R, NB, H, d, M, Tc = w["requests"], w["branches"], w["H"], w["d"], w["M"], w["ctx_tokens"]
+    seed = w["seed"] + 7919 * rank
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    lens = np.random.default_rng(seed).integers(16, 257, size=R * NB)
+    order = np.argsort(-lens, kind="stable")
+    Tq = int(lens.max())
+    counts = [int((lens > t).sum()) for t in range(Tq)]
+    S = R + R * NB
+    ctx = dl.DeltaLog(0, S, H, d, d, M, stream=stream.cuda_stream)
+    ctx.set_state(list(range(R)), gen.initial_state(R, H, d, d, seed, device=dev))
+    t0 = time.time()
+    for t in range(Tc):
+        x = gen.step_inputs(0, R, H, d, d, seed, t, device=dev)
+        ctx.step(list(range(R)), x["q"], x["k"], x["v"], x["g"], x["beta"])
+    torch.cuda.synchronize()
+    log("bases built in %.1fs" % (time.time() - t0))
+    xq = gen.make_inputs(0, Tq, R * NB, H, d, d, seed + 1, device=dev)
+    out = torch.empty((R * NB, H, d), dtype=torch.bfloat16, device=dev)
+    act_slots = [[R + int(b) for b in order[:c]] for c in counts]
+    branches = [[R + r * NB + i for i in range(NB)] for r in range(R)]
+
+    def one():
+        for r in range(R):
+            ctx.fork(r, branches[r])
+        for t in range(Tq):
+            c = counts[t]
+            ctx.step(act_slots[t], xq["q"][t][:c], xq["k"][t][:c], xq["v"][t][:c],
+                     xq["g"][t][:c], xq["beta"][t][:c], out[:c])
+    for _ in range(args.warmup):
+        one()
+    barrier(dist)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        one()
+    e1.record(stream)
+    e1.synchronize()
+    ms = reduce_max(dist, e0.elapsed_time(e1) / args.steps, dev)
+    units = int(lens.sum()) * H
+    result = {"metric": METRIC, "value": units * world / (ms / 1e3), "unit": "tokens·heads/s",
+              "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+              "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+              "data": "synthetic",
+              "config": {"workload": w["desc"], "op": "gdn", "requests": R, "branches": NB,
+                         "H": H, "d_k": d, "d_v": d, "M": M, "ctx_tokens": Tc,
+                         "branch_tokens": int(lens.sum()),
+                         "l2": "inputs larger than L2 (576 slots x 1 MiB state)"},
+              "gpu_launches": (R + 2 * Tq) * args.steps}
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    ctx.close()
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -417,9 +505,14 @@ def main():
     ap.add_argument("--M", type=int, default=0)
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--B", type=int, default=0, help="override the batch (profiling runs only)")
+    ap.add_argument("--tokens", type=int, default=0, help="override the token count (profiling)")
+    ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload == "fork":
+        return run_fork(args)
     return run_ours(args)
 
 

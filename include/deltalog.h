@@ -195,6 +195,21 @@ dl_status dl_read_state(dl_ctx *ctx, const int32_t *slots, int32_t n, float *S_o
  * device table disagrees with the host table. */
 dl_status dl_get_meta(dl_ctx *ctx, int32_t *n_log, int32_t *base_of);
 
+/* Prefix checkpoints (Flide page, "Research method step by step", fourth step:
+ * a growing agent trace resumes from a checkpoint saved at a matching prefix).
+ * A checkpoint is the exact DeltaLog representation of a slot: the dense base
+ * it reads (fp32 [H, d_v, d_k]), its log rows (value side, keys, log-decays)
+ * and its log length, so that a restored slot continues bit for bit as the
+ * saved one would have.  dl_checkpoint_bytes gives the size of one slot's
+ * checkpoint; buffers are device memory owned by the caller, 16-byte aligned,
+ * slot i at offset i * dl_checkpoint_bytes. */
+int64_t dl_checkpoint_bytes(const dl_ctx *ctx);
+dl_status dl_checkpoint_save(dl_ctx *ctx, const int32_t *slots, int32_t n, void *buf);
+/* Restore: each listed slot becomes the saved state (it owns a private copy of
+ * the saved base).  Frozen slots return DL_EBUSY.  Synchronises the stream
+ * (the saved log lengths are read back to update the host table). */
+dl_status dl_checkpoint_load(dl_ctx *ctx, const int32_t *slots, int32_t n, const void *buf);
+
 /* Synchronise the stream and report any CUDA or device-side error. */
 dl_status dl_sync(dl_ctx *ctx);
 

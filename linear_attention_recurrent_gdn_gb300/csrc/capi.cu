@@ -21,6 +21,9 @@
 #include "launch.h"
 #include "layout.h"
 
+extern "C" dl_status dl_table_set_n(dl_table* t, const int32_t* slots, int32_t n,
+                                   const int32_t* len);
+
 namespace {
 
 constexpr int NKIND = 4;   // timing kinds: ReplayPrep, AppendDecode, EagerStep, Merge/ReadState
@@ -582,6 +585,100 @@ dl_status dl_read_state(dl_ctx* c, const int32_t* slots, int32_t n, float* S_out
   rc = dl_table_check(c->table, slots, n);
   if (rc != DL_OK) return set_err(c, rc, "dl_read_state: invalid slot list");
   return merge_or_read(c, slots, n, S_out);
+}
+
+struct CkptLayout {
+  size_t S, A, K, L, N, total;
+};
+
+static CkptLayout ckpt_layout(const dl_ctx* c) {
+  const dl_config& f = c->cfg;
+  const size_t H = f.num_heads, Mcap = c->L.Mcap;
+  auto r16 = [](size_t x) { return (x + 15) & ~(size_t)15; };
+  CkptLayout k;
+  k.S = 0;
+  k.A = k.S + r16(H * f.d_v * f.d_k * 4);
+  k.K = k.A + r16(H * Mcap * f.d_v * (f.op == DL_RWKV6 ? 2 : 4));
+  k.L = k.K + r16(H * Mcap * f.d_k * 2);
+  k.N = k.L + r16(H * Mcap * (f.op == DL_GDN ? 1 : f.d_k) * 4);
+  k.total = k.N + 16;
+  return k;
+}
+
+int64_t dl_checkpoint_bytes(const dl_ctx* c) { return c ? (int64_t)ckpt_layout(c).total : -1; }
+
+dl_status dl_checkpoint_save(dl_ctx* c, const int32_t* slots, int32_t n, void* buf) {
+  dl_status rc = check_ctx(c);
+  if (rc != DL_OK) return rc;
+  if (n < 0 || (n > 0 && (!buf || !aligned16(buf)))) return set_err(c, DL_EINVAL, "bad buffer");
+  rc = dl_table_check(c->table, slots, n);
+  if (rc != DL_OK) return set_err(c, rc, "dl_checkpoint_save: invalid slot list");
+  const CkptLayout k = ckpt_layout(c);
+  const dl_config& f = c->cfg;
+  const size_t H = f.num_heads, Mcap = c->L.Mcap;
+  const size_t sS = H * f.d_v * f.d_k * 4, sA = H * Mcap * f.d_v * (f.op == DL_RWKV6 ? 2 : 4),
+               sK = H * Mcap * f.d_k * 2, sL = H * Mcap * (f.op == DL_GDN ? 1 : f.d_k) * 4;
+  std::vector<int32_t> nl(f.num_slots), bo(f.num_slots);
+  dl_table_get(c->table, nl.data(), bo.data(), nullptr);
+  for (int32_t i = 0; i < n; ++i) {
+    unsigned char* dst = static_cast<unsigned char*>(buf) + (size_t)i * k.total;
+    const size_t s = slots[i], b = bo[slots[i]];
+    DL_CUDA(cudaMemcpyAsync(dst + k.S, reinterpret_cast<unsigned char*>(c->Sbar) + b * sS, sS,
+                            cudaMemcpyDeviceToDevice, c->stream), "checkpoint copy");
+    DL_CUDA(cudaMemcpyAsync(dst + k.A, static_cast<unsigned char*>(c->alog) + s * sA, sA,
+                            cudaMemcpyDeviceToDevice, c->stream), "checkpoint copy");
+    DL_CUDA(cudaMemcpyAsync(dst + k.K, reinterpret_cast<unsigned char*>(c->klog) + s * sK, sK,
+                            cudaMemcpyDeviceToDevice, c->stream), "checkpoint copy");
+    DL_CUDA(cudaMemcpyAsync(dst + k.L, reinterpret_cast<unsigned char*>(c->Llog) + s * sL, sL,
+                            cudaMemcpyDeviceToDevice, c->stream), "checkpoint copy");
+    DL_CUDA(cudaMemcpyAsync(dst + k.N, c->nlog + s, 4, cudaMemcpyDeviceToDevice, c->stream),
+            "checkpoint copy");
+  }
+  return DL_OK;
+}
+
+dl_status dl_checkpoint_load(dl_ctx* c, const int32_t* slots, int32_t n, const void* buf) {
+  dl_status rc = check_ctx(c);
+  if (rc != DL_OK) return rc;
+  if (n < 0 || (n > 0 && (!buf || !aligned16(buf)))) return set_err(c, DL_EINVAL, "bad buffer");
+  rc = dl_table_check(c->table, slots, n);
+  if (rc != DL_OK) return set_err(c, rc, "dl_checkpoint_load: invalid slot list");
+  const CkptLayout k = ckpt_layout(c);
+  std::vector<int32_t> ns(n > 0 ? n : 1);
+  for (int32_t i = 0; i < n; ++i)
+    DL_CUDA(cudaMemcpyAsync(&ns[i], static_cast<const unsigned char*>(buf) + (size_t)i * k.total + k.N,
+                            4, cudaMemcpyDeviceToHost, c->stream), "checkpoint read");
+  DL_CUDA(cudaStreamSynchronize(c->stream), "stream sync");
+  for (int32_t i = 0; i < n; ++i)
+    if (ns[i] < 0 || ns[i] >= c->cfg.merge_interval)
+      return set_err(c, DL_EINVAL, "checkpoint %d holds log length %d, not valid for M=%d", i, ns[i],
+                     c->cfg.merge_interval);
+  rc = dl_table_reset(c->table, slots, n);     // validates frozen slots, owns base, n = 0
+  if (rc != DL_OK) return set_err(c, rc, "dl_checkpoint_load: frozen slot");
+  const dl_config& f = c->cfg;
+  const size_t H = f.num_heads, Mcap = c->L.Mcap;
+  const size_t sS = H * f.d_v * f.d_k * 4, sA = H * Mcap * f.d_v * (f.op == DL_RWKV6 ? 2 : 4),
+               sK = H * Mcap * f.d_k * 2, sL = H * Mcap * (f.op == DL_GDN ? 1 : f.d_k) * 4;
+  for (int32_t i = 0; i < n; ++i) {
+    const unsigned char* src = static_cast<const unsigned char*>(buf) + (size_t)i * k.total;
+    const size_t s = slots[i];
+    DL_CUDA(cudaMemcpyAsync(reinterpret_cast<unsigned char*>(c->Sbar) + s * sS, src + k.S, sS,
+                            cudaMemcpyDeviceToDevice, c->stream), "restore copy");
+    DL_CUDA(cudaMemcpyAsync(static_cast<unsigned char*>(c->alog) + s * sA, src + k.A, sA,
+                            cudaMemcpyDeviceToDevice, c->stream), "restore copy");
+    DL_CUDA(cudaMemcpyAsync(reinterpret_cast<unsigned char*>(c->klog) + s * sK, src + k.K, sK,
+                            cudaMemcpyDeviceToDevice, c->stream), "restore copy");
+    DL_CUDA(cudaMemcpyAsync(reinterpret_cast<unsigned char*>(c->Llog) + s * sL, src + k.L, sL,
+                            cudaMemcpyDeviceToDevice, c->stream), "restore copy");
+    DL_CUDA(cudaMemcpyAsync(c->nlog + s, src + k.N, 4, cudaMemcpyDeviceToDevice, c->stream),
+            "restore copy");
+    const int32_t self = (int32_t)s;
+    DL_CUDA(cudaMemcpyAsync(c->base_of + s, &self, 4, cudaMemcpyHostToDevice, c->stream),
+            "restore copy");
+    DL_CUDA(cudaStreamSynchronize(c->stream), "stream sync");   // `self` lives on the host stack
+  }
+  dl_table_set_n(c->table, slots, n, ns.data());
+  return DL_OK;
 }
 
 dl_status dl_sync(dl_ctx* c) {

@@ -144,6 +144,17 @@ dl_status dl_table_reset(dl_table* t, const int32_t* slots, int32_t n) {
   return DL_OK;
 }
 
+// Internal (not in the public header, not exported): set log lengths after a
+// checkpoint restore.
+__attribute__((visibility("hidden"))) dl_status dl_table_set_n(dl_table* t, const int32_t* slots, int32_t n, const int32_t* len) {
+  dl_status rc = dl_table_check(t, slots, n);
+  if (rc != DL_OK) return rc;
+  for (int32_t i = 0; i < n; ++i)
+    if (len[i] < 0 || len[i] >= t->M) return DL_EINVAL;
+  for (int32_t i = 0; i < n; ++i) t->n[slots[i]] = len[i];
+  return DL_OK;
+}
+
 dl_status dl_table_get(const dl_table* t, int32_t* n_log, int32_t* base_of, int32_t* refs) {
   if (!t) return DL_EINVAL;
   for (int32_t s = 0; s < t->S; ++s) {

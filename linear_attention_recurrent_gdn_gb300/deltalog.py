@@ -28,7 +28,7 @@ EXPORTS = [
     "dl_create", "dl_destroy", "dl_set_stream", "dl_set_state", "dl_set_bonus", "dl_fork",
     "dl_step", "dl_step_host", "dl_step_eager", "dl_merge", "dl_read_state", "dl_get_meta",
     "dl_sync", "dl_set_timing", "dl_get_timing", "dl_last_error", "dl_status_str",
-    "dl_abi_version",
+    "dl_abi_version", "dl_checkpoint_bytes", "dl_checkpoint_save", "dl_checkpoint_load",
 ]
 
 
@@ -79,6 +79,9 @@ def _load():
         "dl_last_error": ([P], ctypes.c_char_p),
         "dl_status_str": ([I32], ctypes.c_char_p),
         "dl_abi_version": ([], I32),
+        "dl_checkpoint_bytes": ([P], I64),
+        "dl_checkpoint_save": ([P, P, I32, P], I32),
+        "dl_checkpoint_load": ([P, P, I32, P], I32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -239,6 +242,20 @@ def dl_get_timing(ctx):
     return ms, cnt
 
 
+def dl_checkpoint_bytes(ctx):
+    return int(_lib.dl_checkpoint_bytes(ctx))
+
+
+def dl_checkpoint_save(ctx, slots, buf):
+    a, p, n = _slots(slots)
+    _check(_lib.dl_checkpoint_save(ctx, p, n, _ptr(buf)), ctx)
+
+
+def dl_checkpoint_load(ctx, slots, buf):
+    a, p, n = _slots(slots)
+    _check(_lib.dl_checkpoint_load(ctx, p, n, _ptr(buf)), ctx)
+
+
 def dl_last_error(ctx):
     return _lib.dl_last_error(ctx).decode()
 
@@ -391,6 +408,18 @@ class DeltaLog:
 
     def get_meta(self):
         return dl_get_meta(self._h, self.num_slots)
+
+    def checkpoint_save(self, slots, buf=None):
+        """Save the exact representation of each slot; returns a uint8 device buffer."""
+        a, _, n = _slots(slots)
+        per = dl_checkpoint_bytes(self._h)
+        if buf is None:
+            buf = self.torch.empty(n * per, dtype=self.torch.uint8, device="cuda")
+        dl_checkpoint_save(self._h, a, buf)
+        return buf
+
+    def checkpoint_load(self, slots, buf):
+        dl_checkpoint_load(self._h, slots, buf)
 
     def sync(self):
         dl_sync(self._h)

@@ -1,0 +1,93 @@
+"""GPU checks of properties beyond element-wise parity.
+
+* Batch invariance (Flide page, fourth step: a batch-invariant mode fixes the
+  summation order and per-question boundaries so that load changes do not
+  change bits): every slot-head's arithmetic here is independent of the batch
+  it runs in — the same reduction order whatever the batch size, the value-tile
+  grouping or the launch chunking — so a slot stepped alone and the same slot
+  stepped inside a large batch give bit-identical outputs and states.
+* Prefix checkpoints (Flide page, fourth step: resume from a checkpoint saved
+  at a matching prefix): a restored slot continues bit for bit as the saved
+  slot, also in another context, and both match the oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import OUT_TOL_F32, STATE_TOL, make_case, max_step_rel, oracle_run, rel_err
+from linear_attention_recurrent_gdn_gb300 import build
+from linear_attention_recurrent_gdn_gb300 import inputs as gen
+
+pytestmark = pytest.mark.gpu
+OPS = [gen.GDN, gen.KDA, gen.RWKV6]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+
+
+@pytest.mark.parametrize("op", OPS)
+def test_batch_invariance_bitwise(op):
+    from linear_attention_recurrent_gdn_gb300 import deltalog as dl
+    B, H, d, M, T = 320, 4, 128, 4, 9          # 1280 slot-heads: whole-slot-head units
+    x, S0, bonus = make_case(op, B, H, d, T, seed=400 + op, device="cuda")
+    probe = [0, 77, 319]
+    big = dl.DeltaLog(op, B, H, d, d, M)
+    big.set_state(list(range(B)), S0)
+    small = dl.DeltaLog(op, B, H, d, d, M)      # same slots, stepped one at a time
+    small.set_state(list(range(B)), S0)
+    if bonus is not None:
+        big.set_bonus(bonus)
+        small.set_bonus(bonus)
+    for t in range(T):
+        b = x["beta"][t] if x["beta"] is not None else None
+        o_big = big.step(list(range(B)), x["q"][t], x["k"][t], x["v"][t], x["g"][t], b)
+        for s in probe:
+            sl = slice(s, s + 1)
+            o_one = small.step([s], x["q"][t][sl], x["k"][t][sl], x["v"][t][sl], x["g"][t][sl],
+                               b[sl] if b is not None else None)
+            assert torch.equal(o_one[0], o_big[s]), (t, s)
+    assert torch.equal(big.read_state(probe), small.read_state(probe))
+
+
+@pytest.mark.parametrize("op", OPS)
+@pytest.mark.parametrize("t_save", [8, 11])
+def test_checkpoint_resume_bitwise(op, t_save):
+    """Save mid-window (t_save=11, M=8: 3 log entries) and on a window edge."""
+    from linear_attention_recurrent_gdn_gb300 import deltalog as dl
+    B, H, d, M, T = 2, 3, 64, 8, 25
+    x, S0, bonus = make_case(op, B, H, d, T, seed=500 + op)
+    dev = {k: (v.cuda() if v is not None else None) for k, v in x.items()}
+    ctx = dl.DeltaLog(op, 4, H, d, d, M, out_bf16=False)
+    other = dl.DeltaLog(op, 3, H, d, d, M, out_bf16=False)
+    ctx.set_state([0, 1], S0.cuda())
+    for c in (ctx, other):
+        if bonus is not None:
+            c.set_bonus(bonus.cuda())
+    beta = lambda t, sl: dev["beta"][t][sl] if dev["beta"] is not None else None
+    outs = []
+    for t in range(T):
+        if t == t_save:
+            buf = ctx.checkpoint_save([1])
+            ctx.checkpoint_load([3], buf)       # same context, another slot
+            other.checkpoint_load([2], buf)     # another context
+            n, base_of = ctx.get_meta()
+            assert n[3] == t_save % M and base_of[3] == 3
+        outs.append(ctx.step([0, 1], dev["q"][t], dev["k"][t], dev["v"][t], dev["g"][t],
+                             beta(t, slice(0, 2))).float())
+        if t >= t_save:
+            sl = slice(1, 2)
+            o3 = ctx.step([3], dev["q"][t][sl], dev["k"][t][sl], dev["v"][t][sl],
+                          dev["g"][t][sl], beta(t, sl))
+            o2 = other.step([2], dev["q"][t][sl], dev["k"][t][sl], dev["v"][t][sl],
+                            dev["g"][t][sl], beta(t, sl))
+            assert torch.equal(o3[0], outs[-1][1]) and torch.equal(o2[0], outs[-1][1]), t
+    assert torch.equal(ctx.read_state([1])[0], ctx.read_state([3])[0])
+    assert torch.equal(ctx.read_state([1])[0], other.read_state([2])[0])
+    o_ref, S_ref, _ = oracle_run(op, x, S0, bonus)
+    o = torch.stack(outs).cpu().reshape(T, B * H, d).numpy()
+    assert max_step_rel(o, o_ref) <= OUT_TOL_F32
+    assert rel_err(ctx.read_state([0, 1]).cpu().reshape(B * H, d, d).numpy(), S_ref) <= STATE_TOL

@@ -1,0 +1,189 @@
+"""GPU parity at the workloads' full sizes, in the launch configuration the
+benchmark times (same context shape, batch and merge interval).  The oracle
+cannot run every slot-head, so a fixed sample of slot-heads (the first, the
+last and seeded random ones) is compared on every token, together with their
+final states; bookkeeping is compared for every slot.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import OUT_TOL_BF16, STATE_TOL, max_step_rel, rel_err
+from linear_attention_recurrent_gdn_gb300 import build
+from linear_attention_recurrent_gdn_gb300 import inputs as gen
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+
+
+def _sample(B, H, k, seed):
+    rng = np.random.default_rng(seed)
+    pairs = {(0, 0), (B - 1, H - 1)}
+    while len(pairs) < k:
+        pairs.add((int(rng.integers(B)), int(rng.integers(H))))
+    return sorted(pairs)
+
+
+def _oracle(op, S0, q, k, v, g, extra):
+    fn = {gen.GDN: oracle.gdn_eager, gen.KDA: oracle.kda_eager, gen.RWKV6: oracle.rwkv6_eager}[op]
+    return fn(S0, q, k, v, g, extra)
+
+
+def _run_fullsize(op, B, H, d, T, M, seed, nsample=12):
+    from linear_attention_recurrent_gdn_gb300 import deltalog as dl
+    dev = torch.device("cuda")
+    sel = _sample(B, H, nsample, seed)
+    bi = torch.tensor([s[0] for s in sel], device=dev)
+    hi = torch.tensor([s[1] for s in sel], device=dev)
+    S0 = gen.initial_state(B, H, d, d, seed, device=dev)
+    bonus = gen.rwkv6_bonus(H, d, seed, device=dev) if op == gen.RWKV6 else None
+    ctx = dl.DeltaLog(op, B, H, d, d, M)
+    slots = list(range(B))
+    ctx.set_state(slots, S0)
+    if bonus is not None:
+        ctx.set_bonus(bonus)
+    keep = {key: [] for key in ("q", "k", "v", "g", "beta")}
+    outs = []
+    for t in range(T):
+        x = gen.step_inputs(op, B, H, d, d, seed, t, device=dev)
+        o = ctx.step(slots, x["q"], x["k"], x["v"], x["g"], x["beta"])
+        outs.append(o[bi, hi].float().cpu())
+        for key in keep:
+            if x[key] is not None:
+                keep[key].append(x[key][bi, hi].cpu())
+    S = ctx.read_state(sorted({s[0] for s in sel}))
+    rows = {b: i for i, b in enumerate(sorted({s[0] for s in sel}))}
+    S_sel = torch.stack([S[rows[b], h] for b, h in sel]).cpu().double().numpy()
+    n, base_of = ctx.get_meta()
+    ctx.close()
+    f = lambda key: torch.stack(keep[key]).double().numpy()
+    S0s = S0[bi, hi].cpu().double().numpy()
+    extra = bonus[hi].cpu().double().numpy() if op == gen.RWKV6 else f("beta")
+    o_ref, S_ref, _ = _oracle(op, S0s, f("q"), f("k"), f("v"), f("g"), extra)
+    o = torch.stack(outs).numpy()
+    return max_step_rel(o, o_ref), rel_err(S_sel, S_ref), n, base_of
+
+
+@pytest.mark.parametrize("M", [16, 1, 32])
+def test_gdn_serving_batch(M):
+    """GDN decode at serving batch: B=256, H=32, d=128, 512 tokens."""
+    eo, es, n, base_of = _run_fullsize(gen.GDN, 256, 32, 128, 512, M, seed=2001)
+    assert eo <= OUT_TOL_BF16, eo
+    assert es <= STATE_TOL, es
+    assert list(n) == [512 % M] * 256 and list(base_of) == list(range(256))
+
+
+def test_kda_decode():
+    """KDA decode: B=128, H=32, d=128, per-key decay, M=16, 512 tokens."""
+    eo, es, n, _ = _run_fullsize(gen.KDA, 128, 32, 128, 512, 16, seed=2002, nsample=8)
+    assert eo <= OUT_TOL_BF16, eo
+    assert es <= STATE_TOL, es
+
+
+def test_rwkv6_decode():
+    """RWKV6 decode: B=128, H=40, head size 64, M=16, 512 tokens."""
+    eo, es, n, _ = _run_fullsize(gen.RWKV6, 128, 40, 64, 512, 16, seed=2003)
+    assert eo <= OUT_TOL_BF16, eo
+    assert es <= STATE_TOL, es
+
+
+def test_fork_workload():
+    """Forked GDN decode: 64 requests build bases over 2048 context tokens
+    (H=16, d=128, M=16); each forks 8 branches by index (512 branch slots);
+    branches run U{16..256} tokens and privatise at their first merge.
+    Sampled branch-heads are compared with the oracle run over context +
+    branch tokens; bookkeeping is compared with the oracle model every token."""
+    from linear_attention_recurrent_gdn_gb300 import deltalog as dl
+    R, NB, H, d, M, Tc = 64, 8, 16, 128, 16, 2048
+    dev = torch.device("cuda")
+    seed_c, seed_q = 2004, 2005
+    rng = np.random.default_rng(7)
+    lens = rng.integers(16, 257, size=R * NB)
+    order = np.argsort(-lens, kind="stable")            # active branches form a prefix
+    S = R + R * NB
+    ctx = dl.DeltaLog(gen.GDN, S, H, d, d, M)
+    model = oracle.SlotTableModel(S, M)
+    S0 = gen.initial_state(R, H, d, d, seed_c, device=dev)
+    ctx.set_state(list(range(R)), S0)
+    model.set_state(list(range(R)))
+    sel_br = [int(order[0]), int(order[-1]), 5, 300]    # longest, shortest, two more (branch ids)
+    sel_req = sorted({b // NB for b in sel_br} | {63})
+    keep_c = {key: [] for key in ("q", "k", "v", "g", "beta")}
+    ri = torch.tensor(sel_req, device=dev)
+    for t in range(Tc):
+        x = gen.step_inputs(gen.GDN, R, H, d, d, seed_c, t, device=dev)
+        ctx.step(list(range(R)), x["q"], x["k"], x["v"], x["g"], x["beta"])
+        model.step(list(range(R)))
+        for key in keep_c:
+            keep_c[key].append(x[key][ri].cpu())
+    for r in range(R):
+        br = [R + r * NB + i for i in range(NB)]
+        ctx.fork(r, br)
+        model.fork(r, br)
+    slot_of = lambda b: R + int(b)
+    Tq = int(lens.max())
+    keep_q = {b: {key: [] for key in keep_c} for b in sel_br}
+    outs = {b: [] for b in sel_br}
+    for t in range(Tq):
+        count = int((lens > t).sum())
+        act = order[:count]
+        x = gen.step_inputs(gen.GDN, count, H, d, d, seed_q, t, device=dev)
+        o = ctx.step([slot_of(b) for b in act], x["q"], x["k"], x["v"], x["g"], x["beta"])
+        model.step([slot_of(b) for b in act])
+        pos = {int(b): i for i, b in enumerate(act)}
+        for b in sel_br:
+            if b in pos:
+                outs[b].append(o[pos[b]].float().cpu())
+                for key in keep_c:
+                    keep_q[b][key].append(x[key][pos[b]].cpu())
+        if t % 32 == 0 or t == Tq - 1:
+            n, base_of = ctx.get_meta()
+            mn, mb, _ = model.snapshot()
+            assert list(n) == mn and list(base_of) == mb, t
+    final = ctx.read_state([slot_of(b) for b in sel_br]).cpu().double().numpy()
+    ctx.close()
+    for i, b in enumerate(sel_br):
+        r = b // NB
+        ctxin = {key: torch.stack(keep_c[key])[:, sel_req.index(r)] for key in keep_c}
+        L = int(lens[b])
+        cat = {key: torch.cat([ctxin[key], torch.stack(keep_q[b][key])]).double().numpy()
+               for key in keep_c}
+        o_ref, S_ref, _ = oracle.gdn_eager(S0[r].cpu().double().numpy(), cat["q"], cat["k"],
+                                           cat["v"], cat["g"], cat["beta"])
+        o = torch.stack(outs[b]).numpy()
+        assert o.shape[0] == L
+        assert max_step_rel(o, o_ref[Tc:]) <= OUT_TOL_BF16, b
+        assert rel_err(final[i], S_ref) <= STATE_TOL, b
+
+
+def test_chunked_rows_and_empty_batch():
+    """More slot rows than one launch takes (1100 > 1024): the step is split
+    into chunks; an empty slot list is a no-op."""
+    from linear_attention_recurrent_gdn_gb300 import deltalog as dl
+    B, H, d, M, T = 1100, 2, 64, 4, 6
+    x = gen.make_inputs(gen.GDN, T, B, H, d, d, 77)
+    S0 = gen.initial_state(B, H, d, d, 77)
+    ctx = dl.DeltaLog(gen.GDN, B, H, d, d, M)
+    ctx.set_state(list(range(B)), S0.cuda())
+    dev = {k: v.cuda() for k, v in x.items()}
+    e = torch.empty(0, H, d, dtype=torch.bfloat16, device="cuda")
+    ctx.step([], e, e, e, torch.empty(0, H, device="cuda"), torch.empty(0, H, device="cuda"),
+             out=torch.empty(0, H, d, dtype=torch.bfloat16, device="cuda"))
+    outs = [ctx.step(list(range(B)), dev["q"][t], dev["k"][t], dev["v"][t], dev["g"][t],
+                     dev["beta"][t]).float().cpu() for t in range(T)]
+    f = lambda t: t.reshape((T, B * H) + t.shape[3:]).double().numpy()
+    o_ref, S_ref, _ = oracle.gdn_eager(S0.reshape(B * H, d, d).double().numpy(), f(x["q"]),
+                                       f(x["k"]), f(x["v"]), f(x["g"]), f(x["beta"]))
+    o = torch.stack(outs).reshape(T, B * H, d).numpy()
+    assert max_step_rel(o, o_ref) <= OUT_TOL_BF16
+    S = ctx.read_state(list(range(B))).cpu().reshape(B * H, d, d).double().numpy()
+    assert rel_err(S, S_ref) <= STATE_TOL
+    n, _ = ctx.get_meta()
+    assert list(n) == [T % M] * B
