@@ -210,6 +210,25 @@ dl_status dl_checkpoint_save(dl_ctx *ctx, const int32_t *slots, int32_t n, void 
  * (the saved log lengths are read back to update the host table). */
 dl_status dl_checkpoint_load(dl_ctx *ctx, const int32_t *slots, int32_t n, const void *buf);
 
+/* CUDA-graph decode loop (Flide page, third step: prepared CUDA graphs cut the
+ * per-step launch cost).  A window is one merge interval — M decode tokens —
+ * of a fixed batch, captured once into a CUDA graph and replayed.  Every
+ * listed slot must own its base and have an empty log when the window is
+ * created and whenever it is launched; the window's last token is the merge,
+ * so windows can be launched back to back.  q, k are [M, n, H, d_k] bf16, v
+ * [M, n, H, d_v] bf16, g [M, n, H] or [M, n, H, d_k] fp32, beta [M, n, H] fp32
+ * (NULL for RWKV6), o [M, n, H, d_v]: token j of a launch reads slice j of each
+ * input and writes slice j of o; the graph keeps these device pointers, and the
+ * caller refills the buffers between launches (in stream order).  n <= 1024.
+ * dl_window_launch validates the slots, enqueues the graph on the context's
+ * stream and advances the slot table by M tokens. */
+typedef struct dl_window dl_window;
+dl_status dl_window_create(dl_ctx *ctx, const int32_t *slots, int32_t n,
+                           const void *q, const void *k, const void *v,
+                           const float *g, const float *beta, void *o, dl_window **out);
+dl_status dl_window_launch(dl_window *w);
+dl_status dl_window_destroy(dl_window *w);
+
 /* Synchronise the stream and report any CUDA or device-side error. */
 dl_status dl_sync(dl_ctx *ctx);
 

@@ -32,16 +32,15 @@ cudaError_t launch_append_decode(int op, int dk, const StepArgs& a, int grid, si
   return launch_ad<RWKV6, 128>(a, grid, smem, pdl, s);
 }
 
+// The attribute must be set on the kernel instance this translation unit
+// launches (each translation unit registers its own copy of a template kernel).
 template <int OP, int DK>
 static cudaError_t cfg_one(size_t smem) {
-  cudaError_t e = cudaFuncSetAttribute(pipe_kernel<OP, DK, DK, APPEND>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(pipe_kernel<OP, DK, DK, EAGER>,
+  return cudaFuncSetAttribute(pipe_kernel<OP, DK, DK, APPEND>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
 }
 
-cudaError_t configure_pipeline(int op, int dk, size_t smem) {
+cudaError_t configure_append_decode(int op, int dk, size_t smem) {
   if (dk == 64) {
     if (op == GDN) return cfg_one<GDN, 64>(smem);
     if (op == KDA) return cfg_one<KDA, 64>(smem);

@@ -173,9 +173,16 @@ dl_status check_step_ptrs(dl_ctx* c, int32_t n, const void* q, const void* k, co
   if (n == 0) return DL_OK;
   if (!q || !k || !v || !g || !o || (c->cfg.op != DL_RWKV6 && !beta))
     return set_err(c, DL_EINVAL, "NULL tensor pointer");
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(o) ||
-      (beta && !aligned16(beta)))
-    return set_err(c, DL_EINVAL, "tensor pointers must be 16-byte aligned");
+  // q, k, v (and the per-key g rows) are moved by bulk copies / vector loads:
+  // 16-byte alignment; the per-head g (GDN), beta and o are accessed per element.
+  const bool perkey = c->cfg.op != DL_GDN;
+  const uintptr_t osz = c->cfg.out_bf16 ? 2 : 4;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) ||
+      (perkey ? !aligned16(g) : (reinterpret_cast<uintptr_t>(g) & 3u) != 0) ||
+      (beta && (reinterpret_cast<uintptr_t>(beta) & 3u) != 0) ||
+      (reinterpret_cast<uintptr_t>(o) & (osz - 1)) != 0)
+    return set_err(c, DL_EINVAL, "misaligned tensor: q, k, v%s need 16-byte alignment, "
+                   "other tensors their element size", perkey ? ", g" : "");
   if (c->cfg.op == DL_RWKV6 && !c->bonus)
     return set_err(c, DL_EINVAL, "RWKV6 needs dl_set_bonus before stepping");
   return DL_OK;
@@ -355,7 +362,8 @@ dl_status dl_create(const dl_config* cfg, void* stream, dl_ctx** out) {
       if (a.smem > smem) smem = a.smem;
       if (b.smem > smem) smem = b.smem;
     }
-    e = dl::configure_pipeline(f.op, f.d_k, smem);
+    e = dl::configure_append_decode(f.op, f.d_k, smem);
+    if (e == cudaSuccess) e = dl::configure_eager_step(f.op, f.d_k, smem);
     if (e != cudaSuccess) { rc = cuda_err(c, e, "kernel attribute"); break; }
   } while (0);
   g_fail_countdown = -1;
@@ -678,6 +686,112 @@ dl_status dl_checkpoint_load(dl_ctx* c, const int32_t* slots, int32_t n, const v
     DL_CUDA(cudaStreamSynchronize(c->stream), "stream sync");   // `self` lives on the host stack
   }
   dl_table_set_n(c->table, slots, n, ns.data());
+  return DL_OK;
+}
+
+}  // extern "C"
+
+struct dl_window {
+  dl_ctx* ctx = nullptr;
+  std::vector<int32_t> slots;
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+};
+
+extern "C" {
+
+dl_status dl_window_create(dl_ctx* c, const int32_t* slots, int32_t n, const void* q,
+                           const void* k, const void* v, const float* g, const float* beta,
+                           void* o, dl_window** out) {
+  if (!out) return DL_EINVAL;
+  *out = nullptr;
+  dl_status rc = check_ctx(c);
+  if (rc != DL_OK) return rc;
+  if (n < 1 || n > dl::MAX_ROWS) return set_err(c, DL_EINVAL, "window batch must be 1..%d", dl::MAX_ROWS);
+  rc = check_step_ptrs(c, n, q, k, v, g, beta, o);
+  if (rc != DL_OK) return rc;
+  rc = dl_table_step_eager(c->table, slots, n);   // own base, empty log, not frozen
+  if (rc != DL_OK) return set_err(c, rc, "dl_window_create: slots must own their base and have an empty log");
+  const dl_config& f = c->cfg;
+  const int M = f.merge_interval;
+  const size_t H = f.num_heads;
+  const size_t sq = (size_t)n * H * f.d_k * 2, sv = (size_t)n * H * f.d_v * 2;
+  const size_t sg = (size_t)n * H * (f.op == DL_GDN ? 1 : f.d_k) * 4, sb = (size_t)n * H * 4;
+  const size_t so = (size_t)n * H * f.d_v * (f.out_bf16 ? 2 : 4);
+  // every per-token slice must keep the alignment dl_step needs (q, k, v and
+  // per-key g rows are always 16-byte multiples; the others are element-sized)
+  (void)sb;
+  std::unique_ptr<dl_window> w(new (std::nothrow) dl_window);
+  if (!w) return set_err(c, DL_ENOMEM, "window allocation");
+  w->ctx = c;
+  w->slots.assign(slots, slots + n);
+  cudaStream_t cap = nullptr;
+  DL_CUDA(cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking), "capture stream");
+  cudaStream_t saved = c->stream;
+  const bool saved_timing = c->timing;
+  c->stream = cap;
+  c->timing = false;
+  cudaError_t e = cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal);
+  dl_status st = DL_OK;
+  if (e == cudaSuccess) {
+    for (int j = 0; j < M && st == DL_OK; ++j) {
+      for (int32_t i = 0; i < n; ++i) {
+        c->plan[4 * (size_t)i + 0] = slots[i];
+        c->plan[4 * (size_t)i + 1] = slots[i];
+        c->plan[4 * (size_t)i + 2] = j;
+        c->plan[4 * (size_t)i + 3] = (j + 1 == M);
+      }
+      st = run_step(c, slots, n, static_cast<const unsigned char*>(q) + j * sq,
+                    static_cast<const unsigned char*>(k) + j * sq,
+                    static_cast<const unsigned char*>(v) + j * sv,
+                    reinterpret_cast<const float*>(reinterpret_cast<const unsigned char*>(g) + j * sg),
+                    beta ? reinterpret_cast<const float*>(reinterpret_cast<const unsigned char*>(beta) + j * sb)
+                         : nullptr,
+                    static_cast<unsigned char*>(o) + j * so, false);
+    }
+    cudaError_t e2 = cudaStreamEndCapture(cap, &w->graph);
+    if (e == cudaSuccess) e = e2;
+  }
+  c->stream = saved;
+  c->timing = saved_timing;
+  cudaStreamDestroy(cap);
+  if (st != DL_OK) {
+    if (w->graph) cudaGraphDestroy(w->graph);
+    c->sticky = DL_OK;   // a failed capture leaves the context usable
+    return set_err(c, DL_ECUDA, "window capture failed: %s", c->err.c_str());
+  }
+  if (e != cudaSuccess) {
+    if (w->graph) cudaGraphDestroy(w->graph);
+    return set_err(c, DL_ECUDA, "window capture: %s", cudaGetErrorString(e));
+  }
+  e = cudaGraphInstantiate(&w->exec, w->graph, 0);
+  if (e != cudaSuccess) {
+    cudaGraphDestroy(w->graph);
+    return set_err(c, DL_ECUDA, "graph instantiate: %s", cudaGetErrorString(e));
+  }
+  *out = w.release();
+  return DL_OK;
+}
+
+dl_status dl_window_launch(dl_window* w) {
+  if (!w) return DL_EINVAL;
+  dl_ctx* c = w->ctx;
+  dl_status rc = check_ctx(c);
+  if (rc != DL_OK) return rc;
+  const int32_t n = (int32_t)w->slots.size();
+  rc = dl_table_step_eager(c->table, w->slots.data(), n);
+  if (rc != DL_OK)
+    return set_err(c, rc, "dl_window_launch: slots must own their base and have an empty log");
+  DL_CUDA(cudaGraphLaunch(w->exec, c->stream), "graph launch");
+  for (int j = 0; j < c->cfg.merge_interval; ++j) dl_table_step(c->table, w->slots.data(), n, nullptr);
+  return DL_OK;
+}
+
+dl_status dl_window_destroy(dl_window* w) {
+  if (!w) return DL_OK;
+  if (w->exec) cudaGraphExecDestroy(w->exec);
+  if (w->graph) cudaGraphDestroy(w->graph);
+  delete w;
   return DL_OK;
 }
 

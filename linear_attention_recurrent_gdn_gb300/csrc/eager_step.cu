@@ -26,4 +26,21 @@ cudaError_t launch_eager_step(int op, int dk, const StepArgs& a, int grid, size_
   return launch_ea<RWKV6, 128>(a, grid, smem, s);
 }
 
+template <int OP, int DK>
+static cudaError_t cfg_one(size_t smem) {
+  return cudaFuncSetAttribute(pipe_kernel<OP, DK, DK, EAGER>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+}
+
+cudaError_t configure_eager_step(int op, int dk, size_t smem) {
+  if (dk == 64) {
+    if (op == GDN) return cfg_one<GDN, 64>(smem);
+    if (op == KDA) return cfg_one<KDA, 64>(smem);
+    return cfg_one<RWKV6, 64>(smem);
+  }
+  if (op == GDN) return cfg_one<GDN, 128>(smem);
+  if (op == KDA) return cfg_one<KDA, 128>(smem);
+  return cfg_one<RWKV6, 128>(smem);
+}
+
 }  // namespace dl

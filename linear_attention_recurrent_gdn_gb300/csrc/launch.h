@@ -18,7 +18,8 @@ cudaError_t launch_eager_step(int op, int dk, const StepArgs& a, int grid, size_
                               cudaStream_t s);
 
 // Allow the pipelined kernels of (op, dk) to use `smem` bytes of dynamic shared memory.
-cudaError_t configure_pipeline(int op, int dk, size_t smem);
+cudaError_t configure_append_decode(int op, int dk, size_t smem);
+cudaError_t configure_eager_step(int op, int dk, size_t smem);
 
 // Standalone merge / read-state (S_out == nullptr: write back into S̄ and reset the log).
 cudaError_t launch_merge(int op, int dk, const SlotListArgs& a, cudaStream_t s);

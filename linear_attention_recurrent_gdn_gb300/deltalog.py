@@ -29,6 +29,7 @@ EXPORTS = [
     "dl_step", "dl_step_host", "dl_step_eager", "dl_merge", "dl_read_state", "dl_get_meta",
     "dl_sync", "dl_set_timing", "dl_get_timing", "dl_last_error", "dl_status_str",
     "dl_abi_version", "dl_checkpoint_bytes", "dl_checkpoint_save", "dl_checkpoint_load",
+    "dl_window_create", "dl_window_launch", "dl_window_destroy",
 ]
 
 
@@ -82,6 +83,9 @@ def _load():
         "dl_checkpoint_bytes": ([P], I64),
         "dl_checkpoint_save": ([P, P, I32, P], I32),
         "dl_checkpoint_load": ([P, P, I32, P], I32),
+        "dl_window_create": ([P, P, I32, P, P, P, P, P, P, PP], I32),
+        "dl_window_launch": ([P], I32),
+        "dl_window_destroy": ([P], I32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -256,6 +260,22 @@ def dl_checkpoint_load(ctx, slots, buf):
     _check(_lib.dl_checkpoint_load(ctx, p, n, _ptr(buf)), ctx)
 
 
+def dl_window_create(ctx, slots, q, k, v, g, beta, o):
+    a, p, n = _slots(slots)
+    h = ctypes.c_void_p()
+    _check(_lib.dl_window_create(ctx, p, n, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                 _ptr(o), ctypes.byref(h)), ctx)
+    return h
+
+
+def dl_window_launch(ctx, w):
+    _check(_lib.dl_window_launch(w), ctx)
+
+
+def dl_window_destroy(w):
+    _lib.dl_window_destroy(w)
+
+
 def dl_last_error(ctx):
     return _lib.dl_last_error(ctx).decode()
 
@@ -294,6 +314,33 @@ class SlotTable:
 
     def get(self):
         return dl_table_get(self._h, self.num_slots)
+
+
+class DecodeWindow:
+    """A captured merge window; launch() replays it on the context's stream."""
+
+    def __init__(self, ctx, slots, q, k, v, g, beta, out):
+        n = len(list(slots))
+        if out is None:
+            out = ctx.torch.empty((ctx.M, n, ctx.H, ctx.d_v), dtype=ctx.out_dtype, device="cuda")
+        self.ctx, self.out = ctx, out
+        self._keep = (q, k, v, g, beta)
+        self._h = dl_window_create(ctx.handle, slots, q, k, v, g, beta, out)
+
+    def launch(self):
+        dl_window_launch(self.ctx.handle, self._h)
+        return self.out
+
+    def close(self):
+        if getattr(self, "_h", None):
+            dl_window_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 class DeltaLog:
@@ -417,6 +464,11 @@ class DeltaLog:
             buf = self.torch.empty(n * per, dtype=self.torch.uint8, device="cuda")
         dl_checkpoint_save(self._h, a, buf)
         return buf
+
+    def window(self, slots, q, k, v, g, beta=None, out=None):
+        """Capture one merge window (M tokens) of `slots` into a CUDA graph; the
+        tensors are [M, n, ...] device buffers that the graph reads at each launch."""
+        return DecodeWindow(self, slots, q, k, v, g, beta, out)
 
     def checkpoint_load(self, slots, buf):
         dl_checkpoint_load(self._h, slots, buf)

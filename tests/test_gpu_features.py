@@ -91,3 +91,44 @@ def test_checkpoint_resume_bitwise(op, t_save):
     o = torch.stack(outs).cpu().reshape(T, B * H, d).numpy()
     assert max_step_rel(o, o_ref) <= OUT_TOL_F32
     assert rel_err(ctx.read_state([0, 1]).cpu().reshape(B * H, d, d).numpy(), S_ref) <= STATE_TOL
+
+
+@pytest.mark.parametrize("op", OPS)
+def test_graph_window_matches_stepping_bitwise(op):
+    """A captured merge window replayed 3 times gives the bits of 3*M plain
+    steps; the inputs are refilled between launches."""
+    from linear_attention_recurrent_gdn_gb300 import deltalog as dl
+    B, H, d, M, W = 8, 4, 64, 4, 3
+    T = M * W
+    x, S0, bonus = make_case(op, B, H, d, T, seed=600 + op, device="cuda")
+    a = dl.DeltaLog(op, B, H, d, d, M)
+    b = dl.DeltaLog(op, B, H, d, d, M)
+    for c in (a, b):
+        c.set_state(list(range(B)), S0)
+        if bonus is not None:
+            c.set_bonus(bonus)
+    ref = []
+    for t in range(T):
+        beta = x["beta"][t] if x["beta"] is not None else None
+        ref.append(a.step(list(range(B)), x["q"][t], x["k"][t], x["v"][t], x["g"][t], beta).clone())
+    buf = {k: (v[:M].clone() if v is not None else None) for k, v in x.items()}
+    win = b.window(list(range(B)), buf["q"], buf["k"], buf["v"], buf["g"], buf["beta"])
+    for w in range(W):
+        for k_, v_ in x.items():
+            if v_ is not None:
+                buf[k_].copy_(v_[w * M:(w + 1) * M])
+        out = win.launch()
+        for j in range(M):
+            assert torch.equal(out[j], ref[w * M + j]), (w, j)
+    assert torch.equal(a.read_state(list(range(B))), b.read_state(list(range(B))))
+    na, ba = a.get_meta()
+    nb, bb = b.get_meta()
+    assert list(na) == list(nb) and list(ba) == list(bb)
+    # a slot with a pending log cannot enter a window
+    sl = slice(0, 1)
+    beta = x["beta"][0][sl] if x["beta"] is not None else None
+    b.step([0], x["q"][0][sl], x["k"][0][sl], x["v"][0][sl], x["g"][0][sl], beta)
+    with pytest.raises(dl.DeltaLogError) as e:
+        win.launch()
+    assert e.value.status == dl.EINVAL
+    win.close()

@@ -246,10 +246,16 @@ def test_argument_errors():
     with pytest.raises(dl.DeltaLogError) as e:
         ctx.fork(1, [1, 2])
     assert e.value.status == dl.EINVAL
-    # misaligned device pointer, through the raw C entry point
-    o = torch.empty(2 * 2 * 64 + 8, dtype=torch.bfloat16, device="cuda")
+    # misaligned q (bulk-copied: needs 16 bytes), through the raw C entry point
+    qb = torch.empty(2 * 2 * 64 + 8, dtype=torch.bfloat16, device="cuda")
+    q_mis = qb[1:1 + 2 * 2 * 64].view(2, 2, 64)
+    o = torch.empty(2, 2, 64, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(dl.DeltaLogError) as e:
-        dl.dl_step(ctx.handle, [0, 1], *args, o[1:])
+        dl.dl_step(ctx.handle, [0, 1], q_mis, *args[1:], o)
+    assert e.value.status == dl.EINVAL
+    ob = torch.empty(2 * 2 * 64 + 8, dtype=torch.uint8, device="cuda")
+    with pytest.raises(dl.DeltaLogError) as e:     # o must be aligned to its element size
+        dl.dl_step(ctx.handle, [0, 1], *args, ob[1:])
     assert e.value.status == dl.EINVAL
     # the context is still usable and nothing was stepped
     n, _ = ctx.get_meta()
