@@ -195,6 +195,21 @@ dl_status dl_read_state(dl_ctx *ctx, const int32_t *slots, int32_t n, float *S_o
  * device table disagrees with the host table. */
 dl_status dl_get_meta(dl_ctx *ctx, int32_t *n_log, int32_t *base_of);
 
+/* Chunked prefill: feed T context tokens to each listed slot in one call and
+ * leave the state after the last token in the slot's dense base (log empty).
+ * Flide page, "Research method step by step", second step: the shared
+ * context is processed once and its final state saved before branches fork.
+ * Inputs are token-major: q, k [T, n, H, d_k] bf16, v [T, n, H, d_v] bf16,
+ * g, beta [T, n, H] fp32; o [T, n, H, d_v] receives every token's output, or
+ * is NULL.  Every slot must own its base and have an empty log.  Tokens are
+ * processed C = 32 at a time: one pass over the state per chunk computes all
+ * chunk outputs (base + log algebra, forward substitution for the delta-rule
+ * factors), and the state is rewritten once per chunk.  GDN only in this
+ * build (DL_EUNSUPPORTED otherwise). */
+dl_status dl_prefill(dl_ctx *ctx, const int32_t *slots, int32_t n, int32_t T,
+                     const void *q, const void *k, const void *v,
+                     const float *g, const float *beta, void *o);
+
 /* Prefix checkpoints (Flide page, "Research method step by step", fourth step:
  * a growing agent trace resumes from a checkpoint saved at a matching prefix).
  * A checkpoint is the exact DeltaLog representation of a slot: the dense base

@@ -17,7 +17,8 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libdeltalog.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-CU_SOURCES = ["replay_prep.cu", "append_decode.cu", "eager_step.cu", "slot_ops.cu", "capi.cu"]
+CU_SOURCES = ["replay_prep.cu", "append_decode.cu", "eager_step.cu", "slot_ops.cu", "prefill.cu",
+              "capi.cu"]
 CPP_SOURCES = ["slot_table.cpp"]
 
 

@@ -126,8 +126,9 @@ void free_all(dl_ctx* c) {
   c->table = nullptr;
 }
 
-// Pipeline shape for a launch with G tiles per unit: the most stages that fit
-// (up to 12), and enough aux slots to cover the units those stages span.
+// Pipeline shape for a launch with G tiles per unit: ns = NCW * R stages (each
+// consumer warp owns R of them), the largest R <= 3 that fits, and enough aux
+// slots to cover the units those stages span.
 struct PipeShape {
   int ns, na;
   size_t smem;
@@ -137,11 +138,16 @@ PipeShape pipe_shape(const dl_ctx* c, int G, bool append) {
   const size_t tile = (size_t)dl::BV * c->cfg.d_k * 4;
   const size_t aux = append ? c->L.aux_bytes : c->L.e_bytes;
   const size_t budget = (size_t)c->smem_optin - dl::BAR_BYTES - 1024;
-  PipeShape best{1, 1, dl::BAR_BYTES + tile + aux};
-  for (int ns = 2; ns <= 12; ++ns) {
+  PipeShape best{0, 0, 0};
+  for (int R = 1; R <= 3; ++R) {
+    const int ns = dl::NCW * R;
     int na = (ns + G - 1) / G + 1;
-    if (na > ns + 1) na = ns + 1;
-    const size_t need = (size_t)ns * tile + (size_t)na * aux;
+    if (na > 16) na = 16;
+    size_t need = (size_t)ns * tile + (size_t)na * aux;
+    while (need > budget && na > 2) {
+      --na;
+      need = (size_t)ns * tile + (size_t)na * aux;
+    }
     if (need <= budget) best = PipeShape{ns, na, dl::BAR_BYTES + need};
   }
   return best;
@@ -253,6 +259,7 @@ dl_status run_step(dl_ctx* c, const int32_t* slots, int32_t n, const void* q, co
     int grid = 0;
     unit_shape(c, a, &grid);
     const PipeShape ps = pipe_shape(c, a.G, !eager);
+    if (ps.ns == 0) return set_err(c, DL_EUNSUPPORTED, "pipeline does not fit in shared memory");
     a.ns = ps.ns;
     a.na = ps.na;
     cudaEvent_t e0;
@@ -593,6 +600,36 @@ dl_status dl_read_state(dl_ctx* c, const int32_t* slots, int32_t n, float* S_out
   rc = dl_table_check(c->table, slots, n);
   if (rc != DL_OK) return set_err(c, rc, "dl_read_state: invalid slot list");
   return merge_or_read(c, slots, n, S_out);
+}
+
+dl_status dl_prefill(dl_ctx* c, const int32_t* slots, int32_t n, int32_t T, const void* q,
+                     const void* k, const void* v, const float* g, const float* beta, void* o) {
+  dl_status rc = check_ctx(c);
+  if (rc != DL_OK) return rc;
+  if (n < 0 || T < 0) return set_err(c, DL_EINVAL, "negative count");
+  if (c->cfg.op != DL_GDN) return set_err(c, DL_EUNSUPPORTED, "dl_prefill: GDN only in this build");
+  if (n == 0 || T == 0) return DL_OK;
+  if (!q || !k || !v || !g || !beta) return set_err(c, DL_EINVAL, "NULL tensor pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || (reinterpret_cast<uintptr_t>(g) & 3u) ||
+      (reinterpret_cast<uintptr_t>(beta) & 3u) ||
+      (o && (reinterpret_cast<uintptr_t>(o) & (c->cfg.out_bf16 ? 1u : 3u))))
+    return set_err(c, DL_EINVAL, "misaligned tensor");
+  if (n > dl::MAX_ROWS) return set_err(c, DL_EINVAL, "dl_prefill takes at most %d slots per call", dl::MAX_ROWS);
+  rc = dl_table_step_eager(c->table, slots, n);
+  if (rc != DL_OK)
+    return set_err(c, rc, "dl_prefill: slots must own their base and have an empty log");
+  dl::SlotListArgs& a = *c->list_args;
+  a = dl::SlotListArgs{};
+  a.Sbar = c->Sbar;
+  a.nlog = c->nlog;
+  a.base_of = c->base_of;
+  a.rows = n;
+  a.H = c->cfg.num_heads;
+  a.Mcap = c->L.Mcap;
+  for (int32_t i = 0; i < n; ++i) a.items[i] = dl::StepItem{slots[i], slots[i], 0};
+  DL_CUDA(dl::launch_prefill(c->cfg.op, c->cfg.d_k, a, q, k, v, g, beta, o, T, c->cfg.out_bf16,
+                             c->cfg.scale, c->stream), "Prefill launch");
+  return DL_OK;
 }
 
 struct CkptLayout {

@@ -34,7 +34,7 @@ namespace dl {
 
 enum Mode : int { APPEND = 0, EAGER = 1 };
 
-constexpr int MAX_NS = 24, MAX_NA = 24;
+constexpr int MAX_NS = 24, MAX_NA = 24;   // (barrier area: 8 bytes each)
 
 struct Bars {
   uint32_t b0;
@@ -44,6 +44,22 @@ struct Bars {
   __device__ uint32_t afull(int x) const { return b0 + 8u * (2 * ns + x); }
   __device__ uint32_t aempty(int x) const { return b0 + 8u * (2 * ns + na + x); }
 };
+
+// Stage ownership: tile i (CTA-local order) belongs to consumer warp i % NCW,
+// and each warp owns R = ns / NCW consecutive stages that it cycles through.
+// A warp therefore waits on a stage only after it released that stage's
+// previous phase itself, so no barrier is ever awaited more than one phase
+// ahead (mbarrier parity waits cannot tell phases two apart).
+__device__ __forceinline__ int stage_of(int i, int R) {
+  return (i % NCW) * R + (i / NCW) % R;
+}
+__device__ __forceinline__ uint32_t stage_parity(int i, int R) {
+  return (uint32_t)((i / NCW) / R) & 1u;
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
 
 struct UnitPos {
   int sh, row, h, grp;
@@ -341,6 +357,7 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) pipe_kernel(const __grid_cons
   constexpr uint32_t TILE_BYTES = BV * DK * 4;
   const Layout Lay = make_layout(OP, a.M, DK, DV);
   const int NS = a.ns, NA = a.na, G = a.G;
+  const int R = NS / NCW;   // stages per consumer warp (ns is a multiple of NCW)
   const uint32_t aux_bytes = (MODE == APPEND) ? Lay.aux_bytes : Lay.e_bytes;
   const Bars bars{smem_u32(smem), NS, NA};
   float* tiles = reinterpret_cast<float*>(smem + BAR_BYTES);
@@ -397,8 +414,8 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) pipe_kernel(const __grid_cons
                                     primary_done);
         ++ka;
       }
-      const int s = ti % NS;
-      if (!mbar_wait(bars.empty(s), ((ti / NS) & 1) ^ 1, a.status, DEV_TIMEOUT_EMPTY)) {
+      const int s = stage_of(ti, R);
+      if (!mbar_wait(bars.empty(s), stage_parity(ti, R) ^ 1u, a.status, DEV_TIMEOUT_EMPTY)) {
         ok = false;
         break;
       }
@@ -421,7 +438,8 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) pipe_kernel(const __grid_cons
     if (!ok) {
       // an error was recorded: let the copies already in flight land before exiting
       if (!primary_done) pdl_wait_primary();
-      for (int t = ti - NS > 0 ? ti - NS : 0; t < ti; ++t) mbar_drain(bars.full(t % NS), (t / NS) & 1);
+      for (int t = ti - NS > 0 ? ti - NS : 0; t < ti; ++t)
+        mbar_drain(bars.full(stage_of(t, R)), stage_parity(t, R));
     }
     return;
   }
@@ -431,19 +449,25 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) pipe_kernel(const __grid_cons
     const int kk = i / G;
     const UnitPos p = unit_pos(a, (int)blockIdx.x + kk * (int)gridDim.x);
     const int vt = p.grp * G + (i - kk * G);
-    const int x = kk % NA, s = i % NS;
+    const int x = kk % NA, s = stage_of(i, R);
     float g_s = 0.f, beta_s = 0.f;
     if constexpr (MODE == EAGER) {
       if (OP == GDN) g_s = a.g[p.sh];
       if (OP != RWKV6) beta_s = a.beta[p.sh];
     }
-    bool ok = mbar_wait(bars.afull(x), (kk / NA) & 1, a.status, DEV_TIMEOUT_AUX);
-    ok = ok && mbar_wait(bars.full(s), (i / NS) & 1, a.status, DEV_TIMEOUT_TILE);
+    // The tile first: it is issued after its unit's aux copies, so once it has
+    // landed the aux barrier is in this unit's phase and the parity test below
+    // is unambiguous.
+    bool ok = mbar_wait(bars.full(s), stage_parity(i, R), a.status, DEV_TIMEOUT_TILE);
+    ok = ok && mbar_wait(bars.afull(x), (kk / NA) & 1, a.status, DEV_TIMEOUT_AUX);
     if (!__all_sync(0xffffffffu, ok)) break;
     const float* T = tiles + (size_t)s * BV * DK;
     unsigned char* ax = auxm + (size_t)x * aux_bytes;
     if constexpr (MODE == APPEND) consume_append<OP, DK, DV>(a, Lay, p, vt, T, ax, lane);
     else consume_eager<OP, DK, DV>(a, Lay, p, vt, T, ax, lane, g_s, beta_s);
+    // order this warp's shared-memory writes (u_t rows of a merge) before the
+    // bulk copies that will refill the slots once they are released
+    fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
       mbar_arrive(bars.empty(s));

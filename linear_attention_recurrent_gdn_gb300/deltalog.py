@@ -29,7 +29,7 @@ EXPORTS = [
     "dl_step", "dl_step_host", "dl_step_eager", "dl_merge", "dl_read_state", "dl_get_meta",
     "dl_sync", "dl_set_timing", "dl_get_timing", "dl_last_error", "dl_status_str",
     "dl_abi_version", "dl_checkpoint_bytes", "dl_checkpoint_save", "dl_checkpoint_load",
-    "dl_window_create", "dl_window_launch", "dl_window_destroy",
+    "dl_window_create", "dl_window_launch", "dl_window_destroy", "dl_prefill",
 ]
 
 
@@ -86,6 +86,7 @@ def _load():
         "dl_window_create": ([P, P, I32, P, P, P, P, P, P, PP], I32),
         "dl_window_launch": ([P], I32),
         "dl_window_destroy": ([P], I32),
+        "dl_prefill": ([P, P, I32, I32, P, P, P, P, P, P], I32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -258,6 +259,13 @@ def dl_checkpoint_save(ctx, slots, buf):
 def dl_checkpoint_load(ctx, slots, buf):
     a, p, n = _slots(slots)
     _check(_lib.dl_checkpoint_load(ctx, p, n, _ptr(buf)), ctx)
+
+
+def dl_prefill(ctx, slots, q, k, v, g, beta, o):
+    a, p, n = _slots(slots)
+    T = int(q.shape[0])
+    _check(_lib.dl_prefill(ctx, p, n, T, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(o)),
+           ctx)
 
 
 def dl_window_create(ctx, slots, q, k, v, g, beta, o):
@@ -464,6 +472,19 @@ class DeltaLog:
             buf = self.torch.empty(n * per, dtype=self.torch.uint8, device="cuda")
         dl_checkpoint_save(self._h, a, buf)
         return buf
+
+    def prefill(self, slots, q, k, v, g, beta, out=None, want_out=True):
+        """Feed T context tokens ([T, n, ...] tensors) to each slot in one call."""
+        a, _, n = _slots(slots)
+        T = int(q.shape[0])
+        for name, t, d in (("q", q, self.d_k), ("k", k, self.d_k), ("v", v, self.d_v)):
+            self._need(t, (T, n, self.H, d), self.torch.bfloat16, name)
+        self._need(g, (T, n, self.H), self.torch.float32, "g")
+        self._need(beta, (T, n, self.H), self.torch.float32, "beta")
+        if out is None and want_out:
+            out = self.torch.empty((T, n, self.H, self.d_v), dtype=self.out_dtype, device="cuda")
+        dl_prefill(self._h, a, q, k, v, g, beta, out)
+        return out
 
     def window(self, slots, q, k, v, g, beta=None, out=None):
         """Capture one merge window (M tokens) of `slots` into a CUDA graph; the

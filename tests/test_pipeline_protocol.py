@@ -1,0 +1,134 @@
+"""CPU model of the mbarrier protocol of the pipelined value-tile kernels.
+
+The producer fills a ring of tile stages and a ring of aux slots with bulk
+copies whose completions can arrive in any order; consumer warps wait with
+parity tests, which cannot tell apart two phases of the same parity.  The
+model replays the producer / consumer programs against that barrier semantic
+under adversarial (newest-first) completion orders and flags any wait that
+returns for a phase that has not completed, and any extra arrival.
+
+The kernels' mapping (each consumer warp owns its stages; tile barrier waited
+before the aux barrier) must pass; the earlier mapping (stage = tile mod ns,
+shared by all warps; aux waited first) is kept as a negative control that the
+model must catch.
+"""
+import random
+
+import pytest
+
+NCW = 8
+
+
+class Bar:
+    def __init__(self, count):
+        self.count, self.done, self.pend, self.tx = count, 0, count, 0
+
+    def arrive(self, tx=0):
+        self.tx += tx
+        self.pend -= 1
+        if self.pend < 0:
+            raise RuntimeError("extra arrival")
+        self._check()
+
+    def complete_tx(self, n):
+        self.tx -= n
+        if self.tx < 0:
+            raise RuntimeError("tx underflow")
+        self._check()
+
+    def _check(self):
+        if self.pend == 0 and self.tx == 0:
+            self.done += 1
+            self.pend = self.count
+
+    def try_wait(self, parity):
+        return (self.done % 2) != parity
+
+
+def simulate(NS, NA, G, n_tiles, owned, tile_first, seed, p_complete=0.03, lifo=0.95):
+    rng = random.Random(seed)
+    R = NS // NCW
+    if owned:
+        stage = lambda i: (i % NCW) * R + (i // NCW) % R
+        phase = lambda i: (i // NCW) // R
+    else:
+        stage = lambda i: i % NS
+        phase = lambda i: i // NS
+    full = [Bar(1) for _ in range(NS)]
+    empty = [Bar(1) for _ in range(NS)]
+    afull = [Bar(1) for _ in range(NA)]
+    aempty = [Bar(G) for _ in range(NA)]
+    inflight, violations = [], []
+    prod = {"ti": 0, "ka": 0}
+    cons = [{"i": w, "step": 0} for w in range(NCW)]
+
+    def producer():
+        ti, ka = prod["ti"], prod["ka"]
+        if ti >= n_tiles:
+            return
+        if ti // G == ka:
+            x = ka % NA
+            if aempty[x].try_wait(((ka // NA) & 1) ^ 1):
+                afull[x].arrive(tx=3)
+                inflight.extend([afull[x]] * 3)
+                prod["ka"] += 1
+            return
+        s = stage(ti)
+        if empty[s].try_wait((phase(ti) & 1) ^ 1):
+            full[s].arrive(tx=1)
+            inflight.append(full[s])
+            prod["ti"] += 1
+
+    def consumer(w):
+        c = cons[w]
+        i = c["i"]
+        if i >= n_tiles:
+            return
+        kk = i // G
+        x, s = kk % NA, stage(i)
+        order = [(full[s], phase(i)), (afull[x], kk // NA)]
+        if not tile_first:
+            order.reverse()
+        if c["step"] < 2:
+            bar, ph = order[c["step"]]
+            if bar.try_wait(ph & 1):
+                if bar.done <= ph:
+                    violations.append((w, i))
+                c["step"] += 1
+            return
+        empty[s].arrive()
+        aempty[x].arrive()
+        c["i"] += NCW
+        c["step"] = 0
+
+    try:
+        for _ in range(2_000_000):
+            r = rng.random()
+            if r < p_complete and inflight:
+                k = len(inflight) - 1 if rng.random() < lifo else rng.randrange(len(inflight))
+                inflight.pop(k).complete_tx(1)
+            elif r < p_complete + 0.2:
+                producer()
+            else:
+                consumer(rng.randrange(NCW))
+            if prod["ti"] >= n_tiles and all(c["i"] >= n_tiles for c in cons):
+                return violations, True
+    except RuntimeError:
+        return violations + ["barrier accounting broken"], False
+    return violations, False
+
+
+@pytest.mark.parametrize("NS,NA,G", [(8, 3, 4), (8, 2, 4), (16, 9, 2), (16, 2, 1), (24, 16, 1),
+                                     (24, 6, 2)])
+def test_owned_stages_tile_first_is_safe(NS, NA, G):
+    for seed in range(12):
+        v, finished = simulate(NS, NA, G, NCW * 4 * 5, owned=True, tile_first=True, seed=seed)
+        assert not v and finished, (seed, v[:3])
+
+
+def test_shared_stages_aux_first_is_caught():
+    caught = 0
+    for seed in range(12):
+        v, finished = simulate(12, 4, 4, NCW * 4 * 5, owned=False, tile_first=False, seed=seed)
+        caught += bool(v) or not finished
+    assert caught >= 6
