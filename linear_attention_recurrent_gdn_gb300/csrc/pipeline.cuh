@@ -137,10 +137,12 @@ __device__ __forceinline__ void issue_coef(const StepArgs& a, const Layout& Lay,
 }
 
 // ---------------------------------------------------------- AppendDecode ----
+// Returns true if it already released the tile stage (append steps release it
+// right after the pass over the tile, so the refill overlaps the epilogue).
 template <int OP, int DK, int DV>
-__device__ __forceinline__ void consume_append(const StepArgs& a, const Layout& Lay,
+__device__ __forceinline__ bool consume_append(const StepArgs& a, const Layout& Lay,
                                                const UnitPos& p, int vt, const float* T,
-                                               unsigned char* ax, int lane) {
+                                               unsigned char* ax, int lane, uint32_t empty_bar) {
   constexpr int VEC = DK / 32;
   constexpr bool DELTA = OP != RWKV6;
   const StepItem it = a.items[p.row];
@@ -176,6 +178,10 @@ __device__ __forceinline__ void consume_append(const StepArgs& a, const Layout& 
     pa[r] = x;
     pb[r] = y;
   }
+  if (!merge) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty_bar);
+  }
   const float A = reduce_scatter32(pa, lane);
   float B = 0.f;
   if constexpr (DELTA) B = reduce_scatter32(pb, lane);
@@ -209,7 +215,7 @@ __device__ __forceinline__ void consume_append(const StepArgs& a, const Layout& 
     o += cf[3] * bf16f(V[n * DV + col]);
     store_out(a, oidx, a.scale * o);
   }
-  if (!merge) return;
+  if (!merge) return true;
 
   // merge: S̄[slot] rows = D ⊙ S̄[base] rows + Σ_{j<=n} a_j[row] K̃_j
   float D[VEC];
@@ -262,6 +268,7 @@ __device__ __forceinline__ void consume_append(const StepArgs& a, const Layout& 
 #pragma unroll
     for (int i = 0; i < 8; ++i) stvec_cs<VEC>(dst + (size_t)(rb * 8 + i) * DK, acc[i]);
   }
+  return false;
 }
 
 // ------------------------------------------------------------- EagerStep ----
@@ -463,14 +470,16 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) pipe_kernel(const __grid_cons
     if (!__all_sync(0xffffffffu, ok)) break;
     const float* T = tiles + (size_t)s * BV * DK;
     unsigned char* ax = auxm + (size_t)x * aux_bytes;
-    if constexpr (MODE == APPEND) consume_append<OP, DK, DV>(a, Lay, p, vt, T, ax, lane);
+    bool released = false;
+    if constexpr (MODE == APPEND)
+      released = consume_append<OP, DK, DV>(a, Lay, p, vt, T, ax, lane, bars.empty(s));
     else consume_eager<OP, DK, DV>(a, Lay, p, vt, T, ax, lane, g_s, beta_s);
     // order this warp's shared-memory writes (u_t rows of a merge) before the
     // bulk copies that will refill the slots once they are released
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
-      mbar_arrive(bars.empty(s));
+      if (!released) mbar_arrive(bars.empty(s));
       mbar_arrive(bars.aempty(x));
     }
   }
