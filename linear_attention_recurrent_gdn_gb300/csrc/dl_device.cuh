@@ -226,6 +226,32 @@ __device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
   return v[0];
 }
 
+// Transposed reduction of NE = 2^E per-entry partial sums (NE <= 32): E halving
+// exchanges over lane bits 4, 3, ... leave one entry per lane group, then the
+// remaining 5-E lane bits are summed.  Returns, on every lane, the full sum of
+// entry (lane >> (5 - E)).
+template <int NE>
+__device__ __forceinline__ float reduce_entries(float (&v)[NE], int lane) {
+  constexpr int E = NE == 32 ? 5 : NE == 16 ? 4 : NE == 8 ? 3 : NE == 4 ? 2 : 1;
+  static_assert((1 << E) == NE, "NE must be a power of two <= 32");
+#pragma unroll
+  for (int s = 0; s < E; ++s) {
+    const int off = 16 >> s;
+    const int half = NE >> (s + 1);
+    const bool up = (lane & off) != 0;
+#pragma unroll
+    for (int j = 0; j < half; ++j) {
+      const float send = up ? v[j] : v[j + half];
+      const float keep = up ? v[j + half] : v[j];
+      v[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+  float r = v[0];
+#pragma unroll
+  for (int off = 16 >> E; off > 0; off >>= 1) r += __shfl_xor_sync(0xffffffffu, r, off);
+  return r;
+}
+
 // Load VEC consecutive floats (VEC = 2 or 4) from shared or global memory.
 template <int VEC>
 __device__ __forceinline__ void ldvec(float (&d)[VEC], const float* p) {

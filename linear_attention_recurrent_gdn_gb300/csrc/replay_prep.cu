@@ -26,8 +26,9 @@
 //
 // Launch: one warp per (row, head), 8 warps per CTA.  Lane l holds d_k/32
 // consecutive key channels; every log row is read (and every K̃ row written)
-// as one coalesced warp access; the per-entry dot products (n <= 31) are
-// finished by the transposed butterfly, which leaves entry j on lane j.
+// as one coalesced warp access; the per-entry dot products (n <= M-1 <= 31)
+// are finished by a transposed butterfly over NE = 8, 16 or 32 entries, which
+// leaves entry j on lanes j*32/NE .. (j+1)*32/NE - 1.
 #include "dl_device.cuh"
 #include "layout.h"
 #include "launch.h"
@@ -36,10 +37,14 @@ namespace dl {
 
 constexpr int RP_WARPS = 8;
 
-template <int OP, int DK, int DV>
+// NE: per-entry partial sums held per lane, the power of two >= M-1 (at least 8).
+template <int OP, int DK, int DV, int NE>
 __global__ void __launch_bounds__(RP_WARPS * 32)
 replay_prep_kernel(const __grid_constant__ StepArgs a) {
   constexpr int VEC = DK / 32;
+  constexpr int SHIFT = NE == 32 ? 0 : NE == 16 ? 1 : 2;   // entry of lane l: l >> SHIFT
+  const int lane_entry = (threadIdx.x & 31) >> SHIFT;
+  const bool entry_writer = ((threadIdx.x & 31) & ((1 << SHIFT) - 1)) == 0;
   // Let AppendDecode start streaming the dense base while this kernel runs.
   pdl_launch_dependents();
 
@@ -61,7 +66,7 @@ replay_prep_kernel(const __grid_constant__ StepArgs a) {
   ldvec_bf16<VEC>(kv, a.k + (size_t)sh * DK + c0);
   ldvec_bf16<VEC>(qv, a.q + (size_t)sh * DK + c0);
 
-  float p1[32], p2[32];                               // per-entry partial dot products
+  float p1[NE], p2[NE];                               // per-entry partial dot products
   if constexpr (OP == GDN) {
     float kq = 0.f;
 #pragma unroll
@@ -70,7 +75,7 @@ replay_prep_kernel(const __grid_constant__ StepArgs a) {
     const float* Lrow = a.Llog + lh * Mcap;
     const float Lt = (n > 0 ? Lrow[n - 1] : 0.f) + a.g[sh];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
+    for (int j = 0; j < NE; ++j) {
       float x = 0.f, y = 0.f;
       if (j < n) {
         float kj[VEC];
@@ -84,13 +89,13 @@ replay_prep_kernel(const __grid_constant__ StepArgs a) {
       p1[j] = x;
       p2[j] = y;
     }
-    const float dkk = reduce_scatter32(p1, lane);
-    const float dkq = reduce_scatter32(p2, lane);
-    if (lane < n) {
-      const float wj = expf(Lt - Lrow[lane]);
-      cf[HDR + lane] = wj * dkk;
-      cf[HDR + Mcap4 + lane] = wj * dkq;
-      if (merge) cf[Lay.P0 + lane] = wj;
+    const float dkk = reduce_entries<NE>(p1, lane);
+    const float dkq = reduce_entries<NE>(p2, lane);
+    if (entry_writer && lane_entry < n) {
+      const float wj = expf(Lt - Lrow[lane_entry]);
+      cf[HDR + lane_entry] = wj * dkk;
+      cf[HDR + Mcap4 + lane_entry] = wj * dkq;
+      if (merge) cf[Lay.P0 + lane_entry] = wj;
     }
     if (lane == 0) {
       cf[0] = expf(Lt);
@@ -155,7 +160,7 @@ replay_prep_kernel(const __grid_constant__ StepArgs a) {
       if (lane == 0) cf[3] = cb;
     }
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
+    for (int j = 0; j < NE; ++j) {
       float x = 0.f, y = 0.f;
       if (j < n) {
         float kj[VEC], lj[VEC];
@@ -185,12 +190,12 @@ replay_prep_kernel(const __grid_constant__ StepArgs a) {
       p1[j] = x;
       p2[j] = y;
     }
-    const float d1 = reduce_scatter32(p1, lane);
+    const float d1 = reduce_entries<NE>(p1, lane);
     float d2 = 0.f;
-    if constexpr (OP == KDA) d2 = reduce_scatter32(p2, lane);
-    if (lane < n) {
-      cf[HDR + lane] = d1;
-      if constexpr (OP == KDA) cf[HDR + Mcap4 + lane] = d2;
+    if constexpr (OP == KDA) d2 = reduce_entries<NE>(p2, lane);
+    if (entry_writer && lane_entry < n) {
+      cf[HDR + lane_entry] = d1;
+      if constexpr (OP == KDA) cf[HDR + Mcap4 + lane_entry] = d2;
     }
     if (!merge) {
       float* Ld = a.Llog + (lh * Mcap + n) * DK + c0;
@@ -221,7 +226,10 @@ replay_prep_kernel(const __grid_constant__ StepArgs a) {
 template <int OP, int DK>
 static cudaError_t launch_rp(const StepArgs& a, cudaStream_t s) {
   const int warps = a.rows * a.H;
-  replay_prep_kernel<OP, DK, DK><<<(warps + RP_WARPS - 1) / RP_WARPS, RP_WARPS * 32, 0, s>>>(a);
+  const int blocks = (warps + RP_WARPS - 1) / RP_WARPS;
+  if (a.M - 1 <= 8) replay_prep_kernel<OP, DK, DK, 8><<<blocks, RP_WARPS * 32, 0, s>>>(a);
+  else if (a.M - 1 <= 16) replay_prep_kernel<OP, DK, DK, 16><<<blocks, RP_WARPS * 32, 0, s>>>(a);
+  else replay_prep_kernel<OP, DK, DK, 32><<<blocks, RP_WARPS * 32, 0, s>>>(a);
   return cudaGetLastError();
 }
 
