@@ -244,6 +244,49 @@ dl_status dl_window_create(dl_ctx *ctx, const int32_t *slots, int32_t n,
 dl_status dl_window_launch(dl_window *w);
 dl_status dl_window_destroy(dl_window *w);
 
+/* ------------------------------------------------------------------------ */
+/* A decode step that allocates no device memory.                            */
+/* The paper has no counterpart: this entry point exists for callers that    */
+/* cannot let a library call cudaMalloc while they run — engines that reserve */
+/* almost all device memory for their own pools at start-up, code whose       */
+/* device buffers must all come from the caller's own allocator, and loops    */
+/* that cannot afford the device synchronisation an allocation can cause.    */
+/* The caller owns every buffer (layouts as in dl_create); the coefficient    */
+/* scratch of the step lives in a static device array of the library.        */
+/* ------------------------------------------------------------------------ */
+#define DL_NOALLOC_SCRATCH_FLOATS (4 * 1024 * 1024)   /* 16 MiB of fp32 scratch */
+
+typedef struct dl_state_view {
+    float *Sbar;         /* [num_slots, H, d_v, d_k] fp32 dense bases                     */
+    void *alog;          /* [num_slots, H, max(M-1,1), d_v] fp32 (bf16 for RWKV6), value log */
+    uint16_t *klog;      /* [num_slots, H, max(M-1,1), d_k] bf16 key log                    */
+    float *Llog;         /* [num_slots, H, max(M-1,1)] (GDN) or [..., d_k] fp32 log-decays  */
+    int32_t *n_log;      /* [num_slots] device slot table: log lengths (written)            */
+    int32_t *base_of;    /* [num_slots] device slot table: base indices (written)           */
+    const float *bonus;  /* [H, d_k] fp32 (RWKV6), else NULL                                */
+} dl_state_view;
+
+/* One token for n slots on caller-owned state, without allocating.  `plan` is
+ * the host array that dl_table_step returns for this step ([n][4]: slot, base
+ * read, log length before the step, merge flag); the caller keeps a dl_table
+ * (host memory) for its slots.  Tensors and stream are as in dl_step.  The
+ * step's coefficient scratch must fit DL_NOALLOC_SCRATCH_FLOATS (n * H * CB
+ * floats; CB grows with M and, for KDA/RWKV6, with M * d_k); larger steps are
+ * refused with DL_EINVAL — split them over several calls.  The scratch is one
+ * array shared by every call and keeps the last call's contents: within a
+ * call every coefficient used is written first, and the status word is
+ * cleared at the start, but calls that overlap on the GPU race, so order
+ * them on one stream.  The first call on a
+ * device does a one-time set-up with that device current (it looks up the
+ * scratch's device address and sets kernel shared-memory limits); make it
+ * before any stream capture.  If errbuf != NULL it receives a one-line reason
+ * for a non-DL_OK status (at most errlen bytes, NUL-terminated). */
+dl_status dl_step_noalloc(const dl_config *cfg, const dl_state_view *st,
+                          const int32_t *plan, int32_t n,
+                          const void *q, const void *k, const void *v,
+                          const float *g, const float *beta, void *o,
+                          void *stream, char *errbuf, int32_t errlen);
+
 /* Synchronise the stream and report any CUDA or device-side error. */
 dl_status dl_sync(dl_ctx *ctx);
 

@@ -18,7 +18,7 @@ OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libdeltalog.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CU_SOURCES = ["replay_prep.cu", "append_decode.cu", "eager_step.cu", "slot_ops.cu", "prefill.cu",
-              "capi.cu"]
+              "capi.cu", "noalloc.cu"]
 CPP_SOURCES = ["slot_table.cpp"]
 
 

@@ -30,6 +30,7 @@ EXPORTS = [
     "dl_sync", "dl_set_timing", "dl_get_timing", "dl_last_error", "dl_status_str",
     "dl_abi_version", "dl_checkpoint_bytes", "dl_checkpoint_save", "dl_checkpoint_load",
     "dl_window_create", "dl_window_launch", "dl_window_destroy", "dl_prefill",
+    "dl_step_noalloc",
 ]
 
 
@@ -44,6 +45,12 @@ class dl_config(ctypes.Structure):
                 ("num_heads", ctypes.c_int32), ("d_k", ctypes.c_int32),
                 ("d_v", ctypes.c_int32), ("merge_interval", ctypes.c_int32),
                 ("out_bf16", ctypes.c_int32), ("scale", ctypes.c_float)]
+
+
+class dl_state_view(ctypes.Structure):
+    _fields_ = [("Sbar", ctypes.c_void_p), ("alog", ctypes.c_void_p), ("klog", ctypes.c_void_p),
+                ("Llog", ctypes.c_void_p), ("n_log", ctypes.c_void_p),
+                ("base_of", ctypes.c_void_p), ("bonus", ctypes.c_void_p)]
 
 
 def _load():
@@ -87,6 +94,8 @@ def _load():
         "dl_window_launch": ([P], I32),
         "dl_window_destroy": ([P], I32),
         "dl_prefill": ([P, P, I32, I32, P, P, P, P, P, P], I32),
+        "dl_step_noalloc": ([ctypes.POINTER(dl_config), ctypes.POINTER(dl_state_view), P, I32,
+                             P, P, P, P, P, P, P, ctypes.c_char_p, I32], I32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -282,6 +291,22 @@ def dl_window_launch(ctx, w):
 
 def dl_window_destroy(w):
     _lib.dl_window_destroy(w)
+
+
+def dl_step_noalloc(cfg, state, plan, q, k, v, g, beta, o, stream=None):
+    """One step on caller-owned buffers with no allocation inside the library.
+    `state` maps dl_state_view field names to torch tensors (bonus may be None);
+    `plan` is the [n, 4] int32 array from dl_table_step."""
+    pl = np.ascontiguousarray(np.asarray(plan, dtype=np.int32).reshape(-1, 4))
+    sv = dl_state_view(*[None if state.get(f) is None else state[f].data_ptr()
+                         for f, _ in dl_state_view._fields_])
+    err = ctypes.create_string_buffer(256)
+    st = ctypes.c_void_p(0 if stream is None else int(stream))
+    rc = _lib.dl_step_noalloc(ctypes.byref(cfg), ctypes.byref(sv),
+                              pl.ctypes.data_as(ctypes.c_void_p), int(pl.shape[0]), _ptr(q),
+                              _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(o), st, err, 256)
+    if rc != OK:
+        raise DeltaLogError(rc, err.value.decode())
 
 
 def dl_last_error(ctx):
