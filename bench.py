@@ -181,8 +181,8 @@ def run_reference(args):
     import oracle
     from linear_attention_recurrent_gdn_gb300 import inputs as gen
     w = WORKLOADS[args.workload]
-    sample_sh = int(os.environ.get("DL_REF_SLOT_HEADS", "256"))
-    tokens = int(os.environ.get("DL_REF_TOKENS", "64"))
+    sample_sh = int(os.environ.get("DL_REF_SLOT_HEADS", "4096"))
+    tokens = int(os.environ.get("DL_REF_TOKENS", "512"))
     oracle.build()
     res = cpu_baseline(w, sample_sh, tokens, args.steps, args.warmup)
     out = {"metric": METRIC, "value": res["value"], "unit": "tokens·heads/s", "n_gpus": 0,
@@ -410,8 +410,9 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu:
         import oracle
         oracle.build()
-        result["cpu_baseline"] = cpu_baseline(w, int(os.environ.get("DL_REF_SLOT_HEADS", "256")),
-                                              int(os.environ.get("DL_REF_TOKENS", "64")))
+        result["cpu_baseline"] = cpu_baseline(w, int(os.environ.get("DL_REF_SLOT_HEADS", "4096")),
+                                              int(os.environ.get("DL_REF_TOKENS", "512")),
+                                              steps=3, warmup=0)
         result["cpu_baseline"].update({"unit": "tokens·heads/s", "kind": "oracle"})
         result["cpu_baseline"].pop("ms_per_step", None)
     if rank == 0:

@@ -8,7 +8,7 @@ template <int OP, int DK>
 static cudaError_t launch_ad(const StepArgs& a, int grid, size_t smem, bool pdl, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(PIPE_THREADS);
+  cfg.blockDim = dim3((a.ncw + 1) * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];

@@ -37,7 +37,7 @@ struct TimedPair {
 struct dl_ctx {
   dl_config cfg{};
   cudaStream_t stream = nullptr;
-  int device = 0, num_sms = 0, smem_optin = 0;
+  int device = 0, num_sms = 0, smem_optin = 0, smem_per_sm = 0;
   dl_table* table = nullptr;
   dl::Layout L{};
   float* Sbar = nullptr;
@@ -126,31 +126,9 @@ void free_all(dl_ctx* c) {
   c->table = nullptr;
 }
 
-// Pipeline shape for a launch with G tiles per unit: ns = NCW * R stages (each
-// consumer warp owns R of them), the largest R <= 3 that fits, and enough aux
-// slots to cover the units those stages span.
-struct PipeShape {
-  int ns, na;
-  size_t smem;
-};
-
-PipeShape pipe_shape(const dl_ctx* c, int G, bool append) {
-  const size_t tile = (size_t)dl::BV * c->cfg.d_k * 4;
-  const size_t aux = append ? c->L.aux_bytes : c->L.e_bytes;
-  const size_t budget = (size_t)c->smem_optin - dl::BAR_BYTES - 1024;
-  PipeShape best{0, 0, 0};
-  for (int R = 1; R <= 3; ++R) {
-    const int ns = dl::NCW * R;
-    int na = (ns + G - 1) / G + 1;
-    if (na > 16) na = 16;
-    size_t need = (size_t)ns * tile + (size_t)na * aux;
-    while (need > budget && na > 2) {
-      --na;
-      need = (size_t)ns * tile + (size_t)na * aux;
-    }
-    if (need <= budget) best = PipeShape{ns, na, dl::BAR_BYTES + need};
-  }
-  return best;
+dl::PipePlan pipe_shape(const dl_ctx* c, int G, bool append) {
+  return dl::plan_pipeline(c->cfg.d_k, append ? c->L.aux_bytes : c->L.e_bytes, G, c->smem_optin,
+                           c->smem_per_sm);
 }
 
 bool record(dl_ctx* c, int kind, cudaEvent_t* ev) {
@@ -233,8 +211,8 @@ void fill_step_args(dl_ctx* c, dl::StepArgs& a, int32_t row0, int32_t rows, cons
   }
 }
 
-// Choose G (value tiles per work unit) and the grid for `rows` slot rows.
-void unit_shape(const dl_ctx* c, dl::StepArgs& a, int* grid) {
+// Choose G (value tiles per work unit) for `rows` slot rows.
+void unit_shape(const dl_ctx* c, dl::StepArgs& a) {
   const int nvt = c->cfg.d_v / dl::BV;
   const long n_sh = (long)a.rows * a.H;
   if (n_sh >= 2L * c->num_sms) {
@@ -244,8 +222,6 @@ void unit_shape(const dl_ctx* c, dl::StepArgs& a, int* grid) {
     a.G = 1;
     a.NG = nvt;
   }
-  const long units = n_sh * a.NG;
-  *grid = (int)(units < c->num_sms ? units : c->num_sms);
 }
 
 dl_status run_step(dl_ctx* c, const int32_t* slots, int32_t n, const void* q, const void* k,
@@ -256,12 +232,15 @@ dl_status run_step(dl_ctx* c, const int32_t* slots, int32_t n, const void* q, co
   for (int32_t row0 = 0; row0 < n; row0 += dl::MAX_ROWS) {
     const int32_t rows = (n - row0) < dl::MAX_ROWS ? (n - row0) : dl::MAX_ROWS;
     fill_step_args(c, a, row0, rows, q, k, v, g, beta, o);
-    int grid = 0;
-    unit_shape(c, a, &grid);
-    const PipeShape ps = pipe_shape(c, a.G, !eager);
+    unit_shape(c, a);
+    const dl::PipePlan ps = pipe_shape(c, a.G, !eager);
     if (ps.ns == 0) return set_err(c, DL_EUNSUPPORTED, "pipeline does not fit in shared memory");
     a.ns = ps.ns;
     a.na = ps.na;
+    a.ncw = ps.ncw;
+    const long units = (long)a.rows * a.H * a.NG;
+    const long slots_gpu = (long)ps.cps * c->num_sms;
+    const int grid = (int)(units < slots_gpu ? units : slots_gpu);
     cudaEvent_t e0;
     if (eager) {
       const bool t = record(c, 2, &e0);
@@ -329,6 +308,8 @@ dl_status dl_create(const dl_config* cfg, void* stream, dl_ctx** out) {
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
     if (e == cudaSuccess)
       e = cudaDeviceGetAttribute(&c->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c->device);
+    if (e == cudaSuccess)
+      e = cudaDeviceGetAttribute(&c->smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, c->device);
     if (e != cudaSuccess) { rc = cuda_err(c, e, "device query"); break; }
     const size_t S = f.num_slots, H = f.num_heads, dk = f.d_k, dv = f.d_v, Mcap = c->L.Mcap;
     const size_t esa = (f.op == DL_RWKV6) ? 2 : 4;
@@ -362,12 +343,11 @@ dl_status dl_create(const dl_config* cfg, void* stream, dl_ctx** out) {
       if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
     }
     if (e != cudaSuccess) { rc = cuda_err(c, e, "context initialisation"); break; }
-    const PipeShape big = pipe_shape(c, 1, true);
-    size_t smem = big.smem;
+    size_t smem = 0;
     for (int G = 1; G <= 4; G *= 2) {
-      const PipeShape a = pipe_shape(c, G, true), b = pipe_shape(c, G, false);
-      if (a.smem > smem) smem = a.smem;
-      if (b.smem > smem) smem = b.smem;
+      const dl::PipePlan a = pipe_shape(c, G, true), b = pipe_shape(c, G, false);
+      if ((size_t)a.smem > smem) smem = a.smem;
+      if ((size_t)b.smem > smem) smem = b.smem;
     }
     e = dl::configure_append_decode(f.op, f.d_k, smem);
     if (e == cudaSuccess) e = dl::configure_eager_step(f.op, f.d_k, smem);

@@ -15,8 +15,8 @@ namespace dl {
 enum Op : int { GDN = 0, KDA = 1, RWKV6 = 2 };
 
 constexpr int BV = 32;            // value rows per tile (one warp owns one tile)
-constexpr int NCW = 8;            // consumer warps per AppendDecode / EagerStep CTA
-constexpr int PIPE_THREADS = (NCW + 1) * 32;
+constexpr int MAX_NCW = 8;        // consumer warps per AppendDecode / EagerStep CTA (at most)
+constexpr int PIPE_THREADS_MAX = (MAX_NCW + 1) * 32;
 constexpr int MAX_ROWS = 1024;    // slot rows per launch (more are split into chunks)
 constexpr int HDR = 8;            // scalar header of a coefficient block (floats)
 constexpr int BAR_BYTES = 1024;   // mbarrier area at the start of the pipelined kernels' shared memory
@@ -54,6 +54,7 @@ struct StepArgs {
   int32_t rows, H, M, Mcap, Mcap4, CB, P0;   // P0: coefficient floats needed on append steps
   int32_t G, NG;         // value tiles per work unit, units per slot-head
   int32_t ns, na;        // pipeline stages (tiles), aux slots
+  int32_t ncw;           // consumer warps per CTA (block = (ncw + 1) warps)
   int32_t aux_bytes;     // bytes of one aux slot
   int32_t out_bf16;
   float scale;
@@ -176,6 +177,20 @@ __device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void* src, uin
       "[%1], %2, [%3], %4;" ::"r"(dst),
       "l"(src), "r"(bytes), "r"(bar), "l"(policy)
       : "memory");
+}
+
+// 16-byte asynchronous copy global -> shared through the load/store unit (not
+// the TMA engine), and an mbarrier arrival that fires when all of this thread's
+// earlier such copies have landed (counted as one of the barrier's expected
+// arrivals).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 // Programmatic dependent launch controls.

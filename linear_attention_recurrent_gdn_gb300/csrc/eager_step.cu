@@ -9,7 +9,7 @@ namespace dl {
 
 template <int OP, int DK>
 static cudaError_t launch_ea(const StepArgs& a, int grid, size_t smem, cudaStream_t s) {
-  pipe_kernel<OP, DK, DK, EAGER><<<grid, PIPE_THREADS, smem, s>>>(a);
+  pipe_kernel<OP, DK, DK, EAGER><<<grid, (a.ncw + 1) * 32, smem, s>>>(a);
   return cudaGetLastError();
 }
 

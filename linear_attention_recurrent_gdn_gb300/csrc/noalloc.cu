@@ -55,6 +55,7 @@ struct DeviceSetup {
   int32_t* status = nullptr;   // device address of g_noalloc_status
   int num_sms = 0;
   int smem_optin = 0;
+  int smem_per_sm = 0;
   size_t smem_configured[3][2] = {{0, 0}, {0, 0}, {0, 0}};   // per (op, d_k 64/128)
 };
 
@@ -82,31 +83,6 @@ struct ErrOut {
     return s;
   }
 };
-
-// Same stage/aux shape rule as the context path (each consumer warp owns R
-// stages; enough aux slots for the units the stages span).
-struct Shape {
-  int ns, na;
-  size_t smem;
-};
-
-Shape shape_for(const dl::Layout& L, int dk, int G, int smem_optin) {
-  const size_t tile = (size_t)dl::BV * dk * 4;
-  const size_t budget = (size_t)smem_optin - dl::BAR_BYTES - 1024;
-  Shape best{0, 0, 0};
-  for (int R = 1; R <= 3; ++R) {
-    const int ns = dl::NCW * R;
-    int na = (ns + G - 1) / G + 1;
-    if (na > 16) na = 16;
-    size_t need = (size_t)ns * tile + (size_t)na * L.aux_bytes;
-    while (need > budget && na > 2) {
-      --na;
-      need = (size_t)ns * tile + (size_t)na * L.aux_bytes;
-    }
-    if (need <= budget) best = Shape{ns, na, dl::BAR_BYTES + need};
-  }
-  return best;
-}
 
 }  // namespace
 
@@ -159,6 +135,8 @@ extern "C" dl_status dl_step_noalloc(const dl_config* cfg, const dl_state_view* 
         return fail(DL_ECUDA, "cudaGetSymbolAddress of the static scratch failed");
       if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
           cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+              cudaSuccess ||
+          cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
               cudaSuccess)
         return fail(DL_ECUDA, "device query failed");
       d.ready = true;
@@ -202,18 +180,20 @@ extern "C" dl_status dl_step_noalloc(const dl_config* cfg, const dl_state_view* 
     a.G = 1;
     a.NG = nvt;
   }
-  const long units = n_sh * a.NG;
-  const int grid = (int)(units < d.num_sms ? units : d.num_sms);
-  const Shape sh = shape_for(L, f.d_k, a.G, d.smem_optin);
+  const dl::PipePlan sh = dl::plan_pipeline(f.d_k, L.aux_bytes, a.G, d.smem_optin, d.smem_per_sm);
   if (sh.ns == 0) return fail(DL_EUNSUPPORTED, "pipeline does not fit in shared memory");
   a.ns = sh.ns;
   a.na = sh.na;
+  a.ncw = sh.ncw;
+  const long units = n_sh * a.NG;
+  const long slots_gpu = (long)sh.cps * d.num_sms;
+  const int grid = (int)(units < slots_gpu ? units : slots_gpu);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
   const int di = f.d_k == 64 ? 0 : 1;
   {
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (d.smem_configured[f.op][di] < sh.smem) {
+    if (d.smem_configured[f.op][di] < (size_t)sh.smem) {
       e = dl::configure_append_decode(f.op, f.d_k, sh.smem);
       if (e == cudaSuccess) d.smem_configured[f.op][di] = sh.smem;
     }

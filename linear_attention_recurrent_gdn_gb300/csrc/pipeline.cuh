@@ -7,22 +7,27 @@
 // factors and log-decay metadata (here: the ReplayPrep coefficient block) are
 // shared by all value tiles of a slot-head.
 //
-// Structure on sm_103a (one CTA per SM, persistent over work units):
+// Structure on sm_103a (persistent over work units; one or two CTAs per SM):
 //   * work unit = (slot-head, group of G value tiles); tile = 32 value rows of
-//     the dense base (32 x d_k fp32, contiguous in HBM);
-//   * warp NCW is the producer: one lane issues 1-D bulk copies (TMA engine)
-//     of each tile into a ring of `ns` shared-memory stages, and of each unit's
-//     small inputs (coefficients, k/q/v, value-side log rows, key log rows on a
-//     merge) into a ring of `na` aux slots, completion tracked in bytes on
-//     mbarriers; the dense base is read with an L2 evict-first policy;
-//   * warps 0..NCW-1 are consumers: one warp owns one tile.  Lane l holds d_k/32
-//     consecutive key channels; a pass over the 32 rows accumulates per-row
-//     partial dot products, a transposed butterfly reduction (31 shuffles for
-//     32 rows) leaves row l's sums on lane l, which then finishes that row:
-//     log replay, output, the appended factor; on a merge step the warp then
-//     re-reads the tile from shared memory and writes the updated rows;
-//   * every wait is bounded (see mbar_wait); a consumer releases its stage and
-//     its share of the aux slot with one mbarrier arrive each.
+//     the dense base (32 x d_k fp32, contiguous in HBM: 16 KiB at d_k = 128);
+//   * the last warp is the producer.  One lane issues one 1-D bulk copy (TMA
+//     engine) per tile into a ring of `ns` shared-memory stages, completion
+//     counted in bytes on an mbarrier, with an L2 evict-first policy (the base
+//     is read once per step).  The unit's small inputs (coefficient block,
+//     k/q/v, value-side log rows, key log rows on a GDN merge) are copied by
+//     all 32 lanes with 16-byte cp.async into a ring of `na` aux slots: a bulk
+//     copy has a fixed issue cost per copy on this GPU, so it is kept for the
+//     tiles;
+//   * the other `ncw` warps are consumers; warp w owns stages w*R .. w*R+R-1
+//     and processes tiles w, w+ncw, ...  Lane l holds d_k/32 consecutive key
+//     channels; a pass over the 32 rows accumulates per-row partial dot
+//     products, a transposed butterfly (31 shuffles for 32 rows) leaves row
+//     l's sums on lane l, which then finishes that row: log replay, output,
+//     the appended factor; on a merge step the warp then re-reads the tile
+//     from shared memory and writes the updated rows;
+//   * every wait is bounded (see mbar_wait).  On an append step a consumer
+//     releases its stage right after the tile pass, so the refill overlaps its
+//     epilogue.
 // AppendDecode launches as a programmatic dependent of ReplayPrep: its
 // producer streams the first ns tiles before it waits for ReplayPrep's
 // coefficient blocks.
@@ -45,16 +50,16 @@ struct Bars {
   __device__ uint32_t aempty(int x) const { return b0 + 8u * (2 * ns + na + x); }
 };
 
-// Stage ownership: tile i (CTA-local order) belongs to consumer warp i % NCW,
-// and each warp owns R = ns / NCW consecutive stages that it cycles through.
+// Stage ownership: tile i (CTA-local order) belongs to consumer warp i % ncw,
+// and each warp owns R = ns / ncw consecutive stages that it cycles through.
 // A warp therefore waits on a stage only after it released that stage's
 // previous phase itself, so no barrier is ever awaited more than one phase
 // ahead (mbarrier parity waits cannot tell phases two apart).
-__device__ __forceinline__ int stage_of(int i, int R) {
-  return (i % NCW) * R + (i / NCW) % R;
+__device__ __forceinline__ int stage_of(int i, int R, int ncw) {
+  return (i % ncw) * R + (i / ncw) % R;
 }
-__device__ __forceinline__ uint32_t stage_parity(int i, int R) {
-  return (uint32_t)((i / NCW) / R) & 1u;
+__device__ __forceinline__ uint32_t stage_parity(int i, int R, int ncw) {
+  return (uint32_t)((i / ncw) / R) & 1u;
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -80,60 +85,59 @@ __device__ __forceinline__ void store_out(const StepArgs& a, size_t idx, float v
 }
 
 // ---------------------------------------------------------------- producer --
+// A unit's small inputs (coefficient block, k/q/v, value-side log rows, key
+// log rows on a GDN merge) are copied by all 32 lanes of the producer warp with
+// 16-byte cp.async (load/store unit path: the TMA engine's per-copy cost is
+// kept for the 16 KiB tiles).  Each lane then arrives once on the unit's aux
+// barrier (expected count 32) when its own copies have landed.
+__device__ __forceinline__ void copy_seg(uint32_t dst, const void* src, uint32_t bytes, int lane) {
+  const unsigned char* s = static_cast<const unsigned char*>(src);
+  for (uint32_t off = (uint32_t)lane * 16u; off < bytes; off += 32u * 16u) cp_async16(dst + off, s + off);
+}
+
 template <int OP, int DK, int DV, int MODE>
 __device__ __forceinline__ void issue_aux(const StepArgs& a, const Layout& Lay, const UnitPos& p,
-                                          unsigned char* ax, uint32_t bar, bool with_coef_now) {
+                                          unsigned char* ax, int lane) {
   constexpr bool DELTA = OP != RWKV6;
   const StepItem it = a.items[p.row];
   const size_t sh = p.sh;
+  const uint32_t base = smem_u32(ax);
   if constexpr (MODE == APPEND) {
     constexpr int ESA = DELTA ? 4 : 2;
     const int n = it.n;
     const bool merge = (n + 1 == a.M);
     const size_t lh = (size_t)it.slot * a.H + p.h;
-    uint32_t bytes = (merge ? Lay.CB : Lay.P0) * 4u;
-    if (OP == GDN) bytes += 2u * DK * 2u;
-    if (DELTA) bytes += DV * 2u;
-    bytes += (uint32_t)n * DV * ESA;
-    if (OP == RWKV6) bytes += DV * 2u;
-    if (OP == GDN && merge) bytes += (uint32_t)(n + 1) * DK * 2u;
-    mbar_arrive_expect_tx(bar, bytes);
     if (OP == GDN) {
-      bulk_g2s(smem_u32(ax + Lay.aux_kq), a.k + sh * DK, DK * 2, bar);
-      bulk_g2s(smem_u32(ax + Lay.aux_kq + DK * 2), a.q + sh * DK, DK * 2, bar);
+      copy_seg(base + Lay.aux_kq, a.k + sh * DK, DK * 2, lane);
+      copy_seg(base + Lay.aux_kq + DK * 2, a.q + sh * DK, DK * 2, lane);
     }
-    if (DELTA) bulk_g2s(smem_u32(ax + Lay.aux_v), a.v + sh * DV, DV * 2, bar);
+    if (DELTA) copy_seg(base + Lay.aux_v, a.v + sh * DV, DV * 2, lane);
     if (n > 0)
-      bulk_g2s(smem_u32(ax + Lay.aux_U),
-               static_cast<const unsigned char*>(a.alog) + lh * Lay.Mcap * DV * ESA,
-               (uint32_t)n * DV * ESA, bar);
-    if (OP == RWKV6) bulk_g2s(smem_u32(ax + Lay.aux_U + n * DV * 2), a.v + sh * DV, DV * 2, bar);
+      copy_seg(base + Lay.aux_U, static_cast<const unsigned char*>(a.alog) + lh * Lay.Mcap * DV * ESA,
+               (uint32_t)n * DV * ESA, lane);
+    if (OP == RWKV6) copy_seg(base + Lay.aux_U + n * DV * 2, a.v + sh * DV, DV * 2, lane);
     if (OP == GDN && merge) {
-      if (n > 0)
-        bulk_g2s(smem_u32(ax + Lay.aux_kl), a.klog + lh * Lay.Mcap * DK, (uint32_t)n * DK * 2,
-                 bar);
-      bulk_g2s(smem_u32(ax + Lay.aux_kl + n * DK * 2), a.k + sh * DK, DK * 2, bar);
+      if (n > 0) copy_seg(base + Lay.aux_kl, a.klog + lh * Lay.Mcap * DK, (uint32_t)n * DK * 2, lane);
+      copy_seg(base + Lay.aux_kl + n * DK * 2, a.k + sh * DK, DK * 2, lane);
     }
-    if (with_coef_now)
-      bulk_g2s(smem_u32(ax + Lay.aux_coef), a.coef + sh * a.CB, (merge ? Lay.CB : Lay.P0) * 4u,
-               bar);
   } else {
-    uint32_t bytes = 2u * DK * 2u + DV * 2u + (OP != GDN ? DK * 4u : 0u);
-    mbar_arrive_expect_tx(bar, bytes);
-    bulk_g2s(smem_u32(ax + Lay.e_kq), a.k + sh * DK, DK * 2, bar);
-    bulk_g2s(smem_u32(ax + Lay.e_kq + DK * 2), a.q + sh * DK, DK * 2, bar);
-    bulk_g2s(smem_u32(ax + Lay.e_v), a.v + sh * DV, DV * 2, bar);
-    if (OP != GDN) bulk_g2s(smem_u32(ax + Lay.e_g), a.g + sh * DK, DK * 4, bar);
+    copy_seg(base + Lay.e_kq, a.k + sh * DK, DK * 2, lane);
+    copy_seg(base + Lay.e_kq + DK * 2, a.q + sh * DK, DK * 2, lane);
+    copy_seg(base + Lay.e_v, a.v + sh * DV, DV * 2, lane);
+    if (OP != GDN) copy_seg(base + Lay.e_g, a.g + sh * DK, DK * 4, lane);
   }
 }
 
+// The coefficient block (written by ReplayPrep), then this lane's arrival.
 template <int OP, int DK, int DV>
-__device__ __forceinline__ void issue_coef(const StepArgs& a, const Layout& Lay, const UnitPos& p,
-                                           unsigned char* ax, uint32_t bar) {
+__device__ __forceinline__ void issue_coef_and_arrive(const StepArgs& a, const Layout& Lay,
+                                                      const UnitPos& p, unsigned char* ax,
+                                                      uint32_t bar, int lane) {
   const StepItem it = a.items[p.row];
   const bool merge = (it.n + 1 == a.M);
-  bulk_g2s(smem_u32(ax + Lay.aux_coef), a.coef + (size_t)p.sh * a.CB,
-           (merge ? Lay.CB : Lay.P0) * 4u, bar);
+  copy_seg(smem_u32(ax + Lay.aux_coef), a.coef + (size_t)p.sh * a.CB,
+           (merge ? Lay.CB : Lay.P0) * 4u, lane);
+  cp_async_arrive_noinc(bar);
 }
 
 // ---------------------------------------------------------- AppendDecode ----
@@ -359,12 +363,12 @@ __device__ __forceinline__ void consume_eager(const StepArgs& a, const Layout& L
 
 // ----------------------------------------------------------------- kernel ---
 template <int OP, int DK, int DV, int MODE>
-__global__ void __launch_bounds__(PIPE_THREADS, 1) pipe_kernel(const __grid_constant__ StepArgs a) {
+__global__ void __launch_bounds__(PIPE_THREADS_MAX, 1) pipe_kernel(const __grid_constant__ StepArgs a) {
   extern __shared__ __align__(1024) unsigned char smem[];
   constexpr uint32_t TILE_BYTES = BV * DK * 4;
   const Layout Lay = make_layout(OP, a.M, DK, DV);
-  const int NS = a.ns, NA = a.na, G = a.G;
-  const int R = NS / NCW;   // stages per consumer warp (ns is a multiple of NCW)
+  const int NS = a.ns, NA = a.na, G = a.G, NCWr = a.ncw;
+  const int R = NS / NCWr;   // stages per consumer warp (ns is a multiple of ncw)
   const uint32_t aux_bytes = (MODE == APPEND) ? Lay.aux_bytes : Lay.e_bytes;
   const Bars bars{smem_u32(smem), NS, NA};
   float* tiles = reinterpret_cast<float*>(smem + BAR_BYTES);
@@ -377,7 +381,7 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) pipe_kernel(const __grid_cons
       mbar_init(bars.empty(s), 1);
     }
     for (int x = 0; x < NA; ++x) {
-      mbar_init(bars.afull(x), 1);
+      mbar_init(bars.afull(x), 32);   // one arrival per producer lane
       mbar_init(bars.aempty(x), G);
     }
     fence_mbar_init();
@@ -389,9 +393,10 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) pipe_kernel(const __grid_cons
       (int)blockIdx.x < n_units ? (n_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
   const int my_tiles = my_units * G;
 
-  if (warp == NCW) {
+  if (warp == NCWr) {
     // ------------------------------------------------------------ producer
-    if (lane != 0) return;
+    // The whole warp runs this loop (uniform control flow); lane 0 also
+    // issues the tile bulk copies.
     const uint64_t pol = policy_evict_first();
     bool primary_done = (MODE != APPEND);
     int pending_from = 0;   // units [pending_from, ka) still need their coefficient copy
@@ -405,58 +410,73 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) pipe_kernel(const __grid_cons
         primary_done = true;
         for (int u = pending_from; u < ka; ++u) {
           const UnitPos p = unit_pos(a, (int)blockIdx.x + u * (int)gridDim.x);
-          issue_coef<OP, DK, DV>(a, Lay, p, auxm + (size_t)(u % NA) * aux_bytes,
-                                 bars.afull(u % NA));
+          issue_coef_and_arrive<OP, DK, DV>(a, Lay, p, auxm + (size_t)(u % NA) * aux_bytes,
+                                            bars.afull(u % NA), lane);
         }
         pending_from = ka;
       }
       if (kt == ka) {
         const int x = ka % NA;
-        if (!mbar_wait(bars.aempty(x), ((ka / NA) & 1) ^ 1, a.status, DEV_TIMEOUT_EMPTY)) {
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(bars.aempty(x), ((ka / NA) & 1) ^ 1, a.status, DEV_TIMEOUT_EMPTY))) {
           ok = false;
           break;
         }
         const UnitPos p = unit_pos(a, (int)blockIdx.x + ka * (int)gridDim.x);
-        issue_aux<OP, DK, DV, MODE>(a, Lay, p, auxm + (size_t)x * aux_bytes, bars.afull(x),
-                                    primary_done);
+        unsigned char* ax = auxm + (size_t)x * aux_bytes;
+        issue_aux<OP, DK, DV, MODE>(a, Lay, p, ax, lane);
+        if constexpr (MODE == APPEND) {
+          if (primary_done) {
+            issue_coef_and_arrive<OP, DK, DV>(a, Lay, p, ax, bars.afull(x), lane);
+            pending_from = ka + 1;
+          }
+        } else {
+          cp_async_arrive_noinc(bars.afull(x));
+        }
         ++ka;
       }
-      const int s = stage_of(ti, R);
-      if (!mbar_wait(bars.empty(s), stage_parity(ti, R) ^ 1u, a.status, DEV_TIMEOUT_EMPTY)) {
+      const int s = stage_of(ti, R, NCWr);
+      if (!__all_sync(0xffffffffu, mbar_wait(bars.empty(s), stage_parity(ti, R, NCWr) ^ 1u,
+                                              a.status, DEV_TIMEOUT_EMPTY))) {
         ok = false;
         break;
       }
-      const UnitPos p = unit_pos(a, (int)blockIdx.x + kt * (int)gridDim.x);
-      const int vt = p.grp * G + (ti - kt * G);
-      const int base = (MODE == APPEND) ? a.items[p.row].base : a.items[p.row].slot;
-      const float* src = a.Sbar + (((size_t)base * a.H + p.h) * DV + vt * BV) * DK;
-      mbar_arrive_expect_tx(bars.full(s), TILE_BYTES);
-      bulk_g2s_hint(smem_u32(tiles + (size_t)s * BV * DK), src, TILE_BYTES, bars.full(s), pol);
+      if (lane == 0) {
+        const UnitPos p = unit_pos(a, (int)blockIdx.x + kt * (int)gridDim.x);
+        const int vt = p.grp * G + (ti - kt * G);
+        const int base = (MODE == APPEND) ? a.items[p.row].base : a.items[p.row].slot;
+        const float* src = a.Sbar + (((size_t)base * a.H + p.h) * DV + vt * BV) * DK;
+        mbar_arrive_expect_tx(bars.full(s), TILE_BYTES);
+        bulk_g2s_hint(smem_u32(tiles + (size_t)s * BV * DK), src, TILE_BYTES, bars.full(s), pol);
+      }
+      __syncwarp();
       ++ti;
     }
     if (ok && !primary_done) {
       pdl_wait_primary();
       for (int u = pending_from; u < ka; ++u) {
         const UnitPos p = unit_pos(a, (int)blockIdx.x + u * (int)gridDim.x);
-        issue_coef<OP, DK, DV>(a, Lay, p, auxm + (size_t)(u % NA) * aux_bytes,
-                               bars.afull(u % NA));
+        issue_coef_and_arrive<OP, DK, DV>(a, Lay, p, auxm + (size_t)(u % NA) * aux_bytes,
+                                          bars.afull(u % NA), lane);
       }
     }
     if (!ok) {
       // an error was recorded: let the copies already in flight land before exiting
       if (!primary_done) pdl_wait_primary();
-      for (int t = ti - NS > 0 ? ti - NS : 0; t < ti; ++t)
-        mbar_drain(bars.full(stage_of(t, R)), stage_parity(t, R));
+      if (lane == 0)
+        for (int t = ti - NS > 0 ? ti - NS : 0; t < ti; ++t)
+          mbar_drain(bars.full(stage_of(t, R, NCWr)), stage_parity(t, R, NCWr));
     }
+    cp_async_wait_all();
     return;
   }
 
   // -------------------------------------------------------------- consumers
-  for (int i = warp; i < my_tiles; i += NCW) {
+  for (int i = warp; i < my_tiles; i += NCWr) {
     const int kk = i / G;
     const UnitPos p = unit_pos(a, (int)blockIdx.x + kk * (int)gridDim.x);
     const int vt = p.grp * G + (i - kk * G);
-    const int x = kk % NA, s = stage_of(i, R);
+    const int x = kk % NA, s = stage_of(i, R, NCWr);
     float g_s = 0.f, beta_s = 0.f;
     if constexpr (MODE == EAGER) {
       if (OP == GDN) g_s = a.g[p.sh];
@@ -465,7 +485,7 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) pipe_kernel(const __grid_cons
     // The tile first: it is issued after its unit's aux copies, so once it has
     // landed the aux barrier is in this unit's phase and the parity test below
     // is unambiguous.
-    bool ok = mbar_wait(bars.full(s), stage_parity(i, R), a.status, DEV_TIMEOUT_TILE);
+    bool ok = mbar_wait(bars.full(s), stage_parity(i, R, NCWr), a.status, DEV_TIMEOUT_TILE);
     ok = ok && mbar_wait(bars.afull(x), (kk / NA) & 1, a.status, DEV_TIMEOUT_AUX);
     if (!__all_sync(0xffffffffu, ok)) break;
     const float* T = tiles + (size_t)s * BV * DK;

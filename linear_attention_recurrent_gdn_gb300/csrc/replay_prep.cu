@@ -68,12 +68,19 @@ replay_prep_kernel(const __grid_constant__ StepArgs a) {
 
   float p1[NE], p2[NE];                               // per-entry partial dot products
   if constexpr (OP == GDN) {
+    // the scalars a lane needs are loaded before any arithmetic, so their
+    // latency overlaps the key-log row loads
+    const float* Lrow = a.Llog + lh * Mcap;
+    const float g_t = a.g[sh];
+    const float beta_t = a.beta[sh];
+    const float L_prev = n > 0 ? Lrow[n - 1] : 0.f;
+    const bool writer = entry_writer && lane_entry < n;
+    const float L_j = writer ? Lrow[lane_entry] : 0.f;
     float kq = 0.f;
 #pragma unroll
     for (int c = 0; c < VEC; ++c) kq += kv[c] * qv[c];
     kq = warp_sum(kq);
-    const float* Lrow = a.Llog + lh * Mcap;
-    const float Lt = (n > 0 ? Lrow[n - 1] : 0.f) + a.g[sh];
+    const float Lt = L_prev + g_t;
 #pragma unroll
     for (int j = 0; j < NE; ++j) {
       float x = 0.f, y = 0.f;
@@ -91,8 +98,8 @@ replay_prep_kernel(const __grid_constant__ StepArgs a) {
     }
     const float dkk = reduce_entries<NE>(p1, lane);
     const float dkq = reduce_entries<NE>(p2, lane);
-    if (entry_writer && lane_entry < n) {
-      const float wj = expf(Lt - Lrow[lane_entry]);
+    if (writer) {
+      const float wj = expf(Lt - L_j);
       cf[HDR + lane_entry] = wj * dkk;
       cf[HDR + Mcap4 + lane_entry] = wj * dkq;
       if (merge) cf[Lay.P0 + lane_entry] = wj;
@@ -100,7 +107,7 @@ replay_prep_kernel(const __grid_constant__ StepArgs a) {
     if (lane == 0) {
       cf[0] = expf(Lt);
       cf[1] = kq;
-      cf[2] = a.beta[sh];
+      cf[2] = beta_t;
       if (merge) cf[Lay.P0 + n] = 1.f;
       if (!merge) a.Llog[lh * Mcap + n] = Lt;
     }
