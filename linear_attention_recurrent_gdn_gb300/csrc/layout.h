@@ -65,10 +65,9 @@ DL_HD inline Layout make_layout(int op, int M, int dk, int dv) {
 }
 
 // Shape of the pipelined kernels for one launch: `cps` CTAs per SM, each with
-// `ncw` consumer warps owning `ns / ncw` tile stages apiece and `na` aux slots.
-// Bulk-copy issue cost is per copy, so tiles stay one 16 KiB (d_k = 128) copy
-// and the number of copies in flight per SM is raised with two CTAs per SM
-// where the shared memory allows.  Returns ns = 0 when nothing fits.
+// `ncw` consumer warps owning `ns / ncw` tile stages apiece and `na` aux slots
+// (at least 2, so the next unit's inputs load while the current one is used).
+// Returns ns = 0 when nothing fits.
 struct PipePlan {
   int cps, ncw, ns, na;
   int smem;   // dynamic shared memory per CTA (bytes)
@@ -76,29 +75,29 @@ struct PipePlan {
 
 inline PipePlan plan_pipeline(int dk, int aux_bytes, int G, int smem_optin, int smem_per_sm) {
   const int tile = 32 * dk * 4;
-  PipePlan best{0, 0, 0, 0, 0};
-  long best_bytes = 0;
-  for (int cps = 2; cps >= 1; --cps) {
-    const int ncw = 8 / cps;
+  // Candidates in order of preference (cps, ncw, R), from read-bandwidth
+  // measurements of this pipeline shape on GB300: two CTAs per SM with one
+  // 16 KiB stage per consumer warp stream best at d_k = 128; 8 KiB tiles
+  // (d_k = 64) need more stages per warp.
+  static const int c128[][3] = {{2, 4, 1}, {2, 3, 1}, {1, 8, 1}, {1, 6, 1}, {1, 4, 1}};
+  static const int c64[][3] = {{2, 4, 3}, {2, 4, 2}, {2, 3, 2}, {1, 8, 2}, {1, 8, 1}, {1, 4, 1}};
+  const int (*cand)[3] = dk >= 128 ? c128 : c64;
+  const int ncand = dk >= 128 ? 5 : 6;
+  for (int ci = 0; ci < ncand; ++ci) {
+    const int cps = cand[ci][0], ncw = cand[ci][1], R = cand[ci][2];
     const int per_cta = smem_per_sm / cps - 1024;     // 1 KiB per CTA is reserved
     const int budget = (per_cta < smem_optin ? per_cta : smem_optin) - 1024 - 1024;
-    for (int R = 1; R <= 3; ++R) {
-      const int ns = ncw * R;
-      int na = (ns + G - 1) / G + 1;
-      if (na > 16) na = 16;
-      long need = (long)ns * tile + (long)na * aux_bytes;
-      while (need > budget && na > 2) {
-        --na;
-        need = (long)ns * tile + (long)na * aux_bytes;
-      }
-      const long in_flight = (long)cps * ns * tile;
-      if (need <= budget && in_flight > best_bytes) {
-        best_bytes = in_flight;
-        best = PipePlan{cps, ncw, ns, na, (int)(1024 + need)};
-      }
+    const int ns = ncw * R;
+    int na = (ns + G - 1) / G + 1;
+    if (na > 16) na = 16;
+    long need = (long)ns * tile + (long)na * aux_bytes;
+    while (need > budget && na > 2) {
+      --na;
+      need = (long)ns * tile + (long)na * aux_bytes;
     }
+    if (need <= budget) return PipePlan{cps, ncw, ns, na, (int)(1024 + need)};
   }
-  return best;
+  return PipePlan{0, 0, 0, 0, 0};
 }
 
 }  // namespace dl
