@@ -126,9 +126,18 @@ void free_all(dl_ctx* c) {
   c->table = nullptr;
 }
 
+// DL_PIPE_SHAPE="cps,ncw,R" overrides the shape choice (a tuning knob for
+// measurements; shapes that do not fit are ignored).
+const int* shape_override() {
+  static int v[3];
+  const char* e = getenv("DL_PIPE_SHAPE");
+  if (!e || sscanf(e, "%d,%d,%d", &v[0], &v[1], &v[2]) != 3) return nullptr;
+  return v;
+}
+
 dl::PipePlan pipe_shape(const dl_ctx* c, int G, bool append) {
   return dl::plan_pipeline(c->cfg.d_k, append ? c->L.aux_bytes : c->L.e_bytes, G, c->smem_optin,
-                           c->smem_per_sm);
+                           c->smem_per_sm, shape_override());
 }
 
 bool record(dl_ctx* c, int kind, cudaEvent_t* ev) {
@@ -238,6 +247,7 @@ dl_status run_step(dl_ctx* c, const int32_t* slots, int32_t n, const void* q, co
     a.ns = ps.ns;
     a.na = ps.na;
     a.ncw = ps.ncw;
+    a.tps = dl::tiles_per_stage(f.d_k, a.G);
     const long units = (long)a.rows * a.H * a.NG;
     const long slots_gpu = (long)ps.cps * c->num_sms;
     const int grid = (int)(units < slots_gpu ? units : slots_gpu);
@@ -343,12 +353,8 @@ dl_status dl_create(const dl_config* cfg, void* stream, dl_ctx** out) {
       if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
     }
     if (e != cudaSuccess) { rc = cuda_err(c, e, "context initialisation"); break; }
-    size_t smem = 0;
-    for (int G = 1; G <= 4; G *= 2) {
-      const dl::PipePlan a = pipe_shape(c, G, true), b = pipe_shape(c, G, false);
-      if ((size_t)a.smem > smem) smem = a.smem;
-      if ((size_t)b.smem > smem) smem = b.smem;
-    }
+    // allow any shape the planner may pick (its budget never exceeds the opt-in limit)
+    const size_t smem = (size_t)c->smem_optin;
     e = dl::configure_append_decode(f.op, f.d_k, smem);
     if (e == cudaSuccess) e = dl::configure_eager_step(f.op, f.d_k, smem);
     if (e != cudaSuccess) { rc = cuda_err(c, e, "kernel attribute"); break; }

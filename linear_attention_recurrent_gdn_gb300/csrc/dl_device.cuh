@@ -55,6 +55,7 @@ struct StepArgs {
   int32_t G, NG;         // value tiles per work unit, units per slot-head
   int32_t ns, na;        // pipeline stages (tiles), aux slots
   int32_t ncw;           // consumer warps per CTA (block = (ncw + 1) warps)
+  int32_t tps;           // value tiles per stage (one bulk copy): 1, or 2 for d_k = 64
   int32_t aux_bytes;     // bytes of one aux slot
   int32_t out_bf16;
   float scale;

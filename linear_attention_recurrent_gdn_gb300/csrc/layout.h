@@ -73,29 +73,51 @@ struct PipePlan {
   int smem;   // dynamic shared memory per CTA (bytes)
 };
 
-inline PipePlan plan_pipeline(int dk, int aux_bytes, int G, int smem_optin, int smem_per_sm) {
-  const int tile = 32 * dk * 4;
+// Fit one candidate shape (cps CTAs per SM, ncw consumer warps, R stages per
+// warp) into the shared-memory budget; ns = 0 if it does not fit.
+inline PipePlan fit_pipeline(int cps, int ncw, int R, int dk, int aux_bytes, int G, int smem_optin,
+                             int smem_per_sm, int tps = 1) {
+  const int tile = 32 * dk * 4 * tps;   // bytes of one stage
+  const int per_cta = smem_per_sm / cps - 1024;     // 1 KiB per CTA is reserved
+  const int budget = (per_cta < smem_optin ? per_cta : smem_optin) - 1024 - 1024;
+  const int ns = ncw * R;
+  const int ipu = G / tps;                         // stage items per unit
+  int na = (ns + ipu - 1) / ipu + 1;
+  if (na > 16) na = 16;
+  long need = (long)ns * tile + (long)na * aux_bytes;
+  while (need > budget && na > 2) {
+    --na;
+    need = (long)ns * tile + (long)na * aux_bytes;
+  }
+  if (ncw < 1 || ncw > 8 || R < 1 || ns > 24 || need > budget) return PipePlan{0, 0, 0, 0, 0};
+  return PipePlan{cps, ncw, ns, na, (int)(1024 + need)};
+}
+
+// Stages hold one 16 KiB bulk copy: one value tile at d_k = 128, two at d_k = 64
+// (when the unit has both tiles), because each bulk copy has a fixed issue cost.
+inline int tiles_per_stage(int dk, int G) { return (dk == 64 && G % 2 == 0) ? 2 : 1; }
+
+inline PipePlan plan_pipeline(int dk, int aux_bytes, int G, int smem_optin, int smem_per_sm,
+                              const int* force = nullptr) {
+  const int tps = tiles_per_stage(dk, G);
+  if (force) {   // tuning override: {cps, ncw, R}
+    const PipePlan p = fit_pipeline(force[0], force[1], force[2], dk, aux_bytes, G, smem_optin,
+                                    smem_per_sm, tps);
+    if (p.ns > 0) return p;
+  }
   // Candidates in order of preference (cps, ncw, R), from read-bandwidth
   // measurements of this pipeline shape on GB300: two CTAs per SM with one
-  // 16 KiB stage per consumer warp stream best at d_k = 128; 8 KiB tiles
-  // (d_k = 64) need more stages per warp.
-  static const int c128[][3] = {{2, 4, 1}, {2, 3, 1}, {1, 8, 1}, {1, 6, 1}, {1, 4, 1}};
-  static const int c64[][3] = {{2, 4, 3}, {2, 4, 2}, {2, 3, 2}, {1, 8, 2}, {1, 8, 1}, {1, 4, 1}};
-  const int (*cand)[3] = dk >= 128 ? c128 : c64;
-  const int ncand = dk >= 128 ? 5 : 6;
+  // 16 KiB stage per consumer warp stream best; 8 KiB stages (d_k = 64 with
+  // one tile per unit) need more stages per warp.
+  static const int c16k[][3] = {{2, 4, 1}, {2, 3, 1}, {1, 8, 1}, {1, 6, 1}, {1, 4, 1}};
+  static const int c8k[][3] = {{2, 4, 3}, {2, 4, 2}, {2, 3, 2}, {1, 8, 2}, {1, 8, 1}, {1, 4, 1}};
+  const bool big = 32 * dk * 4 * tps >= 16384;
+  const int (*cand)[3] = big ? c16k : c8k;
+  const int ncand = big ? 5 : 6;
   for (int ci = 0; ci < ncand; ++ci) {
-    const int cps = cand[ci][0], ncw = cand[ci][1], R = cand[ci][2];
-    const int per_cta = smem_per_sm / cps - 1024;     // 1 KiB per CTA is reserved
-    const int budget = (per_cta < smem_optin ? per_cta : smem_optin) - 1024 - 1024;
-    const int ns = ncw * R;
-    int na = (ns + G - 1) / G + 1;
-    if (na > 16) na = 16;
-    long need = (long)ns * tile + (long)na * aux_bytes;
-    while (need > budget && na > 2) {
-      --na;
-      need = (long)ns * tile + (long)na * aux_bytes;
-    }
-    if (need <= budget) return PipePlan{cps, ncw, ns, na, (int)(1024 + need)};
+    const PipePlan p = fit_pipeline(cand[ci][0], cand[ci][1], cand[ci][2], dk, aux_bytes, G,
+                                    smem_optin, smem_per_sm, tps);
+    if (p.ns > 0) return p;
   }
   return PipePlan{0, 0, 0, 0, 0};
 }

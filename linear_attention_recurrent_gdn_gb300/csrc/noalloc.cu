@@ -185,6 +185,7 @@ extern "C" dl_status dl_step_noalloc(const dl_config* cfg, const dl_state_view* 
   a.ns = sh.ns;
   a.na = sh.na;
   a.ncw = sh.ncw;
+  a.tps = dl::tiles_per_stage(f.d_k, a.G);
   const long units = n_sh * a.NG;
   const long slots_gpu = (long)sh.cps * d.num_sms;
   const int grid = (int)(units < slots_gpu ? units : slots_gpu);

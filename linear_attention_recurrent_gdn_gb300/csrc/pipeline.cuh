@@ -146,7 +146,8 @@ __device__ __forceinline__ void issue_coef_and_arrive(const StepArgs& a, const L
 template <int OP, int DK, int DV>
 __device__ __forceinline__ bool consume_append(const StepArgs& a, const Layout& Lay,
                                                const UnitPos& p, int vt, const float* T,
-                                               unsigned char* ax, int lane, uint32_t empty_bar) {
+                                               unsigned char* ax, int lane, uint32_t empty_bar,
+                                               bool may_release) {
   constexpr int VEC = DK / 32;
   constexpr bool DELTA = OP != RWKV6;
   const StepItem it = a.items[p.row];
@@ -182,7 +183,7 @@ __device__ __forceinline__ bool consume_append(const StepArgs& a, const Layout& 
     pa[r] = x;
     pb[r] = y;
   }
-  if (!merge) {
+  if (!merge && may_release) {
     __syncwarp();
     if (lane == 0) mbar_arrive(empty_bar);
   }
@@ -219,7 +220,7 @@ __device__ __forceinline__ bool consume_append(const StepArgs& a, const Layout& 
     o += cf[3] * bf16f(V[n * DV + col]);
     store_out(a, oidx, a.scale * o);
   }
-  if (!merge) return true;
+  if (!merge) return may_release;
 
   // merge: S̄[slot] rows = D ⊙ S̄[base] rows + Σ_{j<=n} a_j[row] K̃_j
   float D[VEC];
@@ -367,12 +368,14 @@ __global__ void __launch_bounds__(PIPE_THREADS_MAX, 1) pipe_kernel(const __grid_
   extern __shared__ __align__(1024) unsigned char smem[];
   constexpr uint32_t TILE_BYTES = BV * DK * 4;
   const Layout Lay = make_layout(OP, a.M, DK, DV);
-  const int NS = a.ns, NA = a.na, G = a.G, NCWr = a.ncw;
+  const int NS = a.ns, NA = a.na, G = a.G, NCWr = a.ncw, TPS = a.tps;
+  const int IPU = G / TPS;                       // stage items per unit
+  const uint32_t STAGE_BYTES = TILE_BYTES * TPS; // one bulk copy per stage item
   const int R = NS / NCWr;   // stages per consumer warp (ns is a multiple of ncw)
   const uint32_t aux_bytes = (MODE == APPEND) ? Lay.aux_bytes : Lay.e_bytes;
   const Bars bars{smem_u32(smem), NS, NA};
   float* tiles = reinterpret_cast<float*>(smem + BAR_BYTES);
-  unsigned char* auxm = smem + BAR_BYTES + (size_t)NS * TILE_BYTES;
+  unsigned char* auxm = smem + BAR_BYTES + (size_t)NS * STAGE_BYTES;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -382,7 +385,7 @@ __global__ void __launch_bounds__(PIPE_THREADS_MAX, 1) pipe_kernel(const __grid_
     }
     for (int x = 0; x < NA; ++x) {
       mbar_init(bars.afull(x), 32);   // one arrival per producer lane
-      mbar_init(bars.aempty(x), G);
+      mbar_init(bars.aempty(x), IPU);
     }
     fence_mbar_init();
   }
@@ -391,7 +394,7 @@ __global__ void __launch_bounds__(PIPE_THREADS_MAX, 1) pipe_kernel(const __grid_
   const int n_units = a.rows * a.H * a.NG;
   const int my_units =
       (int)blockIdx.x < n_units ? (n_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-  const int my_tiles = my_units * G;
+  const int my_tiles = my_units * IPU;   // stage items of this CTA
 
   if (warp == NCWr) {
     // ------------------------------------------------------------ producer
@@ -403,7 +406,7 @@ __global__ void __launch_bounds__(PIPE_THREADS_MAX, 1) pipe_kernel(const __grid_
     int ti = 0, ka = 0;
     bool ok = true;
     while (ti < my_tiles) {
-      const int kt = ti / G;
+      const int kt = ti / IPU;
       if (!primary_done && (ti >= NS || (kt == ka && ka >= NA))) {
         // the next wait needs consumers to make progress, and they need coefficients
         pdl_wait_primary();
@@ -443,11 +446,12 @@ __global__ void __launch_bounds__(PIPE_THREADS_MAX, 1) pipe_kernel(const __grid_
       }
       if (lane == 0) {
         const UnitPos p = unit_pos(a, (int)blockIdx.x + kt * (int)gridDim.x);
-        const int vt = p.grp * G + (ti - kt * G);
+        const int vt = p.grp * G + (ti - kt * IPU) * TPS;   // first value tile of the item
         const int base = (MODE == APPEND) ? a.items[p.row].base : a.items[p.row].slot;
         const float* src = a.Sbar + (((size_t)base * a.H + p.h) * DV + vt * BV) * DK;
-        mbar_arrive_expect_tx(bars.full(s), TILE_BYTES);
-        bulk_g2s_hint(smem_u32(tiles + (size_t)s * BV * DK), src, TILE_BYTES, bars.full(s), pol);
+        mbar_arrive_expect_tx(bars.full(s), STAGE_BYTES);
+        bulk_g2s_hint(smem_u32(tiles + (size_t)s * TPS * BV * DK), src, STAGE_BYTES, bars.full(s),
+                      pol);
       }
       __syncwarp();
       ++ti;
@@ -473,9 +477,9 @@ __global__ void __launch_bounds__(PIPE_THREADS_MAX, 1) pipe_kernel(const __grid_
 
   // -------------------------------------------------------------- consumers
   for (int i = warp; i < my_tiles; i += NCWr) {
-    const int kk = i / G;
+    const int kk = i / IPU;
     const UnitPos p = unit_pos(a, (int)blockIdx.x + kk * (int)gridDim.x);
-    const int vt = p.grp * G + (i - kk * G);
+    const int vt0 = p.grp * G + (i - kk * IPU) * TPS;
     const int x = kk % NA, s = stage_of(i, R, NCWr);
     float g_s = 0.f, beta_s = 0.f;
     if constexpr (MODE == EAGER) {
@@ -488,12 +492,15 @@ __global__ void __launch_bounds__(PIPE_THREADS_MAX, 1) pipe_kernel(const __grid_
     bool ok = mbar_wait(bars.full(s), stage_parity(i, R, NCWr), a.status, DEV_TIMEOUT_TILE);
     ok = ok && mbar_wait(bars.afull(x), (kk / NA) & 1, a.status, DEV_TIMEOUT_AUX);
     if (!__all_sync(0xffffffffu, ok)) break;
-    const float* T = tiles + (size_t)s * BV * DK;
     unsigned char* ax = auxm + (size_t)x * aux_bytes;
     bool released = false;
-    if constexpr (MODE == APPEND)
-      released = consume_append<OP, DK, DV>(a, Lay, p, vt, T, ax, lane, bars.empty(s));
-    else consume_eager<OP, DK, DV>(a, Lay, p, vt, T, ax, lane, g_s, beta_s);
+    for (int t = 0; t < TPS; ++t) {
+      const float* T = tiles + ((size_t)s * TPS + t) * BV * DK;
+      if constexpr (MODE == APPEND)
+        released = consume_append<OP, DK, DV>(a, Lay, p, vt0 + t, T, ax, lane, bars.empty(s),
+                                              t == TPS - 1);
+      else consume_eager<OP, DK, DV>(a, Lay, p, vt0 + t, T, ax, lane, g_s, beta_s);
+    }
     // order this warp's shared-memory writes (u_t rows of a merge) before the
     // bulk copies that will refill the slots once they are released
     fence_proxy_async_smem();

@@ -166,36 +166,50 @@ replay_prep_kernel(const __grid_constant__ StepArgs a) {
       cb = warp_sum(cb);
       if (lane == 0) cf[3] = cb;
     }
+    // entries in groups of 4: the group's key-log and log-decay rows are all
+    // requested before any of them is used (a few round trips instead of n)
 #pragma unroll
-    for (int j = 0; j < NE; ++j) {
-      float x = 0.f, y = 0.f;
-      if (j < n) {
-        float kj[VEC], lj[VEC];
-        ldvec_bf16<VEC>(kj, a.klog + (lh * Mcap + j) * DK + c0);
-        ldvec<VEC>(lj, Lbase + (size_t)j * DK + c0);
-        float kk[VEC];
+    for (int j0 = 0; j0 < NE; j0 += 4) {
+      float kj[4][VEC], lj[4][VEC];
 #pragma unroll
-        for (int c = 0; c < VEC; ++c) {
-          kk[c] = kj[c] * expf(Lc[c] - lj[c]);
-          if (OP == KDA) {
-            x += kk[c] * kv[c];
-            y += kk[c] * qv[c];
-          } else {
-            x += kk[c] * qv[c];
-          }
-        }
-        if (merge) {
-          float km[VEC];
+      for (int u = 0; u < 4; ++u) {
+        if (j0 + u < n) {
+          ldvec_bf16<VEC>(kj[u], a.klog + (lh * Mcap + j0 + u) * DK + c0);
+          ldvec<VEC>(lj[u], Lbase + (size_t)(j0 + u) * DK + c0);
+        } else {
 #pragma unroll
-          for (int c = 0; c < VEC; ++c) km[c] = kk[c] * wt[c];   // K̃_j = k_j ⊙ e^{Λ_t-Λ_j}
-          if constexpr (VEC == 4)
-            *reinterpret_cast<float4*>(Kt + (size_t)j * DK + c0) = make_float4(km[0], km[1], km[2], km[3]);
-          else
-            *reinterpret_cast<float2*>(Kt + (size_t)j * DK + c0) = make_float2(km[0], km[1]);
+          for (int c = 0; c < VEC; ++c) kj[u][c] = lj[u][c] = 0.f;
         }
       }
-      p1[j] = x;
-      p2[j] = y;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = j0 + u;
+        float x = 0.f, y = 0.f;
+        if (j < n) {
+          float kk[VEC];
+#pragma unroll
+          for (int c = 0; c < VEC; ++c) {
+            kk[c] = kj[u][c] * __expf(Lc[c] - lj[u][c]);
+            if (OP == KDA) {
+              x += kk[c] * kv[c];
+              y += kk[c] * qv[c];
+            } else {
+              x += kk[c] * qv[c];
+            }
+          }
+          if (merge) {
+            float km[VEC];
+#pragma unroll
+            for (int c = 0; c < VEC; ++c) km[c] = kk[c] * wt[c];   // K̃_j = k_j ⊙ e^{Λ_t-Λ_j}
+            if constexpr (VEC == 4)
+              *reinterpret_cast<float4*>(Kt + (size_t)j * DK + c0) = make_float4(km[0], km[1], km[2], km[3]);
+            else
+              *reinterpret_cast<float2*>(Kt + (size_t)j * DK + c0) = make_float2(km[0], km[1]);
+          }
+        }
+        p1[j] = x;
+        p2[j] = y;
+      }
     }
     const float d1 = reduce_entries<NE>(p1, lane);
     float d2 = 0.f;
