@@ -47,6 +47,33 @@ def log(*a):
     print(*a, file=sys.stderr, flush=True)
 
 
+KERNEL_SOURCES = ["pipeline.cuh", "append_decode.cu", "dl_device.cuh", "layout.h"]
+
+
+def kernel_source_hash():
+    """Hash of the AppendDecode sources; ncu traffic figures are tied to it."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, "linear_attention_recurrent_gdn_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(key):
+    """DRAM bytes per launch (read + write) that an ncu capture recorded for this
+    kernel and workload (profiles/traffic.txt), or None when the capture was
+    taken on other kernel sources than the ones built now."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src = kernel_source_hash()
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 3 and not line.startswith("#") and parts[0] == key and parts[2] == src:
+            return float(parts[1])
+    return None
+
+
 # ------------------------------------------------------------ traffic model --
 def algorithmic_bytes(op, d, M, n):
     """Algorithmic HBM bytes of one token for one slot-head with log length n
@@ -303,17 +330,19 @@ def run_ours(args):
 
     units_per_step = T * B * H                    # token·heads per rank per bench step
 
-    # ---- headline: DeltaLog at M
+    # ---- headline: DeltaLog at M (or the eager kernel with --eager)
+    if args.eager:
+        M = 1
     ctx = make_ctx(M)
     with ClockSampler(local) as clk:
-        ms = timed(ctx, args.steps, args.warmup)
+        ms = timed(ctx, args.steps, args.warmup, eager=args.eager)
     ms_max = reduce_max(dist, ms, dev)
     value = units_per_step * world / (ms_max / 1e3)
     launches = 2 * T * args.steps * ((B + 1023) // 1024)
 
     # ---- per-kernel times (instrumented pass: events around every launch)
     ctx.set_timing(True)
-    decode_run(ctx)
+    decode_run(ctx, eager=args.eager)
     kms, kcnt = ctx.get_timing()
     ctx.set_timing(False)
     n_seq = [t % M for t in range(T)]
@@ -325,6 +354,12 @@ def run_ours(args):
         wr_all += c_ * B * H
     ad_ms = kms[1] / max(kcnt[1], 1)
     rp_ms = kms[0] / max(kcnt[0], 1)
+    kernel_name = "AppendDecode"
+    if args.eager:
+        eb_, ew_ = eager_bytes(op, d)
+        ad_b, wr_all, rp_b = eb_ * B * H * T, ew_ * B * H * T, 0
+        ad_ms = kms[2] / max(kcnt[2], 1)
+        kernel_name = "EagerStep"
     ad_gbs = ad_b / T / (ad_ms * 1e-3) / 1e9
     peaks = {}
     try:
@@ -340,7 +375,8 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": w["desc"] + ", merge interval M=%d" % M,
+        "config": {"workload": w["desc"] + (", eager dense step" if args.eager
+                                            else ", merge interval M=%d" % M),
                    "op": gen.OP_NAMES[op], "B": B, "H": H, "d_k": d, "d_v": d, "tokens": T,
                    "M": M, "inputs": "bf16 q/k/v, fp32 g/beta, bf16 o",
                    "l2": "inputs larger than L2 (fp32 state %d MiB per rank)"
@@ -349,10 +385,14 @@ def run_ours(args):
         "gpu_launches": launches,
         "clocks": clk.summary(),
         "roofline": {"bound": "hbm", "achieved": ad_gbs, "peak": peak, "unit": "GB/s",
-                     "frac": ad_gbs / peak, "traffic": None,
-                     "kernel": "AppendDecode", "peak_source": peak_src + " hbm_gbs",
+                     "frac": ad_gbs / peak,
+                     "traffic": measured_traffic("%s_%s_b%d_h%d_d%d_m%d" % (
+                         "eager_step" if args.eager else "append_decode", gen.OP_NAMES[op], B, H, d,
+                         M)),
+                     "kernel": kernel_name, "peak_source": peak_src + " hbm_gbs",
                      "bytes_per_launch": ad_b / T, "ms_per_launch": ad_ms},
-        "kernels_ms_per_token": {"ReplayPrep": rp_ms, "AppendDecode": ad_ms},
+        "kernels_ms_per_token": ({"EagerStep": ad_ms} if args.eager else
+                                 {"ReplayPrep": rp_ms, "AppendDecode": ad_ms}),
         "step_gbs": step_bytes / (ms_max / T * 1e-3) / 1e9,
         "write_bytes_per_token": {"deltalog": wr_all / T,
                                   "deltalog_state_only": B * H * d * d * 4 / M},
@@ -509,6 +549,8 @@ def main():
     ap.add_argument("--B", type=int, default=0, help="override the batch (profiling runs only)")
     ap.add_argument("--tokens", type=int, default=0, help="override the token count (profiling)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--eager", action="store_true",
+                    help="time the in-house eager kernel (dense read-modify-write) instead")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

@@ -37,7 +37,7 @@ struct TimedPair {
 struct dl_ctx {
   dl_config cfg{};
   cudaStream_t stream = nullptr;
-  int device = 0, num_sms = 0, smem_optin = 0, smem_per_sm = 0;
+  int device = 0, num_sms = 0, smem_optin = 0, smem_per_sm = 0, l2_bytes = 0;
   dl_table* table = nullptr;
   dl::Layout L{};
   float* Sbar = nullptr;
@@ -248,6 +248,8 @@ dl_status run_step(dl_ctx* c, const int32_t* slots, int32_t n, const void* q, co
     a.na = ps.na;
     a.ncw = ps.ncw;
     a.tps = dl::tiles_per_stage(f.d_k, a.G);
+    // stream the state through L2 unless the whole batch's state fits in 3/4 of it
+    a.l2_stream = (double)n * f.num_heads * f.d_v * f.d_k * 4 > 0.75 * c->l2_bytes ? 1 : 0;
     const long units = (long)a.rows * a.H * a.NG;
     const long slots_gpu = (long)ps.cps * c->num_sms;
     const int grid = (int)(units < slots_gpu ? units : slots_gpu);
@@ -320,6 +322,7 @@ dl_status dl_create(const dl_config* cfg, void* stream, dl_ctx** out) {
       e = cudaDeviceGetAttribute(&c->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c->device);
     if (e == cudaSuccess)
       e = cudaDeviceGetAttribute(&c->smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, c->device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->l2_bytes, cudaDevAttrL2CacheSize, c->device);
     if (e != cudaSuccess) { rc = cuda_err(c, e, "device query"); break; }
     const size_t S = f.num_slots, H = f.num_heads, dk = f.d_k, dv = f.d_v, Mcap = c->L.Mcap;
     const size_t esa = (f.op == DL_RWKV6) ? 2 : 4;

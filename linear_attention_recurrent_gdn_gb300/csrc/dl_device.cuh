@@ -56,6 +56,7 @@ struct StepArgs {
   int32_t ns, na;        // pipeline stages (tiles), aux slots
   int32_t ncw;           // consumer warps per CTA (block = (ncw + 1) warps)
   int32_t tps;           // value tiles per stage (one bulk copy): 1, or 2 for d_k = 64
+  int32_t l2_stream;     // 1: read S̄ with an L2 evict-first policy (state larger than L2 can keep)
   int32_t aux_bytes;     // bytes of one aux slot
   int32_t out_bf16;
   float scale;
@@ -165,10 +166,16 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
-// Same with an L2 eviction-priority policy (evict_first for data read once).
+// Same with an L2 eviction-priority policy: evict_first for a state that is
+// streamed through once per step, evict_normal for one small enough to stay in L2.
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
 __device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void* src, uint32_t bytes,

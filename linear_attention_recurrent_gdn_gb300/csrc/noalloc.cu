@@ -56,6 +56,7 @@ struct DeviceSetup {
   int num_sms = 0;
   int smem_optin = 0;
   int smem_per_sm = 0;
+  int l2_bytes = 0;
   size_t smem_configured[3][2] = {{0, 0}, {0, 0}, {0, 0}};   // per (op, d_k 64/128)
 };
 
@@ -137,7 +138,8 @@ extern "C" dl_status dl_step_noalloc(const dl_config* cfg, const dl_state_view* 
           cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
               cudaSuccess ||
           cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
-              cudaSuccess)
+              cudaSuccess ||
+          cudaDeviceGetAttribute(&d.l2_bytes, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
         return fail(DL_ECUDA, "device query failed");
       d.ready = true;
     }
@@ -186,6 +188,7 @@ extern "C" dl_status dl_step_noalloc(const dl_config* cfg, const dl_state_view* 
   a.na = sh.na;
   a.ncw = sh.ncw;
   a.tps = dl::tiles_per_stage(f.d_k, a.G);
+  a.l2_stream = (double)n * f.num_heads * f.d_v * f.d_k * 4 > 0.75 * d.l2_bytes ? 1 : 0;
   const long units = n_sh * a.NG;
   const long slots_gpu = (long)sh.cps * d.num_sms;
   const int grid = (int)(units < slots_gpu ? units : slots_gpu);

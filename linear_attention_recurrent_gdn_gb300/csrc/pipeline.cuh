@@ -400,7 +400,7 @@ __global__ void __launch_bounds__(PIPE_THREADS_MAX, 1) pipe_kernel(const __grid_
     // ------------------------------------------------------------ producer
     // The whole warp runs this loop (uniform control flow); lane 0 also
     // issues the tile bulk copies.
-    const uint64_t pol = policy_evict_first();
+    const uint64_t pol = a.l2_stream ? policy_evict_first() : policy_evict_normal();
     bool primary_done = (MODE != APPEND);
     int pending_from = 0;   // units [pending_from, ka) still need their coefficient copy
     int ti = 0, ka = 0;
