@@ -300,8 +300,11 @@ def run_ours(args):
     torch.cuda.synchronize()
     log("inputs generated in %.1fs" % (time.time() - t0))
 
+    staging = dl.STAGE_FUSED if args.staging == "fused" else dl.STAGE_KERNELS
+
     def make_ctx(m):
-        c = dl.DeltaLog(op, B, H, d, d, m, out_bf16=True, stream=stream.cuda_stream)
+        c = dl.DeltaLog(op, B, H, d, d, m, out_bf16=True, stream=stream.cuda_stream,
+                        staging=staging)
         c.set_state(slots, S0)
         if bonus is not None:
             c.set_bonus(bonus)
@@ -378,7 +381,7 @@ def run_ours(args):
         "config": {"workload": w["desc"] + (", eager dense step" if args.eager
                                             else ", merge interval M=%d" % M),
                    "op": gen.OP_NAMES[op], "B": B, "H": H, "d_k": d, "d_v": d, "tokens": T,
-                   "M": M, "inputs": "bf16 q/k/v, fp32 g/beta, bf16 o",
+                   "M": M, "staging": args.staging, "inputs": "bf16 q/k/v, fp32 g/beta, bf16 o",
                    "l2": "inputs larger than L2 (fp32 state %d MiB per rank)"
                          % (B * H * d * d * 4 >> 20),
                    "parallelism": "replicas/batch shards x%d" % world},
@@ -549,6 +552,8 @@ def main():
     ap.add_argument("--B", type=int, default=0, help="override the batch (profiling runs only)")
     ap.add_argument("--tokens", type=int, default=0, help="override the token count (profiling)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--staging", default="fused", choices=["fused", "kernels"],
+                    help="ReplayPrep as a warp role of AppendDecode (fused) or its own kernel")
     ap.add_argument("--eager", action="store_true",
                     help="time the in-house eager kernel (dense read-modify-write) instead")
     args = ap.parse_args()

@@ -71,7 +71,7 @@
 extern "C" {
 #endif
 
-#define DL_ABI_VERSION 1
+#define DL_ABI_VERSION 2
 
 typedef enum dl_status {
     DL_OK = 0,
@@ -94,7 +94,17 @@ typedef struct dl_config {
     int32_t merge_interval;  /* M in [1, 32]; 1 = eager (every step merges)             */
     int32_t out_bf16;        /* 1: o is bf16; 0: o is fp32                              */
     float scale;             /* output scale (1.0 for the decode workloads)             */
+    int32_t staging;         /* DL_STAGE_FUSED (0, default) or DL_STAGE_KERNELS (1)     */
 } dl_config;
+
+/* How a dl_step runs the two stages of the DeltaLog page's "Kernel
+ * implementation" section.  FUSED: one kernel; a warp of each AppendDecode CTA
+ * is the ReplayPrep stage and computes each slot-head's coefficients from the
+ * unit's inputs in shared memory.  KERNELS: a ReplayPrep kernel writes the
+ * coefficient blocks to HBM scratch, then AppendDecode (launched as its
+ * programmatic dependent) reads them.  Both compute the same values. */
+#define DL_STAGE_FUSED 0
+#define DL_STAGE_KERNELS 1
 
 /* ------------------------------------------------------------------------ */
 /* Host bookkeeping (no GPU needed).  This is the slot table every context   */
@@ -161,8 +171,9 @@ dl_status dl_fork(dl_ctx *ctx, int32_t src, const int32_t *dsts, int32_t n);
  *   g                    [n, H] fp32 (GDN) or [n, H, d_k] fp32 (KDA, RWKV6): log-decay
  *   beta                 [n, H] fp32 (GDN, KDA); ignored for RWKV6 (may be NULL)
  *   o                    [n, H, d_v] bf16 or fp32 (dl_config.out_bf16), written
- * Launches ReplayPrep then AppendDecode (merge fused for the slots whose log
- * is full).  A frozen slot in the list returns DL_EBUSY. */
+ * Runs the ReplayPrep and AppendDecode stages (dl_config.staging; the merge is
+ * fused for the slots whose log is full).  A frozen slot in the list returns
+ * DL_EBUSY. */
 dl_status dl_step(dl_ctx *ctx, const int32_t *slots, int32_t n,
                   const void *q, const void *k, const void *v,
                   const float *g, const float *beta, void *o);
@@ -280,7 +291,9 @@ typedef struct dl_state_view {
  * device does a one-time set-up with that device current (it looks up the
  * scratch's device address and sets kernel shared-memory limits); make it
  * before any stream capture.  If errbuf != NULL it receives a one-line reason
- * for a non-DL_OK status (at most errlen bytes, NUL-terminated). */
+ * for a non-DL_OK status (at most errlen bytes, NUL-terminated).  The step
+ * always runs as two kernels (the scratch holds the coefficient blocks that
+ * pass between them); cfg->staging is not used. */
 dl_status dl_step_noalloc(const dl_config *cfg, const dl_state_view *st,
                           const int32_t *plan, int32_t n,
                           const void *q, const void *k, const void *v,

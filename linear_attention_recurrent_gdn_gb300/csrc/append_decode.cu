@@ -4,39 +4,55 @@
 
 namespace dl {
 
-template <int OP, int DK>
+template <int OP, int DK, int MODE>
 static cudaError_t launch_ad(const StepArgs& a, int grid, size_t smem, bool pdl, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3((a.ncw + 1) * 32);
+  cfg.blockDim = dim3((a.ncw + (MODE == FUSED ? 2 : 1)) * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, pipe_kernel<OP, DK, DK, APPEND>, a);
+  cfg.numAttrs = (pdl && MODE == APPEND) ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, pipe_kernel<OP, DK, DK, MODE>, a);
 }
 
 cudaError_t launch_append_decode(int op, int dk, const StepArgs& a, int grid, size_t smem,
                                  bool pdl, cudaStream_t s) {
   if (a.rows <= 0) return cudaSuccess;
   if (dk == 64) {
-    if (op == GDN) return launch_ad<GDN, 64>(a, grid, smem, pdl, s);
-    if (op == KDA) return launch_ad<KDA, 64>(a, grid, smem, pdl, s);
-    return launch_ad<RWKV6, 64>(a, grid, smem, pdl, s);
+    if (op == GDN) return launch_ad<GDN, 64, APPEND>(a, grid, smem, pdl, s);
+    if (op == KDA) return launch_ad<KDA, 64, APPEND>(a, grid, smem, pdl, s);
+    return launch_ad<RWKV6, 64, APPEND>(a, grid, smem, pdl, s);
   }
-  if (op == GDN) return launch_ad<GDN, 128>(a, grid, smem, pdl, s);
-  if (op == KDA) return launch_ad<KDA, 128>(a, grid, smem, pdl, s);
-  return launch_ad<RWKV6, 128>(a, grid, smem, pdl, s);
+  if (op == GDN) return launch_ad<GDN, 128, APPEND>(a, grid, smem, pdl, s);
+  if (op == KDA) return launch_ad<KDA, 128, APPEND>(a, grid, smem, pdl, s);
+  return launch_ad<RWKV6, 128, APPEND>(a, grid, smem, pdl, s);
+}
+
+cudaError_t launch_append_decode_fused(int op, int dk, const StepArgs& a, int grid, size_t smem,
+                                       cudaStream_t s) {
+  if (a.rows <= 0) return cudaSuccess;
+  if (dk == 64) {
+    if (op == GDN) return launch_ad<GDN, 64, FUSED>(a, grid, smem, false, s);
+    if (op == KDA) return launch_ad<KDA, 64, FUSED>(a, grid, smem, false, s);
+    return launch_ad<RWKV6, 64, FUSED>(a, grid, smem, false, s);
+  }
+  if (op == GDN) return launch_ad<GDN, 128, FUSED>(a, grid, smem, false, s);
+  if (op == KDA) return launch_ad<KDA, 128, FUSED>(a, grid, smem, false, s);
+  return launch_ad<RWKV6, 128, FUSED>(a, grid, smem, false, s);
 }
 
 // The attribute must be set on the kernel instance this translation unit
 // launches (each translation unit registers its own copy of a template kernel).
 template <int OP, int DK>
 static cudaError_t cfg_one(size_t smem) {
-  return cudaFuncSetAttribute(pipe_kernel<OP, DK, DK, APPEND>,
+  cudaError_t e = cudaFuncSetAttribute(pipe_kernel<OP, DK, DK, APPEND>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(pipe_kernel<OP, DK, DK, FUSED>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
 }
 

@@ -135,9 +135,11 @@ const int* shape_override() {
   return v;
 }
 
-dl::PipePlan pipe_shape(const dl_ctx* c, int G, bool append) {
-  return dl::plan_pipeline(c->cfg.d_k, append ? c->L.aux_bytes : c->L.e_bytes, G, c->smem_optin,
-                           c->smem_per_sm, shape_override());
+enum class Kern { Append, Fused, Eager };
+
+dl::PipePlan pipe_shape(const dl_ctx* c, int G, Kern k) {
+  const int aux = k == Kern::Append ? c->L.aux_bytes : k == Kern::Fused ? c->L.f_bytes : c->L.e_bytes;
+  return dl::plan_pipeline(c->cfg.d_k, aux, G, c->smem_optin, c->smem_per_sm, shape_override());
 }
 
 bool record(dl_ctx* c, int kind, cudaEvent_t* ev) {
@@ -242,7 +244,9 @@ dl_status run_step(dl_ctx* c, const int32_t* slots, int32_t n, const void* q, co
     const int32_t rows = (n - row0) < dl::MAX_ROWS ? (n - row0) : dl::MAX_ROWS;
     fill_step_args(c, a, row0, rows, q, k, v, g, beta, o);
     unit_shape(c, a);
-    const dl::PipePlan ps = pipe_shape(c, a.G, !eager);
+    const bool fused = !eager && f.staging == DL_STAGE_FUSED;
+    const dl::PipePlan ps =
+        pipe_shape(c, a.G, eager ? Kern::Eager : fused ? Kern::Fused : Kern::Append);
     if (ps.ns == 0) return set_err(c, DL_EUNSUPPORTED, "pipeline does not fit in shared memory");
     a.ns = ps.ns;
     a.na = ps.na;
@@ -258,6 +262,11 @@ dl_status run_step(dl_ctx* c, const int32_t* slots, int32_t n, const void* q, co
       const bool t = record(c, 2, &e0);
       DL_CUDA(dl::launch_eager_step(f.op, f.d_k, a, grid, ps.smem, c->stream), "EagerStep launch");
       if (t) record_end(c, 2, e0);
+    } else if (fused) {
+      const bool t = record(c, 1, &e0);
+      DL_CUDA(dl::launch_append_decode_fused(f.op, f.d_k, a, grid, ps.smem, c->stream),
+              "AppendDecode launch");
+      if (t) record_end(c, 1, e0);
     } else {
       bool t = record(c, 0, &e0);
       DL_CUDA(dl::launch_replay_prep(f.op, f.d_k, a, c->stream), "ReplayPrep launch");
@@ -298,7 +307,8 @@ dl_status dl_create(const dl_config* cfg, void* stream, dl_ctx** out) {
   if (!cfg) return DL_EINVAL;
   const dl_config f = *cfg;
   if (f.op < DL_GDN || f.op > DL_RWKV6 || f.num_slots < 1 || f.num_heads < 1 ||
-      f.merge_interval < 1 || (f.out_bf16 != 0 && f.out_bf16 != 1))
+      f.merge_interval < 1 || (f.out_bf16 != 0 && f.out_bf16 != 1) ||
+      (f.staging != DL_STAGE_FUSED && f.staging != DL_STAGE_KERNELS))
     return DL_EINVAL;
   if (f.merge_interval > 32) return DL_EUNSUPPORTED;
   if ((f.d_k != 64 && f.d_k != 128) || f.d_v != f.d_k) return DL_EUNSUPPORTED;

@@ -16,7 +16,7 @@ enum Op : int { GDN = 0, KDA = 1, RWKV6 = 2 };
 
 constexpr int BV = 32;            // value rows per tile (one warp owns one tile)
 constexpr int MAX_NCW = 8;        // consumer warps per AppendDecode / EagerStep CTA (at most)
-constexpr int PIPE_THREADS_MAX = (MAX_NCW + 1) * 32;
+constexpr int PIPE_THREADS_MAX = (MAX_NCW + 2) * 32;   // consumers + producer + prep warp
 constexpr int MAX_ROWS = 1024;    // slot rows per launch (more are split into chunks)
 constexpr int HDR = 8;            // scalar header of a coefficient block (floats)
 constexpr int BAR_BYTES = 1024;   // mbarrier area at the start of the pipelined kernels' shared memory
@@ -193,6 +193,9 @@ __device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void* src, uin
 // arrivals).
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");

@@ -13,6 +13,10 @@ cudaError_t launch_replay_prep(int op, int dk, const StepArgs& a, cudaStream_t s
 cudaError_t launch_append_decode(int op, int dk, const StepArgs& a, int grid, size_t smem,
                                  bool pdl, cudaStream_t s);
 
+// AppendDecode with the ReplayPrep stage fused in as a warp role (no ReplayPrep launch).
+cudaError_t launch_append_decode_fused(int op, int dk, const StepArgs& a, int grid, size_t smem,
+                                       cudaStream_t s);
+
 // EagerStep: the dense read-modify-write step (the comparison kernel).
 cudaError_t launch_eager_step(int op, int dk, const StepArgs& a, int grid, size_t smem,
                               cudaStream_t s);

@@ -35,6 +35,11 @@ struct Layout {
   int P0, CB;                // coefficient floats for append steps / block stride
   int aux_coef, aux_kq, aux_v, aux_U, aux_kl, aux_bytes;   // AppendDecode aux slot
   int e_kq, e_v, e_g, e_bytes;                              // EagerStep aux slot
+  // AppendDecode with the ReplayPrep stage fused in as a warp role: the aux
+  // slot also holds what that warp reads (key log, log-decays, g, beta, bonus)
+  // and it writes the coefficients into f_coef (the K̃ rows of a per-key merge
+  // go over the log-decay rows, in f_L).
+  int f_coef, f_kq, f_v, f_U, f_kl, f_L, f_g, f_beta, f_bonus, f_bytes;
 };
 
 DL_HD inline int round4(int x) { return (x + 3) & ~3; }
@@ -61,6 +66,17 @@ DL_HD inline Layout make_layout(int op, int M, int dk, int dv) {
   L.e_v = off;      off += round16(dv * 2);
   L.e_g = off;      off += perkey ? dk * 4 : 0;
   L.e_bytes = round16(off);
+  off = 0;
+  L.f_coef = off;   off += round16((L.P0 + (perkey ? dk : L.M4)) * 4);
+  L.f_kq = off;     off += 2 * dk * 2;
+  L.f_v = off;      off += delta ? round16(dv * 2) : 0;
+  L.f_U = off;      off += M * dv * (delta ? 4 : 2);
+  L.f_kl = off;     off += M * dk * 2;
+  L.f_L = off;      off += perkey ? M * dk * 4 : L.M4 * 4;
+  L.f_g = off;      off += perkey ? dk * 4 : 16;
+  L.f_beta = off;   off += delta ? 16 : 0;
+  L.f_bonus = off;  off += (op == 2) ? dk * 4 : 0;
+  L.f_bytes = round16(off);
   return L;
 }
 

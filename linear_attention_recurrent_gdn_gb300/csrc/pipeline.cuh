@@ -37,7 +37,7 @@
 
 namespace dl {
 
-enum Mode : int { APPEND = 0, EAGER = 1 };
+enum Mode : int { APPEND = 0, EAGER = 1, FUSED = 2 };
 
 constexpr int MAX_NS = 24, MAX_NA = 24;   // (barrier area: 8 bytes each)
 
@@ -48,6 +48,7 @@ struct Bars {
   __device__ uint32_t empty(int s) const { return b0 + 8u * (ns + s); }
   __device__ uint32_t afull(int x) const { return b0 + 8u * (2 * ns + x); }
   __device__ uint32_t aempty(int x) const { return b0 + 8u * (2 * ns + na + x); }
+  __device__ uint32_t cready(int x) const { return b0 + 8u * (2 * ns + 2 * na + x); }
 };
 
 // Stage ownership: tile i (CTA-local order) belongs to consumer warp i % ncw,
@@ -120,6 +121,33 @@ __device__ __forceinline__ void issue_aux(const StepArgs& a, const Layout& Lay, 
       if (n > 0) copy_seg(base + Lay.aux_kl, a.klog + lh * Lay.Mcap * DK, (uint32_t)n * DK * 2, lane);
       copy_seg(base + Lay.aux_kl + n * DK * 2, a.k + sh * DK, DK * 2, lane);
     }
+  } else if constexpr (MODE == FUSED) {
+    // everything the fused ReplayPrep stage and the consumers read
+    constexpr int ESA = DELTA ? 4 : 2;
+    const int n = it.n;
+    const bool merge = (n + 1 == a.M);
+    const size_t lh = (size_t)it.slot * a.H + p.h;
+    copy_seg(base + Lay.f_kq, a.k + sh * DK, DK * 2, lane);
+    copy_seg(base + Lay.f_kq + DK * 2, a.q + sh * DK, DK * 2, lane);
+    if (DELTA) copy_seg(base + Lay.f_v, a.v + sh * DV, DV * 2, lane);
+    if (n > 0) {
+      copy_seg(base + Lay.f_U, static_cast<const unsigned char*>(a.alog) + lh * Lay.Mcap * DV * ESA,
+               (uint32_t)n * DV * ESA, lane);
+      copy_seg(base + Lay.f_kl, a.klog + lh * Lay.Mcap * DK, (uint32_t)n * DK * 2, lane);
+    }
+    if (OP == RWKV6) copy_seg(base + Lay.f_U + n * DV * 2, a.v + sh * DV, DV * 2, lane);
+    if (OP == GDN && merge) copy_seg(base + Lay.f_kl + n * DK * 2, a.k + sh * DK, DK * 2, lane);
+    if constexpr (OP == GDN) {
+      // scalar log-decays (rows are not 16-byte aligned): 4-byte copies
+      if (lane < n) cp_async4(base + Lay.f_L + lane * 4, a.Llog + lh * Lay.Mcap + lane);
+      if (lane == 0) cp_async4(base + Lay.f_g, a.g + sh);
+    } else {
+      if (n > 0)
+        copy_seg(base + Lay.f_L, a.Llog + lh * Lay.Mcap * DK, (uint32_t)n * DK * 4, lane);
+      copy_seg(base + Lay.f_g, a.g + sh * DK, DK * 4, lane);
+    }
+    if (DELTA && lane == 0) cp_async4(base + Lay.f_beta, a.beta + sh);
+    if (OP == RWKV6) copy_seg(base + Lay.f_bonus, a.bonus + (size_t)p.h * DK, DK * 4, lane);
   } else {
     copy_seg(base + Lay.e_kq, a.k + sh * DK, DK * 2, lane);
     copy_seg(base + Lay.e_kq + DK * 2, a.q + sh * DK, DK * 2, lane);
@@ -140,25 +168,229 @@ __device__ __forceinline__ void issue_coef_and_arrive(const StepArgs& a, const L
   cp_async_arrive_noinc(bar);
 }
 
+// ------------------------------------------------- ReplayPrep stage (fused) --
+// The per slot-head coefficients of the DeltaLog page's ReplayPrep stage
+// ("Kernel implementation — Staged execution"), computed by one warp of the
+// AppendDecode CTA from the unit's inputs already in shared memory, and
+// written into the unit's aux slot for its value-tile consumers.  The same
+// arithmetic as the ReplayPrep kernel (replay_prep.cu); see there for the
+// formulas.  On an append step the owner unit (value-tile group 0) of the
+// slot-head also appends k_t, Λ_t (and v_t for RWKV6) to the slot's log in HBM,
+// and the (head 0, group 0) unit advances the device slot table.
+template <int OP, int DK, int DV, int NE>
+__device__ __forceinline__ void prep_unit(const StepArgs& a, const Layout& Lay, const UnitPos& p,
+                                          unsigned char* ax, int lane) {
+  constexpr int VEC = DK / 32;
+  constexpr int SHIFT = NE == 32 ? 0 : NE == 16 ? 1 : 2;   // entry of lane l: l >> SHIFT
+  const int lane_entry = lane >> SHIFT;
+  const bool entry_writer = (lane & ((1 << SHIFT) - 1)) == 0;
+  const StepItem it = a.items[p.row];
+  const int n = it.n, slot = it.slot;
+  const bool merge = (n + 1 == a.M);
+  const bool owner = (p.grp == 0);
+  const int Mcap = Lay.Mcap, Mcap4 = Lay.Mcap4;
+  const int vecA = HDR + 2 * Mcap4, vecB = vecA + DK;
+  const size_t lh = (size_t)slot * a.H + p.h;
+  float* cf = reinterpret_cast<float*>(ax + Lay.f_coef);
+  const uint16_t* kq16 = reinterpret_cast<const uint16_t*>(ax + Lay.f_kq);
+  const uint16_t* kl = reinterpret_cast<const uint16_t*>(ax + Lay.f_kl);
+  float* Ls = reinterpret_cast<float*>(ax + Lay.f_L);
+  const float* gs = reinterpret_cast<const float*>(ax + Lay.f_g);
+  const int c0 = lane * VEC;
+  float kv[VEC], qv[VEC];
+  ldvec_bf16<VEC>(kv, kq16 + c0);
+  ldvec_bf16<VEC>(qv, kq16 + DK + c0);
+  float p1[NE], p2[NE];
+  if constexpr (OP == GDN) {
+    const float beta_t = reinterpret_cast<const float*>(ax + Lay.f_beta)[0];
+    const float Lt = (n > 0 ? Ls[n - 1] : 0.f) + gs[0];
+    float kq = 0.f;
+#pragma unroll
+    for (int c = 0; c < VEC; ++c) kq += kv[c] * qv[c];
+    kq = warp_sum(kq);
+#pragma unroll
+    for (int j = 0; j < NE; ++j) {
+      float x = 0.f, y = 0.f;
+      if (j < n) {
+        float kj[VEC];
+        ldvec_bf16<VEC>(kj, kl + j * DK + c0);
+#pragma unroll
+        for (int c = 0; c < VEC; ++c) {
+          x += kj[c] * kv[c];
+          y += kj[c] * qv[c];
+        }
+      }
+      p1[j] = x;
+      p2[j] = y;
+    }
+    const float dkk = reduce_entries<NE>(p1, lane);
+    const float dkq = reduce_entries<NE>(p2, lane);
+    if (entry_writer && lane_entry < n) {
+      const float wj = expf(Lt - Ls[lane_entry]);
+      cf[HDR + lane_entry] = wj * dkk;
+      cf[HDR + Mcap4 + lane_entry] = wj * dkq;
+      if (merge) cf[Lay.P0 + lane_entry] = wj;
+    }
+    if (lane == 0) {
+      cf[0] = expf(Lt);
+      cf[1] = kq;
+      cf[2] = beta_t;
+      if (merge) cf[Lay.P0 + n] = 1.f;
+      if (!merge && owner) a.Llog[lh * Mcap + n] = Lt;
+    }
+  } else {
+    float Lp[VEC], gt[VEC], Lt[VEC], Lc[VEC], wt[VEC];
+    if (n > 0) {
+      ldvec<VEC>(Lp, Ls + (size_t)(n - 1) * DK + c0);
+    } else {
+#pragma unroll
+      for (int c = 0; c < VEC; ++c) Lp[c] = 0.f;
+    }
+    ldvec<VEC>(gt, gs + c0);
+#pragma unroll
+    for (int c = 0; c < VEC; ++c) {
+      Lt[c] = Lp[c] + gt[c];
+      Lc[c] = (OP == KDA) ? Lt[c] : Lp[c];
+      wt[c] = (OP == RWKV6) ? expf(gt[c]) : 1.f;
+    }
+    __syncwarp();   // every lane has read row n-1 before K̃ rows overwrite the log-decay rows
+    if constexpr (OP == KDA) {
+      float kq = 0.f;
+#pragma unroll
+      for (int c = 0; c < VEC; ++c) {
+        const float e = expf(Lt[c]);
+        cf[vecA + c0 + c] = e * kv[c];
+        cf[vecB + c0 + c] = e * qv[c];
+        if (merge) cf[Lay.P0 + c0 + c] = e;
+        kq += kv[c] * qv[c];
+      }
+      kq = warp_sum(kq);
+      if (lane == 0) {
+        cf[1] = kq;
+        cf[2] = reinterpret_cast<const float*>(ax + Lay.f_beta)[0];
+      }
+    } else {
+      float bon[VEC];
+      ldvec<VEC>(bon, reinterpret_cast<const float*>(ax + Lay.f_bonus) + c0);
+      float cb = 0.f;
+#pragma unroll
+      for (int c = 0; c < VEC; ++c) {
+        cf[vecA + c0 + c] = expf(Lp[c]) * qv[c];
+        cb += qv[c] * bon[c] * kv[c];
+        if (merge) cf[Lay.P0 + c0 + c] = expf(Lt[c]);
+      }
+      cb = warp_sum(cb);
+      if (lane == 0) cf[3] = cb;
+    }
+#pragma unroll
+    for (int j = 0; j < NE; ++j) {
+      float x = 0.f, y = 0.f;
+      if (j < n) {
+        float kj[VEC], lj[VEC], kk[VEC];
+        ldvec_bf16<VEC>(kj, kl + j * DK + c0);
+        ldvec<VEC>(lj, Ls + (size_t)j * DK + c0);
+#pragma unroll
+        for (int c = 0; c < VEC; ++c) {
+          kk[c] = kj[c] * __expf(Lc[c] - lj[c]);
+          if (OP == KDA) {
+            x += kk[c] * kv[c];
+            y += kk[c] * qv[c];
+          } else {
+            x += kk[c] * qv[c];
+          }
+        }
+        if (merge) {   // K̃_j = k_j ⊙ e^{Λ_t-Λ_j} over this lane's columns of row j
+#pragma unroll
+          for (int c = 0; c < VEC; ++c) Ls[(size_t)j * DK + c0 + c] = kk[c] * wt[c];
+        }
+      }
+      p1[j] = x;
+      p2[j] = y;
+    }
+    if (merge) {
+#pragma unroll
+      for (int c = 0; c < VEC; ++c) Ls[(size_t)n * DK + c0 + c] = kv[c];   // K̃_n = k_t
+    }
+    const float d1 = reduce_entries<NE>(p1, lane);
+    float d2 = 0.f;
+    if constexpr (OP == KDA) d2 = reduce_entries<NE>(p2, lane);
+    if (entry_writer && lane_entry < n) {
+      cf[HDR + lane_entry] = d1;
+      if constexpr (OP == KDA) cf[HDR + Mcap4 + lane_entry] = d2;
+    }
+    if (!merge && owner) {
+      float* Ld = a.Llog + (lh * Mcap + n) * DK + c0;
+#pragma unroll
+      for (int c = 0; c < VEC; ++c) Ld[c] = Lt[c];
+    }
+  }
+  if (!merge && owner) {
+    uint16_t* kd = a.klog + (lh * Mcap + n) * DK + c0;
+#pragma unroll
+    for (int c = 0; c < VEC; ++c) kd[c] = kq16[c0 + c];
+    if constexpr (OP == RWKV6) {
+      uint16_t* vd = static_cast<uint16_t*>(a.alog) + (lh * Mcap + n) * DV;
+      const uint16_t* vs = reinterpret_cast<const uint16_t*>(ax + Lay.f_U) + n * DV;
+      for (int i = lane; i < DV; i += 32) vd[i] = vs[i];
+    }
+  }
+  if (owner && p.h == 0 && lane == 0) {
+    a.nlog[slot] = merge ? 0 : n + 1;
+    a.base_of[slot] = merge ? slot : it.base;
+  }
+}
+
 // ---------------------------------------------------------- AppendDecode ----
+// Where a unit's inputs sit in its aux slot (they differ between the two-kernel
+// and the fused form).
+struct AuxView {
+  const float* cf;        // coefficient block
+  const uint16_t* kq;     // k_t, q_t (bf16)
+  const uint16_t* v;      // v_t (bf16, delta-rule ops)
+  unsigned char* U;       // value-side log rows (+ row n)
+  const uint16_t* kl;     // key log rows, row n = k_t (GDN merge)
+  const float* Kt;        // K̃ rows (per-key merge)
+};
+
+template <int OP, int DK, int MODE>
+__device__ __forceinline__ AuxView aux_view(const Layout& Lay, unsigned char* ax) {
+  AuxView v;
+  if constexpr (MODE == FUSED) {
+    v.cf = reinterpret_cast<const float*>(ax + Lay.f_coef);
+    v.kq = reinterpret_cast<const uint16_t*>(ax + Lay.f_kq);
+    v.v = reinterpret_cast<const uint16_t*>(ax + Lay.f_v);
+    v.U = ax + Lay.f_U;
+    v.kl = reinterpret_cast<const uint16_t*>(ax + Lay.f_kl);
+    v.Kt = reinterpret_cast<const float*>(ax + Lay.f_L);
+  } else {
+    v.cf = reinterpret_cast<const float*>(ax + Lay.aux_coef);
+    v.kq = reinterpret_cast<const uint16_t*>(ax + Lay.aux_kq);
+    v.v = reinterpret_cast<const uint16_t*>(ax + Lay.aux_v);
+    v.U = ax + Lay.aux_U;
+    v.kl = reinterpret_cast<const uint16_t*>(ax + Lay.aux_kl);
+    v.Kt = v.cf + Lay.P0 + DK;
+  }
+  return v;
+}
+
 // Returns true if it already released the tile stage (append steps release it
 // right after the pass over the tile, so the refill overlaps the epilogue).
 template <int OP, int DK, int DV>
 __device__ __forceinline__ bool consume_append(const StepArgs& a, const Layout& Lay,
                                                const UnitPos& p, int vt, const float* T,
-                                               unsigned char* ax, int lane, uint32_t empty_bar,
+                                               const AuxView& av, int lane, uint32_t empty_bar,
                                                bool may_release) {
   constexpr int VEC = DK / 32;
   constexpr bool DELTA = OP != RWKV6;
   const StepItem it = a.items[p.row];
   const int n = it.n;
   const bool merge = (n + 1 == a.M);
-  const float* cf = reinterpret_cast<const float*>(ax + Lay.aux_coef);
+  const float* cf = av.cf;
   const int vecA = HDR + 2 * Lay.Mcap4;
 
   float kv[VEC], qv[VEC];
   if constexpr (OP == GDN) {
-    const uint16_t* kq16 = reinterpret_cast<const uint16_t*>(ax + Lay.aux_kq);
+    const uint16_t* kq16 = av.kq;
     ldvec_bf16<VEC>(kv, kq16 + lane * VEC);
     ldvec_bf16<VEC>(qv, kq16 + DK + lane * VEC);
   } else if constexpr (OP == KDA) {
@@ -195,7 +427,7 @@ __device__ __forceinline__ bool consume_append(const StepArgs& a, const Layout& 
   const int col = vt * BV + lane;
   const size_t oidx = (size_t)p.sh * DV + col;
   if constexpr (DELTA) {
-    const float* U = reinterpret_cast<const float*>(ax + Lay.aux_U);
+    const float* U = reinterpret_cast<const float*>(av.U);
     float x = (OP == GDN) ? cf[0] * A : A;
     float ob = (OP == GDN) ? cf[0] * B : B;
     for (int j = 0; j < n; ++j) {
@@ -203,18 +435,18 @@ __device__ __forceinline__ bool consume_append(const StepArgs& a, const Layout& 
       x += cf[HDR + j] * uj;
       ob += cf[HDR + Lay.Mcap4 + j] * uj;
     }
-    const float vv = bf16f(reinterpret_cast<const uint16_t*>(ax + Lay.aux_v)[col]);
+    const float vv = bf16f(av.v[col]);
     const float u = cf[2] * (vv - x);
     store_out(a, oidx, a.scale * (ob + cf[1] * u));
     if (!merge) {
       const size_t lh = (size_t)it.slot * a.H + p.h;
       static_cast<float*>(a.alog)[(lh * Lay.Mcap + n) * DV + col] = u;
     } else {
-      reinterpret_cast<float*>(ax + Lay.aux_U)[n * DV + col] = u;
+      reinterpret_cast<float*>(av.U)[n * DV + col] = u;
       __syncwarp();
     }
   } else {
-    const uint16_t* V = reinterpret_cast<const uint16_t*>(ax + Lay.aux_U);
+    const uint16_t* V = reinterpret_cast<const uint16_t*>(av.U);
     float o = A;
     for (int j = 0; j < n; ++j) o += cf[HDR + j] * bf16f(V[j * DV + col]);
     o += cf[3] * bf16f(V[n * DV + col]);
@@ -245,23 +477,23 @@ __device__ __forceinline__ bool consume_append(const StepArgs& a, const Layout& 
     for (int j = 0; j <= n; ++j) {
       float K[VEC];
       if constexpr (OP == GDN) {
-        ldvec_bf16<VEC>(K, reinterpret_cast<const uint16_t*>(ax + Lay.aux_kl) + j * DK + lane * VEC);
+        ldvec_bf16<VEC>(K, av.kl + j * DK + lane * VEC);
         const float w = cf[Lay.P0 + j];
 #pragma unroll
         for (int c = 0; c < VEC; ++c) K[c] *= w;
       } else {
-        ldvec<VEC>(K, cf + Lay.P0 + DK + j * DK + lane * VEC);
+        ldvec<VEC>(K, av.Kt + j * DK + lane * VEC);
       }
       float uu[8];
       if constexpr (DELTA) {
-        const float* U = reinterpret_cast<const float*>(ax + Lay.aux_U) + j * DV + vt * BV + rb * 8;
+        const float* U = reinterpret_cast<const float*>(av.U) + j * DV + vt * BV + rb * 8;
         const float4 u0 = *reinterpret_cast<const float4*>(U);
         const float4 u1 = *reinterpret_cast<const float4*>(U + 4);
         uu[0] = u0.x; uu[1] = u0.y; uu[2] = u0.z; uu[3] = u0.w;
         uu[4] = u1.x; uu[5] = u1.y; uu[6] = u1.z; uu[7] = u1.w;
       } else {
         const uint4 w = *reinterpret_cast<const uint4*>(
-            reinterpret_cast<const uint16_t*>(ax + Lay.aux_U) + j * DV + vt * BV + rb * 8);
+            reinterpret_cast<const uint16_t*>(av.U) + j * DV + vt * BV + rb * 8);
         uu[0] = bf16lo(w.x); uu[1] = bf16hi(w.x); uu[2] = bf16lo(w.y); uu[3] = bf16hi(w.y);
         uu[4] = bf16lo(w.z); uu[5] = bf16hi(w.z); uu[6] = bf16lo(w.w); uu[7] = bf16hi(w.w);
       }
@@ -372,7 +604,8 @@ __global__ void __launch_bounds__(PIPE_THREADS_MAX, 1) pipe_kernel(const __grid_
   const int IPU = G / TPS;                       // stage items per unit
   const uint32_t STAGE_BYTES = TILE_BYTES * TPS; // one bulk copy per stage item
   const int R = NS / NCWr;   // stages per consumer warp (ns is a multiple of ncw)
-  const uint32_t aux_bytes = (MODE == APPEND) ? Lay.aux_bytes : Lay.e_bytes;
+  const uint32_t aux_bytes =
+      (MODE == APPEND) ? Lay.aux_bytes : (MODE == FUSED) ? Lay.f_bytes : Lay.e_bytes;
   const Bars bars{smem_u32(smem), NS, NA};
   float* tiles = reinterpret_cast<float*>(smem + BAR_BYTES);
   unsigned char* auxm = smem + BAR_BYTES + (size_t)NS * STAGE_BYTES;
@@ -386,6 +619,7 @@ __global__ void __launch_bounds__(PIPE_THREADS_MAX, 1) pipe_kernel(const __grid_
     for (int x = 0; x < NA; ++x) {
       mbar_init(bars.afull(x), 32);   // one arrival per producer lane
       mbar_init(bars.aempty(x), IPU);
+      mbar_init(bars.cready(x), 1);   // fused form: the prep warp's arrival
     }
     fence_mbar_init();
   }
@@ -475,6 +709,23 @@ __global__ void __launch_bounds__(PIPE_THREADS_MAX, 1) pipe_kernel(const __grid_
     return;
   }
 
+  if (MODE == FUSED && warp == NCWr + 1) {
+    // ------------------------------------------------- fused ReplayPrep stage
+    for (int kk = 0; kk < my_units; ++kk) {
+      const int x = kk % NA;
+      if (!__all_sync(0xffffffffu, mbar_wait(bars.afull(x), (kk / NA) & 1, a.status, DEV_TIMEOUT_AUX)))
+        break;
+      const UnitPos p = unit_pos(a, (int)blockIdx.x + kk * (int)gridDim.x);
+      unsigned char* ax = auxm + (size_t)x * aux_bytes;
+      if (a.M - 1 <= 8) prep_unit<OP, DK, DV, 8>(a, Lay, p, ax, lane);
+      else if (a.M - 1 <= 16) prep_unit<OP, DK, DV, 16>(a, Lay, p, ax, lane);
+      else prep_unit<OP, DK, DV, 32>(a, Lay, p, ax, lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars.cready(x));
+    }
+    return;
+  }
+
   // -------------------------------------------------------------- consumers
   for (int i = warp; i < my_tiles; i += NCWr) {
     const int kk = i / IPU;
@@ -490,16 +741,20 @@ __global__ void __launch_bounds__(PIPE_THREADS_MAX, 1) pipe_kernel(const __grid_
     // landed the aux barrier is in this unit's phase and the parity test below
     // is unambiguous.
     bool ok = mbar_wait(bars.full(s), stage_parity(i, R, NCWr), a.status, DEV_TIMEOUT_TILE);
-    ok = ok && mbar_wait(bars.afull(x), (kk / NA) & 1, a.status, DEV_TIMEOUT_AUX);
+    ok = ok && mbar_wait(MODE == FUSED ? bars.cready(x) : bars.afull(x), (kk / NA) & 1, a.status,
+                         DEV_TIMEOUT_AUX);
     if (!__all_sync(0xffffffffu, ok)) break;
     unsigned char* ax = auxm + (size_t)x * aux_bytes;
     bool released = false;
     for (int t = 0; t < TPS; ++t) {
       const float* T = tiles + ((size_t)s * TPS + t) * BV * DK;
-      if constexpr (MODE == APPEND)
-        released = consume_append<OP, DK, DV>(a, Lay, p, vt0 + t, T, ax, lane, bars.empty(s),
+      if constexpr (MODE == EAGER) {
+        consume_eager<OP, DK, DV>(a, Lay, p, vt0 + t, T, ax, lane, g_s, beta_s);
+      } else {
+        const AuxView av = aux_view<OP, DK, MODE>(Lay, ax);
+        released = consume_append<OP, DK, DV>(a, Lay, p, vt0 + t, T, av, lane, bars.empty(s),
                                               t == TPS - 1);
-      else consume_eager<OP, DK, DV>(a, Lay, p, vt0 + t, T, ax, lane, g_s, beta_s);
+      }
     }
     // order this warp's shared-memory writes (u_t rows of a merge) before the
     // bulk copies that will refill the slots once they are released

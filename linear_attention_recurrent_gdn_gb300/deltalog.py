@@ -44,7 +44,10 @@ class dl_config(ctypes.Structure):
     _fields_ = [("op", ctypes.c_int32), ("num_slots", ctypes.c_int32),
                 ("num_heads", ctypes.c_int32), ("d_k", ctypes.c_int32),
                 ("d_v", ctypes.c_int32), ("merge_interval", ctypes.c_int32),
-                ("out_bf16", ctypes.c_int32), ("scale", ctypes.c_float)]
+                ("out_bf16", ctypes.c_int32), ("scale", ctypes.c_float),
+                ("staging", ctypes.c_int32)]
+
+STAGE_FUSED, STAGE_KERNELS = 0, 1
 
 
 class dl_state_view(ctypes.Structure):
@@ -385,12 +388,12 @@ class DeltaLog:
     """
 
     def __init__(self, op, num_slots, num_heads, d_k, d_v=None, merge_interval=16,
-                 out_bf16=True, scale=1.0, stream=None):
+                 out_bf16=True, scale=1.0, stream=None, staging=STAGE_FUSED):
         import torch
         self.torch = torch
         d_v = d_k if d_v is None else d_v
         self.cfg = dl_config(int(op), int(num_slots), int(num_heads), int(d_k), int(d_v),
-                             int(merge_interval), 1 if out_bf16 else 0, float(scale))
+                             int(merge_interval), 1 if out_bf16 else 0, float(scale), int(staging))
         if stream is None:
             stream = torch.cuda.current_stream().cuda_stream
         self.stream = int(stream)

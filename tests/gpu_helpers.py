@@ -51,13 +51,14 @@ def oracle_run(op, x, S0, bonus, sel=None, snap=None):
 
 
 def gpu_run(op, x, S0, bonus, M, out_bf16=True, eager=False, snap=(), slots=None,
-            num_slots=None):
+            num_slots=None, staging=0):
     """Run T tokens on all B slots through the C ABI.  Returns o [T, B, H, dv] (fp32 host),
     a dict step -> state [B, H, dv, dk] (host) for steps in `snap`, and the context."""
     from linear_attention_recurrent_gdn_gb300 import deltalog as dl
     T, B, H, d = x["q"].shape
     slots = list(range(B)) if slots is None else list(slots)
-    ctx = dl.DeltaLog(op, num_slots or max(slots) + 1, H, d, d, M, out_bf16=out_bf16)
+    ctx = dl.DeltaLog(op, num_slots or max(slots) + 1, H, d, d, M, out_bf16=out_bf16,
+                      staging=staging)
     dev = {k: (v.cuda() if v is not None else None) for k, v in x.items()}
     ctx.set_state(slots, S0.cuda().contiguous())
     if bonus is not None:

@@ -36,7 +36,7 @@ def test_header_symbols_exported(dl):
     missing = [s for s in sorted(declared) if not hasattr(lib, s)]
     assert not missing, missing
     assert declared == set(dl.EXPORTS)
-    assert dl.dl_abi_version() == 1
+    assert dl.dl_abi_version() == 2
 
 
 def test_status_strings(dl):

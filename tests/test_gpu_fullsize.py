@@ -36,7 +36,7 @@ def _oracle(op, S0, q, k, v, g, extra):
     return fn(S0, q, k, v, g, extra)
 
 
-def _run_fullsize(op, B, H, d, T, M, seed, nsample=12):
+def _run_fullsize(op, B, H, d, T, M, seed, nsample=12, staging=0):
     from linear_attention_recurrent_gdn_gb300 import deltalog as dl
     dev = torch.device("cuda")
     sel = _sample(B, H, nsample, seed)
@@ -44,7 +44,7 @@ def _run_fullsize(op, B, H, d, T, M, seed, nsample=12):
     hi = torch.tensor([s[1] for s in sel], device=dev)
     S0 = gen.initial_state(B, H, d, d, seed, device=dev)
     bonus = gen.rwkv6_bonus(H, d, seed, device=dev) if op == gen.RWKV6 else None
-    ctx = dl.DeltaLog(op, B, H, d, d, M)
+    ctx = dl.DeltaLog(op, B, H, d, d, M, staging=staging)
     slots = list(range(B))
     ctx.set_state(slots, S0)
     if bonus is not None:
@@ -71,25 +71,28 @@ def _run_fullsize(op, B, H, d, T, M, seed, nsample=12):
     return max_step_rel(o, o_ref), rel_err(S_sel, S_ref), n, base_of
 
 
-@pytest.mark.parametrize("M", [16, 1, 32])
-def test_gdn_serving_batch(M):
+@pytest.mark.parametrize("M,staging", [(16, 0), (1, 0), (32, 0), (16, 1)])
+def test_gdn_serving_batch(M, staging):
     """GDN decode at serving batch: B=256, H=32, d=128, 512 tokens."""
-    eo, es, n, base_of = _run_fullsize(gen.GDN, 256, 32, 128, 512, M, seed=2001)
+    eo, es, n, base_of = _run_fullsize(gen.GDN, 256, 32, 128, 512, M, seed=2001, staging=staging)
     assert eo <= OUT_TOL_BF16, eo
     assert es <= STATE_TOL, es
     assert list(n) == [512 % M] * 256 and list(base_of) == list(range(256))
 
 
-def test_kda_decode():
+@pytest.mark.parametrize("staging", [0, 1])
+def test_kda_decode(staging):
     """KDA decode: B=128, H=32, d=128, per-key decay, M=16, 512 tokens."""
-    eo, es, n, _ = _run_fullsize(gen.KDA, 128, 32, 128, 512, 16, seed=2002, nsample=8)
+    eo, es, n, _ = _run_fullsize(gen.KDA, 128, 32, 128, 512, 16, seed=2002, nsample=8,
+                                 staging=staging)
     assert eo <= OUT_TOL_BF16, eo
     assert es <= STATE_TOL, es
 
 
-def test_rwkv6_decode():
+@pytest.mark.parametrize("staging", [0, 1])
+def test_rwkv6_decode(staging):
     """RWKV6 decode: B=128, H=40, head size 64, M=16, 512 tokens."""
-    eo, es, n, _ = _run_fullsize(gen.RWKV6, 128, 40, 64, 512, 16, seed=2003)
+    eo, es, n, _ = _run_fullsize(gen.RWKV6, 128, 40, 64, 512, 16, seed=2003, staging=staging)
     assert eo <= OUT_TOL_BF16, eo
     assert es <= STATE_TOL, es
 

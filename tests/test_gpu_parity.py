@@ -18,6 +18,7 @@ from linear_attention_recurrent_gdn_gb300 import inputs as gen
 pytestmark = pytest.mark.gpu
 
 OPS = [gen.GDN, gen.KDA, gen.RWKV6]
+STAGINGS = [0, 1]   # ReplayPrep fused as a warp role / as its own kernel
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -55,17 +56,18 @@ def test_config0_gdn_full(M):
 
 
 # ------------------------------------------------- all ops, sizes, merge intervals
+@pytest.mark.parametrize("staging", STAGINGS)
 @pytest.mark.parametrize("op", OPS)
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("M", [1, 3, 8, 16])
-def test_ops_small_ragged(op, d, M):
+def test_ops_small_ragged(op, d, M, staging):
     """B=3 slots x H=5 heads (15 slot-heads, several value tiles each), T = 2M+3
     tokens: two merges and a partial window; fp32 output, state at every step."""
     B, H, T = 3, 5, 2 * M + 3
     x, S0, bonus = make_case(op, B, H, d, T, seed=17 + 3 * op + d + M)
     snap = list(range(T))
     o_ref, S_ref, S_snap = oracle_run(op, x, S0, bonus, snap=snap)
-    o, states, ctx = gpu_run(op, x, S0, bonus, M, out_bf16=False, snap=snap)
+    o, states, ctx = gpu_run(op, x, S0, bonus, M, out_bf16=False, snap=snap, staging=staging)
     assert max_step_rel(_flat_o(o), o_ref) <= OUT_TOL_F32
     for t in snap:
         assert rel_err(_flat_S(states[t]), S_snap[t]) <= STATE_TOL, t
@@ -73,14 +75,16 @@ def test_ops_small_ragged(op, d, M):
     assert list(n) == [T % M] * B and list(base_of) == list(range(B))
 
 
+@pytest.mark.parametrize("staging", STAGINGS)
 @pytest.mark.parametrize("op", OPS)
-def test_ops_bf16_output_many_units(op):
-    """320 slot-heads (enough work units for whole-slot-head units), d=128, M=4,
+@pytest.mark.parametrize("d", [64, 128])
+def test_ops_bf16_output_many_units(op, d, staging):
+    """320 slot-heads (enough work units for whole-slot-head units), M=4,
     20 tokens, bf16 output, compared on every slot-head."""
-    B, H, d, T, M = 40, 8, 128, 20, 4
-    x, S0, bonus = make_case(op, B, H, d, T, seed=300 + op)
+    B, H, T, M = 40, 8, 20, 4
+    x, S0, bonus = make_case(op, B, H, d, T, seed=300 + op + d)
     o_ref, S_ref, _ = oracle_run(op, x, S0, bonus)
-    o, _, ctx = gpu_run(op, x, S0, bonus, M, out_bf16=True)
+    o, _, ctx = gpu_run(op, x, S0, bonus, M, out_bf16=True, staging=staging)
     assert max_step_rel(_flat_o(o), o_ref) <= OUT_TOL_BF16
     S = ctx.read_state(list(range(B))).cpu()
     assert rel_err(_flat_S(S), S_ref) <= STATE_TOL
@@ -143,9 +147,10 @@ def test_forced_merge_mid_window(op):
 
 
 # ------------------------------------------------------------------- fork -----
+@pytest.mark.parametrize("staging", STAGINGS)
 @pytest.mark.parametrize("op", OPS)
 @pytest.mark.parametrize("ctx_len", [16, 18])
-def test_fork_by_index(op, ctx_len):
+def test_fork_by_index(op, ctx_len, staging):
     """2 requests build a base over ctx_len tokens (M=8: 16 ends on a merge, 18
     leaves 2 log entries), each forks 3 branches by index; branches run ragged
     lengths; outputs and states match the oracle run from the request's state,
@@ -157,7 +162,7 @@ def test_fork_by_index(op, ctx_len):
     S = R + R * NB
     xc, S0, bonus = make_case(op, R, H, d, ctx_len, seed=90 + op)
     xq, _, _ = make_case(op, R * NB, H, d, Tq, seed=91 + op)
-    ctx = dl.DeltaLog(op, S, H, d, d, M, out_bf16=False)
+    ctx = dl.DeltaLog(op, S, H, d, d, M, out_bf16=False, staging=staging)
     model = oracle.SlotTableModel(S, M)
     ctx.set_state(list(range(R)), S0.cuda())
     model.set_state(list(range(R)))

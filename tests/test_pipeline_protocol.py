@@ -45,12 +45,14 @@ class Bar:
         return (self.done % 2) != parity
 
 
-def simulate(NS, NA, G, n_tiles, owned, tile_first, seed, p_complete=0.03, lifo=0.95):
+def simulate(NS, NA, G, n_tiles, owned, tile_first, seed, p_complete=0.03, lifo=0.95,
+             fused=False, ncw=NCW):
+    NCW_ = ncw
     rng = random.Random(seed)
-    R = NS // NCW
+    R = NS // NCW_
     if owned:
-        stage = lambda i: (i % NCW) * R + (i // NCW) % R
-        phase = lambda i: (i // NCW) // R
+        stage = lambda i: (i % NCW_) * R + (i // NCW_) % R
+        phase = lambda i: (i // NCW_) // R
     else:
         stage = lambda i: i % NS
         phase = lambda i: i // NS
@@ -58,9 +60,23 @@ def simulate(NS, NA, G, n_tiles, owned, tile_first, seed, p_complete=0.03, lifo=
     empty = [Bar(1) for _ in range(NS)]
     afull = [Bar(1) for _ in range(NA)]
     aempty = [Bar(G) for _ in range(NA)]
+    cready = [Bar(1) for _ in range(NA)]   # fused form: the prep warp's signal
     inflight, violations = [], []
     prod = {"ti": 0, "ka": 0}
-    cons = [{"i": w, "step": 0} for w in range(NCW)]
+    prep = {"k": 0}
+    cons = [{"i": w, "step": 0} for w in range(NCW_)]
+    n_units = n_tiles // G
+
+    def prep_warp():
+        k = prep["k"]
+        if k >= n_units:
+            return
+        x = k % NA
+        if afull[x].try_wait((k // NA) & 1):
+            if afull[x].done <= k // NA:
+                violations.append(("prep", k))
+            cready[x].arrive()
+            prep["k"] += 1
 
     def producer():
         ti, ka = prod["ti"], prod["ka"]
@@ -86,7 +102,7 @@ def simulate(NS, NA, G, n_tiles, owned, tile_first, seed, p_complete=0.03, lifo=
             return
         kk = i // G
         x, s = kk % NA, stage(i)
-        order = [(full[s], phase(i)), (afull[x], kk // NA)]
+        order = [(full[s], phase(i)), ((cready if fused else afull)[x], kk // NA)]
         if not tile_first:
             order.reverse()
         if c["step"] < 2:
@@ -98,7 +114,7 @@ def simulate(NS, NA, G, n_tiles, owned, tile_first, seed, p_complete=0.03, lifo=
             return
         empty[s].arrive()
         aempty[x].arrive()
-        c["i"] += NCW
+        c["i"] += NCW_
         c["step"] = 0
 
     try:
@@ -109,8 +125,10 @@ def simulate(NS, NA, G, n_tiles, owned, tile_first, seed, p_complete=0.03, lifo=
                 inflight.pop(k).complete_tx(1)
             elif r < p_complete + 0.2:
                 producer()
+            elif fused and r < p_complete + 0.3:
+                prep_warp()
             else:
-                consumer(rng.randrange(NCW))
+                consumer(rng.randrange(NCW_))
             if prod["ti"] >= n_tiles and all(c["i"] >= n_tiles for c in cons):
                 return violations, True
     except RuntimeError:
@@ -123,6 +141,25 @@ def simulate(NS, NA, G, n_tiles, owned, tile_first, seed, p_complete=0.03, lifo=
 def test_owned_stages_tile_first_is_safe(NS, NA, G):
     for seed in range(12):
         v, finished = simulate(NS, NA, G, NCW * 4 * 5, owned=True, tile_first=True, seed=seed)
+        assert not v and finished, (seed, v[:3])
+
+
+@pytest.mark.parametrize("ncw,NS,NA,G", [(4, 4, 2, 4), (4, 4, 2, 1), (3, 3, 2, 4), (8, 8, 3, 1),
+                                          (4, 12, 2, 2)])
+def test_fused_prep_stage_is_safe(ncw, NS, NA, G):
+    """The fused form: a prep warp waits on each unit's inputs in order and
+    signals a second barrier; consumers wait on their tile, then on that signal."""
+    for seed in range(12):
+        v, finished = simulate(NS, NA, G, 8 * 4 * 5, owned=True, tile_first=True, seed=seed,
+                               fused=True, ncw=ncw)
+        assert not v and finished, (seed, v[:3])
+
+
+@pytest.mark.parametrize("ncw,NS,NA,G", [(4, 4, 2, 4), (3, 3, 2, 4), (4, 8, 3, 2)])
+def test_owned_stages_two_ctas_shape_is_safe(ncw, NS, NA, G):
+    for seed in range(12):
+        v, finished = simulate(NS, NA, G, 8 * 4 * 5, owned=True, tile_first=True, seed=seed,
+                               ncw=ncw)
         assert not v and finished, (seed, v[:3])
 
 
