@@ -97,8 +97,6 @@ def algorithmic_bytes(op, d, M, n):
     lw = dk * 4 if perkey else 4
     # ReplayPrep
     rp_r = 2 * dk * 2 + (dk * 4 if perkey else 4) + (4 if delta else 0) + n * (dk * 2 + lw)
-    if op == 2:
-        rp_r += dk * 4          # bonus
     rp_w = coef + (0 if merge else dk * 2 + lw + (dv * 2 if op == 2 else 0))
     # AppendDecode
     esa = 4 if delta else 2
@@ -109,11 +107,29 @@ def algorithmic_bytes(op, d, M, n):
     return rp_r + rp_w, ad_r + ad_w, rp_w + ad_w
 
 
+def fused_bytes(op, d, M, n):
+    """Algorithmic HBM bytes of one token for one slot-head with log length n
+    before the step, when the ReplayPrep stage runs inside AppendDecode (one
+    kernel): returns (total, writes).  Reads: the dense base, k_t, q_t (r_t),
+    v_t, g_t, beta_t, and n log rows (value side, key, log-decay).  The RWKV6
+    bonus is [H, d_k] per step, shared by all slots, so it is not counted per
+    slot-head.  Writes: o_t (bf16); on an append step the log row of this
+    token (u_t fp32 or v_t bf16, k_t bf16, Λ_t); on the merge step the dense
+    base.  No coefficient block leaves the chip."""
+    dk = dv = d
+    merge = (n + 1 == M)
+    perkey = op != 0
+    delta = op != 2
+    esa = 4 if delta else 2
+    lw = dk * 4 if perkey else 4
+    r = dv * dk * 4 + 2 * dk * 2 + dv * 2 + lw + (4 if delta else 0) + n * (dv * esa + dk * 2 + lw)
+    w = dv * 2 + (dv * dk * 4 if merge else dv * esa + dk * 2 + lw)
+    return r + w, w
+
+
 def eager_bytes(op, d):
     dk = dv = d
     r = dv * dk * 4 + 2 * dk * 2 + dv * 2 + (dk * 4 if op != 0 else 4) + (4 if op != 2 else 0)
-    if op == 2:
-        r += dk * 4
     w = dv * dk * 4 + dv * 2
     return r + w, w
 
@@ -341,7 +357,8 @@ def run_ours(args):
         ms = timed(ctx, args.steps, args.warmup, eager=args.eager)
     ms_max = reduce_max(dist, ms, dev)
     value = units_per_step * world / (ms_max / 1e3)
-    launches = 2 * T * args.steps * ((B + 1023) // 1024)
+    fused = args.staging == "fused" and not args.eager
+    launches = (1 if (fused or args.eager) else 2) * T * args.steps * ((B + 1023) // 1024)
 
     # ---- per-kernel times (instrumented pass: events around every launch)
     ctx.set_timing(True)
@@ -351,13 +368,17 @@ def run_ours(args):
     n_seq = [t % M for t in range(T)]
     rp_b = ad_b = wr_all = 0
     for n in n_seq:
-        a, b_, c_ = algorithmic_bytes(op, d, M, n)
+        if fused:
+            b_, c_ = fused_bytes(op, d, M, n)
+            a = 0
+        else:
+            a, b_, c_ = algorithmic_bytes(op, d, M, n)
         rp_b += a * B * H
         ad_b += b_ * B * H
         wr_all += c_ * B * H
     ad_ms = kms[1] / max(kcnt[1], 1)
     rp_ms = kms[0] / max(kcnt[0], 1)
-    kernel_name = "AppendDecode"
+    kernel_name = "AppendDecode (ReplayPrep fused)" if fused else "AppendDecode"
     if args.eager:
         eb_, ew_ = eager_bytes(op, d)
         ad_b, wr_all, rp_b = eb_ * B * H * T, ew_ * B * H * T, 0
@@ -390,11 +411,13 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": ad_gbs, "peak": peak, "unit": "GB/s",
                      "frac": ad_gbs / peak,
                      "traffic": measured_traffic("%s_%s_b%d_h%d_d%d_m%d" % (
-                         "eager_step" if args.eager else "append_decode", gen.OP_NAMES[op], B, H, d,
-                         M)),
+                         "eager_step" if args.eager else
+                         "append_decode_fused" if fused else "append_decode",
+                         gen.OP_NAMES[op], B, H, d, M)),
                      "kernel": kernel_name, "peak_source": peak_src + " hbm_gbs",
                      "bytes_per_launch": ad_b / T, "ms_per_launch": ad_ms},
         "kernels_ms_per_token": ({"EagerStep": ad_ms} if args.eager else
+                                 {"AppendDecode (ReplayPrep fused)": ad_ms} if fused else
                                  {"ReplayPrep": rp_ms, "AppendDecode": ad_ms}),
         "step_gbs": step_bytes / (ms_max / T * 1e-3) / 1e9,
         "write_bytes_per_token": {"deltalog": wr_all / T,
@@ -490,7 +513,9 @@ def run_fork(args):
     Tq = int(lens.max())
     counts = [int((lens > t).sum()) for t in range(Tq)]
     S = R + R * NB
-    ctx = dl.DeltaLog(0, S, H, d, d, M, stream=stream.cuda_stream)
+    fused = args.staging == "fused"
+    ctx = dl.DeltaLog(0, S, H, d, d, M, stream=stream.cuda_stream,
+                      staging=dl.STAGE_FUSED if fused else dl.STAGE_KERNELS)
     ctx.set_state(list(range(R)), gen.initial_state(R, H, d, d, seed, device=dev))
     t0 = time.time()
     for t in range(Tc):
@@ -528,9 +553,9 @@ def run_fork(args):
               "data": "synthetic",
               "config": {"workload": w["desc"], "op": "gdn", "requests": R, "branches": NB,
                          "H": H, "d_k": d, "d_v": d, "M": M, "ctx_tokens": Tc,
-                         "branch_tokens": int(lens.sum()),
+                         "branch_tokens": int(lens.sum()), "staging": args.staging,
                          "l2": "inputs larger than L2 (576 slots x 1 MiB state)"},
-              "gpu_launches": (R + 2 * Tq) * args.steps}
+              "gpu_launches": (R + (1 if fused else 2) * Tq) * args.steps}
     if rank == 0:
         print(json.dumps(result), flush=True)
     ctx.close()

@@ -49,11 +49,9 @@ cudaError_t launch_append_decode_fused(int op, int dk, const StepArgs& a, int gr
 // launches (each translation unit registers its own copy of a template kernel).
 template <int OP, int DK>
 static cudaError_t cfg_one(size_t smem) {
-  cudaError_t e = cudaFuncSetAttribute(pipe_kernel<OP, DK, DK, APPEND>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = raise_smem_limit(pipe_kernel<OP, DK, DK, APPEND>, smem);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(pipe_kernel<OP, DK, DK, FUSED>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  return raise_smem_limit(pipe_kernel<OP, DK, DK, FUSED>, smem);
 }
 
 cudaError_t configure_append_decode(int op, int dk, size_t smem) {

@@ -79,6 +79,7 @@ dl_status set_err(dl_ctx* c, dl_status s, const char* fmt, ...) {
 }
 
 dl_status cuda_err(dl_ctx* c, cudaError_t e, const char* what) {
+  (void)cudaGetLastError();   // the error is reported here; do not leave it to the caller's next call
   return set_err(c, DL_ECUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 

@@ -28,8 +28,7 @@ cudaError_t launch_eager_step(int op, int dk, const StepArgs& a, int grid, size_
 
 template <int OP, int DK>
 static cudaError_t cfg_one(size_t smem) {
-  return cudaFuncSetAttribute(pipe_kernel<OP, DK, DK, EAGER>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  return raise_smem_limit(pipe_kernel<OP, DK, DK, EAGER>, smem);
 }
 
 cudaError_t configure_eager_step(int op, int dk, size_t smem) {

@@ -21,7 +21,19 @@ cudaError_t launch_append_decode_fused(int op, int dk, const StepArgs& a, int gr
 cudaError_t launch_eager_step(int op, int dk, const StepArgs& a, int grid, size_t smem,
                               cudaStream_t s);
 
-// Allow the pipelined kernels of (op, dk) to use `smem` bytes of dynamic shared memory.
+// Raise a kernel's dynamic shared-memory limit to at least `smem` bytes; never
+// lowers it, so contexts and calls that plan different shapes can share one
+// kernel instance.
+template <class Kernel>
+inline cudaError_t raise_smem_limit(Kernel* kern, size_t smem) {
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+  if (e != cudaSuccess || (size_t)fa.maxDynamicSharedSizeBytes >= smem) return e;
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+}
+
+// Allow the pipelined kernels of (op, dk) to use at least `smem` bytes of
+// dynamic shared memory.
 cudaError_t configure_append_decode(int op, int dk, size_t smem);
 cudaError_t configure_eager_step(int op, int dk, size_t smem);
 

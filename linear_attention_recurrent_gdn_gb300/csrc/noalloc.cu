@@ -205,6 +205,9 @@ extern "C" dl_status dl_step_noalloc(const dl_config* cfg, const dl_state_view* 
   if (e == cudaSuccess) e = cudaMemsetAsync(d.status, 0, sizeof(int32_t), s);   // starts at zero
   if (e == cudaSuccess) e = dl::launch_replay_prep(f.op, f.d_k, a, s);
   if (e == cudaSuccess) e = dl::launch_append_decode(f.op, f.d_k, a, grid, sh.smem, true, s);
-  if (e != cudaSuccess) return fail(DL_ECUDA, "launch failed: %s", cudaGetErrorString(e));
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();   // reported here, not left to the caller's next CUDA call
+    return fail(DL_ECUDA, "launch failed: %s", cudaGetErrorString(e));
+  }
   return DL_OK;
 }

@@ -28,9 +28,14 @@
 //   * every wait is bounded (see mbar_wait).  On an append step a consumer
 //     releases its stage right after the tile pass, so the refill overlaps its
 //     epilogue.
-// AppendDecode launches as a programmatic dependent of ReplayPrep: its
-// producer streams the first ns tiles before it waits for ReplayPrep's
-// coefficient blocks.
+// Two forms of the ReplayPrep stage:
+//   * FUSED (default): one more warp of the same CTA computes each unit's
+//     coefficients from the unit's inputs in its aux slot (prep_unit) and
+//     signals the consumers on a per-slot barrier (cready); no second launch
+//     and no coefficient round trip through HBM;
+//   * APPEND: ReplayPrep is its own kernel (replay_prep.cu) and AppendDecode
+//     launches as its programmatic dependent: the producer streams the first
+//     ns tiles before it waits for the coefficient blocks.
 #pragma once
 #include "dl_device.cuh"
 #include "layout.h"
@@ -681,7 +686,9 @@ __global__ void __launch_bounds__(PIPE_THREADS_MAX, 1) pipe_kernel(const __grid_
       if (lane == 0) {
         const UnitPos p = unit_pos(a, (int)blockIdx.x + kt * (int)gridDim.x);
         const int vt = p.grp * G + (ti - kt * IPU) * TPS;   // first value tile of the item
-        const int base = (MODE == APPEND) ? a.items[p.row].base : a.items[p.row].slot;
+        // DeltaLog steps read the base the slot indexes (a fork source's until
+        // the first merge); the eager step reads the slot's own state
+        const int base = (MODE == EAGER) ? a.items[p.row].slot : a.items[p.row].base;
         const float* src = a.Sbar + (((size_t)base * a.H + p.h) * DV + vt * BV) * DK;
         mbar_arrive_expect_tx(bars.full(s), STAGE_BYTES);
         bulk_g2s_hint(smem_u32(tiles + (size_t)s * TPS * BV * DK), src, STAGE_BYTES, bars.full(s),
