@@ -8,7 +8,7 @@ template <int OP, int DK, int MODE>
 static cudaError_t launch_ad(const StepArgs& a, int grid, size_t smem, bool pdl, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3((a.ncw + (MODE == FUSED ? 2 : 1)) * 32);
+  cfg.blockDim = dim3((a.ncw + 1 + (MODE == FUSED ? a.npw : 0)) * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -43,6 +43,25 @@ cudaError_t launch_append_decode_fused(int op, int dk, const StepArgs& a, int gr
   if (op == GDN) return launch_ad<GDN, 128, FUSED>(a, grid, smem, false, s);
   if (op == KDA) return launch_ad<KDA, 128, FUSED>(a, grid, smem, false, s);
   return launch_ad<RWKV6, 128, FUSED>(a, grid, smem, false, s);
+}
+
+template <int OP, int DK>
+static int regs_one(bool fused) {
+  cudaFuncAttributes fa;
+  const cudaError_t e = fused ? cudaFuncGetAttributes(&fa, pipe_kernel<OP, DK, DK, FUSED>)
+                              : cudaFuncGetAttributes(&fa, pipe_kernel<OP, DK, DK, APPEND>);
+  return e == cudaSuccess ? fa.numRegs : 0;
+}
+
+int append_decode_regs(int op, int dk, bool fused) {
+  if (dk == 64) {
+    if (op == GDN) return regs_one<GDN, 64>(fused);
+    if (op == KDA) return regs_one<KDA, 64>(fused);
+    return regs_one<RWKV6, 64>(fused);
+  }
+  if (op == GDN) return regs_one<GDN, 128>(fused);
+  if (op == KDA) return regs_one<KDA, 128>(fused);
+  return regs_one<RWKV6, 128>(fused);
 }
 
 // The attribute must be set on the kernel instance this translation unit

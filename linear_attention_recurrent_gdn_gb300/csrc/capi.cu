@@ -38,6 +38,7 @@ struct dl_ctx {
   dl_config cfg{};
   cudaStream_t stream = nullptr;
   int device = 0, num_sms = 0, smem_optin = 0, smem_per_sm = 0, l2_bytes = 0;
+  int regs[3] = {0, 0, 0};   // registers per thread: AppendDecode, fused AppendDecode, EagerStep
   dl_table* table = nullptr;
   dl::Layout L{};
   float* Sbar = nullptr;
@@ -129,18 +130,26 @@ void free_all(dl_ctx* c) {
 
 // DL_PIPE_SHAPE="cps,ncw,R" overrides the shape choice (a tuning knob for
 // measurements; shapes that do not fit are ignored).
+// Tuning override of the pipeline shape: DL_PIPE_SHAPE="cps,ncw,R[,npw[,max_na]]".
 const int* shape_override() {
-  static int v[3];
+  static thread_local int v[5];
   const char* e = getenv("DL_PIPE_SHAPE");
-  if (!e || sscanf(e, "%d,%d,%d", &v[0], &v[1], &v[2]) != 3) return nullptr;
+  v[3] = v[4] = 0;
+  if (!e || sscanf(e, "%d,%d,%d,%d,%d", &v[0], &v[1], &v[2], &v[3], &v[4]) < 3) return nullptr;
   return v;
 }
+
+// Prep warps of the fused form: the per-key ops' coefficient work (an
+// exponential per key channel and log entry) takes two warps to keep pace
+// with the value-tile consumers; GDN's scalar decays need one.
+int prep_warps(int op) { return op == DL_GDN ? 1 : 2; }
 
 enum class Kern { Append, Fused, Eager };
 
 dl::PipePlan pipe_shape(const dl_ctx* c, int G, Kern k) {
   const int aux = k == Kern::Append ? c->L.aux_bytes : k == Kern::Fused ? c->L.f_bytes : c->L.e_bytes;
-  return dl::plan_pipeline(c->cfg.d_k, aux, G, c->smem_optin, c->smem_per_sm, shape_override());
+  return dl::plan_pipeline(c->cfg.d_k, aux, G, c->smem_optin, c->smem_per_sm, shape_override(),
+                           k == Kern::Fused ? prep_warps(c->cfg.op) : 1, c->regs[(int)k]);
 }
 
 bool record(dl_ctx* c, int kind, cudaEvent_t* ev) {
@@ -252,6 +261,7 @@ dl_status run_step(dl_ctx* c, const int32_t* slots, int32_t n, const void* q, co
     a.ns = ps.ns;
     a.na = ps.na;
     a.ncw = ps.ncw;
+    a.npw = ps.npw;
     a.tps = dl::tiles_per_stage(f.d_k, a.G);
     // stream the state through L2 unless the whole batch's state fits in 3/4 of it
     a.l2_stream = (double)n * f.num_heads * f.d_v * f.d_k * 4 > 0.75 * c->l2_bytes ? 1 : 0;
@@ -372,6 +382,9 @@ dl_status dl_create(const dl_config* cfg, void* stream, dl_ctx** out) {
     e = dl::configure_append_decode(f.op, f.d_k, smem);
     if (e == cudaSuccess) e = dl::configure_eager_step(f.op, f.d_k, smem);
     if (e != cudaSuccess) { rc = cuda_err(c, e, "kernel attribute"); break; }
+    c->regs[(int)Kern::Append] = dl::append_decode_regs(f.op, f.d_k, false);
+    c->regs[(int)Kern::Fused] = dl::append_decode_regs(f.op, f.d_k, true);
+    c->regs[(int)Kern::Eager] = dl::eager_step_regs(f.op, f.d_k);
   } while (0);
   g_fail_countdown = -1;
   if (rc != DL_OK) {

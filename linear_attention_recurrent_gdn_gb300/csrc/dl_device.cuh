@@ -16,7 +16,8 @@ enum Op : int { GDN = 0, KDA = 1, RWKV6 = 2 };
 
 constexpr int BV = 32;            // value rows per tile (one warp owns one tile)
 constexpr int MAX_NCW = 8;        // consumer warps per AppendDecode / EagerStep CTA (at most)
-constexpr int PIPE_THREADS_MAX = (MAX_NCW + 2) * 32;   // consumers + producer + prep warp
+constexpr int MAX_NPW = 2;        // prep warps per fused AppendDecode CTA (at most)
+constexpr int PIPE_THREADS_MAX = (MAX_NCW + 1 + MAX_NPW) * 32;   // consumers + producer + prep
 constexpr int MAX_ROWS = 1024;    // slot rows per launch (more are split into chunks)
 constexpr int HDR = 8;            // scalar header of a coefficient block (floats)
 constexpr int BAR_BYTES = 1024;   // mbarrier area at the start of the pipelined kernels' shared memory
@@ -54,7 +55,8 @@ struct StepArgs {
   int32_t rows, H, M, Mcap, Mcap4, CB, P0;   // P0: coefficient floats needed on append steps
   int32_t G, NG;         // value tiles per work unit, units per slot-head
   int32_t ns, na;        // pipeline stages (tiles), aux slots
-  int32_t ncw;           // consumer warps per CTA (block = (ncw + 1) warps)
+  int32_t ncw;           // consumer warps per CTA (block = ncw + 1 (+ npw) warps)
+  int32_t npw;           // prep warps of the fused form (divides na)
   int32_t tps;           // value tiles per stage (one bulk copy): 1, or 2 for d_k = 64
   int32_t l2_stream;     // 1: read S̄ with an L2 evict-first policy (state larger than L2 can keep)
   int32_t aux_bytes;     // bytes of one aux slot

@@ -27,6 +27,23 @@ cudaError_t launch_eager_step(int op, int dk, const StepArgs& a, int grid, size_
 }
 
 template <int OP, int DK>
+static int regs_one() {
+  cudaFuncAttributes fa;
+  return cudaFuncGetAttributes(&fa, pipe_kernel<OP, DK, DK, EAGER>) == cudaSuccess ? fa.numRegs : 0;
+}
+
+int eager_step_regs(int op, int dk) {
+  if (dk == 64) {
+    if (op == GDN) return regs_one<GDN, 64>();
+    if (op == KDA) return regs_one<KDA, 64>();
+    return regs_one<RWKV6, 64>();
+  }
+  if (op == GDN) return regs_one<GDN, 128>();
+  if (op == KDA) return regs_one<KDA, 128>();
+  return regs_one<RWKV6, 128>();
+}
+
+template <int OP, int DK>
 static cudaError_t cfg_one(size_t smem) {
   return raise_smem_limit(pipe_kernel<OP, DK, DK, EAGER>, smem);
 }

@@ -37,6 +37,10 @@ inline cudaError_t raise_smem_limit(Kernel* kern, size_t smem) {
 cudaError_t configure_append_decode(int op, int dk, size_t smem);
 cudaError_t configure_eager_step(int op, int dk, size_t smem);
 
+// Registers per thread of the pipelined kernel instances (0 if unknown).
+int append_decode_regs(int op, int dk, bool fused);
+int eager_step_regs(int op, int dk);
+
 // Standalone merge / read-state (S_out == nullptr: write back into S̄ and reset the log).
 cudaError_t launch_merge(int op, int dk, const SlotListArgs& a, cudaStream_t s);
 // Copy initial states into S̄ and reset the listed slots' table entries.

@@ -83,30 +83,39 @@ DL_HD inline Layout make_layout(int op, int M, int dk, int dv) {
 // Shape of the pipelined kernels for one launch: `cps` CTAs per SM, each with
 // `ncw` consumer warps owning `ns / ncw` tile stages apiece and `na` aux slots
 // (at least 2, so the next unit's inputs load while the current one is used).
-// Returns ns = 0 when nothing fits.
+// The fused form adds `npw` prep warps; prep warp w owns the aux slots x with
+// x % npw == w, so na is a multiple of npw.  Returns ns = 0 when nothing fits.
 struct PipePlan {
-  int cps, ncw, ns, na;
+  int cps, ncw, ns, na, npw;
   int smem;   // dynamic shared memory per CTA (bytes)
 };
 
 // Fit one candidate shape (cps CTAs per SM, ncw consumer warps, R stages per
 // warp) into the shared-memory budget; ns = 0 if it does not fit.
 inline PipePlan fit_pipeline(int cps, int ncw, int R, int dk, int aux_bytes, int G, int smem_optin,
-                             int smem_per_sm, int tps = 1) {
+                             int smem_per_sm, int tps = 1, int npw = 1, int regs = 0,
+                             int max_na = 16) {
+  // registers: cps CTAs of (ncw + 1 + npw) warps must be resident together
+  // (64 Ki registers per SM, allocated per warp in multiples of 8 per thread)
+  const int warps = ncw + 1 + (npw > 1 ? npw : 1);
+  if (regs > 0 && (long)cps * warps * 32 * ((regs + 7) / 8 * 8) > 65536L)
+    return PipePlan{0, 0, 0, 0, 0, 0};
   const int tile = 32 * dk * 4 * tps;   // bytes of one stage
   const int per_cta = smem_per_sm / cps - 1024;     // 1 KiB per CTA is reserved
   const int budget = (per_cta < smem_optin ? per_cta : smem_optin) - 1024 - 1024;
   const int ns = ncw * R;
-  const int ipu = G / tps;                         // stage items per unit
-  int na = (ns + ipu - 1) / ipu + 1;
-  if (na > 16) na = 16;
-  long need = (long)ns * tile + (long)na * aux_bytes;
-  while (need > budget && na > 2) {
-    --na;
-    need = (long)ns * tile + (long)na * aux_bytes;
-  }
-  if (ncw < 1 || ncw > 8 || R < 1 || ns > 24 || need > budget) return PipePlan{0, 0, 0, 0, 0};
-  return PipePlan{cps, ncw, ns, na, (int)(1024 + need)};
+  // aux slots: all the shared memory the stages leave, up to 16 (each slot
+  // lets the producer fetch one more unit's inputs ahead of the consumers)
+  const int na_min = npw > 2 ? npw : 2;
+  const long left = (long)budget - (long)ns * tile;
+  int na = left > 0 ? (int)(left / aux_bytes) : 0;
+  if (na > max_na) na = max_na;
+  na = na / npw * npw;
+  const long need = (long)ns * tile + (long)na * aux_bytes;
+  if (na < na_min) return PipePlan{0, 0, 0, 0, 0, 0};
+  if (ncw < 1 || ncw > 8 || R < 1 || ns > 24 || npw < 1 || npw > 2 || na > 24 || need > budget)
+    return PipePlan{0, 0, 0, 0, 0, 0};
+  return PipePlan{cps, ncw, ns, na, npw, (int)(1024 + need)};
 }
 
 // Stages hold one 16 KiB bulk copy: one value tile at d_k = 128, two at d_k = 64
@@ -114,11 +123,12 @@ inline PipePlan fit_pipeline(int cps, int ncw, int R, int dk, int aux_bytes, int
 inline int tiles_per_stage(int dk, int G) { return (dk == 64 && G % 2 == 0) ? 2 : 1; }
 
 inline PipePlan plan_pipeline(int dk, int aux_bytes, int G, int smem_optin, int smem_per_sm,
-                              const int* force = nullptr) {
+                              const int* force = nullptr, int npw = 1, int regs = 0) {
   const int tps = tiles_per_stage(dk, G);
-  if (force) {   // tuning override: {cps, ncw, R}
+  if (force) {   // tuning override: {cps, ncw, R, npw, max_na}
     const PipePlan p = fit_pipeline(force[0], force[1], force[2], dk, aux_bytes, G, smem_optin,
-                                    smem_per_sm, tps);
+                                    smem_per_sm, tps, force[3] > 0 ? force[3] : npw, regs,
+                                    force[4] > 0 ? force[4] : 16);
     if (p.ns > 0) return p;
   }
   // Candidates in order of preference (cps, ncw, R), from read-bandwidth
@@ -132,10 +142,10 @@ inline PipePlan plan_pipeline(int dk, int aux_bytes, int G, int smem_optin, int 
   const int ncand = big ? 5 : 6;
   for (int ci = 0; ci < ncand; ++ci) {
     const PipePlan p = fit_pipeline(cand[ci][0], cand[ci][1], cand[ci][2], dk, aux_bytes, G,
-                                    smem_optin, smem_per_sm, tps);
+                                    smem_optin, smem_per_sm, tps, npw, regs);
     if (p.ns > 0) return p;
   }
-  return PipePlan{0, 0, 0, 0, 0};
+  return PipePlan{0, 0, 0, 0, 0, 0};
 }
 
 }  // namespace dl

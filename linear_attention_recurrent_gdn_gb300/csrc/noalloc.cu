@@ -187,6 +187,7 @@ extern "C" dl_status dl_step_noalloc(const dl_config* cfg, const dl_state_view* 
   a.ns = sh.ns;
   a.na = sh.na;
   a.ncw = sh.ncw;
+  a.npw = sh.npw;
   a.tps = dl::tiles_per_stage(f.d_k, a.G);
   a.l2_stream = (double)n * f.num_heads * f.d_v * f.d_k * 4 > 0.75 * d.l2_bytes ? 1 : 0;
   const long units = n_sh * a.NG;

@@ -716,10 +716,14 @@ __global__ void __launch_bounds__(PIPE_THREADS_MAX, 1) pipe_kernel(const __grid_
     return;
   }
 
-  if (MODE == FUSED && warp == NCWr + 1) {
+  if (MODE == FUSED && warp > NCWr) {
     // ------------------------------------------------- fused ReplayPrep stage
+    // Prep warp pw owns the aux slots x with x % npw == pw and takes their
+    // units in order, so it waits on every phase of those slots' barriers.
+    const int pw = warp - NCWr - 1, NPW = a.npw;
     for (int kk = 0; kk < my_units; ++kk) {
       const int x = kk % NA;
+      if (x % NPW != pw) continue;
       if (!__all_sync(0xffffffffu, mbar_wait(bars.afull(x), (kk / NA) & 1, a.status, DEV_TIMEOUT_AUX)))
         break;
       const UnitPos p = unit_pos(a, (int)blockIdx.x + kk * (int)gridDim.x);

@@ -46,7 +46,7 @@ class Bar:
 
 
 def simulate(NS, NA, G, n_tiles, owned, tile_first, seed, p_complete=0.03, lifo=0.95,
-             fused=False, ncw=NCW):
+             fused=False, ncw=NCW, npw=1, prep_by_unit=False):
     NCW_ = ncw
     rng = random.Random(seed)
     R = NS // NCW_
@@ -63,20 +63,25 @@ def simulate(NS, NA, G, n_tiles, owned, tile_first, seed, p_complete=0.03, lifo=
     cready = [Bar(1) for _ in range(NA)]   # fused form: the prep warp's signal
     inflight, violations = [], []
     prod = {"ti": 0, "ka": 0}
-    prep = {"k": 0}
+    # prep warp pw owns the aux slots x with x % npw == pw (npw divides NA) and
+    # takes their units in order, so it sees every phase of those slots
+    n_units = n_tiles // G
+    prep = [{"ks": [k for k in range(n_units)
+                    if (k % npw if prep_by_unit else (k % NA) % npw) == pw], "j": 0}
+            for pw in range(npw)]
     cons = [{"i": w, "step": 0} for w in range(NCW_)]
     n_units = n_tiles // G
 
-    def prep_warp():
-        k = prep["k"]
-        if k >= n_units:
+    def prep_warp(pw):
+        if prep[pw]["j"] >= len(prep[pw]["ks"]):
             return
+        k = prep[pw]["ks"][prep[pw]["j"]]
         x = k % NA
         if afull[x].try_wait((k // NA) & 1):
             if afull[x].done <= k // NA:
                 violations.append(("prep", k))
             cready[x].arrive()
-            prep["k"] += 1
+            prep[pw]["j"] += 1
 
     def producer():
         ti, ka = prod["ti"], prod["ka"]
@@ -126,7 +131,7 @@ def simulate(NS, NA, G, n_tiles, owned, tile_first, seed, p_complete=0.03, lifo=
             elif r < p_complete + 0.2:
                 producer()
             elif fused and r < p_complete + 0.3:
-                prep_warp()
+                prep_warp(rng.randrange(npw))
             else:
                 consumer(rng.randrange(NCW_))
             if prod["ti"] >= n_tiles and all(c["i"] >= n_tiles for c in cons):
@@ -153,6 +158,28 @@ def test_fused_prep_stage_is_safe(ncw, NS, NA, G):
         v, finished = simulate(NS, NA, G, 8 * 4 * 5, owned=True, tile_first=True, seed=seed,
                                fused=True, ncw=ncw)
         assert not v and finished, (seed, v[:3])
+
+
+@pytest.mark.parametrize("npw,ncw,NS,NA,G", [(2, 4, 4, 2, 1), (2, 4, 4, 4, 1), (3, 3, 3, 6, 2),
+                                              (2, 4, 8, 2, 4), (4, 4, 4, 8, 1), (1, 4, 4, 12, 4),
+                                              (2, 4, 4, 16, 1), (1, 3, 3, 16, 4)])
+def test_fused_several_prep_warps_is_safe(npw, ncw, NS, NA, G):
+    """Several prep warps, each owning the aux slots x with x % npw == pw."""
+    for seed in range(12):
+        v, finished = simulate(NS, NA, G, 8 * 4 * 5, owned=True, tile_first=True, seed=seed,
+                               fused=True, ncw=ncw, npw=npw)
+        assert not v and finished, (seed, v[:3])
+
+
+def test_prep_warps_taking_every_npw_th_unit_is_caught():
+    """Negative control: prep warps that take units pw, pw+npw, ... can wait on a
+    slot whose earlier phase they never saw; the parity test then passes early."""
+    caught = 0
+    for seed in range(6):
+        v, finished = simulate(4, 3, 1, 8 * 4 * 5, owned=True, tile_first=True, seed=seed,
+                               fused=True, ncw=4, npw=2, prep_by_unit=True)
+        caught += bool(v) or not finished
+    assert caught >= 3
 
 
 @pytest.mark.parametrize("ncw,NS,NA,G", [(4, 4, 2, 4), (3, 3, 2, 4), (4, 8, 3, 2)])
