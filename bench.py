@@ -326,21 +326,33 @@ def run_ours(args):
             c.set_bonus(bonus)
         return c
 
-    def decode_run(c, eager=False):
+    def decode_run(c, eager=False, wins=None):
+        if wins:
+            for win in wins:
+                win.launch()
+            return
         fn = c.step_eager if eager else c.step
         for t in range(T):
             fn(slots, x["q"][t], x["k"][t], x["v"][t], x["g"][t],
                x["beta"][t] if x["beta"] is not None else None, out[t])
 
-    def timed(c, steps, warmup, eager=False):
+    def make_windows(c, m):
+        """The decode loop as CUDA graphs: one captured window per M tokens."""
+        if args.no_graph or T % m:
+            return None
+        sl = lambda key, j: x[key][j * m:(j + 1) * m] if x[key] is not None else None
+        return [c.window(slots, sl("q", j), sl("k", j), sl("v", j), sl("g", j), sl("beta", j),
+                         out[j * m:(j + 1) * m]) for j in range(T // m)]
+
+    def timed(c, steps, warmup, eager=False, wins=None):
         for _ in range(warmup):
-            decode_run(c, eager)
+            decode_run(c, eager, wins)
         barrier(dist)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(steps):
-            decode_run(c, eager)
+            decode_run(c, eager, wins)
         e1.record(stream)
         e1.synchronize()
         torch.cuda.synchronize()
@@ -353,14 +365,17 @@ def run_ours(args):
     if args.eager:
         M = 1
     ctx = make_ctx(M)
+    wins = None if args.eager else make_windows(ctx, M)
     with ClockSampler(local) as clk:
-        ms = timed(ctx, args.steps, args.warmup, eager=args.eager)
+        ms = timed(ctx, args.steps, args.warmup, eager=args.eager, wins=wins)
     ms_max = reduce_max(dist, ms, dev)
     value = units_per_step * world / (ms_max / 1e3)
     fused = args.staging == "fused" and not args.eager
     launches = (1 if (fused or args.eager) else 2) * T * args.steps * ((B + 1023) // 1024)
+    for win in wins or []:
+        win.close()
 
-    # ---- per-kernel times (instrumented pass: events around every launch)
+    # ---- per-kernel times (instrumented pass, token by token: events around every launch)
     ctx.set_timing(True)
     decode_run(ctx, eager=args.eager)
     kms, kcnt = ctx.get_timing()
@@ -378,6 +393,11 @@ def run_ours(args):
         wr_all += c_ * B * H
     ad_ms = kms[1] / max(kcnt[1], 1)
     rp_ms = kms[0] / max(kcnt[0], 1)
+    stepping_ms = ad_ms
+    if fused and wins:
+        # one launch per token in the graphs: the launch time is the token time
+        # (inter-launch gaps included, so this never overstates the kernel)
+        ad_ms = ms_max / T
     kernel_name = "AppendDecode (ReplayPrep fused)" if fused else "AppendDecode"
     if args.eager:
         eb_, ew_ = eager_bytes(op, d)
@@ -402,7 +422,9 @@ def run_ours(args):
         "config": {"workload": w["desc"] + (", eager dense step" if args.eager
                                             else ", merge interval M=%d" % M),
                    "op": gen.OP_NAMES[op], "B": B, "H": H, "d_k": d, "d_v": d, "tokens": T,
-                   "M": M, "staging": args.staging, "inputs": "bf16 q/k/v, fp32 g/beta, bf16 o",
+                   "M": M, "staging": args.staging,
+                   "loop": "CUDA graphs, one per M tokens (dl_window)" if wins else "dl_step per token",
+                   "inputs": "bf16 q/k/v, fp32 g/beta, bf16 o",
                    "l2": "inputs larger than L2 (fp32 state %d MiB per rank)"
                          % (B * H * d * d * 4 >> 20),
                    "parallelism": "replicas/batch shards x%d" % world},
@@ -415,7 +437,10 @@ def run_ours(args):
                          "append_decode_fused" if fused else "append_decode",
                          gen.OP_NAMES[op], B, H, d, M)),
                      "kernel": kernel_name, "peak_source": peak_src + " hbm_gbs",
-                     "bytes_per_launch": ad_b / T, "ms_per_launch": ad_ms},
+                     "bytes_per_launch": ad_b / T, "ms_per_launch": ad_ms,
+                     "timing": ("token time in the graph-captured decode loop" if fused and wins
+                                else "CUDA events around each launch"),
+                     "ms_per_launch_stepping": stepping_ms},
         "kernels_ms_per_token": ({"EagerStep": ad_ms} if args.eager else
                                  {"AppendDecode (ReplayPrep fused)": ad_ms} if fused else
                                  {"ReplayPrep": rp_ms, "AppendDecode": ad_ms}),
@@ -429,8 +454,11 @@ def run_ours(args):
         sweep = {}
         for m in (1, 4, 8, 16, 32):
             c = make_ctx(m)
-            sms = reduce_max(dist, timed(c, 2, 1), dev)
+            ws = make_windows(c, m)
+            sms = reduce_max(dist, timed(c, 2, 1, wins=ws), dev)
             sweep[str(m)] = units_per_step * world / (sms / 1e3)
+            for win in ws or []:
+                win.close()
             c.close()
         c = make_ctx(1)
         ems = reduce_max(dist, timed(c, 2, 1, eager=True), dev)
@@ -577,6 +605,8 @@ def main():
     ap.add_argument("--B", type=int, default=0, help="override the batch (profiling runs only)")
     ap.add_argument("--tokens", type=int, default=0, help="override the token count (profiling)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time the decode loop as one dl_step call per token instead of CUDA graphs")
     ap.add_argument("--staging", default="fused", choices=["fused", "kernels"],
                     help="ReplayPrep as a warp role of AppendDecode (fused) or its own kernel")
     ap.add_argument("--eager", action="store_true",

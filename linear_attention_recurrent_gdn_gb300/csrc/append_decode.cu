@@ -15,7 +15,7 @@ static cudaError_t launch_ad(const StepArgs& a, int grid, size_t smem, bool pdl,
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = (pdl && MODE == APPEND) ? 1 : 0;
+  cfg.numAttrs = (pdl && MODE != EAGER) ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, pipe_kernel<OP, DK, DK, MODE>, a);
 }
 
@@ -33,16 +33,16 @@ cudaError_t launch_append_decode(int op, int dk, const StepArgs& a, int grid, si
 }
 
 cudaError_t launch_append_decode_fused(int op, int dk, const StepArgs& a, int grid, size_t smem,
-                                       cudaStream_t s) {
+                                       bool pdl, cudaStream_t s) {
   if (a.rows <= 0) return cudaSuccess;
   if (dk == 64) {
-    if (op == GDN) return launch_ad<GDN, 64, FUSED>(a, grid, smem, false, s);
-    if (op == KDA) return launch_ad<KDA, 64, FUSED>(a, grid, smem, false, s);
-    return launch_ad<RWKV6, 64, FUSED>(a, grid, smem, false, s);
+    if (op == GDN) return launch_ad<GDN, 64, FUSED>(a, grid, smem, pdl, s);
+    if (op == KDA) return launch_ad<KDA, 64, FUSED>(a, grid, smem, pdl, s);
+    return launch_ad<RWKV6, 64, FUSED>(a, grid, smem, pdl, s);
   }
-  if (op == GDN) return launch_ad<GDN, 128, FUSED>(a, grid, smem, false, s);
-  if (op == KDA) return launch_ad<KDA, 128, FUSED>(a, grid, smem, false, s);
-  return launch_ad<RWKV6, 128, FUSED>(a, grid, smem, false, s);
+  if (op == GDN) return launch_ad<GDN, 128, FUSED>(a, grid, smem, pdl, s);
+  if (op == KDA) return launch_ad<KDA, 128, FUSED>(a, grid, smem, pdl, s);
+  return launch_ad<RWKV6, 128, FUSED>(a, grid, smem, pdl, s);
 }
 
 template <int OP, int DK>

@@ -39,6 +39,10 @@ struct dl_ctx {
   cudaStream_t stream = nullptr;
   int device = 0, num_sms = 0, smem_optin = 0, smem_per_sm = 0, l2_bytes = 0;
   int regs[3] = {0, 0, 0};   // registers per thread: AppendDecode, fused AppendDecode, EagerStep
+  // Set while a decode window is captured, from its second step on: the step
+  // launches as a programmatic dependent of the previous step (both ours) and
+  // may stream dense-base tiles of rows with a non-empty log before it waits.
+  int pdl_chain = 0;
   dl_table* table = nullptr;
   dl::Layout L{};
   float* Sbar = nullptr;
@@ -134,22 +138,30 @@ void free_all(dl_ctx* c) {
 const int* shape_override() {
   static thread_local int v[5];
   const char* e = getenv("DL_PIPE_SHAPE");
-  v[3] = v[4] = 0;
+  v[3] = -1;
+  v[4] = 0;
   if (!e || sscanf(e, "%d,%d,%d,%d,%d", &v[0], &v[1], &v[2], &v[3], &v[4]) < 3) return nullptr;
   return v;
 }
 
-// Prep warps of the fused form: the per-key ops' coefficient work (an
-// exponential per key channel and log entry) takes two warps to keep pace
-// with the value-tile consumers; GDN's scalar decays need one.
-int prep_warps(int op) { return op == DL_GDN ? 1 : 2; }
+// Prep warps of the fused form.  A unit that is a single stage is handled by
+// one consumer warp, which computes the unit's coefficients itself (0 prep
+// warps: no hand-off between warps).  Units spread over several consumer
+// warps share one prep warp's work: the per-key ops' coefficients (an
+// exponential per key channel and log entry) take two warps to keep pace with
+// the value-tile consumers; GDN's scalar decays need one.
+int prep_warps(int op, int dk, int G) {
+  if (G / dl::tiles_per_stage(dk, G) == 1) return 0;
+  return op == DL_GDN ? 1 : 2;
+}
 
 enum class Kern { Append, Fused, Eager };
 
 dl::PipePlan pipe_shape(const dl_ctx* c, int G, Kern k) {
   const int aux = k == Kern::Append ? c->L.aux_bytes : k == Kern::Fused ? c->L.f_bytes : c->L.e_bytes;
   return dl::plan_pipeline(c->cfg.d_k, aux, G, c->smem_optin, c->smem_per_sm, shape_override(),
-                           k == Kern::Fused ? prep_warps(c->cfg.op) : 1, c->regs[(int)k]);
+                           k == Kern::Fused ? prep_warps(c->cfg.op, c->cfg.d_k, G) : -1,
+                           c->regs[(int)k]);
 }
 
 bool record(dl_ctx* c, int kind, cudaEvent_t* ev) {
@@ -275,7 +287,9 @@ dl_status run_step(dl_ctx* c, const int32_t* slots, int32_t n, const void* q, co
       if (t) record_end(c, 2, e0);
     } else if (fused) {
       const bool t = record(c, 1, &e0);
-      DL_CUDA(dl::launch_append_decode_fused(f.op, f.d_k, a, grid, ps.smem, c->stream),
+      a.pdl_prefetch = c->pdl_chain;
+      DL_CUDA(dl::launch_append_decode_fused(f.op, f.d_k, a, grid, ps.smem, c->pdl_chain != 0,
+                                             c->stream),
               "AppendDecode launch");
       if (t) record_end(c, 1, e0);
     } else {
@@ -785,6 +799,7 @@ dl_status dl_window_create(dl_ctx* c, const int32_t* slots, int32_t n, const voi
   dl_status st = DL_OK;
   if (e == cudaSuccess) {
     for (int j = 0; j < M && st == DL_OK; ++j) {
+      c->pdl_chain = (j > 0 && f.staging == DL_STAGE_FUSED) ? 1 : 0;
       for (int32_t i = 0; i < n; ++i) {
         c->plan[4 * (size_t)i + 0] = slots[i];
         c->plan[4 * (size_t)i + 1] = slots[i];
@@ -804,6 +819,7 @@ dl_status dl_window_create(dl_ctx* c, const int32_t* slots, int32_t n, const voi
   }
   c->stream = saved;
   c->timing = saved_timing;
+  c->pdl_chain = 0;
   cudaStreamDestroy(cap);
   if (st != DL_OK) {
     if (w->graph) cudaGraphDestroy(w->graph);

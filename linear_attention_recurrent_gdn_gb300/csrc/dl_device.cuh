@@ -59,6 +59,8 @@ struct StepArgs {
   int32_t npw;           // prep warps of the fused form (divides na)
   int32_t tps;           // value tiles per stage (one bulk copy): 1, or 2 for d_k = 64
   int32_t l2_stream;     // 1: read S̄ with an L2 evict-first policy (state larger than L2 can keep)
+  int32_t pdl_prefetch;  // 1: the previous launch on the stream was a step of this context, so
+                         //    tiles of rows with n > 0 may stream before griddepcontrol.wait
   int32_t aux_bytes;     // bytes of one aux slot
   int32_t out_bf16;
   float scale;

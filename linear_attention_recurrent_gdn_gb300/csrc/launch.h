@@ -13,9 +13,11 @@ cudaError_t launch_replay_prep(int op, int dk, const StepArgs& a, cudaStream_t s
 cudaError_t launch_append_decode(int op, int dk, const StepArgs& a, int grid, size_t smem,
                                  bool pdl, cudaStream_t s);
 
-// AppendDecode with the ReplayPrep stage fused in as a warp role (no ReplayPrep launch).
+// AppendDecode with the ReplayPrep stage fused in as a warp role (no ReplayPrep
+// launch).  `pdl` launches it as a programmatic dependent of the preceding
+// kernel in the stream (the previous step).
 cudaError_t launch_append_decode_fused(int op, int dk, const StepArgs& a, int grid, size_t smem,
-                                       cudaStream_t s);
+                                       bool pdl, cudaStream_t s);
 
 // EagerStep: the dense read-modify-write step (the comparison kernel).
 cudaError_t launch_eager_step(int op, int dk, const StepArgs& a, int grid, size_t smem,

@@ -84,38 +84,47 @@ DL_HD inline Layout make_layout(int op, int M, int dk, int dv) {
 // `ncw` consumer warps owning `ns / ncw` tile stages apiece and `na` aux slots
 // (at least 2, so the next unit's inputs load while the current one is used).
 // The fused form adds `npw` prep warps; prep warp w owns the aux slots x with
-// x % npw == w, so na is a multiple of npw.  Returns ns = 0 when nothing fits.
+// x % npw == w, so na is a multiple of npw.  With npw = 0 (one-stage units)
+// each consumer warp computes its units' coefficients itself and owns the aux
+// slots x with x % ncw == w, so na is a multiple of ncw.  Returns ns = 0 when
+// nothing fits.
 struct PipePlan {
   int cps, ncw, ns, na, npw;
   int smem;   // dynamic shared memory per CTA (bytes)
 };
 
 // Fit one candidate shape (cps CTAs per SM, ncw consumer warps, R stages per
-// warp) into the shared-memory budget; ns = 0 if it does not fit.
+// warp) into the shared-memory budget; ns = 0 if it does not fit.  `npw` is
+// the number of prep warps (-1: none, the two-kernel and eager forms).
 inline PipePlan fit_pipeline(int cps, int ncw, int R, int dk, int aux_bytes, int G, int smem_optin,
-                             int smem_per_sm, int tps = 1, int npw = 1, int regs = 0,
+                             int smem_per_sm, int tps = 1, int npw = -1, int regs = 0,
                              int max_na = 16) {
-  // registers: cps CTAs of (ncw + 1 + npw) warps must be resident together
-  // (64 Ki registers per SM, allocated per warp in multiples of 8 per thread)
-  const int warps = ncw + 1 + (npw > 1 ? npw : 1);
-  if (regs > 0 && (long)cps * warps * 32 * ((regs + 7) / 8 * 8) > 65536L)
-    return PipePlan{0, 0, 0, 0, 0, 0};
+  const PipePlan none{0, 0, 0, 0, 0, 0};
+  if (ncw < 1 || ncw > 8 || R < 1 || npw > 2) return none;
+  if (npw == 0 && G / tps != 1) return none;   // consumer prep needs one-stage units
+  // registers: cps CTAs of (ncw + 1 + npw) warps must be resident together.
+  // Each of the SM's 4 sub-partitions holds 16 Ki registers, allocated per
+  // warp in multiples of 8 per thread; a warp lives on one sub-partition.
+  const int warps = ncw + 1 + (npw > 0 ? npw : 0);
+  if (regs > 0) {
+    const int per_sub = 16384 / (32 * ((regs + 7) / 8 * 8));
+    if (cps * warps > 4 * per_sub) return none;
+  }
   const int tile = 32 * dk * 4 * tps;   // bytes of one stage
   const int per_cta = smem_per_sm / cps - 1024;     // 1 KiB per CTA is reserved
   const int budget = (per_cta < smem_optin ? per_cta : smem_optin) - 1024 - 1024;
   const int ns = ncw * R;
-  // aux slots: all the shared memory the stages leave, up to 16 (each slot
+  // aux slots: all the shared memory the stages leave, up to max_na (each slot
   // lets the producer fetch one more unit's inputs ahead of the consumers)
-  const int na_min = npw > 2 ? npw : 2;
+  const int mult = npw > 0 ? npw : npw == 0 ? ncw : 1;
+  const int na_min = mult > 2 ? mult : 2;
   const long left = (long)budget - (long)ns * tile;
   int na = left > 0 ? (int)(left / aux_bytes) : 0;
   if (na > max_na) na = max_na;
-  na = na / npw * npw;
+  na = na / mult * mult;
   const long need = (long)ns * tile + (long)na * aux_bytes;
-  if (na < na_min) return PipePlan{0, 0, 0, 0, 0, 0};
-  if (ncw < 1 || ncw > 8 || R < 1 || ns > 24 || npw < 1 || npw > 2 || na > 24 || need > budget)
-    return PipePlan{0, 0, 0, 0, 0, 0};
-  return PipePlan{cps, ncw, ns, na, npw, (int)(1024 + need)};
+  if (na < na_min || ns > 24 || na > 24 || need > budget) return none;
+  return PipePlan{cps, ncw, ns, na, npw > 0 ? npw : 0, (int)(1024 + need)};
 }
 
 // Stages hold one 16 KiB bulk copy: one value tile at d_k = 128, two at d_k = 64
@@ -123,23 +132,29 @@ inline PipePlan fit_pipeline(int cps, int ncw, int R, int dk, int aux_bytes, int
 inline int tiles_per_stage(int dk, int G) { return (dk == 64 && G % 2 == 0) ? 2 : 1; }
 
 inline PipePlan plan_pipeline(int dk, int aux_bytes, int G, int smem_optin, int smem_per_sm,
-                              const int* force = nullptr, int npw = 1, int regs = 0) {
+                              const int* force = nullptr, int npw = -1, int regs = 0) {
   const int tps = tiles_per_stage(dk, G);
-  if (force) {   // tuning override: {cps, ncw, R, npw, max_na}
+  if (force) {   // tuning override: {cps, ncw, R, npw (-1: default), max_na (0: default)}
     const PipePlan p = fit_pipeline(force[0], force[1], force[2], dk, aux_bytes, G, smem_optin,
-                                    smem_per_sm, tps, force[3] > 0 ? force[3] : npw, regs,
+                                    smem_per_sm, tps, force[3] >= 0 ? force[3] : npw, regs,
                                     force[4] > 0 ? force[4] : 16);
     if (p.ns > 0) return p;
   }
-  // Candidates in order of preference (cps, ncw, R), from read-bandwidth
-  // measurements of this pipeline shape on GB300: two CTAs per SM with one
-  // 16 KiB stage per consumer warp stream best; 8 KiB stages (d_k = 64 with
-  // one tile per unit) need more stages per warp.
+  // Candidates in order of preference (cps, ncw, R), from measurements of
+  // these shapes on GB300.  Two CTAs per SM with one 16 KiB stage per consumer
+  // warp stream best for the two-kernel and eager forms; the fused form does
+  // better still with four CTAs of two consumer warps where their aux slots
+  // fit (more producers, and more units whose coefficients are computed at
+  // once).  8 KiB stages (d_k = 64 with one tile per unit) need more stages
+  // per warp.
   static const int c16k[][3] = {{2, 4, 1}, {2, 3, 1}, {1, 8, 1}, {1, 6, 1}, {1, 4, 1}};
+  static const int c16k_fused[][3] = {{4, 2, 1}, {2, 4, 1}, {3, 2, 1}, {2, 3, 1}, {1, 8, 1},
+                                      {1, 4, 1}};
   static const int c8k[][3] = {{2, 4, 3}, {2, 4, 2}, {2, 3, 2}, {1, 8, 2}, {1, 8, 1}, {1, 4, 1}};
   const bool big = 32 * dk * 4 * tps >= 16384;
-  const int (*cand)[3] = big ? c16k : c8k;
-  const int ncand = big ? 5 : 6;
+  const bool fused = npw >= 0;
+  const int (*cand)[3] = !big ? c8k : fused ? c16k_fused : c16k;
+  const int ncand = !big ? 6 : fused ? 6 : 5;
   for (int ci = 0; ci < ncand; ++ci) {
     const PipePlan p = fit_pipeline(cand[ci][0], cand[ci][1], cand[ci][2], dk, aux_bytes, G,
                                     smem_optin, smem_per_sm, tps, npw, regs);

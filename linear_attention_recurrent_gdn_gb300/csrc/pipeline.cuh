@@ -601,7 +601,7 @@ __device__ __forceinline__ void consume_eager(const StepArgs& a, const Layout& L
 
 // ----------------------------------------------------------------- kernel ---
 template <int OP, int DK, int DV, int MODE>
-__global__ void __launch_bounds__(PIPE_THREADS_MAX, 1) pipe_kernel(const __grid_constant__ StepArgs a) {
+__global__ void __maxnreg__(128) pipe_kernel(const __grid_constant__ StepArgs a) {
   extern __shared__ __align__(1024) unsigned char smem[];
   constexpr uint32_t TILE_BYTES = BV * DK * 4;
   const Layout Lay = make_layout(OP, a.M, DK, DV);
@@ -640,22 +640,47 @@ __global__ void __launch_bounds__(PIPE_THREADS_MAX, 1) pipe_kernel(const __grid_
     // The whole warp runs this loop (uniform control flow); lane 0 also
     // issues the tile bulk copies.
     const uint64_t pol = a.l2_stream ? policy_evict_first() : policy_evict_normal();
-    bool primary_done = (MODE != APPEND);
-    int pending_from = 0;   // units [pending_from, ka) still need their coefficient copy
+    // APPEND and FUSED launch as programmatic dependents (of ReplayPrep, of the
+    // previous step).  Before griddepcontrol.wait the producer only claims aux
+    // slots and streams tiles: APPEND copies the inputs that ReplayPrep does
+    // not write; FUSED copies no inputs at all, and streams only tiles of rows
+    // whose log is non-empty (a.pdl_prefetch), whose dense base the previous
+    // step did not write (only merge rows write it, and they restart at n = 0).
+    bool primary_done = (MODE == EAGER);
+    int pending_from = 0;   // units [pending_from, ka) still need their deferred copies
     int ti = 0, ka = 0;
     bool ok = true;
+    auto issue_pending = [&]() {
+      for (int u = pending_from; u < ka; ++u) {
+        const UnitPos p = unit_pos(a, (int)blockIdx.x + u * (int)gridDim.x);
+        unsigned char* ax = auxm + (size_t)(u % NA) * aux_bytes;
+        if constexpr (MODE == APPEND) {
+          issue_coef_and_arrive<OP, DK, DV>(a, Lay, p, ax, bars.afull(u % NA), lane);
+        } else {
+          issue_aux<OP, DK, DV, MODE>(a, Lay, p, ax, lane);
+          cp_async_arrive_noinc(bars.afull(u % NA));
+        }
+      }
+      pending_from = ka;
+    };
     while (ti < my_tiles) {
       const int kt = ti / IPU;
-      if (!primary_done && (ti >= NS || (kt == ka && ka >= NA))) {
-        // the next wait needs consumers to make progress, and they need coefficients
-        pdl_wait_primary();
-        primary_done = true;
-        for (int u = pending_from; u < ka; ++u) {
-          const UnitPos p = unit_pos(a, (int)blockIdx.x + u * (int)gridDim.x);
-          issue_coef_and_arrive<OP, DK, DV>(a, Lay, p, auxm + (size_t)(u % NA) * aux_bytes,
-                                            bars.afull(u % NA), lane);
+      if (!primary_done) {
+        // the next wait needs consumers to make progress, and they need inputs
+        bool need = ti >= NS || (kt == ka && ka >= NA);
+        if constexpr (MODE == FUSED) {
+          if (!need && !a.pdl_prefetch) need = true;
+          if (!need && a.items[unit_pos(a, (int)blockIdx.x + kt * (int)gridDim.x).row].n == 0)
+            need = true;
         }
-        pending_from = ka;
+        if (need) {
+          pdl_wait_primary();
+          primary_done = true;
+          if constexpr (MODE == FUSED) {
+            if (lane == 0) pdl_launch_dependents();   // the next step may start its prologue
+          }
+          issue_pending();
+        }
       }
       if (kt == ka) {
         const int x = ka % NA;
@@ -666,13 +691,20 @@ __global__ void __launch_bounds__(PIPE_THREADS_MAX, 1) pipe_kernel(const __grid_
         }
         const UnitPos p = unit_pos(a, (int)blockIdx.x + ka * (int)gridDim.x);
         unsigned char* ax = auxm + (size_t)x * aux_bytes;
-        issue_aux<OP, DK, DV, MODE>(a, Lay, p, ax, lane);
         if constexpr (MODE == APPEND) {
+          issue_aux<OP, DK, DV, MODE>(a, Lay, p, ax, lane);
           if (primary_done) {
             issue_coef_and_arrive<OP, DK, DV>(a, Lay, p, ax, bars.afull(x), lane);
             pending_from = ka + 1;
           }
+        } else if constexpr (MODE == FUSED) {
+          if (primary_done) {
+            issue_aux<OP, DK, DV, MODE>(a, Lay, p, ax, lane);
+            cp_async_arrive_noinc(bars.afull(x));
+            pending_from = ka + 1;
+          }
         } else {
+          issue_aux<OP, DK, DV, MODE>(a, Lay, p, ax, lane);
           cp_async_arrive_noinc(bars.afull(x));
         }
         ++ka;
@@ -699,11 +731,11 @@ __global__ void __launch_bounds__(PIPE_THREADS_MAX, 1) pipe_kernel(const __grid_
     }
     if (ok && !primary_done) {
       pdl_wait_primary();
-      for (int u = pending_from; u < ka; ++u) {
-        const UnitPos p = unit_pos(a, (int)blockIdx.x + u * (int)gridDim.x);
-        issue_coef_and_arrive<OP, DK, DV>(a, Lay, p, auxm + (size_t)(u % NA) * aux_bytes,
-                                          bars.afull(u % NA), lane);
+      primary_done = true;
+      if constexpr (MODE == FUSED) {
+        if (lane == 0) pdl_launch_dependents();
       }
+      issue_pending();
     }
     if (!ok) {
       // an error was recorded: let the copies already in flight land before exiting
@@ -715,6 +747,10 @@ __global__ void __launch_bounds__(PIPE_THREADS_MAX, 1) pipe_kernel(const __grid_
     cp_async_wait_all();
     return;
   }
+
+  // Everything below reads or writes global memory only after the previous
+  // step (the primary grid) has completed.
+  if constexpr (MODE == FUSED) pdl_wait_primary();
 
   if (MODE == FUSED && warp > NCWr) {
     // ------------------------------------------------- fused ReplayPrep stage
@@ -748,14 +784,30 @@ __global__ void __launch_bounds__(PIPE_THREADS_MAX, 1) pipe_kernel(const __grid_
       if (OP == GDN) g_s = a.g[p.sh];
       if (OP != RWKV6) beta_s = a.beta[p.sh];
     }
-    // The tile first: it is issued after its unit's aux copies, so once it has
-    // landed the aux barrier is in this unit's phase and the parity test below
-    // is unambiguous.
-    bool ok = mbar_wait(bars.full(s), stage_parity(i, R, NCWr), a.status, DEV_TIMEOUT_TILE);
-    ok = ok && mbar_wait(MODE == FUSED ? bars.cready(x) : bars.afull(x), (kk / NA) & 1, a.status,
-                         DEV_TIMEOUT_AUX);
-    if (!__all_sync(0xffffffffu, ok)) break;
     unsigned char* ax = auxm + (size_t)x * aux_bytes;
+    bool ok;
+    if (MODE == FUSED && a.npw == 0) {
+      // One-stage units, no prep warps: this warp owns aux slot x (na is a
+      // multiple of ncw, so every unit of the slot is this warp's) and has
+      // seen each earlier phase of its barrier itself, so it can wait for the
+      // unit's inputs first and compute the coefficients while the tile is
+      // still landing.
+      ok = mbar_wait(bars.afull(x), (kk / NA) & 1, a.status, DEV_TIMEOUT_AUX);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      if (a.M - 1 <= 8) prep_unit<OP, DK, DV, 8>(a, Lay, p, ax, lane);
+      else if (a.M - 1 <= 16) prep_unit<OP, DK, DV, 16>(a, Lay, p, ax, lane);
+      else prep_unit<OP, DK, DV, 32>(a, Lay, p, ax, lane);
+      __syncwarp();
+      ok = mbar_wait(bars.full(s), stage_parity(i, R, NCWr), a.status, DEV_TIMEOUT_TILE);
+    } else {
+      // The tile first: it is issued after its unit's aux copies, so once it
+      // has landed the aux barrier is in this unit's phase and the parity test
+      // below is unambiguous.
+      ok = mbar_wait(bars.full(s), stage_parity(i, R, NCWr), a.status, DEV_TIMEOUT_TILE);
+      ok = ok && mbar_wait(MODE == FUSED ? bars.cready(x) : bars.afull(x), (kk / NA) & 1, a.status,
+                           DEV_TIMEOUT_AUX);
+    }
+    if (!__all_sync(0xffffffffu, ok)) break;
     bool released = false;
     for (int t = 0; t < TPS; ++t) {
       const float* T = tiles + ((size_t)s * TPS + t) * BV * DK;

@@ -134,6 +134,41 @@ def test_graph_window_matches_stepping_bitwise(op):
     win.close()
 
 
+@pytest.mark.parametrize("op,B,H,d", [(gen.GDN, 96, 32, 128), (gen.KDA, 64, 32, 128),
+                                      (gen.RWKV6, 128, 40, 64)])
+def test_graph_window_many_units_bitwise(op, B, H, d):
+    """Windows at a size where every CTA streams many work units: from the
+    second token of a window on, each step launches as a programmatic
+    dependent of the previous one and streams dense-base tiles before it waits
+    for it.  Two windows back to back must give the bits of plain stepping."""
+    from linear_attention_recurrent_gdn_gb300 import deltalog as dl
+    M, W = 8, 2
+    T = M * W
+    x, S0, bonus = make_case(op, B, H, d, T, seed=650 + op, device="cuda")
+    slots = list(range(B))
+    a = dl.DeltaLog(op, B, H, d, d, M)
+    b = dl.DeltaLog(op, B, H, d, d, M)
+    for c in (a, b):
+        c.set_state(slots, S0)
+        if bonus is not None:
+            c.set_bonus(bonus)
+    ref = torch.empty((T, B, H, d), dtype=torch.bfloat16, device="cuda")
+    for t in range(T):
+        beta = x["beta"][t] if x["beta"] is not None else None
+        a.step(slots, x["q"][t], x["k"][t], x["v"][t], x["g"][t], beta, ref[t])
+    out = torch.empty_like(ref)
+    sl = lambda key, j: x[key][j * M:(j + 1) * M] if x[key] is not None else None
+    wins = [b.window(slots, sl("q", j), sl("k", j), sl("v", j), sl("g", j), sl("beta", j),
+                     out[j * M:(j + 1) * M]) for j in range(W)]
+    for w in wins:
+        w.launch()
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    assert torch.equal(a.read_state(slots), b.read_state(slots))
+    for w in wins:
+        w.close()
+
+
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("T", [75, 32, 1])
 def test_chunked_prefill_then_decode(d, T):

@@ -171,6 +171,28 @@ def test_fused_several_prep_warps_is_safe(npw, ncw, NS, NA, G):
         assert not v and finished, (seed, v[:3])
 
 
+@pytest.mark.parametrize("ncw,NS,NA", [(4, 4, 4), (2, 4, 4), (2, 4, 6), (3, 3, 6), (4, 8, 8), (1, 1, 3)])
+def test_consumer_prep_aux_first_on_owned_slots_is_safe(ncw, NS, NA):
+    """One-tile units whose consumer warp computes the coefficients itself: it
+    waits for the unit's inputs first, then for the tile.  With na a multiple of
+    ncw each warp owns its aux slots as it owns its stages, so the aux wait is
+    never a phase off even though it comes first."""
+    for seed in range(12):
+        v, finished = simulate(NS, NA, 1, 8 * 4 * 5, owned=True, tile_first=False, seed=seed,
+                               ncw=ncw)
+        assert not v and finished, (seed, v[:3])
+
+
+def test_consumer_prep_aux_first_on_shared_slots_is_caught():
+    """Negative control: with na not a multiple of ncw, slots pass between warps
+    and an aux-first wait can pass a phase early."""
+    caught = 0
+    for seed in range(12):
+        v, finished = simulate(4, 5, 1, 8 * 4 * 5, owned=True, tile_first=False, seed=seed, ncw=4)
+        caught += bool(v) or not finished
+    assert caught >= 3
+
+
 def test_prep_warps_taking_every_npw_th_unit_is_caught():
     """Negative control: prep warps that take units pw, pw+npw, ... can wait on a
     slot whose earlier phase they never saw; the parity test then passes early."""
