@@ -47,7 +47,8 @@ def log(*a):
     print(*a, file=sys.stderr, flush=True)
 
 
-KERNEL_SOURCES = ["pipeline.cuh", "append_decode.cu", "dl_device.cuh", "layout.h"]
+KERNEL_SOURCES = ["pipeline.cuh", "append_decode.cu", "append_launch.cuh", "append_fused_ne8.cu",
+                  "append_fused_ne16.cu", "append_fused_ne32.cu", "dl_device.cuh", "layout.h"]
 
 
 def kernel_source_hash():

@@ -396,8 +396,8 @@ dl_status dl_create(const dl_config* cfg, void* stream, dl_ctx** out) {
     e = dl::configure_append_decode(f.op, f.d_k, smem);
     if (e == cudaSuccess) e = dl::configure_eager_step(f.op, f.d_k, smem);
     if (e != cudaSuccess) { rc = cuda_err(c, e, "kernel attribute"); break; }
-    c->regs[(int)Kern::Append] = dl::append_decode_regs(f.op, f.d_k, false);
-    c->regs[(int)Kern::Fused] = dl::append_decode_regs(f.op, f.d_k, true);
+    c->regs[(int)Kern::Append] = dl::append_decode_regs(f.op, f.d_k, false, f.merge_interval);
+    c->regs[(int)Kern::Fused] = dl::append_decode_regs(f.op, f.d_k, true, f.merge_interval);
     c->regs[(int)Kern::Eager] = dl::eager_step_regs(f.op, f.d_k);
   } while (0);
   g_fail_countdown = -1;

@@ -39,8 +39,23 @@ inline cudaError_t raise_smem_limit(Kernel* kern, size_t smem) {
 cudaError_t configure_append_decode(int op, int dk, size_t smem);
 cudaError_t configure_eager_step(int op, int dk, size_t smem);
 
-// Registers per thread of the pipelined kernel instances (0 if unknown).
-int append_decode_regs(int op, int dk, bool fused);
+// Registers per thread of the pipelined kernel instances (0 if unknown); the
+// fused form's instance depends on the merge interval M.
+int append_decode_regs(int op, int dk, bool fused, int M);
+
+// The fused form's translation units, one per bound on log entries (M - 1 <= NE).
+cudaError_t launch_fused_ne8(int op, int dk, const StepArgs& a, int grid, size_t smem, bool pdl,
+                             cudaStream_t s);
+cudaError_t launch_fused_ne16(int op, int dk, const StepArgs& a, int grid, size_t smem, bool pdl,
+                              cudaStream_t s);
+cudaError_t launch_fused_ne32(int op, int dk, const StepArgs& a, int grid, size_t smem, bool pdl,
+                              cudaStream_t s);
+cudaError_t configure_fused_ne8(int op, int dk, size_t smem);
+cudaError_t configure_fused_ne16(int op, int dk, size_t smem);
+cudaError_t configure_fused_ne32(int op, int dk, size_t smem);
+int regs_fused_ne8(int op, int dk);
+int regs_fused_ne16(int op, int dk);
+int regs_fused_ne32(int op, int dk);
 int eager_step_regs(int op, int dk);
 
 // Standalone merge / read-state (S_out == nullptr: write back into S̄ and reset the log).

@@ -101,7 +101,8 @@ inline PipePlan fit_pipeline(int cps, int ncw, int R, int dk, int aux_bytes, int
                              int max_na = 16) {
   const PipePlan none{0, 0, 0, 0, 0, 0};
   if (ncw < 1 || ncw > 8 || R < 1 || npw > 2) return none;
-  if (npw == 0 && G / tps != 1) return none;   // consumer prep needs one-stage units
+  // one-stage units are prepared by their consumer warp, larger ones by prep warps
+  if (npw >= 0 && (npw == 0) != (G / tps == 1)) return none;
   // registers: cps CTAs of (ncw + 1 + npw) warps must be resident together.
   // Each of the SM's 4 sub-partitions holds 16 Ki registers, allocated per
   // warp in multiples of 8 per thread; a warp lives on one sub-partition.

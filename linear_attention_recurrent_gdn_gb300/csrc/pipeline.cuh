@@ -600,8 +600,12 @@ __device__ __forceinline__ void consume_eager(const StepArgs& a, const Layout& L
 }
 
 // ----------------------------------------------------------------- kernel ---
-template <int OP, int DK, int DV, int MODE>
+// NE: the fused form's bound on log entries (8, 16 or 32: M - 1 <= NE), one
+// instance each so that a launch carries only the code its M needs; 0 for the
+// two-kernel and eager forms.
+template <int OP, int DK, int DV, int MODE, int NE = 0>
 __global__ void __maxnreg__(128) pipe_kernel(const __grid_constant__ StepArgs a) {
+  static_assert(MODE != FUSED || NE == 8 || NE == 16 || NE == 32, "fused form needs NE");
   extern __shared__ __align__(1024) unsigned char smem[];
   constexpr uint32_t TILE_BYTES = BV * DK * 4;
   const Layout Lay = make_layout(OP, a.M, DK, DV);
@@ -752,7 +756,8 @@ __global__ void __maxnreg__(128) pipe_kernel(const __grid_constant__ StepArgs a)
   // step (the primary grid) has completed.
   if constexpr (MODE == FUSED) pdl_wait_primary();
 
-  if (MODE == FUSED && warp > NCWr) {
+  if constexpr (MODE == FUSED && DK != 64) {   // (d_k = 64 units are one stage: no prep warps)
+  if (warp > NCWr) {
     // ------------------------------------------------- fused ReplayPrep stage
     // Prep warp pw owns the aux slots x with x % npw == pw and takes their
     // units in order, so it waits on every phase of those slots' barriers.
@@ -764,13 +769,12 @@ __global__ void __maxnreg__(128) pipe_kernel(const __grid_constant__ StepArgs a)
         break;
       const UnitPos p = unit_pos(a, (int)blockIdx.x + kk * (int)gridDim.x);
       unsigned char* ax = auxm + (size_t)x * aux_bytes;
-      if (a.M - 1 <= 8) prep_unit<OP, DK, DV, 8>(a, Lay, p, ax, lane);
-      else if (a.M - 1 <= 16) prep_unit<OP, DK, DV, 16>(a, Lay, p, ax, lane);
-      else prep_unit<OP, DK, DV, 32>(a, Lay, p, ax, lane);
+      prep_unit<OP, DK, DV, NE>(a, Lay, p, ax, lane);
       __syncwarp();
       if (lane == 0) mbar_arrive(bars.cready(x));
     }
     return;
+  }
   }
 
   // -------------------------------------------------------------- consumers
@@ -786,7 +790,9 @@ __global__ void __maxnreg__(128) pipe_kernel(const __grid_constant__ StepArgs a)
     }
     unsigned char* ax = auxm + (size_t)x * aux_bytes;
     bool ok;
-    if (MODE == FUSED && a.npw == 0) {
+    bool cprep = false;
+    if constexpr (MODE == FUSED) cprep = (DK == 64 || a.npw == 0);
+    if (cprep) {
       // One-stage units, no prep warps: this warp owns aux slot x (na is a
       // multiple of ncw, so every unit of the slot is this warp's) and has
       // seen each earlier phase of its barrier itself, so it can wait for the
@@ -794,9 +800,7 @@ __global__ void __maxnreg__(128) pipe_kernel(const __grid_constant__ StepArgs a)
       // still landing.
       ok = mbar_wait(bars.afull(x), (kk / NA) & 1, a.status, DEV_TIMEOUT_AUX);
       if (!__all_sync(0xffffffffu, ok)) break;
-      if (a.M - 1 <= 8) prep_unit<OP, DK, DV, 8>(a, Lay, p, ax, lane);
-      else if (a.M - 1 <= 16) prep_unit<OP, DK, DV, 16>(a, Lay, p, ax, lane);
-      else prep_unit<OP, DK, DV, 32>(a, Lay, p, ax, lane);
+      if constexpr (MODE == FUSED) prep_unit<OP, DK, DV, NE>(a, Lay, p, ax, lane);
       __syncwarp();
       ok = mbar_wait(bars.full(s), stage_parity(i, R, NCWr), a.status, DEV_TIMEOUT_TILE);
     } else {
