@@ -667,8 +667,15 @@ __global__ void __maxnreg__(128) pipe_kernel(const __grid_constant__ StepArgs a)
       }
       pending_from = ka;
     };
+    // Per-tile bookkeeping is incremental (no divisions on the issue path):
+    // unit kt and item j of tile ti, the owning warp w, its stage round r and
+    // phase parity; the unit's tile source is computed once per unit.
+    int kt = 0, j = 0, w = 0, r = 0;
+    uint32_t par = 0;
+    int ax_x = 0;                 // aux slot of unit ka
+    uint32_t ax_par = 0;          // phase parity of that slot for unit ka
+    const float* src_unit = nullptr;
     while (ti < my_tiles) {
-      const int kt = ti / IPU;
       if (!primary_done) {
         // the next wait needs consumers to make progress, and they need inputs
         bool need = ti >= NS || (kt == ka && ka >= NA);
@@ -687,9 +694,9 @@ __global__ void __maxnreg__(128) pipe_kernel(const __grid_constant__ StepArgs a)
         }
       }
       if (kt == ka) {
-        const int x = ka % NA;
+        const int x = ax_x;
         if (!__all_sync(0xffffffffu,
-                        mbar_wait(bars.aempty(x), ((ka / NA) & 1) ^ 1, a.status, DEV_TIMEOUT_EMPTY))) {
+                        mbar_wait(bars.aempty(x), ax_par ^ 1u, a.status, DEV_TIMEOUT_EMPTY))) {
           ok = false;
           break;
         }
@@ -711,27 +718,39 @@ __global__ void __maxnreg__(128) pipe_kernel(const __grid_constant__ StepArgs a)
           issue_aux<OP, DK, DV, MODE>(a, Lay, p, ax, lane);
           cp_async_arrive_noinc(bars.afull(x));
         }
+        // DeltaLog steps read the base the slot indexes (a fork source's until
+        // the first merge); the eager step reads the slot's own state
+        const int base = (MODE == EAGER) ? a.items[p.row].slot : a.items[p.row].base;
+        src_unit = a.Sbar + (((size_t)base * a.H + p.h) * DV + (size_t)p.grp * G * BV) * DK;
         ++ka;
+        if (++ax_x == NA) {
+          ax_x = 0;
+          ax_par ^= 1u;
+        }
       }
-      const int s = stage_of(ti, R, NCWr);
-      if (!__all_sync(0xffffffffu, mbar_wait(bars.empty(s), stage_parity(ti, R, NCWr) ^ 1u,
-                                              a.status, DEV_TIMEOUT_EMPTY))) {
+      const int s = w * R + r;   // = stage_of(ti, R, NCWr)
+      if (!__all_sync(0xffffffffu, mbar_wait(bars.empty(s), par ^ 1u, a.status, DEV_TIMEOUT_EMPTY))) {
         ok = false;
         break;
       }
       if (lane == 0) {
-        const UnitPos p = unit_pos(a, (int)blockIdx.x + kt * (int)gridDim.x);
-        const int vt = p.grp * G + (ti - kt * IPU) * TPS;   // first value tile of the item
-        // DeltaLog steps read the base the slot indexes (a fork source's until
-        // the first merge); the eager step reads the slot's own state
-        const int base = (MODE == EAGER) ? a.items[p.row].slot : a.items[p.row].base;
-        const float* src = a.Sbar + (((size_t)base * a.H + p.h) * DV + vt * BV) * DK;
         mbar_arrive_expect_tx(bars.full(s), STAGE_BYTES);
-        bulk_g2s_hint(smem_u32(tiles + (size_t)s * TPS * BV * DK), src, STAGE_BYTES, bars.full(s),
-                      pol);
+        bulk_g2s_hint(smem_u32(tiles + (size_t)s * TPS * BV * DK),
+                      src_unit + (size_t)j * TPS * BV * DK, STAGE_BYTES, bars.full(s), pol);
       }
       __syncwarp();
       ++ti;
+      if (++j == IPU) {
+        j = 0;
+        ++kt;
+      }
+      if (++w == NCWr) {
+        w = 0;
+        if (++r == R) {
+          r = 0;
+          par ^= 1u;
+        }
+      }
     }
     if (ok && !primary_done) {
       pdl_wait_primary();
@@ -778,11 +797,38 @@ __global__ void __maxnreg__(128) pipe_kernel(const __grid_constant__ StepArgs a)
   }
 
   // -------------------------------------------------------------- consumers
+  // Incremental bookkeeping (tile i of this warp: unit kk, item j within the
+  // unit, aux slot x with phase parity xpar, stage round r with parity spar);
+  // the unit's position is recomputed only when the unit changes.
+  int kk = warp / IPU, j = warp - (warp / IPU) * IPU;
+  int x = kk % NA;
+  uint32_t xpar = (uint32_t)(kk / NA) & 1u;
+  int r = 0;
+  uint32_t spar = 0;
+  int kk_pos = -1;
+  UnitPos p{};
   for (int i = warp; i < my_tiles; i += NCWr) {
-    const int kk = i / IPU;
-    const UnitPos p = unit_pos(a, (int)blockIdx.x + kk * (int)gridDim.x);
-    const int vt0 = p.grp * G + (i - kk * IPU) * TPS;
-    const int x = kk % NA, s = stage_of(i, R, NCWr);
+    if (i != warp) {   // advance from the previous tile of this warp
+      j += NCWr;
+      while (j >= IPU) {
+        j -= IPU;
+        ++kk;
+        if (++x == NA) {
+          x = 0;
+          xpar ^= 1u;
+        }
+      }
+      if (++r == R) {
+        r = 0;
+        spar ^= 1u;
+      }
+    }
+    if (kk != kk_pos) {
+      p = unit_pos(a, (int)blockIdx.x + kk * (int)gridDim.x);
+      kk_pos = kk;
+    }
+    const int vt0 = p.grp * G + j * TPS;
+    const int s = warp * R + r;   // = stage_of(i, R, NCWr)
     float g_s = 0.f, beta_s = 0.f;
     if constexpr (MODE == EAGER) {
       if (OP == GDN) g_s = a.g[p.sh];
@@ -798,17 +844,17 @@ __global__ void __maxnreg__(128) pipe_kernel(const __grid_constant__ StepArgs a)
       // seen each earlier phase of its barrier itself, so it can wait for the
       // unit's inputs first and compute the coefficients while the tile is
       // still landing.
-      ok = mbar_wait(bars.afull(x), (kk / NA) & 1, a.status, DEV_TIMEOUT_AUX);
+      ok = mbar_wait(bars.afull(x), xpar, a.status, DEV_TIMEOUT_AUX);
       if (!__all_sync(0xffffffffu, ok)) break;
       if constexpr (MODE == FUSED) prep_unit<OP, DK, DV, NE>(a, Lay, p, ax, lane);
       __syncwarp();
-      ok = mbar_wait(bars.full(s), stage_parity(i, R, NCWr), a.status, DEV_TIMEOUT_TILE);
+      ok = mbar_wait(bars.full(s), spar, a.status, DEV_TIMEOUT_TILE);
     } else {
       // The tile first: it is issued after its unit's aux copies, so once it
       // has landed the aux barrier is in this unit's phase and the parity test
       // below is unambiguous.
-      ok = mbar_wait(bars.full(s), stage_parity(i, R, NCWr), a.status, DEV_TIMEOUT_TILE);
-      ok = ok && mbar_wait(MODE == FUSED ? bars.cready(x) : bars.afull(x), (kk / NA) & 1, a.status,
+      ok = mbar_wait(bars.full(s), spar, a.status, DEV_TIMEOUT_TILE);
+      ok = ok && mbar_wait(MODE == FUSED ? bars.cready(x) : bars.afull(x), xpar, a.status,
                            DEV_TIMEOUT_AUX);
     }
     if (!__all_sync(0xffffffffu, ok)) break;
