@@ -2,11 +2,14 @@
 """Benchmark of DeltaLog recurrent-state decode on GB300.
 
 One bench step = one full decode run of the workload: `tokens` decode tokens
-for every slot, i.e. `tokens` x (ReplayPrep + AppendDecode) launches, all
-inputs pre-generated in HBM.  Default workload: GDN decode at serving batch,
-B=256 slots, H=32 heads, d_k=d_v=128, fp32 state (512 MiB, larger than L2),
-512 tokens, merge interval M=16; the M sweep {1,4,8,16,32} and the in-house
-eager kernel are measured beside it.
+for every slot, one AppendDecode launch per token (ReplayPrep fused in; two
+launches with --staging kernels), all inputs pre-generated in HBM.  The decode
+loop runs as CUDA graphs of M tokens (dl_window; --no-graph: one dl_step call
+per token).  Default workload: GDN decode at serving batch, B=256 slots, H=32
+heads, d_k=d_v=128, fp32 state (512 MiB, larger than L2), 512 tokens, merge
+interval M=16; the M sweep {1,4,8,16,32} and the in-house eager kernel are
+measured beside it.  The end-to-end figure runs the same decode from pinned
+host buffers through dl_decode_host, copies included.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload gdn|kda|rwkv6] [--M 16] [--no-sweep] [--no-cpu]
@@ -482,9 +485,9 @@ def run_ours(args):
     c = make_ctx(M)
 
     def host_run():
-        for t in range(T):
-            c.step_host(slots, pin["q"][t], pin["k"][t], pin["v"][t], pin["g"][t],
-                        pin["beta"][t] if pin["beta"] is not None else None, hout[t])
+        # one call per bench step: host inputs of all T tokens in, host outputs
+        # out; the library overlaps each token's copies with its neighbours' compute
+        c.decode_host(slots, pin["q"], pin["k"], pin["v"], pin["g"], pin["beta"], hout)
     for _ in range(args.warmup):
         host_run()
     barrier(dist)
@@ -499,7 +502,7 @@ def run_ours(args):
     d2h = hout[0].numel() * hout.element_size() * T
     result["e2e"] = {"value": units_per_step * world / (e2e_ms / 1e3), "unit": "tokens·heads/s",
                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                     "ms_per_step": e2e_ms, "api": "dl_step_host"}
+                     "ms_per_step": e2e_ms, "api": "dl_decode_host"}
 
     # ---- CPU baseline (rank 0, N = 1 only)
     if rank == 0 and world == 1 and not args.no_cpu:

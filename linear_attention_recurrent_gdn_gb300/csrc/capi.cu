@@ -57,6 +57,13 @@ struct dl_ctx {
   int32_t coef_rows = 0;
   void* stage = nullptr;        // device staging for dl_step_host
   size_t stage_bytes = 0;
+  // dl_decode_host: two device staging sets (token t uses set t % 2), an
+  // upload and a download stream, and the events that order them
+  void* pipe_stage = nullptr;
+  size_t pipe_set_bytes = 0;
+  cudaStream_t up = nullptr, down = nullptr;
+  cudaEvent_t ev_in[2] = {nullptr, nullptr}, ev_done[2] = {nullptr, nullptr},
+              ev_out[2] = {nullptr, nullptr};
   std::vector<int32_t> plan;
   std::unique_ptr<dl::StepArgs> step_args;
   std::unique_ptr<dl::SlotListArgs> list_args;
@@ -110,9 +117,19 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 void free_all(dl_ctx* c) {
   void* ptrs[] = {c->Sbar, c->alog, c->klog, c->Llog, c->nlog, c->base_of,
-                  c->coef, c->bonus, c->status, c->stage};
+                  c->coef, c->bonus, c->status, c->stage, c->pipe_stage};
   for (void* p : ptrs)
     if (p) cudaFree(p);
+  c->pipe_stage = nullptr;
+  for (cudaEvent_t* ev : {c->ev_in, c->ev_done, c->ev_out})
+    for (int b = 0; b < 2; ++b)
+      if (ev[b]) {
+        cudaEventDestroy(ev[b]);
+        ev[b] = nullptr;
+      }
+  if (c->up) cudaStreamDestroy(c->up);
+  if (c->down) cudaStreamDestroy(c->down);
+  c->up = c->down = nullptr;
   c->Sbar = nullptr;
   c->alog = nullptr;
   c->klog = nullptr;
@@ -574,6 +591,90 @@ dl_status dl_step_host(dl_ctx* c, const int32_t* slots, int32_t n, const void* q
   if (rc != DL_OK) return rc;
   DL_CUDA(cudaMemcpyAsync(o, dout, bo, cudaMemcpyDeviceToHost, c->stream), "D2H o");
   DL_CUDA(cudaStreamSynchronize(c->stream), "stream sync");
+  return DL_OK;
+}
+
+dl_status dl_decode_host(dl_ctx* c, const int32_t* slots, int32_t n, int32_t T, const void* q,
+                         const void* k, const void* v, const float* g, const float* beta,
+                         void* o) {
+  dl_status rc = check_ctx(c);
+  if (rc != DL_OK) return rc;
+  if (n < 0 || T < 0) return set_err(c, DL_EINVAL, "negative count");
+  if (n == 0 || T == 0) return DL_OK;
+  if (!q || !k || !v || !g || !o || (c->cfg.op != DL_RWKV6 && !beta))
+    return set_err(c, DL_EINVAL, "NULL tensor pointer");
+  rc = dl_table_check(c->table, slots, n);
+  if (rc != DL_OK) return set_err(c, rc, "dl_decode_host: invalid slot list");
+  const dl_config& f = c->cfg;
+  const size_t H = f.num_heads;
+  const size_t bq = (size_t)n * H * f.d_k * 2, bv = (size_t)n * H * f.d_v * 2;
+  const size_t bg = (size_t)n * H * (f.op == DL_GDN ? 1 : f.d_k) * 4;
+  const size_t bb = (size_t)n * H * 4, bo = (size_t)n * H * f.d_v * (f.out_bf16 ? 2 : 4);
+  auto r256 = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  if (!c->pipe_stage) {
+    // one set sized for the largest batch the context can take
+    const size_t Sn = f.num_slots;
+    const size_t set = 2 * r256(Sn * H * f.d_k * 2) + r256(Sn * H * f.d_v * 2) +
+                       r256(Sn * H * (f.op == DL_GDN ? 1 : f.d_k) * 4) + r256(Sn * H * 4) +
+                       r256(Sn * H * f.d_v * 4);
+    if (cudaMalloc(&c->pipe_stage, 2 * set) != cudaSuccess) {
+      c->pipe_stage = nullptr;
+      return set_err(c, DL_ENOMEM, "staging allocation");
+    }
+    c->pipe_set_bytes = set;
+    cudaError_t e = cudaStreamCreateWithFlags(&c->up, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->down, cudaStreamNonBlocking);
+    for (int b = 0; b < 2 && e == cudaSuccess; ++b) {
+      e = cudaEventCreateWithFlags(&c->ev_in[b], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->ev_done[b], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->ev_out[b], cudaEventDisableTiming);
+    }
+    if (e != cudaSuccess) return cuda_err(c, e, "dl_decode_host set-up");
+  }
+  const unsigned char* hq = static_cast<const unsigned char*>(q);
+  const unsigned char* hk = static_cast<const unsigned char*>(k);
+  const unsigned char* hv = static_cast<const unsigned char*>(v);
+  const unsigned char* hg = reinterpret_cast<const unsigned char*>(g);
+  const unsigned char* hb = reinterpret_cast<const unsigned char*>(beta);
+  unsigned char* ho = static_cast<unsigned char*>(o);
+  cudaError_t e = cudaSuccess;
+  for (int32_t t = 0; t < T && rc == DL_OK && e == cudaSuccess; ++t) {
+    const int b = t & 1;
+    unsigned char* p = static_cast<unsigned char*>(c->pipe_stage) + (size_t)b * c->pipe_set_bytes;
+    void* dq = p; p += r256(bq);
+    void* dk = p; p += r256(bq);
+    void* dv = p; p += r256(bv);
+    float* dg = reinterpret_cast<float*>(p); p += r256(bg);
+    float* db = reinterpret_cast<float*>(p); p += r256(bb);
+    void* dout = p;
+    // set b is free once token t-2's output has been downloaded (which also
+    // follows token t-2's kernel, the last reader of its inputs)
+    if (t >= 2) e = cudaStreamWaitEvent(c->up, c->ev_out[b], 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dq, hq + t * bq, bq, cudaMemcpyHostToDevice, c->up);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dk, hk + t * bq, bq, cudaMemcpyHostToDevice, c->up);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dv, hv + t * bv, bv, cudaMemcpyHostToDevice, c->up);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dg, hg + t * bg, bg, cudaMemcpyHostToDevice, c->up);
+    if (e == cudaSuccess && f.op != DL_RWKV6)
+      e = cudaMemcpyAsync(db, hb + t * bb, bb, cudaMemcpyHostToDevice, c->up);
+    if (e == cudaSuccess) e = cudaEventRecord(c->ev_in[b], c->up);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(c->stream, c->ev_in[b], 0);
+    if (e != cudaSuccess) break;
+    rc = dl_step(c, slots, n, dq, dk, dv, dg, f.op != DL_RWKV6 ? db : nullptr, dout);
+    if (rc != DL_OK) break;
+    e = cudaEventRecord(c->ev_done[b], c->stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(c->down, c->ev_done[b], 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(ho + t * bo, dout, bo, cudaMemcpyDeviceToHost, c->down);
+    if (e == cudaSuccess) e = cudaEventRecord(c->ev_out[b], c->down);
+  }
+  // nothing may still write the caller's buffers when the call returns
+  const cudaError_t e1 = cudaStreamSynchronize(c->up);
+  const cudaError_t e2 = cudaStreamSynchronize(c->stream);
+  const cudaError_t e3 = cudaStreamSynchronize(c->down);
+  if (rc != DL_OK) return rc;
+  if (e != cudaSuccess) return cuda_err(c, e, "dl_decode_host copies");
+  if (e1 != cudaSuccess) return cuda_err(c, e1, "dl_decode_host upload");
+  if (e2 != cudaSuccess) return cuda_err(c, e2, "dl_decode_host compute");
+  if (e3 != cudaSuccess) return cuda_err(c, e3, "dl_decode_host download");
   return DL_OK;
 }
 

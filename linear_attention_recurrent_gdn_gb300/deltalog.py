@@ -26,7 +26,7 @@ EXPORTS = [
     "dl_table_create", "dl_table_destroy", "dl_table_step", "dl_table_step_eager",
     "dl_table_fork", "dl_table_reset", "dl_table_check", "dl_table_get",
     "dl_create", "dl_destroy", "dl_set_stream", "dl_set_state", "dl_set_bonus", "dl_fork",
-    "dl_step", "dl_step_host", "dl_step_eager", "dl_merge", "dl_read_state", "dl_get_meta",
+    "dl_step", "dl_step_host", "dl_decode_host", "dl_step_eager", "dl_merge", "dl_read_state", "dl_get_meta",
     "dl_sync", "dl_set_timing", "dl_get_timing", "dl_last_error", "dl_status_str",
     "dl_abi_version", "dl_checkpoint_bytes", "dl_checkpoint_save", "dl_checkpoint_load",
     "dl_window_create", "dl_window_launch", "dl_window_destroy", "dl_prefill",
@@ -80,6 +80,7 @@ def _load():
         "dl_fork": ([P, I32, P, I32], I32),
         "dl_step": ([P, P, I32, P, P, P, P, P, P], I32),
         "dl_step_host": ([P, P, I32, P, P, P, P, P, P], I32),
+        "dl_decode_host": ([P, P, I32, I32, P, P, P, P, P, P], I32),
         "dl_step_eager": ([P, P, I32, P, P, P, P, P, P], I32),
         "dl_merge": ([P, P, I32], I32),
         "dl_read_state": ([P, P, I32, P], I32),
@@ -223,6 +224,15 @@ def dl_step_host(ctx, slots, q, k, v, g, beta, o):
     a, p, n = _slots(slots)
     _check(_lib.dl_step_host(ctx, p, n, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
                              _ptr(o)), ctx)
+
+
+def dl_decode_host(ctx, slots, q, k, v, g, beta, o):
+    """T tokens of host (pinned) torch tensors [T, n, ...] in, host o [T, n, H, d_v] out;
+    copies overlap the computation; synchronous."""
+    a, p, n = _slots(slots)
+    T = int(q.shape[0])
+    _check(_lib.dl_decode_host(ctx, p, n, T, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                               _ptr(o)), ctx)
 
 
 def dl_merge(ctx, slots):
@@ -476,6 +486,18 @@ class DeltaLog:
             if t is not None and (t.is_cuda or not t.is_contiguous()):
                 raise ValueError("step_host takes contiguous host tensors")
         dl_step_host(self._h, a, q, k, v, g, beta, out)
+        return out
+
+    def decode_host(self, slots, q, k, v, g, beta=None, out=None):
+        """T tokens from host tensors q, k, v, g, beta [T, n, ...]; returns o [T, n, H, d_v]."""
+        a, _, n = _slots(slots)
+        T = int(q.shape[0])
+        if out is None:
+            out = self.torch.empty((T, n, self.H, self.d_v), dtype=self.out_dtype, pin_memory=True)
+        for t in (q, k, v, g, beta, out):
+            if t is not None and (t.is_cuda or not t.is_contiguous() or int(t.shape[0]) != T):
+                raise ValueError("decode_host takes contiguous host tensors with T leading rows")
+        dl_decode_host(self._h, a, q, k, v, g, beta, out)
         return out
 
     def merge(self, slots):

@@ -308,3 +308,41 @@ def test_step_host_matches_device_path():
     outs = [ctx.step_host(list(range(B)), pin["q"][t], pin["k"][t], pin["v"][t], pin["g"][t],
                           pin["beta"][t]).float() for t in range(T)]
     assert torch.equal(torch.stack(outs), o_dev)
+
+
+@pytest.mark.parametrize("staging", STAGINGS)
+@pytest.mark.parametrize("op", OPS)
+def test_decode_host_matches_device_path(op, staging):
+    """dl_decode_host (host buffers, copies overlapping the computation) gives
+    the bits of dl_step on device buffers, over two merges and a partial window."""
+    from linear_attention_recurrent_gdn_gb300 import deltalog as dl
+    B, H, d, M = 6, 4, 128 if op != gen.RWKV6 else 64, 4
+    T = 2 * M + 3
+    x, S0, bonus = make_case(op, B, H, d, T, seed=900 + op)
+    o_dev, states, ref = gpu_run(op, x, S0, bonus, M, snap=(T - 1,), staging=staging)
+    ctx = dl.DeltaLog(op, B, H, d, d, M, staging=staging)
+    ctx.set_state(list(range(B)), S0.cuda())
+    if bonus is not None:
+        ctx.set_bonus(bonus.cuda())
+    pin = {k_: (v_.contiguous().pin_memory() if v_ is not None else None) for k_, v_ in x.items()}
+    o = ctx.decode_host(list(range(B)), pin["q"], pin["k"], pin["v"], pin["g"], pin["beta"])
+    assert torch.equal(o.float(), o_dev)
+    assert torch.equal(ctx.read_state(list(range(B))).cpu(), states[T - 1])
+    assert list(ctx.get_meta()[0]) == [T % M] * B
+
+
+def test_decode_host_frozen_slot_is_refused():
+    from linear_attention_recurrent_gdn_gb300 import deltalog as dl
+    B, H, d, M, T = 3, 2, 64, 4, 5
+    x, S0, _ = make_case(gen.GDN, B, H, d, T, seed=950)
+    ctx = dl.DeltaLog(gen.GDN, B + 1, H, d, d, M)
+    ctx.set_state(list(range(B)), S0.cuda())
+    ctx.fork(0, [B])                       # slot 0 is now a fork source: frozen
+    pin = {k_: (v_.contiguous().pin_memory() if v_ is not None else None) for k_, v_ in x.items()}
+    with pytest.raises(dl.DeltaLogError) as e:
+        ctx.decode_host([0, 1, 2], pin["q"], pin["k"], pin["v"], pin["g"], pin["beta"])
+    assert e.value.status == dl.EBUSY
+    o = ctx.decode_host([1, 2], pin["q"][:, 1:].contiguous(), pin["k"][:, 1:].contiguous(),
+                        pin["v"][:, 1:].contiguous(), pin["g"][:, 1:].contiguous(),
+                        pin["beta"][:, 1:].contiguous())
+    assert o.shape == (T, 2, H, d) and torch.isfinite(o.float()).all()
