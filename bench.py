@@ -236,9 +236,10 @@ def run_reference(args):
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic", "impl": "reference",
-           "config": {"workload": w["desc"] + " (oracle sample)", "op": gen.OP_NAMES[w["op"]],
-                      "B": w["B"], "H": w["H"], "d_k": w["d"], "d_v": w["d"],
-                      "tokens": w["tokens"], "M": w["M"]},
+           "config": {"workload": w["desc"] + ", merge interval M=%d" % (args.M or w["M"]),
+                      "op": gen.OP_NAMES[w["op"]], "B": w["B"], "H": w["H"], "d_k": w["d"],
+                      "d_v": w["d"], "tokens": w["tokens"], "M": args.M or w["M"],
+                      "implementation": "fp64 eager oracle (C, OpenMP) on a bounded sample"},
            "cpu_baseline": {"value": res["value"], "unit": "tokens·heads/s",
                             "cores": res["cores"], "kind": "oracle", "sample": res["sample"]},
            "e2e": {"value": res["value"], "unit": "tokens·heads/s", "h2d_bytes_per_step": 0,
