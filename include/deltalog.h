@@ -226,13 +226,15 @@ dl_status dl_get_meta(dl_ctx *ctx, int32_t *n_log, int32_t *base_of);
  * leave the state after the last token in the slot's dense base (log empty).
  * Flide page, "Research method step by step", second step: the shared
  * context is processed once and its final state saved before branches fork.
- * Inputs are token-major: q, k [T, n, H, d_k] bf16, v [T, n, H, d_v] bf16,
- * g, beta [T, n, H] fp32; o [T, n, H, d_v] receives every token's output, or
- * is NULL.  Every slot must own its base and have an empty log.  Tokens are
+ * Inputs are token-major: q (r for RWKV6), k [T, n, H, d_k] bf16, v
+ * [T, n, H, d_v] bf16, g [T, n, H] (GDN) or [T, n, H, d_k] (KDA, RWKV6) fp32,
+ * beta [T, n, H] fp32 (NULL for RWKV6, which needs dl_set_bonus first);
+ * o [T, n, H, d_v] receives every token's output, or is NULL.  Every slot
+ * must own its base and have an empty log (else DL_EINVAL).  Tokens are
  * processed C = 32 at a time: one pass over the state per chunk computes all
- * chunk outputs (base + log algebra, forward substitution for the delta-rule
- * factors), and the state is rewritten once per chunk.  GDN only in this
- * build (DL_EUNSUPPORTED otherwise). */
+ * chunk outputs (base + log algebra with the chunk as the log, forward
+ * substitution for the delta-rule factors), and the state is rewritten once
+ * per chunk. */
 dl_status dl_prefill(dl_ctx *ctx, const int32_t *slots, int32_t n, int32_t T,
                      const void *q, const void *k, const void *v,
                      const float *g, const float *beta, void *o);

@@ -735,11 +735,12 @@ dl_status dl_prefill(dl_ctx* c, const int32_t* slots, int32_t n, int32_t T, cons
   dl_status rc = check_ctx(c);
   if (rc != DL_OK) return rc;
   if (n < 0 || T < 0) return set_err(c, DL_EINVAL, "negative count");
-  if (c->cfg.op != DL_GDN) return set_err(c, DL_EUNSUPPORTED, "dl_prefill: GDN only in this build");
   if (n == 0 || T == 0) return DL_OK;
-  if (!q || !k || !v || !g || !beta) return set_err(c, DL_EINVAL, "NULL tensor pointer");
+  const bool delta = c->cfg.op != DL_RWKV6;
+  if (!q || !k || !v || !g || (delta && !beta)) return set_err(c, DL_EINVAL, "NULL tensor pointer");
+  if (!delta && !c->bonus) return set_err(c, DL_EINVAL, "RWKV6 needs dl_set_bonus before prefill");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || (reinterpret_cast<uintptr_t>(g) & 3u) ||
-      (reinterpret_cast<uintptr_t>(beta) & 3u) ||
+      (delta && (reinterpret_cast<uintptr_t>(beta) & 3u)) ||
       (o && (reinterpret_cast<uintptr_t>(o) & (c->cfg.out_bf16 ? 1u : 3u))))
     return set_err(c, DL_EINVAL, "misaligned tensor");
   if (n > dl::MAX_ROWS) return set_err(c, DL_EINVAL, "dl_prefill takes at most %d slots per call", dl::MAX_ROWS);
@@ -755,8 +756,9 @@ dl_status dl_prefill(dl_ctx* c, const int32_t* slots, int32_t n, int32_t T, cons
   a.H = c->cfg.num_heads;
   a.Mcap = c->L.Mcap;
   for (int32_t i = 0; i < n; ++i) a.items[i] = dl::StepItem{slots[i], slots[i], 0};
-  DL_CUDA(dl::launch_prefill(c->cfg.op, c->cfg.d_k, a, q, k, v, g, beta, o, T, c->cfg.out_bf16,
-                             c->cfg.scale, c->stream), "Prefill launch");
+  DL_CUDA(dl::launch_prefill(c->cfg.op, c->cfg.d_k, a, q, k, v, g, delta ? beta : nullptr,
+                             c->bonus, o, T, c->cfg.out_bf16, c->cfg.scale, c->stream),
+          "Prefill launch");
   return DL_OK;
 }
 

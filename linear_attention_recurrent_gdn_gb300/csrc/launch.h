@@ -65,9 +65,10 @@ cudaError_t launch_set_state(int dk, int dv, const SlotListArgs& a, cudaStream_t
 // Copy the source's log rows into each destination and point it at the source's base.
 cudaError_t launch_fork(int op, int dk, const SlotListArgs& a, cudaStream_t s);
 
-// Chunked prefill of T tokens (GDN): token-major inputs [T, rows, H, d].
+// Chunked prefill of T tokens: token-major inputs [T, rows, H, d]; `bonus`
+// [H, d_k] for RWKV6.
 cudaError_t launch_prefill(int op, int dk, const SlotListArgs& a, const void* q, const void* k,
-                           const void* v, const float* g, const float* beta, void* o, int T,
-                           int out_bf16, float scale, cudaStream_t s);
+                           const void* v, const float* g, const float* beta, const float* bonus,
+                           void* o, int T, int out_bf16, float scale, cudaStream_t s);
 
 }  // namespace dl

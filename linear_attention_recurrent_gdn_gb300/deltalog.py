@@ -529,8 +529,12 @@ class DeltaLog:
         T = int(q.shape[0])
         for name, t, d in (("q", q, self.d_k), ("k", k, self.d_k), ("v", v, self.d_v)):
             self._need(t, (T, n, self.H, d), self.torch.bfloat16, name)
-        self._need(g, (T, n, self.H), self.torch.float32, "g")
-        self._need(beta, (T, n, self.H), self.torch.float32, "beta")
+        gshape = (T, n, self.H) if self.op == GDN else (T, n, self.H, self.d_k)
+        self._need(g, gshape, self.torch.float32, "g")
+        if self.op != RWKV6:
+            self._need(beta, (T, n, self.H), self.torch.float32, "beta")
+        else:
+            beta = None
         if out is None and want_out:
             out = self.torch.empty((T, n, self.H, self.d_v), dtype=self.out_dtype, device="cuda")
         dl_prefill(self._h, a, q, k, v, g, beta, out)

@@ -169,29 +169,32 @@ def test_graph_window_many_units_bitwise(op, B, H, d):
         w.close()
 
 
+@pytest.mark.parametrize("op", OPS)
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("T", [75, 32, 1])
-def test_chunked_prefill_then_decode(d, T):
+def test_chunked_prefill_then_decode(op, d, T):
     """dl_prefill over T context tokens (ragged last chunk for T=75), then 10
     decode steps: every output and the final state match the oracle run over
     the whole sequence."""
     from linear_attention_recurrent_gdn_gb300 import deltalog as dl
     B, H, M, Td = 3, 4, 8, 10
-    x, S0, _ = make_case(gen.GDN, B, H, d, T + Td, seed=700 + d + T)
-    o_ref, S_ref, S_snap = oracle_run(gen.GDN, x, S0, None, snap=[T - 1])
-    ctx = dl.DeltaLog(gen.GDN, B, H, d, d, M, out_bf16=False)
+    x, S0, bonus = make_case(op, B, H, d, T + Td, seed=700 + d + T + 31 * op)
+    o_ref, S_ref, S_snap = oracle_run(op, x, S0, bonus, snap=[T - 1])
+    ctx = dl.DeltaLog(op, B, H, d, d, M, out_bf16=False)
     ctx.set_state(list(range(B)), S0.cuda())
-    dev = {k: v.cuda() for k, v in x.items()}
-    o_pf = ctx.prefill(list(range(B)), dev["q"][:T].contiguous(), dev["k"][:T].contiguous(),
-                       dev["v"][:T].contiguous(), dev["g"][:T].contiguous(),
-                       dev["beta"][:T].contiguous())
+    if bonus is not None:
+        ctx.set_bonus(bonus.cuda())
+    dev = {k: (v.cuda() if v is not None else None) for k, v in x.items()}
+    sl = lambda key: dev[key][:T].contiguous() if dev[key] is not None else None
+    o_pf = ctx.prefill(list(range(B)), sl("q"), sl("k"), sl("v"), sl("g"), sl("beta"))
     S_pf = ctx.read_state(list(range(B))).cpu().reshape(B * H, d, d).numpy()
     assert rel_err(S_pf, S_snap[0]) <= STATE_TOL
     assert max_step_rel(o_pf.cpu().reshape(T, B * H, d).numpy(), o_ref[:T]) <= OUT_TOL_F32
     outs = []
     for t in range(T, T + Td):
+        beta = dev["beta"][t] if dev["beta"] is not None else None
         outs.append(ctx.step(list(range(B)), dev["q"][t], dev["k"][t], dev["v"][t], dev["g"][t],
-                             dev["beta"][t]).float())
+                             beta).float())
     o = torch.stack(outs).cpu().reshape(Td, B * H, d).numpy()
     assert max_step_rel(o, o_ref[T:]) <= OUT_TOL_F32
     S = ctx.read_state(list(range(B))).cpu().reshape(B * H, d, d).numpy()
@@ -200,13 +203,11 @@ def test_chunked_prefill_then_decode(d, T):
 
 def test_prefill_rules():
     from linear_attention_recurrent_gdn_gb300 import deltalog as dl
-    x, S0, _ = make_case(gen.KDA, 1, 2, 64, 4, seed=9)
-    ctx = dl.DeltaLog(gen.KDA, 1, 2, 64, 64, 4)
-    g2 = torch.zeros(4, 1, 2, device="cuda")
-    with pytest.raises(dl.DeltaLogError) as e:
-        dl.dl_prefill(ctx.handle, [0], x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), g2,
-                      x["beta"].cuda(), None)
-    assert e.value.status == dl.EUNSUPPORTED
+    x, S0, _ = make_case(gen.RWKV6, 1, 2, 64, 4, seed=9)
+    ctx = dl.DeltaLog(gen.RWKV6, 1, 2, 64, 64, 4)
+    with pytest.raises(dl.DeltaLogError) as e:     # RWKV6 needs its bonus first
+        ctx.prefill([0], x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), x["g"].cuda(), None)
+    assert e.value.status == dl.EINVAL
     x, S0, _ = make_case(gen.GDN, 1, 2, 64, 4, seed=9)
     ctx = dl.DeltaLog(gen.GDN, 1, 2, 64, 64, 4)
     dev = {k: v.cuda() for k, v in x.items()}
