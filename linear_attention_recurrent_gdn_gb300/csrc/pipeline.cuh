@@ -7,32 +7,38 @@
 // factors and log-decay metadata (here: the ReplayPrep coefficient block) are
 // shared by all value tiles of a slot-head.
 //
-// Structure on sm_103a (persistent over work units; one or two CTAs per SM):
+// Structure on sm_103a (persistent over work units; two to four CTAs per SM):
 //   * work unit = (slot-head, group of G value tiles); tile = 32 value rows of
 //     the dense base (32 x d_k fp32, contiguous in HBM: 16 KiB at d_k = 128);
-//   * the last warp is the producer.  One lane issues one 1-D bulk copy (TMA
-//     engine) per tile into a ring of `ns` shared-memory stages, completion
-//     counted in bytes on an mbarrier, with an L2 evict-first policy (the base
-//     is read once per step).  The unit's small inputs (coefficient block,
-//     k/q/v, value-side log rows, key log rows on a GDN merge) are copied by
-//     all 32 lanes with 16-byte cp.async into a ring of `na` aux slots: a bulk
-//     copy has a fixed issue cost per copy on this GPU, so it is kept for the
-//     tiles;
-//   * the other `ncw` warps are consumers; warp w owns stages w*R .. w*R+R-1
-//     and processes tiles w, w+ncw, ...  Lane l holds d_k/32 consecutive key
-//     channels; a pass over the 32 rows accumulates per-row partial dot
-//     products, a transposed butterfly (31 shuffles for 32 rows) leaves row
-//     l's sums on lane l, which then finishes that row: log replay, output,
-//     the appended factor; on a merge step the warp then re-reads the tile
-//     from shared memory and writes the updated rows;
+//   * warps 0 .. ncw-1 are consumers, warp ncw the producer, and any further
+//     warps (fused form) prep warps;
+//   * producer: one lane issues one 1-D bulk copy (TMA engine) per stage (one
+//     tile, or two at d_k = 64) into the stage ring, completion counted in
+//     bytes on an mbarrier, with an L2 evict-first policy when the state does
+//     not fit in L2.  The unit's small inputs (k/q/v, log rows, log-decays,
+//     g, beta, bonus; the coefficient block in the two-kernel form) are copied
+//     by all 32 lanes with 16-byte cp.async into a ring of `na` aux slots: a
+//     bulk copy has a fixed issue cost per copy on this GPU, so it is kept for
+//     the tiles.  The producer is on the critical path of every refill, so its
+//     per-tile bookkeeping is incremental (no divisions);
+//   * consumers: warp w owns stages w*R .. w*R+R-1 and processes tiles w,
+//     w+ncw, ...  Lane l holds d_k/32 consecutive key channels; a pass over
+//     the 32 rows accumulates per-row partial dot products, a transposed
+//     butterfly (31 shuffles for 32 rows) leaves row l's sums on lane l, which
+//     then finishes that row: log replay, output, the appended factor; on a
+//     merge step the warp then re-reads the tile from shared memory and writes
+//     the updated rows;
 //   * every wait is bounded (see mbar_wait).  On an append step a consumer
 //     releases its stage right after the tile pass, so the refill overlaps its
 //     epilogue.
-// Two forms of the ReplayPrep stage:
-//   * FUSED (default): one more warp of the same CTA computes each unit's
-//     coefficients from the unit's inputs in its aux slot (prep_unit) and
-//     signals the consumers on a per-slot barrier (cready); no second launch
-//     and no coefficient round trip through HBM;
+// Forms of the ReplayPrep stage:
+//   * FUSED (default): the coefficients are computed inside this kernel from
+//     the unit's inputs in its aux slot (prep_unit) -- by `npw` prep warps that
+//     signal the consumers on a per-slot barrier (cready) when a unit spans
+//     several stages, or by the unit's own consumer warp when it is a single
+//     stage.  No second launch and no coefficient round trip through HBM.
+//     Inside a captured decode window each step is a programmatic dependent of
+//     the previous one (see the producer);
 //   * APPEND: ReplayPrep is its own kernel (replay_prep.cu) and AppendDecode
 //     launches as its programmatic dependent: the producer streams the first
 //     ns tiles before it waits for the coefficient blocks.
