@@ -54,12 +54,23 @@ KERNEL_SOURCES = ["pipeline.cuh", "append_decode.cu", "append_launch.cuh", "appe
                   "append_fused_ne16.cu", "append_fused_ne32.cu", "dl_device.cuh", "layout.h"]
 
 
-def kernel_source_hash():
-    """Hash of the AppendDecode sources; ncu traffic figures are tied to it."""
+def strip_comments(src):
+    """C/C++ source without comments and blank space, so that a change to a
+    comment leaves the hash of the code unchanged."""
+    import re
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return " ".join(src.split())
+
+
+def kernel_source_hash(read=None):
+    """Hash of the AppendDecode sources (code only); ncu traffic figures are tied to it."""
     import hashlib
+    read = read or (lambda f: open(os.path.join(ROOT, "linear_attention_recurrent_gdn_gb300",
+                                                  "csrc", f)).read())
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        h.update(open(os.path.join(ROOT, "linear_attention_recurrent_gdn_gb300", "csrc", f), "rb").read())
+        h.update(strip_comments(read(f)).encode())
     return h.hexdigest()[:16]
 
 
