@@ -273,6 +273,30 @@ dl_status dl_window_create(dl_ctx *ctx, const int32_t *slots, int32_t n,
 dl_status dl_window_launch(dl_window *w);
 dl_status dl_window_destroy(dl_window *w);
 
+/* Ragged decode window (the same Flide step, for batches whose active set
+ * changes from token to token, e.g. branches of different lengths).  Captured
+ * once for up to n_max rows per token; the M per-token slot lists and counts
+ * live in device memory and are refreshed from host memory by the graph's
+ * first node at every launch, so one graph serves any active sets.  Token j
+ * reads rows 0 .. counts[j]-1 of slice j of q, k [M, n_max, H, d_k] bf16,
+ * v [M, n_max, H, d_v] bf16, g [M, n_max, H] or [M, n_max, H, d_k] fp32, beta
+ * [M, n_max, H] fp32 (NULL for RWKV6) and writes the same rows of o
+ * [M, n_max, H, d_v]; rows at or past counts[j] are neither read nor written
+ * (a token may have no rows at all).  Unlike the fixed window, slots may have
+ * any log length and may index a fork source's base.
+ * dl_window_launch_ragged takes the slot ids as a host array [M][n_max] (row
+ * i of token j at j*n_max + i) and the counts [M].  It validates every token
+ * first (ids in range, no duplicates within a token, no fork source that
+ * branches still index: DL_EINVAL / DL_EBUSY, and then nothing is launched),
+ * plans the M tokens on the host slot table, and enqueues the graph on the
+ * context's stream.  A launch waits for the previous launch of the same
+ * window to finish before it rewrites the host plan.  n_max <= min(1024,
+ * num_slots). */
+dl_status dl_window_create_ragged(dl_ctx *ctx, int32_t n_max,
+                                  const void *q, const void *k, const void *v,
+                                  const float *g, const float *beta, void *o, dl_window **out);
+dl_status dl_window_launch_ragged(dl_window *w, const int32_t *slots, const int32_t *counts);
+
 /* ------------------------------------------------------------------------ */
 /* A decode step that allocates no device memory.                            */
 /* The paper has no counterpart: this entry point exists for callers that    */

@@ -43,6 +43,10 @@ struct dl_ctx {
   // launches as a programmatic dependent of the previous step (both ours) and
   // may stream dense-base tiles of rows with a non-empty log before it waits.
   int pdl_chain = 0;
+  // Set while a ragged window is captured: the step reads its rows and their
+  // count from these device buffers (see dl_window_create_ragged).
+  const dl::StepItem* dev_plan = nullptr;
+  const int32_t* dev_rows = nullptr;
   dl_table* table = nullptr;
   dl::Layout L{};
   float* Sbar = nullptr;
@@ -253,6 +257,8 @@ void fill_step_args(dl_ctx* c, dl::StepArgs& a, int32_t row0, int32_t rows, cons
   a.out_bf16 = f.out_bf16;
   a.scale = f.scale;
   a.aux_bytes = c->L.aux_bytes;
+  a.plan_dev = c->dev_plan ? c->dev_plan + row0 : nullptr;   // ragged windows only
+  a.rows_dev = c->dev_rows;
   for (int32_t i = 0; i < rows; ++i) {
     const int32_t* p = &c->plan[4 * (size_t)(row0 + i)];
     a.items[i].slot = p[0];
@@ -863,7 +869,29 @@ struct dl_window {
   std::vector<int32_t> slots;
   cudaGraph_t graph = nullptr;
   cudaGraphExec_t exec = nullptr;
+  // ragged windows: per-token plans and counts, written on the host at each
+  // launch and copied to the device by the graph's first node
+  bool ragged = false;
+  int32_t n_max = 0;
+  void* plan_host = nullptr;   // pinned: [M][n_max] StepItem, then [M] int32 counts
+  void* plan_dev = nullptr;
+  size_t plan_bytes = 0;
+  cudaEvent_t done = nullptr;  // end of the last launch (the host plan is free again)
+  bool launched = false;
+  std::vector<int32_t> scratch;   // one token's plan rows (4 ints each)
 };
+
+static void window_free(dl_window* w) {
+  if (w->exec) cudaGraphExecDestroy(w->exec);
+  if (w->graph) cudaGraphDestroy(w->graph);
+  if (w->done) cudaEventDestroy(w->done);
+  if (w->plan_host) cudaFreeHost(w->plan_host);
+  if (w->plan_dev) cudaFree(w->plan_dev);
+  w->exec = nullptr;
+  w->graph = nullptr;
+  w->done = nullptr;
+  w->plan_host = w->plan_dev = nullptr;
+}
 
 extern "C" {
 
@@ -947,6 +975,7 @@ dl_status dl_window_launch(dl_window* w) {
   dl_ctx* c = w->ctx;
   dl_status rc = check_ctx(c);
   if (rc != DL_OK) return rc;
+  if (w->ragged) return set_err(c, DL_EINVAL, "a ragged window launches with dl_window_launch_ragged");
   const int32_t n = (int32_t)w->slots.size();
   rc = dl_table_step_eager(c->table, w->slots.data(), n);
   if (rc != DL_OK)
@@ -958,9 +987,137 @@ dl_status dl_window_launch(dl_window* w) {
 
 dl_status dl_window_destroy(dl_window* w) {
   if (!w) return DL_OK;
-  if (w->exec) cudaGraphExecDestroy(w->exec);
-  if (w->graph) cudaGraphDestroy(w->graph);
+  if (w->done) cudaEventSynchronize(w->done);   // the graph may still read the plan buffers
+  window_free(w);
   delete w;
+  return DL_OK;
+}
+
+dl_status dl_window_create_ragged(dl_ctx* c, int32_t n_max, const void* q, const void* k,
+                                  const void* v, const float* g, const float* beta, void* o,
+                                  dl_window** out) {
+  if (!out) return DL_EINVAL;
+  *out = nullptr;
+  dl_status rc = check_ctx(c);
+  if (rc != DL_OK) return rc;
+  const dl_config& f = c->cfg;
+  if (n_max < 1 || n_max > dl::MAX_ROWS || n_max > f.num_slots)
+    return set_err(c, DL_EINVAL, "ragged window capacity must be 1..min(%d, num_slots)",
+                   dl::MAX_ROWS);
+  rc = check_step_ptrs(c, n_max, q, k, v, g, beta, o);
+  if (rc != DL_OK) return rc;
+  if (f.op == DL_RWKV6 && !c->bonus)
+    return set_err(c, DL_EINVAL, "RWKV6 needs dl_set_bonus before a window is captured");
+  const int M = f.merge_interval;
+  const size_t H = f.num_heads;
+  const size_t sq = (size_t)n_max * H * f.d_k * 2, sv = (size_t)n_max * H * f.d_v * 2;
+  const size_t sg = (size_t)n_max * H * (f.op == DL_GDN ? 1 : f.d_k) * 4, sb = (size_t)n_max * H * 4;
+  const size_t so = (size_t)n_max * H * f.d_v * (f.out_bf16 ? 2 : 4);
+  std::unique_ptr<dl_window> w(new (std::nothrow) dl_window);
+  if (!w) return set_err(c, DL_ENOMEM, "window allocation");
+  w->ctx = c;
+  w->ragged = true;
+  w->n_max = n_max;
+  w->plan_bytes = (size_t)M * n_max * sizeof(dl::StepItem) + (size_t)M * sizeof(int32_t);
+  w->scratch.resize(4 * (size_t)n_max);
+  if (cudaHostAlloc(&w->plan_host, w->plan_bytes, cudaHostAllocDefault) != cudaSuccess ||
+      cudaMalloc(&w->plan_dev, w->plan_bytes) != cudaSuccess) {
+    window_free(w.get());
+    return set_err(c, DL_ENOMEM, "ragged window plan buffers");
+  }
+  memset(w->plan_host, 0, w->plan_bytes);
+  DL_CUDA(cudaEventCreateWithFlags(&w->done, cudaEventDisableTiming), "window event");
+  const dl::StepItem* items_dev = static_cast<const dl::StepItem*>(w->plan_dev);
+  const int32_t* counts_dev =
+      reinterpret_cast<const int32_t*>(static_cast<const unsigned char*>(w->plan_dev) +
+                                       (size_t)M * n_max * sizeof(dl::StepItem));
+  cudaStream_t cap = nullptr;
+  DL_CUDA(cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking), "capture stream");
+  cudaStream_t saved = c->stream;
+  const bool saved_timing = c->timing;
+  c->stream = cap;
+  c->timing = false;
+  cudaError_t e = cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal);
+  dl_status st = DL_OK;
+  if (e == cudaSuccess) {
+    e = cudaMemcpyAsync(w->plan_dev, w->plan_host, w->plan_bytes, cudaMemcpyHostToDevice, cap);
+    for (int j = 0; j < M && st == DL_OK && e == cudaSuccess; ++j) {
+      c->pdl_chain = (j > 0 && f.staging == DL_STAGE_FUSED) ? 1 : 0;
+      c->dev_plan = items_dev + (size_t)j * n_max;
+      c->dev_rows = counts_dev + j;
+      st = run_step(c, nullptr, n_max, static_cast<const unsigned char*>(q) + j * sq,
+                    static_cast<const unsigned char*>(k) + j * sq,
+                    static_cast<const unsigned char*>(v) + j * sv,
+                    reinterpret_cast<const float*>(reinterpret_cast<const unsigned char*>(g) + j * sg),
+                    beta ? reinterpret_cast<const float*>(reinterpret_cast<const unsigned char*>(beta) + j * sb)
+                         : nullptr,
+                    static_cast<unsigned char*>(o) + j * so, false);
+    }
+    cudaError_t e2 = cudaStreamEndCapture(cap, &w->graph);
+    if (e == cudaSuccess) e = e2;
+  }
+  c->stream = saved;
+  c->timing = saved_timing;
+  c->pdl_chain = 0;
+  c->dev_plan = nullptr;
+  c->dev_rows = nullptr;
+  cudaStreamDestroy(cap);
+  if (st != DL_OK) {
+    window_free(w.get());
+    c->sticky = DL_OK;   // a failed capture leaves the context usable
+    return set_err(c, DL_ECUDA, "window capture failed: %s", c->err.c_str());
+  }
+  if (e != cudaSuccess) {
+    window_free(w.get());
+    return set_err(c, DL_ECUDA, "window capture: %s", cudaGetErrorString(e));
+  }
+  e = cudaGraphInstantiate(&w->exec, w->graph, 0);
+  if (e != cudaSuccess) {
+    window_free(w.get());
+    return set_err(c, DL_ECUDA, "graph instantiate: %s", cudaGetErrorString(e));
+  }
+  *out = w.release();
+  return DL_OK;
+}
+
+dl_status dl_window_launch_ragged(dl_window* w, const int32_t* slots, const int32_t* counts) {
+  if (!w) return DL_EINVAL;
+  dl_ctx* c = w->ctx;
+  dl_status rc = check_ctx(c);
+  if (rc != DL_OK) return rc;
+  if (!w->ragged) return set_err(c, DL_EINVAL, "not a ragged window");
+  if (!counts || !slots) return set_err(c, DL_EINVAL, "NULL slot list");
+  const int M = c->cfg.merge_interval;
+  const int32_t n_max = w->n_max;
+  // validate every token before any is applied: ids, duplicates, fork sources
+  std::vector<int32_t> refs(c->cfg.num_slots);
+  dl_table_get(c->table, nullptr, nullptr, refs.data());
+  for (int j = 0; j < M; ++j) {
+    const int32_t cnt = counts[j];
+    if (cnt < 0 || cnt > n_max) return set_err(c, DL_EINVAL, "token %d: count out of range", j);
+    const int32_t* sl = slots + (size_t)j * n_max;
+    rc = dl_table_check(c->table, sl, cnt);
+    if (rc != DL_OK) return set_err(c, rc, "token %d: invalid slot list", j);
+    for (int32_t i = 0; i < cnt; ++i)
+      if (refs[sl[i]] > 0) return set_err(c, DL_EBUSY, "token %d: slot %d is a fork source", j, sl[i]);
+  }
+  // the previous launch's graph has copied the plan only once it has run
+  if (w->launched) DL_CUDA(cudaEventSynchronize(w->done), "window wait");
+  dl::StepItem* items = static_cast<dl::StepItem*>(w->plan_host);
+  int32_t* cnt_host = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(w->plan_host) +
+                                                 (size_t)M * n_max * sizeof(dl::StepItem));
+  for (int j = 0; j < M; ++j) {
+    const int32_t cnt = counts[j];
+    rc = dl_table_step(c->table, slots + (size_t)j * n_max, cnt, w->scratch.data());
+    if (rc != DL_OK) return set_err(c, rc, "token %d: slot table refused the step", j);
+    for (int32_t i = 0; i < cnt; ++i)
+      items[(size_t)j * n_max + i] =
+          dl::StepItem{w->scratch[4 * i], w->scratch[4 * i + 1], w->scratch[4 * i + 2]};
+    cnt_host[j] = cnt;
+  }
+  DL_CUDA(cudaGraphLaunch(w->exec, c->stream), "graph launch");
+  DL_CUDA(cudaEventRecord(w->done, c->stream), "window event");
+  w->launched = true;
   return DL_OK;
 }
 

@@ -64,8 +64,25 @@ struct StepArgs {
   int32_t aux_bytes;     // bytes of one aux slot
   int32_t out_bf16;
   float scale;
+  // Device-resident plan (ragged decode windows): when set, the launch reads
+  // its rows from plan_dev and processes min(*rows_dev, rows) of them; `rows`
+  // is then the capacity the grid was sized for.  Otherwise the rows are
+  // items[0 .. rows).
+  const StepItem* plan_dev;
+  const int32_t* rows_dev;
   StepItem items[MAX_ROWS];
 };
+
+// The plan row `row` of a launch, from the parameters or the device plan.
+__device__ __forceinline__ StepItem step_item(const StepArgs& a, int row) {
+  return a.plan_dev ? a.plan_dev[row] : a.items[row];
+}
+// Rows this launch processes (a device-resident count is clamped to the capacity).
+__device__ __forceinline__ int step_rows(const StepArgs& a) {
+  if (!a.rows_dev) return a.rows;
+  const int r = *a.rows_dev;
+  return r < 0 ? 0 : (r < a.rows ? r : a.rows);
+}
 
 // Arguments of the standalone merge / read-state kernel and of the set-state
 // and fork copy kernels.

@@ -191,6 +191,8 @@ extern "C" dl_status dl_step_noalloc(const dl_config* cfg, const dl_state_view* 
   a.tps = dl::tiles_per_stage(f.d_k, a.G);
   a.l2_stream = (double)n * f.num_heads * f.d_v * f.d_k * 4 > 0.75 * d.l2_bytes ? 1 : 0;
   a.pdl_prefetch = 0;
+  a.plan_dev = nullptr;
+  a.rows_dev = nullptr;
   const long units = n_sh * a.NG;
   const long slots_gpu = (long)sh.cps * d.num_sms;
   const int grid = (int)(units < slots_gpu ? units : slots_gpu);

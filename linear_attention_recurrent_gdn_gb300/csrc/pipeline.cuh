@@ -111,7 +111,7 @@ template <int OP, int DK, int DV, int MODE>
 __device__ __forceinline__ void issue_aux(const StepArgs& a, const Layout& Lay, const UnitPos& p,
                                           unsigned char* ax, int lane) {
   constexpr bool DELTA = OP != RWKV6;
-  const StepItem it = a.items[p.row];
+  const StepItem it = step_item(a, p.row);
   const size_t sh = p.sh;
   const uint32_t base = smem_u32(ax);
   if constexpr (MODE == APPEND) {
@@ -172,7 +172,7 @@ template <int OP, int DK, int DV>
 __device__ __forceinline__ void issue_coef_and_arrive(const StepArgs& a, const Layout& Lay,
                                                       const UnitPos& p, unsigned char* ax,
                                                       uint32_t bar, int lane) {
-  const StepItem it = a.items[p.row];
+  const StepItem it = step_item(a, p.row);
   const bool merge = (it.n + 1 == a.M);
   copy_seg(smem_u32(ax + Lay.aux_coef), a.coef + (size_t)p.sh * a.CB,
            (merge ? Lay.CB : Lay.P0) * 4u, lane);
@@ -195,7 +195,7 @@ __device__ __forceinline__ void prep_unit(const StepArgs& a, const Layout& Lay, 
   constexpr int SHIFT = NE == 32 ? 0 : NE == 16 ? 1 : 2;   // entry of lane l: l >> SHIFT
   const int lane_entry = lane >> SHIFT;
   const bool entry_writer = (lane & ((1 << SHIFT) - 1)) == 0;
-  const StepItem it = a.items[p.row];
+  const StepItem it = step_item(a, p.row);
   const int n = it.n, slot = it.slot;
   const bool merge = (n + 1 == a.M);
   const bool owner = (p.grp == 0);
@@ -393,7 +393,7 @@ __device__ __forceinline__ bool consume_append(const StepArgs& a, const Layout& 
                                                bool may_release) {
   constexpr int VEC = DK / 32;
   constexpr bool DELTA = OP != RWKV6;
-  const StepItem it = a.items[p.row];
+  const StepItem it = step_item(a, p.row);
   const int n = it.n;
   const bool merge = (n + 1 == a.M);
   const float* cf = av.cf;
@@ -525,7 +525,7 @@ __device__ __forceinline__ void consume_eager(const StepArgs& a, const Layout& L
                                               const UnitPos& p, int vt, const float* T,
                                               unsigned char* ax, int lane, float g_s, float beta_s) {
   constexpr int VEC = DK / 32;
-  const StepItem it = a.items[p.row];
+  const StepItem it = step_item(a, p.row);
   float kv[VEC], qv[VEC], D[VEC], kh[VEC], qh[VEC];
   const uint16_t* kq16 = reinterpret_cast<const uint16_t*>(ax + Lay.e_kq);
   ldvec_bf16<VEC>(kv, kq16 + lane * VEC);
@@ -640,7 +640,7 @@ __global__ void __maxnreg__(128) pipe_kernel(const __grid_constant__ StepArgs a)
   }
   __syncthreads();
 
-  const int n_units = a.rows * a.H * a.NG;
+  const int n_units = step_rows(a) * a.H * a.NG;
   const int my_units =
       (int)blockIdx.x < n_units ? (n_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
   const int my_tiles = my_units * IPU;   // stage items of this CTA
@@ -687,7 +687,7 @@ __global__ void __maxnreg__(128) pipe_kernel(const __grid_constant__ StepArgs a)
         bool need = ti >= NS || (kt == ka && ka >= NA);
         if constexpr (MODE == FUSED) {
           if (!need && !a.pdl_prefetch) need = true;
-          if (!need && a.items[unit_pos(a, (int)blockIdx.x + kt * (int)gridDim.x).row].n == 0)
+          if (!need && step_item(a, unit_pos(a, (int)blockIdx.x + kt * (int)gridDim.x).row).n == 0)
             need = true;
         }
         if (need) {
@@ -726,7 +726,8 @@ __global__ void __maxnreg__(128) pipe_kernel(const __grid_constant__ StepArgs a)
         }
         // DeltaLog steps read the base the slot indexes (a fork source's until
         // the first merge); the eager step reads the slot's own state
-        const int base = (MODE == EAGER) ? a.items[p.row].slot : a.items[p.row].base;
+        const StepItem it = step_item(a, p.row);
+        const int base = (MODE == EAGER) ? it.slot : it.base;
         src_unit = a.Sbar + (((size_t)base * a.H + p.h) * DV + (size_t)p.grp * G * BV) * DK;
         ++ka;
         if (++ax_x == NA) {

@@ -50,10 +50,10 @@ replay_prep_kernel(const __grid_constant__ StepArgs a) {
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sh = blockIdx.x * RP_WARPS + warp;      // (row, head) of the step's inputs
-  if (sh >= a.rows * a.H) return;
+  if (sh >= step_rows(a) * a.H) return;
   const int row = sh / a.H, h = sh - row * a.H;
   const Layout Lay = make_layout(OP, a.M, DK, DV);
-  const StepItem it = a.items[row];
+  const StepItem it = step_item(a, row);
   const int n = it.n, slot = it.slot;
   const bool merge = (n + 1 == a.M);
   const int Mcap = Lay.Mcap, Mcap4 = Lay.Mcap4;

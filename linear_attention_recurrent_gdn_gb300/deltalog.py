@@ -29,7 +29,8 @@ EXPORTS = [
     "dl_step", "dl_step_host", "dl_decode_host", "dl_step_eager", "dl_merge", "dl_read_state", "dl_get_meta",
     "dl_sync", "dl_set_timing", "dl_get_timing", "dl_last_error", "dl_status_str",
     "dl_abi_version", "dl_checkpoint_bytes", "dl_checkpoint_save", "dl_checkpoint_load",
-    "dl_window_create", "dl_window_launch", "dl_window_destroy", "dl_prefill",
+    "dl_window_create", "dl_window_launch", "dl_window_destroy", "dl_window_create_ragged",
+    "dl_window_launch_ragged", "dl_prefill",
     "dl_step_noalloc",
 ]
 
@@ -97,6 +98,8 @@ def _load():
         "dl_window_create": ([P, P, I32, P, P, P, P, P, P, PP], I32),
         "dl_window_launch": ([P], I32),
         "dl_window_destroy": ([P], I32),
+        "dl_window_create_ragged": ([P, I32, P, P, P, P, P, P, PP], I32),
+        "dl_window_launch_ragged": ([P, P, P], I32),
         "dl_prefill": ([P, P, I32, I32, P, P, P, P, P, P], I32),
         "dl_step_noalloc": ([ctypes.POINTER(dl_config), ctypes.POINTER(dl_state_view), P, I32,
                              P, P, P, P, P, P, P, ctypes.c_char_p, I32], I32),
@@ -306,6 +309,21 @@ def dl_window_destroy(w):
     _lib.dl_window_destroy(w)
 
 
+def dl_window_create_ragged(ctx, n_max, q, k, v, g, beta, o):
+    h = ctypes.c_void_p()
+    _check(_lib.dl_window_create_ragged(ctx, int(n_max), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                        _ptr(beta), _ptr(o), ctypes.byref(h)), ctx)
+    return h
+
+
+def dl_window_launch_ragged(ctx, w, slots, counts):
+    """slots: int32 host array [M, n_max]; counts: int32 host array [M]."""
+    s = np.ascontiguousarray(slots, dtype=np.int32)
+    c = np.ascontiguousarray(counts, dtype=np.int32)
+    _check(_lib.dl_window_launch_ragged(w, s.ctypes.data_as(ctypes.c_void_p),
+                                        c.ctypes.data_as(ctypes.c_void_p)), ctx)
+
+
 def dl_step_noalloc(cfg, state, plan, q, k, v, g, beta, o, stream=None):
     """One step on caller-owned buffers with no allocation inside the library.
     `state` maps dl_state_view field names to torch tensors (bonus may be None);
@@ -375,6 +393,46 @@ class DecodeWindow:
 
     def launch(self):
         dl_window_launch(self.ctx.handle, self._h)
+        return self.out
+
+    def close(self):
+        if getattr(self, "_h", None):
+            dl_window_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class RaggedWindow:
+    """A captured merge window whose per-token active slots change from launch
+    to launch; launch(slot_lists) replays it on the context's stream."""
+
+    def __init__(self, ctx, n_max, q, k, v, g, beta, out):
+        if out is None:
+            out = ctx.torch.empty((ctx.M, n_max, ctx.H, ctx.d_v), dtype=ctx.out_dtype,
+                                  device="cuda")
+        self.ctx, self.out, self.n_max = ctx, out, int(n_max)
+        self._keep = (q, k, v, g, beta)
+        self._h = dl_window_create_ragged(ctx.handle, n_max, q, k, v, g, beta, out)
+
+    def launch(self, slot_lists):
+        """slot_lists: M lists of slot ids (token j's active rows, in input-row order)."""
+        M = self.ctx.M
+        if len(slot_lists) != M:
+            raise ValueError("a window takes %d slot lists" % M)
+        slots = np.full((M, self.n_max), -1, dtype=np.int32)
+        counts = np.zeros(M, dtype=np.int32)
+        for j, lst in enumerate(slot_lists):
+            lst = list(lst)
+            if len(lst) > self.n_max:
+                raise ValueError("token %d has more than n_max rows" % j)
+            slots[j, :len(lst)] = lst
+            counts[j] = len(lst)
+        dl_window_launch_ragged(self.ctx.handle, self._h, slots, counts)
         return self.out
 
     def close(self):
@@ -539,6 +597,11 @@ class DeltaLog:
             out = self.torch.empty((T, n, self.H, self.d_v), dtype=self.out_dtype, device="cuda")
         dl_prefill(self._h, a, q, k, v, g, beta, out)
         return out
+
+    def window_ragged(self, n_max, q, k, v, g, beta=None, out=None):
+        """Capture one merge window for up to n_max rows per token whose active
+        slots are given at each launch; tensors are [M, n_max, ...] device buffers."""
+        return RaggedWindow(self, n_max, q, k, v, g, beta, out)
 
     def window(self, slots, q, k, v, g, beta=None, out=None):
         """Capture one merge window (M tokens) of `slots` into a CUDA graph; the

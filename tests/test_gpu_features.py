@@ -169,6 +169,93 @@ def test_graph_window_many_units_bitwise(op, B, H, d):
         w.close()
 
 
+@pytest.mark.parametrize("op,d", [(gen.GDN, 128), (gen.KDA, 128), (gen.RWKV6, 64)])
+def test_ragged_window_matches_stepping_bitwise(op, d):
+    """A ragged window (device-resident per-token slot lists and counts, tail
+    padding) replayed over changing active sets gives the bits of plain steps
+    with the same rows: random subsets per token, an empty token, a full token,
+    and branches that index a fork source's base with non-empty logs."""
+    from linear_attention_recurrent_gdn_gb300 import deltalog as dl
+    import random
+    S_, H, M, W = 10, 4, 4, 3
+    T = M * W
+    n_max = S_ - 1                      # slot 0 becomes a fork source (frozen)
+    x, S0, bonus = make_case(op, n_max, H, d, T + 2, seed=660 + op, device="cuda")
+    _, S0a, _ = make_case(op, S_, H, d, 1, seed=661 + op, device="cuda")
+    ctxs = [dl.DeltaLog(op, S_, H, d, d, M) for _ in range(2)]
+    for c in ctxs:
+        c.set_state(list(range(S_)), S0a)
+        if bonus is not None:
+            c.set_bonus(bonus)
+        for t in (T, T + 1):           # two tokens on slot 0, then fork it into 8 and 9
+            sl = slice(0, 1)
+            b = x["beta"][t][sl] if x["beta"] is not None else None
+            c.step([0], x["q"][t][sl], x["k"][t][sl], x["v"][t][sl], x["g"][t][sl], b)
+        c.fork(0, [8, 9])
+    a, r = ctxs
+    rng = random.Random(5 + op)
+    lists = []
+    for t in range(T):
+        if t == 2:
+            lst = []
+        elif t == 5:
+            lst = list(range(1, S_))
+        else:
+            lst = rng.sample(range(1, S_), rng.randint(1, n_max))
+        lists.append(lst)
+    ref = torch.zeros((T, n_max, H, d), dtype=torch.bfloat16, device="cuda")
+    for t, lst in enumerate(lists):
+        k_ = len(lst)
+        if k_:
+            b = x["beta"][t][:k_] if x["beta"] is not None else None
+            a.step(lst, x["q"][t][:k_], x["k"][t][:k_], x["v"][t][:k_], x["g"][t][:k_], b,
+                   ref[t][:k_])
+    buf = {k_: (v_[:M].clone() if v_ is not None else None) for k_, v_ in x.items()}
+    win = r.window_ragged(n_max, buf["q"], buf["k"], buf["v"], buf["g"], buf["beta"])
+    for w in range(W):
+        for k_, v_ in x.items():
+            if v_ is not None:
+                buf[k_].copy_(v_[w * M:(w + 1) * M])
+        out = win.launch(lists[w * M:(w + 1) * M])
+        torch.cuda.synchronize()
+        for j in range(M):
+            k_ = len(lists[w * M + j])
+            assert torch.equal(out[j][:k_], ref[w * M + j][:k_]), (w, j)
+    assert torch.equal(a.read_state(list(range(S_))), r.read_state(list(range(S_))))
+    assert [list(m) for m in a.get_meta()] == [list(m) for m in r.get_meta()]
+    win.close()
+
+
+def test_ragged_window_refusals():
+    from linear_attention_recurrent_gdn_gb300 import deltalog as dl
+    S_, H, d, M = 6, 2, 64, 4
+    x, S0, _ = make_case(gen.GDN, S_, H, d, M, seed=670, device="cuda")
+    c = dl.DeltaLog(gen.GDN, S_, H, d, d, M)
+    c.set_state(list(range(S_)), S0)
+    c.fork(0, [5])
+    win = c.window_ragged(4, x["q"][:, :4].contiguous(), x["k"][:, :4].contiguous(),
+                          x["v"][:, :4].contiguous(), x["g"][:, :4].contiguous(),
+                          x["beta"][:, :4].contiguous())
+    meta = [list(m) for m in c.get_meta()]
+    with pytest.raises(dl.DeltaLogError) as e:          # fork source in token 2
+        win.launch([[1], [2], [0, 3], []])
+    assert e.value.status == dl.EBUSY
+    with pytest.raises(dl.DeltaLogError) as e:          # duplicate in a token
+        win.launch([[1, 1], [], [], []])
+    assert e.value.status == dl.EINVAL
+    with pytest.raises(dl.DeltaLogError) as e:          # id out of range
+        win.launch([[], [], [], [S_]])
+    assert e.value.status == dl.EINVAL
+    assert [list(m) for m in c.get_meta()] == meta       # nothing was applied
+    with pytest.raises(dl.DeltaLogError) as e:          # fixed-window launch of a ragged window
+        dl.dl_window_launch(c.handle, win._h)
+    assert e.value.status == dl.EINVAL
+    win.launch([[1, 2], [5], [3, 4, 1], [2]])
+    torch.cuda.synchronize()
+    assert list(c.get_meta()[0])[1:5] == [2, 2, 1, 1]
+    win.close()
+
+
 @pytest.mark.parametrize("op", OPS)
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("T", [75, 32, 1])
