@@ -562,23 +562,40 @@ def run_fork(args):
                       staging=dl.STAGE_FUSED if fused else dl.STAGE_KERNELS)
     ctx.set_state(list(range(R)), gen.initial_state(R, H, d, d, seed, device=dev))
     t0 = time.time()
-    for t in range(Tc):
-        x = gen.step_inputs(0, R, H, d, d, seed, t, device=dev)
-        ctx.step(list(range(R)), x["q"], x["k"], x["v"], x["g"], x["beta"])
+    xc = gen.make_inputs(0, Tc, R, H, d, d, seed, device=dev)     # the shared contexts
+    ctx.prefill(list(range(R)), xc["q"], xc["k"], xc["v"], xc["g"], xc["beta"], want_out=False)
     torch.cuda.synchronize()
-    log("bases built in %.1fs" % (time.time() - t0))
-    xq = gen.make_inputs(0, Tq, R * NB, H, d, d, seed + 1, device=dev)
-    out = torch.empty((R * NB, H, d), dtype=torch.bfloat16, device=dev)
-    act_slots = [[R + int(b) for b in order[:c]] for c in counts]
+    del xc
+    log("bases built (chunked prefill of %d tokens) in %.1fs" % (Tc, time.time() - t0))
+    NBR = R * NB
+    use_graph = not args.no_graph
+    Tpad = (Tq + M - 1) // M * M if use_graph else Tq   # windows of M tokens; the tail is padding
+    xq = gen.make_inputs(0, Tq, NBR, H, d, d, seed + 1, device=dev)
+    if Tpad > Tq:
+        xq = {k_: torch.cat([v_, torch.zeros((Tpad - Tq,) + tuple(v_.shape[1:]), dtype=v_.dtype,
+                                             device=dev)]).contiguous()
+              for k_, v_ in xq.items()}
+    out = torch.empty((Tpad, NBR, H, d), dtype=torch.bfloat16, device=dev)
+    act_slots = [[R + int(b) for b in order[:c]] for c in counts] + [[]] * (Tpad - Tq)
     branches = [[R + r * NB + i for i in range(NB)] for r in range(R)]
+    wins = None
+    if use_graph:
+        wins = [ctx.window_ragged(NBR, xq["q"][w_ * M:(w_ + 1) * M], xq["k"][w_ * M:(w_ + 1) * M],
+                                  xq["v"][w_ * M:(w_ + 1) * M], xq["g"][w_ * M:(w_ + 1) * M],
+                                  xq["beta"][w_ * M:(w_ + 1) * M], out[w_ * M:(w_ + 1) * M])
+                for w_ in range(Tpad // M)]
 
     def one():
         for r in range(R):
             ctx.fork(r, branches[r])
+        if wins:
+            for w_, win in enumerate(wins):
+                win.launch(act_slots[w_ * M:(w_ + 1) * M])
+            return
         for t in range(Tq):
             c = counts[t]
             ctx.step(act_slots[t], xq["q"][t][:c], xq["k"][t][:c], xq["v"][t][:c],
-                     xq["g"][t][:c], xq["beta"][t][:c], out[:c])
+                     xq["g"][t][:c], xq["beta"][t][:c], out[t][:c])
     for _ in range(args.warmup):
         one()
     barrier(dist)
@@ -598,10 +615,14 @@ def run_fork(args):
               "config": {"workload": w["desc"], "op": "gdn", "requests": R, "branches": NB,
                          "H": H, "d_k": d, "d_v": d, "M": M, "ctx_tokens": Tc,
                          "branch_tokens": int(lens.sum()), "staging": args.staging,
+                         "loop": ("ragged CUDA graphs, one per M tokens (dl_window_*_ragged)"
+                                  if wins else "dl_step per token"),
                          "l2": "inputs larger than L2 (576 slots x 1 MiB state)"},
-              "gpu_launches": (R + (1 if fused else 2) * Tq) * args.steps}
+              "gpu_launches": (R + (1 if fused else 2) * Tpad) * args.steps}
     if rank == 0:
         print(json.dumps(result), flush=True)
+    for win in wins or []:
+        win.close()
     ctx.close()
     if dist is not None:
         dist.destroy_process_group()
