@@ -74,10 +74,6 @@ __device__ __forceinline__ uint32_t stage_parity(int i, int R, int ncw) {
   return (uint32_t)((i / ncw) / R) & 1u;
 }
 
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 struct UnitPos {
   int sh, row, h, grp;
 };
@@ -90,6 +86,46 @@ __device__ __forceinline__ UnitPos unit_pos(const StepArgs& a, int u) {
   p.h = p.sh - p.row * a.H;
   return p;
 }
+
+// Walks a CTA's units u, u + grid, u + 2*grid, ... without dividing: the
+// position advances by the precomputed quotients and remainders of the grid
+// stride (by NG, then by H).
+struct UnitWalk {
+  UnitPos p;
+  int NG, H, sq, sr, hq0, hr0, hq1, hr1;
+  __device__ __forceinline__ void init(const StepArgs& a, int u0) {
+    NG = a.NG;
+    H = a.H;
+    p = unit_pos(a, u0);
+    const int grid = (int)gridDim.x;
+    sq = grid / NG;
+    sr = grid - sq * NG;
+    hq0 = sq / H;
+    hr0 = sq - hq0 * H;
+    hq1 = (sq + 1) / H;
+    hr1 = (sq + 1) - hq1 * H;
+  }
+  __device__ __forceinline__ void next() {
+    int dq, dr;
+    p.grp += sr;
+    if (p.grp >= NG) {
+      p.grp -= NG;
+      p.sh += sq + 1;
+      dq = hq1;
+      dr = hr1;
+    } else {
+      p.sh += sq;
+      dq = hq0;
+      dr = hr0;
+    }
+    p.h += dr;
+    p.row += dq;
+    if (p.h >= H) {
+      p.h -= H;
+      p.row += 1;
+    }
+  }
+};
 
 __device__ __forceinline__ void store_out(const StepArgs& a, size_t idx, float val) {
   if (a.out_bf16) static_cast<uint16_t*>(a.o)[idx] = f2bf16(val);
@@ -681,6 +717,8 @@ __global__ void __maxnreg__(128) pipe_kernel(const __grid_constant__ StepArgs a)
     int ax_x = 0;                 // aux slot of unit ka
     uint32_t ax_par = 0;          // phase parity of that slot for unit ka
     const float* src_unit = nullptr;
+    UnitWalk walk;                // position of unit ka
+    walk.init(a, (int)blockIdx.x);
     while (ti < my_tiles) {
       if (!primary_done) {
         // the next wait needs consumers to make progress, and they need inputs
@@ -706,7 +744,7 @@ __global__ void __maxnreg__(128) pipe_kernel(const __grid_constant__ StepArgs a)
           ok = false;
           break;
         }
-        const UnitPos p = unit_pos(a, (int)blockIdx.x + ka * (int)gridDim.x);
+        const UnitPos p = walk.p;
         unsigned char* ax = auxm + (size_t)x * aux_bytes;
         if constexpr (MODE == APPEND) {
           issue_aux<OP, DK, DV, MODE>(a, Lay, p, ax, lane);
@@ -730,6 +768,7 @@ __global__ void __maxnreg__(128) pipe_kernel(const __grid_constant__ StepArgs a)
         const int base = (MODE == EAGER) ? it.slot : it.base;
         src_unit = a.Sbar + (((size_t)base * a.H + p.h) * DV + (size_t)p.grp * G * BV) * DK;
         ++ka;
+        walk.next();
         if (++ax_x == NA) {
           ax_x = 0;
           ax_par ^= 1u;
@@ -788,12 +827,14 @@ __global__ void __maxnreg__(128) pipe_kernel(const __grid_constant__ StepArgs a)
     // Prep warp pw owns the aux slots x with x % npw == pw and takes their
     // units in order, so it waits on every phase of those slots' barriers.
     const int pw = warp - NCWr - 1, NPW = a.npw;
-    for (int kk = 0; kk < my_units; ++kk) {
+    UnitWalk walk;
+    walk.init(a, (int)blockIdx.x);
+    for (int kk = 0; kk < my_units; ++kk, walk.next()) {
       const int x = kk % NA;
       if (x % NPW != pw) continue;
       if (!__all_sync(0xffffffffu, mbar_wait(bars.afull(x), (kk / NA) & 1, a.status, DEV_TIMEOUT_AUX)))
         break;
-      const UnitPos p = unit_pos(a, (int)blockIdx.x + kk * (int)gridDim.x);
+      const UnitPos p = walk.p;
       unsigned char* ax = auxm + (size_t)x * aux_bytes;
       prep_unit<OP, DK, DV, NE>(a, Lay, p, ax, lane);
       __syncwarp();
@@ -812,14 +853,15 @@ __global__ void __maxnreg__(128) pipe_kernel(const __grid_constant__ StepArgs a)
   uint32_t xpar = (uint32_t)(kk / NA) & 1u;
   int r = 0;
   uint32_t spar = 0;
-  int kk_pos = -1;
-  UnitPos p{};
+  UnitWalk walk;                // position of unit kk
+  walk.init(a, (int)blockIdx.x + kk * (int)gridDim.x);
   for (int i = warp; i < my_tiles; i += NCWr) {
     if (i != warp) {   // advance from the previous tile of this warp
       j += NCWr;
       while (j >= IPU) {
         j -= IPU;
         ++kk;
+        walk.next();
         if (++x == NA) {
           x = 0;
           xpar ^= 1u;
@@ -830,10 +872,7 @@ __global__ void __maxnreg__(128) pipe_kernel(const __grid_constant__ StepArgs a)
         spar ^= 1u;
       }
     }
-    if (kk != kk_pos) {
-      p = unit_pos(a, (int)blockIdx.x + kk * (int)gridDim.x);
-      kk_pos = kk;
-    }
+    const UnitPos p = walk.p;
     const int vt0 = p.grp * G + j * TPS;
     const int s = warp * R + r;   // = stage_of(i, R, NCWr)
     float g_s = 0.f, beta_s = 0.f;
@@ -876,9 +915,10 @@ __global__ void __maxnreg__(128) pipe_kernel(const __grid_constant__ StepArgs a)
                                               t == TPS - 1);
       }
     }
-    // order this warp's shared-memory writes (u_t rows of a merge) before the
-    // bulk copies that will refill the slots once they are released
-    fence_proxy_async_smem();
+    // No proxy fence here: consumers never write shared memory that a bulk
+    // copy refills (tiles are read-only; the aux slots they write are refilled
+    // by cp.async, which is in the generic proxy), so the mbarrier release and
+    // the producer's acquiring wait order everything.
     __syncwarp();
     if (lane == 0) {
       if (!released) mbar_arrive(bars.empty(s));
