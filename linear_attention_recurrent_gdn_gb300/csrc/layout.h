@@ -156,6 +156,29 @@ inline PipePlan plan_pipeline(int dk, int aux_bytes, int G, int smem_optin, int 
   const bool fused = npw >= 0;
   const int (*cand)[3] = !big ? c8k : fused ? c16k_fused : c16k;
   const int ncand = !big ? 6 : fused ? 6 : 5;
+  if (npw == 0) {
+    // One-stage units, each prepared by its own consumer warp: a warp's aux
+    // slots are how far ahead its units' inputs load (measured on GB300: one
+    // slot per warp leaves ~1.3 us of input latency exposed per unit), so take
+    // the shape with the most slots per consumer warp, counting up to 3, and
+    // among those the earliest in the list (more CTAs per SM).  Shapes with
+    // one CTA per SM (one producer) only come in when no other fits.
+    PipePlan best{0, 0, 0, 0, 0, 0};
+    int best_depth = 0;
+    for (int ci = 0; ci < ncand; ++ci) {
+      if (cand[ci][0] < 2) continue;
+      const PipePlan p = fit_pipeline(cand[ci][0], cand[ci][1], cand[ci][2], dk, aux_bytes, G,
+                                      smem_optin, smem_per_sm, tps, npw, regs);
+      if (p.ns == 0) continue;
+      int depth = p.na / p.ncw;
+      if (depth > 3) depth = 3;
+      if (depth > best_depth) {
+        best = p;
+        best_depth = depth;
+      }
+    }
+    if (best.ns > 0) return best;
+  }
   for (int ci = 0; ci < ncand; ++ci) {
     const PipePlan p = fit_pipeline(cand[ci][0], cand[ci][1], cand[ci][2], dk, aux_bytes, G,
                                     smem_optin, smem_per_sm, tps, npw, regs);
