@@ -166,6 +166,93 @@ def test_fork_workload():
         assert rel_err(final[i], S_ref) <= STATE_TOL, b
 
 
+def test_fork_workload_prefill_and_ragged_windows():
+    """The fork workload through the calls a serving loop makes: the bases by one
+    chunked prefill of the 2048 context tokens, the branch decode through one
+    ragged CUDA-graph window (device-resident per-token slot lists, padded
+    tail) relaunched every M tokens.  Sampled branches match the oracle over
+    context + branch tokens; bookkeeping matches the oracle model at every
+    window."""
+    from linear_attention_recurrent_gdn_gb300 import deltalog as dl
+    R, NB, H, d, M, Tc = 64, 8, 16, 128, 16, 2048
+    dev = torch.device("cuda")
+    seed_c, seed_q = 2104, 2105
+    rng = np.random.default_rng(17)
+    lens = rng.integers(16, 257, size=R * NB)
+    order = np.argsort(-lens, kind="stable")
+    S = R + R * NB
+    NBR = R * NB
+    ctx = dl.DeltaLog(gen.GDN, S, H, d, d, M)
+    model = oracle.SlotTableModel(S, M)
+    S0 = gen.initial_state(R, H, d, d, seed_c, device=dev)
+    ctx.set_state(list(range(R)), S0)
+    model.set_state(list(range(R)))
+    xc = gen.make_inputs(gen.GDN, Tc, R, H, d, d, seed_c, device=dev)
+    ctx.prefill(list(range(R)), xc["q"], xc["k"], xc["v"], xc["g"], xc["beta"], want_out=False)
+    sel_br = [int(order[0]), int(order[-1]), 7, 411]
+    sel_req = sorted({b // NB for b in sel_br})
+    ri = torch.tensor(sel_req, device=dev)
+    keep_c = {key: xc[key][:, ri].cpu() for key in xc}
+    del xc
+    for r in range(R):
+        br = [R + r * NB + i for i in range(NB)]
+        ctx.fork(r, br)
+        model.fork(r, br)
+    slot_of = lambda b: R + int(b)
+    Tq = int(lens.max())
+    W = (Tq + M - 1) // M
+    buf = {key: torch.zeros((M, NBR, H) + ((d,) if key in ("q", "k", "v") else ()),
+                            dtype=torch.bfloat16 if key in ("q", "k", "v") else torch.float32,
+                            device=dev) for key in ("q", "k", "v", "g", "beta")}
+    win = ctx.window_ragged(NBR, buf["q"], buf["k"], buf["v"], buf["g"], buf["beta"])
+    keep_q = {b: {key: [] for key in keep_c} for b in sel_br}
+    outs = {b: [] for b in sel_br}
+    for w in range(W):
+        lists, poss = [], []
+        for j in range(M):
+            t = w * M + j
+            count = int((lens > t).sum()) if t < Tq else 0
+            act = order[:count]
+            if count:
+                x = gen.step_inputs(gen.GDN, count, H, d, d, seed_q, t, device=dev)
+                for key in buf:
+                    buf[key][j, :count].copy_(x[key])
+                pos = {int(b): i for i, b in enumerate(act)}
+                for b in sel_br:
+                    if b in pos:
+                        for key in keep_c:
+                            keep_q[b][key].append(x[key][pos[b]].cpu())
+            else:
+                pos = {}
+            lists.append([slot_of(b) for b in act])
+            poss.append(pos)
+        out = win.launch(lists)
+        torch.cuda.synchronize()
+        for j in range(M):
+            model.step(lists[j])
+            for b in sel_br:
+                if b in poss[j]:
+                    outs[b].append(out[j, poss[j][b]].float().cpu())
+        n, base_of = ctx.get_meta()
+        mn, mb, _ = model.snapshot()
+        assert list(n) == mn and list(base_of) == mb, w
+    win.close()
+    final = ctx.read_state([slot_of(b) for b in sel_br]).cpu().double().numpy()
+    ctx.close()
+    for i, b in enumerate(sel_br):
+        r = b // NB
+        ctxin = {key: keep_c[key][:, sel_req.index(r)] for key in keep_c}
+        L = int(lens[b])
+        cat = {key: torch.cat([ctxin[key], torch.stack(keep_q[b][key])]).double().numpy()
+               for key in keep_c}
+        o_ref, S_ref, _ = oracle.gdn_eager(S0[r].cpu().double().numpy(), cat["q"], cat["k"],
+                                           cat["v"], cat["g"], cat["beta"])
+        o = torch.stack(outs[b]).numpy()
+        assert o.shape[0] == L
+        assert max_step_rel(o, o_ref[Tc:]) <= OUT_TOL_BF16, b
+        assert rel_err(final[i], S_ref) <= STATE_TOL, b
+
+
 def test_chunked_rows_and_empty_batch():
     """More slot rows than one launch takes (1100 > 1024): the step is split
     into chunks; an empty slot list is a no-op."""
