@@ -141,7 +141,8 @@ dl_status dl_table_get(const dl_table *t, int32_t *n_log, int32_t *base_of, int3
 /* ------------------------------------------------------------------------ */
 typedef struct dl_ctx dl_ctx;
 
-/* Allocate, on the current CUDA device, the dense bases S̄ [num_slots, H, d_v,
+/* The base + log representation of the DeltaLog page, "Methodology — Base +
+ * Log".  Allocate, on the current CUDA device, the dense bases S̄ [num_slots, H, d_v,
  * d_k] fp32 (zeroed), the bounded log (value side [num_slots, H, M-1, d_v]
  * fp32, or bf16 for RWKV6; keys [num_slots, H, M-1, d_k] bf16; cumulative
  * log-decay [num_slots, H, M-1] or [num_slots, H, M-1, d_k] fp32), the slot
@@ -164,8 +165,9 @@ dl_status dl_set_bonus(dl_ctx *ctx, const float *bonus);
  * only src's log rows (n_src entries) are copied into each dst's log. */
 dl_status dl_fork(dl_ctx *ctx, int32_t src, const int32_t *dsts, int32_t n);
 
-/* One decode token for each listed slot (n slots, row i of every tensor is
- * slot slots[i]):
+/* One decode token for each listed slot: the step of the DeltaLog page,
+ * "Methodology — Base + Log", run as in "Kernel implementation" (n slots, row
+ * i of every tensor is slot slots[i]):
  *   q (r for RWKV6), k   [n, H, d_k] bf16
  *   v                    [n, H, d_v] bf16
  *   g                    [n, H] fp32 (GDN) or [n, H, d_k] fp32 (KDA, RWKV6): log-decay
@@ -178,15 +180,16 @@ dl_status dl_step(dl_ctx *ctx, const int32_t *slots, int32_t n,
                   const void *q, const void *k, const void *v,
                   const float *g, const float *beta, void *o);
 
-/* Same arguments and results as dl_step, but every tensor is in HOST memory
- * (pinned memory gives full copy speed).  The call copies the inputs to
+/* The dl_step operation with every tensor in HOST memory (pinned memory
+ * gives full copy speed): same arguments and results as dl_step.  The call copies the inputs to
  * device staging buffers owned by the context, runs dl_step, copies o back
  * and synchronises the stream before returning. */
 dl_status dl_step_host(dl_ctx *ctx, const int32_t *slots, int32_t n,
                        const void *q, const void *k, const void *v,
                        const float *g, const float *beta, void *o);
 
-/* T decode tokens of the same n slots from HOST buffers: q, k [T, n, H, d_k]
+/* T dl_step operations (DeltaLog page, "Methodology — Base + Log") for the
+ * same n slots from HOST buffers: q, k [T, n, H, d_k]
  * bf16, v [T, n, H, d_v] bf16, g [T, n, H] or [T, n, H, d_k] fp32, beta
  * [T, n, H] fp32 (NULL for RWKV6), o [T, n, H, d_v] (written); token t is
  * slice t of each.  Equivalent to T calls of dl_step_host, but the copies
@@ -210,11 +213,14 @@ dl_status dl_step_eager(dl_ctx *ctx, const int32_t *slots, int32_t n,
                         const void *q, const void *k, const void *v,
                         const float *g, const float *beta, void *o);
 
-/* Force a merge now: S̄[s] <- base + replayed log, log emptied, slot owns its base. */
+/* The merge of the DeltaLog page, "Methodology — Base + Log", forced now:
+ * S̄[s] <- base + replayed log, log emptied, slot owns its base.  Frozen slots
+ * return DL_EBUSY. */
 dl_status dl_merge(dl_ctx *ctx, const int32_t *slots, int32_t n);
 
-/* Materialise the logical state of each listed slot into S_out [n, H, d_v,
- * d_k] fp32 device.  Does not change the context. */
+/* Materialise the logical state of each listed slot (base + replayed log,
+ * DeltaLog page, "Methodology — Base + Log") into S_out [n, H, d_v, d_k] fp32
+ * device.  Does not change the context. */
 dl_status dl_read_state(dl_ctx *ctx, const int32_t *slots, int32_t n, float *S_out);
 
 /* Synchronise and copy the device slot table: n_log and base_of are host
