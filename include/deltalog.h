@@ -193,11 +193,13 @@ dl_status dl_step_host(dl_ctx *ctx, const int32_t *slots, int32_t n,
  * bf16, v [T, n, H, d_v] bf16, g [T, n, H] or [T, n, H, d_k] fp32, beta
  * [T, n, H] fp32 (NULL for RWKV6), o [T, n, H, d_v] (written); token t is
  * slice t of each.  Equivalent to T calls of dl_step_host, but the copies
- * overlap the computation: while token t runs on the context's stream, an
- * upload stream copies token t+1's inputs into the second of two device
- * staging sets and a download stream copies token t-1's output back.  The
- * staging sets and the two streams are owned by the context and made on the
- * first call.  Host memory must be pinned for the copies to run
+ * overlap the computation: tokens travel in groups (one copy per tensor; small
+ * tensors are grouped until a copy reaches 2 MiB, up to 8 tokens and 64 MiB of
+ * staging a group), and while a group's tokens run on the
+ * context's stream an upload stream copies the next group's inputs into the
+ * second of two device staging sets and a download stream copies the previous
+ * group's outputs back.  The staging sets and the two streams are owned by the
+ * context and made on the first call.  Host memory must be pinned for the copies to run
  * asynchronously.  Returns once every output is in host memory; on an error
  * (for example DL_EBUSY for a frozen slot at the first token) the tokens
  * before it have been decoded and copied back. */

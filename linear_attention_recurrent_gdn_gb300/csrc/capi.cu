@@ -65,6 +65,7 @@ struct dl_ctx {
   // upload and a download stream, and the events that order them
   void* pipe_stage = nullptr;
   size_t pipe_set_bytes = 0;
+  int pipe_group = 1;          // tokens per staging set
   cudaStream_t up = nullptr, down = nullptr;
   cudaEvent_t ev_in[2] = {nullptr, nullptr}, ev_done[2] = {nullptr, nullptr},
               ev_out[2] = {nullptr, nullptr};
@@ -618,16 +619,30 @@ dl_status dl_decode_host(dl_ctx* c, const int32_t* slots, int32_t n, int32_t T, 
   const size_t bb = (size_t)n * H * 4, bo = (size_t)n * H * f.d_v * (f.out_bf16 ? 2 : 4);
   auto r256 = [](size_t x) { return (x + 255) & ~(size_t)255; };
   if (!c->pipe_stage) {
-    // one set sized for the largest batch the context can take
+    // Two staging sets, each for a group of tokens of the largest batch the
+    // context can take: a group's inputs travel in one copy per tensor and
+    // its outputs in one copy back.  Each copy has a fixed cost, so small
+    // per-token tensors are grouped until a key tensor's copy reaches 2 MiB
+    // (at most 8 tokens and 64 MiB a set); large ones go token by token,
+    // which keeps the pipeline fine-grained.
     const size_t Sn = f.num_slots;
-    const size_t set = 2 * r256(Sn * H * f.d_k * 2) + r256(Sn * H * f.d_v * 2) +
-                       r256(Sn * H * (f.op == DL_GDN ? 1 : f.d_k) * 4) + r256(Sn * H * 4) +
-                       r256(Sn * H * f.d_v * 4);
+    const size_t per_tok = 2 * Sn * H * f.d_k * 2 + Sn * H * f.d_v * 2 +
+                           Sn * H * (f.op == DL_GDN ? 1 : f.d_k) * 4 + Sn * H * 4 +
+                           Sn * H * f.d_v * 4;
+    const size_t key_bytes = Sn * H * f.d_k * 2;
+    size_t tgz = (((size_t)2 << 20) + key_bytes - 1) / (key_bytes > 0 ? key_bytes : 1);
+    const size_t cap = ((size_t)64 << 20) / (per_tok > 0 ? per_tok : 1);
+    if (tgz > cap) tgz = cap;
+    const int tg = tgz < 1 ? 1 : (tgz > 8 ? 8 : (int)tgz);
+    const size_t set = 2 * r256(tg * Sn * H * f.d_k * 2) + r256(tg * Sn * H * f.d_v * 2) +
+                       r256(tg * Sn * H * (f.op == DL_GDN ? 1 : f.d_k) * 4) +
+                       r256(tg * Sn * H * 4) + r256(tg * Sn * H * f.d_v * 4);
     if (cudaMalloc(&c->pipe_stage, 2 * set) != cudaSuccess) {
       c->pipe_stage = nullptr;
       return set_err(c, DL_ENOMEM, "staging allocation");
     }
     c->pipe_set_bytes = set;
+    c->pipe_group = tg;
     cudaError_t e = cudaStreamCreateWithFlags(&c->up, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->down, cudaStreamNonBlocking);
     for (int b = 0; b < 2 && e == cudaSuccess; ++b) {
@@ -643,33 +658,43 @@ dl_status dl_decode_host(dl_ctx* c, const int32_t* slots, int32_t n, int32_t T, 
   const unsigned char* hg = reinterpret_cast<const unsigned char*>(g);
   const unsigned char* hb = reinterpret_cast<const unsigned char*>(beta);
   unsigned char* ho = static_cast<unsigned char*>(o);
+  const int TG = c->pipe_group;
   cudaError_t e = cudaSuccess;
-  for (int32_t t = 0; t < T && rc == DL_OK && e == cudaSuccess; ++t) {
-    const int b = t & 1;
+  int grp = 0;
+  for (int32_t t0 = 0; t0 < T && rc == DL_OK && e == cudaSuccess; t0 += TG, ++grp) {
+    const int b = grp & 1;
+    const int tn = (T - t0) < TG ? (T - t0) : TG;   // tokens in this group
+    // the set's regions, each holding the group's tokens contiguously
     unsigned char* p = static_cast<unsigned char*>(c->pipe_stage) + (size_t)b * c->pipe_set_bytes;
-    void* dq = p; p += r256(bq);
-    void* dk = p; p += r256(bq);
-    void* dv = p; p += r256(bv);
-    float* dg = reinterpret_cast<float*>(p); p += r256(bg);
-    float* db = reinterpret_cast<float*>(p); p += r256(bb);
-    void* dout = p;
-    // set b is free once token t-2's output has been downloaded (which also
-    // follows token t-2's kernel, the last reader of its inputs)
-    if (t >= 2) e = cudaStreamWaitEvent(c->up, c->ev_out[b], 0);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(dq, hq + t * bq, bq, cudaMemcpyHostToDevice, c->up);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(dk, hk + t * bq, bq, cudaMemcpyHostToDevice, c->up);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(dv, hv + t * bv, bv, cudaMemcpyHostToDevice, c->up);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(dg, hg + t * bg, bg, cudaMemcpyHostToDevice, c->up);
+    unsigned char* dq = p; p += r256((size_t)TG * bq);
+    unsigned char* dk = p; p += r256((size_t)TG * bq);
+    unsigned char* dv = p; p += r256((size_t)TG * bv);
+    unsigned char* dg = p; p += r256((size_t)TG * bg);
+    unsigned char* db = p; p += r256((size_t)TG * bb);
+    unsigned char* dout = p;
+    // set b is free once group grp-2's outputs have been downloaded (which
+    // also follows its kernels, the last readers of its inputs)
+    if (grp >= 2) e = cudaStreamWaitEvent(c->up, c->ev_out[b], 0);
+    const size_t t0s = (size_t)t0;
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dq, hq + t0s * bq, tn * bq, cudaMemcpyHostToDevice, c->up);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dk, hk + t0s * bq, tn * bq, cudaMemcpyHostToDevice, c->up);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dv, hv + t0s * bv, tn * bv, cudaMemcpyHostToDevice, c->up);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dg, hg + t0s * bg, tn * bg, cudaMemcpyHostToDevice, c->up);
     if (e == cudaSuccess && f.op != DL_RWKV6)
-      e = cudaMemcpyAsync(db, hb + t * bb, bb, cudaMemcpyHostToDevice, c->up);
+      e = cudaMemcpyAsync(db, hb + t0s * bb, tn * bb, cudaMemcpyHostToDevice, c->up);
     if (e == cudaSuccess) e = cudaEventRecord(c->ev_in[b], c->up);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(c->stream, c->ev_in[b], 0);
     if (e != cudaSuccess) break;
-    rc = dl_step(c, slots, n, dq, dk, dv, dg, f.op != DL_RWKV6 ? db : nullptr, dout);
+    for (int j = 0; j < tn && rc == DL_OK; ++j)
+      rc = dl_step(c, slots, n, dq + j * bq, dk + j * bq, dv + j * bv,
+                   reinterpret_cast<const float*>(dg + j * bg),
+                   f.op != DL_RWKV6 ? reinterpret_cast<const float*>(db + j * bb) : nullptr,
+                   dout + j * bo);
     if (rc != DL_OK) break;
     e = cudaEventRecord(c->ev_done[b], c->stream);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(c->down, c->ev_done[b], 0);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(ho + t * bo, dout, bo, cudaMemcpyDeviceToHost, c->down);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(ho + t0s * bo, dout, tn * bo, cudaMemcpyDeviceToHost, c->down);
     if (e == cudaSuccess) e = cudaEventRecord(c->ev_out[b], c->down);
   }
   // nothing may still write the caller's buffers when the call returns
