@@ -179,11 +179,12 @@ int prep_warps(int op, int dk, int G) {
 
 enum class Kern { Append, Fused, Eager };
 
-dl::PipePlan pipe_shape(const dl_ctx* c, int G, Kern k) {
+// `merge_launch`: every row of the launch merges (rows known on the host).
+dl::PipePlan pipe_shape(const dl_ctx* c, int G, Kern k, bool merge_launch = false) {
   const int aux = k == Kern::Append ? c->L.aux_bytes : k == Kern::Fused ? c->L.f_bytes : c->L.e_bytes;
   return dl::plan_pipeline(c->cfg.d_k, aux, G, c->smem_optin, c->smem_per_sm, shape_override(),
                            k == Kern::Fused ? prep_warps(c->cfg.op, c->cfg.d_k, G) : -1,
-                           c->regs[(int)k]);
+                           c->regs[(int)k], merge_launch && k == Kern::Fused);
 }
 
 bool record(dl_ctx* c, int kind, cudaEvent_t* ev) {
@@ -291,8 +292,13 @@ dl_status run_step(dl_ctx* c, const int32_t* slots, int32_t n, const void* q, co
     fill_step_args(c, a, row0, rows, q, k, v, g, beta, o);
     unit_shape(c, a);
     const bool fused = !eager && f.staging == DL_STAGE_FUSED;
+    // a launch where every row merges a window of M >= 8 gets the merge shape
+    // (shorter rank-M updates are cheap enough that the append shape wins)
+    bool all_merge = fused && a.plan_dev == nullptr && f.merge_interval >= 8;
+    for (int32_t i = 0; i < rows && all_merge; ++i)
+      all_merge = a.items[i].n + 1 == f.merge_interval;
     const dl::PipePlan ps =
-        pipe_shape(c, a.G, eager ? Kern::Eager : fused ? Kern::Fused : Kern::Append);
+        pipe_shape(c, a.G, eager ? Kern::Eager : fused ? Kern::Fused : Kern::Append, all_merge);
     if (ps.ns == 0) return set_err(c, DL_EUNSUPPORTED, "pipeline does not fit in shared memory");
     a.ns = ps.ns;
     a.na = ps.na;

@@ -133,7 +133,8 @@ inline PipePlan fit_pipeline(int cps, int ncw, int R, int dk, int aux_bytes, int
 inline int tiles_per_stage(int dk, int G) { return (dk == 64 && G % 2 == 0) ? 2 : 1; }
 
 inline PipePlan plan_pipeline(int dk, int aux_bytes, int G, int smem_optin, int smem_per_sm,
-                              const int* force = nullptr, int npw = -1, int regs = 0) {
+                              const int* force = nullptr, int npw = -1, int regs = 0,
+                              bool merge_launch = false) {
   const int tps = tiles_per_stage(dk, G);
   if (force) {   // tuning override: {cps, ncw, R, npw (-1: default), max_na (0: default)}
     const PipePlan p = fit_pipeline(force[0], force[1], force[2], dk, aux_bytes, G, smem_optin,
@@ -156,6 +157,20 @@ inline PipePlan plan_pipeline(int dk, int aux_bytes, int G, int smem_optin, int 
   const bool fused = npw >= 0;
   const int (*cand)[3] = !big ? c8k : fused ? c16k_fused : c16k;
   const int ncand = !big ? 6 : fused ? 6 : 5;
+  if (npw == 0 && merge_launch && dk == 64) {
+    // One-stage d_k = 64 units on a launch where every row merges: each unit's
+    // rank-M update holds its stage for most of the unit's time, so more
+    // consumer warps per CTA pay more than deep input slots (measured on GB300
+    // for 5120 RWKV6 slot-heads at M = 16: 60.4 us a launch at (2,4,1), 62.5 at
+    // (4,2,1), 69.6 at the append steps' (3,2,1)).  Callers ask for it only for
+    // M >= 8: at M = 4 the update is short and the append shape stays faster.
+    static const int cm[][3] = {{2, 4, 1}, {4, 2, 1}};
+    for (const auto& m : cm) {
+      const PipePlan p = fit_pipeline(m[0], m[1], m[2], dk, aux_bytes, G, smem_optin, smem_per_sm,
+                                      tps, npw, regs);
+      if (p.ns > 0) return p;
+    }
+  }
   if (npw == 0) {
     // One-stage units, each prepared by its own consumer warp: a warp's aux
     // slots are how far ahead its units' inputs load (measured on GB300: one

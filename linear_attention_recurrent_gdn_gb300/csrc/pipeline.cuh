@@ -555,6 +555,53 @@ __device__ __forceinline__ bool consume_append(const StepArgs& a, const Layout& 
   return false;
 }
 
+// RWKV6 append step at d_k = 64, where one stage holds both 32-row tiles of the
+// slot-head.  RWKV6 needs one dot product per row, so both tiles' partial sums
+// fit in registers and their reductions and replay chains run interleaved.
+// The arithmetic is consume_append's, in the same order.
+template <int DK, int DV>
+__device__ __forceinline__ void consume_rwkv6_pair(const StepArgs& a, const Layout& Lay,
+                                                   const UnitPos& p, int vt0, const float* T,
+                                                   const AuxView& av, int lane,
+                                                   uint32_t empty_bar, int n) {
+  constexpr int VEC = DK / 32;
+  const float* cf = av.cf;
+  float rv[VEC];
+  ldvec<VEC>(rv, cf + HDR + 2 * Lay.Mcap4 + lane * VEC);   // r̂
+  const float* T1 = T + BV * DK;
+  float pa[32], pb[32];
+#pragma unroll
+  for (int r = 0; r < 32; ++r) {
+    float t0[VEC], t1[VEC];
+    ldvec<VEC>(t0, T + r * DK + lane * VEC);
+    ldvec<VEC>(t1, T1 + r * DK + lane * VEC);
+    float x0 = 0.f, x1 = 0.f;
+#pragma unroll
+    for (int c = 0; c < VEC; ++c) {
+      x0 += t0[c] * rv[c];
+      x1 += t1[c] * rv[c];
+    }
+    pa[r] = x0;
+    pb[r] = x1;
+  }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(empty_bar);
+  const float A0 = reduce_scatter32(pa, lane);
+  const float A1 = reduce_scatter32(pb, lane);
+  const uint16_t* V = reinterpret_cast<const uint16_t*>(av.U);
+  const int col0 = vt0 * BV + lane, col1 = col0 + BV;
+  float o0 = A0, o1 = A1;
+  for (int j = 0; j < n; ++j) {
+    const float c = cf[HDR + j];
+    o0 += c * bf16f(V[j * DV + col0]);
+    o1 += c * bf16f(V[j * DV + col1]);
+  }
+  o0 += cf[3] * bf16f(V[n * DV + col0]);
+  o1 += cf[3] * bf16f(V[n * DV + col1]);
+  store_out(a, (size_t)p.sh * DV + col0, a.scale * o0);
+  store_out(a, (size_t)p.sh * DV + col1, a.scale * o1);
+}
+
 // ------------------------------------------------------------- EagerStep ----
 template <int OP, int DK, int DV>
 __device__ __forceinline__ void consume_eager(const StepArgs& a, const Layout& Lay,
@@ -905,7 +952,16 @@ __global__ void __maxnreg__(128) pipe_kernel(const __grid_constant__ StepArgs a)
     }
     if (!__all_sync(0xffffffffu, ok)) break;
     bool released = false;
-    for (int t = 0; t < TPS; ++t) {
+    bool paired = false;
+    if constexpr (MODE != EAGER && OP == RWKV6 && DK == 64) {
+      const int n = step_item(a, p.row).n;
+      if (TPS == 2 && n + 1 != a.M) {   // append step: both tiles of the stage at once
+        consume_rwkv6_pair<DK, DV>(a, Lay, p, vt0, tiles + (size_t)s * TPS * BV * DK,
+                                   aux_view<OP, DK, MODE>(Lay, ax), lane, bars.empty(s), n);
+        released = paired = true;
+      }
+    }
+    for (int t = 0; t < TPS && !paired; ++t) {
       const float* T = tiles + ((size_t)s * TPS + t) * BV * DK;
       if constexpr (MODE == EAGER) {
         consume_eager<OP, DK, DV>(a, Lay, p, vt0 + t, T, ax, lane, g_s, beta_s);

@@ -59,10 +59,12 @@ def test_config0_gdn_full(M):
 @pytest.mark.parametrize("staging", STAGINGS)
 @pytest.mark.parametrize("op", OPS)
 @pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("M", [1, 3, 8, 16])
+@pytest.mark.parametrize("M", [1, 3, 8, 9, 16, 17])
 def test_ops_small_ragged(op, d, M, staging):
     """B=3 slots x H=5 heads (15 slot-heads, several value tiles each), T = 2M+3
-    tokens: two merges and a partial window; fp32 output, state at every step."""
+    tokens: two merges and a partial window; fp32 output, state at every step.
+    M = 9 and 17 fill every entry slot of their coefficient bound (8, 16) on the
+    merge step."""
     B, H, T = 3, 5, 2 * M + 3
     x, S0, bonus = make_case(op, B, H, d, T, seed=17 + 3 * op + d + M)
     snap = list(range(T))
