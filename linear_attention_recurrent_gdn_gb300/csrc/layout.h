@@ -149,14 +149,19 @@ inline PipePlan plan_pipeline(int dk, int aux_bytes, int G, int smem_optin, int 
   // fit (more producers, and more units whose coefficients are computed at
   // once).  8 KiB stages (d_k = 64 with one tile per unit) need more stages
   // per warp.
-  static const int c16k[][3] = {{2, 4, 1}, {2, 3, 1}, {1, 8, 1}, {1, 6, 1}, {1, 4, 1}};
+  // Each list ends with small shapes that only large aux slots fall back to
+  // (per-key ops at M near 32), so that every supported configuration has one.
+  static const int c16k[][3] = {{2, 4, 1}, {2, 3, 1}, {1, 8, 1}, {1, 6, 1}, {1, 4, 1},
+                                {2, 2, 1}, {1, 2, 1}, {2, 1, 1}, {1, 1, 1}};
   static const int c16k_fused[][3] = {{4, 2, 1}, {2, 4, 1}, {3, 2, 1}, {2, 3, 1}, {1, 8, 1},
-                                      {1, 4, 1}};
-  static const int c8k[][3] = {{2, 4, 3}, {2, 4, 2}, {2, 3, 2}, {1, 8, 2}, {1, 8, 1}, {1, 4, 1}};
+                                      {1, 4, 1}, {2, 2, 1}, {1, 2, 1}, {2, 1, 1}, {1, 1, 1}};
+  static const int c8k[][3] = {{2, 4, 3}, {2, 4, 2}, {2, 3, 2}, {1, 8, 2}, {1, 8, 1}, {1, 4, 1},
+                               {2, 2, 1}, {1, 2, 1}, {2, 1, 1}, {1, 1, 1}};
   const bool big = 32 * dk * 4 * tps >= 16384;
   const bool fused = npw >= 0;
   const int (*cand)[3] = !big ? c8k : fused ? c16k_fused : c16k;
-  const int ncand = !big ? 6 : fused ? 6 : 5;
+  const int ncand = !big ? 10 : fused ? 10 : 9;
+  const int npref = ncand - 4;   // the shapes before the fallbacks
   if (npw == 0 && merge_launch && dk == 64) {
     // One-stage d_k = 64 units on a launch where every row merges: each unit's
     // rank-M update holds its stage for most of the unit's time, so more
@@ -180,7 +185,7 @@ inline PipePlan plan_pipeline(int dk, int aux_bytes, int G, int smem_optin, int 
     // one CTA per SM (one producer) only come in when no other fits.
     PipePlan best{0, 0, 0, 0, 0, 0};
     int best_depth = 0;
-    for (int ci = 0; ci < ncand; ++ci) {
+    for (int ci = 0; ci < npref; ++ci) {
       if (cand[ci][0] < 2) continue;
       const PipePlan p = fit_pipeline(cand[ci][0], cand[ci][1], cand[ci][2], dk, aux_bytes, G,
                                       smem_optin, smem_per_sm, tps, npw, regs);

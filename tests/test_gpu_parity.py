@@ -59,12 +59,13 @@ def test_config0_gdn_full(M):
 @pytest.mark.parametrize("staging", STAGINGS)
 @pytest.mark.parametrize("op", OPS)
 @pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("M", [1, 3, 8, 9, 16, 17])
+@pytest.mark.parametrize("M", [1, 3, 8, 9, 16, 17, 32])
 def test_ops_small_ragged(op, d, M, staging):
     """B=3 slots x H=5 heads (15 slot-heads, several value tiles each), T = 2M+3
     tokens: two merges and a partial window; fp32 output, state at every step.
     M = 9 and 17 fill every entry slot of their coefficient bound (8, 16) on the
-    merge step."""
+    merge step. M = 32 gives KDA at d=128 aux slots of 41.5 KB, which only the
+    planner's fallback shapes fit with one-tile units."""
     B, H, T = 3, 5, 2 * M + 3
     x, S0, bonus = make_case(op, B, H, d, T, seed=17 + 3 * op + d + M)
     snap = list(range(T))
