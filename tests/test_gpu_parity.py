@@ -81,10 +81,12 @@ def test_ops_small_ragged(op, d, M, staging):
 @pytest.mark.parametrize("staging", STAGINGS)
 @pytest.mark.parametrize("op", OPS)
 @pytest.mark.parametrize("d", [64, 128])
-def test_ops_bf16_output_many_units(op, d, staging):
-    """320 slot-heads (enough work units for whole-slot-head units), M=4,
-    20 tokens, bf16 output, compared on every slot-head."""
-    B, H, T, M = 40, 8, 20, 4
+@pytest.mark.parametrize("M", [4, 16])
+def test_ops_bf16_output_many_units(op, d, M, staging):
+    """320 slot-heads (enough work units for whole-slot-head units, so d=128
+    runs with prep warps), 20 tokens, bf16 output, compared on every
+    slot-head. M=16 takes the log to 15 entries before its merge."""
+    B, H, T = 40, 8, 20
     x, S0, bonus = make_case(op, B, H, d, T, seed=300 + op + d)
     o_ref, S_ref, _ = oracle_run(op, x, S0, bonus)
     o, _, ctx = gpu_run(op, x, S0, bonus, M, out_bf16=True, staging=staging)
