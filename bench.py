@@ -44,6 +44,13 @@ WORKLOADS = {
                       "(512 branch slots) of U{16..256} tokens, H=16 d_k=d_v=128"),
 }
 METRIC = "state-update tokens·heads/s and achieved HBM GB/s vs ~8 TB/s; write bytes/step"
+# Chunked prefill of the decode workloads' shapes: one call feeds every slot a
+# 512-token context (the Flide page's first call, which builds a fork base).
+PREFILL = {"prefill_gdn": "gdn", "prefill_kda": "kda", "prefill_rwkv6": "rwkv6"}
+PREFILL_C = 32                      # tokens per chunk (csrc/prefill.cu)
+# FP32 FMA peak from the unit counts and clock: 152 SMs x 128 FP32 lanes x
+# 2 FLOP x 2.07 GHz (maximum SM clock).
+FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
 
 def log(*a):
@@ -238,7 +245,8 @@ def run_reference(args):
     import torch
     import oracle
     from linear_attention_recurrent_gdn_gb300 import inputs as gen
-    w = WORKLOADS[args.workload]
+    # a prefill computes the decode recurrence over its context: same oracle
+    w = WORKLOADS[PREFILL.get(args.workload, args.workload)]
     sample_sh = int(os.environ.get("DL_REF_SLOT_HEADS", "4096"))
     tokens = int(os.environ.get("DL_REF_TOKENS", "512"))
     oracle.build()
@@ -532,6 +540,88 @@ def run_ours(args):
     return 0
 
 
+def prefill_flops(op, d, C=PREFILL_C):
+    """FLOPs (an FMA counts 2) per token·head of the chunked prefill, d_k = d_v = d.
+    Per token: the products with S̄ (S̄K^T and S̄Q^T, 2 d^2; RWKV6 only S̄R̂^T, d^2),
+    S̄'s rewrite (the rank-C update d^2 and the chunk-end scaling d^2 / C), the
+    decay-weighted pair products of the chunk's lower triangle (delta rule: k·k
+    strictly below and k·q on and below the diagonal, C d; RWKV6: k·r strictly
+    below, (C - 1) d / 2), and the forward substitution with the outputs
+    (C d; RWKV6 the outputs, (C - 1) d / 2).  Exponentials are not counted."""
+    if op == 2:
+        fma = 2 * d * d + d * d / C + (C - 1) * d
+    else:
+        fma = 3 * d * d + d * d / C + 2 * C * d
+    return 2 * fma
+
+
+def run_prefill(args):
+    """Chunked prefill: one bench step is one dl_prefill call that feeds all B
+    slots a T-token context (inputs resident in HBM)."""
+    import torch
+    rank, world, dist = dist_setup("cuda")
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    from linear_attention_recurrent_gdn_gb300 import build
+    if rank == 0:
+        build.build()
+    barrier(dist)
+    from linear_attention_recurrent_gdn_gb300 import deltalog as dl
+    from linear_attention_recurrent_gdn_gb300 import inputs as gen
+    w = WORKLOADS[PREFILL[args.workload]]
+    op, B, H, d, M = w["op"], args.B or w["B"], w["H"], w["d"], w["M"]
+    T = args.tokens or w["tokens"]
+    seed = w["seed"] + 7919 * rank
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    x = gen.make_inputs(op, T, B, H, d, d, seed, device=dev)
+    ctx = dl.DeltaLog(op, B, H, d, d, M, stream=stream.cuda_stream)
+    slots = list(range(B))
+    ctx.set_state(slots, gen.initial_state(B, H, d, d, seed, device=dev))
+    if op == 2:
+        ctx.set_bonus(gen.rwkv6_bonus(H, d, seed, device=dev))
+    out = torch.empty((T, B, H, d), dtype=torch.bfloat16, device=dev)
+
+    def one():
+        ctx.prefill(slots, x["q"], x["k"], x["v"], x["g"], x["beta"], out=out)
+
+    for _ in range(args.warmup):
+        one()
+    barrier(dist)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            one()
+        e1.record(stream)
+        e1.synchronize()
+    ms = reduce_max(dist, e0.elapsed_time(e1) / args.steps, dev)
+    units = B * H * T
+    tflops = units * prefill_flops(op, d) / (ms / 1e3) / 1e12
+    result = {"metric": "prefill tokens·heads/s", "value": units * world / (ms / 1e3),
+              "unit": "tokens·heads/s", "n_gpus": world, "steps": args.steps,
+              "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+              "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+              "config": {"workload": "chunked prefill, " + w["desc"].split(",")[0] +
+                         ", %d-token context per slot, outputs written" % T,
+                         "op": gen.OP_NAMES[op], "B": B, "H": H, "d_k": d, "d_v": d,
+                         "T": T, "chunk": PREFILL_C,
+                         "l2": "inputs and state larger than L2"},
+              "roofline": {"bound": "alu", "achieved": tflops, "peak": FP32_PEAK_TFLOPS,
+                           "unit": "TFLOP/s", "frac": tflops / FP32_PEAK_TFLOPS,
+                           "traffic": None, "peak_source": "derived: 152 SMs x 128 FP32 "
+                           "lanes x 2 FLOP x 2.07 GHz",
+                           "flops_per_token_head": prefill_flops(op, d)},
+              "clocks": clk.summary(), "gpu_launches": args.steps * ((B + 1023) // 1024)}
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    ctx.close()
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
 def run_fork(args):
     """Forked decode: bases are built once (setup, untimed); one bench step =
     fork every request into its branches (by index, no state copy) + the
@@ -635,7 +725,7 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="gdn", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="gdn", choices=sorted(WORKLOADS) + sorted(PREFILL))
     ap.add_argument("--M", type=int, default=0)
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
@@ -653,6 +743,8 @@ def main():
         return run_reference(args)
     if args.workload == "fork":
         return run_fork(args)
+    if args.workload in PREFILL:
+        return run_prefill(args)
     return run_ours(args)
 
 

@@ -47,13 +47,23 @@ struct PfSmem {
   static constexpr int PK_OFF = V_OFF + PF_C * DV;
   static constexpr int PQ_OFF = PK_OFF + DV * PP;
   static constexpr int U_OFF = PQ_OFF + DV * PP;
-  static constexpr int AKK_OFF = U_OFF + DV * PP;
-  static constexpr int AKQ_OFF = AKK_OFF + PF_C * PF_C;
-  static constexpr int L_OFF = AKQ_OFF + PF_C * PF_C;
+  static constexpr int AKK_OFF = U_OFF + DV * PP;            // [C][PP]: padded rows
+  static constexpr int AKQ_OFF = AKK_OFF + PF_C * PP;
+  static constexpr int L_OFF = AKQ_OFF + PF_C * PP;
   static constexpr int B_OFF = L_OFF + PF_C;
-  static constexpr int FLOATS = B_OFF + PF_C;
+  static constexpr int EL_OFF = B_OFF + PF_C;                  // e^{Λ_j}
+  static constexpr int EW_OFF = EL_OFF + PF_C;                 // e^{Λ_C - Λ_j}
+  static constexpr int FLOATS = EW_OFF + PF_C;
   static constexpr size_t BYTES = FLOATS * sizeof(float);
 };
+
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float dot4(float acc, const float4 a, const float4 b) {
+  acc += a.x * b.x;
+  acc += a.y * b.y;
+  acc += a.z * b.z;
+  return acc + a.w * b.w;
+}
 
 template <int DK, int DV>
 __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gdn_kernel(const __grid_constant__ SlotListArgs a,
@@ -77,6 +87,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gdn_kernel(const __grid
   float* Akq = sm + L::AKQ_OFF;
   float* Lm = sm + L::L_OFF;
   float* Bt = sm + L::B_OFF;
+  float* El = sm + L::EL_OFF;
+  float* Ew = sm + L::EW_OFF;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int sh = blockIdx.x, row = sh / a.H, h = sh - row * a.H;
   const int slot = a.items[row].slot;
@@ -115,106 +127,143 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gdn_kernel(const __grid
         const float y = __shfl_up_sync(0xffffffffu, gj, o2);
         if (lane >= o2) gj += y;
       }
+      const float LC = __shfl_sync(0xffffffffu, gj, Cc - 1);
       Lm[lane] = gj;
+      El[lane] = expf(gj);
+      Ew[lane] = lane < Cc ? expf(LC - gj) : 0.f;   // padding tokens add nothing
       Bt[lane] = lane < Cc ? beta[(size_t)(t0 + lane) * nH + sh] : 0.f;
     }
     __syncthreads();
-    // ---- decay-weighted key-key (strictly lower) and query-key (lower) products
-    for (int p = tid; p < PF_C * PF_C; p += PF_THREADS) {
-      const int j = p / PF_C, i = p - j * PF_C;
-      float kk = 0.f, qk = 0.f;
-      if (i <= j && j < Cc) {
-        const float* kj = Kc + j * L::SP;
-        const float* qj = Qc + j * L::SP;
-        const float* ki = Kc + i * L::SP;
-#pragma unroll 8
-        for (int c = 0; c < DK; c += 4) {
-          const float4 a4 = *reinterpret_cast<const float4*>(ki + c);
-          const float4 b4 = *reinterpret_cast<const float4*>(kj + c);
-          const float4 c4 = *reinterpret_cast<const float4*>(qj + c);
-          kk += a4.x * b4.x + a4.y * b4.y + a4.z * b4.z + a4.w * b4.w;
-          qk += a4.x * c4.x + a4.y * c4.y + a4.z * c4.z + a4.w * c4.w;
-        }
-        const float w = expf(Lm[j] - Lm[i]);
-        kk *= w;
-        qk *= w;
-        if (i == j) kk = 0.f;
-      }
-      Akk[p] = kk;
-      Akq[p] = qk;
-    }
-    // ---- S̄ K^T and S̄ Q^T: two threads per value row, 16 tokens each
-    if ((tid >> 1) < DV) {
-      const int r = tid >> 1, jh = (tid & 1) * (PF_C / 2);
-      float pk[PF_C / 2], pq[PF_C / 2];
-#pragma unroll
-      for (int j = 0; j < PF_C / 2; ++j) pk[j] = pq[j] = 0.f;
-      const float* sr = Sb + r * L::SP;
+    // Register tiles below are laid out so that each warp-wide load of a
+    // padded row (stride DK + 4 floats, 4 banks apart) touches distinct banks.
+    // ---- decay-weighted key-key (strictly lower) and query-key (lower) products:
+    //      a 2x2 block (tokens j = jg, jg + 16; i = ig, ig + 16) per thread
+    {
+      const int jg = tid >> 4, ig = tid & 15;
+      float kk[2][2] = {{0.f, 0.f}, {0.f, 0.f}}, qk[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll 4
       for (int c = 0; c < DK; c += 4) {
-        const float4 s4 = *reinterpret_cast<const float4*>(sr + c);
+        const float4 ki0 = ld4(Kc + ig * L::SP + c), ki1 = ld4(Kc + (ig + 16) * L::SP + c);
+        const float4 kj0 = ld4(Kc + jg * L::SP + c), kj1 = ld4(Kc + (jg + 16) * L::SP + c);
+        const float4 qj0 = ld4(Qc + jg * L::SP + c), qj1 = ld4(Qc + (jg + 16) * L::SP + c);
+        kk[0][0] = dot4(kk[0][0], kj0, ki0);
+        kk[0][1] = dot4(kk[0][1], kj0, ki1);
+        kk[1][0] = dot4(kk[1][0], kj1, ki0);
+        kk[1][1] = dot4(kk[1][1], kj1, ki1);
+        qk[0][0] = dot4(qk[0][0], qj0, ki0);
+        qk[0][1] = dot4(qk[0][1], qj0, ki1);
+        qk[1][0] = dot4(qk[1][0], qj1, ki0);
+        qk[1][1] = dot4(qk[1][1], qj1, ki1);
+      }
 #pragma unroll
-        for (int j = 0; j < PF_C / 2; ++j) {
-          const float4 k4 = *reinterpret_cast<const float4*>(Kc + (jh + j) * L::SP + c);
-          const float4 q4 = *reinterpret_cast<const float4*>(Qc + (jh + j) * L::SP + c);
-          pk[j] += s4.x * k4.x + s4.y * k4.y + s4.z * k4.z + s4.w * k4.w;
-          pq[j] += s4.x * q4.x + s4.y * q4.y + s4.z * q4.z + s4.w * q4.w;
+      for (int x = 0; x < 2; ++x)
+#pragma unroll
+        for (int y = 0; y < 2; ++y) {
+          const int j = jg + 16 * x, i = ig + 16 * y;
+          const float w = (i <= j && j < Cc) ? expf(Lm[j] - Lm[i]) : 0.f;   // exponent <= 0
+          Akk[j * L::PP + i] = i < j ? kk[x][y] * w : 0.f;
+          Akq[j * L::PP + i] = qk[x][y] * w;
         }
+    }
+    // ---- S̄ K^T and S̄ Q^T: rows rg + 32 m, tokens tg + 8 t per thread
+    {
+      constexpr int RPT = DV / 32;
+      const int rg = tid >> 3, tg = tid & 7;
+      float pk[RPT][4], pq[RPT][4];
+#pragma unroll
+      for (int m = 0; m < RPT; ++m)
+#pragma unroll
+        for (int t = 0; t < 4; ++t) pk[m][t] = pq[m][t] = 0.f;
+#pragma unroll 2
+      for (int c = 0; c < DK; c += 4) {
+        float4 s4[RPT], k4[4], q4[4];
+#pragma unroll
+        for (int m = 0; m < RPT; ++m) s4[m] = ld4(Sb + (rg + 32 * m) * L::SP + c);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          k4[t] = ld4(Kc + (tg + 8 * t) * L::SP + c);
+          q4[t] = ld4(Qc + (tg + 8 * t) * L::SP + c);
+        }
+#pragma unroll
+        for (int m = 0; m < RPT; ++m)
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            pk[m][t] = dot4(pk[m][t], s4[m], k4[t]);
+            pq[m][t] = dot4(pq[m][t], s4[m], q4[t]);
+          }
       }
 #pragma unroll
-      for (int j = 0; j < PF_C / 2; ++j) {
-        Pk[r * L::PP + jh + j] = pk[j];
-        Pq[r * L::PP + jh + j] = pq[j];
-      }
+      for (int m = 0; m < RPT; ++m)
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          Pk[(rg + 32 * m) * L::PP + tg + 8 * t] = pk[m][t];
+          Pq[(rg + 32 * m) * L::PP + tg + 8 * t] = pq[m][t];
+        }
     }
     __syncthreads();
-    // ---- forward substitution for u, then the outputs: one thread per value row
+    // ---- forward substitution for u, then the outputs: one thread per value
+    //      row; each sum runs in four partial sums to shorten its chain
     if (tid < DV) {
       const int r = tid;
       float u[PF_C];
 #pragma unroll
       for (int j = 0; j < PF_C; ++j) {
-        float x = expf(Lm[j]) * Pk[r * L::PP + j];
+        float x[4] = {El[j] * Pk[r * L::PP + j], 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < j; ++i) x += Akk[j * PF_C + i] * u[i];
-        u[j] = (j < Cc) ? Bt[j] * (Vc[j * DV + r] - x) : 0.f;
+        for (int i = 0; i < j; ++i) x[i & 3] += Akk[j * L::PP + i] * u[i];
+        u[j] = Bt[j] * (Vc[j * DV + r] - ((x[0] + x[1]) + (x[2] + x[3])));   // 0 past Cc
       }
 #pragma unroll
       for (int j = 0; j < PF_C; ++j) {
         Us[r * L::PP + j] = u[j];
         if (o != nullptr && j < Cc) {
-          float y = expf(Lm[j]) * Pq[r * L::PP + j];
+          float y[4] = {El[j] * Pq[r * L::PP + j], 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int i = 0; i <= j; ++i) y += Akq[j * PF_C + i] * u[i];
+          for (int i = 0; i <= j; ++i) y[i & 3] += Akq[j * L::PP + i] * u[i];
+          const float yo = (y[0] + y[1]) + (y[2] + y[3]);
           const size_t oi = ((size_t)(t0 + j) * nH + sh) * DV + r;
-          if (out_bf16) static_cast<uint16_t*>(o)[oi] = f2bf16(scale * y);
-          else static_cast<float*>(o)[oi] = scale * y;
+          if (out_bf16) static_cast<uint16_t*>(o)[oi] = f2bf16(scale * yo);
+          else static_cast<float*>(o)[oi] = scale * yo;
         }
       }
     }
     __syncthreads();
-    // ---- S̄ <- e^{Λ_C} S̄ + Σ_j u_j (e^{Λ_C-Λ_j} k_j)^T: two threads per row, half a row each
-    if ((tid >> 1) < DV) {
-      const int r = tid >> 1, c0 = (tid & 1) * (DK / 2);
-      const float LC = Lm[Cc - 1];
-      float acc[DK / 2];
-      const float eC = expf(LC);
+    // ---- S̄ <- e^{Λ_C} S̄ + Σ_j u_j (e^{Λ_C-Λ_j} k_j)^T: rows rg + 32 m and
+    //      column quads 4 tg + 32 n per thread
+    {
+      constexpr int RPT = DV / 32, CPT = DK / 32;
+      const int rg = tid >> 3, tg = tid & 7;
+      const float eC = El[Cc - 1];
+      float4 acc[RPT][CPT];
 #pragma unroll
-      for (int c = 0; c < DK / 2; c += 4) {
-        const float4 s4 = *reinterpret_cast<const float4*>(Sb + r * L::SP + c0 + c);
-        acc[c] = eC * s4.x; acc[c + 1] = eC * s4.y; acc[c + 2] = eC * s4.z; acc[c + 3] = eC * s4.w;
-      }
+      for (int m = 0; m < RPT; ++m)
+#pragma unroll
+        for (int n4 = 0; n4 < CPT; ++n4) {
+          const float4 s4 = ld4(Sb + (rg + 32 * m) * L::SP + 4 * tg + 32 * n4);
+          acc[m][n4] = make_float4(eC * s4.x, eC * s4.y, eC * s4.z, eC * s4.w);
+        }
       for (int j = 0; j < Cc; ++j) {
-        const float w = Us[r * L::PP + j] * expf(LC - Lm[j]);
+        const float ew = Ew[j];
+        float w[RPT];
 #pragma unroll
-        for (int c = 0; c < DK / 2; c += 4) {
-          const float4 k4 = *reinterpret_cast<const float4*>(Kc + j * L::SP + c0 + c);
-          acc[c] += w * k4.x; acc[c + 1] += w * k4.y; acc[c + 2] += w * k4.z; acc[c + 3] += w * k4.w;
+        for (int m = 0; m < RPT; ++m) w[m] = Us[(rg + 32 * m) * L::PP + j] * ew;
+#pragma unroll
+        for (int n4 = 0; n4 < CPT; ++n4) {
+          const float4 k4 = ld4(Kc + j * L::SP + 4 * tg + 32 * n4);
+#pragma unroll
+          for (int m = 0; m < RPT; ++m) {
+            acc[m][n4].x += w[m] * k4.x;
+            acc[m][n4].y += w[m] * k4.y;
+            acc[m][n4].z += w[m] * k4.z;
+            acc[m][n4].w += w[m] * k4.w;
+          }
         }
       }
 #pragma unroll
-      for (int c = 0; c < DK / 2; c += 4)
-        *reinterpret_cast<float4*>(Sb + r * L::SP + c0 + c) =
-            make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
+      for (int m = 0; m < RPT; ++m)
+#pragma unroll
+        for (int n4 = 0; n4 < CPT; ++n4)
+          *reinterpret_cast<float4*>(Sb + (rg + 32 * m) * L::SP + 4 * tg + 32 * n4) = acc[m][n4];
     }
   }
   __syncthreads();
