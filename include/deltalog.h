@@ -237,8 +237,10 @@ dl_status dl_get_meta(dl_ctx *ctx, int32_t *n_log, int32_t *base_of);
  * Inputs are token-major: q (r for RWKV6), k [T, n, H, d_k] bf16, v
  * [T, n, H, d_v] bf16, g [T, n, H] (GDN) or [T, n, H, d_k] (KDA, RWKV6) fp32,
  * beta [T, n, H] fp32 (NULL for RWKV6, which needs dl_set_bonus first);
- * o [T, n, H, d_v] receives every token's output, or is NULL.  Every slot
- * must own its base and have an empty log (else DL_EINVAL).  Tokens are
+ * o [T, n, H, d_v] receives every token's output, or is NULL.  q, k, v (and g
+ * for KDA, RWKV6) must be 16-byte aligned, the other tensors aligned to their
+ * element size (else DL_EINVAL).  Every slot must own its base and have an
+ * empty log (else DL_EINVAL).  Tokens are
  * processed C = 32 at a time: one pass over the state per chunk computes all
  * chunk outputs (base + log algebra with the chunk as the log, forward
  * substitution for the delta-rule factors), and the state is rewritten once

@@ -776,10 +776,14 @@ dl_status dl_prefill(dl_ctx* c, const int32_t* slots, int32_t n, int32_t T, cons
   const bool delta = c->cfg.op != DL_RWKV6;
   if (!q || !k || !v || !g || (delta && !beta)) return set_err(c, DL_EINVAL, "NULL tensor pointer");
   if (!delta && !c->bonus) return set_err(c, DL_EINVAL, "RWKV6 needs dl_set_bonus before prefill");
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || (reinterpret_cast<uintptr_t>(g) & 3u) ||
+  // q, k, v and the per-key g rows are read as 16-byte vectors
+  const bool perkey = c->cfg.op != DL_GDN;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) ||
+      (perkey ? !aligned16(g) : (reinterpret_cast<uintptr_t>(g) & 3u) != 0) ||
       (delta && (reinterpret_cast<uintptr_t>(beta) & 3u)) ||
       (o && (reinterpret_cast<uintptr_t>(o) & (c->cfg.out_bf16 ? 1u : 3u))))
-    return set_err(c, DL_EINVAL, "misaligned tensor");
+    return set_err(c, DL_EINVAL, "misaligned tensor: q, k, v%s need 16-byte alignment, "
+                   "other tensors their element size", perkey ? ", g" : "");
   if (n > dl::MAX_ROWS) return set_err(c, DL_EINVAL, "dl_prefill takes at most %d slots per call", dl::MAX_ROWS);
   rc = dl_table_step_eager(c->table, slots, n);
   if (rc != DL_OK)

@@ -58,6 +58,62 @@ struct PfSmem {
 };
 
 __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+
+// One chunk's inputs in registers, between their 16-byte global loads and their
+// shared-memory stores: the next chunk's loads are in flight while the current
+// chunk computes.  (q, k, v are 16-byte aligned and each token's row of a
+// slot-head is d * 2 bytes, so every vector load is aligned.)
+template <int D>
+struct PfStage {
+  static constexpr int VPR = D / 8;                         // 16-byte vectors per row
+  static constexpr int NV = PF_C * VPR / PF_THREADS;        // vectors per thread per tensor
+  static_assert(NV >= 1 && NV * PF_THREADS == PF_C * VPR, "chunk rows must split evenly");
+  uint4 k[NV], q[NV], v[NV];
+  float g, b;
+
+  __device__ __forceinline__ void load(const uint16_t* __restrict__ qg,
+                                       const uint16_t* __restrict__ kg,
+                                       const uint16_t* __restrict__ vg, const float* __restrict__ gg,
+                                       const float* __restrict__ bg, int t0, int Cc, size_t nH,
+                                       int sh, int tid) {
+#pragma unroll
+    for (int e = 0; e < NV; ++e) {
+      const int idx = tid + e * PF_THREADS, j = idx / VPR, cv = idx - j * VPR;
+      if (j < Cc) {
+        const size_t base = ((size_t)(t0 + j) * nH + sh) * D + cv * 8;
+        k[e] = *reinterpret_cast<const uint4*>(kg + base);
+        q[e] = *reinterpret_cast<const uint4*>(qg + base);
+        v[e] = *reinterpret_cast<const uint4*>(vg + base);
+      } else {
+        k[e] = q[e] = v[e] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    if (tid < 32) {
+      g = tid < Cc ? gg[(size_t)(t0 + tid) * nH + sh] : 0.f;
+      b = tid < Cc ? bg[(size_t)(t0 + tid) * nH + sh] : 0.f;
+    }
+  }
+
+  // K and Q rows at stride SP (padded), V rows at stride D, as fp32
+  __device__ __forceinline__ void store(float* Kc, float* Qc, float* Vc, int SP, int tid) const {
+#pragma unroll
+    for (int e = 0; e < NV; ++e) {
+      const int idx = tid + e * PF_THREADS, j = idx / VPR, cv = idx - j * VPR;
+      put8(Kc + j * SP + cv * 8, k[e]);
+      put8(Qc + j * SP + cv * 8, q[e]);
+      put8(Vc + j * D + cv * 8, v[e]);
+    }
+  }
+
+  static __device__ __forceinline__ void put8(float* dst, const uint4 w) {
+    *reinterpret_cast<float4*>(dst) =
+        make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
+                    __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+    *reinterpret_cast<float4*>(dst + 4) =
+        make_float4(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xffff0000u),
+                    __uint_as_float(w.w << 16), __uint_as_float(w.w & 0xffff0000u));
+  }
+};
 __device__ __forceinline__ float dot4(float acc, const float4 a, const float4 b) {
   acc += a.x * b.x;
   acc += a.y * b.y;
@@ -101,27 +157,17 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gdn_kernel(const __grid
     *reinterpret_cast<float4*>(Sb + r * L::SP + c) = *reinterpret_cast<const float4*>(gS + idx);
   }
 
+  static_assert(DK == DV, "square state");
+  PfStage<DK> st;
+  st.load(q, k, v, g, beta, 0, T < PF_C ? T : PF_C, nH, sh, tid);
   for (int t0 = 0; t0 < T; t0 += PF_C) {
     const int Cc = (T - t0) < PF_C ? (T - t0) : PF_C;
     __syncthreads();   // S̄ ready / previous chunk done with K, Q, V, U
-    // ---- stage the chunk: K, Q, V as fp32, Λ (inclusive scan of g), beta
-    for (int idx = tid; idx < PF_C * DK; idx += PF_THREADS) {
-      const int j = idx / DK, c = idx - j * DK;
-      float kx = 0.f, qx = 0.f;
-      if (j < Cc) {
-        const size_t base = ((size_t)(t0 + j) * nH + sh) * DK + c;
-        kx = bf16f(k[base]);
-        qx = bf16f(q[base]);
-      }
-      Kc[j * L::SP + c] = kx;
-      Qc[j * L::SP + c] = qx;
-    }
-    for (int idx = tid; idx < PF_C * DV; idx += PF_THREADS) {
-      const int j = idx / DV, c = idx - j * DV;
-      Vc[idx] = j < Cc ? bf16f(v[((size_t)(t0 + j) * nH + sh) * DV + c]) : 0.f;
-    }
+    // ---- stage the chunk from registers: K, Q, V as fp32, Λ (inclusive scan
+    //      of g), beta; then start loading the next chunk
+    st.store(Kc, Qc, Vc, L::SP, tid);
     if (warp == 0) {
-      float gj = lane < Cc ? g[(size_t)(t0 + lane) * nH + sh] : 0.f;
+      float gj = st.g;
 #pragma unroll
       for (int o2 = 1; o2 < 32; o2 <<= 1) {
         const float y = __shfl_up_sync(0xffffffffu, gj, o2);
@@ -131,7 +177,11 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gdn_kernel(const __grid
       Lm[lane] = gj;
       El[lane] = expf(gj);
       Ew[lane] = lane < Cc ? expf(LC - gj) : 0.f;   // padding tokens add nothing
-      Bt[lane] = lane < Cc ? beta[(size_t)(t0 + lane) * nH + sh] : 0.f;
+      Bt[lane] = st.b;                               // 0 past Cc
+    }
+    if (t0 + PF_C < T) {
+      const int Cn = (T - t0 - PF_C) < PF_C ? (T - t0 - PF_C) : PF_C;
+      st.load(q, k, v, g, beta, t0 + PF_C, Cn, nH, sh, tid);
     }
     __syncthreads();
     // Register tiles below are laid out so that each warp-wide load of a
@@ -306,14 +356,88 @@ struct PkSmem {
   static constexpr int PK_OFF = V_OFF + PF_C * DV;
   static constexpr int PQ_OFF = PK_OFF + DV * PP;
   static constexpr int U_OFF = PQ_OFF + DV * PP;
-  static constexpr int AKK_OFF = U_OFF + DV * PP;
-  static constexpr int AKQ_OFF = AKK_OFF + PF_C * PF_C;
-  static constexpr int B_OFF = AKQ_OFF + PF_C * PF_C;
+  static constexpr int AKK_OFF = U_OFF + DV * PP;            // [C][PP]: padded rows
+  static constexpr int AKQ_OFF = AKK_OFF + PF_C * PP;
+  static constexpr int B_OFF = AKQ_OFF + PF_C * PP;
   static constexpr int CB_OFF = B_OFF + PF_C;
   static constexpr int E_OFF = CB_OFF + PF_C;
   static constexpr int FLOATS = E_OFF + DK;
   static constexpr size_t BYTES = FLOATS * sizeof(float);
 };
+
+// The per-key ops' chunk inputs in registers: k, q (r), v as in PfStage, and
+// the g rows (fp32, one log-decay per key channel; 16-byte aligned rows).
+template <int D>
+struct PkStage {
+  static constexpr int VPR = D / 8, NV = PF_C * VPR / PF_THREADS;
+  static constexpr int GPR = D / 4, NG = PF_C * GPR / PF_THREADS;   // float4 of g
+  static_assert(NV * PF_THREADS == PF_C * VPR && NG * PF_THREADS == PF_C * GPR, "even split");
+  uint4 k[NV], q[NV], v[NV];
+  float4 gv[NG];
+  float b;
+
+  __device__ __forceinline__ void load(const uint16_t* __restrict__ qg,
+                                       const uint16_t* __restrict__ kg,
+                                       const uint16_t* __restrict__ vg, const float* __restrict__ gg,
+                                       const float* __restrict__ bg, int t0, int Cc, size_t nH,
+                                       int sh, int tid) {
+#pragma unroll
+    for (int e = 0; e < NV; ++e) {
+      const int idx = tid + e * PF_THREADS, j = idx / VPR, cv = idx - j * VPR;
+      if (j < Cc) {
+        const size_t base = ((size_t)(t0 + j) * nH + sh) * D + cv * 8;
+        k[e] = *reinterpret_cast<const uint4*>(kg + base);
+        q[e] = *reinterpret_cast<const uint4*>(qg + base);
+        v[e] = *reinterpret_cast<const uint4*>(vg + base);
+      } else {
+        k[e] = q[e] = v[e] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < NG; ++e) {
+      const int idx = tid + e * PF_THREADS, j = idx / GPR, c4 = idx - j * GPR;
+      gv[e] = j < Cc ? *reinterpret_cast<const float4*>(gg + ((size_t)(t0 + j) * nH + sh) * D + c4 * 4)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (tid < 32) b = (bg != nullptr && tid < Cc) ? bg[(size_t)(t0 + tid) * nH + sh] : 0.f;
+  }
+
+  // k, q rows and the g rows at stride SP, v rows at stride D, as fp32
+  __device__ __forceinline__ void store(float* Kc, float* Qc, float* Lc, float* Vc, int SP,
+                                        int tid) const {
+#pragma unroll
+    for (int e = 0; e < NV; ++e) {
+      const int idx = tid + e * PF_THREADS, j = idx / VPR, cv = idx - j * VPR;
+      PfStage<D>::put8(Kc + j * SP + cv * 8, k[e]);
+      PfStage<D>::put8(Qc + j * SP + cv * 8, q[e]);
+      PfStage<D>::put8(Vc + j * D + cv * 8, v[e]);
+    }
+#pragma unroll
+    for (int e = 0; e < NG; ++e) {
+      const int idx = tid + e * PF_THREADS, j = idx / GPR, c4 = idx - j * GPR;
+      *reinterpret_cast<float4*>(Lc + j * SP + c4 * 4) = gv[e];
+    }
+  }
+};
+
+// One channel quad of a decay-weighted pair product: w_c = e^{Λ_j[c] - Λ_i[c]}
+// (for a pair that is not live the exponent is replaced by 0, so the unused
+// result stays finite), kk += k_i[c] w_c k_j[c], qk += k_i[c] w_c q_j[c].
+template <bool DELTA>
+__device__ __forceinline__ void pair_quad(float& kk, float& qk, const float4 ki, const float4 li,
+                                          const float4 lj, const float4 kj, const float4 qj,
+                                          bool live) {
+  const float a[4] = {ki.x, ki.y, ki.z, ki.w}, l0[4] = {li.x, li.y, li.z, li.w};
+  const float l1[4] = {lj.x, lj.y, lj.z, lj.w}, b[4] = {kj.x, kj.y, kj.z, kj.w};
+  const float c[4] = {qj.x, qj.y, qj.z, qj.w};
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const float w = __expf(live ? l1[t] - l0[t] : 0.f);
+    const float kw = a[t] * w;
+    if (DELTA) kk += kw * b[t];
+    qk += kw * c[t];
+  }
+}
 
 template <int OP, int DK, int DV>
 __global__ void __launch_bounds__(PF_THREADS, 1) prefill_perkey_kernel(
@@ -349,28 +473,20 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_perkey_kernel(
     *reinterpret_cast<float4*>(Sb + r * L::SP + c) = *reinterpret_cast<const float4*>(gS + idx);
   }
 
+  static_assert(DK == DV, "square state");
+  PkStage<DK> st;
+  st.load(q, k, v, g, DELTA ? beta : nullptr, 0, T < PF_C ? T : PF_C, nH, sh, tid);
   for (int t0 = 0; t0 < T; t0 += PF_C) {
     const int Cc = (T - t0) < PF_C ? (T - t0) : PF_C;
     __syncthreads();   // S̄ ready / previous chunk done with every buffer
-    // ---- stage the chunk (tokens past the end: zero inputs, zero decay)
-    for (int idx = tid; idx < PF_C * DK; idx += PF_THREADS) {
-      const int j = idx / DK, c = idx - j * DK;
-      float kx = 0.f, qx = 0.f, gx = 0.f;
-      if (j < Cc) {
-        const size_t base = ((size_t)(t0 + j) * nH + sh) * DK + c;
-        kx = bf16f(k[base]);
-        qx = bf16f(q[base]);
-        gx = g[base];
-      }
-      Kc[j * L::SP + c] = kx;
-      Qc[j * L::SP + c] = qx;
-      Lc[j * L::SP + c] = gx;
+    // ---- stage the chunk from registers (tokens past the end: zero inputs,
+    //      zero decay), then start loading the next chunk
+    st.store(Kc, Qc, Lc, Vc, L::SP, tid);
+    if (DELTA && warp == 0) Bt[lane] = st.b;   // 0 past Cc
+    if (t0 + PF_C < T) {
+      const int Cn = (T - t0 - PF_C) < PF_C ? (T - t0 - PF_C) : PF_C;
+      st.load(q, k, v, g, DELTA ? beta : nullptr, t0 + PF_C, Cn, nH, sh, tid);
     }
-    for (int idx = tid; idx < PF_C * DV; idx += PF_THREADS) {
-      const int j = idx / DV, c = idx - j * DV;
-      Vc[idx] = j < Cc ? bf16f(v[((size_t)(t0 + j) * nH + sh) * DV + c]) : 0.f;
-    }
-    if (DELTA && warp == 0) Bt[lane] = lane < Cc ? beta[(size_t)(t0 + lane) * nH + sh] : 0.f;
     __syncthreads();
     // ---- Λ: inclusive scan of g down each key channel; e^{Λ_C}
     if (tid < DK) {
@@ -392,28 +508,41 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_perkey_kernel(
       }
     }
     __syncthreads();
-    // ---- decay-weighted pair coefficients (i <= j; the exponents are <= 0)
-    for (int p = tid; p < PF_C * PF_C; p += PF_THREADS) {
-      const int j = p / PF_C, i = p - j * PF_C;
-      float kk = 0.f, qk = 0.f;
-      const bool live = DELTA ? (i <= j && j < Cc) : (i < j && j < Cc);
-      if (live) {
-        const float* ki = Kc + i * L::SP;
-        const float* kj = Kc + j * L::SP;
-        const float* qj = Qc + j * L::SP;
-        const float* li = Lc + i * L::SP;
-        const float* lj = Lc + (DELTA ? j : j - 1) * L::SP;   // RWKV6 reads S_{j-1}
-#pragma unroll 4
-        for (int c = 0; c < DK; ++c) {
-          const float w = __expf(lj[c] - li[c]);
-          const float kw = ki[c] * w;
-          if (DELTA) kk += kw * kj[c];
-          qk += kw * qj[c];
+    // ---- decay-weighted pair coefficients (live pairs: i <= j for KDA, i < j
+    //      for RWKV6, whose exponents Λ_j - Λ_i (RWKV6: Λ_{j-1} - Λ_i) are <= 0).
+    //      Each thread takes pairs (jg + 16x, ig + 16y); (x, y) = (0, 1) has i > j
+    //      and is never live, (1, 0) always is, the diagonal blocks when ig <= jg
+    //      (RWKV6: ig < jg).  Rows ig and jg keep a warp's quad loads conflict-free.
+    {
+      const int jg = tid >> 4, ig = tid & 15;
+      const int j0 = jg, j1 = jg + 16, i0 = ig, i1 = ig + 16;
+      const bool dl = DELTA ? ig <= jg : ig < jg;
+      const int lr0 = DELTA ? j0 : (j0 > 0 ? j0 - 1 : 0), lr1 = DELTA ? j1 : j1 - 1;
+      float kk[3] = {0.f, 0.f, 0.f}, qk[3] = {0.f, 0.f, 0.f};   // pairs (0,0), (1,0), (1,1)
+#pragma unroll 2
+      for (int c = 0; c < DK; c += 4) {
+        const float4 ki0 = ld4(Kc + i0 * L::SP + c), ki1 = ld4(Kc + i1 * L::SP + c);
+        const float4 li0 = ld4(Lc + i0 * L::SP + c), li1 = ld4(Lc + i1 * L::SP + c);
+        const float4 lj0 = ld4(Lc + lr0 * L::SP + c), lj1 = ld4(Lc + lr1 * L::SP + c);
+        const float4 qj0 = ld4(Qc + j0 * L::SP + c), qj1 = ld4(Qc + j1 * L::SP + c);
+        float4 kj0 = make_float4(0.f, 0.f, 0.f, 0.f), kj1 = kj0;
+        if (DELTA) {
+          kj0 = ld4(Kc + j0 * L::SP + c);
+          kj1 = ld4(Kc + j1 * L::SP + c);
         }
-        if (DELTA && i == j) kk = 0.f;
+        pair_quad<DELTA>(kk[0], qk[0], ki0, li0, lj0, kj0, qj0, dl);
+        pair_quad<DELTA>(kk[1], qk[1], ki0, li0, lj1, kj1, qj1, true);
+        pair_quad<DELTA>(kk[2], qk[2], ki1, li1, lj1, kj1, qj1, dl);
       }
-      Akk[p] = kk;
-      Akq[p] = qk;
+      auto put = [&](int j, int i, float kv, float qv, bool live) {
+        const bool ok = live && j < Cc;
+        Akk[j * L::PP + i] = (DELTA && ok && i != j) ? kv : 0.f;
+        Akq[j * L::PP + i] = ok ? qv : 0.f;
+      };
+      put(j0, i0, kk[0], qk[0], dl);
+      put(j0, i1, 0.f, 0.f, false);
+      put(j1, i0, kk[1], qk[1], true);
+      put(j1, i1, kk[2], qk[2], dl);
     }
     __syncthreads();
     // ---- hats: e^{Λ_j}⊙k_j (KDA) into X; e^{Λ_j}⊙q_j (KDA) or e^{Λ_{j-1}}⊙r_j in place
@@ -428,43 +557,54 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_perkey_kernel(
       }
     }
     __syncthreads();
-    // ---- S̄ products: two threads per value row, 16 tokens each
-    if ((tid >> 1) < DV) {
-      const int r = tid >> 1, jh = (tid & 1) * (PF_C / 2);
-      float pk[PF_C / 2], pq[PF_C / 2];
+    // ---- S̄ products: rows rg + 32 m, tokens tg + 8 t per thread
+    {
+      constexpr int RPT = DV / 32;
+      const int rg = tid >> 3, tg = tid & 7;
+      float pk[RPT][4], pq[RPT][4];
 #pragma unroll
-      for (int j = 0; j < PF_C / 2; ++j) pk[j] = pq[j] = 0.f;
-      const float* sr = Sb + r * L::SP;
+      for (int m = 0; m < RPT; ++m)
+#pragma unroll
+        for (int t = 0; t < 4; ++t) pk[m][t] = pq[m][t] = 0.f;
+#pragma unroll 2
       for (int c = 0; c < DK; c += 4) {
-        const float4 s4 = *reinterpret_cast<const float4*>(sr + c);
+        float4 s4[RPT], x4[4], q4[4];
 #pragma unroll
-        for (int j = 0; j < PF_C / 2; ++j) {
-          const float4 q4 = *reinterpret_cast<const float4*>(Qc + (jh + j) * L::SP + c);
-          pq[j] += s4.x * q4.x + s4.y * q4.y + s4.z * q4.z + s4.w * q4.w;
-          if (DELTA) {
-            const float4 k4 = *reinterpret_cast<const float4*>(Xc + (jh + j) * L::SP + c);
-            pk[j] += s4.x * k4.x + s4.y * k4.y + s4.z * k4.z + s4.w * k4.w;
-          }
+        for (int m = 0; m < RPT; ++m) s4[m] = ld4(Sb + (rg + 32 * m) * L::SP + c);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          q4[t] = ld4(Qc + (tg + 8 * t) * L::SP + c);
+          if (DELTA) x4[t] = ld4(Xc + (tg + 8 * t) * L::SP + c);
         }
+#pragma unroll
+        for (int m = 0; m < RPT; ++m)
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            pq[m][t] = dot4(pq[m][t], s4[m], q4[t]);
+            if (DELTA) pk[m][t] = dot4(pk[m][t], s4[m], x4[t]);
+          }
       }
 #pragma unroll
-      for (int j = 0; j < PF_C / 2; ++j) {
-        Pk[r * L::PP + jh + j] = pk[j];
-        Pq[r * L::PP + jh + j] = pq[j];
-      }
+      for (int m = 0; m < RPT; ++m)
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          Pk[(rg + 32 * m) * L::PP + tg + 8 * t] = pk[m][t];
+          Pq[(rg + 32 * m) * L::PP + tg + 8 * t] = pq[m][t];
+        }
     }
     __syncthreads();
-    // ---- the appended factors and the outputs: one thread per value row
+    // ---- the appended factors and the outputs: one thread per value row; each
+    //      sum runs in four partial sums to shorten its chain
     if (tid < DV) {
       const int r = tid;
       float u[PF_C];
 #pragma unroll
       for (int j = 0; j < PF_C; ++j) {
         if (DELTA) {
-          float x = Pk[r * L::PP + j];
+          float x[4] = {Pk[r * L::PP + j], 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int i = 0; i < j; ++i) x += Akk[j * PF_C + i] * u[i];
-          u[j] = (j < Cc) ? Bt[j] * (Vc[j * DV + r] - x) : 0.f;
+          for (int i = 0; i < j; ++i) x[i & 3] += Akk[j * L::PP + i] * u[i];
+          u[j] = Bt[j] * (Vc[j * DV + r] - ((x[0] + x[1]) + (x[2] + x[3])));   // 0 past Cc
         } else {
           u[j] = Vc[j * DV + r];
         }
@@ -473,13 +613,14 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_perkey_kernel(
       for (int j = 0; j < PF_C; ++j) {
         Us[r * L::PP + j] = u[j];
         if (o != nullptr && j < Cc) {
-          float y = Pq[r * L::PP + j];
+          float y[4] = {Pq[r * L::PP + j], 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int i = 0; i <= j; ++i) y += Akq[j * PF_C + i] * u[i];   // (RWKV6: zero at i = j)
-          if (!DELTA) y += Cb[j] * u[j];
+          for (int i = 0; i <= j; ++i) y[i & 3] += Akq[j * L::PP + i] * u[i];   // (RWKV6: zero at i = j)
+          float yo = (y[0] + y[1]) + (y[2] + y[3]);
+          if (!DELTA) yo += Cb[j] * u[j];
           const size_t oi = ((size_t)(t0 + j) * nH + sh) * DV + r;
-          if (out_bf16) static_cast<uint16_t*>(o)[oi] = f2bf16(scale * y);
-          else static_cast<float*>(o)[oi] = scale * y;
+          if (out_bf16) static_cast<uint16_t*>(o)[oi] = f2bf16(scale * yo);
+          else static_cast<float*>(o)[oi] = scale * yo;
         }
       }
     }
@@ -490,28 +631,42 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_perkey_kernel(
           Kc[j * L::SP + c] * expf(Lc[(PF_C - 1) * L::SP + c] - Lc[j * L::SP + c]);
     }
     __syncthreads();
-    // ---- S̄ <- S̄ Diag(e^{Λ_C}) + Σ_j a_j (k_j ⊙ e^{Λ_C-Λ_j})^T: two threads per row
-    if ((tid >> 1) < DV) {
-      const int r = tid >> 1, c0 = (tid & 1) * (DK / 2);
-      float acc[DK / 2];
+    // ---- S̄ <- S̄ Diag(e^{Λ_C}) + Σ_j a_j (k_j ⊙ e^{Λ_C-Λ_j})^T: rows rg + 32 m
+    //      and column quads 4 tg + 32 n per thread
+    {
+      constexpr int RPT = DV / 32, CPT = DK / 32;
+      const int rg = tid >> 3, tg = tid & 7;
+      float4 acc[RPT][CPT];
 #pragma unroll
-      for (int c = 0; c < DK / 2; c += 4) {
-        const float4 s4 = *reinterpret_cast<const float4*>(Sb + r * L::SP + c0 + c);
-        const float4 e4 = *reinterpret_cast<const float4*>(Ec + c0 + c);
-        acc[c] = e4.x * s4.x; acc[c + 1] = e4.y * s4.y; acc[c + 2] = e4.z * s4.z; acc[c + 3] = e4.w * s4.w;
+      for (int n4 = 0; n4 < CPT; ++n4) {
+        const float4 e4 = ld4(Ec + 4 * tg + 32 * n4);
+#pragma unroll
+        for (int m = 0; m < RPT; ++m) {
+          const float4 s4 = ld4(Sb + (rg + 32 * m) * L::SP + 4 * tg + 32 * n4);
+          acc[m][n4] = make_float4(e4.x * s4.x, e4.y * s4.y, e4.z * s4.z, e4.w * s4.w);
+        }
       }
       for (int j = 0; j < Cc; ++j) {
-        const float w = Us[r * L::PP + j];
+        float w[RPT];
 #pragma unroll
-        for (int c = 0; c < DK / 2; c += 4) {
-          const float4 k4 = *reinterpret_cast<const float4*>(Xc + j * L::SP + c0 + c);
-          acc[c] += w * k4.x; acc[c + 1] += w * k4.y; acc[c + 2] += w * k4.z; acc[c + 3] += w * k4.w;
+        for (int m = 0; m < RPT; ++m) w[m] = Us[(rg + 32 * m) * L::PP + j];
+#pragma unroll
+        for (int n4 = 0; n4 < CPT; ++n4) {
+          const float4 k4 = ld4(Xc + j * L::SP + 4 * tg + 32 * n4);
+#pragma unroll
+          for (int m = 0; m < RPT; ++m) {
+            acc[m][n4].x += w[m] * k4.x;
+            acc[m][n4].y += w[m] * k4.y;
+            acc[m][n4].z += w[m] * k4.z;
+            acc[m][n4].w += w[m] * k4.w;
+          }
         }
       }
 #pragma unroll
-      for (int c = 0; c < DK / 2; c += 4)
-        *reinterpret_cast<float4*>(Sb + r * L::SP + c0 + c) =
-            make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
+      for (int m = 0; m < RPT; ++m)
+#pragma unroll
+        for (int n4 = 0; n4 < CPT; ++n4)
+          *reinterpret_cast<float4*>(Sb + (rg + 32 * m) * L::SP + 4 * tg + 32 * n4) = acc[m][n4];
     }
   }
   __syncthreads();
