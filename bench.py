@@ -245,8 +245,9 @@ def run_reference(args):
     import torch
     import oracle
     from linear_attention_recurrent_gdn_gb300 import inputs as gen
-    # a prefill computes the decode recurrence over its context: same oracle
-    w = WORKLOADS[PREFILL.get(args.workload, args.workload)]
+    # a prefill computes the decode recurrence over its context, and a checkpoint
+    # belongs to the GDN serving batch: same oracle
+    w = WORKLOADS[PREFILL.get(args.workload, "gdn" if args.workload == "checkpoint" else args.workload)]
     sample_sh = int(os.environ.get("DL_REF_SLOT_HEADS", "4096"))
     tokens = int(os.environ.get("DL_REF_TOKENS", "512"))
     oracle.build()
@@ -622,6 +623,82 @@ def run_prefill(args):
     return 0
 
 
+def hbm_peak():
+    """HBM copy bandwidth (GB/s): MEASURED_PEAKS.json, else the fallback figure."""
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        return float(peaks["hbm_gbs"]), "measured hbm_gbs"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def run_checkpoint(args):
+    """Prefix checkpoints: one bench step saves every slot of the GDN serving
+    batch (its base, log rows and log length) into a device buffer and restores
+    it.  Each slot holds an 8-entry log."""
+    import torch
+    rank, world, dist = dist_setup("cuda")
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    from linear_attention_recurrent_gdn_gb300 import build
+    if rank == 0:
+        build.build()
+    barrier(dist)
+    from linear_attention_recurrent_gdn_gb300 import deltalog as dl
+    from linear_attention_recurrent_gdn_gb300 import inputs as gen
+    w = WORKLOADS["gdn"]
+    op, B, H, d, M = w["op"], args.B or w["B"], w["H"], w["d"], w["M"]
+    seed = w["seed"] + 7919 * rank
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    ctx = dl.DeltaLog(op, B, H, d, d, M, stream=stream.cuda_stream)
+    slots = list(range(B))
+    ctx.set_state(slots, gen.initial_state(B, H, d, d, seed, device=dev))
+    x = gen.make_inputs(op, 8, B, H, d, d, seed, device=dev)
+    for t in range(8):
+        ctx.step(slots, x["q"][t], x["k"][t], x["v"][t], x["g"][t], x["beta"][t])
+    per = dl.dl_checkpoint_bytes(ctx._h)
+    buf = torch.empty(B * per, dtype=torch.uint8, device=dev)
+
+    def one():
+        ctx.checkpoint_save(slots, buf)
+        ctx.checkpoint_load(slots, buf)
+
+    for _ in range(args.warmup):
+        one()
+    barrier(dist)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            one()
+        e1.record(stream)
+        e1.synchronize()
+    ms = reduce_max(dist, e0.elapsed_time(e1) / args.steps, dev)
+    moved = 4 * B * per          # save reads and writes a record's bytes, restore too
+    gbs = moved / (ms / 1e3) / 1e9
+    peak, src = hbm_peak()
+    result = {"metric": "checkpoint save + restore GB/s", "value": gbs * world, "unit": "GB/s",
+              "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+              "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+              "data": "synthetic",
+              "config": {"workload": "checkpoint save + restore of every slot, " +
+                         w["desc"].split(",")[0] + ", M=%d, 8 log entries" % M,
+                         "slots": B, "record_bytes": per,
+                         "l2": "records larger than L2 (%.0f MB)" % (B * per / 1e6)},
+              "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                           "frac": gbs / peak, "traffic": None, "peak_source": src},
+              "clocks": clk.summary(),
+              "gpu_launches": args.steps * 2 * ((B + 1023) // 1024)}
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    ctx.close()
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
 def run_fork(args):
     """Forked decode: bases are built once (setup, untimed); one bench step =
     fork every request into its branches (by index, no state copy) + the
@@ -725,7 +802,8 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="gdn", choices=sorted(WORKLOADS) + sorted(PREFILL))
+    ap.add_argument("--workload", default="gdn",
+                    choices=sorted(WORKLOADS) + sorted(PREFILL) + ["checkpoint"])
     ap.add_argument("--M", type=int, default=0)
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
@@ -745,6 +823,8 @@ def main():
         return run_fork(args)
     if args.workload in PREFILL:
         return run_prefill(args)
+    if args.workload == "checkpoint":
+        return run_checkpoint(args)
     return run_ours(args)
 
 

@@ -72,6 +72,7 @@ struct dl_ctx {
   std::vector<int32_t> plan;
   std::unique_ptr<dl::StepArgs> step_args;
   std::unique_ptr<dl::SlotListArgs> list_args;
+  std::unique_ptr<dl::CkptArgs> ckpt_args;
   std::string err = "no error";
   dl_status sticky = DL_OK;
   bool timing = false;
@@ -376,10 +377,11 @@ dl_status dl_create(const dl_config* cfg, void* stream, dl_ctx** out) {
   c->plan.resize(4 * (size_t)f.num_slots);
   c->step_args.reset(new (std::nothrow) dl::StepArgs());
   c->list_args.reset(new (std::nothrow) dl::SlotListArgs());
+  c->ckpt_args.reset(new (std::nothrow) dl::CkptArgs());
   if (const char* s = getenv("DL_TEST_FAIL_ALLOC")) g_fail_countdown = atoi(s);
   dl_status rc = DL_OK;
   do {
-    if (!c->step_args || !c->list_args) { rc = DL_ENOMEM; break; }
+    if (!c->step_args || !c->list_args || !c->ckpt_args) { rc = DL_ENOMEM; break; }
     if (dl_table_create(f.num_slots, f.merge_interval, &c->table) != DL_OK) { rc = DL_ENOMEM; break; }
     cudaError_t e = cudaGetDevice(&c->device);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
@@ -823,34 +825,49 @@ static CkptLayout ckpt_layout(const dl_ctx* c) {
 
 int64_t dl_checkpoint_bytes(const dl_ctx* c) { return c ? (int64_t)ckpt_layout(c).total : -1; }
 
+// One launch per MAX_ROWS slots moves the records (checkpoint_kernel).
+static dl_status checkpoint_copy(dl_ctx* c, const int32_t* slots, int32_t n, unsigned char* buf,
+                                 const int32_t* bases, int save) {
+  const CkptLayout k = ckpt_layout(c);
+  const dl_config& f = c->cfg;
+  for (int32_t r0 = 0; r0 < n; r0 += dl::MAX_ROWS) {
+    const int32_t rows = (n - r0) < dl::MAX_ROWS ? (n - r0) : dl::MAX_ROWS;
+    dl::CkptArgs& a = *c->ckpt_args;
+    a.Sbar = c->Sbar;
+    a.alog = c->alog;
+    a.klog = c->klog;
+    a.Llog = c->Llog;
+    a.nlog = c->nlog;
+    a.base_of = c->base_of;
+    a.buf = buf + (size_t)r0 * k.total;
+    a.total = k.total;
+    a.offS = k.S;
+    a.offA = k.A;
+    a.offK = k.K;
+    a.offL = k.L;
+    a.offN = k.N;
+    a.rows = rows;
+    a.H = f.num_heads;
+    a.Mcap = c->L.Mcap;
+    a.save = save;
+    for (int32_t i = 0; i < rows; ++i)
+      a.items[i] = dl::StepItem{slots[r0 + i], bases ? bases[r0 + i] : slots[r0 + i], 0};
+    DL_CUDA(dl::launch_checkpoint(f.op, f.d_k, a, c->stream), save ? "checkpoint save" : "checkpoint restore");
+  }
+  return DL_OK;
+}
+
 dl_status dl_checkpoint_save(dl_ctx* c, const int32_t* slots, int32_t n, void* buf) {
   dl_status rc = check_ctx(c);
   if (rc != DL_OK) return rc;
   if (n < 0 || (n > 0 && (!buf || !aligned16(buf)))) return set_err(c, DL_EINVAL, "bad buffer");
   rc = dl_table_check(c->table, slots, n);
   if (rc != DL_OK) return set_err(c, rc, "dl_checkpoint_save: invalid slot list");
-  const CkptLayout k = ckpt_layout(c);
-  const dl_config& f = c->cfg;
-  const size_t H = f.num_heads, Mcap = c->L.Mcap;
-  const size_t sS = H * f.d_v * f.d_k * 4, sA = H * Mcap * f.d_v * (f.op == DL_RWKV6 ? 2 : 4),
-               sK = H * Mcap * f.d_k * 2, sL = H * Mcap * (f.op == DL_GDN ? 1 : f.d_k) * 4;
-  std::vector<int32_t> nl(f.num_slots), bo(f.num_slots);
+  if (n == 0) return DL_OK;
+  std::vector<int32_t> nl(c->cfg.num_slots), bo(c->cfg.num_slots), bases(n);
   dl_table_get(c->table, nl.data(), bo.data(), nullptr);
-  for (int32_t i = 0; i < n; ++i) {
-    unsigned char* dst = static_cast<unsigned char*>(buf) + (size_t)i * k.total;
-    const size_t s = slots[i], b = bo[slots[i]];
-    DL_CUDA(cudaMemcpyAsync(dst + k.S, reinterpret_cast<unsigned char*>(c->Sbar) + b * sS, sS,
-                            cudaMemcpyDeviceToDevice, c->stream), "checkpoint copy");
-    DL_CUDA(cudaMemcpyAsync(dst + k.A, static_cast<unsigned char*>(c->alog) + s * sA, sA,
-                            cudaMemcpyDeviceToDevice, c->stream), "checkpoint copy");
-    DL_CUDA(cudaMemcpyAsync(dst + k.K, reinterpret_cast<unsigned char*>(c->klog) + s * sK, sK,
-                            cudaMemcpyDeviceToDevice, c->stream), "checkpoint copy");
-    DL_CUDA(cudaMemcpyAsync(dst + k.L, reinterpret_cast<unsigned char*>(c->Llog) + s * sL, sL,
-                            cudaMemcpyDeviceToDevice, c->stream), "checkpoint copy");
-    DL_CUDA(cudaMemcpyAsync(dst + k.N, c->nlog + s, 4, cudaMemcpyDeviceToDevice, c->stream),
-            "checkpoint copy");
-  }
-  return DL_OK;
+  for (int32_t i = 0; i < n; ++i) bases[i] = bo[slots[i]];
+  return checkpoint_copy(c, slots, n, static_cast<unsigned char*>(buf), bases.data(), 1);
 }
 
 dl_status dl_checkpoint_load(dl_ctx* c, const int32_t* slots, int32_t n, const void* buf) {
@@ -859,11 +876,13 @@ dl_status dl_checkpoint_load(dl_ctx* c, const int32_t* slots, int32_t n, const v
   if (n < 0 || (n > 0 && (!buf || !aligned16(buf)))) return set_err(c, DL_EINVAL, "bad buffer");
   rc = dl_table_check(c->table, slots, n);
   if (rc != DL_OK) return set_err(c, rc, "dl_checkpoint_load: invalid slot list");
+  if (n == 0) return DL_OK;
   const CkptLayout k = ckpt_layout(c);
-  std::vector<int32_t> ns(n > 0 ? n : 1);
-  for (int32_t i = 0; i < n; ++i)
-    DL_CUDA(cudaMemcpyAsync(&ns[i], static_cast<const unsigned char*>(buf) + (size_t)i * k.total + k.N,
-                            4, cudaMemcpyDeviceToHost, c->stream), "checkpoint read");
+  // the saved log lengths, one strided copy, validated before anything changes
+  std::vector<int32_t> ns(n);
+  DL_CUDA(cudaMemcpy2DAsync(ns.data(), 4, static_cast<const unsigned char*>(buf) + k.N, k.total, 4,
+                            n, cudaMemcpyDeviceToHost, c->stream),
+          "checkpoint read");
   DL_CUDA(cudaStreamSynchronize(c->stream), "stream sync");
   for (int32_t i = 0; i < n; ++i)
     if (ns[i] < 0 || ns[i] >= c->cfg.merge_interval)
@@ -871,28 +890,9 @@ dl_status dl_checkpoint_load(dl_ctx* c, const int32_t* slots, int32_t n, const v
                      c->cfg.merge_interval);
   rc = dl_table_reset(c->table, slots, n);     // validates frozen slots, owns base, n = 0
   if (rc != DL_OK) return set_err(c, rc, "dl_checkpoint_load: frozen slot");
-  const dl_config& f = c->cfg;
-  const size_t H = f.num_heads, Mcap = c->L.Mcap;
-  const size_t sS = H * f.d_v * f.d_k * 4, sA = H * Mcap * f.d_v * (f.op == DL_RWKV6 ? 2 : 4),
-               sK = H * Mcap * f.d_k * 2, sL = H * Mcap * (f.op == DL_GDN ? 1 : f.d_k) * 4;
-  for (int32_t i = 0; i < n; ++i) {
-    const unsigned char* src = static_cast<const unsigned char*>(buf) + (size_t)i * k.total;
-    const size_t s = slots[i];
-    DL_CUDA(cudaMemcpyAsync(reinterpret_cast<unsigned char*>(c->Sbar) + s * sS, src + k.S, sS,
-                            cudaMemcpyDeviceToDevice, c->stream), "restore copy");
-    DL_CUDA(cudaMemcpyAsync(static_cast<unsigned char*>(c->alog) + s * sA, src + k.A, sA,
-                            cudaMemcpyDeviceToDevice, c->stream), "restore copy");
-    DL_CUDA(cudaMemcpyAsync(reinterpret_cast<unsigned char*>(c->klog) + s * sK, src + k.K, sK,
-                            cudaMemcpyDeviceToDevice, c->stream), "restore copy");
-    DL_CUDA(cudaMemcpyAsync(reinterpret_cast<unsigned char*>(c->Llog) + s * sL, src + k.L, sL,
-                            cudaMemcpyDeviceToDevice, c->stream), "restore copy");
-    DL_CUDA(cudaMemcpyAsync(c->nlog + s, src + k.N, 4, cudaMemcpyDeviceToDevice, c->stream),
-            "restore copy");
-    const int32_t self = (int32_t)s;
-    DL_CUDA(cudaMemcpyAsync(c->base_of + s, &self, 4, cudaMemcpyHostToDevice, c->stream),
-            "restore copy");
-    DL_CUDA(cudaStreamSynchronize(c->stream), "stream sync");   // `self` lives on the host stack
-  }
+  rc = checkpoint_copy(c, slots, n,
+                       const_cast<unsigned char*>(static_cast<const unsigned char*>(buf)), nullptr, 0);
+  if (rc != DL_OK) return rc;
   dl_table_set_n(c->table, slots, n, ns.data());
   return DL_OK;
 }

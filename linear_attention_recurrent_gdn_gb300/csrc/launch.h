@@ -65,6 +65,25 @@ cudaError_t launch_set_state(int dk, int dv, const SlotListArgs& a, cudaStream_t
 // Copy the source's log rows into each destination and point it at the source's base.
 cudaError_t launch_fork(int op, int dk, const SlotListArgs& a, cudaStream_t s);
 
+// Checkpoint records (one fixed-size record per listed slot, at buf + row *
+// total): the dense base the slot reads [H, d_v, d_k] at offS, its log rows —
+// value side at offA, keys at offK, log-decays at offL — and its log length at
+// offN.  save = 1 copies the slots into the records (items[row].base names the
+// base the slot reads); save = 0 restores them (the slot then owns its base).
+struct CkptArgs {
+  float* Sbar;
+  void* alog;
+  uint16_t* klog;
+  float* Llog;
+  int32_t* nlog;
+  int32_t* base_of;
+  unsigned char* buf;
+  size_t total, offS, offA, offK, offL, offN;
+  int32_t rows, H, Mcap, save;
+  StepItem items[MAX_ROWS];
+};
+cudaError_t launch_checkpoint(int op, int dk, const CkptArgs& a, cudaStream_t s);
+
 // Chunked prefill of T tokens: token-major inputs [T, rows, H, d]; `bonus`
 // [H, d_k] for RWKV6.
 cudaError_t launch_prefill(int op, int dk, const SlotListArgs& a, const void* q, const void* k,

@@ -4,7 +4,10 @@
 //     caller buffer (read-out; the context is unchanged);
 //   * SetState — load initial states into S̄;
 //   * Fork — Flide page, "Research method step by step", second step: a branch
-//     indexes the source's saved state; only the source's log rows are copied.
+//     indexes the source's saved state; only the source's log rows are copied;
+//   * Checkpoint save / restore — Flide page, fourth step: a slot's exact
+//     representation (the base it reads, its log rows and length) to and from a
+//     caller-owned record.
 #include "dl_device.cuh"
 #include "layout.h"
 #include "launch.h"
@@ -121,6 +124,71 @@ __global__ void __launch_bounds__(128) fork_kernel(const __grid_constant__ SlotL
     a.nlog[dst] = n;
     a.base_of[dst] = a.src_base;
   }
+}
+
+// One CTA per (row, head): the head's slice of each record segment.
+template <int OP, int DK, int DV>
+__global__ void __launch_bounds__(256) checkpoint_kernel(const __grid_constant__ CkptArgs a) {
+  constexpr int ESA = (OP == RWKV6) ? 2 : 4;
+  constexpr int LW = (OP == GDN) ? 1 : DK;    // log-decay floats per entry
+  const int b = blockIdx.x, h = b % a.H, row = b / a.H;
+  const StepItem it = a.items[row];
+  const size_t Mcap = a.Mcap;
+  unsigned char* rec = a.buf + (size_t)row * a.total;
+  const size_t lh = (size_t)it.slot * a.H + h;
+  auto copy16 = [&](unsigned char* dst, const unsigned char* src, size_t bytes) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+    for (size_t i = threadIdx.x; i < bytes / 16; i += 256) d4[i] = s4[i];
+  };
+  const size_t sS = (size_t)DV * DK * 4, sA = Mcap * DV * ESA, sK = Mcap * DK * 2;
+  unsigned char* gS = reinterpret_cast<unsigned char*>(a.Sbar) +
+                      ((size_t)(a.save ? it.base : it.slot) * a.H + h) * sS;
+  unsigned char* gA = static_cast<unsigned char*>(a.alog) + lh * sA;
+  unsigned char* gK = reinterpret_cast<unsigned char*>(a.klog) + lh * sK;
+  unsigned char* cS = rec + a.offS + h * sS;
+  unsigned char* cA = rec + a.offA + h * sA;
+  unsigned char* cK = rec + a.offK + h * sK;
+  float* gL = a.Llog + lh * Mcap * LW;
+  float* cL = reinterpret_cast<float*>(rec + a.offL) + h * Mcap * LW;
+  if (a.save) {
+    copy16(cS, gS, sS);
+    copy16(cA, gA, sA);
+    copy16(cK, gK, sK);
+    for (size_t i = threadIdx.x; i < Mcap * LW; i += 256) cL[i] = gL[i];
+  } else {
+    copy16(gS, cS, sS);
+    copy16(gA, cA, sA);
+    copy16(gK, cK, sK);
+    for (size_t i = threadIdx.x; i < Mcap * LW; i += 256) gL[i] = cL[i];
+  }
+  if (h == 0 && threadIdx.x == 0) {
+    int32_t* rn = reinterpret_cast<int32_t*>(rec + a.offN);
+    if (a.save) {
+      *rn = a.nlog[it.slot];
+    } else {
+      a.nlog[it.slot] = *rn;
+      a.base_of[it.slot] = it.slot;
+    }
+  }
+}
+
+template <int OP, int DK>
+static cudaError_t checkpoint_dispatch(const CkptArgs& a, cudaStream_t s) {
+  checkpoint_kernel<OP, DK, DK><<<a.rows * a.H, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_checkpoint(int op, int dk, const CkptArgs& a, cudaStream_t s) {
+  if (a.rows <= 0) return cudaSuccess;
+  if (dk == 64) {
+    if (op == GDN) return checkpoint_dispatch<GDN, 64>(a, s);
+    if (op == KDA) return checkpoint_dispatch<KDA, 64>(a, s);
+    return checkpoint_dispatch<RWKV6, 64>(a, s);
+  }
+  if (op == GDN) return checkpoint_dispatch<GDN, 128>(a, s);
+  if (op == KDA) return checkpoint_dispatch<KDA, 128>(a, s);
+  return checkpoint_dispatch<RWKV6, 128>(a, s);
 }
 
 template <int OP, int DK>

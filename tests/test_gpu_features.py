@@ -94,6 +94,40 @@ def test_checkpoint_resume_bitwise(op, t_save):
 
 
 @pytest.mark.parametrize("op", OPS)
+def test_checkpoint_many_slots_with_fork_branch(op):
+    """One save of three slots, one of them a fork branch that still reads its
+    source's base and holds a log entry of its own, restored under other slot
+    ids in another context: both then step bit for bit alike. M=3 leaves GDN's
+    log-decay rows at 12 bytes a head."""
+    from linear_attention_recurrent_gdn_gb300 import deltalog as dl
+    H, d, M, T0, T1 = 5, 128, 3, 4, 5
+    T = T0 + 1 + T1
+    x, S0, bonus = make_case(op, 3, H, d, T, seed=520 + op, device="cuda")
+    ctx = dl.DeltaLog(op, 6, H, d, d, M, out_bf16=False)
+    other = dl.DeltaLog(op, 4, H, d, d, M, out_bf16=False)
+    ctx.set_state([0, 1, 2], S0)
+    for c in (ctx, other):
+        if bonus is not None:
+            c.set_bonus(bonus)
+    beta = lambda t: x["beta"][t] if x["beta"] is not None else None
+    for t in range(T0):
+        ctx.step([0, 1, 2], x["q"][t], x["k"][t], x["v"][t], x["g"][t], beta(t))
+    ctx.fork(0, [3])
+    ctx.step([1, 2, 3], x["q"][T0], x["k"][T0], x["v"][T0], x["g"][T0], beta(T0))
+    n, base_of = ctx.get_meta()
+    assert base_of[3] == 0 and n[3] == T0 % M + 1     # still on the source's base
+    buf = ctx.checkpoint_save([1, 3, 2])
+    other.checkpoint_load([0, 1, 2], buf)
+    n2, base2 = other.get_meta()
+    assert list(n2[:3]) == [n[1], n[3], n[2]] and list(base2[:3]) == [0, 1, 2]
+    for t in range(T0 + 1, T):
+        oa = ctx.step([1, 3, 2], x["q"][t], x["k"][t], x["v"][t], x["g"][t], beta(t))
+        ob = other.step([0, 1, 2], x["q"][t], x["k"][t], x["v"][t], x["g"][t], beta(t))
+        assert torch.equal(oa, ob), t
+    assert torch.equal(ctx.read_state([1, 3, 2]), other.read_state([0, 1, 2]))
+
+
+@pytest.mark.parametrize("op", OPS)
 def test_graph_window_matches_stepping_bitwise(op):
     """A captured merge window replayed 3 times gives the bits of 3*M plain
     steps; the inputs are refilled between launches."""
