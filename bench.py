@@ -768,13 +768,19 @@ def run_fork(args):
     barrier(dist)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        one()
-    e1.record(stream)
-    e1.synchronize()
+    with ClockSampler(local) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            one()
+        e1.record(stream)
+        e1.synchronize()
     ms = reduce_max(dist, e0.elapsed_time(e1) / args.steps, dev)
     units = int(lens.sum()) * H
+    # every branch starts at the source's log length 0, so the branches active at
+    # token t all step with log length t mod M
+    step_bytes = sum(counts[t] * H * fused_bytes(0, d, M, t % M)[0] for t in range(Tq))
+    gbs = step_bytes / (ms / 1e3) / 1e9
+    peak, peak_src = hbm_peak()
     result = {"metric": METRIC, "value": units * world / (ms / 1e3), "unit": "tokens·heads/s",
               "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
               "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
@@ -785,6 +791,12 @@ def run_fork(args):
                          "loop": ("ragged CUDA graphs, one per M tokens (dl_window_*_ragged)"
                                   if wins else "dl_step per token"),
                          "l2": "inputs larger than L2 (576 slots x 1 MiB state)"},
+              "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                           "frac": gbs / peak, "traffic": None, "peak_source": peak_src,
+                           "kernel": "AppendDecode over the ragged branch batch, fork "
+                                     "launches included",
+                           "algorithmic_bytes_per_step": step_bytes},
+              "clocks": clk.summary(),
               "gpu_launches": (R + (1 if fused else 2) * Tpad) * args.steps}
     if rank == 0:
         print(json.dumps(result), flush=True)
