@@ -542,15 +542,16 @@ def run_ours(args):
 
 
 def prefill_flops(op, d, C=PREFILL_C):
-    """FLOPs (an FMA counts 2) per token·head of the chunked prefill, d_k = d_v = d.
-    Per token: the products with S̄ (S̄K^T and S̄Q^T, 2 d^2; RWKV6 only S̄R̂^T, d^2),
-    S̄'s rewrite (the rank-C update d^2 and the chunk-end scaling d^2 / C), the
-    decay-weighted pair products of the chunk's lower triangle (delta rule: k·k
-    strictly below and k·q on and below the diagonal, C d; RWKV6: k·r strictly
-    below, (C - 1) d / 2), and the forward substitution with the outputs
-    (C d; RWKV6 the outputs, (C - 1) d / 2).  Exponentials are not counted."""
+    """FLOPs (an FMA counts 2) per token·head of the chunked prefill's
+    contractions, d_k = d_v = d.  Per token: the products with S̄ (S̄K^T and S̄Q^T,
+    2 d^2; RWKV6 only S̄R̂^T, d^2), S̄'s rewrite (the rank-C update d^2 and the
+    chunk-end scaling d^2 / C), the decay-weighted pair products of the chunk's
+    lower triangle (delta rule: k·k strictly below and k·q on and below the
+    diagonal, C d; RWKV6: k·r strictly below, (C - 1) d / 2), and the forward
+    substitution with the outputs (C d; RWKV6 the outputs, (C - 1) d / 2, and
+    their bonus term, d).  Exponentials and elementwise scalings are not counted."""
     if op == 2:
-        fma = 2 * d * d + d * d / C + (C - 1) * d
+        fma = 2 * d * d + d * d / C + C * d
     else:
         fma = 3 * d * d + d * d / C + 2 * C * d
     return 2 * fma
