@@ -80,7 +80,7 @@ typedef enum dl_status {
     DL_ECUDA = 3,        /* a CUDA runtime call failed                              */
     DL_EBUSY = 4,        /* slot frozen: its base is indexed by a forked branch     */
     DL_EDEVICE = 5,      /* a kernel reported an error through the status word      */
-    DL_EUNSUPPORTED = 6  /* configuration this build has no kernel for              */
+    DL_EUNSUPPORTED = 6  /* configuration this library has no kernel for            */
 } dl_status;
 
 typedef enum dl_op { DL_GDN = 0, DL_KDA = 1, DL_RWKV6 = 2 } dl_op;
@@ -90,7 +90,7 @@ typedef struct dl_config {
     int32_t num_slots;       /* state slots (requests + branches), >= 1                 */
     int32_t num_heads;       /* H, >= 1                                                 */
     int32_t d_k;             /* key dimension: 64 or 128                                */
-    int32_t d_v;             /* value dimension: equal to d_k in this build             */
+    int32_t d_v;             /* value dimension: equal to d_k in this library           */
     int32_t merge_interval;  /* M in [1, 32]; 1 = eager (every step merges)             */
     int32_t out_bf16;        /* 1: o is bf16; 0: o is fp32                              */
     float scale;             /* output scale (1.0 for the decode workloads)             */
