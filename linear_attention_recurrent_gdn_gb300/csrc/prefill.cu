@@ -187,7 +187,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gdn_kernel(const __grid
     // Register tiles below are laid out so that each warp-wide load of a
     // padded row (stride DK + 4 floats, 4 banks apart) touches distinct banks.
     // ---- decay-weighted key-key (strictly lower) and query-key (lower) products:
-    //      a 2x2 block (tokens j = jg, jg + 16; i = ig, ig + 16) per thread
+    //      a 2x2 block (tokens j = jg, jg + 16; i = ig, ig + 16) per thread, whose
+    //      corner (jg, ig + 16) lies above the diagonal and is not computed
     {
       const int jg = tid >> 4, ig = tid & 15;
       float kk[2][2] = {{0.f, 0.f}, {0.f, 0.f}}, qk[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
@@ -197,11 +198,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gdn_kernel(const __grid
         const float4 kj0 = ld4(Kc + jg * L::SP + c), kj1 = ld4(Kc + (jg + 16) * L::SP + c);
         const float4 qj0 = ld4(Qc + jg * L::SP + c), qj1 = ld4(Qc + (jg + 16) * L::SP + c);
         kk[0][0] = dot4(kk[0][0], kj0, ki0);
-        kk[0][1] = dot4(kk[0][1], kj0, ki1);
         kk[1][0] = dot4(kk[1][0], kj1, ki0);
         kk[1][1] = dot4(kk[1][1], kj1, ki1);
         qk[0][0] = dot4(qk[0][0], qj0, ki0);
-        qk[0][1] = dot4(qk[0][1], qj0, ki1);
         qk[1][0] = dot4(qk[1][0], qj1, ki0);
         qk[1][1] = dot4(qk[1][1], qj1, ki1);
       }
