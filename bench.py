@@ -247,7 +247,8 @@ def run_reference(args):
     from linear_attention_recurrent_gdn_gb300 import inputs as gen
     # a prefill computes the decode recurrence over its context, and a checkpoint
     # belongs to the GDN serving batch: same oracle
-    w = WORKLOADS[PREFILL.get(args.workload, "gdn" if args.workload == "checkpoint" else args.workload)]
+    w = WORKLOADS[PREFILL.get(args.workload, "gdn" if args.workload in ("checkpoint", "readstate")
+                              else args.workload)]
     sample_sh = int(os.environ.get("DL_REF_SLOT_HEADS", "4096"))
     tokens = int(os.environ.get("DL_REF_TOKENS", "512"))
     oracle.build()
@@ -700,6 +701,72 @@ def run_checkpoint(args):
     return 0
 
 
+def run_readstate(args):
+    """Standalone Merge / ReadState kernel: one bench step materialises base +
+    replayed log of every slot of the GDN serving batch (8-entry logs) into a
+    caller buffer."""
+    import torch
+    rank, world, dist = dist_setup("cuda")
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    from linear_attention_recurrent_gdn_gb300 import build
+    if rank == 0:
+        build.build()
+    barrier(dist)
+    from linear_attention_recurrent_gdn_gb300 import deltalog as dl
+    from linear_attention_recurrent_gdn_gb300 import inputs as gen
+    w = WORKLOADS["gdn"]
+    op, B, H, d, M = w["op"], args.B or w["B"], w["H"], w["d"], w["M"]
+    n_log = 8
+    seed = w["seed"] + 7919 * rank
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    ctx = dl.DeltaLog(op, B, H, d, d, M, stream=stream.cuda_stream)
+    slots = list(range(B))
+    ctx.set_state(slots, gen.initial_state(B, H, d, d, seed, device=dev))
+    x = gen.make_inputs(op, n_log, B, H, d, d, seed, device=dev)
+    for t in range(n_log):
+        ctx.step(slots, x["q"][t], x["k"][t], x["v"][t], x["g"][t], x["beta"][t])
+    out = torch.empty((B, H, d, d), dtype=torch.float32, device=dev)
+
+    def one():
+        ctx.read_state(slots, out)
+
+    for _ in range(args.warmup):
+        one()
+    barrier(dist)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            one()
+        e1.record(stream)
+        e1.synchronize()
+    ms = reduce_max(dist, e0.elapsed_time(e1) / args.steps, dev)
+    row = 4 * d + 2 * d + 4                       # one log entry: u fp32, k bf16, Λ
+    moved = B * H * (2 * d * d * 4 + n_log * row)  # base read, state written, log rows read
+    gbs = moved / (ms / 1e3) / 1e9
+    peak, src = hbm_peak()
+    result = {"metric": "read-state GB/s", "value": gbs * world, "unit": "GB/s",
+              "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+              "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+              "data": "synthetic",
+              "config": {"workload": "base + replayed log of every slot into a buffer, " +
+                         w["desc"].split(",")[0] + ", M=%d, %d log entries" % (M, n_log),
+                         "slots": B, "H": H, "d_k": d, "d_v": d,
+                         "l2": "state larger than L2 (%.0f MB)" % (B * H * d * d * 4 / 1e6)},
+              "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                           "frac": gbs / peak, "traffic": None, "peak_source": src},
+              "clocks": clk.summary(), "gpu_launches": args.steps}
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    ctx.close()
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
 def run_fork(args):
     """Forked decode: bases are built once (setup, untimed); one bench step =
     fork every request into its branches (by index, no state copy) + the
@@ -816,7 +883,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="gdn",
-                    choices=sorted(WORKLOADS) + sorted(PREFILL) + ["checkpoint"])
+                    choices=sorted(WORKLOADS) + sorted(PREFILL) + ["checkpoint", "readstate"])
     ap.add_argument("--M", type=int, default=0)
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
@@ -838,6 +905,8 @@ def main():
         return run_prefill(args)
     if args.workload == "checkpoint":
         return run_checkpoint(args)
+    if args.workload == "readstate":
+        return run_readstate(args)
     return run_ours(args)
 
 

@@ -33,12 +33,21 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ Slot
   float* sD = U + n * BV;            // [DK]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
+  // This warp's 4 rows of the dense base, loaded first so that they land while
+  // the log rows are staged.
+  float t[4][VEC];
+#pragma unroll
+  for (int rr = 0; rr < 4; ++rr)
+    ldvec<VEC>(t[rr], a.Sbar + (((size_t)it.base * a.H + h) * DV + vt * BV + warp * 4 + rr) * DK +
+                          lane * VEC);
+
   if constexpr (PERKEY) {
     for (int i = tid; i < DK; i += 256) {
       const float Lc = n > 0 ? a.Llog[(lh * Mcap + n - 1) * DK + i] : 0.f;
       sD[i] = expf(Lc);
     }
-    for (int idx = tid; idx < n * DK; idx += 256) {
+#pragma unroll 4
+    for (int idx = tid; idx < n * DK; idx += 256) {   // unrolled: the loads go out together
       const int j = idx / DK, i = idx - j * DK;
       const float Lc = a.Llog[(lh * Mcap + n - 1) * DK + i];
       Kt[idx] = bf16f(a.klog[(lh * Mcap + j) * DK + i]) * expf(Lc - a.Llog[(lh * Mcap + j) * DK + i]);
@@ -46,11 +55,13 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ Slot
   } else {
     const float Lc = n > 0 ? a.Llog[lh * Mcap + n - 1] : 0.f;
     for (int i = tid; i < DK; i += 256) sD[i] = expf(Lc);
-    for (int idx = tid; idx < n * DK; idx += 256) {
+#pragma unroll 4
+    for (int idx = tid; idx < n * DK; idx += 256) {   // unrolled: the loads go out together
       const int j = idx / DK, i = idx - j * DK;
       Kt[idx] = bf16f(a.klog[(lh * Mcap + j) * DK + i]) * expf(Lc - a.Llog[lh * Mcap + j]);
     }
   }
+#pragma unroll 2
   for (int idx = tid; idx < n * BV; idx += 256) {
     const int j = idx / BV, r = idx - j * BV;
     const size_t src = (lh * Mcap + j) * DV + vt * BV + r;
@@ -61,20 +72,19 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ Slot
 
   float D[VEC];
   ldvec<VEC>(D, sD + lane * VEC);
-  for (int r = warp * 4; r < warp * 4 + 4; ++r) {
-    const int vrow = vt * BV + r;
-    float t[VEC];
-    ldvec<VEC>(t, a.Sbar + (((size_t)it.base * a.H + h) * DV + vrow) * DK + lane * VEC);
 #pragma unroll
-    for (int c = 0; c < VEC; ++c) t[c] *= D[c];
+  for (int rr = 0; rr < 4; ++rr) {
+    const int r = warp * 4 + rr, vrow = vt * BV + r;
+#pragma unroll
+    for (int c = 0; c < VEC; ++c) t[rr][c] *= D[c];
     for (int j = 0; j < n; ++j) {
       const float uj = U[j * BV + r];
 #pragma unroll
-      for (int c = 0; c < VEC; ++c) t[c] += uj * Kt[j * DK + lane * VEC + c];
+      for (int c = 0; c < VEC; ++c) t[rr][c] += uj * Kt[j * DK + lane * VEC + c];
     }
     float* dst = a.S_out ? a.S_out + (((size_t)row * a.H + h) * DV + vrow) * DK
                          : a.Sbar + (((size_t)it.slot * a.H + h) * DV + vrow) * DK;
-    stvec_cs<VEC>(dst + lane * VEC, t);
+    stvec_cs<VEC>(dst + lane * VEC, t[rr]);
   }
   if (!a.S_out && h == 0 && vt == 0 && tid == 0) {
     a.nlog[it.slot] = 0;
