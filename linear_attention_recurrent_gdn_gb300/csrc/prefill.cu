@@ -17,6 +17,10 @@
 //
 // One CTA (256 threads) per slot-head, looping over the chunks; S̄ stays in
 // shared memory (rows padded to avoid bank conflicts) and goes to HBM at the end.
+// The work is FP32 arithmetic.  Each thread keeps register tiles of the chunk's
+// contractions (rows rg + 32m against tokens tg + 8t or column quads), laid out
+// so that every warp-wide 16-byte shared-memory load touches distinct banks,
+// and the next chunk's inputs load into registers while the current one computes.
 //
 // The per-key ops (KDA, RWKV6) use the same algebra with a log-decay vector per
 // key channel: Λ_j = Σ_{i<=j} g_i inside the chunk and, for i <= j,
