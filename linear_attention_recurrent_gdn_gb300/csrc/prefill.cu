@@ -295,6 +295,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_gdn_kernel(const __grid
           const float4 s4 = ld4(Sb + (rg + 32 * m) * L::SP + 4 * tg + 32 * n4);
           acc[m][n4] = make_float4(eC * s4.x, eC * s4.y, eC * s4.z, eC * s4.w);
         }
+#pragma unroll 4
       for (int j = 0; j < Cc; ++j) {
         const float ew = Ew[j];
         float w[RPT];
@@ -649,6 +650,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_perkey_kernel(
           acc[m][n4] = make_float4(e4.x * s4.x, e4.y * s4.y, e4.z * s4.z, e4.w * s4.w);
         }
       }
+#pragma unroll 4
       for (int j = 0; j < Cc; ++j) {
         float w[RPT];
 #pragma unroll
