@@ -477,6 +477,7 @@ __device__ __forceinline__ bool consume_append(const StepArgs& a, const Layout& 
     const float* U = reinterpret_cast<const float*>(av.U);
     float x = (OP == GDN) ? cf[0] * A : A;
     float ob = (OP == GDN) ? cf[0] * B : B;
+#pragma unroll 4
     for (int j = 0; j < n; ++j) {
       const float uj = U[j * DV + col];
       x += cf[HDR + j] * uj;
@@ -495,6 +496,7 @@ __device__ __forceinline__ bool consume_append(const StepArgs& a, const Layout& 
   } else {
     const uint16_t* V = reinterpret_cast<const uint16_t*>(av.U);
     float o = A;
+#pragma unroll 4
     for (int j = 0; j < n; ++j) o += cf[HDR + j] * bf16f(V[j * DV + col]);
     o += cf[3] * bf16f(V[n * DV + col]);
     store_out(a, oidx, a.scale * o);
@@ -591,6 +593,7 @@ __device__ __forceinline__ void consume_rwkv6_pair(const StepArgs& a, const Layo
   const uint16_t* V = reinterpret_cast<const uint16_t*>(av.U);
   const int col0 = vt0 * BV + lane, col1 = col0 + BV;
   float o0 = A0, o1 = A1;
+#pragma unroll 4
   for (int j = 0; j < n; ++j) {
     const float c = cf[HDR + j];
     o0 += c * bf16f(V[j * DV + col0]);
