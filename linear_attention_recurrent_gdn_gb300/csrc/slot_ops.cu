@@ -14,32 +14,33 @@
 
 namespace dl {
 
-// One CTA per (row, head, value tile), 8 warps x 4 rows.  The logical state of
-// slot s with n log entries and cumulative log-decay Λ_{n-1} is
+// One CTA per (row, head): the slot-head's K̃ and value-side rows are staged
+// once, then each of the 8 warps takes DV/8 rows in batches of 4, loading the
+// next batch of the dense base while it finishes the current one.  The logical
+// state of slot s with n log entries and cumulative log-decay Λ_{n-1} is
 //   S = D ⊙ S̄[base] + Σ_{j<n} a_j K̃_j^T,  D = e^{Λ_{n-1}},  K̃_j = k_j ⊙ e^{Λ_{n-1} - Λ_j}
 // (scalar decay for GDN, per key channel for KDA and RWKV6).
 template <int OP, int DK, int DV>
 __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ SlotListArgs a) {
-  constexpr int VEC = DK / 32, NVT = DV / BV;
+  constexpr int VEC = DK / 32, RPW = DV / 8, NB = RPW / 4;   // rows per warp, batches of 4
   constexpr bool PERKEY = OP != GDN;
   extern __shared__ __align__(16) float sm[];
-  const int b = blockIdx.x;
-  const int vt = b % NVT, sh = b / NVT, h = sh % a.H, row = sh / a.H;
+  const int sh = blockIdx.x, h = sh % a.H, row = sh / a.H;
   const StepItem it = a.items[row];
   const int n = it.n, Mcap = a.Mcap;
   const size_t lh = (size_t)it.slot * a.H + h;
   float* Kt = sm;                    // [n][DK]
-  float* U = sm + n * DK;            // [n][BV]
-  float* sD = U + n * BV;            // [DK]
+  float* U = sm + n * DK;            // [n][DV]
+  float* sD = U + n * DV;            // [DK]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const float* base = a.Sbar + ((size_t)it.base * a.H + h) * DV * DK + lane * VEC;
+  float* dst = (a.S_out ? a.S_out + ((size_t)row * a.H + h) * DV * DK
+                        : a.Sbar + ((size_t)it.slot * a.H + h) * DV * DK) + lane * VEC;
 
-  // This warp's 4 rows of the dense base, loaded first so that they land while
-  // the log rows are staged.
-  float t[4][VEC];
+  // the first batch of this warp's rows loads while the log rows are staged
+  float t[4][VEC], tn[4][VEC];
 #pragma unroll
-  for (int rr = 0; rr < 4; ++rr)
-    ldvec<VEC>(t[rr], a.Sbar + (((size_t)it.base * a.H + h) * DV + vt * BV + warp * 4 + rr) * DK +
-                          lane * VEC);
+  for (int rr = 0; rr < 4; ++rr) ldvec<VEC>(t[rr], base + (size_t)(warp * RPW + rr) * DK);
 
   if constexpr (PERKEY) {
     for (int i = tid; i < DK; i += 256) {
@@ -61,10 +62,9 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ Slot
       Kt[idx] = bf16f(a.klog[(lh * Mcap + j) * DK + i]) * expf(Lc - a.Llog[lh * Mcap + j]);
     }
   }
-#pragma unroll 2
-  for (int idx = tid; idx < n * BV; idx += 256) {
-    const int j = idx / BV, r = idx - j * BV;
-    const size_t src = (lh * Mcap + j) * DV + vt * BV + r;
+#pragma unroll 4
+  for (int idx = tid; idx < n * DV; idx += 256) {
+    const size_t src = lh * Mcap * DV + idx;          // rows j of the slot-head, contiguous
     U[idx] = (OP == RWKV6) ? bf16f(static_cast<const uint16_t*>(a.alog)[src])
                            : static_cast<const float*>(a.alog)[src];
   }
@@ -72,21 +72,33 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ Slot
 
   float D[VEC];
   ldvec<VEC>(D, sD + lane * VEC);
+#pragma unroll 1
+  for (int b = 0; b < NB; ++b) {
+    if (b + 1 < NB) {
 #pragma unroll
-  for (int rr = 0; rr < 4; ++rr) {
-    const int r = warp * 4 + rr, vrow = vt * BV + r;
-#pragma unroll
-    for (int c = 0; c < VEC; ++c) t[rr][c] *= D[c];
-    for (int j = 0; j < n; ++j) {
-      const float uj = U[j * BV + r];
-#pragma unroll
-      for (int c = 0; c < VEC; ++c) t[rr][c] += uj * Kt[j * DK + lane * VEC + c];
+      for (int rr = 0; rr < 4; ++rr)
+        ldvec<VEC>(tn[rr], base + (size_t)(warp * RPW + (b + 1) * 4 + rr) * DK);
     }
-    float* dst = a.S_out ? a.S_out + (((size_t)row * a.H + h) * DV + vrow) * DK
-                         : a.Sbar + (((size_t)it.slot * a.H + h) * DV + vrow) * DK;
-    stvec_cs<VEC>(dst + lane * VEC, t[rr]);
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+      const int r = warp * RPW + b * 4 + rr;
+#pragma unroll
+      for (int c = 0; c < VEC; ++c) t[rr][c] *= D[c];
+      for (int j = 0; j < n; ++j) {
+        const float uj = U[j * DV + r];
+#pragma unroll
+        for (int c = 0; c < VEC; ++c) t[rr][c] += uj * Kt[j * DK + lane * VEC + c];
+      }
+      stvec_cs<VEC>(dst + (size_t)r * DK, t[rr]);
+    }
+    if (b + 1 < NB) {
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr)
+#pragma unroll
+        for (int c = 0; c < VEC; ++c) t[rr][c] = tn[rr][c];
+    }
   }
-  if (!a.S_out && h == 0 && vt == 0 && tid == 0) {
+  if (!a.S_out && h == 0 && tid == 0) {
     a.nlog[it.slot] = 0;
     a.base_of[it.slot] = it.slot;
   }
@@ -203,11 +215,10 @@ cudaError_t launch_checkpoint(int op, int dk, const CkptArgs& a, cudaStream_t s)
 
 template <int OP, int DK>
 static cudaError_t merge_dispatch(const SlotListArgs& a, cudaStream_t s) {
-  constexpr int NVT = DK / BV;
   int nmax = 0;
   for (int i = 0; i < a.rows; ++i) nmax = a.items[i].n > nmax ? a.items[i].n : nmax;
-  const size_t smem = ((size_t)nmax * DK + (size_t)nmax * BV + DK) * sizeof(float);
-  merge_kernel<OP, DK, DK><<<a.rows * a.H * NVT, 256, smem, s>>>(a);
+  const size_t smem = ((size_t)nmax * DK + (size_t)nmax * DK + DK) * sizeof(float);
+  merge_kernel<OP, DK, DK><<<a.rows * a.H, 256, smem, s>>>(a);
   return cudaGetLastError();
 }
 
