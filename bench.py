@@ -558,9 +558,9 @@ def prefill_flops(op, d, C=PREFILL_C):
     return 2 * fma
 
 
-def run_prefill(args):
-    """Chunked prefill: one bench step is one dl_prefill call that feeds all B
-    slots a T-token context (inputs resident in HBM)."""
+def gpu_setup():
+    """Rank, world, process group, device and stream of this process, after the
+    library is built (rank 0) and every rank has it."""
     import torch
     rank, world, dist = dist_setup("cuda")
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -569,25 +569,14 @@ def run_prefill(args):
     if rank == 0:
         build.build()
     barrier(dist)
-    from linear_attention_recurrent_gdn_gb300 import deltalog as dl
-    from linear_attention_recurrent_gdn_gb300 import inputs as gen
-    w = WORKLOADS[PREFILL[args.workload]]
-    op, B, H, d, M = w["op"], args.B or w["B"], w["H"], w["d"], w["M"]
-    T = args.tokens or w["tokens"]
-    seed = w["seed"] + 7919 * rank
-    dev = torch.device("cuda", local)
-    stream = torch.cuda.current_stream()
-    x = gen.make_inputs(op, T, B, H, d, d, seed, device=dev)
-    ctx = dl.DeltaLog(op, B, H, d, d, M, stream=stream.cuda_stream)
-    slots = list(range(B))
-    ctx.set_state(slots, gen.initial_state(B, H, d, d, seed, device=dev))
-    if op == 2:
-        ctx.set_bonus(gen.rwkv6_bonus(H, d, seed, device=dev))
-    out = torch.empty((T, B, H, d), dtype=torch.bfloat16, device=dev)
+    return rank, world, dist, local, torch.device("cuda", local), torch.cuda.current_stream()
 
-    def one():
-        ctx.prefill(slots, x["q"], x["k"], x["v"], x["g"], x["beta"], out=out)
 
+def timed_steps(one, args, dist, local, dev, stream):
+    """W untimed warm-up steps, then K steps between CUDA events on the launching
+    stream (barrier + synchronize before), with the clocks sampled meanwhile.
+    Returns (ms per step, max over ranks; clock summary)."""
+    import torch
     for _ in range(args.warmup):
         one()
     barrier(dist)
@@ -599,7 +588,32 @@ def run_prefill(args):
             one()
         e1.record(stream)
         e1.synchronize()
-    ms = reduce_max(dist, e0.elapsed_time(e1) / args.steps, dev)
+    return reduce_max(dist, e0.elapsed_time(e1) / args.steps, dev), clk.summary()
+
+
+def run_prefill(args):
+    """Chunked prefill: one bench step is one dl_prefill call that feeds all B
+    slots a T-token context (inputs resident in HBM)."""
+    import torch
+    rank, world, dist, local, dev, stream = gpu_setup()
+    from linear_attention_recurrent_gdn_gb300 import deltalog as dl
+    from linear_attention_recurrent_gdn_gb300 import inputs as gen
+    w = WORKLOADS[PREFILL[args.workload]]
+    op, B, H, d, M = w["op"], args.B or w["B"], w["H"], w["d"], w["M"]
+    T = args.tokens or w["tokens"]
+    seed = w["seed"] + 7919 * rank
+    x = gen.make_inputs(op, T, B, H, d, d, seed, device=dev)
+    ctx = dl.DeltaLog(op, B, H, d, d, M, stream=stream.cuda_stream)
+    slots = list(range(B))
+    ctx.set_state(slots, gen.initial_state(B, H, d, d, seed, device=dev))
+    if op == 2:
+        ctx.set_bonus(gen.rwkv6_bonus(H, d, seed, device=dev))
+    out = torch.empty((T, B, H, d), dtype=torch.bfloat16, device=dev)
+
+    def one():
+        ctx.prefill(slots, x["q"], x["k"], x["v"], x["g"], x["beta"], out=out)
+
+    ms, clocks = timed_steps(one, args, dist, local, dev, stream)
     units = B * H * T
     tflops = units * prefill_flops(op, d) / (ms / 1e3) / 1e12
     result = {"metric": "prefill tokens·heads/s", "value": units * world / (ms / 1e3),
@@ -616,7 +630,7 @@ def run_prefill(args):
                            "traffic": None, "peak_source": "derived: 152 SMs x 128 FP32 "
                            "lanes x 2 FLOP x 2.07 GHz",
                            "flops_per_token_head": prefill_flops(op, d)},
-              "clocks": clk.summary(), "gpu_launches": args.steps * ((B + 1023) // 1024)}
+              "clocks": clocks, "gpu_launches": args.steps * ((B + 1023) // 1024)}
     if rank == 0:
         print(json.dumps(result), flush=True)
     ctx.close()
@@ -639,20 +653,12 @@ def run_checkpoint(args):
     batch (its base, log rows and log length) into a device buffer and restores
     it.  Each slot holds an 8-entry log."""
     import torch
-    rank, world, dist = dist_setup("cuda")
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    from linear_attention_recurrent_gdn_gb300 import build
-    if rank == 0:
-        build.build()
-    barrier(dist)
+    rank, world, dist, local, dev, stream = gpu_setup()
     from linear_attention_recurrent_gdn_gb300 import deltalog as dl
     from linear_attention_recurrent_gdn_gb300 import inputs as gen
     w = WORKLOADS["gdn"]
     op, B, H, d, M = w["op"], args.B or w["B"], w["H"], w["d"], w["M"]
     seed = w["seed"] + 7919 * rank
-    dev = torch.device("cuda", local)
-    stream = torch.cuda.current_stream()
     ctx = dl.DeltaLog(op, B, H, d, d, M, stream=stream.cuda_stream)
     slots = list(range(B))
     ctx.set_state(slots, gen.initial_state(B, H, d, d, seed, device=dev))
@@ -666,18 +672,7 @@ def run_checkpoint(args):
         ctx.checkpoint_save(slots, buf)
         ctx.checkpoint_load(slots, buf)
 
-    for _ in range(args.warmup):
-        one()
-    barrier(dist)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
-        e0.record(stream)
-        for _ in range(args.steps):
-            one()
-        e1.record(stream)
-        e1.synchronize()
-    ms = reduce_max(dist, e0.elapsed_time(e1) / args.steps, dev)
+    ms, clocks = timed_steps(one, args, dist, local, dev, stream)
     moved = 4 * B * per          # save reads and writes a record's bytes, restore too
     gbs = moved / (ms / 1e3) / 1e9
     peak, src = hbm_peak()
@@ -691,7 +686,7 @@ def run_checkpoint(args):
                          "l2": "records larger than L2 (%.0f MB)" % (B * per / 1e6)},
               "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
                            "frac": gbs / peak, "traffic": None, "peak_source": src},
-              "clocks": clk.summary(),
+              "clocks": clocks,
               "gpu_launches": args.steps * 2 * ((B + 1023) // 1024)}
     if rank == 0:
         print(json.dumps(result), flush=True)
@@ -706,21 +701,13 @@ def run_readstate(args):
     replayed log of every slot of the GDN serving batch (8-entry logs) into a
     caller buffer."""
     import torch
-    rank, world, dist = dist_setup("cuda")
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    from linear_attention_recurrent_gdn_gb300 import build
-    if rank == 0:
-        build.build()
-    barrier(dist)
+    rank, world, dist, local, dev, stream = gpu_setup()
     from linear_attention_recurrent_gdn_gb300 import deltalog as dl
     from linear_attention_recurrent_gdn_gb300 import inputs as gen
     w = WORKLOADS["gdn"]
     op, B, H, d, M = w["op"], args.B or w["B"], w["H"], w["d"], w["M"]
     n_log = 8
     seed = w["seed"] + 7919 * rank
-    dev = torch.device("cuda", local)
-    stream = torch.cuda.current_stream()
     ctx = dl.DeltaLog(op, B, H, d, d, M, stream=stream.cuda_stream)
     slots = list(range(B))
     ctx.set_state(slots, gen.initial_state(B, H, d, d, seed, device=dev))
@@ -732,18 +719,7 @@ def run_readstate(args):
     def one():
         ctx.read_state(slots, out)
 
-    for _ in range(args.warmup):
-        one()
-    barrier(dist)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
-        e0.record(stream)
-        for _ in range(args.steps):
-            one()
-        e1.record(stream)
-        e1.synchronize()
-    ms = reduce_max(dist, e0.elapsed_time(e1) / args.steps, dev)
+    ms, clocks = timed_steps(one, args, dist, local, dev, stream)
     row = 4 * d + 2 * d + 4                       # one log entry: u fp32, k bf16, Λ
     moved = B * H * (2 * d * d * 4 + n_log * row)  # base read, state written, log rows read
     gbs = moved / (ms / 1e3) / 1e9
@@ -758,7 +734,7 @@ def run_readstate(args):
                          "l2": "state larger than L2 (%.0f MB)" % (B * H * d * d * 4 / 1e6)},
               "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
                            "frac": gbs / peak, "traffic": None, "peak_source": src},
-              "clocks": clk.summary(), "gpu_launches": args.steps}
+              "clocks": clocks, "gpu_launches": args.steps}
     if rank == 0:
         print(json.dumps(result), flush=True)
     ctx.close()
