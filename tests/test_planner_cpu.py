@@ -26,9 +26,10 @@ DRIVER = r"""
 #include <cstdio>
 #include "layout.h"
 // prep warps of the fused form, as the step launcher picks them
-static int prep_warps(int op, int dk, int G) {
+static int prep_warps(int op, int dk, int G, int M) {
   if (G / dl::tiles_per_stage(dk, G) == 1) return 0;
-  return op == 0 ? 1 : 2;
+  if (op == 0) return 1;
+  return M <= 16 ? 1 : 2;
 }
 int main() {
   const int optin = 232448, per_sm = 233472;
@@ -43,7 +44,7 @@ int main() {
                 const int dk = dks[di], G = whole ? dk / 32 : 1;
                 const dl::Layout L = dl::make_layout(op, M, dk, dk);
                 const int aux = kind == 0 ? L.aux_bytes : kind == 1 ? L.f_bytes : L.e_bytes;
-                const int npw = kind == 1 ? prep_warps(op, dk, G) : -1;
+                const int npw = kind == 1 ? prep_warps(op, dk, G, M) : -1;
                 const bool ml = kind == 1 && merge && M >= 8;
                 const dl::PipePlan p = dl::plan_pipeline(dk, aux, G, optin, per_sm, nullptr, npw,
                                                          regss[ri], ml);
@@ -116,15 +117,15 @@ def test_merge_launches_of_one_stage_d64_units_widen(plans):
 
 def test_shapes_of_the_three_workloads(plans):
     """The shapes the M = 16 decode workloads run with whole-slot-head units:
-    GDN and KDA (2,4,1) with one and two prep warps; RWKV6 append launches
-    (3,2,1) with two aux slots per consumer warp, its merge launches (2,4,1)."""
+    GDN and KDA (2,4,1) with one prep warp; RWKV6 append launches (3,2,1) with
+    two aux slots per consumer warp, its merge launches (2,4,1)."""
     def pick(op, dk, M, merge, regs=128):
         return next(p for p in plans if p["op"] == op and p["dk"] == dk and p["M"] == M
                     and p["G"] == dk // 32 and p["kind"] == 1 and p["merge"] == merge
                     and p["regs"] == regs)
     gdn, kda = pick(0, 128, 16, 0), pick(1, 128, 16, 0)
     assert (gdn["cps"], gdn["ncw"], gdn["ns"], gdn["npw"]) == (2, 4, 4, 1)
-    assert (kda["cps"], kda["ncw"], kda["ns"], kda["npw"]) == (2, 4, 4, 2)
+    assert (kda["cps"], kda["ncw"], kda["ns"], kda["npw"]) == (2, 4, 4, 1)
     rw, rwm = pick(2, 64, 16, 0), pick(2, 64, 16, 1)
     assert (rw["cps"], rw["ncw"], rw["ns"], rw["na"], rw["npw"]) == (3, 2, 2, 4, 0)
     assert (rwm["cps"], rwm["ncw"], rwm["ns"], rwm["npw"]) == (2, 4, 4, 0)
