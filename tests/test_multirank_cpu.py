@@ -36,9 +36,9 @@ def _worker(rank, world, port, num_requests, out):
 @pytest.mark.parametrize("num_requests", [64, 7])
 def test_two_gloo_ranks_shard_and_reduce(num_requests):
     world = 2
-    mgr = mp.Manager()
+    ctx = mp.get_context("spawn")     # no fork after threads (the manager too)
+    mgr = ctx.Manager()
     out = mgr.dict()
-    ctx = mp.get_context("spawn")
     port = _free_port()
     procs = [ctx.Process(target=_worker, args=(r, world, port, num_requests, out))
              for r in range(world)]
