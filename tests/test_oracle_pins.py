@@ -13,7 +13,9 @@ token, a wrong factor order) fails at least one of them:
              delta rule's overwrite), RWKV6 with w = 1 and no bonus
   P4         the base + log + merge-every-M model equals eager at every step,
              for every M in 1..T+1 (DeltaLog's claim that only the schedule
-             changes, not the function)
+             changes, not the function); forced merges at random tokens and
+             slots, of plain and of forked slots, keep it equal to eager, empty
+             the log and privatise the base (planted mistakes fail it)
   P5         fork by base index equals copy-then-run, and equals eager from
              the source's materialised state
   P6         the integer bookkeeping model on hand-written traces and invariants
@@ -240,6 +242,126 @@ def test_p4_base_plus_log_equals_eager_every_M(op):
         assert _rel(states, snaps) < 1e-12, M
         n, _ = model.meta()
         assert all(x == T % M for x in n), (M, n)
+
+
+def _check_forced_merges(model_cls, op, M, seed):
+    """Forced merges (DeltaLog page, "Methodology — Base + Log", merge phase,
+    taken early): after merging a slot, its materialised state is still eager's
+    state at that token, its log is empty and it owns its base; the outputs of
+    every later token still equal eager's.  Part A: plain slots.  Part B: a
+    source forked into two branches by base index; merging a branch must write
+    the branch's own storage and leave the source's base untouched."""
+    T, B, H, dk, dv = 12, 3, 2, 5, 4
+    r = np.random.default_rng(seed)
+    S0, q, k, v, g, extra = _tiny(op, T, B * H, dk, dv, seed=seed)
+    if op == oracle.RWKV6:
+        extra = np.tile(extra[:H], (B, 1))
+    o_ref, _, snaps = _eager(op, S0, q, k, v, g, extra, snap=list(range(T)))
+    slots = list(range(B))
+    model = model_cls(op, B, H, dk, dv, M, bonus=extra[:H] if op == oracle.RWKV6 else None)
+    model.set_state(slots, S0.reshape(B, H, dv, dk))
+    rs = lambda x, t: x[t].reshape((B, H) + x.shape[2:])
+    merged_any = False
+    for t in range(T):
+        beta = None if op == oracle.RWKV6 else extra[t].reshape(B, H)
+        o = model.step(slots, rs(q, t), rs(k, t), rs(v, t), rs(g, t), beta)
+        assert _rel(o.reshape(B * H, dv), o_ref[t]) < 1e-12, ("output", t)
+        if r.random() < 0.5:
+            sel = sorted(int(s) for s in r.choice(B, size=int(r.integers(1, B + 1)), replace=False))
+            model.merge(sel)
+            merged_any = True
+            n, base_of = model.meta()
+            for s in sel:
+                assert n[s] == 0 and base_of[s] == s and model.log[s] == [], ("bookkeeping", t, s)
+        state = model.read_state(slots).reshape(B * H, dv, dk)
+        assert _rel(state, snaps[t]) < 1e-12, ("state", t)
+    assert merged_any
+
+    # Part B: fork, then merge a branch before and between its own steps
+    Tctx, Tq = 5, 7
+    S0, q, k, v, g, extra = _tiny(op, Tctx + Tq, 3 * H, dk, dv, seed=seed + 1)
+    bonus = extra[:H] if op == oracle.RWKV6 else None
+    model = model_cls(op, 3, H, dk, dv, M, bonus=bonus)
+    model.set_state([0], S0.reshape(3, H, dv, dk)[:1])
+    row = lambda x, t, s: x[t].reshape((3, H) + x.shape[2:])[s:s + 1]
+    beta = lambda t, s: None if op == oracle.RWKV6 else extra[t].reshape(3, H)[s:s + 1]
+    for t in range(Tctx):
+        model.step([0], row(q, t, 0), row(k, t, 0), row(v, t, 0), row(g, t, 0), beta(t, 0))
+    src_state = model.read_state([0])[0].copy()
+    src_store = model.store[0].copy()
+    model.fork(0, [1, 2])
+    model.merge([1])                                   # privatise branch 1 before it steps
+    n, base_of = model.meta()
+    assert base_of[1] == 1 and n[1] == 0 and model.log[1] == [], "fork-merge bookkeeping"
+    assert np.array_equal(model.store[0], src_store), "source base changed by a branch merge"
+    assert _rel(model.read_state([1])[0], src_state) < 1e-12, "branch state after merge"
+    assert _rel(model.read_state([0])[0], src_state) < 1e-12, "source state after branch merge"
+    for s in (1, 2):
+        sel = lambda x: x[Tctx:].reshape((Tq, 3, H) + x.shape[2:])[:, s]
+        ex = bonus if op == oracle.RWKV6 else sel(extra)
+        o_e, _, snap_e = _eager(op, src_state, sel(q), sel(k), sel(v), sel(g), ex,
+                                snap=list(range(Tq)))
+        for j, t in enumerate(range(Tctx, Tctx + Tq)):
+            o = model.step([s], row(q, t, s), row(k, t, s), row(v, t, s), row(g, t, s), beta(t, s))
+            assert _rel(o[0], o_e[j]) < 1e-12, ("branch output", s, j)
+            if j % 3 == 1:
+                model.merge([s])
+                assert model.meta()[1][s] == s and model.log[s] == []
+            assert _rel(model.read_state([s])[0], snap_e[j]) < 1e-12, ("branch state", s, j)
+            assert np.array_equal(model.store[0], src_store), "source base changed"
+
+
+class _MergeKeepsLog(oracle.DeltaLogModel):
+    """Planted mistake: the forced merge writes the base but leaves the log."""
+
+    def merge(self, slots):
+        logs = {s: list(self.log[s]) for s in slots}
+        super().merge(slots)
+        for s in slots:
+            self.log[s] = logs[s]
+
+
+class _MergeStoresIntoReadBase(oracle.DeltaLogModel):
+    """Planted mistake: the merged state goes to the storage the slot read
+    (a fork source's base) instead of the slot's own."""
+
+    def merge(self, slots):
+        mats = [self._materialise(s, self.table.base_of[s], self._L_prev(s)) for s in slots]
+        targets = [self.table.base_of[s] for s in slots]
+        assert self.table.merge(list(slots)) == oracle.OK
+        for s, tgt, S in zip(slots, targets, mats):
+            self.store[tgt] = S
+            self.log[s] = []
+
+
+class _MergeDropsDecay(oracle.DeltaLogModel):
+    """Planted mistake: the materialisation forgets the base's decay D."""
+
+    def merge(self, slots):
+        mats = []
+        for s in slots:
+            L0 = self._L_prev(s)
+            S = self._materialise(s, self.table.base_of[s], L0)
+            Sb = self.store[self.table.base_of[s]]
+            D = np.exp(L0)[:, None, None] if self.op == oracle.GDN else np.exp(L0)[:, None, :]
+            mats.append(S - D * Sb + Sb)
+        assert self.table.merge(list(slots)) == oracle.OK
+        for s, S in zip(slots, mats):
+            self.store[s] = S
+            self.log[s] = []
+
+
+@pytest.mark.parametrize("op", [oracle.GDN, oracle.KDA, oracle.RWKV6])
+@pytest.mark.parametrize("M", [1, 2, 3, 5, 13])
+def test_p4_forced_merges_keep_eager(op, M):
+    _check_forced_merges(oracle.DeltaLogModel, op, M, seed=100 + 10 * op + M)
+
+
+@pytest.mark.parametrize("op", [oracle.GDN, oracle.KDA, oracle.RWKV6])
+@pytest.mark.parametrize("mutant", [_MergeKeepsLog, _MergeStoresIntoReadBase, _MergeDropsDecay])
+def test_p4_forced_merge_check_catches_planted_mistakes(op, mutant):
+    with pytest.raises(AssertionError):
+        _check_forced_merges(mutant, op, 5, seed=100 + 10 * op + 5)
 
 
 # ---------------------------------------------------------------- P5 ---------
