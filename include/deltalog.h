@@ -337,20 +337,38 @@ typedef struct dl_state_view {
  * floats; CB grows with M and, for KDA/RWKV6, with M * d_k); larger steps are
  * refused with DL_EINVAL — split them over several calls.  The scratch is one
  * array shared by every call and keeps the last call's contents: within a
- * call every coefficient used is written first, and the status word is
- * cleared at the start, but calls that overlap on the GPU race, so order
- * them on one stream.  The first call on a
- * device does a one-time set-up with that device current (it looks up the
- * scratch's device address and sets kernel shared-memory limits); make it
- * before any stream capture.  If errbuf != NULL it receives a one-line reason
+ * call every coefficient used is written first, but calls that overlap on
+ * the GPU race, so order them on one stream.  The first call on a device does
+ * a one-time set-up with that device current (it looks up the device
+ * addresses of the scratch and the status word, and sets kernel shared-memory
+ * limits); make it before any stream capture.  If errbuf != NULL it receives a one-line reason
  * for a non-DL_OK status (at most errlen bytes, NUL-terminated).  The step
  * always runs as two kernels (the scratch holds the coefficient blocks that
- * pass between them); cfg->staging is not used. */
+ * pass between them); cfg->staging is not used.
+ * Checked on the host before anything is enqueued (DL_EINVAL, nothing runs):
+ * the plan's ids and log lengths are in range and its merge flags agree with
+ * them, no slot appears twice, and no row reads the base of a slot that
+ * merges in the same call (dl_table_step never plans that: a fork source is
+ * frozen); q, k, v (and g for KDA / RWKV6), Sbar, alog, klog, the per-key
+ * Llog and bonus are 16-byte aligned, the other pointers aligned to their
+ * element size.
+ * Device-side errors (a bounded wait in a kernel gave up) are recorded in one
+ * static status word per device, which starts at zero and keeps the first
+ * code until dl_noalloc_sync reads it. */
 dl_status dl_step_noalloc(const dl_config *cfg, const dl_state_view *st,
                           const int32_t *plan, int32_t n,
                           const void *q, const void *k, const void *v,
                           const float *g, const float *beta, void *o,
                           void *stream, char *errbuf, int32_t errlen);
+
+/* Companion of dl_step_noalloc (no paper counterpart either; allocates
+ * nothing): synchronise `stream`, then read the current device's static status
+ * word.  DL_OK if no dl_step_noalloc call since the last dl_noalloc_sync
+ * reported a device-side error.  Otherwise DL_EDEVICE, *device_code (if not
+ * NULL) receives the code, errbuf a one-line reason, and the word is cleared:
+ * the outputs and state written by the calls since the last dl_noalloc_sync
+ * must not be trusted.  A CUDA error returns DL_ECUDA. */
+dl_status dl_noalloc_sync(void *stream, int32_t *device_code, char *errbuf, int32_t errlen);
 
 /* Synchronise the stream and report any CUDA or device-side error. */
 dl_status dl_sync(dl_ctx *ctx);

@@ -75,6 +75,12 @@ struct dl_ctx {
   std::unique_ptr<dl::CkptArgs> ckpt_args;
   std::string err = "no error";
   dl_status sticky = DL_OK;
+  // Bounded waits give up after wait_ns.  Tests may shorten it
+  // (DL_TEST_WAIT_MS at dl_create) and set test_stall (DL_TEST_STALL=1), which
+  // makes one consumer warp of each launch wait on a barrier nothing arrives
+  // on, so that the device-side error path runs without any fault.
+  unsigned long long wait_ns = dl::WAIT_LIMIT_NS;
+  int test_stall = 0;
   bool timing = false;
   std::vector<TimedPair> timed[NKIND];
   double timed_ms[NKIND] = {0, 0, 0, 0};
@@ -263,6 +269,8 @@ void fill_step_args(dl_ctx* c, dl::StepArgs& a, int32_t row0, int32_t rows, cons
   a.out_bf16 = f.out_bf16;
   a.scale = f.scale;
   a.aux_bytes = c->L.aux_bytes;
+  a.wait_ns = c->wait_ns;
+  a.test_stall = c->test_stall;
   a.plan_dev = c->dev_plan ? c->dev_plan + row0 : nullptr;   // ragged windows only
   a.rows_dev = c->dev_rows;
   for (int32_t i = 0; i < rows; ++i) {
@@ -287,7 +295,7 @@ void unit_shape(const dl_ctx* c, dl::StepArgs& a) {
 }
 
 dl_status run_step(dl_ctx* c, const int32_t* slots, int32_t n, const void* q, const void* k,
-                   const void* v, const float* g, const float* beta, void* o, bool eager) {
+                   const void* v, const float* g, const float* beta, void* o, bool eager_call) {
   (void)slots;
   const dl_config& f = c->cfg;
   dl::StepArgs& a = *c->step_args;
@@ -295,6 +303,7 @@ dl_status run_step(dl_ctx* c, const int32_t* slots, int32_t n, const void* q, co
     const int32_t rows = (n - row0) < dl::MAX_ROWS ? (n - row0) : dl::MAX_ROWS;
     fill_step_args(c, a, row0, rows, q, k, v, g, beta, o);
     unit_shape(c, a);
+    const bool eager = eager_call;
     const bool fused = !eager && f.staging == DL_STAGE_FUSED;
     // a launch where every row merges a window of M >= 8 gets the merge shape
     // (shorter rank-M updates are cheap enough that the append shape wins)
@@ -382,6 +391,11 @@ dl_status dl_create(const dl_config* cfg, void* stream, dl_ctx** out) {
   c->list_args.reset(new (std::nothrow) dl::SlotListArgs());
   c->ckpt_args.reset(new (std::nothrow) dl::CkptArgs());
   if (const char* s = getenv("DL_TEST_FAIL_ALLOC")) g_fail_countdown = atoi(s);
+  if (const char* s = getenv("DL_TEST_WAIT_MS")) {
+    const long ms = atol(s);
+    if (ms > 0 && ms < 2000) c->wait_ns = (unsigned long long)ms * 1000000ull;
+  }
+  if (const char* s = getenv("DL_TEST_STALL")) c->test_stall = atoi(s) == 1 ? 1 : 0;
   dl_status rc = DL_OK;
   do {
     if (!c->step_args || !c->list_args || !c->ckpt_args) { rc = DL_ENOMEM; break; }
@@ -1166,7 +1180,8 @@ dl_status dl_sync(dl_ctx* c) {
   DL_CUDA(cudaGetLastError(), "pending CUDA error");
   int32_t st = 0;
   DL_CUDA(cudaMemcpy(&st, c->status, 4, cudaMemcpyDeviceToHost), "status read");
-  if (st != 0) return set_err(c, DL_EDEVICE, "kernel reported device status %d (bounded wait gave up)", st);
+  if (st != 0)
+    return set_err(c, DL_EDEVICE, "kernel reported device status %d (%s)", st, dl::device_status_str(st));
   return DL_OK;
 }
 

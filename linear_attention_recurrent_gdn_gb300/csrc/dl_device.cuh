@@ -27,7 +27,20 @@ constexpr int32_t DEV_TIMEOUT_TILE = 1;
 constexpr int32_t DEV_TIMEOUT_AUX = 2;
 constexpr int32_t DEV_TIMEOUT_EMPTY = 3;
 constexpr int32_t DEV_BAD_ITEM = 4;
-constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;  // 2 s
+constexpr int32_t DEV_TEST_STALL = 5;   // the test-only stall below ran out (nothing else sets it)
+constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;  // 2 s (default per-launch limit)
+
+// One-line meaning of a device status code (host side).
+inline const char* device_status_str(int32_t code) {
+  switch (code) {
+    case DEV_TIMEOUT_TILE: return "a wait for a state tile gave up";
+    case DEV_TIMEOUT_AUX: return "a wait for a unit's inputs or coefficients gave up";
+    case DEV_TIMEOUT_EMPTY: return "a wait for a stage or input slot to be released gave up";
+    case DEV_BAD_ITEM: return "a plan row was out of range";
+    case DEV_TEST_STALL: return "the test-only stall's bounded wait gave up";
+    default: return "unknown device status";
+  }
+}
 
 struct StepItem {
   int32_t slot;   // slot stepped (log owner, and the storage a merge writes)
@@ -64,6 +77,14 @@ struct StepArgs {
   int32_t aux_bytes;     // bytes of one aux slot
   int32_t out_bf16;
   float scale;
+  // How long a bounded wait spins before it records an error and gives up
+  // (WAIT_LIMIT_NS unless a test asks for less).
+  unsigned long long wait_ns;
+  // Test only (0 in normal use): the first consumer warp of CTA 0 also waits
+  // (for wait_ns / 2) on a barrier that nothing arrives on, so that its
+  // bounded wait runs out, records DEV_TEST_STALL and the kernel takes its
+  // error exit.
+  int32_t test_stall;
   // Device-resident plan (ragged decode windows): when set, the launch reads
   // its rows from plan_dev and processes min(*rows_dev, rows) of them; `rows`
   // is then the capacity the grid was sized for.  Otherwise the rows are
@@ -150,17 +171,18 @@ __device__ __forceinline__ unsigned long long globaltimer() {
 }
 
 // Wait until the phase with the given parity has completed.  Gives up after
-// WAIT_LIMIT_NS, or early once another warp has recorded an error, and then
+// limit_ns, or early once another warp has recorded an error, and then
 // returns false (after recording `code` if nobody did before).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* status,
-                                          int32_t code) {
+                                          int32_t code,
+                                          unsigned long long limit_ns = WAIT_LIMIT_NS) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*reinterpret_cast<volatile int32_t*>(status) != 0) return false;
-      if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+      if (globaltimer() - t0 > limit_ns) {
         atomicCAS(status, 0, code);
         return false;
       }

@@ -60,6 +60,9 @@ struct Bars {
   __device__ uint32_t afull(int x) const { return b0 + 8u * (2 * ns + x); }
   __device__ uint32_t aempty(int x) const { return b0 + 8u * (2 * ns + na + x); }
   __device__ uint32_t cready(int x) const { return b0 + 8u * (2 * ns + 2 * na + x); }
+  // The last barrier of the area (ns, na <= 24 use at most 120 of its 128):
+  // initialised and never arrived on (the test-only stall waits on it).
+  __device__ uint32_t never() const { return b0 + (uint32_t)BAR_BYTES - 8u; }
 };
 
 // Stage ownership: tile i (CTA-local order) belongs to consumer warp i % ncw,
@@ -722,6 +725,7 @@ __global__ void __maxnreg__(128) pipe_kernel(const __grid_constant__ StepArgs a)
       mbar_init(bars.aempty(x), IPU);
       mbar_init(bars.cready(x), 1);   // fused form: the prep warp's arrival
     }
+    mbar_init(bars.never(), 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -790,7 +794,7 @@ __global__ void __maxnreg__(128) pipe_kernel(const __grid_constant__ StepArgs a)
       if (kt == ka) {
         const int x = ax_x;
         if (!__all_sync(0xffffffffu,
-                        mbar_wait(bars.aempty(x), ax_par ^ 1u, a.status, DEV_TIMEOUT_EMPTY))) {
+                        mbar_wait(bars.aempty(x), ax_par ^ 1u, a.status, DEV_TIMEOUT_EMPTY, a.wait_ns))) {
           ok = false;
           break;
         }
@@ -825,7 +829,7 @@ __global__ void __maxnreg__(128) pipe_kernel(const __grid_constant__ StepArgs a)
         }
       }
       const int s = w * R + r;   // = stage_of(ti, R, NCWr)
-      if (!__all_sync(0xffffffffu, mbar_wait(bars.empty(s), par ^ 1u, a.status, DEV_TIMEOUT_EMPTY))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(bars.empty(s), par ^ 1u, a.status, DEV_TIMEOUT_EMPTY, a.wait_ns))) {
         ok = false;
         break;
       }
@@ -882,7 +886,7 @@ __global__ void __maxnreg__(128) pipe_kernel(const __grid_constant__ StepArgs a)
     for (int kk = 0; kk < my_units; ++kk, walk.next()) {
       const int x = kk % NA;
       if (x % NPW != pw) continue;
-      if (!__all_sync(0xffffffffu, mbar_wait(bars.afull(x), (kk / NA) & 1, a.status, DEV_TIMEOUT_AUX)))
+      if (!__all_sync(0xffffffffu, mbar_wait(bars.afull(x), (kk / NA) & 1, a.status, DEV_TIMEOUT_AUX, a.wait_ns)))
         break;
       const UnitPos p = walk.p;
       unsigned char* ax = auxm + (size_t)x * aux_bytes;
@@ -940,19 +944,24 @@ __global__ void __maxnreg__(128) pipe_kernel(const __grid_constant__ StepArgs a)
       // seen each earlier phase of its barrier itself, so it can wait for the
       // unit's inputs first and compute the coefficients while the tile is
       // still landing.
-      ok = mbar_wait(bars.afull(x), xpar, a.status, DEV_TIMEOUT_AUX);
+      ok = mbar_wait(bars.afull(x), xpar, a.status, DEV_TIMEOUT_AUX, a.wait_ns);
       if (!__all_sync(0xffffffffu, ok)) break;
       if constexpr (MODE == FUSED) prep_unit<OP, DK, DV, NE>(a, Lay, p, ax, lane);
       __syncwarp();
-      ok = mbar_wait(bars.full(s), spar, a.status, DEV_TIMEOUT_TILE);
+      ok = mbar_wait(bars.full(s), spar, a.status, DEV_TIMEOUT_TILE, a.wait_ns);
     } else {
       // The tile first: it is issued after its unit's aux copies, so once it
       // has landed the aux barrier is in this unit's phase and the parity test
       // below is unambiguous.
-      ok = mbar_wait(bars.full(s), spar, a.status, DEV_TIMEOUT_TILE);
+      ok = mbar_wait(bars.full(s), spar, a.status, DEV_TIMEOUT_TILE, a.wait_ns);
       ok = ok && mbar_wait(MODE == FUSED ? bars.cready(x) : bars.afull(x), xpar, a.status,
-                           DEV_TIMEOUT_AUX);
+                           DEV_TIMEOUT_AUX, a.wait_ns);
     }
+    // Test only: wait on a barrier that nothing arrives on, with half the
+    // limit, so that this wait runs out before the waits that depend on this
+    // warp (the producer's, for the stage it holds) and its code is recorded.
+    if (a.test_stall && blockIdx.x == 0 && i == 0)
+      ok = ok && mbar_wait(bars.never(), 0u, a.status, DEV_TEST_STALL, a.wait_ns / 2);
     if (!__all_sync(0xffffffffu, ok)) break;
     bool released = false;
     bool paired = false;

@@ -17,6 +17,11 @@ from . import build as _build
 
 GDN, KDA, RWKV6 = 0, 1, 2
 OK, EINVAL, ENOMEM, ECUDA, EBUSY, EDEVICE, EUNSUPPORTED = range(7)
+# Codes a kernel writes into a device status word (the library reports them as
+# EDEVICE): a bounded wait for a state tile, for a unit's inputs or
+# coefficients, or for a stage / input slot to be released gave up; a plan row
+# was out of range; the test-only stall ran out.
+DEV_TIMEOUT_TILE, DEV_TIMEOUT_AUX, DEV_TIMEOUT_EMPTY, DEV_BAD_ITEM, DEV_TEST_STALL = 1, 2, 3, 4, 5
 STATUS_NAMES = ["DL_OK", "DL_EINVAL", "DL_ENOMEM", "DL_ECUDA", "DL_EBUSY", "DL_EDEVICE",
                 "DL_EUNSUPPORTED"]
 LIB_PATH = _build.LIB
@@ -31,7 +36,7 @@ EXPORTS = [
     "dl_abi_version", "dl_checkpoint_bytes", "dl_checkpoint_save", "dl_checkpoint_load",
     "dl_window_create", "dl_window_launch", "dl_window_destroy", "dl_window_create_ragged",
     "dl_window_launch_ragged", "dl_prefill",
-    "dl_step_noalloc",
+    "dl_step_noalloc", "dl_noalloc_sync",
 ]
 
 
@@ -103,6 +108,7 @@ def _load():
         "dl_prefill": ([P, P, I32, I32, P, P, P, P, P, P], I32),
         "dl_step_noalloc": ([ctypes.POINTER(dl_config), ctypes.POINTER(dl_state_view), P, I32,
                              P, P, P, P, P, P, P, ctypes.c_char_p, I32], I32),
+        "dl_noalloc_sync": ([P, ctypes.POINTER(I32), ctypes.c_char_p, I32], I32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -178,7 +184,10 @@ def dl_table_get(t, num_slots):
 
 
 def _ptr(t):
-    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+    """Device address of a tensor (an int passes through as an address)."""
+    if t is None:
+        return ctypes.c_void_p(0)
+    return ctypes.c_void_p(t if isinstance(t, int) else t.data_ptr())
 
 
 def dl_create(cfg, stream=None):
@@ -329,8 +338,7 @@ def dl_step_noalloc(cfg, state, plan, q, k, v, g, beta, o, stream=None):
     `state` maps dl_state_view field names to torch tensors (bonus may be None);
     `plan` is the [n, 4] int32 array from dl_table_step."""
     pl = np.ascontiguousarray(np.asarray(plan, dtype=np.int32).reshape(-1, 4))
-    sv = dl_state_view(*[None if state.get(f) is None else state[f].data_ptr()
-                         for f, _ in dl_state_view._fields_])
+    sv = dl_state_view(*[_ptr(state.get(f)).value for f, _ in dl_state_view._fields_])
     err = ctypes.create_string_buffer(256)
     st = ctypes.c_void_p(0 if stream is None else int(stream))
     rc = _lib.dl_step_noalloc(ctypes.byref(cfg), ctypes.byref(sv),
@@ -338,6 +346,17 @@ def dl_step_noalloc(cfg, state, plan, q, k, v, g, beta, o, stream=None):
                               _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(o), st, err, 256)
     if rc != OK:
         raise DeltaLogError(rc, err.value.decode())
+
+
+def dl_noalloc_sync(stream=None):
+    """Synchronise the stream and read the static device status word of the
+    allocation-free step.  Returns (status, device code, message); the word is
+    cleared when it held an error."""
+    err = ctypes.create_string_buffer(256)
+    code = ctypes.c_int32(0)
+    st = ctypes.c_void_p(0 if stream is None else int(stream))
+    rc = _lib.dl_noalloc_sync(st, ctypes.byref(code), err, 256)
+    return int(rc), int(code.value), err.value.decode()
 
 
 def dl_last_error(ctx):
