@@ -32,6 +32,8 @@ sys.path.insert(0, ROOT)
 
 WORKLOADS = {
     # name: op, B, H, d, tokens, M (headline), seed
+    "gdn_small": dict(op=0, B=1, H=4, d=64, tokens=64, M=8, seed=1000,
+                      desc="GDN decode B=1 H=4 d_k=d_v=64 fp32 state, 64 tokens"),
     "gdn": dict(op=0, B=256, H=32, d=128, tokens=512, M=16, seed=1001,
                 desc="GDN decode B=256 H=32 d_k=d_v=128 fp32 state, 512 tokens"),
     "kda": dict(op=1, B=128, H=32, d=128, tokens=512, M=16, seed=1002,
@@ -177,6 +179,10 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            t0 = time.time()
+            while not self.rows and time.time() - t0 < 3.0:   # first sample before timing starts
+                time.sleep(0.01)
+            self.rows.clear()
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
@@ -235,6 +241,56 @@ def barrier(dist):
         dist.barrier()
 
 
+# ------------------------------------------------------------- configs -------
+def decode_loop(w, M, args, eager=False):
+    """How the decode loop runs: CUDA graphs of M tokens unless --no-graph, the
+    eager kernel, or a token count that is not a whole number of windows."""
+    graphs = not (args.no_graph or eager or M == 1 or w["tokens"] % M)
+    return "CUDA graphs, one per M tokens (dl_window)" if graphs else "dl_step per token"
+
+
+def decode_config(w, M, args, world, eager=False):
+    """The `config` object of a decode line; both arms print the same one."""
+    B, H, d = w["B"], w["H"], w["d"]
+    return {"workload": w["desc"] + (", eager dense step" if eager else ", merge interval M=%d" % M),
+            "op": ("gdn", "kda", "rwkv6")[w["op"]], "B": B, "H": H, "d_k": d, "d_v": d,
+            "tokens": w["tokens"], "M": M, "staging": args.staging,
+            "loop": decode_loop(w, M, args, eager),
+            "inputs": "bf16 q/k/v, fp32 g/beta, bf16 o",
+            "l2": l2_note(w),
+            "parallelism": "replicas/batch shards x%d" % world}
+
+
+def l2_note(w):
+    """How the timed region relates to L2 (129 MB on GB300): no flush between
+    timed runs; the per-token inputs of one run are read once each."""
+    B, H, d, T = w["B"], w["H"], w["d"], w["tokens"]
+    state = B * H * d * d * 4
+    per_tok = B * H * (3 * d * 2 + (d * 4 if w["op"] else 4) + (4 if w["op"] != 2 else 0))
+    inputs = per_tok * T
+    text = "no L2 flush; per-token inputs %.1f MB a run%s; fp32 state %.1f MB per rank" % (
+        inputs / 1e6, " (larger than L2)" if inputs > 129e6 else "", state / 1e6)
+    if state > 129e6:
+        return "inputs larger than L2: " + text + " (larger than L2)"
+    return text + " (fits in L2 and is re-read every token, as decoding does)"
+
+
+def fork_plan(w, seed):
+    """Branch lengths U{16..256} of the fork workload (uniform integers, seeded)."""
+    import numpy as np
+    return np.random.default_rng(seed).integers(16, 257, size=w["requests"] * w["branches"])
+
+
+def fork_config(w, args, lens):
+    return {"workload": w["desc"], "op": "gdn", "requests": w["requests"],
+            "branches": w["branches"], "H": w["H"], "d_k": w["d"], "d_v": w["d"], "M": w["M"],
+            "ctx_tokens": w["ctx_tokens"], "branch_tokens": int(lens.sum()),
+            "staging": args.staging,
+            "loop": ("dl_step per token" if args.no_graph else
+                     "ragged CUDA graphs, one per M tokens (dl_window_*_ragged)"),
+            "l2": "inputs larger than L2 (576 slots x 1 MiB state)"}
+
+
 # ------------------------------------------------------------- reference -----
 def run_reference(args):
     """Reference arm: the fp64 oracle (C, OpenMP) on the host cores, timed on a
@@ -253,14 +309,18 @@ def run_reference(args):
     tokens = int(os.environ.get("DL_REF_TOKENS", "512"))
     oracle.build()
     res = cpu_baseline(w, sample_sh, tokens, args.steps, args.warmup)
+    if args.workload == "fork":
+        config = fork_config(w, args, fork_plan(w, w["seed"]))
+    elif args.workload in WORKLOADS:
+        config = decode_config(w, 1 if args.eager else (args.M or w["M"]), args, 1, args.eager)
+    else:   # prefill, checkpoint and read-state lines: the decode workload they belong to
+        config = {"workload": args.workload + " of " + w["desc"]}
     out = {"metric": METRIC, "value": res["value"], "unit": "tokens·heads/s", "n_gpus": 0,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic", "impl": "reference",
-           "config": {"workload": w["desc"] + ", merge interval M=%d" % (args.M or w["M"]),
-                      "op": gen.OP_NAMES[w["op"]], "B": w["B"], "H": w["H"], "d_k": w["d"],
-                      "d_v": w["d"], "tokens": w["tokens"], "M": args.M or w["M"],
-                      "implementation": "fp64 eager oracle (C, OpenMP) on a bounded sample"},
+           "implementation": "fp64 eager oracle (C, OpenMP) on a bounded sample of the workload",
+           "config": config,
            "cpu_baseline": {"value": res["value"], "unit": "tokens·heads/s",
                             "cores": res["cores"], "kind": "oracle", "sample": res["sample"]},
            "e2e": {"value": res["value"], "unit": "tokens·heads/s", "h2d_bytes_per_step": 0,
@@ -305,6 +365,83 @@ def cpu_baseline(w, sample_sh, tokens, steps=1, warmup=0):
 
 
 # ------------------------------------------------------------------ ours -----
+def roofline_window_bytes(op, d, M, T, slot_heads):
+    """Algorithmic bytes per launch of the fused kernel, averaged over the T
+    tokens of a decode run (token t has log length t mod M), and the writes."""
+    tot = sum(fused_bytes(op, d, M, t % M)[0] for t in range(T)) * slot_heads / T
+    wr = sum(fused_bytes(op, d, M, t % M)[1] for t in range(T)) * slot_heads / T
+    return tot, wr
+
+
+def measure_decode(w, args, dist, world, rank, local, dev, stream):
+    """One decode workload at its merge interval, in its own timed region:
+    W warm-up runs, then K runs of all its tokens (CUDA graphs of M tokens when
+    the token count allows), inputs resident in HBM.  Returns the workload's
+    entry: throughput, roofline of the fused kernel (one launch per token, so
+    the launch time is the token time), algorithmic write cut against the eager
+    kernel, clocks sampled during its own timed region."""
+    import torch
+    from linear_attention_recurrent_gdn_gb300 import deltalog as dl
+    from linear_attention_recurrent_gdn_gb300 import inputs as gen
+    op, B, H, d, T, M = w["op"], w["B"], w["H"], w["d"], w["tokens"], w["M"]
+    seed = w["seed"] + 7919 * rank
+    x = gen.make_inputs(op, T, B, H, d, d, seed, device=dev)
+    out = torch.empty((T, B, H, d), dtype=torch.bfloat16, device=dev)
+    slots = list(range(B))
+    c = dl.DeltaLog(op, B, H, d, d, M, out_bf16=True, stream=stream.cuda_stream,
+                    staging=dl.STAGE_FUSED if args.staging == "fused" else dl.STAGE_KERNELS)
+    c.set_state(slots, gen.initial_state(B, H, d, d, seed, device=dev))
+    if op == 2:
+        c.set_bonus(gen.rwkv6_bonus(H, d, seed, device=dev))
+    graphs = decode_loop(w, M, args).startswith("CUDA graphs")
+    sl = lambda key, j: x[key][j * M:(j + 1) * M] if x[key] is not None else None
+    wins = ([c.window(slots, sl("q", j), sl("k", j), sl("v", j), sl("g", j), sl("beta", j),
+                      out[j * M:(j + 1) * M]) for j in range(T // M)] if graphs else None)
+
+    def one():
+        if wins:
+            for win in wins:
+                win.launch()
+            return
+        for t in range(T):
+            c.step(slots, x["q"][t], x["k"][t], x["v"][t], x["g"][t],
+                   x["beta"][t] if x["beta"] is not None else None, out[t])
+
+    ms, clocks = timed_steps(one, args, dist, local, dev, stream)
+    for win in wins or []:
+        win.close()
+    c.close()
+    fused = args.staging == "fused"
+    sh = B * H
+    bpl, wpl = roofline_window_bytes(op, d, M, T, sh)
+    ew = eager_bytes(op, d)[1] * sh
+    ms_tok = ms / T
+    gbs = bpl / (ms_tok * 1e-3) / 1e9
+    peak, src = hbm_peak()
+    latency_bound = sh * d * d * 4 < (4 << 20)
+    entry = {"value": sh * T * world / (ms / 1e3), "unit": "tokens·heads/s", "ms_per_step": ms,
+             "us_per_token": ms_tok * 1e3, "config": decode_config(w, M, args, world),
+             "roofline": {"bound": "latency" if latency_bound else "hbm", "achieved": gbs,
+                          "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                          "traffic": measured_traffic("%s_%s_b%d_h%d_d%d_m%d" % (
+                              "append_decode_fused" if fused else "append_decode",
+                              ("gdn", "kda", "rwkv6")[op], B, H, d, M)),
+                          "peak_source": src, "bytes_per_launch": bpl, "ms_per_launch": ms_tok,
+                          "kernel": "AppendDecode (ReplayPrep fused)" if fused else "AppendDecode",
+                          "timing": ("token time in the graph-captured decode loop" if graphs
+                                     else "token time, one dl_step call per token")},
+             "write_bytes_per_token": {"deltalog": wpl, "eager": ew},
+             "write_cut_vs_eager": ew / wpl,
+             "clocks": clocks,
+             "gpu_launches": (1 if fused else 2) * T * args.steps * clocks.get("reps", 1)}
+    if latency_bound:
+        entry["note"] = ("%d KiB of state: launch latency, not HBM, bounds a token; the "
+                         "fraction is reported for completeness" % (sh * d * d * 4 >> 10))
+    del x, out
+    torch.cuda.empty_cache()
+    return entry
+
+
 def run_ours(args):
     import torch
     if not torch.cuda.is_available():
@@ -364,7 +501,7 @@ def run_ours(args):
 
     def make_windows(c, m):
         """The decode loop as CUDA graphs: one captured window per M tokens."""
-        if args.no_graph or T % m:
+        if args.no_graph or T % m or m == 1:   # a one-token window gains nothing from a graph
             return None
         sl = lambda key, j: x[key][j * m:(j + 1) * m] if x[key] is not None else None
         return [c.window(slots, sl("q", j), sl("k", j), sl("v", j), sl("g", j), sl("beta", j),
@@ -445,15 +582,7 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": w["desc"] + (", eager dense step" if args.eager
-                                            else ", merge interval M=%d" % M),
-                   "op": gen.OP_NAMES[op], "B": B, "H": H, "d_k": d, "d_v": d, "tokens": T,
-                   "M": M, "staging": args.staging,
-                   "loop": "CUDA graphs, one per M tokens (dl_window)" if wins else "dl_step per token",
-                   "inputs": "bf16 q/k/v, fp32 g/beta, bf16 o",
-                   "l2": "inputs larger than L2 (fp32 state %d MiB per rank)"
-                         % (B * H * d * d * 4 >> 20),
-                   "parallelism": "replicas/batch shards x%d" % world},
+        "config": decode_config(w, M, args, world, args.eager),
         "gpu_launches": launches,
         "clocks": clk.summary(),
         "roofline": {"bound": "hbm", "achieved": ad_gbs, "peak": peak, "unit": "GB/s",
@@ -497,6 +626,18 @@ def run_ours(args):
         result["write_cut_vs_eager"] = ew * B * H / result["write_bytes_per_token"]["deltalog"]
         result["note_writes"] = "algorithmic bytes; DRAM-measured writes are in profiles/"
 
+    # ---- the other decode workloads, each in its own timed region
+    if (not args.no_workloads and args.workload == "gdn" and not args.eager and not args.B
+            and not args.tokens and not args.M):
+        del x, out
+        torch.cuda.empty_cache()
+        result["workloads"] = {}
+        for name in ("gdn_small", "kda", "rwkv6"):
+            result["workloads"][name] = measure_decode(WORKLOADS[name], args, dist, world, rank,
+                                                       local, dev, stream)
+        result["workloads"]["fork"] = measure_fork(args, dist, world, rank, local, dev, stream)
+        x = gen.make_inputs(op, T, B, H, d, d, seed, device=dev)   # for the end-to-end run
+
     # ---- end to end through the public API with host buffers
     if args.no_e2e:
         if rank == 0:
@@ -524,7 +665,9 @@ def run_ours(args):
     d2h = hout[0].numel() * hout.element_size() * T
     result["e2e"] = {"value": units_per_step * world / (e2e_ms / 1e3), "unit": "tokens·heads/s",
                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                     "ms_per_step": e2e_ms, "api": "dl_decode_host"}
+                     "ms_per_step": e2e_ms, "api": "dl_decode_host",
+                     "copy_ceiling": copy_ceiling(pin, hout, dev, T, decode_host_group(op, B, H, d),
+                                                  units_per_step * world, args)}
 
     # ---- CPU baseline (rank 0, N = 1 only)
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -540,6 +683,58 @@ def run_ours(args):
     if dist is not None:
         dist.destroy_process_group()
     return 0
+
+
+def decode_host_group(op, S, H, d):
+    """Tokens per copy group of dl_decode_host for a context of S slots: small
+    per-token tensors are grouped until a key tensor's copy reaches 2 MiB, at
+    most 8 tokens and 64 MiB of staging a group."""
+    key = S * H * d * 2
+    per_tok = 2 * key + S * H * d * 2 + S * H * (d * 4 if op else 4) + S * H * 4 + S * H * d * 4
+    g = min(-(-(2 << 20) // key), (64 << 20) // per_tok)
+    return max(1, min(8, g))
+
+
+def copy_ceiling(pin, hout, dev, T, group, units, args):
+    """The end-to-end run's copies alone: the same uploads (one copy per input
+    tensor per group of tokens, pinned host to device) on one stream and the
+    same downloads (one copy of the outputs per group) on another, with no
+    compute.  Returns the throughput this bounds the end-to-end figure to and
+    the bandwidth each direction reached, best of a few runs."""
+    import torch
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    dbuf = {k: torch.empty((2 * group,) + tuple(v.shape[1:]), dtype=v.dtype, device=dev)
+            for k, v in pin.items() if v is not None}
+    dout = torch.empty((2 * group,) + tuple(hout.shape[1:]), dtype=hout.dtype, device=dev)
+    h2d = sum(v[0].numel() * v.element_size() for v in pin.values() if v is not None) * T
+    d2h = hout[0].numel() * hout.element_size() * T
+
+    def run():
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        ev[0].record(up)
+        ev[2].record(down)
+        for g0 in range(0, T, group):
+            n = min(group, T - g0)
+            b = (g0 // group) % 2 * group
+            with torch.cuda.stream(up):
+                for k, v in pin.items():
+                    if v is not None:
+                        dbuf[k][b:b + n].copy_(v[g0:g0 + n], non_blocking=True)
+            with torch.cuda.stream(down):
+                hout[g0:g0 + n].copy_(dout[b:b + n], non_blocking=True)
+        ev[1].record(up)
+        ev[3].record(down)
+        torch.cuda.synchronize()
+        return (time.perf_counter() - t0) * 1e3, ev[0].elapsed_time(ev[1]), ev[2].elapsed_time(ev[3])
+
+    runs = [run() for _ in range(max(2, min(args.steps, 4)))]
+    wall, t_up, t_dn = min(runs)
+    return {"value": units / (wall / 1e3), "unit": "tokens·heads/s", "ms_per_step": wall,
+            "h2d_gbs": h2d / (t_up * 1e-3) / 1e9, "d2h_gbs": d2h / (t_dn * 1e-3) / 1e9,
+            "copies": "%d-token groups: one cudaMemcpyAsync per input tensor up, one down for "
+                      "the outputs, on two streams, no compute" % group}
 
 
 def prefill_flops(op, d, C=PREFILL_C):
@@ -572,23 +767,38 @@ def gpu_setup():
     return rank, world, dist, local, torch.device("cuda", local), torch.cuda.current_stream()
 
 
+MIN_REGION_S = 0.3   # shortest timed region: the clock sampler needs a few samples
+
+
 def timed_steps(one, args, dist, local, dev, stream):
     """W untimed warm-up steps, then K steps between CUDA events on the launching
     stream (barrier + synchronize before), with the clocks sampled meanwhile.
-    Returns (ms per step, max over ranks; clock summary)."""
+    When K steps last less than MIN_REGION_S (latency-bound workloads), the
+    timed region runs the K steps `reps` times over and the time per step is
+    the region's time / (K * reps).  Returns (ms per step, max over ranks;
+    clock summary, with `reps`)."""
     import torch
     for _ in range(args.warmup):
         one()
     barrier(dist)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    one()
+    torch.cuda.synchronize()
+    est = max(time.perf_counter() - t0, 1e-6) * max(args.steps, 1)
+    reps = 1 if est >= MIN_REGION_S else int(MIN_REGION_S / est) + 1
+    reps = int(reduce_max(dist, reps, dev))
+    barrier(dist)
     with ClockSampler(local) as clk:
         e0.record(stream)
-        for _ in range(args.steps):
+        for _ in range(args.steps * reps):
             one()
         e1.record(stream)
         e1.synchronize()
-    return reduce_max(dist, e0.elapsed_time(e1) / args.steps, dev), clk.summary()
+    summary = clk.summary()
+    summary["reps"] = reps
+    return reduce_max(dist, e0.elapsed_time(e1) / (args.steps * reps), dev), summary
 
 
 def run_prefill(args):
@@ -630,7 +840,8 @@ def run_prefill(args):
                            "traffic": None, "peak_source": "derived: 152 SMs x 128 FP32 "
                            "lanes x 2 FLOP x 2.07 GHz",
                            "flops_per_token_head": prefill_flops(op, d)},
-              "clocks": clocks, "gpu_launches": args.steps * ((B + 1023) // 1024)}
+              "clocks": clocks,
+              "gpu_launches": args.steps * clocks.get("reps", 1) * ((B + 1023) // 1024)}
     if rank == 0:
         print(json.dumps(result), flush=True)
     ctx.close()
@@ -687,7 +898,7 @@ def run_checkpoint(args):
               "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
                            "frac": gbs / peak, "traffic": None, "peak_source": src},
               "clocks": clocks,
-              "gpu_launches": args.steps * 2 * ((B + 1023) // 1024)}
+              "gpu_launches": args.steps * clocks.get("reps", 1) * 2 * ((B + 1023) // 1024)}
     if rank == 0:
         print(json.dumps(result), flush=True)
     ctx.close()
@@ -734,7 +945,7 @@ def run_readstate(args):
                          "l2": "state larger than L2 (%.0f MB)" % (B * H * d * d * 4 / 1e6)},
               "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
                            "frac": gbs / peak, "traffic": None, "peak_source": src},
-              "clocks": clocks, "gpu_launches": args.steps}
+              "clocks": clocks, "gpu_launches": args.steps * clocks.get("reps", 1)}
     if rank == 0:
         print(json.dumps(result), flush=True)
     ctx.close()
@@ -744,26 +955,31 @@ def run_readstate(args):
 
 
 def run_fork(args):
+    """Forked decode as its own bench line (see measure_fork)."""
+    rank, world, dist, local, dev, stream = gpu_setup()
+    result = measure_fork(args, dist, world, rank, local, dev, stream)
+    result.update({"metric": METRIC, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                   "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                   "dtype": "f32", "data": "synthetic"})
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def measure_fork(args, dist, world, rank, local, dev, stream):
     """Forked decode: bases are built once (setup, untimed); one bench step =
     fork every request into its branches (by index, no state copy) + the
     ragged branch decode until the longest branch ends."""
     import numpy as np
     import torch
-    rank, world, dist = dist_setup("cuda")
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    from linear_attention_recurrent_gdn_gb300 import build
-    if rank == 0:
-        build.build()
-    barrier(dist)
     from linear_attention_recurrent_gdn_gb300 import deltalog as dl
     from linear_attention_recurrent_gdn_gb300 import inputs as gen
     w = WORKLOADS["fork"]
     R, NB, H, d, M, Tc = w["requests"], w["branches"], w["H"], w["d"], w["M"], w["ctx_tokens"]
     seed = w["seed"] + 7919 * rank
-    dev = torch.device("cuda", local)
-    stream = torch.cuda.current_stream()
-    lens = np.random.default_rng(seed).integers(16, 257, size=R * NB)
+    lens = fork_plan(w, seed)
     order = np.argsort(-lens, kind="stable")
     Tq = int(lens.max())
     counts = [int((lens > t).sum()) for t in range(Tq)]
@@ -807,49 +1023,34 @@ def run_fork(args):
             c = counts[t]
             ctx.step(act_slots[t], xq["q"][t][:c], xq["k"][t][:c], xq["v"][t][:c],
                      xq["g"][t][:c], xq["beta"][t][:c], out[t][:c])
-    for _ in range(args.warmup):
-        one()
-    barrier(dist)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
-        e0.record(stream)
-        for _ in range(args.steps):
-            one()
-        e1.record(stream)
-        e1.synchronize()
-    ms = reduce_max(dist, e0.elapsed_time(e1) / args.steps, dev)
+
+    ms, clocks = timed_steps(one, args, dist, local, dev, stream)
     units = int(lens.sum()) * H
     # every branch starts at the source's log length 0, so the branches active at
     # token t all step with log length t mod M
     step_bytes = sum(counts[t] * H * fused_bytes(0, d, M, t % M)[0] for t in range(Tq))
+    step_writes = sum(counts[t] * H * fused_bytes(0, d, M, t % M)[1] for t in range(Tq))
+    eager_writes = units * eager_bytes(0, d)[1]
     gbs = step_bytes / (ms / 1e3) / 1e9
     peak, peak_src = hbm_peak()
-    result = {"metric": METRIC, "value": units * world / (ms / 1e3), "unit": "tokens·heads/s",
-              "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-              "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-              "data": "synthetic",
-              "config": {"workload": w["desc"], "op": "gdn", "requests": R, "branches": NB,
-                         "H": H, "d_k": d, "d_v": d, "M": M, "ctx_tokens": Tc,
-                         "branch_tokens": int(lens.sum()), "staging": args.staging,
-                         "loop": ("ragged CUDA graphs, one per M tokens (dl_window_*_ragged)"
-                                  if wins else "dl_step per token"),
-                         "l2": "inputs larger than L2 (576 slots x 1 MiB state)"},
+    result = {"value": units * world / (ms / 1e3), "unit": "tokens·heads/s", "ms_per_step": ms,
+              "config": fork_config(w, args, lens),
               "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
                            "frac": gbs / peak, "traffic": None, "peak_source": peak_src,
                            "kernel": "AppendDecode over the ragged branch batch, fork "
                                      "launches included",
-                           "algorithmic_bytes_per_step": step_bytes},
-              "clocks": clk.summary(),
-              "gpu_launches": (R + (1 if fused else 2) * Tpad) * args.steps}
-    if rank == 0:
-        print(json.dumps(result), flush=True)
+                           "bytes_per_step": step_bytes,
+                           "timing": "whole bench step (forks + every branch token)"},
+              "write_bytes_per_step": {"deltalog": step_writes, "eager": eager_writes},
+              "write_cut_vs_eager": eager_writes / step_writes,
+              "clocks": clocks,
+              "gpu_launches": (R + (1 if fused else 2) * Tpad) * args.steps * clocks.get("reps", 1)}
     for win in wins or []:
         win.close()
     ctx.close()
-    if dist is not None:
-        dist.destroy_process_group()
-    return 0
+    del xq, out
+    torch.cuda.empty_cache()
+    return result
 
 
 def main():
@@ -872,6 +1073,9 @@ def main():
                     help="ReplayPrep as a warp role of AppendDecode (fused) or its own kernel")
     ap.add_argument("--eager", action="store_true",
                     help="time the in-house eager kernel (dense read-modify-write) instead")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the other decode workloads the default run measures beside "
+                         "the headline")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

@@ -174,8 +174,10 @@ dl_status dl_fork(dl_ctx *ctx, int32_t src, const int32_t *dsts, int32_t n);
  *   beta                 [n, H] fp32 (GDN, KDA); ignored for RWKV6 (may be NULL)
  *   o                    [n, H, d_v] bf16 or fp32 (dl_config.out_bf16), written
  * Runs the ReplayPrep and AppendDecode stages (dl_config.staging; the merge is
- * fused for the slots whose log is full).  A frozen slot in the list returns
- * DL_EBUSY. */
+ * fused for the slots whose log is full).  With M = 1 every step is the eager
+ * update; when every listed slot reads its own base it runs as the EagerStep
+ * kernel (as dl_step_eager), else through the merge path.  A frozen slot in the
+ * list returns DL_EBUSY. */
 dl_status dl_step(dl_ctx *ctx, const int32_t *slots, int32_t n,
                   const void *q, const void *k, const void *v,
                   const float *g, const float *beta, void *o);

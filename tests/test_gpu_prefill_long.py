@@ -1,0 +1,57 @@
+"""Chunked prefill over long contexts against the fp64 oracle.
+
+The Flide page's first call builds a request's base from its whole shared
+context ("Research method step by step", second step); the fork workload does
+this over 2048 tokens, and the prefill bench lines run 512-token contexts.
+Here dl_prefill runs those lengths for every operator at its decode workload's
+head size, with bf16 outputs, and a sample of slot-heads is checked against the
+eager fp64 oracle: every token's output (max relative error <= 5e-3, the
+DeltaLog page's "Results" bound) and the final state (<= 1e-4).  RWKV6's
+per-key decays reach cumulative log-decays of about -100 inside a window, so
+a long context is where fp32 drift in the chunked form would show.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import OUT_TOL_BF16, STATE_TOL, make_case, max_step_rel, oracle_run, rel_err
+from linear_attention_recurrent_gdn_gb300 import build
+from linear_attention_recurrent_gdn_gb300 import inputs as gen
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+
+
+@pytest.mark.parametrize("T", [512, 2048])
+@pytest.mark.parametrize("op,d", [(gen.GDN, 128), (gen.KDA, 128), (gen.RWKV6, 64)])
+def test_long_prefill_matches_oracle(op, d, T):
+    from linear_attention_recurrent_gdn_gb300 import deltalog as dl
+    B, H, M = 8, 4, 16
+    x, S0, bonus = make_case(op, B, H, d, T, seed=5100 + op + T)
+    rng = np.random.default_rng(T + op)
+    n_sel = 4 if T > 1024 else 8
+    flat = rng.choice(B * H, size=n_sel, replace=False)
+    sel = [(int(i) // H, int(i) % H) for i in flat]
+    o_ref, S_ref, _ = oracle_run(op, x, S0, bonus, sel=sel)
+    ctx = dl.DeltaLog(op, B, H, d, d, M, out_bf16=True)
+    slots = list(range(B))
+    ctx.set_state(slots, S0.cuda())
+    if bonus is not None:
+        ctx.set_bonus(bonus.cuda())
+    dev = {k: (v.cuda() if v is not None else None) for k, v in x.items()}
+    o = ctx.prefill(slots, dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"])
+    S = ctx.read_state(slots).cpu()
+    n, base_of = ctx.get_meta()
+    ctx.close()
+    bi = torch.tensor([s[0] for s in sel])
+    hi = torch.tensor([s[1] for s in sel])
+    o_sel = o.float().cpu()[:, bi, hi].numpy()
+    assert max_step_rel(o_sel, o_ref) <= OUT_TOL_BF16
+    assert rel_err(S[bi, hi].numpy(), S_ref) <= STATE_TOL
+    assert list(n) == [0] * B and list(base_of) == slots
