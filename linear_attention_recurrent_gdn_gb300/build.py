@@ -18,7 +18,7 @@ OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libdeltalog.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CU_SOURCES = ["replay_prep.cu", "append_decode.cu", "append_fused_ne8.cu", "append_fused_ne16.cu",
-              "append_fused_ne32.cu", "eager_step.cu", "slot_ops.cu", "prefill.cu", "capi.cu",
+              "append_fused_ne32.cu", "eager_step.cu", "slot_ops.cu", "prefill.cu", "prefill_tc.cu", "capi.cu",
               "noalloc.cu"]
 CPP_SOURCES = ["slot_table.cpp"]
 

@@ -829,7 +829,8 @@ dl_status dl_prefill(dl_ctx* c, const int32_t* slots, int32_t n, int32_t T, cons
   a.Mcap = c->L.Mcap;
   for (int32_t i = 0; i < n; ++i) a.items[i] = dl::StepItem{slots[i], slots[i], 0};
   DL_CUDA(dl::launch_prefill(c->cfg.op, c->cfg.d_k, a, q, k, v, g, delta ? beta : nullptr,
-                             c->bonus, o, T, c->cfg.out_bf16, c->cfg.scale, c->stream),
+                             c->bonus, o, T, c->cfg.out_bf16, c->cfg.scale, c->status,
+                             c->stream),
           "Prefill launch");
   return DL_OK;
 }

@@ -28,6 +28,7 @@ constexpr int32_t DEV_TIMEOUT_AUX = 2;
 constexpr int32_t DEV_TIMEOUT_EMPTY = 3;
 constexpr int32_t DEV_BAD_ITEM = 4;
 constexpr int32_t DEV_TEST_STALL = 5;   // the test-only stall below ran out (nothing else sets it)
+constexpr int32_t DEV_TIMEOUT_MMA = 6;  // a wait for tensor-core MMAs to complete gave up
 constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;  // 2 s (default per-launch limit)
 
 // One-line meaning of a device status code (host side).
@@ -38,6 +39,7 @@ inline const char* device_status_str(int32_t code) {
     case DEV_TIMEOUT_EMPTY: return "a wait for a stage or input slot to be released gave up";
     case DEV_BAD_ITEM: return "a plan row was out of range";
     case DEV_TEST_STALL: return "the test-only stall's bounded wait gave up";
+    case DEV_TIMEOUT_MMA: return "a wait for tensor-core MMAs to complete gave up";
     default: return "unknown device status";
   }
 }

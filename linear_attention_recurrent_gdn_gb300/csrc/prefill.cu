@@ -701,11 +701,12 @@ static cudaError_t pk_dispatch(const SlotListArgs& a, const void* q, const void*
 
 cudaError_t launch_prefill(int op, int dk, const SlotListArgs& a, const void* q, const void* k,
                            const void* v, const float* g, const float* beta, const float* bonus,
-                           void* o, int T, int out_bf16, float scale, cudaStream_t s) {
+                           void* o, int T, int out_bf16, float scale, int32_t* status,
+                           cudaStream_t s) {
   if (a.rows <= 0 || T <= 0) return cudaSuccess;
   if (op == GDN) {
     if (dk == 64) return pf_dispatch<64>(a, q, k, v, g, beta, o, T, out_bf16, scale, s);
-    return pf_dispatch<128>(a, q, k, v, g, beta, o, T, out_bf16, scale, s);
+    return launch_prefill_gdn_tc(a, q, k, v, g, beta, o, T, out_bf16, scale, status, s);
   }
   if (op == KDA) {
     if (dk == 64) return pk_dispatch<KDA, 64>(a, q, k, v, g, beta, bonus, o, T, out_bf16, scale, s);

@@ -1,0 +1,451 @@
+// Chunked prefill of GDN at d_k = d_v = 128 on the 5th-generation tensor cores.
+//
+// Same algebra as the CUDA-core kernel in prefill.cu (the DeltaLog page's
+// base + log form inside a chunk of C = 32 tokens, the Flide page's first call
+// that builds a request's state from its shared context): with S̄ the state at
+// the chunk start, Λ_j the cumulative log-decay inside the chunk,
+//   x_j = e^{Λ_j} (S̄ k_j) + Σ_{i<j} e^{Λ_j-Λ_i} (k_i·k_j) u_i,  u_j = β_j (v_j - x_j)
+//   o_j = e^{Λ_j} (S̄ q_j) + Σ_{i<=j} e^{Λ_j-Λ_i} (k_i·q_j) u_i
+//   S̄'  = e^{Λ_C} S̄ + Σ_j (e^{Λ_C-Λ_j} u_j) k_j^T
+// The three dense contractions of a chunk run as tcgen05 MMAs (bf16 operands,
+// fp32 accumulators in tensor memory):
+//   D0 [128 x 32]  = [K; Q; 0] K^T           the key-key and query-key products (exact: k, q are bf16)
+//   D1 [128 x 64]  = (S̄_hi + S̄_lo) [K; Q]^T  S̄ k_j and S̄ q_j for all 32 tokens
+//   D2 [128 x 128] = (U_hi + U_lo) K          the rank-32 rewrite, U = e^{Λ_C-Λ_j} u_j
+// S̄ and U are fp32; each is carried as two bf16 terms (hi = bf16(x), lo =
+// bf16(x - hi)), which leaves |x - hi - lo| <= 2^-17 |x|, so the products keep
+// the state's 1e-4 tolerance.  The fp32 state itself never leaves the
+// registers of the CTA (thread (row r, half h) holds S̄[r][64h .. 64h + 63]); the
+// decay e^{Λ_C} and the rank-32 term are added there, and the bf16 terms of the
+// new S̄ are written back to shared memory for the next chunk.  The forward
+// substitution for u (a chain over the chunk's tokens) and the outputs run on
+// the CUDA cores, one thread per value row.
+//
+// One CTA of 256 threads per slot-head.  Warp w reads tensor-memory lanes
+// 32 (w % 4) .. +31, i.e. value rows r = 32 (w % 4) + lane.  Thread 0 issues the
+// MMAs and waits on their mbarrier (bounded: a wait that runs out records
+// DEV_TIMEOUT_MMA in the status word, lets the outstanding MMAs land and frees
+// the tensor memory before the CTA returns).
+#include "dl_device.cuh"
+#include "launch.h"
+#include "layout.h"
+#include "tc_device.cuh"
+
+namespace dl {
+
+namespace {
+
+constexpr int TC_C = 32;           // tokens per chunk
+constexpr int TC_THREADS = 256;
+constexpr int TC_D = 128;          // d_k = d_v
+constexpr uint32_t TC_COLS = 256;  // TMEM columns: D0 [0, 32), D1 [32, 96), D2 [128, 256)
+constexpr uint32_t D0_COL = 0, D1_COL = 32, D2_COL = 128;
+// Row strides: v rows padded to 136 bf16 (272 bytes: a warp's staging stores of
+// 8 rows x 64 bytes spread over all banks); pair-coefficient rows of 36 floats
+// (16-byte aligned, read as float4 broadcasts).
+constexpr int VP = TC_D + 8, AP = 36;
+
+// Byte offsets in the dynamic shared memory (operands 16-byte aligned).
+struct TcSmem {
+  static constexpr uint32_t SHI = 0;                       // S̄ hi, K-major [128 x 128] bf16
+  static constexpr uint32_t SLO = SHI + TC_D * TC_D * 2;   // S̄ lo
+  static constexpr uint32_t KQ = SLO + TC_D * TC_D * 2;    // rows 0-31 k_j, 32-63 q_j, 64-127 zero
+  static constexpr uint32_t KT = KQ + TC_D * TC_D * 2;     // K as [i (128)] x [j (32)], K-major
+  static constexpr uint32_t UHI = KT + TC_D * TC_C * 2;    // U hi [v (128)] x [j (32)], K-major
+  static constexpr uint32_t ULO = UHI + TC_D * TC_C * 2;   // U lo
+  static constexpr uint32_t VS = ULO + TC_D * TC_C * 2;    // v_j[r] bf16, rows of VP
+  static constexpr uint32_t AKK = VS + TC_C * VP * 2;      // fp32 [32][AP], 16-byte rows
+  static constexpr uint32_t AKQ = AKK + TC_C * AP * 4;     // fp32 [32][AP]
+  static constexpr uint32_t US = AKQ + TC_C * AP * 4;      // u fp32 [128][33]
+  static constexpr uint32_t SC = US + TC_D * 33 * 4;       // Λ_j, e^{Λ_j}, e^{Λ_C-Λ_j}, β_j: [4][32] fp32
+  static constexpr uint32_t BAR = SC + 4 * TC_C * 4;       // 2 mbarriers, TMEM base, ok flag
+  static constexpr uint32_t BYTES = BAR + 32;
+};
+static_assert(TcSmem::BYTES <= 227 * 1024, "shared memory");
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo_elem, float hi_elem) {
+  return (uint32_t)f2bf16(lo_elem) | ((uint32_t)f2bf16(hi_elem) << 16);
+}
+
+// 8 consecutive fp32 values -> the bf16 high parts (h) and low parts (l).
+__device__ __forceinline__ void split8(const float* x, uint4& h, uint4& l) {
+  uint32_t hw[4], lw[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float a = x[2 * e], b = x[2 * e + 1];
+    const float ah = bf16f(f2bf16(a)), bh = bf16f(f2bf16(b));
+    hw[e] = pack_bf16x2(ah, bh);
+    lw[e] = pack_bf16x2(a - ah, b - bh);
+  }
+  h = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+  l = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+}
+
+// One chunk's k, q, v (bf16) and g, β in registers between their global loads
+// and their shared-memory stores.
+struct TcStage {
+  uint4 k[2], q[2], v[2];
+  float g, b;
+
+  // Element idx of the chunk's 32 x 16 grid of 16-byte pieces (token j, column
+  // piece cv): a warp's lanes take 8 consecutive tokens x 4 consecutive pieces,
+  // so its global loads read 64 contiguous bytes of each of 8 rows and its
+  // stores into the K-major operands fill whole 128-byte core-matrix rows.
+  static __device__ __forceinline__ void piece(int idx, int& j, int& cv) {
+    const int rest = idx >> 5;
+    j = (idx & 7) + 8 * (rest & 3);
+    cv = ((idx >> 3) & 3) + 4 * (rest >> 2);
+  }
+
+  __device__ __forceinline__ void load(const uint16_t* __restrict__ qg, const uint16_t* __restrict__ kg,
+                                       const uint16_t* __restrict__ vg, const float* __restrict__ gg,
+                                       const float* __restrict__ bg, int t0, int Cc, size_t nH,
+                                       int sh, int tid) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      int j, cv;
+      piece(tid + e * TC_THREADS, j, cv);
+      if (j < Cc) {
+        const size_t base = ((size_t)(t0 + j) * nH + sh) * TC_D + cv * 8;
+        k[e] = *reinterpret_cast<const uint4*>(kg + base);
+        q[e] = *reinterpret_cast<const uint4*>(qg + base);
+        v[e] = *reinterpret_cast<const uint4*>(vg + base);
+      } else {
+        k[e] = q[e] = v[e] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    if (tid < 32) {
+      g = tid < Cc ? gg[(size_t)(t0 + tid) * nH + sh] : 0.f;
+      b = tid < Cc ? bg[(size_t)(t0 + tid) * nH + sh] : 0.f;
+    }
+  }
+
+  // k, q into the KQ operand, k into the transposed KT operand, v into VS
+  __device__ __forceinline__ void store(unsigned char* sm, int tid) const {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      int j, cv;
+      piece(tid + e * TC_THREADS, j, cv);
+      *reinterpret_cast<uint4*>(sm + TcSmem::KQ + tc::kmaj_off(j, cv * 8, TC_D)) = k[e];
+      *reinterpret_cast<uint4*>(sm + TcSmem::KQ + tc::kmaj_off(TC_C + j, cv * 8, TC_D)) = q[e];
+      *reinterpret_cast<uint4*>(sm + TcSmem::VS + (j * VP + cv * 8) * 2) = v[e];
+      const uint32_t w[4] = {k[e].x, k[e].y, k[e].z, k[e].w};
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {   // k_j[i], i = 8 cv + t, at KT row i, column j
+        const uint16_t x = (uint16_t)((t & 1) ? (w[t >> 1] >> 16) : (w[t >> 1] & 0xffffu));
+        *reinterpret_cast<uint16_t*>(sm + TcSmem::KT + tc::kmaj_off(cv * 8 + t, j, TC_C)) = x;
+      }
+    }
+  }
+};
+
+// Outputs o_j = scale (e^{Λ_j} pq_j + Σ_{i<=j} A_kq[j][i] u_i) of row r for the
+// tokens j = P, P + 2, ... below Cc (the two halves of the CTA take the two parities).
+template <int P>
+__device__ __forceinline__ void outputs_parity(const float (&u)[TC_C], const float (&pq)[TC_C],
+                                               const float* __restrict__ El, const float* __restrict__ Akq,
+                                               void* o, int out_bf16, float scale, size_t obase,
+                                               size_t ostride, int Cc) {
+#pragma unroll
+  for (int j2 = 0; j2 < TC_C / 2; ++j2) {
+    const int j = 2 * j2 + P;
+    if (j < Cc) {
+      float y[4] = {El[j] * pq[j], 0.f, 0.f, 0.f};
+      // coefficients past the diagonal are zero, so whole quads can be used
+#pragma unroll
+      for (int i4 = 0; i4 <= j / 4; ++i4) {
+        const float4 c = *reinterpret_cast<const float4*>(Akq + j * AP + 4 * i4);
+        y[0] += c.x * u[4 * i4];
+        y[1] += c.y * u[4 * i4 + 1];
+        y[2] += c.z * u[4 * i4 + 2];
+        y[3] += c.w * u[4 * i4 + 3];
+      }
+      const float yo = scale * ((y[0] + y[1]) + (y[2] + y[3]));
+      const size_t oi = obase + (size_t)j * ostride;
+      if (out_bf16) static_cast<uint16_t*>(o)[oi] = f2bf16(yo);
+      else static_cast<float*>(o)[oi] = yo;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(TC_THREADS, 1)
+prefill_gdn_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* __restrict__ q,
+                      const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
+                      const float* __restrict__ g, const float* __restrict__ beta, void* o, int T,
+                      int out_bf16, float scale, int32_t* status) {
+  extern __shared__ __align__(1024) unsigned char sm[];
+  float* Akk = reinterpret_cast<float*>(sm + TcSmem::AKK);
+  float* Akq = reinterpret_cast<float*>(sm + TcSmem::AKQ);
+  float* Us = reinterpret_cast<float*>(sm + TcSmem::US);
+  float* Lm = reinterpret_cast<float*>(sm + TcSmem::SC);
+  float* El = Lm + TC_C;
+  float* Ew = El + TC_C;
+  float* Bt = Ew + TC_C;
+  const uint16_t* Vs = reinterpret_cast<const uint16_t*>(sm + TcSmem::VS);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + TcSmem::BAR + 16);
+  int32_t* ok_flag = reinterpret_cast<int32_t*>(sm + TcSmem::BAR + 20);
+  const uint32_t sbase = smem_u32(sm);
+  const uint32_t bar1 = sbase + TcSmem::BAR, bar2 = sbase + TcSmem::BAR + 8;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int q4 = warp & 3, hw = warp >> 2;      // TMEM lane quarter, column half
+  const int r = 32 * q4 + lane;                 // this thread's value row
+  const int sh = blockIdx.x, row = sh / a.H, h = sh - row * a.H;
+  const int slot = a.items[row].slot;
+  const size_t nH = (size_t)a.rows * a.H;
+  float* gS = a.Sbar + ((size_t)slot * a.H + h) * TC_D * TC_D;
+
+  if (warp == 0) tc::tmem_alloc(sbase + TcSmem::BAR + 16, TC_COLS);
+  if (tid == 0) {
+    mbar_init(bar1, 1);
+    mbar_init(bar2, 1);
+    fence_mbar_init();
+    *ok_flag = 1;
+  }
+  // rows 64-127 of the KQ operand stay zero (D0's rows 64-127 are unused)
+  for (int idx = tid; idx < 64 * TC_D * 2 / 16; idx += TC_THREADS)
+    reinterpret_cast<uint4*>(sm + TcSmem::KQ + 64 * TC_D * 2)[idx] = make_uint4(0u, 0u, 0u, 0u);
+
+  // the fp32 state of this thread's row half, and its bf16 terms for the MMAs
+  float S[64];
+  {
+    const float4* src = reinterpret_cast<const float4*>(gS + (size_t)r * TC_D + 64 * hw);
+#pragma unroll
+    for (int c4 = 0; c4 < 16; ++c4) {
+      const float4 x = src[c4];
+      S[4 * c4] = x.x;
+      S[4 * c4 + 1] = x.y;
+      S[4 * c4 + 2] = x.z;
+      S[4 * c4 + 3] = x.w;
+    }
+#pragma unroll
+    for (int c8 = 0; c8 < 8; ++c8) {
+      uint4 hv, lv;
+      split8(S + 8 * c8, hv, lv);
+      const uint32_t off = tc::kmaj_off(r, 64 * hw + 8 * c8, TC_D);
+      *reinterpret_cast<uint4*>(sm + TcSmem::SHI + off) = hv;
+      *reinterpret_cast<uint4*>(sm + TcSmem::SLO + off) = lv;
+    }
+  }
+
+  TcStage st;
+  st.load(q, k, v, g, beta, 0, T < TC_C ? T : TC_C, nH, sh, tid);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tm = *tmem_slot;
+  const uint32_t tlane = tm + ((uint32_t)(32 * q4) << 16);   // this warp's lane quarter
+  bool ok = true;
+  int chunk = 0;
+  for (int t0 = 0; t0 < T && ok; t0 += TC_C, ++chunk) {
+    const int Cc = (T - t0) < TC_C ? (T - t0) : TC_C;
+    const uint32_t par = (uint32_t)chunk & 1u;
+    // ---- stage the chunk (tokens past the end: zero inputs, zero decay)
+    st.store(sm, tid);
+    if (warp == 0) {
+      float gj = st.g;
+#pragma unroll
+      for (int o2 = 1; o2 < 32; o2 <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, gj, o2);
+        if (lane >= o2) gj += y;
+      }
+      const float LC = __shfl_sync(0xffffffffu, gj, Cc - 1);
+      Lm[lane] = gj;
+      El[lane] = expf(gj);
+      Ew[lane] = lane < Cc ? expf(LC - gj) : 0.f;   // padding tokens add nothing
+      Bt[lane] = st.b;                               // 0 past Cc
+    }
+    tc::fence_smem_to_async();   // KQ, KT and the S̄ terms, for the tensor cores
+    tc::fence_before_sync();
+    __syncthreads();
+    // ---- D0 = [K; Q; 0] K^T and D1 = (S̄_hi + S̄_lo) [K; Q]^T
+    if (tid == 0) {
+      tc::fence_after_sync();
+      constexpr uint32_t id0 = tc::idesc_bf16_f32(128, 32), id1 = tc::idesc_bf16_f32(128, 64);
+#pragma unroll
+      for (int kk = 0; kk < TC_D / 16; ++kk)
+        tc::mma_bf16(tm + D0_COL, tc::kmaj_desc(sbase + TcSmem::KQ, TC_D, kk),
+                     tc::kmaj_desc(sbase + TcSmem::KQ, TC_D, kk), id0, kk > 0);
+#pragma unroll
+      for (int kk = 0; kk < TC_D / 16; ++kk)
+        tc::mma_bf16(tm + D1_COL, tc::kmaj_desc(sbase + TcSmem::SHI, TC_D, kk),
+                     tc::kmaj_desc(sbase + TcSmem::KQ, TC_D, kk), id1, kk > 0);
+#pragma unroll
+      for (int kk = 0; kk < TC_D / 16; ++kk)
+        tc::mma_bf16(tm + D1_COL, tc::kmaj_desc(sbase + TcSmem::SLO, TC_D, kk),
+                     tc::kmaj_desc(sbase + TcSmem::KQ, TC_D, kk), id1, 1u);
+      tc::mma_commit(bar1);
+    }
+    // the next chunk's inputs load while the tensor cores run
+    if (t0 + TC_C < T) {
+      const int Cn = (T - t0 - TC_C) < TC_C ? (T - t0 - TC_C) : TC_C;
+      st.load(q, k, v, g, beta, t0 + TC_C, Cn, nH, sh, tid);
+    }
+    if (tid == 0 && !mbar_wait(bar1, par, status, DEV_TIMEOUT_MMA)) *ok_flag = -1;
+    __syncthreads();
+    if (*ok_flag != 1) {
+      ok = false;
+      break;
+    }
+    tc::fence_after_sync();
+    // ---- read D0 (warps 0, 1: pair products with their decays) and D1
+    float pk[TC_C], pq[TC_C];
+    {
+      uint32_t x[TC_C];
+      tc::tmem_ld32(tlane + D1_COL + TC_C, x);   // S̄ q_j
+      tc::tmem_wait_ld(x);
+#pragma unroll
+      for (int j = 0; j < TC_C; ++j) pq[j] = __uint_as_float(x[j]);
+      if (hw == 0) {
+        tc::tmem_ld32(tlane + D1_COL, x);        // S̄ k_j
+        tc::tmem_wait_ld(x);
+#pragma unroll
+        for (int j = 0; j < TC_C; ++j) pk[j] = __uint_as_float(x[j]);
+      }
+      if (warp < 2) {
+        tc::tmem_ld32(tlane + D0_COL, x);        // row j = lane: k_j·k_i (warp 0), q_j·k_i (warp 1)
+        tc::tmem_wait_ld(x);
+        const int j = lane;
+        const float lj = Lm[j];
+        float* A = warp == 0 ? Akk : Akq;
+#pragma unroll
+        for (int i = 0; i < AP; ++i) {
+          if (i >= TC_C) {   // row padding: zero, read by the quad loads
+            A[j * AP + i] = 0.f;
+            continue;
+          }
+          const bool live = (warp == 0 ? i < j : i <= j) && j < Cc;
+          A[j * AP + i] = live ? __uint_as_float(x[i]) * expf(lj - Lm[i]) : 0.f;   // exponent <= 0
+        }
+      }
+    }
+    __syncthreads();
+    // ---- forward substitution (warps 0-3, one value row each)
+    float u[TC_C];
+    if (hw == 0) {
+#pragma unroll
+      for (int j = 0; j < TC_C; ++j) u[j] = 0.f;   // entries not yet solved multiply zero coefficients
+#pragma unroll
+      for (int j = 0; j < TC_C; ++j) {
+        float x[4] = {El[j] * pk[j], 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i4 = 0; i4 < (j + 3) / 4; ++i4) {
+          const float4 c = *reinterpret_cast<const float4*>(Akk + j * AP + 4 * i4);
+          x[0] += c.x * u[4 * i4];
+          x[1] += c.y * u[4 * i4 + 1];
+          x[2] += c.z * u[4 * i4 + 2];
+          x[3] += c.w * u[4 * i4 + 3];
+        }
+        u[j] = Bt[j] * (bf16f(Vs[j * VP + r]) - ((x[0] + x[1]) + (x[2] + x[3])));   // 0 past Cc
+      }
+#pragma unroll
+      for (int c8 = 0; c8 < TC_C / 8; ++c8) {
+        float w8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) w8[e] = u[8 * c8 + e] * Ew[8 * c8 + e];
+        uint4 hv, lv;
+        split8(w8, hv, lv);
+        const uint32_t off = tc::kmaj_off(r, 8 * c8, TC_C);
+        *reinterpret_cast<uint4*>(sm + TcSmem::UHI + off) = hv;
+        *reinterpret_cast<uint4*>(sm + TcSmem::ULO + off) = lv;
+      }
+#pragma unroll
+      for (int j = 0; j < TC_C; ++j) Us[r * 33 + j] = u[j];
+    }
+    tc::fence_smem_to_async();   // U terms, for the tensor cores
+    tc::fence_before_sync();
+    __syncthreads();
+    // ---- D2 = (U_hi + U_lo) K, while the outputs are computed
+    if (tid == 0) {
+      tc::fence_after_sync();
+      constexpr uint32_t id2 = tc::idesc_bf16_f32(128, 128);
+#pragma unroll
+      for (int kk = 0; kk < TC_C / 16; ++kk)
+        tc::mma_bf16(tm + D2_COL, tc::kmaj_desc(sbase + TcSmem::UHI, TC_C, kk),
+                     tc::kmaj_desc(sbase + TcSmem::KT, TC_C, kk), id2, kk > 0);
+#pragma unroll
+      for (int kk = 0; kk < TC_C / 16; ++kk)
+        tc::mma_bf16(tm + D2_COL, tc::kmaj_desc(sbase + TcSmem::ULO, TC_C, kk),
+                     tc::kmaj_desc(sbase + TcSmem::KT, TC_C, kk), id2, 1u);
+      tc::mma_commit(bar2);
+    }
+    if (o != nullptr) {
+      const size_t obase = ((size_t)t0 * nH + sh) * TC_D + r, ostride = nH * TC_D;
+      if (hw == 0) {
+        outputs_parity<0>(u, pq, El, Akq, o, out_bf16, scale, obase, ostride, Cc);
+      } else {
+#pragma unroll
+        for (int j = 0; j < TC_C; ++j) u[j] = Us[r * 33 + j];
+        outputs_parity<1>(u, pq, El, Akq, o, out_bf16, scale, obase, ostride, Cc);
+      }
+    }
+    if (tid == 0 && !mbar_wait(bar2, par, status, DEV_TIMEOUT_MMA)) *ok_flag = -2;
+    __syncthreads();
+    if (*ok_flag != 1) {
+      ok = false;
+      break;
+    }
+    tc::fence_after_sync();
+    // ---- S̄ <- e^{Λ_C} S̄ + D2 in registers; its bf16 terms for the next chunk
+    {
+      const float eC = El[Cc - 1];
+      uint32_t x0[32], x1[32];
+      tc::tmem_ld32(tlane + D2_COL + 64 * hw, x0);
+      tc::tmem_ld32(tlane + D2_COL + 64 * hw + 32, x1);
+      tc::tmem_wait_ld(x0);
+      tc::tmem_wait_ld(x1);
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        S[c] = eC * S[c] + __uint_as_float(x0[c]);
+        S[32 + c] = eC * S[32 + c] + __uint_as_float(x1[c]);
+      }
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8) {
+        uint4 hv, lv;
+        split8(S + 8 * c8, hv, lv);
+        const uint32_t off = tc::kmaj_off(r, 64 * hw + 8 * c8, TC_D);
+        *reinterpret_cast<uint4*>(sm + TcSmem::SHI + off) = hv;
+        *reinterpret_cast<uint4*>(sm + TcSmem::SLO + off) = lv;
+      }
+    }
+    tc::fence_before_sync();
+    __syncthreads();   // every thread is done with this chunk's shared buffers
+  }
+  if (!ok && tid == 0) {
+    // let the MMAs still in flight (those of the wait that gave up) land
+    // before the tensor memory is freed; the drain is bounded too
+    mbar_drain(*ok_flag == -1 ? bar1 : bar2, (uint32_t)chunk & 1u);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tm, TC_COLS);
+  }
+  if (!ok) return;
+  float4* dst = reinterpret_cast<float4*>(gS + (size_t)r * TC_D + 64 * hw);
+#pragma unroll
+  for (int c4 = 0; c4 < 16; ++c4)
+    dst[c4] = make_float4(S[4 * c4], S[4 * c4 + 1], S[4 * c4 + 2], S[4 * c4 + 3]);
+  if (h == 0 && tid == 0) {
+    a.nlog[slot] = 0;
+    a.base_of[slot] = slot;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_gdn_tc(const SlotListArgs& a, const void* q, const void* k,
+                                  const void* v, const float* g, const float* beta, void* o, int T,
+                                  int out_bf16, float scale, int32_t* status, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(prefill_gdn_tc_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)TcSmem::BYTES);
+  if (e != cudaSuccess) return e;
+  prefill_gdn_tc_kernel<<<a.rows * a.H, TC_THREADS, TcSmem::BYTES, s>>>(
+      a, static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(k),
+      static_cast<const uint16_t*>(v), g, beta, o, T, out_bf16, scale, status);
+  return cudaGetLastError();
+}
+
+}  // namespace dl

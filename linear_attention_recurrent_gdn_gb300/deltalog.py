@@ -20,8 +20,10 @@ OK, EINVAL, ENOMEM, ECUDA, EBUSY, EDEVICE, EUNSUPPORTED = range(7)
 # Codes a kernel writes into a device status word (the library reports them as
 # EDEVICE): a bounded wait for a state tile, for a unit's inputs or
 # coefficients, or for a stage / input slot to be released gave up; a plan row
-# was out of range; the test-only stall ran out.
+# was out of range; the test-only stall ran out; a wait for tensor-core MMAs
+# (chunked prefill) gave up.
 DEV_TIMEOUT_TILE, DEV_TIMEOUT_AUX, DEV_TIMEOUT_EMPTY, DEV_BAD_ITEM, DEV_TEST_STALL = 1, 2, 3, 4, 5
+DEV_TIMEOUT_MMA = 6
 STATUS_NAMES = ["DL_OK", "DL_EINVAL", "DL_ENOMEM", "DL_ECUDA", "DL_EBUSY", "DL_EDEVICE",
                 "DL_EUNSUPPORTED"]
 LIB_PATH = _build.LIB
