@@ -7,19 +7,21 @@
 //   x_j = e^{Λ_j} (S̄ k_j) + Σ_{i<j} e^{Λ_j-Λ_i} (k_i·k_j) u_i,  u_j = β_j (v_j - x_j)
 //   o_j = e^{Λ_j} (S̄ q_j) + Σ_{i<=j} e^{Λ_j-Λ_i} (k_i·q_j) u_i
 //   S̄'  = e^{Λ_C} S̄ + Σ_j (e^{Λ_C-Λ_j} u_j) k_j^T
-// The three dense contractions of a chunk run as tcgen05 MMAs (bf16 operands,
-// fp32 accumulators in tensor memory):
-//   D0 [128 x 32]  = [K; Q; 0] K^T           the key-key and query-key products (exact: k, q are bf16)
-//   D1 [128 x 64]  = (S̄_hi + S̄_lo) [K; Q]^T  S̄ k_j and S̄ q_j for all 32 tokens
-//   D2 [128 x 128] = (U_hi + U_lo) K          the rank-32 rewrite, U = e^{Λ_C-Λ_j} u_j
-// S̄ and U are fp32; each is carried as two bf16 terms (hi = bf16(x), lo =
-// bf16(x - hi)), which leaves |x - hi - lo| <= 2^-17 |x|, so the products keep
-// the state's 1e-4 tolerance.  The fp32 state itself never leaves the
+// The dense contractions of a chunk run as tcgen05 MMAs (bf16 operands, fp32
+// accumulators in tensor memory):
+//   D0 [128 x 32]  = [K; Q; 0] K^T              key-key and query-key products (exact: k, q are bf16)
+//   D1 [128 x 64]  = (S̄_hi + S̄_lo) [K; Q]^T     S̄ k_j and S̄ q_j for all 32 tokens
+//   D2 [128 x 128] = (W_hi + W_lo) K             the rank-32 rewrite, W = e^{Λ_C-Λ_j} u_j
+//   D3 [128 x 32]  = U_hi A_hi + U_lo A_hi + U_hi A_lo   the outputs' log terms,
+//                    A[j][i] = e^{Λ_j-Λ_i} (k_i·q_j) for i <= j
+// S̄, W, U and A are fp32; each is carried as two bf16 terms (hi = bf16(x),
+// lo = bf16(x - hi)), which leaves |x - hi - lo| <= 2^-17 |x|, so the products
+// keep the state's 1e-4 tolerance.  The fp32 state itself never leaves the
 // registers of the CTA (thread (row r, half h) holds S̄[r][64h .. 64h + 63]); the
 // decay e^{Λ_C} and the rank-32 term are added there, and the bf16 terms of the
 // new S̄ are written back to shared memory for the next chunk.  The forward
-// substitution for u (a chain over the chunk's tokens) and the outputs run on
-// the CUDA cores, one thread per value row.
+// substitution for u (a chain over the chunk's tokens) runs on the CUDA cores,
+// one thread per value row.
 //
 // One CTA of 256 threads per slot-head.  Warp w reads tensor-memory lanes
 // 32 (w % 4) .. +31, i.e. value rows r = 32 (w % 4) + lane.  Thread 0 issues the
@@ -38,8 +40,8 @@ namespace {
 constexpr int TC_C = 32;           // tokens per chunk
 constexpr int TC_THREADS = 256;
 constexpr int TC_D = 128;          // d_k = d_v
-constexpr uint32_t TC_COLS = 256;  // TMEM columns: D0 [0, 32), D1 [32, 96), D2 [128, 256)
-constexpr uint32_t D0_COL = 0, D1_COL = 32, D2_COL = 128;
+constexpr uint32_t TC_COLS = 256;  // TMEM columns: D0 [0, 32), D1 [32, 96), D3 [96, 128), D2 [128, 256)
+constexpr uint32_t D0_COL = 0, D1_COL = 32, D3_COL = 96, D2_COL = 128;
 // Row strides: v rows padded to 136 bf16 (272 bytes: a warp's staging stores of
 // 8 rows x 64 bytes spread over all banks); pair-coefficient rows of 36 floats
 // (16-byte aligned, read as float4 broadcasts).
@@ -51,20 +53,24 @@ struct TcSmem {
   static constexpr uint32_t SLO = SHI + TC_D * TC_D * 2;   // S̄ lo
   static constexpr uint32_t KQ = SLO + TC_D * TC_D * 2;    // rows 0-31 k_j, 32-63 q_j, 64-127 zero
   static constexpr uint32_t KT = KQ + TC_D * TC_D * 2;     // K as [i (128)] x [j (32)], K-major
-  static constexpr uint32_t UHI = KT + TC_D * TC_C * 2;    // U hi [v (128)] x [j (32)], K-major
+  static constexpr uint32_t WHI = KT + TC_D * TC_C * 2;    // W hi [v (128)] x [j (32)], K-major
+  static constexpr uint32_t WLO = WHI + TC_D * TC_C * 2;   // W lo
+  static constexpr uint32_t UHI = WLO + TC_D * TC_C * 2;   // U hi [v (128)] x [i (32)], K-major
   static constexpr uint32_t ULO = UHI + TC_D * TC_C * 2;   // U lo
-  static constexpr uint32_t VS = ULO + TC_D * TC_C * 2;    // v_j[r] bf16, rows of VP
+  static constexpr uint32_t AHI = ULO + TC_D * TC_C * 2;   // A hi [j (32)] x [i (32)], K-major
+  static constexpr uint32_t ALO = AHI + TC_C * TC_C * 2;   // A lo
+  static constexpr uint32_t VS = ALO + TC_C * TC_C * 2;    // v_j[r] bf16, rows of VP
   static constexpr uint32_t AKK = VS + TC_C * VP * 2;      // fp32 [32][AP], 16-byte rows
-  static constexpr uint32_t AKQ = AKK + TC_C * AP * 4;     // fp32 [32][AP]
-  static constexpr uint32_t US = AKQ + TC_C * AP * 4;      // u fp32 [128][33]
-  static constexpr uint32_t SC = US + TC_D * 33 * 4;       // Λ_j, e^{Λ_j}, e^{Λ_C-Λ_j}, β_j: [4][32] fp32
+  static constexpr uint32_t SC = AKK + TC_C * AP * 4;      // Λ_j, e^{Λ_j}, e^{Λ_C-Λ_j}, β_j: [4][32] fp32
   static constexpr uint32_t BAR = SC + 4 * TC_C * 4;       // 2 mbarriers, TMEM base, ok flag
   static constexpr uint32_t BYTES = BAR + 32;
 };
 static_assert(TcSmem::BYTES <= 227 * 1024, "shared memory");
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo_elem, float hi_elem) {
-  return (uint32_t)f2bf16(lo_elem) | ((uint32_t)f2bf16(hi_elem) << 16);
+// Two fp32 values rounded to bf16 as one word (first value in the low half).
+__device__ __forceinline__ uint32_t bf16x2(float a, float b) {
+  const __nv_bfloat162 p = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&p);
 }
 
 // 8 consecutive fp32 values -> the bf16 high parts (h) and low parts (l).
@@ -73,9 +79,8 @@ __device__ __forceinline__ void split8(const float* x, uint4& h, uint4& l) {
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     const float a = x[2 * e], b = x[2 * e + 1];
-    const float ah = bf16f(f2bf16(a)), bh = bf16f(f2bf16(b));
-    hw[e] = pack_bf16x2(ah, bh);
-    lw[e] = pack_bf16x2(a - ah, b - bh);
+    hw[e] = bf16x2(a, b);
+    lw[e] = bf16x2(a - __uint_as_float(hw[e] << 16), b - __uint_as_float(hw[e] & 0xffff0000u));
   }
   h = make_uint4(hw[0], hw[1], hw[2], hw[3]);
   l = make_uint4(lw[0], lw[1], lw[2], lw[3]);
@@ -139,35 +144,6 @@ struct TcStage {
   }
 };
 
-// Outputs o_j = scale (e^{Λ_j} pq_j + Σ_{i<=j} A_kq[j][i] u_i) of row r for the
-// tokens j = P, P + 2, ... below Cc (the two halves of the CTA take the two parities).
-template <int P>
-__device__ __forceinline__ void outputs_parity(const float (&u)[TC_C], const float (&pq)[TC_C],
-                                               const float* __restrict__ El, const float* __restrict__ Akq,
-                                               void* o, int out_bf16, float scale, size_t obase,
-                                               size_t ostride, int Cc) {
-#pragma unroll
-  for (int j2 = 0; j2 < TC_C / 2; ++j2) {
-    const int j = 2 * j2 + P;
-    if (j < Cc) {
-      float y[4] = {El[j] * pq[j], 0.f, 0.f, 0.f};
-      // coefficients past the diagonal are zero, so whole quads can be used
-#pragma unroll
-      for (int i4 = 0; i4 <= j / 4; ++i4) {
-        const float4 c = *reinterpret_cast<const float4*>(Akq + j * AP + 4 * i4);
-        y[0] += c.x * u[4 * i4];
-        y[1] += c.y * u[4 * i4 + 1];
-        y[2] += c.z * u[4 * i4 + 2];
-        y[3] += c.w * u[4 * i4 + 3];
-      }
-      const float yo = scale * ((y[0] + y[1]) + (y[2] + y[3]));
-      const size_t oi = obase + (size_t)j * ostride;
-      if (out_bf16) static_cast<uint16_t*>(o)[oi] = f2bf16(yo);
-      else static_cast<float*>(o)[oi] = yo;
-    }
-  }
-}
-
 __global__ void __launch_bounds__(TC_THREADS, 1)
 prefill_gdn_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* __restrict__ q,
                       const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
@@ -175,8 +151,6 @@ prefill_gdn_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* __
                       int out_bf16, float scale, int32_t* status) {
   extern __shared__ __align__(1024) unsigned char sm[];
   float* Akk = reinterpret_cast<float*>(sm + TcSmem::AKK);
-  float* Akq = reinterpret_cast<float*>(sm + TcSmem::AKQ);
-  float* Us = reinterpret_cast<float*>(sm + TcSmem::US);
   float* Lm = reinterpret_cast<float*>(sm + TcSmem::SC);
   float* El = Lm + TC_C;
   float* Ew = El + TC_C;
@@ -288,34 +262,45 @@ prefill_gdn_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* __
       break;
     }
     tc::fence_after_sync();
-    // ---- read D0 (warps 0, 1: pair products with their decays) and D1
-    float pk[TC_C], pq[TC_C];
-    {
+    // ---- S̄ k_j (warps 0-3, for the substitution); the pair products with
+    //      their decays (warps 0, 1, 4, 5: D0 rows 0-63, 16 columns each):
+    //      A_kk[j][i] = e^{Λ_j-Λ_i} k_i·k_j (i < j) as fp32 rows, and
+    //      A[j][i] = e^{Λ_j-Λ_i} k_i·q_j (i <= j) as the bf16 terms of D3's B operand
+    float pk[TC_C];
+    if (hw == 0) {
       uint32_t x[TC_C];
-      tc::tmem_ld32(tlane + D1_COL + TC_C, x);   // S̄ q_j
+      tc::tmem_ld32(tlane + D1_COL, x);
       tc::tmem_wait_ld(x);
 #pragma unroll
-      for (int j = 0; j < TC_C; ++j) pq[j] = __uint_as_float(x[j]);
-      if (hw == 0) {
-        tc::tmem_ld32(tlane + D1_COL, x);        // S̄ k_j
-        tc::tmem_wait_ld(x);
+      for (int j = 0; j < TC_C; ++j) pk[j] = __uint_as_float(x[j]);
+    }
+    if (q4 < 2) {
+      uint32_t x[16];
+      tc::tmem_ld16(tlane + D0_COL + 16 * hw, x);
+      tc::tmem_wait_ld16(x);
+      const int j = lane, i0 = 16 * hw;
+      const float lj = Lm[j];
+      float w[16];
 #pragma unroll
-        for (int j = 0; j < TC_C; ++j) pk[j] = __uint_as_float(x[j]);
+      for (int e = 0; e < 16; ++e) {
+        const int i = i0 + e;
+        const bool live = (q4 == 0 ? i < j : i <= j) && j < Cc;
+        w[e] = live ? __uint_as_float(x[e]) * __expf(lj - Lm[i]) : 0.f;   // exponent <= 0
       }
-      if (warp < 2) {
-        tc::tmem_ld32(tlane + D0_COL, x);        // row j = lane: k_j·k_i (warp 0), q_j·k_i (warp 1)
-        tc::tmem_wait_ld(x);
-        const int j = lane;
-        const float lj = Lm[j];
-        float* A = warp == 0 ? Akk : Akq;
+      if (q4 == 0) {
 #pragma unroll
-        for (int i = 0; i < AP; ++i) {
-          if (i >= TC_C) {   // row padding: zero, read by the quad loads
-            A[j * AP + i] = 0.f;
-            continue;
-          }
-          const bool live = (warp == 0 ? i < j : i <= j) && j < Cc;
-          A[j * AP + i] = live ? __uint_as_float(x[i]) * expf(lj - Lm[i]) : 0.f;   // exponent <= 0
+        for (int e4 = 0; e4 < 4; ++e4)
+          *reinterpret_cast<float4*>(Akk + j * AP + i0 + 4 * e4) =
+              make_float4(w[4 * e4], w[4 * e4 + 1], w[4 * e4 + 2], w[4 * e4 + 3]);
+        if (hw == 1) *reinterpret_cast<float4*>(Akk + j * AP + TC_C) = make_float4(0.f, 0.f, 0.f, 0.f);
+      } else {
+#pragma unroll
+        for (int c8 = 0; c8 < 2; ++c8) {
+          uint4 hv, lv;
+          split8(w + 8 * c8, hv, lv);
+          const uint32_t off = tc::kmaj_off(j, i0 + 8 * c8, TC_C);
+          *reinterpret_cast<uint4*>(sm + TcSmem::AHI + off) = hv;
+          *reinterpret_cast<uint4*>(sm + TcSmem::ALO + off) = lv;
         }
       }
     }
@@ -344,40 +329,43 @@ prefill_gdn_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* __
 #pragma unroll
         for (int e = 0; e < 8; ++e) w8[e] = u[8 * c8 + e] * Ew[8 * c8 + e];
         uint4 hv, lv;
-        split8(w8, hv, lv);
         const uint32_t off = tc::kmaj_off(r, 8 * c8, TC_C);
+        split8(w8, hv, lv);
+        *reinterpret_cast<uint4*>(sm + TcSmem::WHI + off) = hv;
+        *reinterpret_cast<uint4*>(sm + TcSmem::WLO + off) = lv;
+        split8(u + 8 * c8, hv, lv);
         *reinterpret_cast<uint4*>(sm + TcSmem::UHI + off) = hv;
         *reinterpret_cast<uint4*>(sm + TcSmem::ULO + off) = lv;
       }
-#pragma unroll
-      for (int j = 0; j < TC_C; ++j) Us[r * 33 + j] = u[j];
     }
-    tc::fence_smem_to_async();   // U terms, for the tensor cores
+    tc::fence_smem_to_async();   // W, U terms, for the tensor cores
     tc::fence_before_sync();
     __syncthreads();
-    // ---- D2 = (U_hi + U_lo) K, while the outputs are computed
+    // ---- D2 = (W_hi + W_lo) K and D3 = U_hi A_hi^T + U_lo A_hi^T + U_hi A_lo^T
     if (tid == 0) {
       tc::fence_after_sync();
-      constexpr uint32_t id2 = tc::idesc_bf16_f32(128, 128);
+      constexpr uint32_t id2 = tc::idesc_bf16_f32(128, 128), id3 = tc::idesc_bf16_f32(128, 32);
 #pragma unroll
       for (int kk = 0; kk < TC_C / 16; ++kk)
-        tc::mma_bf16(tm + D2_COL, tc::kmaj_desc(sbase + TcSmem::UHI, TC_C, kk),
+        tc::mma_bf16(tm + D2_COL, tc::kmaj_desc(sbase + TcSmem::WHI, TC_C, kk),
                      tc::kmaj_desc(sbase + TcSmem::KT, TC_C, kk), id2, kk > 0);
 #pragma unroll
       for (int kk = 0; kk < TC_C / 16; ++kk)
-        tc::mma_bf16(tm + D2_COL, tc::kmaj_desc(sbase + TcSmem::ULO, TC_C, kk),
+        tc::mma_bf16(tm + D2_COL, tc::kmaj_desc(sbase + TcSmem::WLO, TC_C, kk),
                      tc::kmaj_desc(sbase + TcSmem::KT, TC_C, kk), id2, 1u);
-      tc::mma_commit(bar2);
-    }
-    if (o != nullptr) {
-      const size_t obase = ((size_t)t0 * nH + sh) * TC_D + r, ostride = nH * TC_D;
-      if (hw == 0) {
-        outputs_parity<0>(u, pq, El, Akq, o, out_bf16, scale, obase, ostride, Cc);
-      } else {
 #pragma unroll
-        for (int j = 0; j < TC_C; ++j) u[j] = Us[r * 33 + j];
-        outputs_parity<1>(u, pq, El, Akq, o, out_bf16, scale, obase, ostride, Cc);
-      }
+      for (int kk = 0; kk < TC_C / 16; ++kk)
+        tc::mma_bf16(tm + D3_COL, tc::kmaj_desc(sbase + TcSmem::UHI, TC_C, kk),
+                     tc::kmaj_desc(sbase + TcSmem::AHI, TC_C, kk), id3, kk > 0);
+#pragma unroll
+      for (int kk = 0; kk < TC_C / 16; ++kk)
+        tc::mma_bf16(tm + D3_COL, tc::kmaj_desc(sbase + TcSmem::ULO, TC_C, kk),
+                     tc::kmaj_desc(sbase + TcSmem::AHI, TC_C, kk), id3, 1u);
+#pragma unroll
+      for (int kk = 0; kk < TC_C / 16; ++kk)
+        tc::mma_bf16(tm + D3_COL, tc::kmaj_desc(sbase + TcSmem::UHI, TC_C, kk),
+                     tc::kmaj_desc(sbase + TcSmem::ALO, TC_C, kk), id3, 1u);
+      tc::mma_commit(bar2);
     }
     if (tid == 0 && !mbar_wait(bar2, par, status, DEV_TIMEOUT_MMA)) *ok_flag = -2;
     __syncthreads();
@@ -386,6 +374,27 @@ prefill_gdn_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* __
       break;
     }
     tc::fence_after_sync();
+    // ---- outputs of tokens 16 h .. 16 h + 15 of row r:
+    //      o_j = scale (e^{Λ_j} S̄ q_j + Σ_{i<=j} A[j][i] u_i)
+    if (o != nullptr) {
+      uint32_t xq[16], x3[16];
+      tc::tmem_ld16(tlane + D1_COL + TC_C + 16 * hw, xq);
+      tc::tmem_ld16(tlane + D3_COL + 16 * hw, x3);
+      tc::tmem_wait_ld16(xq);
+      tc::tmem_wait_ld16(x3);
+      const size_t ostride = nH * TC_D;
+      const size_t obase = ((size_t)(t0 + 16 * hw) * nH + sh) * TC_D + r;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int j = 16 * hw + e;
+        if (j < Cc) {
+          const float yo = scale * (El[j] * __uint_as_float(xq[e]) + __uint_as_float(x3[e]));
+          const size_t oi = obase + (size_t)e * ostride;
+          if (out_bf16) static_cast<uint16_t*>(o)[oi] = f2bf16(yo);
+          else static_cast<float*>(o)[oi] = yo;
+        }
+      }
+    }
     // ---- S̄ <- e^{Λ_C} S̄ + D2 in registers; its bf16 terms for the next chunk
     {
       const float eC = El[Cc - 1];
