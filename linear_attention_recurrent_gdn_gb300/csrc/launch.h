@@ -86,13 +86,16 @@ cudaError_t launch_checkpoint(int op, int dk, const CkptArgs& a, cudaStream_t s)
 
 // Chunked prefill of T tokens: token-major inputs [T, rows, H, d]; `bonus`
 // [H, d_k] for RWKV6.
-// GDN at d_k = d_v = 128 runs on the tensor cores (prefill_tc.cu); a bounded
+// GDN and KDA at d_k = d_v = 128 run on the tensor cores (prefill_tc.cu); a bounded
 // wait there that runs out records DEV_TIMEOUT_MMA in `status`.
 cudaError_t launch_prefill(int op, int dk, const SlotListArgs& a, const void* q, const void* k,
                            const void* v, const float* g, const float* beta, const float* bonus,
                            void* o, int T, int out_bf16, float scale, int32_t* status,
                            cudaStream_t s);
 cudaError_t launch_prefill_gdn_tc(const SlotListArgs& a, const void* q, const void* k,
+                                  const void* v, const float* g, const float* beta, void* o, int T,
+                                  int out_bf16, float scale, int32_t* status, cudaStream_t s);
+cudaError_t launch_prefill_kda_tc(const SlotListArgs& a, const void* q, const void* k,
                                   const void* v, const float* g, const float* beta, void* o, int T,
                                   int out_bf16, float scale, int32_t* status, cudaStream_t s);
 

@@ -710,7 +710,7 @@ cudaError_t launch_prefill(int op, int dk, const SlotListArgs& a, const void* q,
   }
   if (op == KDA) {
     if (dk == 64) return pk_dispatch<KDA, 64>(a, q, k, v, g, beta, bonus, o, T, out_bf16, scale, s);
-    return pk_dispatch<KDA, 128>(a, q, k, v, g, beta, bonus, o, T, out_bf16, scale, s);
+    return launch_prefill_kda_tc(a, q, k, v, g, beta, o, T, out_bf16, scale, status, s);
   }
   if (dk == 64) return pk_dispatch<RWKV6, 64>(a, q, k, v, g, beta, bonus, o, T, out_bf16, scale, s);
   return pk_dispatch<RWKV6, 128>(a, q, k, v, g, beta, bonus, o, T, out_bf16, scale, s);

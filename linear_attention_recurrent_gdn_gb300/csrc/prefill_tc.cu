@@ -46,6 +46,7 @@ constexpr uint32_t D0_COL = 0, D1_COL = 32, D3_COL = 96, D2_COL = 128;
 // 8 rows x 64 bytes spread over all banks); pair-coefficient rows of 36 floats
 // (16-byte aligned, read as float4 broadcasts).
 constexpr int VP = TC_D + 8, AP = 36;
+constexpr int LPAD = TC_D + 4;   // fp32 rows of k, q, Λ (KDA): quad loads of rows ig, jg spread over banks
 
 // Byte offsets in the dynamic shared memory (operands 16-byte aligned).
 struct TcSmem {
@@ -442,6 +443,428 @@ prefill_gdn_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* __
   }
 }
 
+// ------------------------------------------------------------------- KDA ----
+// KDA (per-key decay, delta rule) at d_k = d_v = 128.  With Λ_j the per-channel
+// cumulative log-decay inside the chunk (Λ_j[c] = Σ_{i<=j} g_i[c]):
+//   x_j = S̄ k̂_j + Σ_{i<j} A_kk[j][i] u_i,  u_j = β_j (v_j - x_j),  k̂_j = e^{Λ_j} ⊙ k_j
+//   o_j = S̄ q̂_j + Σ_{i<=j} A[j][i] u_i,                            q̂_j = e^{Λ_j} ⊙ q_j
+//   A_kk[j][i] = Σ_c k_i[c] k_j[c] e^{Λ_j[c]-Λ_i[c]},  A[j][i] likewise with q_j
+//   S̄' = S̄ Diag(e^{Λ_C}) + Σ_j u_j k̃_j^T,            k̃_j = e^{Λ_C-Λ_j} ⊙ k_j
+// on the tensor cores:
+//   D1 [128 x 64]  = S̄ [k̂; q̂]^T    three terms: S̄_hi B_hi + S̄_lo B_hi + S̄_hi B_lo
+//   D2 [128 x 128] = U k̃            three terms
+//   D3 [128 x 32]  = U A^T           three terms
+// The pair coefficients A_kk, A need one exponential per channel and pair, so
+// they stay on the CUDA cores; they run while D1 is on the tensor cores.
+struct KdaSmem {
+  static constexpr uint32_t SHI = 0;                        // S̄ hi [128 x 128] K-major
+  static constexpr uint32_t SLO = SHI + TC_D * TC_D * 2;
+  static constexpr uint32_t BHI = SLO + TC_D * TC_D * 2;    // [k̂; q̂] hi [64 x 128] K-major
+  static constexpr uint32_t BLO = BHI + 2 * TC_C * TC_D * 2;
+  static constexpr uint32_t KTHI = BLO + 2 * TC_C * TC_D * 2;  // k̃ hi as [c (128)] x [j (32)]
+  static constexpr uint32_t KTLO = KTHI + TC_D * TC_C * 2;
+  static constexpr uint32_t UHI = KTLO + TC_D * TC_C * 2;   // U hi [v (128)] x [i (32)]
+  static constexpr uint32_t ULO = UHI + TC_D * TC_C * 2;
+  static constexpr uint32_t AHI = ULO + TC_D * TC_C * 2;    // A hi [j (32)] x [i (32)]
+  static constexpr uint32_t ALO = AHI + TC_C * TC_C * 2;
+  static constexpr uint32_t VS = ALO + TC_C * TC_C * 2;     // v_j[r] bf16, rows of VP
+  static constexpr uint32_t KP = VS + TC_C * VP * 2;        // k_j[c] fp32, rows of LPAD
+  static constexpr uint32_t QP = KP + TC_C * LPAD * 4;      // q_j[c] fp32
+  static constexpr uint32_t LP = QP + TC_C * LPAD * 4;      // g, then Λ_j[c] fp32
+  static constexpr uint32_t AKK = LP + TC_C * LPAD * 4;     // A_kk fp32 [32][AP]
+  static constexpr uint32_t EC = AKK + TC_C * AP * 4;       // e^{Λ_C[c]} [128]
+  static constexpr uint32_t BT = EC + TC_D * 4;             // β_j [32]
+  static constexpr uint32_t BAR = BT + TC_C * 4;            // 2 mbarriers, TMEM base, ok flag
+  static constexpr uint32_t BYTES = BAR + 32;
+};
+static_assert(KdaSmem::BYTES <= 227 * 1024, "shared memory");
+
+// One channel quad of KDA's decay-weighted pair products for token pair (j, i):
+// with w_c = e^{Λ_j[c] - Λ_i[c]}, kk += Σ k_i[c] w_c k_j[c] and qk += Σ k_i[c] w_c q_j[c].
+// A pair that is not live gets exponent 0, so its unused sums stay finite.
+__device__ __forceinline__ void kda_pair_quad(float& kk, float& qk, const float4 ki, const float4 li,
+                                              const float4 lj, const float4 kj, const float4 qj,
+                                              bool live) {
+  const float w0 = __expf(live ? lj.x - li.x : 0.f), w1 = __expf(live ? lj.y - li.y : 0.f);
+  const float w2 = __expf(live ? lj.z - li.z : 0.f), w3 = __expf(live ? lj.w - li.w : 0.f);
+  const float a0 = ki.x * w0, a1 = ki.y * w1, a2 = ki.z * w2, a3 = ki.w * w3;
+  kk += a0 * kj.x + a1 * kj.y + a2 * kj.z + a3 * kj.w;
+  qk += a0 * qj.x + a1 * qj.y + a2 * qj.z + a3 * qj.w;
+}
+
+// KDA chunk inputs in registers: k, q, v (bf16) as in TcStage, the g rows as
+// float4 (4 per thread: row j = idx / 32, channel quad idx % 32), and β.
+struct KdaStage {
+  uint4 k[2], q[2], v[2];
+  float4 gv[4];
+  float b;
+
+  __device__ __forceinline__ void load(const uint16_t* __restrict__ qg, const uint16_t* __restrict__ kg,
+                                       const uint16_t* __restrict__ vg, const float* __restrict__ gg,
+                                       const float* __restrict__ bg, int t0, int Cc, size_t nH,
+                                       int sh, int tid) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      int j, cv;
+      TcStage::piece(tid + e * TC_THREADS, j, cv);
+      if (j < Cc) {
+        const size_t base = ((size_t)(t0 + j) * nH + sh) * TC_D + cv * 8;
+        k[e] = *reinterpret_cast<const uint4*>(kg + base);
+        q[e] = *reinterpret_cast<const uint4*>(qg + base);
+        v[e] = *reinterpret_cast<const uint4*>(vg + base);
+      } else {
+        k[e] = q[e] = v[e] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int idx = tid + e * TC_THREADS, j = idx >> 5, c4 = idx & 31;
+      gv[e] = j < Cc ? *reinterpret_cast<const float4*>(gg + ((size_t)(t0 + j) * nH + sh) * TC_D + 4 * c4)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (tid < 32) b = tid < Cc ? bg[(size_t)(t0 + tid) * nH + sh] : 0.f;
+  }
+
+  static __device__ __forceinline__ void put8(float* dst, const uint4 w) {
+    *reinterpret_cast<float4*>(dst) =
+        make_float4(bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y));
+    *reinterpret_cast<float4*>(dst + 4) =
+        make_float4(bf16lo(w.z), bf16hi(w.z), bf16lo(w.w), bf16hi(w.w));
+  }
+
+  // k, q as fp32 rows, v as bf16 rows, g rows (scanned in place later), β
+  __device__ __forceinline__ void store(unsigned char* sm, int tid) const {
+    float* Kp = reinterpret_cast<float*>(sm + KdaSmem::KP);
+    float* Qp = reinterpret_cast<float*>(sm + KdaSmem::QP);
+    float* Lp = reinterpret_cast<float*>(sm + KdaSmem::LP);
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      int j, cv;
+      TcStage::piece(tid + e * TC_THREADS, j, cv);
+      put8(Kp + j * LPAD + cv * 8, k[e]);
+      put8(Qp + j * LPAD + cv * 8, q[e]);
+      *reinterpret_cast<uint4*>(sm + KdaSmem::VS + (j * VP + cv * 8) * 2) = v[e];
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int idx = tid + e * TC_THREADS, j = idx >> 5, c4 = idx & 31;
+      *reinterpret_cast<float4*>(Lp + j * LPAD + 4 * c4) = gv[e];
+    }
+    if (tid < 32) reinterpret_cast<float*>(sm + KdaSmem::BT)[tid] = b;   // 0 past Cc
+  }
+};
+
+__global__ void __launch_bounds__(TC_THREADS, 1)
+prefill_kda_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* __restrict__ q,
+                      const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
+                      const float* __restrict__ g, const float* __restrict__ beta, void* o, int T,
+                      int out_bf16, float scale, int32_t* status) {
+  extern __shared__ __align__(1024) unsigned char sm[];
+  const float* Kp = reinterpret_cast<const float*>(sm + KdaSmem::KP);
+  const float* Qp = reinterpret_cast<const float*>(sm + KdaSmem::QP);
+  float* Lp = reinterpret_cast<float*>(sm + KdaSmem::LP);
+  float* Akk = reinterpret_cast<float*>(sm + KdaSmem::AKK);
+  float* Ec = reinterpret_cast<float*>(sm + KdaSmem::EC);
+  const float* Bt = reinterpret_cast<const float*>(sm + KdaSmem::BT);
+  const uint16_t* Vs = reinterpret_cast<const uint16_t*>(sm + KdaSmem::VS);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + KdaSmem::BAR + 16);
+  int32_t* ok_flag = reinterpret_cast<int32_t*>(sm + KdaSmem::BAR + 20);
+  const uint32_t sbase = smem_u32(sm);
+  const uint32_t bar1 = sbase + KdaSmem::BAR, bar2 = sbase + KdaSmem::BAR + 8;
+  constexpr uint32_t K_D1 = 0, K_D3 = 64, K_D2 = 128;   // TMEM columns
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int q4 = warp & 3, hw = warp >> 2;
+  const int r = 32 * q4 + lane;
+  const int sh = blockIdx.x, row = sh / a.H, h = sh - row * a.H;
+  const int slot = a.items[row].slot;
+  const size_t nH = (size_t)a.rows * a.H;
+  float* gS = a.Sbar + ((size_t)slot * a.H + h) * TC_D * TC_D;
+
+  if (warp == 0) tc::tmem_alloc(sbase + KdaSmem::BAR + 16, TC_COLS);
+  if (tid == 0) {
+    mbar_init(bar1, 1);
+    mbar_init(bar2, 1);
+    fence_mbar_init();
+    *ok_flag = 1;
+  }
+  float S[64];
+  {
+    const float4* src = reinterpret_cast<const float4*>(gS + (size_t)r * TC_D + 64 * hw);
+#pragma unroll
+    for (int c4 = 0; c4 < 16; ++c4) {
+      const float4 x = src[c4];
+      S[4 * c4] = x.x;
+      S[4 * c4 + 1] = x.y;
+      S[4 * c4 + 2] = x.z;
+      S[4 * c4 + 3] = x.w;
+    }
+#pragma unroll
+    for (int c8 = 0; c8 < 8; ++c8) {
+      uint4 hv, lv;
+      split8(S + 8 * c8, hv, lv);
+      const uint32_t off = tc::kmaj_off(r, 64 * hw + 8 * c8, TC_D);
+      *reinterpret_cast<uint4*>(sm + KdaSmem::SHI + off) = hv;
+      *reinterpret_cast<uint4*>(sm + KdaSmem::SLO + off) = lv;
+    }
+  }
+  KdaStage st;
+  st.load(q, k, v, g, beta, 0, T < TC_C ? T : TC_C, nH, sh, tid);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tm = *tmem_slot;
+  const uint32_t tlane = tm + ((uint32_t)(32 * q4) << 16);
+  bool ok = true;
+  int chunk = 0;
+  for (int t0 = 0; t0 < T && ok; t0 += TC_C, ++chunk) {
+    const int Cc = (T - t0) < TC_C ? (T - t0) : TC_C;
+    const uint32_t par = (uint32_t)chunk & 1u;
+    // ---- stage; Λ = inclusive scan of g down each channel (padding tokens: g = 0)
+    st.store(sm, tid);
+    __syncthreads();
+    if (tid < TC_D) {
+      float acc = 0.f;
+#pragma unroll 8
+      for (int j = 0; j < TC_C; ++j) {
+        acc += Lp[j * LPAD + tid];
+        Lp[j * LPAD + tid] = acc;
+      }
+      Ec[tid] = expf(acc);
+    }
+    __syncthreads();
+    // ---- decayed operands, 8 channels of one token per piece:
+    //      [k̂_j; q̂_j] (hi, lo) and k̃_j (hi, lo; zero past Cc) transposed
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      int j, cv;
+      TcStage::piece(tid + e * TC_THREADS, j, cv);
+      float kh[8], qh[8], kt[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const int c = cv * 8 + t;
+        const float lj = Lp[j * LPAD + c];
+        const float el = __expf(lj);                                      // Λ <= 0
+        const float ew = j < Cc ? __expf(Lp[(Cc - 1) * LPAD + c] - lj) : 0.f;   // Λ_C - Λ_j <= 0
+        const float kc = Kp[j * LPAD + c];
+        kh[t] = el * kc;
+        qh[t] = el * Qp[j * LPAD + c];
+        kt[t] = ew * kc;
+      }
+      uint4 hv, lv;
+      split8(kh, hv, lv);
+      *reinterpret_cast<uint4*>(sm + KdaSmem::BHI + tc::kmaj_off(j, cv * 8, TC_D)) = hv;
+      *reinterpret_cast<uint4*>(sm + KdaSmem::BLO + tc::kmaj_off(j, cv * 8, TC_D)) = lv;
+      split8(qh, hv, lv);
+      *reinterpret_cast<uint4*>(sm + KdaSmem::BHI + tc::kmaj_off(TC_C + j, cv * 8, TC_D)) = hv;
+      *reinterpret_cast<uint4*>(sm + KdaSmem::BLO + tc::kmaj_off(TC_C + j, cv * 8, TC_D)) = lv;
+      split8(kt, hv, lv);
+      const uint32_t hw4[4] = {hv.x, hv.y, hv.z, hv.w}, lw4[4] = {lv.x, lv.y, lv.z, lv.w};
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {   // k̃_j[c] at row c, column j
+        const uint32_t off = tc::kmaj_off(cv * 8 + t, j, TC_C);
+        *reinterpret_cast<uint16_t*>(sm + KdaSmem::KTHI + off) =
+            (uint16_t)((t & 1) ? (hw4[t >> 1] >> 16) : (hw4[t >> 1] & 0xffffu));
+        *reinterpret_cast<uint16_t*>(sm + KdaSmem::KTLO + off) =
+            (uint16_t)((t & 1) ? (lw4[t >> 1] >> 16) : (lw4[t >> 1] & 0xffffu));
+      }
+    }
+    tc::fence_smem_to_async();   // S̄ terms, [k̂; q̂] and k̃ terms, for the tensor cores
+    tc::fence_before_sync();
+    __syncthreads();
+    // ---- D1 = S̄ [k̂; q̂]^T on the tensor cores ...
+    if (tid == 0) {
+      tc::fence_after_sync();
+      constexpr uint32_t id1 = tc::idesc_bf16_f32(128, 64);
+#pragma unroll
+      for (int kk = 0; kk < TC_D / 16; ++kk)
+        tc::mma_bf16(tm + K_D1, tc::kmaj_desc(sbase + KdaSmem::SHI, TC_D, kk),
+                     tc::kmaj_desc(sbase + KdaSmem::BHI, TC_D, kk), id1, kk > 0);
+#pragma unroll
+      for (int kk = 0; kk < TC_D / 16; ++kk)
+        tc::mma_bf16(tm + K_D1, tc::kmaj_desc(sbase + KdaSmem::SLO, TC_D, kk),
+                     tc::kmaj_desc(sbase + KdaSmem::BHI, TC_D, kk), id1, 1u);
+#pragma unroll
+      for (int kk = 0; kk < TC_D / 16; ++kk)
+        tc::mma_bf16(tm + K_D1, tc::kmaj_desc(sbase + KdaSmem::SHI, TC_D, kk),
+                     tc::kmaj_desc(sbase + KdaSmem::BLO, TC_D, kk), id1, 1u);
+      tc::mma_commit(bar1);
+    }
+    // ... while the CUDA cores form the pair coefficients: pairs (jg + 16x,
+    // ig + 16y) per thread, (x, y) = (0, 1) lies above the diagonal; a dead
+    // pair's exponent is replaced by 0 so that its unused sums stay finite
+    {
+      const int jg = tid >> 4, ig = tid & 15;
+      const int j0 = jg, j1 = jg + 16, i0 = ig, i1 = ig + 16;
+      const bool dl = ig <= jg;
+      float kk3[3] = {0.f, 0.f, 0.f}, qk3[3] = {0.f, 0.f, 0.f};   // pairs (0,0), (1,0), (1,1)
+#pragma unroll 2
+      for (int c = 0; c < TC_D; c += 4) {
+        const float4 ki0 = *reinterpret_cast<const float4*>(Kp + i0 * LPAD + c);
+        const float4 ki1 = *reinterpret_cast<const float4*>(Kp + i1 * LPAD + c);
+        const float4 li0 = *reinterpret_cast<const float4*>(Lp + i0 * LPAD + c);
+        const float4 li1 = *reinterpret_cast<const float4*>(Lp + i1 * LPAD + c);
+        const float4 lj0 = *reinterpret_cast<const float4*>(Lp + j0 * LPAD + c);
+        const float4 lj1 = *reinterpret_cast<const float4*>(Lp + j1 * LPAD + c);
+        const float4 kj0 = *reinterpret_cast<const float4*>(Kp + j0 * LPAD + c);
+        const float4 kj1 = *reinterpret_cast<const float4*>(Kp + j1 * LPAD + c);
+        const float4 qj0 = *reinterpret_cast<const float4*>(Qp + j0 * LPAD + c);
+        const float4 qj1 = *reinterpret_cast<const float4*>(Qp + j1 * LPAD + c);
+        kda_pair_quad(kk3[0], qk3[0], ki0, li0, lj0, kj0, qj0, dl);
+        kda_pair_quad(kk3[1], qk3[1], ki0, li0, lj1, kj1, qj1, true);
+        kda_pair_quad(kk3[2], qk3[2], ki1, li1, lj1, kj1, qj1, dl);
+      }
+      auto put = [&](int j, int i, float kv, float qv, bool live) {
+        const bool ok2 = live && j < Cc;
+        Akk[j * AP + i] = (ok2 && i != j) ? kv : 0.f;
+        const float av = ok2 ? qv : 0.f;
+        const uint32_t hv = bf16x2(av, 0.f) & 0xffffu;
+        const uint32_t lv = bf16x2(av - __uint_as_float(hv << 16), 0.f) & 0xffffu;
+        const uint32_t off = tc::kmaj_off(j, i, TC_C);
+        *reinterpret_cast<uint16_t*>(sm + KdaSmem::AHI + off) = (uint16_t)hv;
+        *reinterpret_cast<uint16_t*>(sm + KdaSmem::ALO + off) = (uint16_t)lv;
+      };
+      put(j0, i0, kk3[0], qk3[0], dl);
+      put(j0, i1, 0.f, 0.f, false);
+      put(j1, i0, kk3[1], qk3[1], true);
+      put(j1, i1, kk3[2], qk3[2], dl);
+      if (tid < TC_C) *reinterpret_cast<float4*>(Akk + tid * AP + TC_C) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (t0 + TC_C < T) {
+      const int Cn = (T - t0 - TC_C) < TC_C ? (T - t0 - TC_C) : TC_C;
+      st.load(q, k, v, g, beta, t0 + TC_C, Cn, nH, sh, tid);
+    }
+    if (tid == 0 && !mbar_wait(bar1, par, status, DEV_TIMEOUT_MMA)) *ok_flag = -1;
+    __syncthreads();
+    if (*ok_flag != 1) {
+      ok = false;
+      break;
+    }
+    tc::fence_after_sync();
+    // ---- forward substitution (warps 0-3, one value row each)
+    if (hw == 0) {
+      float pk[TC_C], u[TC_C];
+      {
+        uint32_t x[TC_C];
+        tc::tmem_ld32(tlane + K_D1, x);
+        tc::tmem_wait_ld(x);
+#pragma unroll
+        for (int j = 0; j < TC_C; ++j) pk[j] = __uint_as_float(x[j]);
+      }
+#pragma unroll
+      for (int j = 0; j < TC_C; ++j) u[j] = 0.f;
+#pragma unroll
+      for (int j = 0; j < TC_C; ++j) {
+        float x[4] = {pk[j], 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i4 = 0; i4 < (j + 3) / 4; ++i4) {
+          const float4 c = *reinterpret_cast<const float4*>(Akk + j * AP + 4 * i4);
+          x[0] += c.x * u[4 * i4];
+          x[1] += c.y * u[4 * i4 + 1];
+          x[2] += c.z * u[4 * i4 + 2];
+          x[3] += c.w * u[4 * i4 + 3];
+        }
+        u[j] = Bt[j] * (bf16f(Vs[j * VP + r]) - ((x[0] + x[1]) + (x[2] + x[3])));   // 0 past Cc
+      }
+#pragma unroll
+      for (int c8 = 0; c8 < TC_C / 8; ++c8) {
+        uint4 hv, lv;
+        split8(u + 8 * c8, hv, lv);
+        const uint32_t off = tc::kmaj_off(r, 8 * c8, TC_C);
+        *reinterpret_cast<uint4*>(sm + KdaSmem::UHI + off) = hv;
+        *reinterpret_cast<uint4*>(sm + KdaSmem::ULO + off) = lv;
+      }
+    }
+    tc::fence_smem_to_async();   // U and A terms, for the tensor cores
+    tc::fence_before_sync();
+    __syncthreads();
+    // ---- D2 = U k̃ and D3 = U A^T, three terms each
+    if (tid == 0) {
+      tc::fence_after_sync();
+      constexpr uint32_t id2 = tc::idesc_bf16_f32(128, 128), id3 = tc::idesc_bf16_f32(128, 32);
+      const uint32_t ua[3] = {KdaSmem::UHI, KdaSmem::ULO, KdaSmem::UHI};
+      const uint32_t kb[3] = {KdaSmem::KTHI, KdaSmem::KTHI, KdaSmem::KTLO};
+      const uint32_t ab[3] = {KdaSmem::AHI, KdaSmem::AHI, KdaSmem::ALO};
+#pragma unroll
+      for (int term = 0; term < 3; ++term)
+#pragma unroll
+        for (int kk = 0; kk < TC_C / 16; ++kk) {
+          tc::mma_bf16(tm + K_D2, tc::kmaj_desc(sbase + ua[term], TC_C, kk),
+                       tc::kmaj_desc(sbase + kb[term], TC_C, kk), id2, (term | kk) != 0);
+          tc::mma_bf16(tm + K_D3, tc::kmaj_desc(sbase + ua[term], TC_C, kk),
+                       tc::kmaj_desc(sbase + ab[term], TC_C, kk), id3, (term | kk) != 0);
+        }
+      tc::mma_commit(bar2);
+    }
+    if (tid == 0 && !mbar_wait(bar2, par, status, DEV_TIMEOUT_MMA)) *ok_flag = -2;
+    __syncthreads();
+    if (*ok_flag != 1) {
+      ok = false;
+      break;
+    }
+    tc::fence_after_sync();
+    // ---- outputs of tokens 16 h .. 16 h + 15 of row r: o_j = scale (S̄ q̂_j + D3)
+    if (o != nullptr) {
+      uint32_t xq[16], x3[16];
+      tc::tmem_ld16(tlane + K_D1 + TC_C + 16 * hw, xq);
+      tc::tmem_ld16(tlane + K_D3 + 16 * hw, x3);
+      tc::tmem_wait_ld16(xq);
+      tc::tmem_wait_ld16(x3);
+      const size_t ostride = nH * TC_D;
+      const size_t obase = ((size_t)(t0 + 16 * hw) * nH + sh) * TC_D + r;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        if (16 * hw + e < Cc) {
+          const float yo = scale * (__uint_as_float(xq[e]) + __uint_as_float(x3[e]));
+          const size_t oi = obase + (size_t)e * ostride;
+          if (out_bf16) static_cast<uint16_t*>(o)[oi] = f2bf16(yo);
+          else static_cast<float*>(o)[oi] = yo;
+        }
+      }
+    }
+    // ---- S̄ <- S̄ Diag(e^{Λ_C}) + D2; its bf16 terms for the next chunk
+    {
+      uint32_t x0[32], x1[32];
+      tc::tmem_ld32(tlane + K_D2 + 64 * hw, x0);
+      tc::tmem_ld32(tlane + K_D2 + 64 * hw + 32, x1);
+      tc::tmem_wait_ld(x0);
+      tc::tmem_wait_ld(x1);
+      const float* ec = Ec + 64 * hw;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        S[c] = ec[c] * S[c] + __uint_as_float(x0[c]);
+        S[32 + c] = ec[32 + c] * S[32 + c] + __uint_as_float(x1[c]);
+      }
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8) {
+        uint4 hv, lv;
+        split8(S + 8 * c8, hv, lv);
+        const uint32_t off = tc::kmaj_off(r, 64 * hw + 8 * c8, TC_D);
+        *reinterpret_cast<uint4*>(sm + KdaSmem::SHI + off) = hv;
+        *reinterpret_cast<uint4*>(sm + KdaSmem::SLO + off) = lv;
+      }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+  }
+  if (!ok && tid == 0) mbar_drain(*ok_flag == -1 ? bar1 : bar2, (uint32_t)chunk & 1u);
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tm, TC_COLS);
+  }
+  if (!ok) return;
+  float4* dst = reinterpret_cast<float4*>(gS + (size_t)r * TC_D + 64 * hw);
+#pragma unroll
+  for (int c4 = 0; c4 < 16; ++c4)
+    dst[c4] = make_float4(S[4 * c4], S[4 * c4 + 1], S[4 * c4 + 2], S[4 * c4 + 3]);
+  if (h == 0 && tid == 0) {
+    a.nlog[slot] = 0;
+    a.base_of[slot] = slot;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_prefill_gdn_tc(const SlotListArgs& a, const void* q, const void* k,
@@ -452,6 +875,19 @@ cudaError_t launch_prefill_gdn_tc(const SlotListArgs& a, const void* q, const vo
                                        (int)TcSmem::BYTES);
   if (e != cudaSuccess) return e;
   prefill_gdn_tc_kernel<<<a.rows * a.H, TC_THREADS, TcSmem::BYTES, s>>>(
+      a, static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(k),
+      static_cast<const uint16_t*>(v), g, beta, o, T, out_bf16, scale, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_kda_tc(const SlotListArgs& a, const void* q, const void* k,
+                                  const void* v, const float* g, const float* beta, void* o, int T,
+                                  int out_bf16, float scale, int32_t* status, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(prefill_kda_tc_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)KdaSmem::BYTES);
+  if (e != cudaSuccess) return e;
+  prefill_kda_tc_kernel<<<a.rows * a.H, TC_THREADS, KdaSmem::BYTES, s>>>(
       a, static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(k),
       static_cast<const uint16_t*>(v), g, beta, o, T, out_bf16, scale, status);
   return cudaGetLastError();
