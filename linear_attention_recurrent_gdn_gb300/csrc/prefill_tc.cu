@@ -450,27 +450,34 @@ prefill_gdn_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* __
 //   o_j = S̄ q̂_j + Σ_{i<=j} A[j][i] u_i,                            q̂_j = e^{Λ_j} ⊙ q_j
 //   A_kk[j][i] = Σ_c k_i[c] k_j[c] e^{Λ_j[c]-Λ_i[c]},  A[j][i] likewise with q_j
 //   S̄' = S̄ Diag(e^{Λ_C}) + Σ_j u_j k̃_j^T,            k̃_j = e^{Λ_C-Λ_j} ⊙ k_j
-// on the tensor cores:
-//   D1 [128 x 64]  = S̄ [k̂; q̂]^T    three terms: S̄_hi B_hi + S̄_lo B_hi + S̄_hi B_lo
-//   D2 [128 x 128] = U k̃            three terms
-//   D3 [128 x 32]  = U A^T           three terms
-// The pair coefficients A_kk, A need one exponential per channel and pair, so
-// they stay on the CUDA cores; they run while D1 is on the tensor cores.
+// The pair weights factor through the chunk start: e^{Λ_j-Λ_i} = e^{Λ_j} e^{-Λ_i},
+// so with k̄_i = e^{-Λ_i} ⊙ k_i the pair coefficients are A_kk = k̂ k̄^T and
+// A = q̂ k̄^T.  For a live pair (i <= j) every channel's product k̂_j[c] k̄_i[c] =
+// k_j[c] k_i[c] e^{Λ_j[c]-Λ_i[c]} is bounded by |k_j[c] k_i[c]|, so nothing
+// cancels; the factors themselves stay finite while the chunk's total decay
+// stays above -60 in every channel (e^{60} ~ 1e26).  A chunk with stronger
+// decay (a block-wide vote after the scan) forms its pair coefficients
+// directly on the CUDA cores, one exponential per channel and pair.
+// On the tensor cores (fp32 operands as hi + lo bf16 terms, three products each):
+//   D0 [128 x 32]  = [k̂; q̂; 0] k̄^T    the pair coefficients (fast chunks)
+//   D1 [128 x 64]  = S̄ [k̂; q̂]^T
+//   D2 [128 x 128] = U k̃
+//   D3 [128 x 32]  = U A^T
 struct KdaSmem {
   static constexpr uint32_t SHI = 0;                        // S̄ hi [128 x 128] K-major
   static constexpr uint32_t SLO = SHI + TC_D * TC_D * 2;
-  static constexpr uint32_t BHI = SLO + TC_D * TC_D * 2;    // [k̂; q̂] hi [64 x 128] K-major
-  static constexpr uint32_t BLO = BHI + 2 * TC_C * TC_D * 2;
-  static constexpr uint32_t KTHI = BLO + 2 * TC_C * TC_D * 2;  // k̃ hi as [c (128)] x [j (32)]
+  static constexpr uint32_t BHI = SLO + TC_D * TC_D * 2;    // [k̂; q̂; 0] hi [128 x 128] K-major
+  static constexpr uint32_t BLO = BHI + TC_D * TC_D * 2;
+  static constexpr uint32_t KBHI = BLO + TC_D * TC_D * 2;   // k̄ hi [32 x 128] K-major
+  static constexpr uint32_t KBLO = KBHI + TC_C * TC_D * 2;
+  static constexpr uint32_t KTHI = KBLO + TC_C * TC_D * 2;  // k̃ hi as [c (128)] x [j (32)]
   static constexpr uint32_t KTLO = KTHI + TC_D * TC_C * 2;
   static constexpr uint32_t UHI = KTLO + TC_D * TC_C * 2;   // U hi [v (128)] x [i (32)]
   static constexpr uint32_t ULO = UHI + TC_D * TC_C * 2;
   static constexpr uint32_t AHI = ULO + TC_D * TC_C * 2;    // A hi [j (32)] x [i (32)]
   static constexpr uint32_t ALO = AHI + TC_C * TC_C * 2;
   static constexpr uint32_t VS = ALO + TC_C * TC_C * 2;     // v_j[r] bf16, rows of VP
-  static constexpr uint32_t KP = VS + TC_C * VP * 2;        // k_j[c] fp32, rows of LPAD
-  static constexpr uint32_t QP = KP + TC_C * LPAD * 4;      // q_j[c] fp32
-  static constexpr uint32_t LP = QP + TC_C * LPAD * 4;      // g, then Λ_j[c] fp32
+  static constexpr uint32_t LP = VS + TC_C * VP * 2;        // g, then Λ_j[c] fp32, rows of LPAD
   static constexpr uint32_t AKK = LP + TC_C * LPAD * 4;     // A_kk fp32 [32][AP]
   static constexpr uint32_t EC = AKK + TC_C * AP * 4;       // e^{Λ_C[c]} [128]
   static constexpr uint32_t BT = EC + TC_D * 4;             // β_j [32]
@@ -478,19 +485,7 @@ struct KdaSmem {
   static constexpr uint32_t BYTES = BAR + 32;
 };
 static_assert(KdaSmem::BYTES <= 227 * 1024, "shared memory");
-
-// One channel quad of KDA's decay-weighted pair products for token pair (j, i):
-// with w_c = e^{Λ_j[c] - Λ_i[c]}, kk += Σ k_i[c] w_c k_j[c] and qk += Σ k_i[c] w_c q_j[c].
-// A pair that is not live gets exponent 0, so its unused sums stay finite.
-__device__ __forceinline__ void kda_pair_quad(float& kk, float& qk, const float4 ki, const float4 li,
-                                              const float4 lj, const float4 kj, const float4 qj,
-                                              bool live) {
-  const float w0 = __expf(live ? lj.x - li.x : 0.f), w1 = __expf(live ? lj.y - li.y : 0.f);
-  const float w2 = __expf(live ? lj.z - li.z : 0.f), w3 = __expf(live ? lj.w - li.w : 0.f);
-  const float a0 = ki.x * w0, a1 = ki.y * w1, a2 = ki.z * w2, a3 = ki.w * w3;
-  kk += a0 * kj.x + a1 * kj.y + a2 * kj.z + a3 * kj.w;
-  qk += a0 * qj.x + a1 * qj.y + a2 * qj.z + a3 * qj.w;
-}
+constexpr float KDA_FACTOR_FLOOR = -60.f;   // lowest chunk log-decay the factored pair products take
 
 // KDA chunk inputs in registers: k, q, v (bf16) as in TcStage, the g rows as
 // float4 (4 per thread: row j = idx / 32, channel quad idx % 32), and β.
@@ -525,24 +520,14 @@ struct KdaStage {
     if (tid < 32) b = tid < Cc ? bg[(size_t)(t0 + tid) * nH + sh] : 0.f;
   }
 
-  static __device__ __forceinline__ void put8(float* dst, const uint4 w) {
-    *reinterpret_cast<float4*>(dst) =
-        make_float4(bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y));
-    *reinterpret_cast<float4*>(dst + 4) =
-        make_float4(bf16lo(w.z), bf16hi(w.z), bf16lo(w.w), bf16hi(w.w));
-  }
-
-  // k, q as fp32 rows, v as bf16 rows, g rows (scanned in place later), β
+  // v as bf16 rows, the g rows (scanned in place later), β; k and q stay in
+  // registers until the decayed operands are formed
   __device__ __forceinline__ void store(unsigned char* sm, int tid) const {
-    float* Kp = reinterpret_cast<float*>(sm + KdaSmem::KP);
-    float* Qp = reinterpret_cast<float*>(sm + KdaSmem::QP);
     float* Lp = reinterpret_cast<float*>(sm + KdaSmem::LP);
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       int j, cv;
       TcStage::piece(tid + e * TC_THREADS, j, cv);
-      put8(Kp + j * LPAD + cv * 8, k[e]);
-      put8(Qp + j * LPAD + cv * 8, q[e]);
       *reinterpret_cast<uint4*>(sm + KdaSmem::VS + (j * VP + cv * 8) * 2) = v[e];
     }
 #pragma unroll
@@ -554,14 +539,18 @@ struct KdaStage {
   }
 };
 
+// The 8 bf16 values of a 16-byte piece as fp32.
+__device__ __forceinline__ void unpack8(const uint4 w, float (&x)[8]) {
+  x[0] = bf16lo(w.x); x[1] = bf16hi(w.x); x[2] = bf16lo(w.y); x[3] = bf16hi(w.y);
+  x[4] = bf16lo(w.z); x[5] = bf16hi(w.z); x[6] = bf16lo(w.w); x[7] = bf16hi(w.w);
+}
+
 __global__ void __launch_bounds__(TC_THREADS, 1)
 prefill_kda_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* __restrict__ q,
                       const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
                       const float* __restrict__ g, const float* __restrict__ beta, void* o, int T,
                       int out_bf16, float scale, int32_t* status) {
   extern __shared__ __align__(1024) unsigned char sm[];
-  const float* Kp = reinterpret_cast<const float*>(sm + KdaSmem::KP);
-  const float* Qp = reinterpret_cast<const float*>(sm + KdaSmem::QP);
   float* Lp = reinterpret_cast<float*>(sm + KdaSmem::LP);
   float* Akk = reinterpret_cast<float*>(sm + KdaSmem::AKK);
   float* Ec = reinterpret_cast<float*>(sm + KdaSmem::EC);
@@ -571,7 +560,7 @@ prefill_kda_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* __
   int32_t* ok_flag = reinterpret_cast<int32_t*>(sm + KdaSmem::BAR + 20);
   const uint32_t sbase = smem_u32(sm);
   const uint32_t bar1 = sbase + KdaSmem::BAR, bar2 = sbase + KdaSmem::BAR + 8;
-  constexpr uint32_t K_D1 = 0, K_D3 = 64, K_D2 = 128;   // TMEM columns
+  constexpr uint32_t K_D0 = 0, K_D1 = 32, K_D3 = 96, K_D2 = 128;   // TMEM columns
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int q4 = warp & 3, hw = warp >> 2;
@@ -588,6 +577,12 @@ prefill_kda_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* __
     fence_mbar_init();
     *ok_flag = 1;
   }
+  // rows 64-127 of the [k̂; q̂; 0] operands stay zero; A_kk's row padding too
+  for (int idx = tid; idx < 64 * TC_D * 2 / 16; idx += TC_THREADS) {
+    reinterpret_cast<uint4*>(sm + KdaSmem::BHI + 64 * TC_D * 2)[idx] = make_uint4(0u, 0u, 0u, 0u);
+    reinterpret_cast<uint4*>(sm + KdaSmem::BLO + 64 * TC_D * 2)[idx] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  if (tid < TC_C) *reinterpret_cast<float4*>(Akk + tid * AP + TC_C) = make_float4(0.f, 0.f, 0.f, 0.f);
   float S[64];
   {
     const float4* src = reinterpret_cast<const float4*>(gS + (size_t)r * TC_D + 64 * hw);
@@ -620,44 +615,56 @@ prefill_kda_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* __
   for (int t0 = 0; t0 < T && ok; t0 += TC_C, ++chunk) {
     const int Cc = (T - t0) < TC_C ? (T - t0) : TC_C;
     const uint32_t par = (uint32_t)chunk & 1u;
-    // ---- stage; Λ = inclusive scan of g down each channel (padding tokens: g = 0)
+    // ---- stage; Λ = inclusive scan of g down each channel (padding tokens: g = 0);
+    //      the vote: does every channel's chunk log-decay stay above the floor?
     st.store(sm, tid);
     __syncthreads();
+    float lc = 0.f;
     if (tid < TC_D) {
-      float acc = 0.f;
 #pragma unroll 8
       for (int j = 0; j < TC_C; ++j) {
-        acc += Lp[j * LPAD + tid];
-        Lp[j * LPAD + tid] = acc;
+        lc += Lp[j * LPAD + tid];
+        Lp[j * LPAD + tid] = lc;
       }
-      Ec[tid] = expf(acc);
+      Ec[tid] = expf(lc);
     }
-    __syncthreads();
-    // ---- decayed operands, 8 channels of one token per piece:
-    //      [k̂_j; q̂_j] (hi, lo) and k̃_j (hi, lo; zero past Cc) transposed
+    const bool direct = __syncthreads_or(tid < TC_D && !(lc >= KDA_FACTOR_FLOOR)) != 0;
+    // ---- decayed operands, 8 channels of one token per piece (k, q from registers):
+    //      [k̂_j; q̂_j] and k̄_j (hi, lo), k̃_j (hi, lo; zero past Cc) transposed
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       int j, cv;
       TcStage::piece(tid + e * TC_THREADS, j, cv);
-      float kh[8], qh[8], kt[8];
+      float kx[8], qx[8], kh[8], qh[8], kb[8], kt[8];
+      unpack8(st.k[e], kx);
+      unpack8(st.q[e], qx);
 #pragma unroll
       for (int t = 0; t < 8; ++t) {
         const int c = cv * 8 + t;
         const float lj = Lp[j * LPAD + c];
-        const float el = __expf(lj);                                      // Λ <= 0
-        const float ew = j < Cc ? __expf(Lp[(Cc - 1) * LPAD + c] - lj) : 0.f;   // Λ_C - Λ_j <= 0
-        const float kc = Kp[j * LPAD + c];
-        kh[t] = el * kc;
-        qh[t] = el * Qp[j * LPAD + c];
-        kt[t] = ew * kc;
+        const float el = __expf(lj);                                  // Λ <= 0
+        kh[t] = el * kx[t];
+        qh[t] = el * qx[t];
+        if (direct) {
+          kb[t] = 0.f;
+          kt[t] = j < Cc ? __expf(Lp[(Cc - 1) * LPAD + c] - lj) * kx[t] : 0.f;   // Λ_C - Λ_j <= 0
+        } else {
+          const float eb = __expf(-lj);                               // <= e^{60}
+          kb[t] = eb * kx[t];
+          kt[t] = j < Cc ? fminf(Ec[cv * 8 + t] * eb, 1.f) * kx[t] : 0.f;
+        }
       }
       uint4 hv, lv;
+      const uint32_t okq = tc::kmaj_off(j, cv * 8, TC_D);
       split8(kh, hv, lv);
-      *reinterpret_cast<uint4*>(sm + KdaSmem::BHI + tc::kmaj_off(j, cv * 8, TC_D)) = hv;
-      *reinterpret_cast<uint4*>(sm + KdaSmem::BLO + tc::kmaj_off(j, cv * 8, TC_D)) = lv;
+      *reinterpret_cast<uint4*>(sm + KdaSmem::BHI + okq) = hv;
+      *reinterpret_cast<uint4*>(sm + KdaSmem::BLO + okq) = lv;
       split8(qh, hv, lv);
       *reinterpret_cast<uint4*>(sm + KdaSmem::BHI + tc::kmaj_off(TC_C + j, cv * 8, TC_D)) = hv;
       *reinterpret_cast<uint4*>(sm + KdaSmem::BLO + tc::kmaj_off(TC_C + j, cv * 8, TC_D)) = lv;
+      split8(kb, hv, lv);
+      *reinterpret_cast<uint4*>(sm + KdaSmem::KBHI + okq) = hv;
+      *reinterpret_cast<uint4*>(sm + KdaSmem::KBLO + okq) = lv;
       split8(kt, hv, lv);
       const uint32_t hw4[4] = {hv.x, hv.y, hv.z, hv.w}, lw4[4] = {lv.x, lv.y, lv.z, lv.w};
 #pragma unroll
@@ -669,66 +676,55 @@ prefill_kda_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* __
             (uint16_t)((t & 1) ? (lw4[t >> 1] >> 16) : (lw4[t >> 1] & 0xffffu));
       }
     }
-    tc::fence_smem_to_async();   // S̄ terms, [k̂; q̂] and k̃ terms, for the tensor cores
+    tc::fence_smem_to_async();   // S̄ terms and the decayed operands, for the tensor cores
     tc::fence_before_sync();
     __syncthreads();
-    // ---- D1 = S̄ [k̂; q̂]^T on the tensor cores ...
+    // ---- D0 = [k̂; q̂; 0] k̄^T (fast chunks) and D1 = S̄ [k̂; q̂]^T, three terms each
     if (tid == 0) {
       tc::fence_after_sync();
-      constexpr uint32_t id1 = tc::idesc_bf16_f32(128, 64);
+      constexpr uint32_t id0 = tc::idesc_bf16_f32(128, 32), id1 = tc::idesc_bf16_f32(128, 64);
+      const uint32_t sa[3] = {KdaSmem::SHI, KdaSmem::SLO, KdaSmem::SHI};
+      const uint32_t ba[3] = {KdaSmem::BHI, KdaSmem::BLO, KdaSmem::BHI};
+      const uint32_t bb[3] = {KdaSmem::BHI, KdaSmem::BHI, KdaSmem::BLO};
+      const uint32_t kb3[3] = {KdaSmem::KBHI, KdaSmem::KBHI, KdaSmem::KBLO};
 #pragma unroll
-      for (int kk = 0; kk < TC_D / 16; ++kk)
-        tc::mma_bf16(tm + K_D1, tc::kmaj_desc(sbase + KdaSmem::SHI, TC_D, kk),
-                     tc::kmaj_desc(sbase + KdaSmem::BHI, TC_D, kk), id1, kk > 0);
+      for (int term = 0; term < 3; ++term)
 #pragma unroll
-      for (int kk = 0; kk < TC_D / 16; ++kk)
-        tc::mma_bf16(tm + K_D1, tc::kmaj_desc(sbase + KdaSmem::SLO, TC_D, kk),
-                     tc::kmaj_desc(sbase + KdaSmem::BHI, TC_D, kk), id1, 1u);
-#pragma unroll
-      for (int kk = 0; kk < TC_D / 16; ++kk)
-        tc::mma_bf16(tm + K_D1, tc::kmaj_desc(sbase + KdaSmem::SHI, TC_D, kk),
-                     tc::kmaj_desc(sbase + KdaSmem::BLO, TC_D, kk), id1, 1u);
+        for (int kk = 0; kk < TC_D / 16; ++kk) {
+          if (!direct)
+            tc::mma_bf16(tm + K_D0, tc::kmaj_desc(sbase + ba[term], TC_D, kk),
+                         tc::kmaj_desc(sbase + kb3[term], TC_D, kk), id0, (term | kk) != 0);
+          tc::mma_bf16(tm + K_D1, tc::kmaj_desc(sbase + sa[term], TC_D, kk),
+                       tc::kmaj_desc(sbase + bb[term], TC_D, kk), id1, (term | kk) != 0);
+        }
       tc::mma_commit(bar1);
     }
-    // ... while the CUDA cores form the pair coefficients: pairs (jg + 16x,
-    // ig + 16y) per thread, (x, y) = (0, 1) lies above the diagonal; a dead
-    // pair's exponent is replaced by 0 so that its unused sums stay finite
-    {
-      const int jg = tid >> 4, ig = tid & 15;
-      const int j0 = jg, j1 = jg + 16, i0 = ig, i1 = ig + 16;
-      const bool dl = ig <= jg;
-      float kk3[3] = {0.f, 0.f, 0.f}, qk3[3] = {0.f, 0.f, 0.f};   // pairs (0,0), (1,0), (1,1)
-#pragma unroll 2
-      for (int c = 0; c < TC_D; c += 4) {
-        const float4 ki0 = *reinterpret_cast<const float4*>(Kp + i0 * LPAD + c);
-        const float4 ki1 = *reinterpret_cast<const float4*>(Kp + i1 * LPAD + c);
-        const float4 li0 = *reinterpret_cast<const float4*>(Lp + i0 * LPAD + c);
-        const float4 li1 = *reinterpret_cast<const float4*>(Lp + i1 * LPAD + c);
-        const float4 lj0 = *reinterpret_cast<const float4*>(Lp + j0 * LPAD + c);
-        const float4 lj1 = *reinterpret_cast<const float4*>(Lp + j1 * LPAD + c);
-        const float4 kj0 = *reinterpret_cast<const float4*>(Kp + j0 * LPAD + c);
-        const float4 kj1 = *reinterpret_cast<const float4*>(Kp + j1 * LPAD + c);
-        const float4 qj0 = *reinterpret_cast<const float4*>(Qp + j0 * LPAD + c);
-        const float4 qj1 = *reinterpret_cast<const float4*>(Qp + j1 * LPAD + c);
-        kda_pair_quad(kk3[0], qk3[0], ki0, li0, lj0, kj0, qj0, dl);
-        kda_pair_quad(kk3[1], qk3[1], ki0, li0, lj1, kj1, qj1, true);
-        kda_pair_quad(kk3[2], qk3[2], ki1, li1, lj1, kj1, qj1, dl);
+    auto put_a = [&](int j, int i, float av) {   // A[j][i] as the bf16 terms of D3's B operand
+      const uint32_t hv = bf16x2(av, 0.f) & 0xffffu;
+      const uint32_t lv = bf16x2(av - __uint_as_float(hv << 16), 0.f) & 0xffffu;
+      const uint32_t off = tc::kmaj_off(j, i, TC_C);
+      *reinterpret_cast<uint16_t*>(sm + KdaSmem::AHI + off) = (uint16_t)hv;
+      *reinterpret_cast<uint16_t*>(sm + KdaSmem::ALO + off) = (uint16_t)lv;
+    };
+    if (direct) {
+      // strong decay: every pair (j, i) directly, e^{Λ_j[c]-Λ_i[c]} per channel,
+      // with k, q read back from global memory (pairs tid, tid + 256, tid + 512)
+      for (int p = tid; p < TC_C * TC_C; p += TC_THREADS) {
+        const int j = p >> 5, i = p & 31;
+        float kk = 0.f, qk = 0.f;
+        if (i <= j && j < Cc) {
+          const uint16_t* kj = k + ((size_t)(t0 + j) * nH + sh) * TC_D;
+          const uint16_t* qj = q + ((size_t)(t0 + j) * nH + sh) * TC_D;
+          const uint16_t* ki = k + ((size_t)(t0 + i) * nH + sh) * TC_D;
+          for (int c = 0; c < TC_D; ++c) {
+            const float w = __expf(Lp[j * LPAD + c] - Lp[i * LPAD + c]) * bf16f(ki[c]);
+            kk += w * bf16f(kj[c]);
+            qk += w * bf16f(qj[c]);
+          }
+        }
+        Akk[j * AP + i] = i < j ? kk : 0.f;
+        put_a(j, i, qk);
       }
-      auto put = [&](int j, int i, float kv, float qv, bool live) {
-        const bool ok2 = live && j < Cc;
-        Akk[j * AP + i] = (ok2 && i != j) ? kv : 0.f;
-        const float av = ok2 ? qv : 0.f;
-        const uint32_t hv = bf16x2(av, 0.f) & 0xffffu;
-        const uint32_t lv = bf16x2(av - __uint_as_float(hv << 16), 0.f) & 0xffffu;
-        const uint32_t off = tc::kmaj_off(j, i, TC_C);
-        *reinterpret_cast<uint16_t*>(sm + KdaSmem::AHI + off) = (uint16_t)hv;
-        *reinterpret_cast<uint16_t*>(sm + KdaSmem::ALO + off) = (uint16_t)lv;
-      };
-      put(j0, i0, kk3[0], qk3[0], dl);
-      put(j0, i1, 0.f, 0.f, false);
-      put(j1, i0, kk3[1], qk3[1], true);
-      put(j1, i1, kk3[2], qk3[2], dl);
-      if (tid < TC_C) *reinterpret_cast<float4*>(Akk + tid * AP + TC_C) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     if (t0 + TC_C < T) {
       const int Cn = (T - t0 - TC_C) < TC_C ? (T - t0 - TC_C) : TC_C;
@@ -741,6 +737,37 @@ prefill_kda_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* __
       break;
     }
     tc::fence_after_sync();
+    // ---- fast chunks: the pair coefficients from D0 (warps 0, 1, 4, 5: rows
+    //      0-63, 16 columns each), live below the diagonal (A_kk) or on and below it (A)
+    if (!direct && q4 < 2) {
+      uint32_t x[16];
+      tc::tmem_ld16(tlane + K_D0 + 16 * hw, x);
+      tc::tmem_wait_ld16(x);
+      const int j = lane, i0 = 16 * hw;
+      float w[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int i = i0 + e;
+        const bool live = (q4 == 0 ? i < j : i <= j) && j < Cc;
+        w[e] = live ? __uint_as_float(x[e]) : 0.f;
+      }
+      if (q4 == 0) {
+#pragma unroll
+        for (int e4 = 0; e4 < 4; ++e4)
+          *reinterpret_cast<float4*>(Akk + j * AP + i0 + 4 * e4) =
+              make_float4(w[4 * e4], w[4 * e4 + 1], w[4 * e4 + 2], w[4 * e4 + 3]);
+      } else {
+#pragma unroll
+        for (int c8 = 0; c8 < 2; ++c8) {
+          uint4 hv, lv;
+          split8(w + 8 * c8, hv, lv);
+          const uint32_t off = tc::kmaj_off(j, i0 + 8 * c8, TC_C);
+          *reinterpret_cast<uint4*>(sm + KdaSmem::AHI + off) = hv;
+          *reinterpret_cast<uint4*>(sm + KdaSmem::ALO + off) = lv;
+        }
+      }
+    }
+    __syncthreads();
     // ---- forward substitution (warps 0-3, one value row each)
     if (hw == 0) {
       float pk[TC_C], u[TC_C];

@@ -55,3 +55,33 @@ def test_long_prefill_matches_oracle(op, d, T):
     assert max_step_rel(o_sel, o_ref) <= OUT_TOL_BF16
     assert rel_err(S[bi, hi].numpy(), S_ref) <= STATE_TOL
     assert list(n) == [0] * B and list(base_of) == slots
+
+
+@pytest.mark.parametrize("strong", ["all", "mixed"])
+def test_kda_prefill_strong_decay_matches_oracle(strong):
+    """KDA's pair coefficients factor through the chunk start while a chunk's
+    total log-decay stays above -60 in every channel; a chunk with stronger
+    decay takes the direct path (one exponential per channel and pair).  Here
+    the log-decays are scaled up (about -2.8 a token: -90 over a chunk) for
+    every token, or for the tokens of every other chunk only, so that both
+    paths run and alternate; the result must still match the oracle."""
+    from linear_attention_recurrent_gdn_gb300 import deltalog as dl
+    B, H, d, M, T = 2, 4, 128, 16, 160
+    x, S0, _ = make_case(gen.KDA, B, H, d, T, seed=5300 + len(strong))
+    g = x["g"].clone()
+    if strong == "all":
+        g *= 40.0
+    else:
+        for c0 in range(0, T, 64):
+            g[c0:c0 + 32] *= 40.0
+    x["g"] = g.contiguous()
+    o_ref, S_ref, _ = oracle_run(gen.KDA, x, S0, None)
+    ctx = dl.DeltaLog(gen.KDA, B, H, d, d, M, out_bf16=False)
+    slots = list(range(B))
+    ctx.set_state(slots, S0.cuda())
+    dev = {k_: (v_.cuda() if v_ is not None else None) for k_, v_ in x.items()}
+    o = ctx.prefill(slots, dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"])
+    S = ctx.read_state(slots).cpu().reshape(B * H, d, d).numpy()
+    ctx.close()
+    assert max_step_rel(o.float().cpu().reshape(T, B * H, d).numpy(), o_ref) <= 1e-4
+    assert rel_err(S, S_ref) <= STATE_TOL
