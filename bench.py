@@ -737,6 +737,18 @@ def copy_ceiling(pin, hout, dev, T, group, units, args):
                       "the outputs, on two streams, no compute" % group}
 
 
+def prefill_mma_flops(op, d, C=PREFILL_C):
+    """FLOPs (an FMA counts 2) the tensor-core prefill's MMAs execute per
+    token·head at d = 128, C = 32, every operand term and padded row included
+    (csrc/prefill_tc.cu): GDN D0 [K;Q;0]K^T (M=128, N=C, K=d), D1 S̄[K;Q]^T in two
+    terms (N=2C), D2 the rank-C rewrite in two terms (N=d, K=C), D3 the outputs'
+    log terms in three (N=C, K=C); KDA the same with three terms each."""
+    terms = {0: (1, 2, 2, 3), 1: (3, 3, 3, 3)}[op]
+    mac = (terms[0] * 128 * C * d + terms[1] * 128 * 2 * C * d + terms[2] * 128 * d * C
+           + terms[3] * 128 * C * C)
+    return 2 * mac / C
+
+
 def prefill_flops(op, d, C=PREFILL_C):
     """FLOPs (an FMA counts 2) per token·head of the chunked prefill's
     contractions, d_k = d_v = d.  Per token: the products with S̄ (S̄K^T and S̄Q^T,
@@ -826,6 +838,28 @@ def run_prefill(args):
     ms, clocks = timed_steps(one, args, dist, local, dev, stream)
     units = B * H * T
     tflops = units * prefill_flops(op, d) / (ms / 1e3) / 1e12
+    tensor = op in (0, 1) and d == 128      # GDN and KDA at d = 128 run on the tensor cores
+    if tensor:
+        try:
+            bf16_peak = float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["bf16_tflops"])
+            bf16_src = "measured bf16_tflops (cuBLAS bf16 GEMM, burst)"
+        except (OSError, KeyError, ValueError):
+            bf16_peak, bf16_src = 1900.0, "fallback"
+        mma = prefill_mma_flops(op, d)
+        roofline = {"bound": "tensor", "achieved": tflops, "peak": bf16_peak, "unit": "TFLOP/s",
+                    "frac": tflops / bf16_peak, "traffic": None, "peak_source": bf16_src,
+                    "flops_per_token_head": prefill_flops(op, d),
+                    "note": "algorithmic FLOPs of the chunk contractions (fp32 formulation) over "
+                            "the dense bf16 tensor peak; the kernel's MMAs execute "
+                            "mma_flops_per_token_head (hi/lo operand terms and padded rows)",
+                    "mma_flops_per_token_head": mma,
+                    "mma_tflops": units * mma / (ms / 1e3) / 1e12,
+                    "fp32_equivalent_frac": tflops / FP32_PEAK_TFLOPS}
+    else:
+        roofline = {"bound": "alu", "achieved": tflops, "peak": FP32_PEAK_TFLOPS,
+                    "unit": "TFLOP/s", "frac": tflops / FP32_PEAK_TFLOPS, "traffic": None,
+                    "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 FLOP x 2.07 GHz",
+                    "flops_per_token_head": prefill_flops(op, d)}
     result = {"metric": "prefill tokens·heads/s", "value": units * world / (ms / 1e3),
               "unit": "tokens·heads/s", "n_gpus": world, "steps": args.steps,
               "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
@@ -835,11 +869,7 @@ def run_prefill(args):
                          "op": gen.OP_NAMES[op], "B": B, "H": H, "d_k": d, "d_v": d,
                          "T": T, "chunk": PREFILL_C,
                          "l2": "inputs and state larger than L2"},
-              "roofline": {"bound": "alu", "achieved": tflops, "peak": FP32_PEAK_TFLOPS,
-                           "unit": "TFLOP/s", "frac": tflops / FP32_PEAK_TFLOPS,
-                           "traffic": None, "peak_source": "derived: 152 SMs x 128 FP32 "
-                           "lanes x 2 FLOP x 2.07 GHz",
-                           "flops_per_token_head": prefill_flops(op, d)},
+              "roofline": roofline,
               "clocks": clocks,
               "gpu_launches": args.steps * clocks.get("reps", 1) * ((B + 1023) // 1024)}
     if rank == 0:
