@@ -9,7 +9,7 @@
 //   S̄'  = e^{Λ_C} S̄ + Σ_j (e^{Λ_C-Λ_j} u_j) k_j^T
 // The dense contractions of a chunk run as tcgen05 MMAs (bf16 operands, fp32
 // accumulators in tensor memory):
-//   D0 [128 x 32]  = [K; Q; 0] K^T              key-key and query-key products (exact: k, q are bf16)
+//   D0 [128 x 32]  = [K; Q; K; Q] K^T           key-key and query-key products (exact: k, q are bf16)
 //   D1 [128 x 64]  = (S̄_hi + S̄_lo) [K; Q]^T     S̄ k_j and S̄ q_j for all 32 tokens
 //   D2 [128 x 128] = (W_hi + W_lo) K             the rank-32 rewrite, W = e^{Λ_C-Λ_j} u_j
 //   D3 [128 x 32]  = U_hi A_hi + U_lo A_hi + U_hi A_lo   the outputs' log terms,
@@ -48,25 +48,31 @@ constexpr uint32_t D0_COL = 0, D1_COL = 32, D3_COL = 96, D2_COL = 128;
 constexpr int VP = TC_D + 8, AP = 36;
 constexpr int LPAD = TC_D + 4;   // fp32 rows of k, q, Λ (KDA): quad loads of rows ig, jg spread over banks
 
-// Byte offsets in the dynamic shared memory (operands 16-byte aligned).
+// Byte offsets in the dynamic shared memory (operands 16-byte aligned).  The
+// per-chunk buffers that the next chunk's preparation fills while the current
+// chunk still reads them are doubled (index b = chunk & 1).
 struct TcSmem {
   static constexpr uint32_t SHI = 0;                       // S̄ hi, K-major [128 x 128] bf16
   static constexpr uint32_t SLO = SHI + TC_D * TC_D * 2;   // S̄ lo
-  static constexpr uint32_t KQ = SLO + TC_D * TC_D * 2;    // rows 0-31 k_j, 32-63 q_j, 64-127 zero
-  static constexpr uint32_t KT = KQ + TC_D * TC_D * 2;     // K as [i (128)] x [j (32)], K-major
-  static constexpr uint32_t WHI = KT + TC_D * TC_C * 2;    // W hi [v (128)] x [j (32)], K-major
+  static constexpr uint32_t KQ = SLO + TC_D * TC_D * 2;    // rows 0-31 k_j, 32-63 q_j, 64-127 again
+  static constexpr uint32_t WHI = KQ + TC_D * TC_D * 2;    // W hi [v (128)] x [j (32)], K-major
   static constexpr uint32_t WLO = WHI + TC_D * TC_C * 2;   // W lo
   static constexpr uint32_t UHI = WLO + TC_D * TC_C * 2;   // U hi [v (128)] x [i (32)], K-major
   static constexpr uint32_t ULO = UHI + TC_D * TC_C * 2;   // U lo
-  static constexpr uint32_t AHI = ULO + TC_D * TC_C * 2;   // A hi [j (32)] x [i (32)], K-major
-  static constexpr uint32_t ALO = AHI + TC_C * TC_C * 2;   // A lo
-  static constexpr uint32_t VS = ALO + TC_C * TC_C * 2;    // v_j[r] bf16, rows of VP
-  static constexpr uint32_t AKK = VS + TC_C * VP * 2;      // fp32 [32][AP], 16-byte rows
-  static constexpr uint32_t SC = AKK + TC_C * AP * 4;      // Λ_j, e^{Λ_j}, e^{Λ_C-Λ_j}, β_j: [4][32] fp32
-  static constexpr uint32_t BAR = SC + 4 * TC_C * 4;       // 2 mbarriers, TMEM base, ok flag
+  // doubled: K^T (K as [i (128)] x [j (32)], K-major), A hi / lo ([j] x [i], K-major),
+  // v_j[r] (bf16 rows of VP), A_kk (fp32 [32][AP]), Λ_j, e^{Λ_j}, e^{Λ_C-Λ_j}, β_j ([4][32])
+  static constexpr uint32_t KT_SZ = TC_D * TC_C * 2, A_SZ = TC_C * TC_C * 2, VS_SZ = TC_C * VP * 2,
+                            AKK_SZ = TC_C * AP * 4, SC_SZ = 4 * TC_C * 4;
+  static constexpr uint32_t BUF = KT_SZ + 2 * A_SZ + VS_SZ + AKK_SZ + SC_SZ;   // one set
+  static constexpr uint32_t SET0 = ULO + TC_D * TC_C * 2;
+  static constexpr uint32_t KT = 0, AHI = KT + KT_SZ, ALO = AHI + A_SZ, VS = ALO + A_SZ,
+                            AKK = VS + VS_SZ, SC = AKK + AKK_SZ;   // offsets inside a set
+  static constexpr uint32_t BAR = SET0 + 2 * BUF;          // 3 mbarriers, TMEM base, ok flag
   static constexpr uint32_t BYTES = BAR + 32;
+  static __host__ __device__ constexpr uint32_t set(int b) { return SET0 + (uint32_t)b * BUF; }
 };
 static_assert(TcSmem::BYTES <= 227 * 1024, "shared memory");
+static_assert(TcSmem::BUF % 16 == 0 && TcSmem::SET0 % 16 == 0, "16-byte aligned buffers");
 
 // Two fp32 values rounded to bf16 as one word (first value in the low half).
 __device__ __forceinline__ uint32_t bf16x2(float a, float b) {
@@ -87,30 +93,30 @@ __device__ __forceinline__ void split8(const float* x, uint4& h, uint4& l) {
   l = make_uint4(lw[0], lw[1], lw[2], lw[3]);
 }
 
-// One chunk's k, q, v (bf16) and g, β in registers between their global loads
-// and their shared-memory stores.
-struct TcStage {
-  uint4 k[2], q[2], v[2];
-  float g, b;
+// Element idx of a chunk's 32 x 16 grid of 16-byte pieces (token j, column
+// piece cv): a warp's lanes take 8 consecutive tokens x 4 consecutive pieces,
+// so its global loads read 64 contiguous bytes of each of 8 rows and its
+// stores into the K-major operands fill whole 128-byte core-matrix rows.
+__device__ __forceinline__ void chunk_piece(int idx, int& j, int& cv) {
+  const int rest = idx >> 5;
+  j = (idx & 7) + 8 * (rest & 3);
+  cv = ((idx >> 3) & 3) + 4 * (rest >> 2);
+}
 
-  // Element idx of the chunk's 32 x 16 grid of 16-byte pieces (token j, column
-  // piece cv): a warp's lanes take 8 consecutive tokens x 4 consecutive pieces,
-  // so its global loads read 64 contiguous bytes of each of 8 rows and its
-  // stores into the K-major operands fill whole 128-byte core-matrix rows.
-  static __device__ __forceinline__ void piece(int idx, int& j, int& cv) {
-    const int rest = idx >> 5;
-    j = (idx & 7) + 8 * (rest & 3);
-    cv = ((idx >> 3) & 3) + 4 * (rest >> 2);
-  }
+// One chunk's k, q, v (bf16) and g, β in the registers of the 128 threads that
+// prepare chunks, between their global loads and their shared-memory stores.
+struct TcStage {
+  uint4 k[4], q[4], v[4];
+  float g, b;
 
   __device__ __forceinline__ void load(const uint16_t* __restrict__ qg, const uint16_t* __restrict__ kg,
                                        const uint16_t* __restrict__ vg, const float* __restrict__ gg,
                                        const float* __restrict__ bg, int t0, int Cc, size_t nH,
-                                       int sh, int tid) {
+                                       int sh, int ptid) {
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
+    for (int e = 0; e < 4; ++e) {
       int j, cv;
-      piece(tid + e * TC_THREADS, j, cv);
+      chunk_piece(ptid + e * 128, j, cv);
       if (j < Cc) {
         const size_t base = ((size_t)(t0 + j) * nH + sh) * TC_D + cv * 8;
         k[e] = *reinterpret_cast<const uint4*>(kg + base);
@@ -120,30 +126,130 @@ struct TcStage {
         k[e] = q[e] = v[e] = make_uint4(0u, 0u, 0u, 0u);
       }
     }
-    if (tid < 32) {
-      g = tid < Cc ? gg[(size_t)(t0 + tid) * nH + sh] : 0.f;
-      b = tid < Cc ? bg[(size_t)(t0 + tid) * nH + sh] : 0.f;
+    if (ptid < 32) {
+      g = ptid < Cc ? gg[(size_t)(t0 + ptid) * nH + sh] : 0.f;
+      b = ptid < Cc ? bg[(size_t)(t0 + ptid) * nH + sh] : 0.f;
     }
   }
 
-  // k, q into the KQ operand, k into the transposed KT operand, v into VS
-  __device__ __forceinline__ void store(unsigned char* sm, int tid) const {
+  // k, q into the KQ operand, twice: rows 0-63 and again rows 64-127, so that
+  // D0's rows 64-127 repeat its rows 0-63 in the TMEM lanes of warps 6 and 7
+  __device__ __forceinline__ void store_kq(unsigned char* sm, int ptid) const {
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
+    for (int e = 0; e < 4; ++e) {
       int j, cv;
-      piece(tid + e * TC_THREADS, j, cv);
-      *reinterpret_cast<uint4*>(sm + TcSmem::KQ + tc::kmaj_off(j, cv * 8, TC_D)) = k[e];
-      *reinterpret_cast<uint4*>(sm + TcSmem::KQ + tc::kmaj_off(TC_C + j, cv * 8, TC_D)) = q[e];
-      *reinterpret_cast<uint4*>(sm + TcSmem::VS + (j * VP + cv * 8) * 2) = v[e];
+      chunk_piece(ptid + e * 128, j, cv);
+#pragma unroll
+      for (int rep = 0; rep < 2; ++rep) {
+        *reinterpret_cast<uint4*>(sm + TcSmem::KQ + tc::kmaj_off(64 * rep + j, cv * 8, TC_D)) = k[e];
+        *reinterpret_cast<uint4*>(sm + TcSmem::KQ + tc::kmaj_off(64 * rep + TC_C + j, cv * 8, TC_D)) = q[e];
+      }
+    }
+  }
+
+  // k into the transposed K^T operand of set `set`, v into its VS
+  __device__ __forceinline__ void store_rest(unsigned char* sm, uint32_t set, int ptid) const {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      int j, cv;
+      chunk_piece(ptid + e * 128, j, cv);
+      *reinterpret_cast<uint4*>(sm + set + TcSmem::VS + (j * VP + cv * 8) * 2) = v[e];
       const uint32_t w[4] = {k[e].x, k[e].y, k[e].z, k[e].w};
 #pragma unroll
-      for (int t = 0; t < 8; ++t) {   // k_j[i], i = 8 cv + t, at KT row i, column j
+      for (int t = 0; t < 8; ++t) {   // k_j[i], i = 8 cv + t, at K^T row i, column j
         const uint16_t x = (uint16_t)((t & 1) ? (w[t >> 1] >> 16) : (w[t >> 1] & 0xffffu));
-        *reinterpret_cast<uint16_t*>(sm + TcSmem::KT + tc::kmaj_off(cv * 8 + t, j, TC_C)) = x;
+        *reinterpret_cast<uint16_t*>(sm + set + TcSmem::KT + tc::kmaj_off(cv * 8 + t, j, TC_C)) = x;
       }
     }
   }
 };
+
+// Barrier among the 128 threads (warps 4-7) that prepare the next chunk.
+__device__ __forceinline__ void prep_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// The per-chunk work that does not depend on S̄, done by warps 4-7 for a chunk
+// while warps 0-3 run the previous chunk's forward substitution: stage k, q,
+// v, the decays (Λ by a scan over the chunk, e^{Λ_j}, e^{Λ_C-Λ_j}) and β;
+// D0 = [K; Q; K; Q] K^T; from it the pair coefficients A_kk (fp32 rows) and A
+// (bf16 terms of D3's B operand), each with its decay e^{Λ_j-Λ_i}.
+__device__ __forceinline__ void gdn_prepare(unsigned char* sm, const TcStage& st, uint32_t set,
+                                            int Cc, int chunk, uint32_t tm, uint32_t sbase,
+                                            uint32_t bar0, int32_t* status, int32_t* ok_flag) {
+  const int ptid = threadIdx.x - 128, lane = threadIdx.x & 31, pw = ptid >> 5;
+  float* Lm = reinterpret_cast<float*>(sm + set + TcSmem::SC);
+  float* El = Lm + TC_C;
+  float* Ew = El + TC_C;
+  float* Bt = Ew + TC_C;
+  // k, q first: D0 needs only them, and runs while the rest is staged
+  st.store_kq(sm, ptid);
+  tc::fence_smem_to_async();   // KQ for the tensor cores
+  tc::fence_before_sync();
+  prep_sync();
+  if (ptid == 0) {
+    tc::fence_after_sync();
+    constexpr uint32_t id0 = tc::idesc_bf16_f32(128, 32);
+#pragma unroll
+    for (int kk = 0; kk < TC_D / 16; ++kk)
+      tc::mma_bf16(tm, tc::kmaj_desc(sbase + TcSmem::KQ, TC_D, kk),
+                   tc::kmaj_desc(sbase + TcSmem::KQ, TC_D, kk), id0, kk > 0);
+    tc::mma_commit(bar0);
+  }
+  st.store_rest(sm, set, ptid);
+  if (pw == 0) {
+    float gj = st.g;
+#pragma unroll
+    for (int o2 = 1; o2 < 32; o2 <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, gj, o2);
+      if (lane >= o2) gj += y;
+    }
+    const float LC = __shfl_sync(0xffffffffu, gj, Cc - 1);
+    Lm[lane] = gj;
+    El[lane] = expf(gj);
+    Ew[lane] = lane < Cc ? expf(LC - gj) : 0.f;   // padding tokens add nothing
+    Bt[lane] = st.b;                               // 0 past Cc
+  }
+  // a wait that gives up records which phase it waited for (-3: parity 0, -4: parity 1)
+  if (ptid == 0 && !mbar_wait(bar0, (uint32_t)chunk & 1u, status, DEV_TIMEOUT_MMA))
+    *ok_flag = -3 - (chunk & 1);
+  prep_sync();
+  tc::fence_after_sync();
+  // D0 rows 0-31 and 64-95 hold k_j·k_i, rows 32-63 and 96-127 q_j·k_i (row j
+  // = lane of the quarter).  Each warp reads its own lane quarter (warp 4 + pw
+  // owns lanes 32 pw .. 32 pw + 31): warps 4, 5 columns 0-15, warps 6, 7 columns 16-31.
+  {
+    const int half = pw >> 1, which = pw & 1, i0 = 16 * half;
+    uint32_t x[16];
+    tc::tmem_ld16(tm + ((uint32_t)(32 * pw) << 16) + i0, x);
+    tc::tmem_wait_ld16(x);
+    const int j = lane;
+    const float lj = Lm[j];
+    float w[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const int i = i0 + e;
+      const bool live = (which == 0 ? i < j : i <= j) && j < Cc;
+      w[e] = live ? __uint_as_float(x[e]) * __expf(lj - Lm[i]) : 0.f;   // exponent <= 0
+    }
+    if (which == 0) {
+      float* Akk = reinterpret_cast<float*>(sm + set + TcSmem::AKK);
+#pragma unroll
+      for (int e4 = 0; e4 < 4; ++e4)
+        *reinterpret_cast<float4*>(Akk + j * AP + i0 + 4 * e4) =
+            make_float4(w[4 * e4], w[4 * e4 + 1], w[4 * e4 + 2], w[4 * e4 + 3]);
+      if (half == 1) *reinterpret_cast<float4*>(Akk + j * AP + TC_C) = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+#pragma unroll
+      for (int c8 = 0; c8 < 2; ++c8) {
+        uint4 hv, lv;
+        split8(w + 8 * c8, hv, lv);
+        const uint32_t off = tc::kmaj_off(j, i0 + 8 * c8, TC_C);
+        *reinterpret_cast<uint4*>(sm + set + TcSmem::AHI + off) = hv;
+        *reinterpret_cast<uint4*>(sm + set + TcSmem::ALO + off) = lv;
+      }
+    }
+  }
+  tc::fence_before_sync();
+}
 
 __global__ void __launch_bounds__(TC_THREADS, 1)
 prefill_gdn_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* __restrict__ q,
@@ -151,36 +257,29 @@ prefill_gdn_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* __
                       const float* __restrict__ g, const float* __restrict__ beta, void* o, int T,
                       int out_bf16, float scale, int32_t* status) {
   extern __shared__ __align__(1024) unsigned char sm[];
-  float* Akk = reinterpret_cast<float*>(sm + TcSmem::AKK);
-  float* Lm = reinterpret_cast<float*>(sm + TcSmem::SC);
-  float* El = Lm + TC_C;
-  float* Ew = El + TC_C;
-  float* Bt = Ew + TC_C;
-  const uint16_t* Vs = reinterpret_cast<const uint16_t*>(sm + TcSmem::VS);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + TcSmem::BAR + 16);
-  int32_t* ok_flag = reinterpret_cast<int32_t*>(sm + TcSmem::BAR + 20);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + TcSmem::BAR + 24);
+  int32_t* ok_flag = reinterpret_cast<int32_t*>(sm + TcSmem::BAR + 28);
   const uint32_t sbase = smem_u32(sm);
-  const uint32_t bar1 = sbase + TcSmem::BAR, bar2 = sbase + TcSmem::BAR + 8;
+  const uint32_t bar1 = sbase + TcSmem::BAR, bar2 = bar1 + 8, bar0 = bar1 + 16;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int q4 = warp & 3, hw = warp >> 2;      // TMEM lane quarter, column half
   const int r = 32 * q4 + lane;                 // this thread's value row
+  const bool prep = warp >= 4;                  // warps 4-7 prepare the next chunk
   const int sh = blockIdx.x, row = sh / a.H, h = sh - row * a.H;
   const int slot = a.items[row].slot;
   const size_t nH = (size_t)a.rows * a.H;
   float* gS = a.Sbar + ((size_t)slot * a.H + h) * TC_D * TC_D;
+  const int nch = (T + TC_C - 1) / TC_C;
 
-  if (warp == 0) tc::tmem_alloc(sbase + TcSmem::BAR + 16, TC_COLS);
+  if (warp == 0) tc::tmem_alloc(sbase + TcSmem::BAR + 24, TC_COLS);
   if (tid == 0) {
     mbar_init(bar1, 1);
     mbar_init(bar2, 1);
+    mbar_init(bar0, 1);
     fence_mbar_init();
     *ok_flag = 1;
   }
-  // rows 64-127 of the KQ operand stay zero (D0's rows 64-127 are unused)
-  for (int idx = tid; idx < 64 * TC_D * 2 / 16; idx += TC_THREADS)
-    reinterpret_cast<uint4*>(sm + TcSmem::KQ + 64 * TC_D * 2)[idx] = make_uint4(0u, 0u, 0u, 0u);
-
   // the fp32 state of this thread's row half, and its bf16 terms for the MMAs
   float S[64];
   {
@@ -204,58 +303,46 @@ prefill_gdn_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* __
   }
 
   TcStage st;
-  st.load(q, k, v, g, beta, 0, T < TC_C ? T : TC_C, nH, sh, tid);
+  if (prep) st.load(q, k, v, g, beta, 0, T < TC_C ? T : TC_C, nH, sh, tid - 128);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tm = *tmem_slot;
   const uint32_t tlane = tm + ((uint32_t)(32 * q4) << 16);   // this warp's lane quarter
-  bool ok = true;
+  // chunk 0 prepared, chunk 1's inputs on their way, then D1 of chunk 0
+  if (prep) {
+    gdn_prepare(sm, st, TcSmem::set(0), T < TC_C ? T : TC_C, 0, tm + D0_COL, sbase, bar0, status,
+                ok_flag);
+    if (nch > 1) st.load(q, k, v, g, beta, TC_C, (T - TC_C) < TC_C ? (T - TC_C) : TC_C, nH, sh, tid - 128);
+  }
+  tc::fence_smem_to_async();
+  tc::fence_before_sync();
+  __syncthreads();
+  bool ok = *ok_flag == 1;
+  if (ok && tid == 0) {
+    tc::fence_after_sync();
+    constexpr uint32_t id1 = tc::idesc_bf16_f32(128, 64);
+#pragma unroll
+    for (int kk = 0; kk < TC_D / 16; ++kk)
+      tc::mma_bf16(tm + D1_COL, tc::kmaj_desc(sbase + TcSmem::SHI, TC_D, kk),
+                   tc::kmaj_desc(sbase + TcSmem::KQ, TC_D, kk), id1, kk > 0);
+#pragma unroll
+    for (int kk = 0; kk < TC_D / 16; ++kk)
+      tc::mma_bf16(tm + D1_COL, tc::kmaj_desc(sbase + TcSmem::SLO, TC_D, kk),
+                   tc::kmaj_desc(sbase + TcSmem::KQ, TC_D, kk), id1, 1u);
+    tc::mma_commit(bar1);
+  }
   int chunk = 0;
-  for (int t0 = 0; t0 < T && ok; t0 += TC_C, ++chunk) {
+  for (; chunk < nch && ok; ++chunk) {
+    const int t0 = chunk * TC_C;
     const int Cc = (T - t0) < TC_C ? (T - t0) : TC_C;
     const uint32_t par = (uint32_t)chunk & 1u;
-    // ---- stage the chunk (tokens past the end: zero inputs, zero decay)
-    st.store(sm, tid);
-    if (warp == 0) {
-      float gj = st.g;
-#pragma unroll
-      for (int o2 = 1; o2 < 32; o2 <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, gj, o2);
-        if (lane >= o2) gj += y;
-      }
-      const float LC = __shfl_sync(0xffffffffu, gj, Cc - 1);
-      Lm[lane] = gj;
-      El[lane] = expf(gj);
-      Ew[lane] = lane < Cc ? expf(LC - gj) : 0.f;   // padding tokens add nothing
-      Bt[lane] = st.b;                               // 0 past Cc
-    }
-    tc::fence_smem_to_async();   // KQ, KT and the S̄ terms, for the tensor cores
-    tc::fence_before_sync();
-    __syncthreads();
-    // ---- D0 = [K; Q; 0] K^T and D1 = (S̄_hi + S̄_lo) [K; Q]^T
-    if (tid == 0) {
-      tc::fence_after_sync();
-      constexpr uint32_t id0 = tc::idesc_bf16_f32(128, 32), id1 = tc::idesc_bf16_f32(128, 64);
-#pragma unroll
-      for (int kk = 0; kk < TC_D / 16; ++kk)
-        tc::mma_bf16(tm + D0_COL, tc::kmaj_desc(sbase + TcSmem::KQ, TC_D, kk),
-                     tc::kmaj_desc(sbase + TcSmem::KQ, TC_D, kk), id0, kk > 0);
-#pragma unroll
-      for (int kk = 0; kk < TC_D / 16; ++kk)
-        tc::mma_bf16(tm + D1_COL, tc::kmaj_desc(sbase + TcSmem::SHI, TC_D, kk),
-                     tc::kmaj_desc(sbase + TcSmem::KQ, TC_D, kk), id1, kk > 0);
-#pragma unroll
-      for (int kk = 0; kk < TC_D / 16; ++kk)
-        tc::mma_bf16(tm + D1_COL, tc::kmaj_desc(sbase + TcSmem::SLO, TC_D, kk),
-                     tc::kmaj_desc(sbase + TcSmem::KQ, TC_D, kk), id1, 1u);
-      tc::mma_commit(bar1);
-    }
-    // the next chunk's inputs load while the tensor cores run
-    if (t0 + TC_C < T) {
-      const int Cn = (T - t0 - TC_C) < TC_C ? (T - t0 - TC_C) : TC_C;
-      st.load(q, k, v, g, beta, t0 + TC_C, Cn, nH, sh, tid);
-    }
+    const uint32_t set = TcSmem::set(chunk & 1);
+    const float* Lm = reinterpret_cast<const float*>(sm + set + TcSmem::SC);
+    const float* El = Lm + TC_C;
+    const float* Ew = El + TC_C;
+    const float* Bt = Ew + TC_C;
+    // ---- D1 = (S̄_hi + S̄_lo) [K; Q]^T of this chunk has landed
     if (tid == 0 && !mbar_wait(bar1, par, status, DEV_TIMEOUT_MMA)) *ok_flag = -1;
     __syncthreads();
     if (*ok_flag != 1) {
@@ -263,52 +350,18 @@ prefill_gdn_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* __
       break;
     }
     tc::fence_after_sync();
-    // ---- S̄ k_j (warps 0-3, for the substitution); the pair products with
-    //      their decays (warps 0, 1, 4, 5: D0 rows 0-63, 16 columns each):
-    //      A_kk[j][i] = e^{Λ_j-Λ_i} k_i·k_j (i < j) as fp32 rows, and
-    //      A[j][i] = e^{Λ_j-Λ_i} k_i·q_j (i <= j) as the bf16 terms of D3's B operand
-    float pk[TC_C];
-    if (hw == 0) {
-      uint32_t x[TC_C];
-      tc::tmem_ld32(tlane + D1_COL, x);
-      tc::tmem_wait_ld(x);
+    if (!prep) {
+      // ---- forward substitution (warps 0-3, one value row each)
+      const float* Akk = reinterpret_cast<const float*>(sm + set + TcSmem::AKK);
+      const uint16_t* Vs = reinterpret_cast<const uint16_t*>(sm + set + TcSmem::VS);
+      float pk[TC_C], u[TC_C];
+      {
+        uint32_t x[TC_C];
+        tc::tmem_ld32(tlane + D1_COL, x);
+        tc::tmem_wait_ld(x);
 #pragma unroll
-      for (int j = 0; j < TC_C; ++j) pk[j] = __uint_as_float(x[j]);
-    }
-    if (q4 < 2) {
-      uint32_t x[16];
-      tc::tmem_ld16(tlane + D0_COL + 16 * hw, x);
-      tc::tmem_wait_ld16(x);
-      const int j = lane, i0 = 16 * hw;
-      const float lj = Lm[j];
-      float w[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const int i = i0 + e;
-        const bool live = (q4 == 0 ? i < j : i <= j) && j < Cc;
-        w[e] = live ? __uint_as_float(x[e]) * __expf(lj - Lm[i]) : 0.f;   // exponent <= 0
+        for (int j = 0; j < TC_C; ++j) pk[j] = __uint_as_float(x[j]);
       }
-      if (q4 == 0) {
-#pragma unroll
-        for (int e4 = 0; e4 < 4; ++e4)
-          *reinterpret_cast<float4*>(Akk + j * AP + i0 + 4 * e4) =
-              make_float4(w[4 * e4], w[4 * e4 + 1], w[4 * e4 + 2], w[4 * e4 + 3]);
-        if (hw == 1) *reinterpret_cast<float4*>(Akk + j * AP + TC_C) = make_float4(0.f, 0.f, 0.f, 0.f);
-      } else {
-#pragma unroll
-        for (int c8 = 0; c8 < 2; ++c8) {
-          uint4 hv, lv;
-          split8(w + 8 * c8, hv, lv);
-          const uint32_t off = tc::kmaj_off(j, i0 + 8 * c8, TC_C);
-          *reinterpret_cast<uint4*>(sm + TcSmem::AHI + off) = hv;
-          *reinterpret_cast<uint4*>(sm + TcSmem::ALO + off) = lv;
-        }
-      }
-    }
-    __syncthreads();
-    // ---- forward substitution (warps 0-3, one value row each)
-    float u[TC_C];
-    if (hw == 0) {
 #pragma unroll
       for (int j = 0; j < TC_C; ++j) u[j] = 0.f;   // entries not yet solved multiply zero coefficients
 #pragma unroll
@@ -338,37 +391,52 @@ prefill_gdn_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* __
         *reinterpret_cast<uint4*>(sm + TcSmem::UHI + off) = hv;
         *reinterpret_cast<uint4*>(sm + TcSmem::ULO + off) = lv;
       }
+    } else if (chunk + 1 < nch) {
+      // ---- meanwhile warps 4-7 prepare the next chunk and start loading the one after
+      const int Cn = (T - t0 - TC_C) < TC_C ? (T - t0 - TC_C) : TC_C;
+      gdn_prepare(sm, st, TcSmem::set((chunk + 1) & 1), Cn, chunk + 1, tm + D0_COL, sbase, bar0,
+                  status, ok_flag);
+      if (chunk + 2 < nch) {
+        const int C2 = (T - t0 - 2 * TC_C) < TC_C ? (T - t0 - 2 * TC_C) : TC_C;
+        st.load(q, k, v, g, beta, t0 + 2 * TC_C, C2, nH, sh, tid - 128);
+      }
     }
-    tc::fence_smem_to_async();   // W, U terms, for the tensor cores
+    tc::fence_smem_to_async();   // W, U and the next chunk's operands, for the tensor cores
     tc::fence_before_sync();
     __syncthreads();
+    if (*ok_flag != 1) {
+      ok = false;
+      break;
+    }
     // ---- D2 = (W_hi + W_lo) K and D3 = U_hi A_hi^T + U_lo A_hi^T + U_hi A_lo^T
     if (tid == 0) {
       tc::fence_after_sync();
       constexpr uint32_t id2 = tc::idesc_bf16_f32(128, 128), id3 = tc::idesc_bf16_f32(128, 32);
+      const uint32_t kt = sbase + set + TcSmem::KT;
+      const uint32_t ahi = sbase + set + TcSmem::AHI, alo = sbase + set + TcSmem::ALO;
 #pragma unroll
       for (int kk = 0; kk < TC_C / 16; ++kk)
         tc::mma_bf16(tm + D2_COL, tc::kmaj_desc(sbase + TcSmem::WHI, TC_C, kk),
-                     tc::kmaj_desc(sbase + TcSmem::KT, TC_C, kk), id2, kk > 0);
+                     tc::kmaj_desc(kt, TC_C, kk), id2, kk > 0);
 #pragma unroll
       for (int kk = 0; kk < TC_C / 16; ++kk)
         tc::mma_bf16(tm + D2_COL, tc::kmaj_desc(sbase + TcSmem::WLO, TC_C, kk),
-                     tc::kmaj_desc(sbase + TcSmem::KT, TC_C, kk), id2, 1u);
+                     tc::kmaj_desc(kt, TC_C, kk), id2, 1u);
 #pragma unroll
       for (int kk = 0; kk < TC_C / 16; ++kk)
         tc::mma_bf16(tm + D3_COL, tc::kmaj_desc(sbase + TcSmem::UHI, TC_C, kk),
-                     tc::kmaj_desc(sbase + TcSmem::AHI, TC_C, kk), id3, kk > 0);
+                     tc::kmaj_desc(ahi, TC_C, kk), id3, kk > 0);
 #pragma unroll
       for (int kk = 0; kk < TC_C / 16; ++kk)
         tc::mma_bf16(tm + D3_COL, tc::kmaj_desc(sbase + TcSmem::ULO, TC_C, kk),
-                     tc::kmaj_desc(sbase + TcSmem::AHI, TC_C, kk), id3, 1u);
+                     tc::kmaj_desc(ahi, TC_C, kk), id3, 1u);
 #pragma unroll
       for (int kk = 0; kk < TC_C / 16; ++kk)
         tc::mma_bf16(tm + D3_COL, tc::kmaj_desc(sbase + TcSmem::UHI, TC_C, kk),
-                     tc::kmaj_desc(sbase + TcSmem::ALO, TC_C, kk), id3, 1u);
+                     tc::kmaj_desc(alo, TC_C, kk), id3, 1u);
       tc::mma_commit(bar2);
+      if (!mbar_wait(bar2, par, status, DEV_TIMEOUT_MMA)) *ok_flag = -2;
     }
-    if (tid == 0 && !mbar_wait(bar2, par, status, DEV_TIMEOUT_MMA)) *ok_flag = -2;
     __syncthreads();
     if (*ok_flag != 1) {
       ok = false;
@@ -396,7 +464,7 @@ prefill_gdn_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* __
         }
       }
     }
-    // ---- S̄ <- e^{Λ_C} S̄ + D2 in registers; its bf16 terms for the next chunk
+    // ---- S̄ <- e^{Λ_C} S̄ + D2 in registers; its bf16 terms for the next chunk's D1
     {
       const float eC = El[Cc - 1];
       uint32_t x0[32], x1[32];
@@ -418,13 +486,31 @@ prefill_gdn_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* __
         *reinterpret_cast<uint4*>(sm + TcSmem::SLO + off) = lv;
       }
     }
+    tc::fence_smem_to_async();   // the S̄ terms, for the next D1
     tc::fence_before_sync();
-    __syncthreads();   // every thread is done with this chunk's shared buffers
+    __syncthreads();
+    // ---- D1 of the next chunk (its K, Q were staged during the substitution)
+    if (chunk + 1 < nch && tid == 0) {
+      tc::fence_after_sync();
+      constexpr uint32_t id1 = tc::idesc_bf16_f32(128, 64);
+#pragma unroll
+      for (int kk = 0; kk < TC_D / 16; ++kk)
+        tc::mma_bf16(tm + D1_COL, tc::kmaj_desc(sbase + TcSmem::SHI, TC_D, kk),
+                     tc::kmaj_desc(sbase + TcSmem::KQ, TC_D, kk), id1, kk > 0);
+#pragma unroll
+      for (int kk = 0; kk < TC_D / 16; ++kk)
+        tc::mma_bf16(tm + D1_COL, tc::kmaj_desc(sbase + TcSmem::SLO, TC_D, kk),
+                     tc::kmaj_desc(sbase + TcSmem::KQ, TC_D, kk), id1, 1u);
+      tc::mma_commit(bar1);
+    }
   }
   if (!ok && tid == 0) {
-    // let the MMAs still in flight (those of the wait that gave up) land
-    // before the tensor memory is freed; the drain is bounded too
-    mbar_drain(*ok_flag == -1 ? bar1 : bar2, (uint32_t)chunk & 1u);
+    // let the MMAs still in flight (those of the wait that gave up) land before
+    // the tensor memory is freed; the drain is bounded too
+    const int f = *ok_flag;
+    if (f == -1) mbar_drain(bar1, (uint32_t)chunk & 1u);
+    else if (f == -2) mbar_drain(bar2, (uint32_t)chunk & 1u);
+    else if (f == -3 || f == -4) mbar_drain(bar0, (uint32_t)(-3 - f));
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -501,7 +587,7 @@ struct KdaStage {
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       int j, cv;
-      TcStage::piece(tid + e * TC_THREADS, j, cv);
+      chunk_piece(tid + e * TC_THREADS, j, cv);
       if (j < Cc) {
         const size_t base = ((size_t)(t0 + j) * nH + sh) * TC_D + cv * 8;
         k[e] = *reinterpret_cast<const uint4*>(kg + base);
@@ -527,7 +613,7 @@ struct KdaStage {
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       int j, cv;
-      TcStage::piece(tid + e * TC_THREADS, j, cv);
+      chunk_piece(tid + e * TC_THREADS, j, cv);
       *reinterpret_cast<uint4*>(sm + KdaSmem::VS + (j * VP + cv * 8) * 2) = v[e];
     }
 #pragma unroll
@@ -634,7 +720,7 @@ prefill_kda_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* __
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       int j, cv;
-      TcStage::piece(tid + e * TC_THREADS, j, cv);
+      chunk_piece(tid + e * TC_THREADS, j, cv);
       float kx[8], qx[8], kh[8], qh[8], kb[8], kt[8];
       unpack8(st.k[e], kx);
       unpack8(st.q[e], qx);
