@@ -85,3 +85,36 @@ def test_kda_prefill_strong_decay_matches_oracle(strong):
     ctx.close()
     assert max_step_rel(o.float().cpu().reshape(T, B * H, d).numpy(), o_ref) <= 1e-4
     assert rel_err(S, S_ref) <= STATE_TOL
+
+
+@pytest.mark.parametrize("T", [33, 64, 97, 130])
+@pytest.mark.parametrize("op", [gen.GDN, gen.KDA])
+def test_tensor_core_prefill_chunk_counts(op, T):
+    """The tensor-core kernels at d = 128 pipeline their chunks: the next
+    chunk's operands go to the other half of doubled buffers while the current
+    chunk is solved, and inputs two chunks ahead are prefetched.  Chunk counts
+    2, 2, 4 and 5 (T = 33, 64, 97, 130: ragged and full last chunks), fp32
+    outputs, then decode steps from the prefilled state: every output and the
+    state match the oracle."""
+    from linear_attention_recurrent_gdn_gb300 import deltalog as dl
+    B, H, d, M, Td = 3, 4, 128, 8, 5
+    x, S0, bonus = make_case(op, B, H, d, T + Td, seed=5400 + op * 7 + T)
+    o_ref, S_ref, S_snap = oracle_run(op, x, S0, bonus, snap=[T - 1])
+    ctx = dl.DeltaLog(op, B, H, d, d, M, out_bf16=False)
+    slots = list(range(B))
+    ctx.set_state(slots, S0.cuda())
+    dev = {k_: (v_.cuda() if v_ is not None else None) for k_, v_ in x.items()}
+    sl = lambda key: dev[key][:T].contiguous() if dev[key] is not None else None
+    o_pf = ctx.prefill(slots, sl("q"), sl("k"), sl("v"), sl("g"), sl("beta"))
+    S_pf = ctx.read_state(slots).cpu().reshape(B * H, d, d).numpy()
+    assert rel_err(S_pf, S_snap[0]) <= STATE_TOL
+    assert max_step_rel(o_pf.cpu().reshape(T, B * H, d).numpy(), o_ref[:T]) <= 1e-4
+    outs = []
+    for t in range(T, T + Td):
+        beta = dev["beta"][t] if dev["beta"] is not None else None
+        outs.append(ctx.step(slots, dev["q"][t], dev["k"][t], dev["v"][t], dev["g"][t], beta).float())
+    o = torch.stack(outs).cpu().reshape(Td, B * H, d).numpy()
+    assert max_step_rel(o, o_ref[T:]) <= 1e-4
+    S = ctx.read_state(slots).cpu().reshape(B * H, d, d).numpy()
+    assert rel_err(S, S_ref) <= STATE_TOL
+    ctx.close()
