@@ -198,10 +198,11 @@ dl_status dl_step_host(dl_ctx *ctx, const int32_t *slots, int32_t n,
  * overlap the computation: tokens travel in groups (one copy per tensor; small
  * tensors are grouped until a copy reaches 2 MiB, up to 8 tokens and 64 MiB of
  * staging a group), and while a group's tokens run on the
- * context's stream an upload stream copies the next group's inputs into the
- * second of two device staging sets and a download stream copies the previous
- * group's outputs back.  The staging sets and the two streams are owned by the
- * context and made on the first call.  Host memory must be pinned for the copies to run
+ * context's stream an upload stream copies the next groups' inputs into the
+ * next of four device staging sets (a set is reused once its group's outputs
+ * are back) and a download stream copies earlier groups' outputs back.  The
+ * staging sets and the two streams are owned by the context and made on the
+ * first call.  Host memory must be pinned for the copies to run
  * asynchronously.  Returns once every output is in host memory; on an error
  * (for example DL_EBUSY for a frozen slot at the first token) the tokens
  * before it have been decoded and copied back. */

@@ -34,6 +34,15 @@ struct TimedPair {
 
 }  // namespace
 
+// Staging sets of dl_decode_host.  A set is reused only after the download of
+// the group before it, so with two sets the upload of group j + 2 waited on the
+// download of group j and the chain download -> upload -> compute set the pace
+// whenever the two copies together took longer than a group's compute.
+// Measured on GB300 (GDN, 256 slots x 32 heads, one token a group, copies at
+// 81 GB/s up and 27 GB/s down): two sets gave 59.1 M tokens·heads/s end to end,
+// four give 83.7 M, against 87.1 M on the device.
+constexpr int PIPE_SETS = 4;
+
 struct dl_ctx {
   dl_config cfg{};
   cudaStream_t stream = nullptr;
@@ -61,14 +70,14 @@ struct dl_ctx {
   int32_t coef_rows = 0;
   void* stage = nullptr;        // device staging for dl_step_host
   size_t stage_bytes = 0;
-  // dl_decode_host: two device staging sets (token t uses set t % 2), an
-  // upload and a download stream, and the events that order them
+  // dl_decode_host: PIPE_SETS device staging sets (token group j uses set
+  // j % PIPE_SETS), an upload and a download stream, and the events that
+  // order them
   void* pipe_stage = nullptr;
   size_t pipe_set_bytes = 0;
   int pipe_group = 1;          // tokens per staging set
   cudaStream_t up = nullptr, down = nullptr;
-  cudaEvent_t ev_in[2] = {nullptr, nullptr}, ev_done[2] = {nullptr, nullptr},
-              ev_out[2] = {nullptr, nullptr};
+  cudaEvent_t ev_in[PIPE_SETS] = {}, ev_done[PIPE_SETS] = {}, ev_out[PIPE_SETS] = {};
   std::vector<int32_t> plan;
   std::unique_ptr<dl::StepArgs> step_args;
   std::unique_ptr<dl::SlotListArgs> list_args;
@@ -134,7 +143,7 @@ void free_all(dl_ctx* c) {
     if (p) cudaFree(p);
   c->pipe_stage = nullptr;
   for (cudaEvent_t* ev : {c->ev_in, c->ev_done, c->ev_out})
-    for (int b = 0; b < 2; ++b)
+    for (int b = 0; b < PIPE_SETS; ++b)
       if (ev[b]) {
         cudaEventDestroy(ev[b]);
         ev[b] = nullptr;
@@ -189,9 +198,11 @@ int prep_warps(int op, int dk, int G, int M) {
 
 enum class Kern { Append, Fused, Eager };
 
-// `merge_launch`: every row of the launch merges (rows known on the host).
-dl::PipePlan pipe_shape(const dl_ctx* c, int G, Kern k, bool merge_launch = false) {
-  const int aux = k == Kern::Append ? c->L.aux_bytes : k == Kern::Fused ? c->L.f_bytes : c->L.e_bytes;
+// `L`: the launch's layout (its aux slots' size); `merge_launch`: every row of
+// the launch merges (rows known on the host).
+dl::PipePlan pipe_shape(const dl_ctx* c, const dl::Layout& L, int G, Kern k,
+                        bool merge_launch = false) {
+  const int aux = k == Kern::Append ? L.aux_bytes : k == Kern::Fused ? L.f_bytes : L.e_bytes;
   return dl::plan_pipeline(c->cfg.d_k, aux, G, c->smem_optin, c->smem_per_sm, shape_override(),
                            k == Kern::Fused ? prep_warps(c->cfg.op, c->cfg.d_k, G, c->cfg.merge_interval) : -1,
                            c->regs[(int)k], merge_launch && k == Kern::Fused);
@@ -322,8 +333,19 @@ dl_status run_step(dl_ctx* c, const int32_t* slots, int32_t n, const void* q, co
     bool all_merge = fused && a.plan_dev == nullptr && f.merge_interval >= 8;
     for (int32_t i = 0; i < rows && all_merge; ++i)
       all_merge = a.items[i].n + 1 == f.merge_interval;
-    const dl::PipePlan ps =
-        pipe_shape(c, a.G, eager ? Kern::Eager : fused ? Kern::Fused : Kern::Append, all_merge);
+    // Aux slots hold the launch's longest log (plus the current token's row)
+    // when every row's log length is known on the host; a ragged window's
+    // rows are only known on the device, so its slots hold M rows.
+    a.arows = 0;
+    if (a.plan_dev == nullptr) {
+      int32_t nmax = 0;
+      for (int32_t i = 0; i < rows; ++i) nmax = a.items[i].n > nmax ? a.items[i].n : nmax;
+      a.arows = nmax + 1;
+    }
+    const dl::Layout Ll = dl::make_layout(f.op, f.merge_interval, f.d_k, f.d_v, a.arows);
+    a.aux_bytes = Ll.aux_bytes;
+    const dl::PipePlan ps = pipe_shape(c, Ll, a.G, eager ? Kern::Eager : fused ? Kern::Fused : Kern::Append,
+                                       all_merge);
     if (ps.ns == 0) return set_err(c, DL_EUNSUPPORTED, "pipeline does not fit in shared memory");
     a.ns = ps.ns;
     a.na = ps.na;
@@ -656,9 +678,9 @@ dl_status dl_decode_host(dl_ctx* c, const int32_t* slots, int32_t n, int32_t T, 
   const size_t bb = (size_t)n * H * 4, bo = (size_t)n * H * f.d_v * (f.out_bf16 ? 2 : 4);
   auto r256 = [](size_t x) { return (x + 255) & ~(size_t)255; };
   if (!c->pipe_stage) {
-    // Two staging sets, each for a group of tokens of the largest batch the
-    // context can take: a group's inputs travel in one copy per tensor and
-    // its outputs in one copy back.  Each copy has a fixed cost, so small
+    // PIPE_SETS staging sets, each for a group of tokens of the largest batch
+    // the context can take: a group's inputs travel in one copy per tensor
+    // and its outputs in one copy back.  Each copy has a fixed cost, so small
     // per-token tensors are grouped until a key tensor's copy reaches 2 MiB
     // (at most 8 tokens and 64 MiB a set); large ones go token by token,
     // which keeps the pipeline fine-grained.
@@ -674,7 +696,7 @@ dl_status dl_decode_host(dl_ctx* c, const int32_t* slots, int32_t n, int32_t T, 
     const size_t set = 2 * r256(tg * Sn * H * f.d_k * 2) + r256(tg * Sn * H * f.d_v * 2) +
                        r256(tg * Sn * H * (f.op == DL_GDN ? 1 : f.d_k) * 4) +
                        r256(tg * Sn * H * 4) + r256(tg * Sn * H * f.d_v * 4);
-    if (cudaMalloc(&c->pipe_stage, 2 * set) != cudaSuccess) {
+    if (cudaMalloc(&c->pipe_stage, PIPE_SETS * set) != cudaSuccess) {
       c->pipe_stage = nullptr;
       return set_err(c, DL_ENOMEM, "staging allocation");
     }
@@ -682,7 +704,7 @@ dl_status dl_decode_host(dl_ctx* c, const int32_t* slots, int32_t n, int32_t T, 
     c->pipe_group = tg;
     cudaError_t e = cudaStreamCreateWithFlags(&c->up, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->down, cudaStreamNonBlocking);
-    for (int b = 0; b < 2 && e == cudaSuccess; ++b) {
+    for (int b = 0; b < PIPE_SETS && e == cudaSuccess; ++b) {
       e = cudaEventCreateWithFlags(&c->ev_in[b], cudaEventDisableTiming);
       if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->ev_done[b], cudaEventDisableTiming);
       if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->ev_out[b], cudaEventDisableTiming);
@@ -699,7 +721,7 @@ dl_status dl_decode_host(dl_ctx* c, const int32_t* slots, int32_t n, int32_t T, 
   cudaError_t e = cudaSuccess;
   int grp = 0;
   for (int32_t t0 = 0; t0 < T && rc == DL_OK && e == cudaSuccess; t0 += TG, ++grp) {
-    const int b = grp & 1;
+    const int b = grp % PIPE_SETS;
     const int tn = (T - t0) < TG ? (T - t0) : TG;   // tokens in this group
     // the set's regions, each holding the group's tokens contiguously
     unsigned char* p = static_cast<unsigned char*>(c->pipe_stage) + (size_t)b * c->pipe_set_bytes;
@@ -709,9 +731,9 @@ dl_status dl_decode_host(dl_ctx* c, const int32_t* slots, int32_t n, int32_t T, 
     unsigned char* dg = p; p += r256((size_t)TG * bg);
     unsigned char* db = p; p += r256((size_t)TG * bb);
     unsigned char* dout = p;
-    // set b is free once group grp-2's outputs have been downloaded (which
-    // also follows its kernels, the last readers of its inputs)
-    if (grp >= 2) e = cudaStreamWaitEvent(c->up, c->ev_out[b], 0);
+    // set b is free once group grp - PIPE_SETS's outputs have been downloaded
+    // (which also follows its kernels, the last readers of its inputs)
+    if (grp >= PIPE_SETS) e = cudaStreamWaitEvent(c->up, c->ev_out[b], 0);
     const size_t t0s = (size_t)t0;
     if (e == cudaSuccess) e = cudaMemcpyAsync(dq, hq + t0s * bq, tn * bq, cudaMemcpyHostToDevice, c->up);
     if (e == cudaSuccess) e = cudaMemcpyAsync(dk, hk + t0s * bq, tn * bq, cudaMemcpyHostToDevice, c->up);

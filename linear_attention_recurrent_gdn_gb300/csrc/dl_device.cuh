@@ -77,6 +77,8 @@ struct StepArgs {
   int32_t pdl_prefetch;  // 1: the previous launch on the stream was a step of this context, so
                          //    tiles of rows with n > 0 may stream before griddepcontrol.wait
   int32_t aux_bytes;     // bytes of one aux slot
+  int32_t arows;         // log rows an aux slot holds in this launch (0: M); every row's
+                         // log length n must be below it
   int32_t out_bf16;
   float scale;
   // How long a bounded wait spins before it records an error and gives up

@@ -20,6 +20,10 @@
 //   U      value-side log rows 0..n-1 (fp32 u_j; bf16 v_j for RWKV6) and one
 //          more row: u_t written by the consumer at a merge, or v_t (RWKV6)
 //   kl     GDN merge: key log rows 0..n-1 and k_t as row n, bf16 [M][d_k]
+// The log-row sections hold `arows` rows: M by default, or the largest log
+// length n of a launch's rows plus one (the current token's row), when the
+// launcher knows every row's n, so that short logs leave room for more units
+// in flight.
 #pragma once
 
 #ifdef __CUDACC__
@@ -45,10 +49,11 @@ struct Layout {
 DL_HD inline int round4(int x) { return (x + 3) & ~3; }
 DL_HD inline int round16(int x) { return (x + 15) & ~15; }
 
-DL_HD inline Layout make_layout(int op, int M, int dk, int dv) {
+DL_HD inline Layout make_layout(int op, int M, int dk, int dv, int arows = 0) {
   Layout L{};
   const bool perkey = (op != 0);
   const bool delta = (op != 2);
+  const int R = (arows > 0 && arows < M) ? arows : M;   // log rows of an aux slot
   L.Mcap = M > 1 ? M - 1 : 1;
   L.Mcap4 = round4(L.Mcap);
   L.M4 = round4(M);
@@ -58,8 +63,8 @@ DL_HD inline Layout make_layout(int op, int M, int dk, int dv) {
   L.aux_coef = off; off += round16(L.CB * 4);
   L.aux_kq = off;   off += (op == 0) ? 2 * dk * 2 : 0;
   L.aux_v = off;    off += delta ? round16(dv * 2) : 0;
-  L.aux_U = off;    off += M * dv * (delta ? 4 : 2);
-  L.aux_kl = off;   off += (op == 0) ? M * dk * 2 : 0;
+  L.aux_U = off;    off += R * dv * (delta ? 4 : 2);
+  L.aux_kl = off;   off += (op == 0) ? R * dk * 2 : 0;
   L.aux_bytes = round16(off);
   off = 0;
   L.e_kq = off;     off += 2 * dk * 2;
@@ -70,9 +75,9 @@ DL_HD inline Layout make_layout(int op, int M, int dk, int dv) {
   L.f_coef = off;   off += round16((L.P0 + (perkey ? dk : L.M4)) * 4);
   L.f_kq = off;     off += 2 * dk * 2;
   L.f_v = off;      off += delta ? round16(dv * 2) : 0;
-  L.f_U = off;      off += M * dv * (delta ? 4 : 2);
-  L.f_kl = off;     off += M * dk * 2;
-  L.f_L = off;      off += perkey ? M * dk * 4 : L.M4 * 4;
+  L.f_U = off;      off += R * dv * (delta ? 4 : 2);
+  L.f_kl = off;     off += R * dk * 2;
+  L.f_L = off;      off += perkey ? R * dk * 4 : round4(R) * 4;
   L.f_g = off;      off += perkey ? dk * 4 : 16;
   L.f_beta = off;   off += delta ? 16 : 0;
   L.f_bonus = off;  off += (op == 2) ? dk * 4 : 0;
@@ -90,7 +95,7 @@ DL_HD inline Layout make_layout(int op, int M, int dk, int dv) {
 // nothing fits.
 struct PipePlan {
   int cps, ncw, ns, na, npw;
-  int smem;   // dynamic shared memory per CTA (bytes)
+  int smem;   // dynamic shared memory per CTA (bytes): the CTA's share of the SM
 };
 
 // Fit one candidate shape (cps CTAs per SM, ncw consumer warps, R stages per
@@ -125,7 +130,15 @@ inline PipePlan fit_pipeline(int cps, int ncw, int R, int dk, int aux_bytes, int
   na = na / mult * mult;
   const long need = (long)ns * tile + (long)na * aux_bytes;
   if (na < na_min || ns > 24 || na > 24 || need > budget) return none;
-  return PipePlan{cps, ncw, ns, na, npw > 0 ? npw : 0, (int)(1024 + need)};
+  // Each CTA claims its whole share of the SM's shared memory, not just what
+  // its stages and slots need: consecutive launches of a decode loop then ask
+  // for the same amount whenever they run the same number of CTAs per SM,
+  // whatever their log lengths.  Measured on GB300 (RWKV6 decode, aux slots
+  // sized by the launch's log length): launches whose dynamic shared memory
+  // changed from one to the next ran M = 4 windows at 221.6 M tokens·heads/s,
+  // against 280.2 M once each claimed its full share.
+  const int claim = (per_cta < smem_optin ? per_cta : smem_optin) & ~127;
+  return PipePlan{cps, ncw, ns, na, npw > 0 ? npw : 0, claim};
 }
 
 // Stages hold one 16 KiB bulk copy: one value tile at d_k = 128, two at d_k = 64
@@ -144,22 +157,28 @@ inline PipePlan plan_pipeline(int dk, int aux_bytes, int G, int smem_optin, int 
   }
   // Candidates in order of preference (cps, ncw, R), from measurements of
   // these shapes on GB300.  Two CTAs per SM with one 16 KiB stage per consumer
-  // warp stream best for the two-kernel and eager forms; the fused form does
-  // better still with four CTAs of two consumer warps where their aux slots
-  // fit (more producers, and more units whose coefficients are computed at
-  // once).  8 KiB stages (d_k = 64 with one tile per unit) need more stages
-  // per warp.
+  // warp stream best for the two-kernel and eager forms, and for the fused
+  // form's units of several stages (their prep warps): measured with aux slots
+  // sized by the launch's log length, (2,4,1) beat (4,2,1), (3,2,1), (2,3,1)
+  // and (1,8,1) for GDN and KDA at every M of 4 to 32 where it fits (GDN
+  // M = 32: 75.1 against 68.6 M tokens·heads/s for (4,2,1); M = 4: 78.2
+  // against 67.2).  The fused form's one-stage units (d_k = 64) do better
+  // with four CTAs of two consumer warps where their aux slots fit (more
+  // producers, and more units whose coefficients are computed at once).
+  // 8 KiB stages (d_k = 64 with one tile per unit) need more stages per warp.
   // Each list ends with small shapes that only large aux slots fall back to
   // (per-key ops at M near 32), so that every supported configuration has one.
   static const int c16k[][3] = {{2, 4, 1}, {2, 3, 1}, {1, 8, 1}, {1, 6, 1}, {1, 4, 1},
                                 {2, 2, 1}, {1, 2, 1}, {2, 1, 1}, {1, 1, 1}};
   static const int c16k_fused[][3] = {{4, 2, 1}, {2, 4, 1}, {3, 2, 1}, {2, 3, 1}, {1, 8, 1},
                                       {1, 4, 1}, {2, 2, 1}, {1, 2, 1}, {2, 1, 1}, {1, 1, 1}};
+  static const int c16k_prep[][3] = {{2, 4, 1}, {3, 2, 1}, {2, 3, 1}, {4, 2, 1}, {1, 8, 1},
+                                     {1, 4, 1}, {2, 2, 1}, {1, 2, 1}, {2, 1, 1}, {1, 1, 1}};
   static const int c8k[][3] = {{2, 4, 3}, {2, 4, 2}, {2, 3, 2}, {1, 8, 2}, {1, 8, 1}, {1, 4, 1},
                                {2, 2, 1}, {1, 2, 1}, {2, 1, 1}, {1, 1, 1}};
   const bool big = 32 * dk * 4 * tps >= 16384;
   const bool fused = npw >= 0;
-  const int (*cand)[3] = !big ? c8k : fused ? c16k_fused : c16k;
+  const int (*cand)[3] = !big ? c8k : !fused ? c16k : npw == 0 ? c16k_fused : c16k_prep;
   const int ncand = !big ? 10 : fused ? 10 : 9;
   const int npref = ncand - 4;   // the shapes before the fallbacks
   if (npw == 0 && merge_launch && dk == 64) {

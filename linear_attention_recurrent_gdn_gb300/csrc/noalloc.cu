@@ -210,6 +210,7 @@ extern "C" dl_status dl_step_noalloc(const dl_config* cfg, const dl_state_view* 
   a.out_bf16 = f.out_bf16;
   a.scale = f.scale;
   a.aux_bytes = L.aux_bytes;
+  a.arows = 0;   // aux slots sized for M log rows
   for (int32_t i = 0; i < n; ++i)
     a.items[i] = dl::StepItem{plan[4 * (size_t)i], plan[4 * (size_t)i + 1], plan[4 * (size_t)i + 2]};
   const int nvt = f.d_v / dl::BV;

@@ -703,7 +703,7 @@ __global__ void __maxnreg__(128) pipe_kernel(const __grid_constant__ StepArgs a)
   static_assert(MODE != FUSED || NE == 8 || NE == 16 || NE == 32, "fused form needs NE");
   extern __shared__ __align__(1024) unsigned char smem[];
   constexpr uint32_t TILE_BYTES = BV * DK * 4;
-  const Layout Lay = make_layout(OP, a.M, DK, DV);
+  const Layout Lay = make_layout(OP, a.M, DK, DV, a.arows);
   const int NS = a.ns, NA = a.na, G = a.G, NCWr = a.ncw, TPS = a.tps;
   const int IPU = G / TPS;                       // stage items per unit
   const uint32_t STAGE_BYTES = TILE_BYTES * TPS; // one bulk copy per stage item

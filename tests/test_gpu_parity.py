@@ -336,6 +336,28 @@ def test_decode_host_matches_device_path(op, staging):
     assert list(ctx.get_meta()[0]) == [T % M] * B
 
 
+@pytest.mark.parametrize("op", OPS)
+def test_decode_host_wraps_the_staging_ring(op):
+    """Enough token groups (eight tokens a group at this batch) that each of
+    the four staging sets is reused twice, with a ragged last group: the
+    outputs, the state and the log lengths are the bits of dl_step on device
+    buffers."""
+    from linear_attention_recurrent_gdn_gb300 import deltalog as dl
+    B, H, d, M = 6, 4, 128 if op != gen.RWKV6 else 64, 4
+    T = 8 * 9 + 3
+    x, S0, bonus = make_case(op, B, H, d, T, seed=960 + op)
+    o_dev, states, ref = gpu_run(op, x, S0, bonus, M, snap=(T - 1,))
+    ctx = dl.DeltaLog(op, B, H, d, d, M)
+    ctx.set_state(list(range(B)), S0.cuda())
+    if bonus is not None:
+        ctx.set_bonus(bonus.cuda())
+    pin = {k_: (v_.contiguous().pin_memory() if v_ is not None else None) for k_, v_ in x.items()}
+    o = ctx.decode_host(list(range(B)), pin["q"], pin["k"], pin["v"], pin["g"], pin["beta"])
+    assert torch.equal(o.float(), o_dev)
+    assert torch.equal(ctx.read_state(list(range(B))).cpu(), states[T - 1])
+    assert list(ctx.get_meta()[0]) == [T % M] * B
+
+
 def test_decode_host_frozen_slot_is_refused():
     from linear_attention_recurrent_gdn_gb300 import deltalog as dl
     B, H, d, M, T = 3, 2, 64, 4, 5
