@@ -561,38 +561,37 @@ __device__ __forceinline__ bool consume_append(const StepArgs& a, const Layout& 
 }
 
 // RWKV6 append step at d_k = 64, where one stage holds both 32-row tiles of the
-// slot-head.  RWKV6 needs one dot product per row, so both tiles' partial sums
-// fit in registers and their reductions and replay chains run interleaved.
-// The arithmetic is consume_append's, in the same order.
+// slot-head.  RWKV6 needs one dot product per row, so each lane computes its
+// row of both tiles alone, and the two replay chains run interleaved.  The
+// arithmetic is consume_append's, with the row sums in another order.
 template <int DK, int DV>
 __device__ __forceinline__ void consume_rwkv6_pair(const StepArgs& a, const Layout& Lay,
                                                    const UnitPos& p, int vt0, const float* T,
                                                    const AuxView& av, int lane,
                                                    uint32_t empty_bar, int n) {
-  constexpr int VEC = DK / 32;
+  static_assert(DK == 64, "one 16 KiB stage holds both tiles at d_k = 64");
   const float* cf = av.cf;
-  float rv[VEC];
-  ldvec<VEC>(rv, cf + HDR + 2 * Lay.Mcap4 + lane * VEC);   // r̂
-  const float* T1 = T + BV * DK;
-  float pa[32], pb[32];
+  // Lane l takes row l of each tile whole (no cross-lane reduction): it reads
+  // the row and r̂ in 16-byte chunks, starting at chunk l mod 16, so that the
+  // eight lanes of each quarter-warp read eight different chunks, which sit in
+  // different banks.  Four partial sums per row.
+  const float* R = cf + HDR + 2 * Lay.Mcap4;   // r̂
+  const float* T0 = T + lane * DK;
+  const float* T1 = T + BV * DK + lane * DK;
+  float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int r = 0; r < 32; ++r) {
-    float t0[VEC], t1[VEC];
-    ldvec<VEC>(t0, T + r * DK + lane * VEC);
-    ldvec<VEC>(t1, T1 + r * DK + lane * VEC);
-    float x0 = 0.f, x1 = 0.f;
-#pragma unroll
-    for (int c = 0; c < VEC; ++c) {
-      x0 += t0[c] * rv[c];
-      x1 += t1[c] * rv[c];
-    }
-    pa[r] = x0;
-    pb[r] = x1;
+  for (int k = 0; k < DK / 4; ++k) {
+    const int ch = ((k + lane) & (DK / 4 - 1)) * 4;
+    const float4 r = *reinterpret_cast<const float4*>(R + ch);
+    const float4 x = *reinterpret_cast<const float4*>(T0 + ch);
+    const float4 y = *reinterpret_cast<const float4*>(T1 + ch);
+    s0[0] += x.x * r.x; s0[1] += x.y * r.y; s0[2] += x.z * r.z; s0[3] += x.w * r.w;
+    s1[0] += y.x * r.x; s1[1] += y.y * r.y; s1[2] += y.z * r.z; s1[3] += y.w * r.w;
   }
   __syncwarp();
   if (lane == 0) mbar_arrive(empty_bar);
-  const float A0 = reduce_scatter32(pa, lane);
-  const float A1 = reduce_scatter32(pb, lane);
+  const float A0 = (s0[0] + s0[1]) + (s0[2] + s0[3]);
+  const float A1 = (s1[0] + s1[1]) + (s1[2] + s1[3]);
   const uint16_t* V = reinterpret_cast<const uint16_t*>(av.U);
   const int col0 = vt0 * BV + lane, col1 = col0 + BV;
   float o0 = A0, o1 = A1;
