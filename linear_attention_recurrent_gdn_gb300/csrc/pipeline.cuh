@@ -423,6 +423,23 @@ __device__ __forceinline__ AuxView aux_view(const Layout& Lay, unsigned char* ax
   return v;
 }
 
+// RWKV6's row sum S̄[row]·r̂ for row `lane` of a 32-row tile T (d_k floats a
+// row), computed by that lane alone: it reads the row and r̂ in 16-byte
+// chunks, starting at chunk lane mod (d_k / 4), so that the eight lanes of a
+// quarter-warp read eight different chunks, which sit in distinct banks
+// although the rows are a multiple of 128 bytes apart.  Four partial sums.
+// The one-tile pass and the two-tile pass both use it, so a row's sum has
+// the same bits whatever the unit size (batch invariance).
+template <int DK>
+__device__ __forceinline__ void rwkv6_row_chunk(float (&s)[4], const float* Trow, const float* R,
+                                                int kc, int lane) {
+  const int ch = ((kc + lane) & (DK / 4 - 1)) * 4;
+  const float4 r = *reinterpret_cast<const float4*>(R + ch);
+  const float4 x = *reinterpret_cast<const float4*>(Trow + ch);
+  s[0] += x.x * r.x; s[1] += x.y * r.y; s[2] += x.z * r.z; s[3] += x.w * r.w;
+}
+__device__ __forceinline__ float sum4(const float (&s)[4]) { return (s[0] + s[1]) + (s[2] + s[3]); }
+
 // Returns true if it already released the tile stage (append steps release it
 // right after the pass over the tile, so the refill overlaps the epilogue).
 template <int OP, int DK, int DV>
@@ -438,40 +455,50 @@ __device__ __forceinline__ bool consume_append(const StepArgs& a, const Layout& 
   const float* cf = av.cf;
   const int vecA = HDR + 2 * Lay.Mcap4;
 
-  float kv[VEC], qv[VEC];
-  if constexpr (OP == GDN) {
-    const uint16_t* kq16 = av.kq;
-    ldvec_bf16<VEC>(kv, kq16 + lane * VEC);
-    ldvec_bf16<VEC>(qv, kq16 + DK + lane * VEC);
-  } else if constexpr (OP == KDA) {
-    ldvec<VEC>(kv, cf + vecA + lane * VEC);
-    ldvec<VEC>(qv, cf + vecA + DK + lane * VEC);
-  } else {
-    ldvec<VEC>(kv, cf + vecA + lane * VEC);   // r̂
-  }
-
-  // pass 1: per-row partial dot products over this lane's key channels
-  float pa[32], pb[32];
-#pragma unroll
-  for (int r = 0; r < 32; ++r) {
-    float t[VEC];
-    ldvec<VEC>(t, T + r * DK + lane * VEC);
-    float x = 0.f, y = 0.f;
-#pragma unroll
-    for (int c = 0; c < VEC; ++c) {
-      x += t[c] * kv[c];
-      if (DELTA) y += t[c] * qv[c];
+  float A = 0.f, B = 0.f;
+  if constexpr (DELTA) {
+    // pass 1: per-row partial dot products over this lane's key channels (k̂
+    // and q̂ stay in registers), then a transposed reduction leaves row l's
+    // sums on lane l
+    float kv[VEC], qv[VEC];
+    if constexpr (OP == GDN) {
+      ldvec_bf16<VEC>(kv, av.kq + lane * VEC);
+      ldvec_bf16<VEC>(qv, av.kq + DK + lane * VEC);
+    } else {
+      ldvec<VEC>(kv, cf + vecA + lane * VEC);
+      ldvec<VEC>(qv, cf + vecA + DK + lane * VEC);
     }
-    pa[r] = x;
-    pb[r] = y;
+    float pa[32], pb[32];
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+      float t[VEC];
+      ldvec<VEC>(t, T + r * DK + lane * VEC);
+      float x = 0.f, y = 0.f;
+#pragma unroll
+      for (int c = 0; c < VEC; ++c) {
+        x += t[c] * kv[c];
+        y += t[c] * qv[c];
+      }
+      pa[r] = x;
+      pb[r] = y;
+    }
+    if (!merge && may_release) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty_bar);
+    }
+    A = reduce_scatter32(pa, lane);
+    B = reduce_scatter32(pb, lane);
+  } else {
+    // pass 1, RWKV6: lane l computes row l alone (rwkv6_row_chunk)
+    float s0[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kc = 0; kc < DK / 4; ++kc) rwkv6_row_chunk<DK>(s0, T + lane * DK, cf + vecA, kc, lane);
+    if (!merge && may_release) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty_bar);
+    }
+    A = sum4(s0);
   }
-  if (!merge && may_release) {
-    __syncwarp();
-    if (lane == 0) mbar_arrive(empty_bar);
-  }
-  const float A = reduce_scatter32(pa, lane);
-  float B = 0.f;
-  if constexpr (DELTA) B = reduce_scatter32(pb, lane);
 
   // row epilogue on lane = row
   const int col = vt * BV + lane;
@@ -563,7 +590,7 @@ __device__ __forceinline__ bool consume_append(const StepArgs& a, const Layout& 
 // RWKV6 append step at d_k = 64, where one stage holds both 32-row tiles of the
 // slot-head.  RWKV6 needs one dot product per row, so each lane computes its
 // row of both tiles alone, and the two replay chains run interleaved.  The
-// arithmetic is consume_append's, with the row sums in another order.
+// arithmetic and its order are consume_append's.
 template <int DK, int DV>
 __device__ __forceinline__ void consume_rwkv6_pair(const StepArgs& a, const Layout& Lay,
                                                    const UnitPos& p, int vt0, const float* T,
@@ -571,27 +598,19 @@ __device__ __forceinline__ void consume_rwkv6_pair(const StepArgs& a, const Layo
                                                    uint32_t empty_bar, int n) {
   static_assert(DK == 64, "one 16 KiB stage holds both tiles at d_k = 64");
   const float* cf = av.cf;
-  // Lane l takes row l of each tile whole (no cross-lane reduction): it reads
-  // the row and r̂ in 16-byte chunks, starting at chunk l mod 16, so that the
-  // eight lanes of each quarter-warp read eight different chunks, which sit in
-  // different banks.  Four partial sums per row.
+  // Lane l takes row l of each tile whole (rwkv6_row_chunk), both rows in one
+  // loop; the two tiles' chunks of r̂ are the same loads.
   const float* R = cf + HDR + 2 * Lay.Mcap4;   // r̂
-  const float* T0 = T + lane * DK;
-  const float* T1 = T + BV * DK + lane * DK;
   float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int k = 0; k < DK / 4; ++k) {
-    const int ch = ((k + lane) & (DK / 4 - 1)) * 4;
-    const float4 r = *reinterpret_cast<const float4*>(R + ch);
-    const float4 x = *reinterpret_cast<const float4*>(T0 + ch);
-    const float4 y = *reinterpret_cast<const float4*>(T1 + ch);
-    s0[0] += x.x * r.x; s0[1] += x.y * r.y; s0[2] += x.z * r.z; s0[3] += x.w * r.w;
-    s1[0] += y.x * r.x; s1[1] += y.y * r.y; s1[2] += y.z * r.z; s1[3] += y.w * r.w;
+  for (int kc = 0; kc < DK / 4; ++kc) {
+    rwkv6_row_chunk<DK>(s0, T + lane * DK, R, kc, lane);
+    rwkv6_row_chunk<DK>(s1, T + BV * DK + lane * DK, R, kc, lane);
   }
   __syncwarp();
   if (lane == 0) mbar_arrive(empty_bar);
-  const float A0 = (s0[0] + s0[1]) + (s0[2] + s0[3]);
-  const float A1 = (s1[0] + s1[1]) + (s1[2] + s1[3]);
+  const float A0 = sum4(s0);
+  const float A1 = sum4(s1);
   const uint16_t* V = reinterpret_cast<const uint16_t*>(av.U);
   const int col0 = vt0 * BV + lane, col1 = col0 + BV;
   float o0 = A0, o1 = A1;

@@ -30,14 +30,20 @@ def _lib():
 
 
 @pytest.mark.parametrize("op", OPS)
-def test_batch_invariance_bitwise(op):
+@pytest.mark.parametrize("d", [64, 128])
+def test_batch_invariance_bitwise(op, d):
+    """A slot stepped alone (one-tile units) gives the bits it gets inside a
+    1280 slot-head batch (whole-slot-head units: at d = 64 both tiles in one
+    stage, RWKV6's append steps through the two-tile pass), over two merges.
+    Outputs in fp32, so that a change of summation order cannot hide behind
+    bf16 rounding."""
     from linear_attention_recurrent_gdn_gb300 import deltalog as dl
-    B, H, d, M, T = 320, 4, 128, 4, 9          # 1280 slot-heads: whole-slot-head units
+    B, H, M, T = 320, 4, 4, 9                  # 1280 slot-heads: whole-slot-head units
     x, S0, bonus = make_case(op, B, H, d, T, seed=400 + op, device="cuda")
     probe = [0, 77, 319]
-    big = dl.DeltaLog(op, B, H, d, d, M)
+    big = dl.DeltaLog(op, B, H, d, d, M, out_bf16=False)
     big.set_state(list(range(B)), S0)
-    small = dl.DeltaLog(op, B, H, d, d, M)      # same slots, stepped one at a time
+    small = dl.DeltaLog(op, B, H, d, d, M, out_bf16=False)   # same slots, stepped one at a time
     small.set_state(list(range(B)), S0)
     if bonus is not None:
         big.set_bonus(bonus)
