@@ -95,6 +95,45 @@ def test_ops_bf16_output_many_units(op, d, M, staging):
     assert rel_err(_flat_S(S), S_ref) <= STATE_TOL
 
 
+@pytest.mark.parametrize("op", OPS)
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("M", [16, 32])
+def test_staggered_logs_in_one_launch(op, d, M):
+    """Slots that joined at different tokens share every launch, so one launch
+    carries rows from an empty log to a merge (its aux slots are sized for the
+    longest log among them). Each slot's outputs (fp32) and final state match
+    the oracle run over that slot's own tokens."""
+    from linear_attention_recurrent_gdn_gb300 import deltalog as dl
+    H = 3
+    lead = [0, 5, 11, 17, M - 3, M - 1]                 # tokens each slot runs before the last joins
+    B, T2 = len(lead), M + 3
+    Ttot = max(lead) + T2
+    x, S0, bonus = make_case(op, B, H, d, Ttot, seed=980 + 7 * op + d + M)
+    start = [max(lead) - L for L in lead]               # the global token at which slot s joins
+    ctx = dl.DeltaLog(op, B, H, d, d, M, out_bf16=False)
+    ctx.set_state(list(range(B)), S0.cuda())
+    if bonus is not None:
+        ctx.set_bonus(bonus.cuda())
+    dev = {k_: (v_.cuda() if v_ is not None else None) for k_, v_ in x.items()}
+    outs = {s: [] for s in range(B)}
+    for t in range(Ttot):
+        act = [s for s in range(B) if start[s] <= t]
+        idx = torch.tensor(act, device="cuda")
+        sel = lambda key: dev[key][t].index_select(0, idx).contiguous() if dev[key] is not None else None
+        o = ctx.step(act, sel("q"), sel("k"), sel("v"), sel("g"), sel("beta")).cpu()
+        for i, s in enumerate(act):
+            outs[s].append(o[i])
+    S_gpu = ctx.read_state(list(range(B))).cpu()
+    for s in range(B):
+        xs = {k_: (v_[start[s]:, s:s + 1] if v_ is not None else None) for k_, v_ in x.items()}
+        o_ref, S_ref, _ = oracle_run(op, xs, S0[s:s + 1], bonus)
+        o_s = torch.stack(outs[s]).reshape(len(outs[s]), H, d).numpy()
+        assert max_step_rel(o_s, o_ref) <= OUT_TOL_F32, s
+        assert rel_err(S_gpu[s].numpy(), S_ref) <= STATE_TOL, s
+    n, _ = ctx.get_meta()
+    assert list(n) == [(Ttot - start[s]) % M for s in range(B)]
+
+
 # ------------------------------------------------------------------- eager ----
 @pytest.mark.parametrize("op", OPS)
 @pytest.mark.parametrize("d", [64, 128])
