@@ -444,7 +444,7 @@ __device__ __forceinline__ void pair_quad(float& kk, float& qk, const float4 ki,
 }
 
 template <int OP, int DK, int DV>
-__global__ void __launch_bounds__(PF_THREADS, 1) prefill_perkey_kernel(
+__global__ void __launch_bounds__(PF_THREADS, DK == 64 ? 2 : 1) prefill_perkey_kernel(
     const __grid_constant__ SlotListArgs a, const uint16_t* __restrict__ q,
     const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, const float* __restrict__ g,
     const float* __restrict__ beta, const float* __restrict__ bonus, void* o, int T,
@@ -492,14 +492,29 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_perkey_kernel(
       st.load(q, k, v, g, DELTA ? beta : nullptr, t0 + PF_C, Cn, nH, sh, tid);
     }
     __syncthreads();
-    // ---- Λ: inclusive scan of g down each key channel; e^{Λ_C}
-    if (tid < DK) {
+    // ---- Λ: inclusive scan of g down each key channel, in PF_THREADS / d_k
+    //      groups of consecutive tokens per channel (each thread scans its group,
+    //      then adds the totals of the groups before it); e^{Λ_C}.  Pk is free
+    //      until the S̄ products and holds the group totals.
+    {
+      constexpr int NGRP = PF_THREADS / DK, TPG = PF_C / NGRP;
+      static_assert(NGRP * DK == PF_THREADS && TPG * NGRP == PF_C, "scan groups");
+      const int c = tid % DK, grp = tid / DK;
       float acc = 0.f;
-      for (int j = 0; j < PF_C; ++j) {
-        acc += Lc[j * L::SP + tid];
-        Lc[j * L::SP + tid] = acc;
+#pragma unroll
+      for (int j = grp * TPG; j < (grp + 1) * TPG; ++j) {
+        acc += Lc[j * L::SP + c];
+        Lc[j * L::SP + c] = acc;
       }
-      Ec[tid] = expf(acc);
+      Pk[grp * DK + c] = acc;
+      __syncthreads();
+      float pre = 0.f;
+      for (int q = 0; q < grp; ++q) pre += Pk[q * DK + c];
+      if (grp > 0) {
+#pragma unroll
+        for (int j = grp * TPG; j < (grp + 1) * TPG; ++j) Lc[j * L::SP + c] += pre;
+      }
+      if (grp == NGRP - 1) Ec[c] = expf(pre + acc);
     }
     if constexpr (!DELTA) {
       // bonus coefficient of each token: Σ_c r_j[c] b[c] k_j[c] (one warp per token)
@@ -597,21 +612,44 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_perkey_kernel(
         }
     }
     __syncthreads();
-    // ---- the appended factors and the outputs: one thread per value row; each
-    //      sum runs in four partial sums to shorten its chain
-    if (tid < DV) {
+    // ---- the appended factors and the outputs
+    if constexpr (!DELTA) {
+      // RWKV6: u_j = v_j, so every output is independent.  Row r = tid % d_v,
+      // tokens j ≡ tid / d_v (mod PF_THREADS / d_v).  The pair coefficients
+      // of dead pairs (i >= j) are zero, so each sum runs over every i, in
+      // four partial sums.
+      constexpr int JG = PF_THREADS / DV;
+      static_assert(JG * DV == PF_THREADS && PF_C % JG == 0, "output groups");
+      const int r = tid % DV, jq = tid / DV;
+      float vr[PF_C];
+#pragma unroll
+      for (int i = 0; i < PF_C; ++i) vr[i] = Vc[i * DV + r];
+#pragma unroll
+      for (int t = 0; t < PF_C / JG; ++t) {
+        const int j = jq + JG * t;
+        const float vj = Vc[j * DV + r];
+        Us[r * L::PP + j] = vj;
+        if (o != nullptr && j < Cc) {
+          float y[4] = {Pq[r * L::PP + j], 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int i = 0; i < PF_C; ++i) y[i & 3] += Akq[j * L::PP + i] * vr[i];
+          const float yo = (y[0] + y[1]) + (y[2] + y[3]) + Cb[j] * vj;
+          const size_t oi = ((size_t)(t0 + j) * nH + sh) * DV + r;
+          if (out_bf16) static_cast<uint16_t*>(o)[oi] = f2bf16(scale * yo);
+          else static_cast<float*>(o)[oi] = scale * yo;
+        }
+      }
+    } else if (tid < DV) {
+      // KDA: one thread per value row (u_j needs u_i, i < j); each sum runs in
+      // four partial sums to shorten its chain
       const int r = tid;
       float u[PF_C];
 #pragma unroll
       for (int j = 0; j < PF_C; ++j) {
-        if (DELTA) {
-          float x[4] = {Pk[r * L::PP + j], 0.f, 0.f, 0.f};
+        float x[4] = {Pk[r * L::PP + j], 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int i = 0; i < j; ++i) x[i & 3] += Akk[j * L::PP + i] * u[i];
-          u[j] = Bt[j] * (Vc[j * DV + r] - ((x[0] + x[1]) + (x[2] + x[3])));   // 0 past Cc
-        } else {
-          u[j] = Vc[j * DV + r];
-        }
+        for (int i = 0; i < j; ++i) x[i & 3] += Akk[j * L::PP + i] * u[i];
+        u[j] = Bt[j] * (Vc[j * DV + r] - ((x[0] + x[1]) + (x[2] + x[3])));   // 0 past Cc
       }
 #pragma unroll
       for (int j = 0; j < PF_C; ++j) {
@@ -619,9 +657,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_perkey_kernel(
         if (o != nullptr && j < Cc) {
           float y[4] = {Pq[r * L::PP + j], 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int i = 0; i <= j; ++i) y[i & 3] += Akq[j * L::PP + i] * u[i];   // (RWKV6: zero at i = j)
-          float yo = (y[0] + y[1]) + (y[2] + y[3]);
-          if (!DELTA) yo += Cb[j] * u[j];
+          for (int i = 0; i <= j; ++i) y[i & 3] += Akq[j * L::PP + i] * u[i];
+          const float yo = (y[0] + y[1]) + (y[2] + y[3]);
           const size_t oi = ((size_t)(t0 + j) * nH + sh) * DV + r;
           if (out_bf16) static_cast<uint16_t*>(o)[oi] = f2bf16(scale * yo);
           else static_cast<float*>(o)[oi] = scale * yo;
