@@ -360,9 +360,10 @@ struct PkSmem {
   static constexpr int PK_OFF = V_OFF + PF_C * DV;
   static constexpr int PQ_OFF = PK_OFF + DV * PP;
   static constexpr int U_OFF = PQ_OFF + DV * PP;
-  static constexpr int AKK_OFF = U_OFF + DV * PP;            // [C][PP]: padded rows
-  static constexpr int AKQ_OFF = AKK_OFF + PF_C * PP;
-  static constexpr int B_OFF = AKQ_OFF + PF_C * PP;
+  static constexpr int PA = PF_C + 4;       // row stride of Akk, Akq (16-byte aligned rows)
+  static constexpr int AKK_OFF = U_OFF + DV * PP;            // [C][PA]
+  static constexpr int AKQ_OFF = AKK_OFF + PF_C * PA;
+  static constexpr int B_OFF = AKQ_OFF + PF_C * PA;
   static constexpr int CB_OFF = B_OFF + PF_C;
   static constexpr int E_OFF = CB_OFF + PF_C;
   static constexpr int FLOATS = E_OFF + DK;
@@ -478,6 +479,9 @@ __global__ void __launch_bounds__(PF_THREADS, DK == 64 ? 2 : 1) prefill_perkey_k
   }
 
   static_assert(DK == DV, "square state");
+  float bon[DK / 32];   // RWKV6 bonus of this head: channels lane + 32 cc
+#pragma unroll
+  for (int cc = 0; cc < DK / 32; ++cc) bon[cc] = DELTA ? 0.f : bonus[(size_t)h * DK + lane + 32 * cc];
   PkStage<DK> st;
   st.load(q, k, v, g, DELTA ? beta : nullptr, 0, T < PF_C ? T : PF_C, nH, sh, tid);
   for (int t0 = 0; t0 < T; t0 += PF_C) {
@@ -520,8 +524,11 @@ __global__ void __launch_bounds__(PF_THREADS, DK == 64 ? 2 : 1) prefill_perkey_k
       // bonus coefficient of each token: Σ_c r_j[c] b[c] k_j[c] (one warp per token)
       for (int j = warp; j < PF_C; j += PF_THREADS / 32) {
         float s = 0.f;
-        for (int c = lane; c < DK; c += 32)
-          s += Qc[j * L::SP + c] * bonus[(size_t)h * DK + c] * Kc[j * L::SP + c];
+#pragma unroll
+        for (int cc = 0; cc < DK / 32; ++cc) {
+          const int c = lane + 32 * cc;
+          s += Qc[j * L::SP + c] * bon[cc] * Kc[j * L::SP + c];
+        }
         s = warp_sum(s);
         if (lane == 0) Cb[j] = s;
       }
@@ -555,8 +562,8 @@ __global__ void __launch_bounds__(PF_THREADS, DK == 64 ? 2 : 1) prefill_perkey_k
       }
       auto put = [&](int j, int i, float kv, float qv, bool live) {
         const bool ok = live && j < Cc;
-        Akk[j * L::PP + i] = (DELTA && ok && i != j) ? kv : 0.f;
-        Akq[j * L::PP + i] = ok ? qv : 0.f;
+        Akk[j * L::PA + i] = (DELTA && ok && i != j) ? kv : 0.f;
+        Akq[j * L::PA + i] = ok ? qv : 0.f;
       };
       put(j0, i0, kk[0], qk[0], dl);
       put(j0, i1, 0.f, 0.f, false);
@@ -572,7 +579,7 @@ __global__ void __launch_bounds__(PF_THREADS, DK == 64 ? 2 : 1) prefill_perkey_k
         Xc[j * L::SP + c] = e * Kc[j * L::SP + c];
         Qc[j * L::SP + c] *= e;
       } else {
-        Qc[j * L::SP + c] *= (j > 0) ? expf(Lc[(j - 1) * L::SP + c]) : 1.f;
+        Qc[j * L::SP + c] *= (j > 0) ? __expf(Lc[(j - 1) * L::SP + c]) : 1.f;
       }
     }
     __syncthreads();
@@ -632,7 +639,13 @@ __global__ void __launch_bounds__(PF_THREADS, DK == 64 ? 2 : 1) prefill_perkey_k
         if (o != nullptr && j < Cc) {
           float y[4] = {Pq[r * L::PP + j], 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int i = 0; i < PF_C; ++i) y[i & 3] += Akq[j * L::PP + i] * vr[i];
+          for (int i = 0; i < PF_C; i += 4) {   // one broadcast 16-byte load per four pairs
+            const float4 c4 = ld4(Akq + j * L::PA + i);
+            y[0] += c4.x * vr[i];
+            y[1] += c4.y * vr[i + 1];
+            y[2] += c4.z * vr[i + 2];
+            y[3] += c4.w * vr[i + 3];
+          }
           const float yo = (y[0] + y[1]) + (y[2] + y[3]) + Cb[j] * vj;
           const size_t oi = ((size_t)(t0 + j) * nH + sh) * DV + r;
           if (out_bf16) static_cast<uint16_t*>(o)[oi] = f2bf16(scale * yo);
@@ -648,7 +661,7 @@ __global__ void __launch_bounds__(PF_THREADS, DK == 64 ? 2 : 1) prefill_perkey_k
       for (int j = 0; j < PF_C; ++j) {
         float x[4] = {Pk[r * L::PP + j], 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < j; ++i) x[i & 3] += Akk[j * L::PP + i] * u[i];
+        for (int i = 0; i < j; ++i) x[i & 3] += Akk[j * L::PA + i] * u[i];
         u[j] = Bt[j] * (Vc[j * DV + r] - ((x[0] + x[1]) + (x[2] + x[3])));   // 0 past Cc
       }
 #pragma unroll
@@ -657,7 +670,7 @@ __global__ void __launch_bounds__(PF_THREADS, DK == 64 ? 2 : 1) prefill_perkey_k
         if (o != nullptr && j < Cc) {
           float y[4] = {Pq[r * L::PP + j], 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int i = 0; i <= j; ++i) y[i & 3] += Akq[j * L::PP + i] * u[i];
+          for (int i = 0; i <= j; ++i) y[i & 3] += Akq[j * L::PA + i] * u[i];
           const float yo = (y[0] + y[1]) + (y[2] + y[3]);
           const size_t oi = ((size_t)(t0 + j) * nH + sh) * DV + r;
           if (out_bf16) static_cast<uint16_t*>(o)[oi] = f2bf16(scale * yo);
@@ -669,7 +682,7 @@ __global__ void __launch_bounds__(PF_THREADS, DK == 64 ? 2 : 1) prefill_perkey_k
     for (int idx = tid; idx < PF_C * DK; idx += PF_THREADS) {
       const int j = idx / DK, c = idx - j * DK;
       Xc[j * L::SP + c] =
-          Kc[j * L::SP + c] * expf(Lc[(PF_C - 1) * L::SP + c] - Lc[j * L::SP + c]);
+          Kc[j * L::SP + c] * __expf(Lc[(PF_C - 1) * L::SP + c] - Lc[j * L::SP + c]);
     }
     __syncthreads();
     // ---- S̄ <- S̄ Diag(e^{Λ_C}) + Σ_j a_j (k_j ⊙ e^{Λ_C-Λ_j})^T: rows rg + 32 m
