@@ -315,7 +315,10 @@ def run_reference(args):
         config = decode_config(w, 1 if args.eager else (args.M or w["M"]), args, 1, args.eager)
     else:   # prefill, checkpoint and read-state lines: the decode workload they belong to
         config = {"workload": args.workload + " of " + w["desc"]}
-    out = {"metric": METRIC, "value": res["value"], "unit": "tokens·heads/s", "n_gpus": 0,
+    # n_gpus: the N the arm was launched with (rank 0 alone times the oracle on the
+    # host cores; gpus_used says that no GPU takes part)
+    out = {"metric": METRIC, "value": res["value"], "unit": "tokens·heads/s",
+           "n_gpus": max(world, args.gpus), "gpus_used": 0,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic", "impl": "reference",

@@ -200,9 +200,15 @@ dl_status dl_step_host(dl_ctx *ctx, const int32_t *slots, int32_t n,
  * staging a group), and while a group's tokens run on the
  * context's stream an upload stream copies the next groups' inputs into the
  * next of four device staging sets (a set is reused once its group's outputs
- * are back) and a download stream copies earlier groups' outputs back.  The
- * staging sets and the two streams are owned by the context and made on the
- * first call.  Host memory must be pinned for the copies to run
+ * are back) and a download stream copies earlier groups' outputs back.  When
+ * every listed slot owns its base with an empty log and T is a multiple of M
+ * (M >= 2), each group is a whole decode window of M tokens, run as a window
+ * graph (dl_window_create) captured on its staging set: the same kernels and
+ * results, one graph launch per M tokens.  These windows are captured at the
+ * first such call for a slot list and kept until a call with another list
+ * (their staging takes at most 2 GiB; larger batches use the per-token path).
+ * The staging sets, windows and streams are owned by the context and made on
+ * first use.  Host memory must be pinned for the copies to run
  * asynchronously.  Returns once every output is in host memory; on an error
  * (for example DL_EBUSY for a frozen slot at the first token) the tokens
  * before it have been decoded and copied back. */

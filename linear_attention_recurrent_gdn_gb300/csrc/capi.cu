@@ -5,6 +5,7 @@
 // host slot table (slot_table.cpp) validates every call and yields the per-row
 // step plan (slot, base read, log length) that is passed to the kernels as a
 // launch parameter, so that no host-device synchronisation is needed per step.
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -78,6 +79,13 @@ struct dl_ctx {
   int pipe_group = 1;          // tokens per staging set
   cudaStream_t up = nullptr, down = nullptr;
   cudaEvent_t ev_in[PIPE_SETS] = {}, ev_done[PIPE_SETS] = {}, ev_out[PIPE_SETS] = {};
+  // dl_decode_host over whole decode windows: PIPE_SETS staging sets of M
+  // tokens for the batch `wslots`, each with a decode window (CUDA graph)
+  // captured on its buffers
+  void* wstage = nullptr;
+  size_t wset_bytes = 0;
+  std::vector<int32_t> wslots;
+  dl_window* wwin[PIPE_SETS] = {};
   std::vector<int32_t> plan;
   std::unique_ptr<dl::StepArgs> step_args;
   std::unique_ptr<dl::SlotListArgs> list_args;
@@ -136,7 +144,19 @@ cudaError_t dev_alloc(void** p, size_t bytes) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+void free_windows(dl_ctx* c) {
+  for (int b = 0; b < PIPE_SETS; ++b) {
+    if (c->wwin[b]) dl_window_destroy(c->wwin[b]);
+    c->wwin[b] = nullptr;
+  }
+  if (c->wstage) cudaFree(c->wstage);
+  c->wstage = nullptr;
+  c->wset_bytes = 0;
+  c->wslots.clear();
+}
+
 void free_all(dl_ctx* c) {
+  free_windows(c);
   void* ptrs[] = {c->Sbar, c->alog, c->klog, c->Llog, c->nlog, c->base_of,
                   c->coef, c->bonus, c->status, c->stage, c->pipe_stage};
   for (void* p : ptrs)
@@ -660,6 +680,116 @@ dl_status dl_step_host(dl_ctx* c, const int32_t* slots, int32_t n, const void* q
   return DL_OK;
 }
 
+// The upload and download streams of dl_decode_host and the events that order
+// them (made once per context).
+static cudaError_t copy_streams(dl_ctx* c) {
+  cudaError_t e = cudaSuccess;
+  if (!c->up) e = cudaStreamCreateWithFlags(&c->up, cudaStreamNonBlocking);
+  if (e == cudaSuccess && !c->down) e = cudaStreamCreateWithFlags(&c->down, cudaStreamNonBlocking);
+  for (int b = 0; b < PIPE_SETS && e == cudaSuccess; ++b) {
+    if (!c->ev_in[b]) e = cudaEventCreateWithFlags(&c->ev_in[b], cudaEventDisableTiming);
+    if (e == cudaSuccess && !c->ev_done[b]) e = cudaEventCreateWithFlags(&c->ev_done[b], cudaEventDisableTiming);
+    if (e == cudaSuccess && !c->ev_out[b]) e = cudaEventCreateWithFlags(&c->ev_out[b], cudaEventDisableTiming);
+  }
+  return e;
+}
+
+// Staging of window mode: at most this much device memory for the sets.
+constexpr size_t WINDOW_STAGE_CAP = (size_t)2 << 30;
+
+// dl_decode_host in whole decode windows (every slot owns its base and starts
+// with an empty log, T a multiple of M): each staging set holds M tokens and
+// runs as one decode window captured on its buffers (dl_window_create), so the
+// host enqueues one graph per M tokens instead of M steps, and the steps inside
+// a window chain as programmatic dependents.  The windows are captured once per
+// batch (slot list) and kept.  Returns DL_EUNSUPPORTED, having enqueued
+// nothing, when the staging would exceed WINDOW_STAGE_CAP.
+static dl_status decode_host_windows(dl_ctx* c, const int32_t* slots, int32_t n, int32_t T,
+                                     const unsigned char* hq, const unsigned char* hk,
+                                     const unsigned char* hv, const unsigned char* hg,
+                                     const unsigned char* hb, unsigned char* ho) {
+  const dl_config& f = c->cfg;
+  const int M = f.merge_interval;
+  const size_t H = f.num_heads;
+  const size_t bq = (size_t)n * H * f.d_k * 2, bv = (size_t)n * H * f.d_v * 2;
+  const size_t bg = (size_t)n * H * (f.op == DL_GDN ? 1 : f.d_k) * 4;
+  const size_t bb = (size_t)n * H * 4, bo = (size_t)n * H * f.d_v * (f.out_bf16 ? 2 : 4);
+  auto r256 = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  const size_t Mz = (size_t)M;
+  const size_t set = 2 * r256(Mz * bq) + r256(Mz * bv) + r256(Mz * bg) + r256(Mz * bb) + r256(Mz * bo);
+  if (set * PIPE_SETS > WINDOW_STAGE_CAP) return DL_EUNSUPPORTED;
+  auto region = [&](int b, unsigned char** dq, unsigned char** dk, unsigned char** dv,
+                    unsigned char** dg, unsigned char** db, unsigned char** dout) {
+    unsigned char* p = static_cast<unsigned char*>(c->wstage) + (size_t)b * c->wset_bytes;
+    *dq = p; p += r256(Mz * bq);
+    *dk = p; p += r256(Mz * bq);
+    *dv = p; p += r256(Mz * bv);
+    *dg = p; p += r256(Mz * bg);
+    *db = p; p += r256(Mz * bb);
+    *dout = p;
+  };
+  const bool same = c->wstage && c->wset_bytes == set && c->wslots.size() == (size_t)n &&
+                    std::equal(c->wslots.begin(), c->wslots.end(), slots);
+  if (!same) {
+    cudaStreamSynchronize(c->stream);   // earlier windows may still run
+    free_windows(c);
+    if (dev_alloc(&c->wstage, PIPE_SETS * set) != cudaSuccess) {
+      c->wstage = nullptr;
+      return set_err(c, DL_ENOMEM, "window staging allocation");
+    }
+    c->wset_bytes = set;
+    for (int b = 0; b < PIPE_SETS; ++b) {
+      unsigned char *dq, *dk, *dv, *dg, *db, *dout;
+      region(b, &dq, &dk, &dv, &dg, &db, &dout);
+      dl_status rc = dl_window_create(c, slots, n, dq, dk, dv, reinterpret_cast<const float*>(dg),
+                                      f.op != DL_RWKV6 ? reinterpret_cast<const float*>(db) : nullptr,
+                                      dout, &c->wwin[b]);
+      if (rc != DL_OK) {
+        free_windows(c);
+        return rc;
+      }
+    }
+    c->wslots.assign(slots, slots + n);
+  }
+  const cudaError_t es = copy_streams(c);
+  if (es != cudaSuccess) return cuda_err(c, es, "dl_decode_host set-up");
+  dl_status rc = DL_OK;
+  cudaError_t e = cudaSuccess;
+  const int W = T / M;
+  for (int w = 0; w < W && rc == DL_OK && e == cudaSuccess; ++w) {
+    const int b = w % PIPE_SETS;
+    unsigned char *dq, *dk, *dv, *dg, *db, *dout;
+    region(b, &dq, &dk, &dv, &dg, &db, &dout);
+    const size_t t0 = (size_t)w * Mz;
+    // set b is free once window w - PIPE_SETS's outputs are back
+    if (w >= PIPE_SETS) e = cudaStreamWaitEvent(c->up, c->ev_out[b], 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dq, hq + t0 * bq, Mz * bq, cudaMemcpyHostToDevice, c->up);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dk, hk + t0 * bq, Mz * bq, cudaMemcpyHostToDevice, c->up);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dv, hv + t0 * bv, Mz * bv, cudaMemcpyHostToDevice, c->up);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dg, hg + t0 * bg, Mz * bg, cudaMemcpyHostToDevice, c->up);
+    if (e == cudaSuccess && f.op != DL_RWKV6)
+      e = cudaMemcpyAsync(db, hb + t0 * bb, Mz * bb, cudaMemcpyHostToDevice, c->up);
+    if (e == cudaSuccess) e = cudaEventRecord(c->ev_in[b], c->up);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(c->stream, c->ev_in[b], 0);
+    if (e != cudaSuccess) break;
+    rc = dl_window_launch(c->wwin[b]);
+    if (rc != DL_OK) break;
+    e = cudaEventRecord(c->ev_done[b], c->stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(c->down, c->ev_done[b], 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(ho + t0 * bo, dout, Mz * bo, cudaMemcpyDeviceToHost, c->down);
+    if (e == cudaSuccess) e = cudaEventRecord(c->ev_out[b], c->down);
+  }
+  const cudaError_t e1 = cudaStreamSynchronize(c->up);
+  const cudaError_t e2 = cudaStreamSynchronize(c->stream);
+  const cudaError_t e3 = cudaStreamSynchronize(c->down);
+  if (rc != DL_OK) return rc;
+  if (e != cudaSuccess) return cuda_err(c, e, "dl_decode_host copies");
+  if (e1 != cudaSuccess) return cuda_err(c, e1, "dl_decode_host upload");
+  if (e2 != cudaSuccess) return cuda_err(c, e2, "dl_decode_host compute");
+  if (e3 != cudaSuccess) return cuda_err(c, e3, "dl_decode_host download");
+  return DL_OK;
+}
+
 dl_status dl_decode_host(dl_ctx* c, const int32_t* slots, int32_t n, int32_t T, const void* q,
                          const void* k, const void* v, const float* g, const float* beta,
                          void* o) {
@@ -672,6 +802,15 @@ dl_status dl_decode_host(dl_ctx* c, const int32_t* slots, int32_t n, int32_t T, 
   rc = dl_table_check(c->table, slots, n);
   if (rc != DL_OK) return set_err(c, rc, "dl_decode_host: invalid slot list");
   const dl_config& f = c->cfg;
+  // whole windows when every slot starts a window on its own base
+  if (f.merge_interval >= 2 && T % f.merge_interval == 0 && n <= dl::MAX_ROWS &&
+      dl_table_step_eager(c->table, slots, n) == DL_OK) {
+    rc = decode_host_windows(c, slots, n, T, static_cast<const unsigned char*>(q),
+                             static_cast<const unsigned char*>(k), static_cast<const unsigned char*>(v),
+                             reinterpret_cast<const unsigned char*>(g),
+                             reinterpret_cast<const unsigned char*>(beta), static_cast<unsigned char*>(o));
+    if (rc != DL_EUNSUPPORTED) return rc;
+  }
   const size_t H = f.num_heads;
   const size_t bq = (size_t)n * H * f.d_k * 2, bv = (size_t)n * H * f.d_v * 2;
   const size_t bg = (size_t)n * H * (f.op == DL_GDN ? 1 : f.d_k) * 4;
@@ -702,13 +841,7 @@ dl_status dl_decode_host(dl_ctx* c, const int32_t* slots, int32_t n, int32_t T, 
     }
     c->pipe_set_bytes = set;
     c->pipe_group = tg;
-    cudaError_t e = cudaStreamCreateWithFlags(&c->up, cudaStreamNonBlocking);
-    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->down, cudaStreamNonBlocking);
-    for (int b = 0; b < PIPE_SETS && e == cudaSuccess; ++b) {
-      e = cudaEventCreateWithFlags(&c->ev_in[b], cudaEventDisableTiming);
-      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->ev_done[b], cudaEventDisableTiming);
-      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->ev_out[b], cudaEventDisableTiming);
-    }
+    const cudaError_t e = copy_streams(c);
     if (e != cudaSuccess) return cuda_err(c, e, "dl_decode_host set-up");
   }
   const unsigned char* hq = static_cast<const unsigned char*>(q);

@@ -397,6 +397,46 @@ def test_decode_host_wraps_the_staging_ring(op):
     assert list(ctx.get_meta()[0]) == [T % M] * B
 
 
+@pytest.mark.parametrize("op", OPS)
+def test_decode_host_whole_windows_bitwise(op):
+    """Slots that start on their own bases with empty logs, and T a multiple of
+    M, go through captured decode windows, one per staging set: nine windows
+    wrap the four sets twice. A second batch captures new windows. A call of
+    T = M + 3 (not whole windows), and the next call (its slots then start
+    mid-window), take the per-token path. Every output, the states and the log
+    lengths are the bits of dl_step on device buffers."""
+    from linear_attention_recurrent_gdn_gb300 import deltalog as dl
+    B, H, M = 6, 4, 4
+    d = 64 if op == gen.RWKV6 else 128
+    calls = [(list(range(B)), 0, 9 * M),        # whole windows, sets wrap
+             ([0, 2, 4], 9 * M, 11 * M),        # another batch: new windows
+             ([1, 3, 5], 9 * M, 10 * M + 3),    # not whole windows: per token
+             ([1, 3, 5], 10 * M + 3, 12 * M + 3)]   # mid-window start: per token
+    Ttot = max(c[2] for c in calls)
+    x, S0, bonus = make_case(op, B, H, d, Ttot, seed=970 + op)
+    ref = dl.DeltaLog(op, B, H, d, d, M)
+    hst = dl.DeltaLog(op, B, H, d, d, M)
+    for c in (ref, hst):
+        c.set_state(list(range(B)), S0.cuda())
+        if bonus is not None:
+            c.set_bonus(bonus.cuda())
+    dev = {k_: (v_.cuda() if v_ is not None else None) for k_, v_ in x.items()}
+    for slots, t0, t1 in calls:
+        idx = torch.tensor(slots)
+        outs = []
+        for t in range(t0, t1):
+            sel = lambda key: (dev[key][t].index_select(0, idx.cuda()).contiguous()
+                               if dev[key] is not None else None)
+            outs.append(ref.step(slots, sel("q"), sel("k"), sel("v"), sel("g"), sel("beta")))
+        o_ref = torch.stack(outs).cpu()
+        pin = {k_: (v_[t0:t1].index_select(1, idx).contiguous().pin_memory() if v_ is not None else None)
+               for k_, v_ in x.items()}
+        o = hst.decode_host(slots, pin["q"], pin["k"], pin["v"], pin["g"], pin["beta"])
+        assert torch.equal(o, o_ref), (slots, t0, t1)
+    assert torch.equal(hst.read_state(list(range(B))), ref.read_state(list(range(B))))
+    assert [list(m) for m in hst.get_meta()] == [list(m) for m in ref.get_meta()]
+
+
 def test_decode_host_frozen_slot_is_refused():
     from linear_attention_recurrent_gdn_gb300 import deltalog as dl
     B, H, d, M, T = 3, 2, 64, 4, 5
