@@ -666,10 +666,11 @@ def run_ours(args):
     c.close()
     h2d = sum(v[0].numel() * v.element_size() for v in pin.values() if v is not None) * T
     d2h = hout[0].numel() * hout.element_size() * T
+    group, path = decode_host_group(op, B, H, d, M, T)
     result["e2e"] = {"value": units_per_step * world / (e2e_ms / 1e3), "unit": "tokens·heads/s",
                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                     "ms_per_step": e2e_ms, "api": "dl_decode_host",
-                     "copy_ceiling": copy_ceiling(pin, hout, dev, T, decode_host_group(op, B, H, d),
+                     "ms_per_step": e2e_ms, "api": "dl_decode_host", "path": path,
+                     "copy_ceiling": copy_ceiling(pin, hout, dev, T, group,
                                                   units_per_step * world, args)}
 
     # ---- CPU baseline (rank 0, N = 1 only)
@@ -688,14 +689,19 @@ def run_ours(args):
     return 0
 
 
-def decode_host_group(op, S, H, d):
-    """Tokens per copy group of dl_decode_host for a context of S slots: small
-    per-token tensors are grouped until a key tensor's copy reaches 2 MiB, at
-    most 8 tokens and 64 MiB of staging a group."""
+def decode_host_group(op, S, H, d, M, T):
+    """Tokens per copy group of dl_decode_host for S slots that start on their own
+    bases with empty logs: a whole window of M tokens when T is a multiple of
+    M >= 2 and four sets of such windows take at most 2 GiB (window graphs);
+    otherwise small per-token tensors are grouped until a key tensor's copy
+    reaches 2 MiB, at most 8 tokens and 64 MiB of staging a group.  Returns the
+    group and the path's name."""
     key = S * H * d * 2
     per_tok = 2 * key + S * H * d * 2 + S * H * (d * 4 if op else 4) + S * H * 4 + S * H * d * 4
+    if M >= 2 and T % M == 0 and 4 * M * per_tok <= (2 << 30):
+        return M, "window graphs, one per M tokens"
     g = min(-(-(2 << 20) // key), (64 << 20) // per_tok)
-    return max(1, min(8, g))
+    return max(1, min(8, g)), "token by token"
 
 
 def copy_ceiling(pin, hout, dev, T, group, units, args):
