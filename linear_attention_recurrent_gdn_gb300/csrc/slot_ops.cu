@@ -111,7 +111,15 @@ __global__ void __launch_bounds__(256) set_state_kernel(const __grid_constant__ 
   const StepItem it = a.items[row];
   const float4* src = reinterpret_cast<const float4*>(a.S_in + (size_t)sh * DV * DK);
   float4* dst = reinterpret_cast<float4*>(a.Sbar + ((size_t)it.slot * a.H + h) * DV * DK);
-  for (int i = threadIdx.x; i < DV * DK / 4; i += 256) dst[i] = src[i];
+  constexpr int NV = DV * DK / 4;   // a multiple of 4 x 256 at d = 64 and 128
+  static_assert(NV % (4 * 256) == 0, "whole batches of four loads per thread");
+  for (int i = threadIdx.x; i < NV; i += 4 * 256) {   // four loads in flight per thread
+    const float4 r0 = src[i], r1 = src[i + 256], r2 = src[i + 512], r3 = src[i + 768];
+    dst[i] = r0;
+    dst[i + 256] = r1;
+    dst[i + 512] = r2;
+    dst[i + 768] = r3;
+  }
   if (h == 0 && threadIdx.x == 0) {
     a.nlog[it.slot] = 0;
     a.base_of[it.slot] = it.slot;
@@ -158,10 +166,21 @@ __global__ void __launch_bounds__(256) checkpoint_kernel(const __grid_constant__
   const size_t Mcap = a.Mcap;
   unsigned char* rec = a.buf + (size_t)row * a.total;
   const size_t lh = (size_t)it.slot * a.H + h;
+  // four 16-byte loads in flight per thread before their stores (one at a
+  // time leaves the copy bound by latency); the tail one at a time
   auto copy16 = [&](unsigned char* dst, const unsigned char* src, size_t bytes) {
     const uint4* s4 = reinterpret_cast<const uint4*>(src);
     uint4* d4 = reinterpret_cast<uint4*>(dst);
-    for (size_t i = threadIdx.x; i < bytes / 16; i += 256) d4[i] = s4[i];
+    const size_t nv = bytes / 16;
+    size_t i = threadIdx.x;
+    for (; i + 3 * 256 < nv; i += 4 * 256) {
+      const uint4 r0 = s4[i], r1 = s4[i + 256], r2 = s4[i + 512], r3 = s4[i + 768];
+      d4[i] = r0;
+      d4[i + 256] = r1;
+      d4[i + 512] = r2;
+      d4[i + 768] = r3;
+    }
+    for (; i < nv; i += 256) d4[i] = s4[i];
   };
   const size_t sS = (size_t)DV * DK * 4, sA = Mcap * DV * ESA, sK = Mcap * DK * 2;
   unsigned char* gS = reinterpret_cast<unsigned char*>(a.Sbar) +
