@@ -282,7 +282,9 @@ dl_status dl_checkpoint_load(dl_ctx *ctx, const int32_t *slots, int32_t n, const
  * [M, n, H, d_v] bf16, g [M, n, H] or [M, n, H, d_k] fp32, beta [M, n, H] fp32
  * (NULL for RWKV6), o [M, n, H, d_v]: token j of a launch reads slice j of each
  * input and writes slice j of o; the graph keeps these device pointers, and the
- * caller refills the buffers between launches (in stream order).  n <= 1024.
+ * caller refills the buffers between launches (in stream order).  The inputs
+ * must not overlap o: a step may read its inputs while the step before it is
+ * still writing its outputs.  n <= 1024.
  * dl_window_launch validates the slots, enqueues the graph on the context's
  * stream and advances the slot table by M tokens. */
 typedef struct dl_window dl_window;

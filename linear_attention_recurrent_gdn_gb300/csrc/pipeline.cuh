@@ -146,9 +146,12 @@ __device__ __forceinline__ void copy_seg(uint32_t dst, const void* src, uint32_t
   for (uint32_t off = (uint32_t)lane * 16u; off < bytes; off += 32u * 16u) cp_async16(dst + off, s + off);
 }
 
+// Fused form: `part` 1 copies the unit's inputs (the step's own tensors, the
+// bonus), 2 its log rows (which the previous step may still be writing), 3
+// both.  The other forms copy everything.
 template <int OP, int DK, int DV, int MODE>
 __device__ __forceinline__ void issue_aux(const StepArgs& a, const Layout& Lay, const UnitPos& p,
-                                          unsigned char* ax, int lane) {
+                                          unsigned char* ax, int lane, int part = 3) {
   constexpr bool DELTA = OP != RWKV6;
   const StepItem it = step_item(a, p.row);
   const size_t sh = p.sh;
@@ -177,27 +180,31 @@ __device__ __forceinline__ void issue_aux(const StepArgs& a, const Layout& Lay, 
     const int n = it.n;
     const bool merge = (n + 1 == a.M);
     const size_t lh = (size_t)it.slot * a.H + p.h;
-    copy_seg(base + Lay.f_kq, a.k + sh * DK, DK * 2, lane);
-    copy_seg(base + Lay.f_kq + DK * 2, a.q + sh * DK, DK * 2, lane);
-    if (DELTA) copy_seg(base + Lay.f_v, a.v + sh * DV, DV * 2, lane);
-    if (n > 0) {
+    if (part & 1) {   // the step's inputs
+      copy_seg(base + Lay.f_kq, a.k + sh * DK, DK * 2, lane);
+      copy_seg(base + Lay.f_kq + DK * 2, a.q + sh * DK, DK * 2, lane);
+      if (DELTA) copy_seg(base + Lay.f_v, a.v + sh * DV, DV * 2, lane);
+      if (OP == RWKV6) copy_seg(base + Lay.f_U + n * DV * 2, a.v + sh * DV, DV * 2, lane);
+      if (OP == GDN && merge) copy_seg(base + Lay.f_kl + n * DK * 2, a.k + sh * DK, DK * 2, lane);
+      if constexpr (OP == GDN) {
+        if (lane == 0) cp_async4(base + Lay.f_g, a.g + sh);
+      } else {
+        copy_seg(base + Lay.f_g, a.g + sh * DK, DK * 4, lane);
+      }
+      if (DELTA && lane == 0) cp_async4(base + Lay.f_beta, a.beta + sh);
+      if (OP == RWKV6) copy_seg(base + Lay.f_bonus, a.bonus + (size_t)p.h * DK, DK * 4, lane);
+    }
+    if ((part & 2) && n > 0) {   // the slot's log rows
       copy_seg(base + Lay.f_U, static_cast<const unsigned char*>(a.alog) + lh * Lay.Mcap * DV * ESA,
                (uint32_t)n * DV * ESA, lane);
       copy_seg(base + Lay.f_kl, a.klog + lh * Lay.Mcap * DK, (uint32_t)n * DK * 2, lane);
-    }
-    if (OP == RWKV6) copy_seg(base + Lay.f_U + n * DV * 2, a.v + sh * DV, DV * 2, lane);
-    if (OP == GDN && merge) copy_seg(base + Lay.f_kl + n * DK * 2, a.k + sh * DK, DK * 2, lane);
-    if constexpr (OP == GDN) {
-      // scalar log-decays (rows are not 16-byte aligned): 4-byte copies
-      if (lane < n) cp_async4(base + Lay.f_L + lane * 4, a.Llog + lh * Lay.Mcap + lane);
-      if (lane == 0) cp_async4(base + Lay.f_g, a.g + sh);
-    } else {
-      if (n > 0)
+      if constexpr (OP == GDN) {
+        // scalar log-decays (rows are not 16-byte aligned): 4-byte copies
+        if (lane < n) cp_async4(base + Lay.f_L + lane * 4, a.Llog + lh * Lay.Mcap + lane);
+      } else {
         copy_seg(base + Lay.f_L, a.Llog + lh * Lay.Mcap * DK, (uint32_t)n * DK * 4, lane);
-      copy_seg(base + Lay.f_g, a.g + sh * DK, DK * 4, lane);
+      }
     }
-    if (DELTA && lane == 0) cp_async4(base + Lay.f_beta, a.beta + sh);
-    if (OP == RWKV6) copy_seg(base + Lay.f_bonus, a.bonus + (size_t)p.h * DK, DK * 4, lane);
   } else {
     copy_seg(base + Lay.e_kq, a.k + sh * DK, DK * 2, lane);
     copy_seg(base + Lay.e_kq + DK * 2, a.q + sh * DK, DK * 2, lane);
@@ -760,10 +767,12 @@ __global__ void __maxnreg__(128) pipe_kernel(const __grid_constant__ StepArgs a)
     const uint64_t pol = a.l2_stream ? policy_evict_first() : policy_evict_normal();
     // APPEND and FUSED launch as programmatic dependents (of ReplayPrep, of the
     // previous step).  Before griddepcontrol.wait the producer only claims aux
-    // slots and streams tiles: APPEND copies the inputs that ReplayPrep does
-    // not write; FUSED copies no inputs at all, and streams only tiles of rows
-    // whose log is non-empty (a.pdl_prefetch), whose dense base the previous
-    // step did not write (only merge rows write it, and they restart at n = 0).
+    // slots, copies inputs and streams tiles: APPEND copies the inputs that
+    // ReplayPrep does not write; FUSED copies the step's own tensors (not the
+    // log rows, which the previous step appends to), and streams only tiles of
+    // rows whose log is non-empty (a.pdl_prefetch), whose dense base the
+    // previous step did not write (only merge rows write it, and they restart
+    // at n = 0).
     bool primary_done = (MODE == EAGER);
     int pending_from = 0;   // units [pending_from, ka) still need their deferred copies
     int ti = 0, ka = 0;
@@ -774,8 +783,8 @@ __global__ void __maxnreg__(128) pipe_kernel(const __grid_constant__ StepArgs a)
         unsigned char* ax = auxm + (size_t)(u % NA) * aux_bytes;
         if constexpr (MODE == APPEND) {
           issue_coef_and_arrive<OP, DK, DV>(a, Lay, p, ax, bars.afull(u % NA), lane);
-        } else {
-          issue_aux<OP, DK, DV, MODE>(a, Lay, p, ax, lane);
+        } else {   // FUSED: the inputs went out when the slot was claimed
+          issue_aux<OP, DK, DV, MODE>(a, Lay, p, ax, lane, 2);
           cp_async_arrive_noinc(bars.afull(u % NA));
         }
       }
@@ -829,6 +838,10 @@ __global__ void __maxnreg__(128) pipe_kernel(const __grid_constant__ StepArgs a)
             issue_aux<OP, DK, DV, MODE>(a, Lay, p, ax, lane);
             cp_async_arrive_noinc(bars.afull(x));
             pending_from = ka + 1;
+          } else {
+            // before the previous step has completed: only the step's own
+            // inputs (the log rows follow after the wait, then the arrival)
+            issue_aux<OP, DK, DV, MODE>(a, Lay, p, ax, lane, 1);
           }
         } else {
           issue_aux<OP, DK, DV, MODE>(a, Lay, p, ax, lane);
