@@ -397,8 +397,9 @@ def test_decode_host_wraps_the_staging_ring(op):
     assert list(ctx.get_meta()[0]) == [T % M] * B
 
 
+@pytest.mark.parametrize("out_bf16", [True, False])
 @pytest.mark.parametrize("op", OPS)
-def test_decode_host_whole_windows_bitwise(op):
+def test_decode_host_whole_windows_bitwise(op, out_bf16):
     """Slots that start on their own bases with empty logs, and T a multiple of
     M, go through captured decode windows, one per staging set: nine windows
     wrap the four sets twice. A second batch captures new windows. A call of
@@ -414,8 +415,8 @@ def test_decode_host_whole_windows_bitwise(op):
              ([1, 3, 5], 10 * M + 3, 12 * M + 3)]   # mid-window start: per token
     Ttot = max(c[2] for c in calls)
     x, S0, bonus = make_case(op, B, H, d, Ttot, seed=970 + op)
-    ref = dl.DeltaLog(op, B, H, d, d, M)
-    hst = dl.DeltaLog(op, B, H, d, d, M)
+    ref = dl.DeltaLog(op, B, H, d, d, M, out_bf16=out_bf16)
+    hst = dl.DeltaLog(op, B, H, d, d, M, out_bf16=out_bf16)
     for c in (ref, hst):
         c.set_state(list(range(B)), S0.cuda())
         if bonus is not None:
