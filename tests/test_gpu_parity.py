@@ -134,6 +134,38 @@ def test_staggered_logs_in_one_launch(op, d, M):
     assert list(n) == [(Ttot - start[s]) % M for s in range(B)]
 
 
+@pytest.mark.parametrize("op", OPS)
+@pytest.mark.parametrize("d", [64, 128])
+def test_extreme_decays_and_gates(op, d):
+    """Degenerate and extreme gates inside merge windows: no decay (g = 0) next
+    to decays of e^-30 a token (a window's cumulative log-decay reaches -450,
+    far below fp32's range for e^Λ), β = 0 (the delta rule writes nothing) and
+    β = 1, and zero value vectors. Outputs (fp32) and states match the oracle,
+    with nothing infinite or NaN."""
+    B, H, M = 3, 4, 16
+    T = 2 * M + 5
+    x, S0, bonus = make_case(op, B, H, d, T, seed=1200 + 5 * op + d)
+    g = x["g"].clone()
+    gen_ = torch.Generator().manual_seed(77 + op)
+    pick = torch.randint(0, 3, g.shape, generator=gen_)
+    g = torch.where(pick == 0, torch.zeros_like(g), torch.where(pick == 1, torch.full_like(g, -30.0), g))
+    x["g"] = g.contiguous()
+    if x["beta"] is not None:
+        pb = torch.randint(0, 3, x["beta"].shape, generator=gen_)
+        beta = torch.where(pb == 0, torch.zeros_like(x["beta"]),
+                           torch.where(pb == 1, torch.ones_like(x["beta"]), x["beta"]))
+        x["beta"] = beta.contiguous()
+    v = x["v"].clone()
+    v[3] = 0
+    v[M - 1, 1] = 0
+    x["v"] = v.contiguous()
+    o_ref, S_ref, _ = oracle_run(op, x, S0, bonus)
+    o, states, ctx = gpu_run(op, x, S0, bonus, M, out_bf16=False, snap=(T - 1,))
+    assert torch.isfinite(o).all()
+    assert max_step_rel(_flat_o(o), o_ref) <= OUT_TOL_F32
+    assert rel_err(_flat_S(states[T - 1]), S_ref) <= STATE_TOL
+
+
 # ------------------------------------------------------------------- eager ----
 @pytest.mark.parametrize("op", OPS)
 @pytest.mark.parametrize("d", [64, 128])
