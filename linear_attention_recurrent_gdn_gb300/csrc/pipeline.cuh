@@ -315,10 +315,13 @@ __device__ __forceinline__ void prep_unit(const StepArgs& a, const Layout& Lay, 
       float kq = 0.f;
 #pragma unroll
       for (int c = 0; c < VEC; ++c) {
-        const float e = expf(Lt[c]);
+        // the fast exponential for this step's k̂, q̂ (the prep warp is on the
+        // consumers' path: measured on GB300, 77.6 -> 78.3 M tokens·heads/s);
+        // the merge's decay, which scales the base from here on, stays exact
+        const float e = __expf(Lt[c]);
         cf[vecA + c0 + c] = e * kv[c];
         cf[vecB + c0 + c] = e * qv[c];
-        if (merge) cf[Lay.P0 + c0 + c] = e;
+        if (merge) cf[Lay.P0 + c0 + c] = expf(Lt[c]);
         kq += kv[c] * qv[c];
       }
       kq = warp_sum(kq);
