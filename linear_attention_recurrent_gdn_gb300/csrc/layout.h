@@ -93,6 +93,8 @@ DL_HD inline Layout make_layout(int op, int M, int dk, int dv, int arows = 0) {
 // each consumer warp computes its units' coefficients itself and owns the aux
 // slots x with x % ncw == w, so na is a multiple of ncw.  Returns ns = 0 when
 // nothing fits.
+constexpr int BAR_SLOTS = 128;   // 8-byte mbarriers in the pipelined kernels' barrier area
+
 struct PipePlan {
   int cps, ncw, ns, na, npw;
   int smem;   // dynamic shared memory per CTA (bytes): the CTA's share of the SM
@@ -127,6 +129,11 @@ inline PipePlan fit_pipeline(int cps, int ncw, int R, int dk, int aux_bytes, int
   const long left = (long)budget - (long)ns * tile;
   int na = left > 0 ? (int)(left / aux_bytes) : 0;
   if (na > max_na) na = max_na;
+  // the mbarrier area holds BAR_SLOTS barriers: full and empty per stage,
+  // three per aux slot (four with prep warps: their early "vectors ready"),
+  // and one spare
+  const int per_slot = npw > 0 ? 4 : 3;
+  if (2 * ns + per_slot * na + 1 > BAR_SLOTS) na = (BAR_SLOTS - 1 - 2 * ns) / per_slot;
   na = na / mult * mult;
   const long need = (long)ns * tile + (long)na * aux_bytes;
   if (na < na_min || ns > 24 || na > 24 || need > budget) return none;

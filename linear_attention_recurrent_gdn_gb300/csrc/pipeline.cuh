@@ -52,6 +52,8 @@ enum Mode : int { APPEND = 0, EAGER = 1, FUSED = 2 };
 
 constexpr int MAX_NS = 24, MAX_NA = 24;   // (barrier area: 8 bytes each)
 
+static_assert(BAR_BYTES == 8 * BAR_SLOTS, "barrier area and planner agree");
+
 struct Bars {
   uint32_t b0;
   int ns, na;
@@ -60,7 +62,10 @@ struct Bars {
   __device__ uint32_t afull(int x) const { return b0 + 8u * (2 * ns + x); }
   __device__ uint32_t aempty(int x) const { return b0 + 8u * (2 * ns + na + x); }
   __device__ uint32_t cready(int x) const { return b0 + 8u * (2 * ns + 2 * na + x); }
-  // The last barrier of the area (ns, na <= 24 use at most 120 of its 128):
+  // fused form with prep warps: the unit's key-side vectors are written (the
+  // consumers' pass over the tile may start; cready follows with the rest)
+  __device__ uint32_t vready(int x) const { return b0 + 8u * (2 * ns + 3 * na + x); }
+  // The last barrier of the area (the planner keeps the others below it):
   // initialised and never arrived on (the test-only stall waits on it).
   __device__ uint32_t never() const { return b0 + (uint32_t)BAR_BYTES - 8u; }
 };
@@ -234,9 +239,12 @@ __device__ __forceinline__ void issue_coef_and_arrive(const StepArgs& a, const L
 // formulas.  On an append step the owner unit (value-tile group 0) of the
 // slot-head also appends k_t, Λ_t (and v_t for RWKV6) to the slot's log in HBM,
 // and the (head 0, group 0) unit advances the device slot table.
+// `vbar` (prep warps only, else 0): arrived on once the consumers' pass over
+// the tile has what it reads (GDN: at once, it reads k_t, q_t from the aux
+// slot; KDA and RWKV6: once k̂, q̂ or r̂ are written).
 template <int OP, int DK, int DV, int NE>
 __device__ __forceinline__ void prep_unit(const StepArgs& a, const Layout& Lay, const UnitPos& p,
-                                          unsigned char* ax, int lane) {
+                                          unsigned char* ax, int lane, uint32_t vbar = 0) {
   constexpr int VEC = DK / 32;
   constexpr int SHIFT = NE == 32 ? 0 : NE == 16 ? 1 : 2;   // entry of lane l: l >> SHIFT
   const int lane_entry = lane >> SHIFT;
@@ -259,6 +267,7 @@ __device__ __forceinline__ void prep_unit(const StepArgs& a, const Layout& Lay, 
   ldvec_bf16<VEC>(qv, kq16 + DK + c0);
   float p1[NE], p2[NE];
   if constexpr (OP == GDN) {
+    if (vbar && lane == 0) mbar_arrive(vbar);
     const float beta_t = reinterpret_cast<const float*>(ax + Lay.f_beta)[0];
     const float Lt = (n > 0 ? Ls[n - 1] : 0.f) + gs[0];
     float kq = 0.f;
@@ -341,6 +350,10 @@ __device__ __forceinline__ void prep_unit(const StepArgs& a, const Layout& Lay, 
       }
       cb = warp_sum(cb);
       if (lane == 0) cf[3] = cb;
+    }
+    if (vbar) {   // k̂, q̂ (KDA) or r̂ (RWKV6) are in place
+      __syncwarp();
+      if (lane == 0) mbar_arrive(vbar);
     }
 #pragma unroll
     for (int j = 0; j < NE; ++j) {
@@ -452,11 +465,16 @@ __device__ __forceinline__ float sum4(const float (&s)[4]) { return (s[0] + s[1]
 
 // Returns true if it already released the tile stage (append steps release it
 // right after the pass over the tile, so the refill overlaps the epilogue).
+// With `coef_bar` set (fused form with prep warps) the pass over the tile
+// runs as soon as its vectors are in place, and the coefficients are awaited
+// on coef_bar (phase parity coef_par) before the epilogue; if that wait gives
+// up, *failed is set and nothing more is written.
 template <int OP, int DK, int DV>
 __device__ __forceinline__ bool consume_append(const StepArgs& a, const Layout& Lay,
                                                const UnitPos& p, int vt, const float* T,
                                                const AuxView& av, int lane, uint32_t empty_bar,
-                                               bool may_release) {
+                                               bool may_release, uint32_t coef_bar = 0,
+                                               uint32_t coef_par = 0, bool* failed = nullptr) {
   constexpr int VEC = DK / 32;
   constexpr bool DELTA = OP != RWKV6;
   const StepItem it = step_item(a, p.row);
@@ -508,6 +526,12 @@ __device__ __forceinline__ bool consume_append(const StepArgs& a, const Layout& 
       if (lane == 0) mbar_arrive(empty_bar);
     }
     A = sum4(s0);
+  }
+
+  if (coef_bar &&
+      !__all_sync(0xffffffffu, mbar_wait(coef_bar, coef_par, a.status, DEV_TIMEOUT_AUX, a.wait_ns))) {
+    *failed = true;
+    return !merge && may_release;
   }
 
   // row epilogue on lane = row
@@ -729,6 +753,13 @@ __device__ __forceinline__ void consume_eager(const StepArgs& a, const Layout& L
 template <int OP, int DK, int DV, int MODE, int NE = 0>
 __global__ void __maxnreg__(128) pipe_kernel(const __grid_constant__ StepArgs a) {
   static_assert(MODE != FUSED || NE == 8 || NE == 16 || NE == 32, "fused form needs NE");
+  // Per-key ops' prep warps signal a unit's vectors before its coefficients,
+  // and consumers run their pass over the tile in between, for logs of up to
+  // 32 entries (measured on GB300, KDA M = 32: 48.0 against 45.5 M
+  // tokens·heads/s).  With 16 at most the prep is short and waiting for all of
+  // it first is faster (KDA M = 16: 77.1 against 75.6); GDN's prep is short at
+  // any M (M = 32: 75.1 against 75.3).
+  constexpr bool SPLIT_PREP = MODE == FUSED && NE == 32 && OP != GDN;
   extern __shared__ __align__(1024) unsigned char smem[];
   constexpr uint32_t TILE_BYTES = BV * DK * 4;
   const Layout Lay = make_layout(OP, a.M, DK, DV, a.arows);
@@ -752,6 +783,7 @@ __global__ void __maxnreg__(128) pipe_kernel(const __grid_constant__ StepArgs a)
       mbar_init(bars.afull(x), 32);   // one arrival per producer lane
       mbar_init(bars.aempty(x), IPU);
       mbar_init(bars.cready(x), 1);   // fused form: the prep warp's arrival
+      if (SPLIT_PREP && a.npw > 0) mbar_init(bars.vready(x), 1);
     }
     mbar_init(bars.never(), 1);
     fence_mbar_init();
@@ -924,7 +956,7 @@ __global__ void __maxnreg__(128) pipe_kernel(const __grid_constant__ StepArgs a)
         break;
       const UnitPos p = walk.p;
       unsigned char* ax = auxm + (size_t)x * aux_bytes;
-      prep_unit<OP, DK, DV, NE>(a, Lay, p, ax, lane);
+      prep_unit<OP, DK, DV, NE>(a, Lay, p, ax, lane, SPLIT_PREP ? bars.vready(x) : 0u);
       __syncwarp();
       if (lane == 0) mbar_arrive(bars.cready(x));
     }
@@ -988,8 +1020,12 @@ __global__ void __maxnreg__(128) pipe_kernel(const __grid_constant__ StepArgs a)
       // has landed the aux barrier is in this unit's phase and the parity test
       // below is unambiguous.
       ok = mbar_wait(bars.full(s), spar, a.status, DEV_TIMEOUT_TILE, a.wait_ns);
-      ok = ok && mbar_wait(MODE == FUSED ? bars.cready(x) : bars.afull(x), xpar, a.status,
-                           DEV_TIMEOUT_AUX, a.wait_ns);
+      // fused form: the whole prep (cready), or, with SPLIT_PREP, only the
+      // unit's vectors (vready): consume_append then awaits the coefficients
+      // after its pass over the tile
+      ok = ok && mbar_wait(MODE == FUSED ? (SPLIT_PREP ? bars.vready(x) : bars.cready(x))
+                                         : bars.afull(x),
+                           xpar, a.status, DEV_TIMEOUT_AUX, a.wait_ns);
     }
     // Test only: wait on a barrier that nothing arrives on, with half the
     // limit, so that this wait runs out before the waits that depend on this
@@ -1007,16 +1043,20 @@ __global__ void __maxnreg__(128) pipe_kernel(const __grid_constant__ StepArgs a)
         released = paired = true;
       }
     }
-    for (int t = 0; t < TPS && !paired; ++t) {
+    bool failed = false;
+    for (int t = 0; t < TPS && !paired && !failed; ++t) {
       const float* T = tiles + ((size_t)s * TPS + t) * BV * DK;
       if constexpr (MODE == EAGER) {
         consume_eager<OP, DK, DV>(a, Lay, p, vt0 + t, T, ax, lane, g_s, beta_s);
       } else {
         const AuxView av = aux_view<OP, DK, MODE>(Lay, ax);
+        const bool split = SPLIT_PREP && !cprep;   // prep warps: coefficients come later
         released = consume_append<OP, DK, DV>(a, Lay, p, vt0 + t, T, av, lane, bars.empty(s),
-                                              t == TPS - 1);
+                                              t == TPS - 1, split ? bars.cready(x) : 0u, xpar,
+                                              &failed);
       }
     }
+    if (failed) break;
     // No proxy fence here: consumers never write shared memory that a bulk
     // copy refills (tiles are read-only; the aux slots they write are refilled
     // by cp.async, which is in the generic proxy), so the mbarrier release and

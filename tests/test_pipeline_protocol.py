@@ -46,7 +46,7 @@ class Bar:
 
 
 def simulate(NS, NA, G, n_tiles, owned, tile_first, seed, p_complete=0.03, lifo=0.95,
-             fused=False, ncw=NCW, npw=1, prep_by_unit=False):
+             fused=False, ncw=NCW, npw=1, prep_by_unit=False, split=False):
     NCW_ = ncw
     rng = random.Random(seed)
     R = NS // NCW_
@@ -61,13 +61,14 @@ def simulate(NS, NA, G, n_tiles, owned, tile_first, seed, p_complete=0.03, lifo=
     afull = [Bar(1) for _ in range(NA)]
     aempty = [Bar(G) for _ in range(NA)]
     cready = [Bar(1) for _ in range(NA)]   # fused form: the prep warp's signal
+    vready = [Bar(1) for _ in range(NA)]   # split: the unit's vectors, before cready
     inflight, violations = [], []
     prod = {"ti": 0, "ka": 0}
     # prep warp pw owns the aux slots x with x % npw == pw (npw divides NA) and
     # takes their units in order, so it sees every phase of those slots
     n_units = n_tiles // G
     prep = [{"ks": [k for k in range(n_units)
-                    if (k % npw if prep_by_unit else (k % NA) % npw) == pw], "j": 0}
+                    if (k % npw if prep_by_unit else (k % NA) % npw) == pw], "j": 0, "half": 0}
             for pw in range(npw)]
     cons = [{"i": w, "step": 0} for w in range(NCW_)]
     n_units = n_tiles // G
@@ -77,9 +78,18 @@ def simulate(NS, NA, G, n_tiles, owned, tile_first, seed, p_complete=0.03, lifo=
             return
         k = prep[pw]["ks"][prep[pw]["j"]]
         x = k % NA
+        if split and prep[pw]["half"] == 1:   # the coefficients, after the vectors
+            cready[x].arrive()
+            prep[pw]["half"] = 0
+            prep[pw]["j"] += 1
+            return
         if afull[x].try_wait((k // NA) & 1):
             if afull[x].done <= k // NA:
                 violations.append(("prep", k))
+            if split:
+                vready[x].arrive()
+                prep[pw]["half"] = 1
+                return
             cready[x].arrive()
             prep[pw]["j"] += 1
 
@@ -110,7 +120,9 @@ def simulate(NS, NA, G, n_tiles, owned, tile_first, seed, p_complete=0.03, lifo=
         order = [(full[s], phase(i)), ((cready if fused else afull)[x], kk // NA)]
         if not tile_first:
             order.reverse()
-        if c["step"] < 2:
+        if split:   # tile, then vectors (the pass over the tile), then coefficients
+            order = [(full[s], phase(i)), (vready[x], kk // NA), (cready[x], kk // NA)]
+        if c["step"] < len(order):
             bar, ph = order[c["step"]]
             if bar.try_wait(ph & 1):
                 if bar.done <= ph:
@@ -168,6 +180,19 @@ def test_fused_several_prep_warps_is_safe(npw, ncw, NS, NA, G):
     for seed in range(12):
         v, finished = simulate(NS, NA, G, 8 * 4 * 5, owned=True, tile_first=True, seed=seed,
                                fused=True, ncw=ncw, npw=npw)
+        assert not v and finished, (seed, v[:3])
+
+
+@pytest.mark.parametrize("npw,ncw,NS,NA,G", [(1, 4, 4, 2, 4), (1, 4, 4, 6, 4), (2, 4, 4, 4, 4),
+                                            (2, 8, 8, 2, 4), (1, 2, 2, 3, 4)])
+def test_fused_split_vectors_then_coefficients_is_safe(npw, ncw, NS, NA, G):
+    """The fused form with prep warps as the kernel runs it: a prep warp
+    arrives on a unit's vector barrier, then on its coefficient barrier; each
+    consumer waits for its tile, then the vectors (its pass over the tile),
+    then the coefficients (its epilogue)."""
+    for seed in range(10):
+        v, finished = simulate(NS, NA, G, ncw * G * 5, owned=True, tile_first=True, seed=seed,
+                               fused=True, ncw=ncw, npw=npw, split=True)
         assert not v and finished, (seed, v[:3])
 
 

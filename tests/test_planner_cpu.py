@@ -95,6 +95,10 @@ def test_every_plan_exists_and_fits_the_budgets(plans):
         assert p["cps"] * (p["smem"] + 1024) <= PER_SM, p
         stage = 32 * p["dk"] * 4 * p["tps"]
         assert p["smem"] >= p["ns"] * stage + p["na"] * p["aux"], p
+        # the mbarrier area (128): full and empty per stage, three per aux slot
+        # (four with prep warps), one spare
+        per_slot = 4 if p["npw"] > 0 else 3
+        assert 2 * p["ns"] + per_slot * p["na"] + 1 <= 128, p
         if p["regs"]:
             warps = p["ncw"] + 1 + p["npw"]
             alloc = 32 * ((p["regs"] + 7) // 8 * 8)
