@@ -202,19 +202,10 @@ __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
   }
 }
 
-// 1-D bulk copy global -> shared (TMA engine), completion counted in bytes on `bar`.
-// dst, src 16-byte aligned; bytes a non-zero multiple of 16.
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
-                                         uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
-// Same with an L2 eviction-priority policy: evict_first for a state that is
-// streamed through once per step, evict_normal for one small enough to stay in L2.
+// 1-D bulk copy global -> shared (TMA engine), completion counted in bytes on
+// `bar`, with an L2 eviction-priority policy: evict_first for a state that is
+// streamed through once per step, evict_normal for one small enough to stay in
+// L2.  dst, src 16-byte aligned; bytes a non-zero multiple of 16.
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
