@@ -568,6 +568,52 @@ __device__ __forceinline__ bool consume_append(const StepArgs& a, const Layout& 
   if (!merge) return may_release;
 
   // merge: S̄[slot] rows = D ⊙ S̄[base] rows + Σ_{j<=n} a_j[row] K̃_j
+  if constexpr (OP == RWKV6 && DK == 64) {
+    // Half-warp h takes rows 16h..16h+15 of the tile and lane l of it columns
+    // 4l..4l+3, so that one load of a value row feeds sixteen rows, and each
+    // packed FMA updates two adjacent rows of a column from one bf16 word.
+    // Per element: the same product D·S̄, then the same fused multiply-adds in
+    // the same order of j as the general loop below.
+    const int hr = (lane >> 4) * 16, c4 = (lane & 15) * 4;
+    const float4 Dv = *reinterpret_cast<const float4*>(cf + Lay.P0 + c4);
+    float2 acc[8][4];   // [row pair m][column]: rows hr + 2m, hr + 2m + 1
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const float4 t0 = *reinterpret_cast<const float4*>(T + (hr + 2 * m) * DK + c4);
+      const float4 t1 = *reinterpret_cast<const float4*>(T + (hr + 2 * m + 1) * DK + c4);
+      acc[m][0] = make_float2(Dv.x * t0.x, Dv.x * t1.x);
+      acc[m][1] = make_float2(Dv.y * t0.y, Dv.y * t1.y);
+      acc[m][2] = make_float2(Dv.z * t0.z, Dv.z * t1.z);
+      acc[m][3] = make_float2(Dv.w * t0.w, Dv.w * t1.w);
+    }
+    const uint16_t* Vb = reinterpret_cast<const uint16_t*>(av.U) + vt * BV + hr;
+#pragma unroll 1
+    for (int j = 0; j <= n; ++j) {
+      const float4 K = *reinterpret_cast<const float4*>(av.Kt + j * DK + c4);
+      const uint4 w0 = *reinterpret_cast<const uint4*>(Vb + j * DV);
+      const uint4 w1 = *reinterpret_cast<const uint4*>(Vb + j * DV + 8);
+      const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+      const float2 k0 = make_float2(K.x, K.x), k1 = make_float2(K.y, K.y);
+      const float2 k2 = make_float2(K.z, K.z), k3 = make_float2(K.w, K.w);
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const float2 vp = make_float2(bf16lo(w[m]), bf16hi(w[m]));
+        acc[m][0] = __ffma2_rn(vp, k0, acc[m][0]);
+        acc[m][1] = __ffma2_rn(vp, k1, acc[m][1]);
+        acc[m][2] = __ffma2_rn(vp, k2, acc[m][2]);
+        acc[m][3] = __ffma2_rn(vp, k3, acc[m][3]);
+      }
+    }
+    float* dst = a.Sbar + (((size_t)it.slot * a.H + p.h) * DV + vt * BV + hr) * DK + c4;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const float r0[4] = {acc[m][0].x, acc[m][1].x, acc[m][2].x, acc[m][3].x};
+      const float r1[4] = {acc[m][0].y, acc[m][1].y, acc[m][2].y, acc[m][3].y};
+      stvec_cs<4>(dst + (size_t)(2 * m) * DK, r0);
+      stvec_cs<4>(dst + (size_t)(2 * m + 1) * DK, r1);
+    }
+    return false;
+  }
   float D[VEC];
   if constexpr (OP == GDN) {
 #pragma unroll
