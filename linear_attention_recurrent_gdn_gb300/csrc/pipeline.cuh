@@ -622,6 +622,61 @@ __device__ __forceinline__ bool consume_append(const StepArgs& a, const Layout& 
     ldvec<VEC>(D, cf + Lay.P0 + lane * VEC);
   }
   float* dst = a.Sbar + (((size_t)it.slot * a.H + p.h) * DV + vt * BV) * DK + lane * VEC;
+  if constexpr (OP == GDN && DK == 128) {
+    // Sixteen rows at a time, each packed FMA updating two adjacent rows of a
+    // column: one load of a u row's sixteen values feeds 64 accumulators.
+    // Per element the same operations in the same order as the loop below.
+    // (Measured on GB300: GDN M = 16 windows 1.1 % faster; KDA, whose K̃ rows
+    // are fp32, 0.4 % slower at M = 16 and 1.7 % at M = 32, so it keeps the
+    // loop below.)
+#pragma unroll 1
+    for (int rb = 0; rb < 2; ++rb) {
+      float2 acc[8][VEC];   // [row pair m][column]: rows 16 rb + 2m, 16 rb + 2m + 1
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        float t0[VEC], t1[VEC];
+        ldvec<VEC>(t0, T + (rb * 16 + 2 * m) * DK + lane * VEC);
+        ldvec<VEC>(t1, T + (rb * 16 + 2 * m + 1) * DK + lane * VEC);
+#pragma unroll
+        for (int c = 0; c < VEC; ++c) acc[m][c] = make_float2(D[c] * t0[c], D[c] * t1[c]);
+      }
+#pragma unroll 1
+      for (int j = 0; j <= n; ++j) {
+        float K[VEC];
+        ldvec_bf16<VEC>(K, av.kl + j * DK + lane * VEC);
+        const float w = cf[Lay.P0 + j];
+#pragma unroll
+        for (int c = 0; c < VEC; ++c) K[c] *= w;
+        const float4* U =
+            reinterpret_cast<const float4*>(reinterpret_cast<const float*>(av.U) + j * DV + vt * BV + rb * 16);
+        float2 up[8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 u = U[q];
+          up[2 * q] = make_float2(u.x, u.y);
+          up[2 * q + 1] = make_float2(u.z, u.w);
+        }
+#pragma unroll
+        for (int c = 0; c < VEC; ++c) {
+          const float2 kk = make_float2(K[c], K[c]);
+#pragma unroll
+          for (int m = 0; m < 8; ++m) acc[m][c] = __ffma2_rn(up[m], kk, acc[m][c]);
+        }
+      }
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        float r0[VEC], r1[VEC];
+#pragma unroll
+        for (int c = 0; c < VEC; ++c) {
+          r0[c] = acc[m][c].x;
+          r1[c] = acc[m][c].y;
+        }
+        stvec_cs<VEC>(dst + (size_t)(rb * 16 + 2 * m) * DK, r0);
+        stvec_cs<VEC>(dst + (size_t)(rb * 16 + 2 * m + 1) * DK, r1);
+      }
+    }
+    return false;
+  }
 #pragma unroll 1
   for (int rb = 0; rb < 4; ++rb) {
     float acc[8][VEC];
