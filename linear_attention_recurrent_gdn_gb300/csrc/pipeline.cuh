@@ -464,7 +464,8 @@ __device__ __forceinline__ void rwkv6_row_chunk(float (&s)[4], const float* Trow
 __device__ __forceinline__ float sum4(const float (&s)[4]) { return (s[0] + s[1]) + (s[2] + s[3]); }
 
 // Returns true if it already released the tile stage (append steps release it
-// right after the pass over the tile, so the refill overlaps the epilogue).
+// right after the pass over the tile, so the refill overlaps the epilogue;
+// GDN and RWKV6 merge steps once the update has read the tile's last rows).
 // With `coef_bar` set (fused form with prep warps) the pass over the tile
 // runs as soon as its vectors are in place, and the coefficients are awaited
 // on coef_bar (phase parity coef_par) before the epilogue; if that wait gives
@@ -568,6 +569,15 @@ __device__ __forceinline__ bool consume_append(const StepArgs& a, const Layout& 
   if (!merge) return may_release;
 
   // merge: S̄[slot] rows = D ⊙ S̄[base] rows + Σ_{j<=n} a_j[row] K̃_j
+  // The tile is read only for D ⊙ S̄: once the last of its rows are in
+  // registers, the stage goes back to the producer (if this call may release
+  // it), so that the next unit's tile lands while the update runs.
+  auto release_stage = [&]() {
+    if (may_release) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty_bar);
+    }
+  };
   if constexpr (OP == RWKV6 && DK == 64) {
     // Half-warp h takes rows 16h..16h+15 of the tile and lane l of it columns
     // 4l..4l+3, so that one load of a value row feeds sixteen rows, and each
@@ -586,6 +596,7 @@ __device__ __forceinline__ bool consume_append(const StepArgs& a, const Layout& 
       acc[m][2] = make_float2(Dv.z * t0.z, Dv.z * t1.z);
       acc[m][3] = make_float2(Dv.w * t0.w, Dv.w * t1.w);
     }
+    release_stage();
     const uint16_t* Vb = reinterpret_cast<const uint16_t*>(av.U) + vt * BV + hr;
 #pragma unroll 1
     for (int j = 0; j <= n; ++j) {
@@ -612,7 +623,7 @@ __device__ __forceinline__ bool consume_append(const StepArgs& a, const Layout& 
       stvec_cs<4>(dst + (size_t)(2 * m) * DK, r0);
       stvec_cs<4>(dst + (size_t)(2 * m + 1) * DK, r1);
     }
-    return false;
+    return may_release;
   }
   float D[VEC];
   if constexpr (OP == GDN) {
@@ -640,6 +651,7 @@ __device__ __forceinline__ bool consume_append(const StepArgs& a, const Layout& 
 #pragma unroll
         for (int c = 0; c < VEC; ++c) acc[m][c] = make_float2(D[c] * t0[c], D[c] * t1[c]);
       }
+      if (rb == 1) release_stage();
 #pragma unroll 1
       for (int j = 0; j <= n; ++j) {
         float K[VEC];
@@ -675,7 +687,7 @@ __device__ __forceinline__ bool consume_append(const StepArgs& a, const Layout& 
         stvec_cs<VEC>(dst + (size_t)(rb * 16 + 2 * m + 1) * DK, r1);
       }
     }
-    return false;
+    return may_release;
   }
 #pragma unroll 1
   for (int rb = 0; rb < 4; ++rb) {
@@ -719,6 +731,9 @@ __device__ __forceinline__ bool consume_append(const StepArgs& a, const Layout& 
 #pragma unroll
     for (int i = 0; i < 8; ++i) stvec_cs<VEC>(dst + (size_t)(rb * 8 + i) * DK, acc[i]);
   }
+  // The general loop (KDA, and every op at other head sizes) keeps the stage
+  // to the end: releasing it before the last quarter's update measured 0.6 %
+  // slower for KDA at M = 32 on GB300, and no faster at M = 16.
   return false;
 }
 
