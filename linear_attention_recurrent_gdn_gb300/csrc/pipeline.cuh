@@ -355,41 +355,76 @@ __device__ __forceinline__ void prep_unit(const StepArgs& a, const Layout& Lay, 
       __syncwarp();
       if (lane == 0) mbar_arrive(vbar);
     }
+    if constexpr (OP == KDA) {
+      // Entries in groups of four, one transposed reduction per group and
+      // product, in a rolled loop: the prep's code stays small enough for the
+      // instruction cache next to the consumers', and short logs stop early.
+      // Measured on GB300: the fully unrolled loop left KDA launches at a 77 %
+      // instruction-cache hit rate (91 % now); M = 16 windows 849 -> 787 us,
+      // M = 32 2731 -> 2086 us.
+#pragma unroll 1
+      for (int j0 = 0; j0 < n; j0 += 4) {
+        float q1[4], q2[4];
 #pragma unroll
-    for (int j = 0; j < NE; ++j) {
-      float x = 0.f, y = 0.f;
-      if (j < n) {
-        float kj[VEC], lj[VEC], kk[VEC];
-        ldvec_bf16<VEC>(kj, kl + j * DK + c0);
-        ldvec<VEC>(lj, Ls + (size_t)j * DK + c0);
+        for (int jj = 0; jj < 4; ++jj) {
+          const int j = j0 + jj;
+          float x = 0.f, y = 0.f;
+          if (j < n) {
+            float kj[VEC], lj[VEC], kk[VEC];
+            ldvec_bf16<VEC>(kj, kl + j * DK + c0);
+            ldvec<VEC>(lj, Ls + (size_t)j * DK + c0);
 #pragma unroll
-        for (int c = 0; c < VEC; ++c) {
-          kk[c] = kj[c] * __expf(Lc[c] - lj[c]);
-          if (OP == KDA) {
-            x += kk[c] * kv[c];
-            y += kk[c] * qv[c];
-          } else {
-            x += kk[c] * qv[c];
+            for (int c = 0; c < VEC; ++c) {
+              kk[c] = kj[c] * __expf(Lc[c] - lj[c]);
+              x += kk[c] * kv[c];
+              y += kk[c] * qv[c];
+            }
+            if (merge) {   // K̃_j = k_j ⊙ e^{Λ_t-Λ_j} over this lane's columns of row j
+#pragma unroll
+              for (int c = 0; c < VEC; ++c) Ls[(size_t)j * DK + c0 + c] = kk[c];
+            }
           }
+          q1[jj] = x;
+          q2[jj] = y;
         }
-        if (merge) {   // K̃_j = k_j ⊙ e^{Λ_t-Λ_j} over this lane's columns of row j
-#pragma unroll
-          for (int c = 0; c < VEC; ++c) Ls[(size_t)j * DK + c0 + c] = kk[c] * wt[c];
+        const float d1 = reduce_entries<4>(q1, lane);   // entry j0 + lane / 8
+        const float d2 = reduce_entries<4>(q2, lane);
+        const int e = j0 + (lane >> 3);
+        if ((lane & 7) == 0 && e < n) {
+          cf[HDR + e] = d1;
+          cf[HDR + Mcap4 + e] = d2;
         }
       }
-      p1[j] = x;
-      p2[j] = y;
-    }
-    if (merge) {
+      if (merge) {
 #pragma unroll
-      for (int c = 0; c < VEC; ++c) Ls[(size_t)n * DK + c0 + c] = kv[c];   // K̃_n = k_t
-    }
-    const float d1 = reduce_entries<NE>(p1, lane);
-    float d2 = 0.f;
-    if constexpr (OP == KDA) d2 = reduce_entries<NE>(p2, lane);
-    if (entry_writer && lane_entry < n) {
-      cf[HDR + lane_entry] = d1;
-      if constexpr (OP == KDA) cf[HDR + Mcap4 + lane_entry] = d2;
+        for (int c = 0; c < VEC; ++c) Ls[(size_t)n * DK + c0 + c] = kv[c];   // K̃_n = k_t
+      }
+    } else {   // RWKV6
+#pragma unroll
+      for (int j = 0; j < NE; ++j) {
+        float x = 0.f;
+        if (j < n) {
+          float kj[VEC], lj[VEC], kk[VEC];
+          ldvec_bf16<VEC>(kj, kl + j * DK + c0);
+          ldvec<VEC>(lj, Ls + (size_t)j * DK + c0);
+#pragma unroll
+          for (int c = 0; c < VEC; ++c) {
+            kk[c] = kj[c] * __expf(Lc[c] - lj[c]);
+            x += kk[c] * qv[c];
+          }
+          if (merge) {   // K̃_j = k_j ⊙ e^{Λ_t-Λ_j} over this lane's columns of row j
+#pragma unroll
+            for (int c = 0; c < VEC; ++c) Ls[(size_t)j * DK + c0 + c] = kk[c] * wt[c];
+          }
+        }
+        p1[j] = x;
+      }
+      if (merge) {
+#pragma unroll
+        for (int c = 0; c < VEC; ++c) Ls[(size_t)n * DK + c0 + c] = kv[c];   // K̃_n = k_t
+      }
+      const float d1 = reduce_entries<NE>(p1, lane);
+      if (entry_writer && lane_entry < n) cf[HDR + lane_entry] = d1;
     }
     if (!merge && owner) {
       float* Ld = a.Llog + (lh * Mcap + n) * DK + c0;
