@@ -246,9 +246,6 @@ template <int OP, int DK, int DV, int NE>
 __device__ __forceinline__ void prep_unit(const StepArgs& a, const Layout& Lay, const UnitPos& p,
                                           unsigned char* ax, int lane, uint32_t vbar = 0) {
   constexpr int VEC = DK / 32;
-  constexpr int SHIFT = NE == 32 ? 0 : NE == 16 ? 1 : 2;   // entry of lane l: l >> SHIFT
-  const int lane_entry = lane >> SHIFT;
-  const bool entry_writer = (lane & ((1 << SHIFT) - 1)) == 0;
   const StepItem it = step_item(a, p.row);
   const int n = it.n, slot = it.slot;
   const bool merge = (n + 1 == a.M);
@@ -265,7 +262,6 @@ __device__ __forceinline__ void prep_unit(const StepArgs& a, const Layout& Lay, 
   float kv[VEC], qv[VEC];
   ldvec_bf16<VEC>(kv, kq16 + c0);
   ldvec_bf16<VEC>(qv, kq16 + DK + c0);
-  float p1[NE], p2[NE];
   if constexpr (OP == GDN) {
     if (vbar && lane == 0) mbar_arrive(vbar);
     const float beta_t = reinterpret_cast<const float*>(ax + Lay.f_beta)[0];
@@ -274,28 +270,35 @@ __device__ __forceinline__ void prep_unit(const StepArgs& a, const Layout& Lay, 
 #pragma unroll
     for (int c = 0; c < VEC; ++c) kq += kv[c] * qv[c];
     kq = warp_sum(kq);
+    // entries in groups of four in a rolled loop (as KDA's below)
+#pragma unroll 1
+    for (int j0 = 0; j0 < n; j0 += 4) {
+      float q1[4], q2[4];
 #pragma unroll
-    for (int j = 0; j < NE; ++j) {
-      float x = 0.f, y = 0.f;
-      if (j < n) {
-        float kj[VEC];
-        ldvec_bf16<VEC>(kj, kl + j * DK + c0);
+      for (int jj = 0; jj < 4; ++jj) {
+        const int j = j0 + jj;
+        float x = 0.f, y = 0.f;
+        if (j < n) {
+          float kj[VEC];
+          ldvec_bf16<VEC>(kj, kl + j * DK + c0);
 #pragma unroll
-        for (int c = 0; c < VEC; ++c) {
-          x += kj[c] * kv[c];
-          y += kj[c] * qv[c];
+          for (int c = 0; c < VEC; ++c) {
+            x += kj[c] * kv[c];
+            y += kj[c] * qv[c];
+          }
         }
+        q1[jj] = x;
+        q2[jj] = y;
       }
-      p1[j] = x;
-      p2[j] = y;
-    }
-    const float dkk = reduce_entries<NE>(p1, lane);
-    const float dkq = reduce_entries<NE>(p2, lane);
-    if (entry_writer && lane_entry < n) {
-      const float wj = expf(Lt - Ls[lane_entry]);
-      cf[HDR + lane_entry] = wj * dkk;
-      cf[HDR + Mcap4 + lane_entry] = wj * dkq;
-      if (merge) cf[Lay.P0 + lane_entry] = wj;
+      const float dkk = reduce_entries<4>(q1, lane);   // entry j0 + lane / 8
+      const float dkq = reduce_entries<4>(q2, lane);
+      const int e = j0 + (lane >> 3);
+      if ((lane & 7) == 0 && e < n) {
+        const float wj = expf(Lt - Ls[e]);
+        cf[HDR + e] = wj * dkk;
+        cf[HDR + Mcap4 + e] = wj * dkq;
+        if (merge) cf[Lay.P0 + e] = wj;
+      }
     }
     if (lane == 0) {
       cf[0] = expf(Lt);
@@ -399,32 +402,38 @@ __device__ __forceinline__ void prep_unit(const StepArgs& a, const Layout& Lay, 
 #pragma unroll
         for (int c = 0; c < VEC; ++c) Ls[(size_t)n * DK + c0 + c] = kv[c];   // K̃_n = k_t
       }
-    } else {   // RWKV6
+    } else {   // RWKV6: the same grouping
+#pragma unroll 1
+      for (int j0 = 0; j0 < n; j0 += 4) {
+        float q1[4];
 #pragma unroll
-      for (int j = 0; j < NE; ++j) {
-        float x = 0.f;
-        if (j < n) {
-          float kj[VEC], lj[VEC], kk[VEC];
-          ldvec_bf16<VEC>(kj, kl + j * DK + c0);
-          ldvec<VEC>(lj, Ls + (size_t)j * DK + c0);
+        for (int jj = 0; jj < 4; ++jj) {
+          const int j = j0 + jj;
+          float x = 0.f;
+          if (j < n) {
+            float kj[VEC], lj[VEC], kk[VEC];
+            ldvec_bf16<VEC>(kj, kl + j * DK + c0);
+            ldvec<VEC>(lj, Ls + (size_t)j * DK + c0);
 #pragma unroll
-          for (int c = 0; c < VEC; ++c) {
-            kk[c] = kj[c] * __expf(Lc[c] - lj[c]);
-            x += kk[c] * qv[c];
+            for (int c = 0; c < VEC; ++c) {
+              kk[c] = kj[c] * __expf(Lc[c] - lj[c]);
+              x += kk[c] * qv[c];
+            }
+            if (merge) {   // K̃_j = k_j ⊙ e^{Λ_t-Λ_j} over this lane's columns of row j
+#pragma unroll
+              for (int c = 0; c < VEC; ++c) Ls[(size_t)j * DK + c0 + c] = kk[c] * wt[c];
+            }
           }
-          if (merge) {   // K̃_j = k_j ⊙ e^{Λ_t-Λ_j} over this lane's columns of row j
-#pragma unroll
-            for (int c = 0; c < VEC; ++c) Ls[(size_t)j * DK + c0 + c] = kk[c] * wt[c];
-          }
+          q1[jj] = x;
         }
-        p1[j] = x;
+        const float d1 = reduce_entries<4>(q1, lane);   // entry j0 + lane / 8
+        const int e = j0 + (lane >> 3);
+        if ((lane & 7) == 0 && e < n) cf[HDR + e] = d1;
       }
       if (merge) {
 #pragma unroll
         for (int c = 0; c < VEC; ++c) Ls[(size_t)n * DK + c0 + c] = kv[c];   // K̃_n = k_t
       }
-      const float d1 = reduce_entries<NE>(p1, lane);
-      if (entry_writer && lane_entry < n) cf[HDR + lane_entry] = d1;
     }
     if (!merge && owner) {
       float* Ld = a.Llog + (lh * Mcap + n) * DK + c0;
@@ -723,53 +732,54 @@ __device__ __forceinline__ bool consume_append(const StepArgs& a, const Layout& 
       }
     }
     return may_release;
-  }
+  } else {
 #pragma unroll 1
-  for (int rb = 0; rb < 4; ++rb) {
-    float acc[8][VEC];
+    for (int rb = 0; rb < 4; ++rb) {
+      float acc[8][VEC];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      float t[VEC];
-      ldvec<VEC>(t, T + (rb * 8 + i) * DK + lane * VEC);
+      for (int i = 0; i < 8; ++i) {
+        float t[VEC];
+        ldvec<VEC>(t, T + (rb * 8 + i) * DK + lane * VEC);
 #pragma unroll
-      for (int c = 0; c < VEC; ++c) acc[i][c] = D[c] * t[c];
-    }
+        for (int c = 0; c < VEC; ++c) acc[i][c] = D[c] * t[c];
+      }
 #pragma unroll 2
-    for (int j = 0; j <= n; ++j) {
-      float K[VEC];
-      if constexpr (OP == GDN) {
-        ldvec_bf16<VEC>(K, av.kl + j * DK + lane * VEC);
-        const float w = cf[Lay.P0 + j];
+      for (int j = 0; j <= n; ++j) {
+        float K[VEC];
+        if constexpr (OP == GDN) {
+          ldvec_bf16<VEC>(K, av.kl + j * DK + lane * VEC);
+          const float w = cf[Lay.P0 + j];
 #pragma unroll
-        for (int c = 0; c < VEC; ++c) K[c] *= w;
-      } else {
-        ldvec<VEC>(K, av.Kt + j * DK + lane * VEC);
+          for (int c = 0; c < VEC; ++c) K[c] *= w;
+        } else {
+          ldvec<VEC>(K, av.Kt + j * DK + lane * VEC);
+        }
+        float uu[8];
+        if constexpr (DELTA) {
+          const float* U = reinterpret_cast<const float*>(av.U) + j * DV + vt * BV + rb * 8;
+          const float4 u0 = *reinterpret_cast<const float4*>(U);
+          const float4 u1 = *reinterpret_cast<const float4*>(U + 4);
+          uu[0] = u0.x; uu[1] = u0.y; uu[2] = u0.z; uu[3] = u0.w;
+          uu[4] = u1.x; uu[5] = u1.y; uu[6] = u1.z; uu[7] = u1.w;
+        } else {
+          const uint4 w = *reinterpret_cast<const uint4*>(
+              reinterpret_cast<const uint16_t*>(av.U) + j * DV + vt * BV + rb * 8);
+          uu[0] = bf16lo(w.x); uu[1] = bf16hi(w.x); uu[2] = bf16lo(w.y); uu[3] = bf16hi(w.y);
+          uu[4] = bf16lo(w.z); uu[5] = bf16hi(w.z); uu[6] = bf16lo(w.w); uu[7] = bf16hi(w.w);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+          for (int c = 0; c < VEC; ++c) acc[i][c] += uu[i] * K[c];
       }
-      float uu[8];
-      if constexpr (DELTA) {
-        const float* U = reinterpret_cast<const float*>(av.U) + j * DV + vt * BV + rb * 8;
-        const float4 u0 = *reinterpret_cast<const float4*>(U);
-        const float4 u1 = *reinterpret_cast<const float4*>(U + 4);
-        uu[0] = u0.x; uu[1] = u0.y; uu[2] = u0.z; uu[3] = u0.w;
-        uu[4] = u1.x; uu[5] = u1.y; uu[6] = u1.z; uu[7] = u1.w;
-      } else {
-        const uint4 w = *reinterpret_cast<const uint4*>(
-            reinterpret_cast<const uint16_t*>(av.U) + j * DV + vt * BV + rb * 8);
-        uu[0] = bf16lo(w.x); uu[1] = bf16hi(w.x); uu[2] = bf16lo(w.y); uu[3] = bf16hi(w.y);
-        uu[4] = bf16lo(w.z); uu[5] = bf16hi(w.z); uu[6] = bf16lo(w.w); uu[7] = bf16hi(w.w);
-      }
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int c = 0; c < VEC; ++c) acc[i][c] += uu[i] * K[c];
+      for (int i = 0; i < 8; ++i) stvec_cs<VEC>(dst + (size_t)(rb * 8 + i) * DK, acc[i]);
     }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) stvec_cs<VEC>(dst + (size_t)(rb * 8 + i) * DK, acc[i]);
+    // The general loop (KDA, and every op at other head sizes) keeps the stage
+    // to the end: releasing it before the last quarter's update measured 0.6 %
+    // slower for KDA at M = 32 on GB300, and no faster at M = 16.
+    return false;
   }
-  // The general loop (KDA, and every op at other head sizes) keeps the stage
-  // to the end: releasing it before the last quarter's update measured 0.6 %
-  // slower for KDA at M = 32 on GB300, and no faster at M = 16.
-  return false;
 }
 
 // RWKV6 append step at d_k = 64, where one stage holds both 32-row tiles of the
