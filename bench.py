@@ -622,19 +622,28 @@ def run_ours(args):
         for _ in range(args.warmup):
             host_run()
         barrier(dist)
-        t0 = time.perf_counter()
-        e2e_steps = max(1, min(args.steps, 5))
-        for _ in range(e2e_steps):
-            host_run()
-        torch.cuda.synchronize()
-        e2e_ms = reduce_max(dist, (time.perf_counter() - t0) * 1e3 / e2e_steps, dev)
+        # up to 20 calls (about a second for the serving batch): a call now and
+        # then runs ~20 ms long (no clock event, no host load behind it), and
+        # more calls keep one such call from moving the mean by more than ~2 %
+        e2e_steps = max(1, min(args.steps, 20))
+        call_ms = []   # each call returns once its outputs are on the host
+        with ClockSampler(local) as e2e_clk:
+            t0 = time.perf_counter()
+            for _ in range(e2e_steps):
+                t1 = time.perf_counter()
+                host_run()
+                call_ms.append((time.perf_counter() - t1) * 1e3)
+            torch.cuda.synchronize()
+            e2e_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
+        e2e_ms = reduce_max(dist, e2e_ms, dev)
         c.close()
         h2d = sum(v[0].numel() * v.element_size() for v in pin.values() if v is not None) * T
         d2h = hout[0].numel() * hout.element_size() * T
         group, path = decode_host_group(op, B, H, d, M, T)
         result["e2e"] = {"value": units_per_step * world / (e2e_ms / 1e3), "unit": "tokens·heads/s",
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                         "ms_per_step": e2e_ms, "api": "dl_decode_host", "path": path,
+                         "ms_per_step": e2e_ms, "ms_per_call": [round(t, 2) for t in call_ms],
+                         "clocks": e2e_clk.summary(), "api": "dl_decode_host", "path": path,
                          "copy_ceiling": copy_ceiling(pin, hout, dev, T, group,
                                                       units_per_step * world, args)}
         del pin, hout
