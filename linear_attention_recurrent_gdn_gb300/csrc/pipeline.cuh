@@ -235,10 +235,14 @@ __device__ __forceinline__ void issue_coef_and_arrive(const StepArgs& a, const L
 // ("Kernel implementation — Staged execution"), computed by one warp of the
 // AppendDecode CTA from the unit's inputs already in shared memory, and
 // written into the unit's aux slot for its value-tile consumers.  The same
-// arithmetic as the ReplayPrep kernel (replay_prep.cu); see there for the
-// formulas.  On an append step the owner unit (value-tile group 0) of the
-// slot-head also appends k_t, Λ_t (and v_t for RWKV6) to the slot's log in HBM,
-// and the (head 0, group 0) unit advances the device slot table.
+// formulas as the ReplayPrep kernel (replay_prep.cu, which states them); this
+// stage sums each entry's lane partials in groups of four entries, that kernel
+// in one butterfly over all entries, so the two agree to rounding.  Every
+// fused launch runs this stage, whatever its batch, so a slot-head's bits do
+// not depend on the batch.  On an append step the owner unit (value-tile
+// group 0) of the slot-head also appends k_t, Λ_t (and v_t for RWKV6) to the
+// slot's log in HBM, and the (head 0, group 0) unit advances the device slot
+// table.
 // `vbar` (prep warps only, else 0): arrived on once the consumers' pass over
 // the tile has what it reads (GDN: at once, it reads k_t, q_t from the aux
 // slot; KDA and RWKV6: once k̂, q̂ or r̂ are written).
@@ -703,8 +707,8 @@ __device__ __forceinline__ bool consume_append(const StepArgs& a, const Layout& 
         const float w = cf[Lay.P0 + j];
 #pragma unroll
         for (int c = 0; c < VEC; ++c) K[c] *= w;
-        const float4* U =
-            reinterpret_cast<const float4*>(reinterpret_cast<const float*>(av.U) + j * DV + vt * BV + rb * 16);
+        const float* Urow = reinterpret_cast<const float*>(av.U) + j * DV + vt * BV + rb * 16;
+        const float4* U = reinterpret_cast<const float4*>(Urow);
         float2 up[8];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
