@@ -31,14 +31,16 @@ def _lib():
 
 @pytest.mark.parametrize("op", OPS)
 @pytest.mark.parametrize("d", [64, 128])
-def test_batch_invariance_bitwise(op, d):
+@pytest.mark.parametrize("M", [4, 16, 32])
+def test_batch_invariance_bitwise(op, d, M):
     """A slot stepped alone (one-tile units) gives the bits it gets inside a
     1280 slot-head batch (whole-slot-head units: at d = 64 both tiles in one
-    stage, RWKV6's append steps through the two-tile pass), over two merges.
-    Outputs in fp32, so that a change of summation order cannot hide behind
-    bf16 rounding."""
+    stage, RWKV6's append steps through the two-tile pass; at d = 128 prep
+    warps, with split waits for per-key logs of up to 32 entries), over two
+    merges, for each log-entry bound (8, 16, 32).  Outputs in fp32, so that a
+    change of summation order cannot hide behind bf16 rounding."""
     from linear_attention_recurrent_gdn_gb300 import deltalog as dl
-    B, H, M, T = 320, 4, 4, 9                  # 1280 slot-heads: whole-slot-head units
+    B, H, T = 320, 4, 2 * M + 1                # 1280 slot-heads: whole-slot-head units
     x, S0, bonus = make_case(op, B, H, d, T, seed=400 + op, device="cuda")
     probe = [0, 77, 319]
     big = dl.DeltaLog(op, B, H, d, d, M, out_bf16=False)
