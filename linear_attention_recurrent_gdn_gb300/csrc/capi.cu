@@ -353,14 +353,21 @@ dl_status run_step(dl_ctx* c, const int32_t* slots, int32_t n, const void* q, co
     bool all_merge = fused && a.plan_dev == nullptr && f.merge_interval >= 8;
     for (int32_t i = 0; i < rows && all_merge; ++i)
       all_merge = a.items[i].n + 1 == f.merge_interval;
-    // Aux slots hold the launch's longest log (plus the current token's row)
-    // when every row's log length is known on the host; a ragged window's
-    // rows are only known on the device, so its slots hold M rows.
+    // Aux slots hold the launch's longest log when every row's log length is
+    // known on the host, plus the current token's row where a step uses it:
+    // RWKV6's v_t, and a merge step's u_t and k_t (delta-rule appends write
+    // u_t straight to the log in HBM).  A ragged window's rows are only known
+    // on the device, so its slots hold M rows.
     a.arows = 0;
     if (a.plan_dev == nullptr) {
       int32_t nmax = 0;
-      for (int32_t i = 0; i < rows; ++i) nmax = a.items[i].n > nmax ? a.items[i].n : nmax;
-      a.arows = nmax + 1;
+      bool any_merge = false;
+      for (int32_t i = 0; i < rows; ++i) {
+        nmax = a.items[i].n > nmax ? a.items[i].n : nmax;
+        any_merge = any_merge || a.items[i].n + 1 == f.merge_interval;
+      }
+      const bool row_n = f.op == DL_RWKV6 || any_merge;
+      a.arows = row_n ? nmax + 1 : (nmax > 0 ? nmax : 1);
     }
     const dl::Layout Ll = dl::make_layout(f.op, f.merge_interval, f.d_k, f.d_v, a.arows);
     a.aux_bytes = Ll.aux_bytes;

@@ -78,7 +78,8 @@ struct StepArgs {
                          //    tiles of rows with n > 0 may stream before griddepcontrol.wait
   int32_t aux_bytes;     // bytes of one aux slot
   int32_t arows;         // log rows an aux slot holds in this launch (0: M); every row's
-                         // log length n must be below it
+                         // log length n is at most arows, and below it where the step
+                         // uses the current token's row n (RWKV6, merge steps)
   int32_t out_bf16;
   float scale;
   // How long a bounded wait spins before it records an error and gives up

@@ -20,10 +20,10 @@
 //   U      value-side log rows 0..n-1 (fp32 u_j; bf16 v_j for RWKV6) and one
 //          more row: u_t written by the consumer at a merge, or v_t (RWKV6)
 //   kl     GDN merge: key log rows 0..n-1 and k_t as row n, bf16 [M][d_k]
-// The log-row sections hold `arows` rows: M by default, or the largest log
-// length n of a launch's rows plus one (the current token's row), when the
-// launcher knows every row's n, so that short logs leave room for more units
-// in flight.
+// The log-row sections hold `arows` rows: M by default, or, when the launcher
+// knows every row's n, the largest log length n of a launch's rows, plus one
+// where a step uses the current token's row (RWKV6's v_t, a merge step's u_t
+// and k_t), so that short logs leave room for more units in flight.
 #pragma once
 
 #ifdef __CUDACC__
