@@ -759,10 +759,17 @@ def copy_ceiling(pin, hout, dev, T, group, units, args):
 
 def prefill_mma_flops(op, d, C=PREFILL_C):
     """FLOPs (an FMA counts 2) the tensor-core prefill's MMAs execute per
-    token·head at d = 128, C = 32, every operand term and padded row included
-    (csrc/prefill_tc.cu): GDN D0 [K;Q;0]K^T (M=128, N=C, K=d), D1 S̄[K;Q]^T in two
-    terms (N=2C), D2 the rank-C rewrite in two terms (N=d, K=C), D3 the outputs'
-    log terms in three (N=C, K=C); KDA the same with three terms each."""
+    token·head, C = 32, every operand term and padded row included
+    (csrc/prefill_tc.cu).  At d = 128: GDN D0 [K;Q;0]K^T (M=128, N=C, K=d), D1
+    S̄[K;Q]^T in two terms (N=2C), D2 the rank-C rewrite in two terms (N=d, K=C),
+    D3 the outputs' log terms in three (N=C, K=C); KDA the same with three terms
+    each.  RWKV6 at d = 64 stacks two slot-heads in each M = 128 MMA and forms
+    both heads' blocks of every product: D0 [r̂;0]k̄^T and D1 S̄r̂^T in three terms
+    (N=2C, K=d), D3 VA^T in two (N=2C, K=C), D2 Vk̃ in two (N=2d, K=C), over 2C
+    token·heads."""
+    if op == 2:
+        mac = 3 * 128 * 2 * C * d * 2 + 2 * 128 * 2 * C * C + 2 * 128 * 2 * d * C
+        return 2 * mac / (2 * C)
     terms = {0: (1, 2, 2, 3), 1: (3, 3, 3, 3)}[op]
     mac = (terms[0] * 128 * C * d + terms[1] * 128 * 2 * C * d + terms[2] * 128 * d * C
            + terms[3] * 128 * C * C)
@@ -858,7 +865,8 @@ def run_prefill(args):
     ms, clocks = timed_steps(one, args, dist, local, dev, stream)
     units = B * H * T
     tflops = units * prefill_flops(op, d) / (ms / 1e3) / 1e12
-    tensor = op in (0, 1) and d == 128      # GDN and KDA at d = 128 run on the tensor cores
+    # GDN and KDA at d = 128 and RWKV6 at d = 64 run on the tensor cores
+    tensor = (op in (0, 1) and d == 128) or (op == 2 and d == 64)
     if tensor:
         try:
             bf16_peak = float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["bf16_tflops"])

@@ -86,8 +86,9 @@ cudaError_t launch_checkpoint(int op, int dk, const CkptArgs& a, cudaStream_t s)
 
 // Chunked prefill of T tokens: token-major inputs [T, rows, H, d]; `bonus`
 // [H, d_k] for RWKV6.
-// GDN and KDA at d_k = d_v = 128 run on the tensor cores (prefill_tc.cu); a bounded
-// wait there that runs out records DEV_TIMEOUT_MMA in `status`.
+// GDN and KDA at d_k = d_v = 128 and RWKV6 at 64 run on the tensor cores
+// (prefill_tc.cu); a bounded wait there that runs out records DEV_TIMEOUT_MMA
+// in `status`.
 cudaError_t launch_prefill(int op, int dk, const SlotListArgs& a, const void* q, const void* k,
                            const void* v, const float* g, const float* beta, const float* bonus,
                            void* o, int T, int out_bf16, float scale, int32_t* status,
@@ -98,5 +99,10 @@ cudaError_t launch_prefill_gdn_tc(const SlotListArgs& a, const void* q, const vo
 cudaError_t launch_prefill_kda_tc(const SlotListArgs& a, const void* q, const void* k,
                                   const void* v, const float* g, const float* beta, void* o, int T,
                                   int out_bf16, float scale, int32_t* status, cudaStream_t s);
+// RWKV6 at d_k = d_v = 64: two slot-heads per CTA on the tensor cores (r in `r`).
+cudaError_t launch_prefill_rwkv6_tc(const SlotListArgs& a, const void* r, const void* k,
+                                    const void* v, const float* g, const float* bonus, void* o,
+                                    int T, int out_bf16, float scale, int32_t* status,
+                                    cudaStream_t s);
 
 }  // namespace dl

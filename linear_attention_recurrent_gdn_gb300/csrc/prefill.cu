@@ -762,7 +762,7 @@ cudaError_t launch_prefill(int op, int dk, const SlotListArgs& a, const void* q,
     if (dk == 64) return pk_dispatch<KDA, 64>(a, q, k, v, g, beta, bonus, o, T, out_bf16, scale, s);
     return launch_prefill_kda_tc(a, q, k, v, g, beta, o, T, out_bf16, scale, status, s);
   }
-  if (dk == 64) return pk_dispatch<RWKV6, 64>(a, q, k, v, g, beta, bonus, o, T, out_bf16, scale, s);
+  if (dk == 64) return launch_prefill_rwkv6_tc(a, q, k, v, g, bonus, o, T, out_bf16, scale, status, s);
   return pk_dispatch<RWKV6, 128>(a, q, k, v, g, beta, bonus, o, T, out_bf16, scale, s);
 }
 

@@ -978,6 +978,439 @@ prefill_kda_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* __
   }
 }
 
+
+// ------------------------------------------------------------------ RWKV6 ----
+// Chunked prefill of RWKV6 at d_k = d_v = 64 on the tensor cores, two
+// slot-heads per CTA (flattened slot-heads 2b and 2b + 1) stacked into the
+// 128 rows of an M = 128 MMA.  RWKV6 has no delta rule: with Λ_j the inclusive
+// cumulative log-decay inside the chunk (Λ_{-1} = 0), r̂_j = e^{Λ_{j-1}} ⊙ r_j,
+// k̄_s = e^{-Λ_s} ⊙ k_s and k̃_s = e^{Λ_C-Λ_s} ⊙ k_s,
+//   o_j = scale (S̄ r̂_j + Σ_{s<j} (r̂_j·k̄_s) v_s + c_j v_j),  c_j = Σ_c r_j[c] u[c] k_j[c]
+//   S̄'  = S̄ Diag(e^{Λ_C}) + Σ_s v_s k̃_s^T
+// (the same algebra as prefill_perkey_kernel in prefill.cu).  Value rows of
+// head e sit at rows 64 e + v, its tokens at rows 32 e + j of the token-row
+// operands, its key channels at rows 64 e + c of k̃; each product is formed for
+// both heads at once and only head e's block of it is read:
+//   D0 [128 x 64]  = [r̂; 0] k̄^T    pair coefficients (rows 32 e + j, columns 32 e + s)
+//   D1 [128 x 64]  = S̄ r̂^T         rows 64 e + v, columns 32 e + j
+//   D3 [128 x 64]  = V A^T           the outputs' log terms, the same blocks
+//   D2 [128 x 128] = V k̃            rows 64 e + v, columns 64 e + c
+// S̄, r̂, k̄, k̃ and A are fp32, carried as hi + lo bf16 terms (three products
+// for S̄ r̂ and r̂ k̄, two with the exact bf16 V).  The factored pair products
+// stay finite while the chunk's log-decay stays above -60 in every channel,
+// as in KDA's kernel; a chunk below it forms A directly on the CUDA cores.
+constexpr int RW_D = 64;
+constexpr uint32_t RW_COLS = 512;   // TMEM: D0 [0, 64), D1 [64, 128), D3 [128, 192), D2 [256, 384)
+constexpr int RW_LP = 2 * RW_D + 4;   // fp32 Λ rows: 128 columns (64 e + c), padded
+
+struct RwSmem {
+  static constexpr uint32_t SHI = 0;                          // S̄ hi [128 x 64] K-major
+  static constexpr uint32_t SLO = SHI + 128 * RW_D * 2;
+  static constexpr uint32_t RHI = SLO + 128 * RW_D * 2;       // [r̂ (64 rows: 32 e + j); 0 (64)] x 64
+  static constexpr uint32_t RLO = RHI + 128 * RW_D * 2;
+  static constexpr uint32_t KBHI = RLO + 128 * RW_D * 2;      // k̄ [64 rows (32 e + s)] x 64
+  static constexpr uint32_t KBLO = KBHI + 64 * RW_D * 2;
+  static constexpr uint32_t KTHI = KBLO + 64 * RW_D * 2;      // k̃ [128 rows (64 e + c)] x [32 tokens]
+  static constexpr uint32_t KTLO = KTHI + 128 * TC_C * 2;
+  static constexpr uint32_t VO = KTLO + 128 * TC_C * 2;       // V [128 rows (64 e + v)] x [32 tokens]
+  static constexpr uint32_t AHI = VO + 128 * TC_C * 2;        // A [64 rows (32 e + j)] x [32 (s)]
+  static constexpr uint32_t ALO = AHI + 64 * TC_C * 2;
+  static constexpr uint32_t LP = ALO + 64 * TC_C * 2;         // g, then Λ_j, fp32 [32][RW_LP]
+  static constexpr uint32_t EC = LP + TC_C * RW_LP * 4;       // e^{Λ_C} [128]
+  static constexpr uint32_t UB = EC + 128 * 4;                // bonus u of both heads [128]
+  static constexpr uint32_t CBP = UB + 128 * 4;               // c_j partials [2][32][8]
+  static constexpr uint32_t CB = CBP + 2 * TC_C * 8 * 4;      // c_j [2][32]
+  static constexpr uint32_t BAR = CB + 2 * TC_C * 4;          // 2 mbarriers, TMEM base, ok flag
+  static constexpr uint32_t BYTES = BAR + 32;
+};
+static_assert(RwSmem::BYTES <= 227 * 1024, "shared memory");
+static_assert(RwSmem::LP % 16 == 0 && RwSmem::BAR % 16 == 0, "16-byte aligned buffers");
+
+// One chunk's r, k, v (bf16) and g of the CTA's two slot-heads, in registers
+// between the global loads and the shared-memory stores.  The two slot-heads'
+// rows of a token are adjacent in the token-major inputs, so a token's 128
+// values (64 e + c) are one contiguous run; a second slot-head past the batch
+// (`two` false) loads zeros.
+struct RwStage {
+  uint4 r[2], k[2], v[2];
+  float4 gv[4];
+
+  __device__ __forceinline__ void load(const uint16_t* __restrict__ rg, const uint16_t* __restrict__ kg,
+                                       const uint16_t* __restrict__ vg, const float* __restrict__ gg,
+                                       int t0, int Cc, size_t nH, int sh0, bool two, int tid) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      int j, cv;
+      chunk_piece(tid + e * TC_THREADS, j, cv);   // cv / 8: slot-head, (cv % 8) * 8: channel
+      if (j < Cc && (two || cv < 8)) {
+        const size_t base = ((size_t)(t0 + j) * nH + sh0) * RW_D + cv * 8;
+        r[e] = *reinterpret_cast<const uint4*>(rg + base);
+        k[e] = *reinterpret_cast<const uint4*>(kg + base);
+        v[e] = *reinterpret_cast<const uint4*>(vg + base);
+      } else {
+        r[e] = k[e] = v[e] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int idx = tid + e * TC_THREADS, j = idx >> 5, c4 = idx & 31;
+      gv[e] = (j < Cc && (two || c4 < 16))
+                  ? *reinterpret_cast<const float4*>(gg + ((size_t)(t0 + j) * nH + sh0) * RW_D + 4 * c4)
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+
+  __device__ __forceinline__ void store_g(unsigned char* sm, int tid) const {
+    float* Lp = reinterpret_cast<float*>(sm + RwSmem::LP);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int idx = tid + e * TC_THREADS, j = idx >> 5, c4 = idx & 31;
+      *reinterpret_cast<float4*>(Lp + j * RW_LP + 4 * c4) = gv[e];
+    }
+  }
+};
+
+// A bf16 value of piece word w (element t of 8) as its 16 bits.
+__device__ __forceinline__ uint16_t piece_bits(const uint4 w, int t) {
+  const uint32_t x = (t >> 1) == 0 ? w.x : (t >> 1) == 1 ? w.y : (t >> 1) == 2 ? w.z : w.w;
+  return (uint16_t)((t & 1) ? (x >> 16) : (x & 0xffffu));
+}
+
+__global__ void __launch_bounds__(TC_THREADS, 1)
+prefill_rwkv6_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* __restrict__ r_in,
+                        const uint16_t* __restrict__ k_in, const uint16_t* __restrict__ v_in,
+                        const float* __restrict__ g, const float* __restrict__ bonus, void* o, int T,
+                        int out_bf16, float scale, int32_t* status) {
+  extern __shared__ __align__(1024) unsigned char sm[];
+  float* Lp = reinterpret_cast<float*>(sm + RwSmem::LP);
+  float* Ec = reinterpret_cast<float*>(sm + RwSmem::EC);
+  float* Ub = reinterpret_cast<float*>(sm + RwSmem::UB);
+  float* Cbp = reinterpret_cast<float*>(sm + RwSmem::CBP);
+  float* Cb = reinterpret_cast<float*>(sm + RwSmem::CB);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + RwSmem::BAR + 16);
+  int32_t* ok_flag = reinterpret_cast<int32_t*>(sm + RwSmem::BAR + 20);
+  const uint32_t sbase = smem_u32(sm);
+  const uint32_t bar1 = sbase + RwSmem::BAR, bar2 = sbase + RwSmem::BAR + 8;
+  constexpr uint32_t K_D0 = 0, K_D1 = 64, K_D3 = 128, K_D2 = 256;   // TMEM columns
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int q4 = warp & 3, hw = warp >> 2;
+  const int r = 32 * q4 + lane;          // row: slot-head e = r / 64, value row r % 64
+  const int he = r >> 6, vrow = r & 63;  // (he is uniform over a warp)
+  const int nH = a.rows * a.H;
+  const int sh0 = 2 * (int)blockIdx.x;
+  const bool two = sh0 + 1 < nH;
+  const int she = sh0 + he;
+  const bool mine = he == 0 || two;      // this thread's row belongs to a slot-head of the batch
+  auto state_of = [&](int sh) {
+    const int row = sh / a.H, h = sh - row * a.H;
+    return a.Sbar + ((size_t)a.items[row].slot * a.H + h) * RW_D * RW_D;
+  };
+
+  if (warp == 0) tc::tmem_alloc(sbase + RwSmem::BAR + 16, RW_COLS);
+  if (tid == 0) {
+    mbar_init(bar1, 1);
+    mbar_init(bar2, 1);
+    fence_mbar_init();
+    *ok_flag = 1;
+  }
+  // rows 64-127 of the [r̂; 0] operand stay zero
+  for (int idx = tid; idx < 64 * RW_D * 2 / 16; idx += TC_THREADS) {
+    reinterpret_cast<uint4*>(sm + RwSmem::RHI + 64 * RW_D * 2)[idx] = make_uint4(0u, 0u, 0u, 0u);
+    reinterpret_cast<uint4*>(sm + RwSmem::RLO + 64 * RW_D * 2)[idx] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  if (tid < 128) {   // bonus u of slot-head tid / 64, channel tid % 64
+    const int sh = sh0 + (tid >> 6);
+    Ub[tid] = sh < nH ? bonus[(size_t)(sh % a.H) * RW_D + (tid & 63)] : 0.f;
+  }
+  // this thread's state: S̄ of slot-head he, value row vrow, channels 32 hw .. 32 hw + 31
+  float S[32];
+  {
+    if (mine) {
+      const float4* src = reinterpret_cast<const float4*>(state_of(she) + (size_t)vrow * RW_D + 32 * hw);
+#pragma unroll
+      for (int c4 = 0; c4 < 8; ++c4) {
+        const float4 x = src[c4];
+        S[4 * c4] = x.x;
+        S[4 * c4 + 1] = x.y;
+        S[4 * c4 + 2] = x.z;
+        S[4 * c4 + 3] = x.w;
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < 32; ++c) S[c] = 0.f;
+    }
+#pragma unroll
+    for (int c8 = 0; c8 < 4; ++c8) {
+      uint4 hv, lv;
+      split8(S + 8 * c8, hv, lv);
+      const uint32_t off = tc::kmaj_off(r, 32 * hw + 8 * c8, RW_D);
+      *reinterpret_cast<uint4*>(sm + RwSmem::SHI + off) = hv;
+      *reinterpret_cast<uint4*>(sm + RwSmem::SLO + off) = lv;
+    }
+  }
+  RwStage st;
+  st.load(r_in, k_in, v_in, g, 0, T < TC_C ? T : TC_C, (size_t)nH, sh0, two, tid);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tm = *tmem_slot;
+  const uint32_t tlane = tm + ((uint32_t)(32 * q4) << 16);
+  bool ok = true;
+  int chunk = 0;
+  for (int t0 = 0; t0 < T && ok; t0 += TC_C, ++chunk) {
+    const int Cc = (T - t0) < TC_C ? (T - t0) : TC_C;
+    const uint32_t par = (uint32_t)chunk & 1u;
+    // ---- stage g; Λ = inclusive scan of g down each of the 128 columns (64 e + c;
+    //      padding tokens and a missing second slot-head have g = 0); the vote:
+    //      does every column's chunk log-decay stay above the floor?
+    st.store_g(sm, tid);
+    __syncthreads();
+    float lc = 0.f;
+    if (tid < 128) {
+#pragma unroll 8
+      for (int j = 0; j < TC_C; ++j) {
+        lc += Lp[j * RW_LP + tid];
+        Lp[j * RW_LP + tid] = lc;
+      }
+      Ec[tid] = expf(lc);
+    }
+    const bool direct = __syncthreads_or(tid < 128 && !(lc >= KDA_FACTOR_FLOOR)) != 0;
+    // ---- operands, 8 channels of one token of one slot-head per piece (r, k, v
+    //      from registers): r̂ and k̄ (hi, lo) as token rows; k̃ (hi, lo) and V
+    //      transposed, as channel and value rows; the bonus sums' partials
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      int j, cv;
+      chunk_piece(tid + e * TC_THREADS, j, cv);
+      const int hd = cv >> 3, c0 = (cv & 7) * 8, col0 = 8 * cv;   // col0 = 64 hd + c0
+      float rx[8], kx[8], rh[8], kb[8], kt[8];
+      unpack8(st.r[e], rx);
+      unpack8(st.k[e], kx);
+      float cb = 0.f;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const int col = col0 + t;
+        const float lj = Lp[j * RW_LP + col];
+        const float lprev = j > 0 ? Lp[(j - 1) * RW_LP + col] : 0.f;
+        rh[t] = __expf(lprev) * rx[t];                                 // Λ_{j-1} <= 0
+        if (direct) {
+          kb[t] = 0.f;
+          kt[t] = j < Cc ? __expf(Lp[(TC_C - 1) * RW_LP + col] - lj) * kx[t] : 0.f;   // Λ_C - Λ_j <= 0
+        } else {
+          const float eb = __expf(-lj);                                // <= e^{60}
+          kb[t] = eb * kx[t];
+          kt[t] = j < Cc ? fminf(Ec[col] * eb, 1.f) * kx[t] : 0.f;
+        }
+        cb += rx[t] * Ub[col] * kx[t];
+      }
+      Cbp[(hd * TC_C + j) * 8 + (cv & 7)] = cb;
+      uint4 hv, lv;
+      const uint32_t otok = tc::kmaj_off(TC_C * hd + j, c0, RW_D);
+      split8(rh, hv, lv);
+      *reinterpret_cast<uint4*>(sm + RwSmem::RHI + otok) = hv;
+      *reinterpret_cast<uint4*>(sm + RwSmem::RLO + otok) = lv;
+      split8(kb, hv, lv);
+      *reinterpret_cast<uint4*>(sm + RwSmem::KBHI + otok) = hv;
+      *reinterpret_cast<uint4*>(sm + RwSmem::KBLO + otok) = lv;
+      split8(kt, hv, lv);
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {   // k̃_j[c] and v_j[c] at row 64 hd + c, column j
+        const uint32_t off = tc::kmaj_off(col0 + t, j, TC_C);
+        *reinterpret_cast<uint16_t*>(sm + RwSmem::KTHI + off) = piece_bits(hv, t);
+        *reinterpret_cast<uint16_t*>(sm + RwSmem::KTLO + off) = piece_bits(lv, t);
+        *reinterpret_cast<uint16_t*>(sm + RwSmem::VO + off) = piece_bits(st.v[e], t);
+      }
+    }
+    tc::fence_smem_to_async();   // S̄ terms and the chunk's operands, for the tensor cores
+    tc::fence_before_sync();
+    __syncthreads();
+    // ---- D0 = [r̂; 0] k̄^T (fast chunks) and D1 = S̄ r̂^T, three terms each
+    if (tid == 0) {
+      tc::fence_after_sync();
+      constexpr uint32_t id64 = tc::idesc_bf16_f32(128, 64);
+      const uint32_t sa[3] = {RwSmem::SHI, RwSmem::SLO, RwSmem::SHI};
+      const uint32_t ra[3] = {RwSmem::RHI, RwSmem::RLO, RwSmem::RHI};
+      const uint32_t rb[3] = {RwSmem::RHI, RwSmem::RHI, RwSmem::RLO};
+      const uint32_t kb3[3] = {RwSmem::KBHI, RwSmem::KBHI, RwSmem::KBLO};
+#pragma unroll
+      for (int term = 0; term < 3; ++term)
+#pragma unroll
+        for (int kk = 0; kk < RW_D / 16; ++kk) {
+          if (!direct)
+            tc::mma_bf16(tm + K_D0, tc::kmaj_desc(sbase + ra[term], RW_D, kk),
+                         tc::kmaj_desc(sbase + kb3[term], RW_D, kk), id64, (term | kk) != 0);
+          tc::mma_bf16(tm + K_D1, tc::kmaj_desc(sbase + sa[term], RW_D, kk),
+                       tc::kmaj_desc(sbase + rb[term], RW_D, kk), id64, (term | kk) != 0);
+        }
+      tc::mma_commit(bar1);
+    }
+    // the bonus sums c_j, in a fixed order
+    if (tid < 2 * TC_C) {
+      const float* p = Cbp + tid * 8;
+      Cb[tid] = ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
+    }
+    auto put_a = [&](int row, int s, float av) {   // A's bf16 terms, row 32 e + j, column s
+      const uint32_t hv = bf16x2(av, 0.f) & 0xffffu;
+      const uint32_t lv = bf16x2(av - __uint_as_float(hv << 16), 0.f) & 0xffffu;
+      const uint32_t off = tc::kmaj_off(row, s, TC_C);
+      *reinterpret_cast<uint16_t*>(sm + RwSmem::AHI + off) = (uint16_t)hv;
+      *reinterpret_cast<uint16_t*>(sm + RwSmem::ALO + off) = (uint16_t)lv;
+    };
+    if (direct) {
+      // strong decay: every pair (j, s < j) of both slot-heads directly,
+      // e^{Λ_{j-1}[c]-Λ_s[c]} per channel, with r and k read back from global
+      // memory (pairs tid + 256 p)
+      for (int pr = tid; pr < 2 * TC_C * TC_C; pr += TC_THREADS) {
+        const int hd = pr >> 10, j = (pr >> 5) & 31, s = pr & 31;
+        float av = 0.f;
+        if (s < j && j < Cc && (hd == 0 || two)) {
+          const uint16_t* rj = r_in + ((size_t)(t0 + j) * nH + sh0 + hd) * RW_D;
+          const uint16_t* ks = k_in + ((size_t)(t0 + s) * nH + sh0 + hd) * RW_D;
+          for (int c = 0; c < RW_D; ++c) {
+            const int col = RW_D * hd + c;
+            av += bf16f(rj[c]) * bf16f(ks[c]) *
+                  __expf(Lp[(j - 1) * RW_LP + col] - Lp[s * RW_LP + col]);
+          }
+        }
+        put_a(TC_C * hd + j, s, av);
+      }
+    }
+    if (t0 + TC_C < T) {
+      const int Cn = (T - t0 - TC_C) < TC_C ? (T - t0 - TC_C) : TC_C;
+      st.load(r_in, k_in, v_in, g, t0 + TC_C, Cn, (size_t)nH, sh0, two, tid);
+    }
+    if (tid == 0 && !mbar_wait(bar1, par, status, DEV_TIMEOUT_MMA)) *ok_flag = -1;
+    __syncthreads();
+    if (*ok_flag != 1) {
+      ok = false;
+      break;
+    }
+    tc::fence_after_sync();
+    // ---- fast chunks: A from D0 (warps with q4 = e < 2 read rows 32 e + j, the
+    //      columns 32 e + 16 hw .. +15 of their slot-head's block), live below
+    //      the diagonal
+    if (!direct && q4 < 2) {
+      uint32_t x[16];
+      tc::tmem_ld16(tlane + K_D0 + 32 * q4 + 16 * hw, x);
+      tc::tmem_wait_ld16(x);
+      const int j = lane, s0 = 16 * hw;
+      float w[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) w[e] = (s0 + e < j && j < Cc) ? __uint_as_float(x[e]) : 0.f;
+#pragma unroll
+      for (int c8 = 0; c8 < 2; ++c8) {
+        uint4 hv, lv;
+        split8(w + 8 * c8, hv, lv);
+        const uint32_t off = tc::kmaj_off(TC_C * q4 + j, s0 + 8 * c8, TC_C);
+        *reinterpret_cast<uint4*>(sm + RwSmem::AHI + off) = hv;
+        *reinterpret_cast<uint4*>(sm + RwSmem::ALO + off) = lv;
+      }
+    }
+    tc::fence_smem_to_async();   // A terms, for the tensor cores
+    tc::fence_before_sync();
+    __syncthreads();
+    // ---- D3 = V A^T and D2 = V k̃, two terms each (V is exact in bf16)
+    if (tid == 0) {
+      tc::fence_after_sync();
+      constexpr uint32_t id3 = tc::idesc_bf16_f32(128, 64), id2 = tc::idesc_bf16_f32(128, 128);
+      const uint32_t ab[2] = {RwSmem::AHI, RwSmem::ALO};
+      const uint32_t kb2[2] = {RwSmem::KTHI, RwSmem::KTLO};
+#pragma unroll
+      for (int term = 0; term < 2; ++term)
+#pragma unroll
+        for (int kk = 0; kk < TC_C / 16; ++kk) {
+          tc::mma_bf16(tm + K_D3, tc::kmaj_desc(sbase + RwSmem::VO, TC_C, kk),
+                       tc::kmaj_desc(sbase + ab[term], TC_C, kk), id3, (term | kk) != 0);
+          tc::mma_bf16(tm + K_D2, tc::kmaj_desc(sbase + RwSmem::VO, TC_C, kk),
+                       tc::kmaj_desc(sbase + kb2[term], TC_C, kk), id2, (term | kk) != 0);
+        }
+      tc::mma_commit(bar2);
+    }
+    if (tid == 0 && !mbar_wait(bar2, par, status, DEV_TIMEOUT_MMA)) *ok_flag = -2;
+    __syncthreads();
+    if (*ok_flag != 1) {
+      ok = false;
+      break;
+    }
+    tc::fence_after_sync();
+    // ---- outputs of tokens 16 hw .. 16 hw + 15 of row r:
+    //      o_j = scale (S̄ r̂_j + D3 + c_j v_j), from slot-head he's columns 32 he + j
+    if (o != nullptr && mine) {
+      uint32_t x1[16], x3[16];
+      tc::tmem_ld16(tlane + K_D1 + 32 * he + 16 * hw, x1);
+      tc::tmem_ld16(tlane + K_D3 + 32 * he + 16 * hw, x3);
+      const uint4 va = *reinterpret_cast<const uint4*>(sm + RwSmem::VO + tc::kmaj_off(r, 16 * hw, TC_C));
+      const uint4 vb = *reinterpret_cast<const uint4*>(sm + RwSmem::VO + tc::kmaj_off(r, 16 * hw + 8, TC_C));
+      float vj[16];
+      {
+        float t8[8];
+        unpack8(va, t8);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) vj[e] = t8[e];
+        unpack8(vb, t8);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) vj[8 + e] = t8[e];
+      }
+      tc::tmem_wait_ld16(x1);
+      tc::tmem_wait_ld16(x3);
+      const float* cbh = Cb + TC_C * he + 16 * hw;
+      const size_t ostride = (size_t)nH * RW_D;
+      const size_t obase = ((size_t)(t0 + 16 * hw) * nH + she) * RW_D + vrow;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        if (16 * hw + e < Cc) {
+          const float yo =
+              scale * ((__uint_as_float(x1[e]) + __uint_as_float(x3[e])) + cbh[e] * vj[e]);
+          const size_t oi = obase + (size_t)e * ostride;
+          if (out_bf16) static_cast<uint16_t*>(o)[oi] = f2bf16(yo);
+          else static_cast<float*>(o)[oi] = yo;
+        }
+      }
+    }
+    // ---- S̄ <- S̄ Diag(e^{Λ_C}) + D2 (slot-head he's columns 64 he + c); its
+    //      bf16 terms for the next chunk
+    {
+      uint32_t x[32];
+      tc::tmem_ld32(tlane + K_D2 + 64 * he + 32 * hw, x);
+      tc::tmem_wait_ld(x);
+      const float* ec = Ec + 64 * he + 32 * hw;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) S[c] = ec[c] * S[c] + __uint_as_float(x[c]);
+#pragma unroll
+      for (int c8 = 0; c8 < 4; ++c8) {
+        uint4 hv, lv;
+        split8(S + 8 * c8, hv, lv);
+        const uint32_t off = tc::kmaj_off(r, 32 * hw + 8 * c8, RW_D);
+        *reinterpret_cast<uint4*>(sm + RwSmem::SHI + off) = hv;
+        *reinterpret_cast<uint4*>(sm + RwSmem::SLO + off) = lv;
+      }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+  }
+  if (!ok && tid == 0) mbar_drain(*ok_flag == -1 ? bar1 : bar2, (uint32_t)chunk & 1u);
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tm, RW_COLS);
+  }
+  if (!ok || !mine) return;
+  float4* dst = reinterpret_cast<float4*>(state_of(she) + (size_t)vrow * RW_D + 32 * hw);
+#pragma unroll
+  for (int c4 = 0; c4 < 8; ++c4)
+    dst[c4] = make_float4(S[4 * c4], S[4 * c4 + 1], S[4 * c4 + 2], S[4 * c4 + 3]);
+  if (tid == 0 || (tid == 64 && two)) {   // each slot's table entry, from its head 0
+    const int row = she / a.H;
+    if (she - row * a.H == 0) {
+      const int slot = a.items[row].slot;
+      a.nlog[slot] = 0;
+      a.base_of[slot] = slot;
+    }
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_prefill_gdn_tc(const SlotListArgs& a, const void* q, const void* k,
@@ -1003,6 +1436,21 @@ cudaError_t launch_prefill_kda_tc(const SlotListArgs& a, const void* q, const vo
   prefill_kda_tc_kernel<<<a.rows * a.H, TC_THREADS, KdaSmem::BYTES, s>>>(
       a, static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(k),
       static_cast<const uint16_t*>(v), g, beta, o, T, out_bf16, scale, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_rwkv6_tc(const SlotListArgs& a, const void* r, const void* k,
+                                    const void* v, const float* g, const float* bonus, void* o,
+                                    int T, int out_bf16, float scale, int32_t* status,
+                                    cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(prefill_rwkv6_tc_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)RwSmem::BYTES);
+  if (e != cudaSuccess) return e;
+  const int nH = a.rows * a.H;
+  prefill_rwkv6_tc_kernel<<<(nH + 1) / 2, TC_THREADS, RwSmem::BYTES, s>>>(
+      a, static_cast<const uint16_t*>(r), static_cast<const uint16_t*>(k),
+      static_cast<const uint16_t*>(v), g, bonus, o, T, out_bf16, scale, status);
   return cudaGetLastError();
 }
 

@@ -58,33 +58,71 @@ def test_long_prefill_matches_oracle(op, d, T):
 
 
 @pytest.mark.parametrize("strong", ["all", "mixed"])
-def test_kda_prefill_strong_decay_matches_oracle(strong):
-    """KDA's pair coefficients factor through the chunk start while a chunk's
-    total log-decay stays above -60 in every channel; a chunk with stronger
-    decay takes the direct path (one exponential per channel and pair).  Here
-    the log-decays are scaled up (about -2.8 a token: -90 over a chunk) for
-    every token, or for the tokens of every other chunk only, so that both
-    paths run and alternate; the result must still match the oracle."""
+@pytest.mark.parametrize("op,d,gain", [(gen.KDA, 128, 40.0), (gen.RWKV6, 64, 4.0)])
+def test_prefill_strong_decay_matches_oracle(op, d, gain, strong):
+    """The tensor-core kernels of the per-key ops factor their pair
+    coefficients through the chunk start while a chunk's total log-decay stays
+    above -60 in every channel; a chunk with stronger decay takes the direct
+    path (one exponential per channel and pair).  Here the log-decays are
+    scaled up (to about -2.8 a token: -90 over a chunk) for every token, or for
+    the tokens of every other chunk only, so that both paths run and
+    alternate; the result must still match the oracle."""
     from linear_attention_recurrent_gdn_gb300 import deltalog as dl
-    B, H, d, M, T = 2, 4, 128, 16, 160
-    x, S0, _ = make_case(gen.KDA, B, H, d, T, seed=5300 + len(strong))
+    B, H, M, T = 2, 4, 16, 160
+    x, S0, bonus = make_case(op, B, H, d, T, seed=5300 + len(strong) + 11 * op)
     g = x["g"].clone()
     if strong == "all":
-        g *= 40.0
+        g *= gain
     else:
         for c0 in range(0, T, 64):
-            g[c0:c0 + 32] *= 40.0
+            g[c0:c0 + 32] *= gain
     x["g"] = g.contiguous()
-    o_ref, S_ref, _ = oracle_run(gen.KDA, x, S0, None)
-    ctx = dl.DeltaLog(gen.KDA, B, H, d, d, M, out_bf16=False)
+    o_ref, S_ref, _ = oracle_run(op, x, S0, bonus)
+    ctx = dl.DeltaLog(op, B, H, d, d, M, out_bf16=False)
     slots = list(range(B))
     ctx.set_state(slots, S0.cuda())
+    if bonus is not None:
+        ctx.set_bonus(bonus.cuda())
     dev = {k_: (v_.cuda() if v_ is not None else None) for k_, v_ in x.items()}
     o = ctx.prefill(slots, dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"])
     S = ctx.read_state(slots).cpu().reshape(B * H, d, d).numpy()
     ctx.close()
     assert max_step_rel(o.float().cpu().reshape(T, B * H, d).numpy(), o_ref) <= 1e-4
     assert rel_err(S, S_ref) <= STATE_TOL
+
+
+@pytest.mark.parametrize("T", [33, 97])
+@pytest.mark.parametrize("B,H", [(3, 3), (1, 1), (2, 4)])
+def test_rwkv6_tensor_core_prefill_slot_head_pairs(B, H, T):
+    """RWKV6's tensor-core prefill takes two slot-heads per CTA (flattened
+    slot-heads 2b and 2b + 1, which may belong to different slots); with an odd
+    count the last CTA holds one.  Ragged and full chunk counts, fp32 outputs,
+    then decode steps from the prefilled state: every output and the state
+    match the oracle, and each slot's table entry is reset."""
+    from linear_attention_recurrent_gdn_gb300 import deltalog as dl
+    d, M, Td = 64, 8, 5
+    x, S0, bonus = make_case(gen.RWKV6, B, H, d, T + Td, seed=5500 + 13 * B + 7 * H + T)
+    o_ref, S_ref, S_snap = oracle_run(gen.RWKV6, x, S0, bonus, snap=[T - 1])
+    ctx = dl.DeltaLog(gen.RWKV6, B, H, d, d, M, out_bf16=False)
+    slots = list(range(B))
+    ctx.set_state(slots, S0.cuda())
+    ctx.set_bonus(bonus.cuda())
+    dev = {k_: (v_.cuda() if v_ is not None else None) for k_, v_ in x.items()}
+    sl = lambda key: dev[key][:T].contiguous() if dev[key] is not None else None
+    o_pf = ctx.prefill(slots, sl("q"), sl("k"), sl("v"), sl("g"), None)
+    S_pf = ctx.read_state(slots).cpu().reshape(B * H, d, d).numpy()
+    assert rel_err(S_pf, S_snap[0]) <= STATE_TOL
+    assert max_step_rel(o_pf.cpu().reshape(T, B * H, d).numpy(), o_ref[:T]) <= 1e-4
+    n, base_of = ctx.get_meta()
+    assert list(n) == [0] * B and list(base_of) == slots
+    outs = []
+    for t in range(T, T + Td):
+        outs.append(ctx.step(slots, dev["q"][t], dev["k"][t], dev["v"][t], dev["g"][t], None).float())
+    o = torch.stack(outs).cpu().reshape(Td, B * H, d).numpy()
+    assert max_step_rel(o, o_ref[T:]) <= 1e-4
+    S = ctx.read_state(slots).cpu().reshape(B * H, d, d).numpy()
+    assert rel_err(S, S_ref) <= STATE_TOL
+    ctx.close()
 
 
 @pytest.mark.parametrize("T", [33, 64, 97, 130])
