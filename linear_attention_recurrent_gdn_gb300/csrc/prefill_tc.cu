@@ -1001,7 +1001,7 @@ prefill_kda_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* __
 // as in KDA's kernel; a chunk below it forms A directly on the CUDA cores.
 constexpr int RW_D = 64;
 constexpr uint32_t RW_COLS = 512;   // TMEM: D0 [0, 64), D1 [64, 128), D3 [128, 192), D2 [256, 384)
-constexpr int RW_LP = 2 * RW_D + 4;   // fp32 Λ rows: 128 columns (64 e + c), padded
+constexpr int RW_LT = TC_C + 1;   // fp32 Λ, channel-major: column 64 e + c at col * RW_LT, token j at + j
 
 struct RwSmem {
   static constexpr uint32_t SHI = 0;                          // S̄ hi [128 x 64] K-major
@@ -1015,8 +1015,11 @@ struct RwSmem {
   static constexpr uint32_t VO = KTLO + 128 * TC_C * 2;       // V [128 rows (64 e + v)] x [32 tokens]
   static constexpr uint32_t AHI = VO + 128 * TC_C * 2;        // A [64 rows (32 e + j)] x [32 (s)]
   static constexpr uint32_t ALO = AHI + 64 * TC_C * 2;
-  static constexpr uint32_t LP = ALO + 64 * TC_C * 2;         // g, then Λ_j, fp32 [32][RW_LP]
-  static constexpr uint32_t EC = LP + TC_C * RW_LP * 4;       // e^{Λ_C} [128]
+  static constexpr uint32_t LP = ALO + 64 * TC_C * 2;         // g, then Λ_j, fp32 [128][RW_LT]
+  static constexpr uint32_t ER = LP + 128 * RW_LT * 4;        // e^{Λ_{j-1}}, same layout
+  static constexpr uint32_t EB = ER + 128 * RW_LT * 4;        // e^{-Λ_j}, same layout
+  static constexpr uint32_t HT = EB + 128 * RW_LT * 4;        // Λ_15 of each column [128]
+  static constexpr uint32_t EC = HT + 128 * 4;                // e^{Λ_C} [128]
   static constexpr uint32_t UB = EC + 128 * 4;                // bonus u of both heads [128]
   static constexpr uint32_t CBP = UB + 128 * 4;               // c_j partials [2][32][8]
   static constexpr uint32_t CB = CBP + 2 * TC_C * 8 * 4;      // c_j [2][32]
@@ -1060,15 +1063,51 @@ struct RwStage {
     }
   }
 
+  // g channel-major (column 64 e + c, token j at column * RW_LT + j).  Lane
+  // group (lane / 8) of a warp starts at component lane / 8 of its quad, so
+  // that each store's 32 lanes reach 32 distinct banks.
   __device__ __forceinline__ void store_g(unsigned char* sm, int tid) const {
     float* Lp = reinterpret_cast<float*>(sm + RwSmem::LP);
+    const int rot = (tid >> 3) & 3;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int idx = tid + e * TC_THREADS, j = idx >> 5, c4 = idx & 31;
-      *reinterpret_cast<float4*>(Lp + j * RW_LP + 4 * c4) = gv[e];
+      float x0 = gv[e].x, x1 = gv[e].y, x2 = gv[e].z, x3 = gv[e].w;   // rotated by rot
+      if (rot & 1) {
+        const float t = x0;
+        x0 = x1; x1 = x2; x2 = x3; x3 = t;
+      }
+      if (rot & 2) {
+        float t = x0;
+        x0 = x2; x2 = t;
+        t = x1;
+        x1 = x3; x3 = t;
+      }
+      float* col = Lp + 4 * c4 * RW_LT + j;
+      col[((0 + rot) & 3) * RW_LT] = x0;
+      col[((1 + rot) & 3) * RW_LT] = x1;
+      col[((2 + rot) & 3) * RW_LT] = x2;
+      col[((3 + rot) & 3) * RW_LT] = x3;
     }
   }
 };
+
+// The four 32-bit words of a piece rotated by `rot` (word i <- word i + rot,
+// mod 4), so that element t of the result is element t + 2 rot (mod 8).
+__device__ __forceinline__ uint4 rot_words(const uint4 w, int rot) {
+  uint32_t a0 = w.x, a1 = w.y, a2 = w.z, a3 = w.w;
+  if (rot & 1) {
+    const uint32_t t = a0;
+    a0 = a1; a1 = a2; a2 = a3; a3 = t;
+  }
+  if (rot & 2) {
+    uint32_t t = a0;
+    a0 = a2; a2 = t;
+    t = a1;
+    a1 = a3; a3 = t;
+  }
+  return make_uint4(a0, a1, a2, a3);
+}
 
 // A bf16 value of piece word w (element t of 8) as its 16 bits.
 __device__ __forceinline__ uint16_t piece_bits(const uint4 w, int t) {
@@ -1083,6 +1122,9 @@ prefill_rwkv6_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* 
                         int out_bf16, float scale, int32_t* status) {
   extern __shared__ __align__(1024) unsigned char sm[];
   float* Lp = reinterpret_cast<float*>(sm + RwSmem::LP);
+  float* Er = reinterpret_cast<float*>(sm + RwSmem::ER);
+  float* Eb = reinterpret_cast<float*>(sm + RwSmem::EB);
+  float* Ht = reinterpret_cast<float*>(sm + RwSmem::HT);
   float* Ec = reinterpret_cast<float*>(sm + RwSmem::EC);
   float* Ub = reinterpret_cast<float*>(sm + RwSmem::UB);
   float* Cbp = reinterpret_cast<float*>(sm + RwSmem::CBP);
@@ -1164,21 +1206,47 @@ prefill_rwkv6_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* 
     // ---- stage g; Λ = inclusive scan of g down each of the 128 columns (64 e + c;
     //      padding tokens and a missing second slot-head have g = 0); the vote:
     //      does every column's chunk log-decay stay above the floor?
+    //      Thread (half hf, column cl) scans tokens 16 hf .. 16 hf + 15 of its
+    //      column, the second half then adds the first half's total, and each
+    //      thread forms its tokens' decay factors e^{Λ_{j-1}} (for r̂) and
+    //      e^{-Λ_j} (for k̄ and k̃; only used while the vote passes).
     st.store_g(sm, tid);
     __syncthreads();
     float lc = 0.f;
-    if (tid < 128) {
-#pragma unroll 8
-      for (int j = 0; j < TC_C; ++j) {
-        lc += Lp[j * RW_LP + tid];
-        Lp[j * RW_LP + tid] = lc;
+    {
+      const int cl = tid & 127, hf = tid >> 7;
+      float* col = Lp + cl * RW_LT + 16 * hf;
+      float lam[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        lc += col[j];
+        lam[j] = lc;
       }
-      Ec[tid] = expf(lc);
+      if (hf == 0) Ht[cl] = lc;
+      __syncthreads();
+      const float pre = hf ? Ht[cl] : 0.f;   // Λ at the half's first token minus one
+      float* er = Er + cl * RW_LT + 16 * hf;
+      float* eb = Eb + cl * RW_LT + 16 * hf;
+      float prev = pre;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float l = pre + lam[j];
+        col[j] = l;
+        er[j] = __expf(prev);   // Λ_{j-1} <= 0
+        eb[j] = __expf(-l);     // <= e^{60} while the vote passes
+        prev = l;
+      }
+      lc = pre + lc;            // Λ_C for the second half's threads
+      if (hf) Ec[cl] = expf(lc);
     }
-    const bool direct = __syncthreads_or(tid < 128 && !(lc >= KDA_FACTOR_FLOOR)) != 0;
+    const bool direct = __syncthreads_or(tid >= 128 && !(lc >= KDA_FACTOR_FLOOR)) != 0;
     // ---- operands, 8 channels of one token of one slot-head per piece (r, k, v
     //      from registers): r̂ and k̄ (hi, lo) as token rows; k̃ (hi, lo) and V
-    //      transposed, as channel and value rows; the bonus sums' partials
+    //      transposed, as channel and value rows; the bonus sums' partials.  A
+    //      transposed row's bank depends only on its channel within the piece and
+    //      the token's low bits, so the four lane groups of a warp (pieces cv ..
+    //      cv + 3) store channels t + 2 g (mod 8) at step t: 16 distinct banks.
+    const int rot = (tid >> 3) & 3;   // lane group g of the warp
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       int j, cv;
@@ -1191,14 +1259,13 @@ prefill_rwkv6_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* 
 #pragma unroll
       for (int t = 0; t < 8; ++t) {
         const int col = col0 + t;
-        const float lj = Lp[j * RW_LP + col];
-        const float lprev = j > 0 ? Lp[(j - 1) * RW_LP + col] : 0.f;
-        rh[t] = __expf(lprev) * rx[t];                                 // Λ_{j-1} <= 0
+        const int cj = col * RW_LT + j;
+        rh[t] = Er[cj] * rx[t];
         if (direct) {
           kb[t] = 0.f;
-          kt[t] = j < Cc ? __expf(Lp[(TC_C - 1) * RW_LP + col] - lj) * kx[t] : 0.f;   // Λ_C - Λ_j <= 0
+          kt[t] = j < Cc ? __expf(Lp[col * RW_LT + TC_C - 1] - Lp[cj]) * kx[t] : 0.f;   // <= 0
         } else {
-          const float eb = __expf(-lj);                                // <= e^{60}
+          const float eb = Eb[cj];                                     // <= e^{60}
           kb[t] = eb * kx[t];
           kt[t] = j < Cc ? fminf(Ec[col] * eb, 1.f) * kx[t] : 0.f;
         }
@@ -1214,12 +1281,14 @@ prefill_rwkv6_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* 
       *reinterpret_cast<uint4*>(sm + RwSmem::KBHI + otok) = hv;
       *reinterpret_cast<uint4*>(sm + RwSmem::KBLO + otok) = lv;
       split8(kt, hv, lv);
+      const uint4 kh = rot_words(hv, rot), kl = rot_words(lv, rot), vv = rot_words(st.v[e], rot);
+      const uint32_t ocol = tc::kmaj_off(col0, j, TC_C);   // + 16 per channel row
 #pragma unroll
-      for (int t = 0; t < 8; ++t) {   // k̃_j[c] and v_j[c] at row 64 hd + c, column j
-        const uint32_t off = tc::kmaj_off(col0 + t, j, TC_C);
-        *reinterpret_cast<uint16_t*>(sm + RwSmem::KTHI + off) = piece_bits(hv, t);
-        *reinterpret_cast<uint16_t*>(sm + RwSmem::KTLO + off) = piece_bits(lv, t);
-        *reinterpret_cast<uint16_t*>(sm + RwSmem::VO + off) = piece_bits(st.v[e], t);
+      for (int t = 0; t < 8; ++t) {   // channel col0 + t' of token j, t' = t + 2 rot (mod 8)
+        const uint32_t off = ocol + (uint32_t)(((t + 2 * rot) & 7) * 16);
+        *reinterpret_cast<uint16_t*>(sm + RwSmem::KTHI + off) = piece_bits(kh, t);
+        *reinterpret_cast<uint16_t*>(sm + RwSmem::KTLO + off) = piece_bits(kl, t);
+        *reinterpret_cast<uint16_t*>(sm + RwSmem::VO + off) = piece_bits(vv, t);
       }
     }
     tc::fence_smem_to_async();   // S̄ terms and the chunk's operands, for the tensor cores
@@ -1269,8 +1338,7 @@ prefill_rwkv6_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* 
           const uint16_t* ks = k_in + ((size_t)(t0 + s) * nH + sh0 + hd) * RW_D;
           for (int c = 0; c < RW_D; ++c) {
             const int col = RW_D * hd + c;
-            av += bf16f(rj[c]) * bf16f(ks[c]) *
-                  __expf(Lp[(j - 1) * RW_LP + col] - Lp[s * RW_LP + col]);
+            av += bf16f(rj[c]) * bf16f(ks[c]) * __expf(Lp[col * RW_LT + j - 1] - Lp[col * RW_LT + s]);
           }
         }
         put_a(TC_C * hd + j, s, av);
