@@ -1255,6 +1255,13 @@ prefill_rwkv6_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* 
       float rx[8], kx[8], rh[8], kb[8], kt[8];
       unpack8(st.r[e], rx);
       unpack8(st.k[e], kx);
+      // e^{Λ_C} and the bonus u of the piece's 8 columns (two 16-byte loads each)
+      const float4 e0 = *reinterpret_cast<const float4*>(Ec + col0);
+      const float4 e1 = *reinterpret_cast<const float4*>(Ec + col0 + 4);
+      const float4 u0 = *reinterpret_cast<const float4*>(Ub + col0);
+      const float4 u1 = *reinterpret_cast<const float4*>(Ub + col0 + 4);
+      const float ec8[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+      const float ub8[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
       float cb = 0.f;
 #pragma unroll
       for (int t = 0; t < 8; ++t) {
@@ -1267,9 +1274,9 @@ prefill_rwkv6_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* 
         } else {
           const float eb = Eb[cj];                                     // <= e^{60}
           kb[t] = eb * kx[t];
-          kt[t] = j < Cc ? fminf(Ec[col] * eb, 1.f) * kx[t] : 0.f;
+          kt[t] = j < Cc ? fminf(ec8[t] * eb, 1.f) * kx[t] : 0.f;
         }
-        cb += rx[t] * Ub[col] * kx[t];
+        cb += rx[t] * ub8[t] * kx[t];
       }
       Cbp[(hd * TC_C + j) * 8 + (cv & 7)] = cb;
       uint4 hv, lv;
@@ -1402,45 +1409,18 @@ prefill_rwkv6_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* 
       break;
     }
     tc::fence_after_sync();
-    // ---- outputs of tokens 16 hw .. 16 hw + 15 of row r:
-    //      o_j = scale (S̄ r̂_j + D3 + c_j v_j), from slot-head he's columns 32 he + j
-    if (o != nullptr && mine) {
-      uint32_t x1[16], x3[16];
-      tc::tmem_ld16(tlane + K_D1 + 32 * he + 16 * hw, x1);
-      tc::tmem_ld16(tlane + K_D3 + 32 * he + 16 * hw, x3);
-      const uint4 va = *reinterpret_cast<const uint4*>(sm + RwSmem::VO + tc::kmaj_off(r, 16 * hw, TC_C));
-      const uint4 vb = *reinterpret_cast<const uint4*>(sm + RwSmem::VO + tc::kmaj_off(r, 16 * hw + 8, TC_C));
-      float vj[16];
-      {
-        float t8[8];
-        unpack8(va, t8);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) vj[e] = t8[e];
-        unpack8(vb, t8);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) vj[8 + e] = t8[e];
-      }
-      tc::tmem_wait_ld16(x1);
-      tc::tmem_wait_ld16(x3);
-      const float* cbh = Cb + TC_C * he + 16 * hw;
-      const size_t ostride = (size_t)nH * RW_D;
-      const size_t obase = ((size_t)(t0 + 16 * hw) * nH + she) * RW_D + vrow;
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        if (16 * hw + e < Cc) {
-          const float yo =
-              scale * ((__uint_as_float(x1[e]) + __uint_as_float(x3[e])) + cbh[e] * vj[e]);
-          const size_t oi = obase + (size_t)e * ostride;
-          if (out_bf16) static_cast<uint16_t*>(o)[oi] = f2bf16(yo);
-          else static_cast<float*>(o)[oi] = yo;
-        }
-      }
-    }
-    // ---- S̄ <- S̄ Diag(e^{Λ_C}) + D2 (slot-head he's columns 64 he + c); its
-    //      bf16 terms for the next chunk
+    // ---- S̄ <- S̄ Diag(e^{Λ_C}) + D2 (slot-head he's columns 64 he + c) and its
+    //      bf16 terms for the next chunk; the outputs of tokens 16 hw .. 16 hw + 15
+    //      of row r, o_j = scale (S̄ r̂_j + D3 + c_j v_j), from columns 32 he + j.
+    //      The three tensor-memory loads go out together.
     {
-      uint32_t x[32];
+      const bool outs = o != nullptr && mine;   // uniform over the warp
+      uint32_t x[32], x1[16], x3[16];
       tc::tmem_ld32(tlane + K_D2 + 64 * he + 32 * hw, x);
+      if (outs) {
+        tc::tmem_ld16(tlane + K_D1 + 32 * he + 16 * hw, x1);
+        tc::tmem_ld16(tlane + K_D3 + 32 * he + 16 * hw, x3);
+      }
       tc::tmem_wait_ld(x);
       const float* ec = Ec + 64 * he + 32 * hw;
 #pragma unroll
@@ -1452,6 +1432,35 @@ prefill_rwkv6_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* 
         const uint32_t off = tc::kmaj_off(r, 32 * hw + 8 * c8, RW_D);
         *reinterpret_cast<uint4*>(sm + RwSmem::SHI + off) = hv;
         *reinterpret_cast<uint4*>(sm + RwSmem::SLO + off) = lv;
+      }
+      if (outs) {
+        const uint4 va = *reinterpret_cast<const uint4*>(sm + RwSmem::VO + tc::kmaj_off(r, 16 * hw, TC_C));
+        const uint4 vb = *reinterpret_cast<const uint4*>(sm + RwSmem::VO + tc::kmaj_off(r, 16 * hw + 8, TC_C));
+        float vj[16];
+        {
+          float t8[8];
+          unpack8(va, t8);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) vj[e] = t8[e];
+          unpack8(vb, t8);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) vj[8 + e] = t8[e];
+        }
+        tc::tmem_wait_ld16(x1);   // (complete already: the wait above covers every load)
+        tc::tmem_wait_ld16(x3);
+        const float* cbh = Cb + TC_C * he + 16 * hw;
+        const size_t ostride = (size_t)nH * RW_D;
+        const size_t obase = ((size_t)(t0 + 16 * hw) * nH + she) * RW_D + vrow;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          if (16 * hw + e < Cc) {
+            const float yo =
+                scale * ((__uint_as_float(x1[e]) + __uint_as_float(x3[e])) + cbh[e] * vj[e]);
+            const size_t oi = obase + (size_t)e * ostride;
+            if (out_bf16) static_cast<uint16_t*>(o)[oi] = f2bf16(yo);
+            else static_cast<float*>(o)[oi] = yo;
+          }
+        }
       }
     }
     tc::fence_before_sync();
