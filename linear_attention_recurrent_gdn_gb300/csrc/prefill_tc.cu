@@ -103,6 +103,29 @@ __device__ __forceinline__ void chunk_piece(int idx, int& j, int& cv) {
   cv = ((idx >> 3) & 3) + 4 * (rest >> 2);
 }
 
+// The four 32-bit words of a piece rotated by `rot` (word i <- word i + rot,
+// mod 4), so that element t of the result is element t + 2 rot (mod 8).
+__device__ __forceinline__ uint4 rot_words(const uint4 w, int rot) {
+  uint32_t a0 = w.x, a1 = w.y, a2 = w.z, a3 = w.w;
+  if (rot & 1) {
+    const uint32_t t = a0;
+    a0 = a1; a1 = a2; a2 = a3; a3 = t;
+  }
+  if (rot & 2) {
+    uint32_t t = a0;
+    a0 = a2; a2 = t;
+    t = a1;
+    a1 = a3; a3 = t;
+  }
+  return make_uint4(a0, a1, a2, a3);
+}
+
+// A bf16 value of piece word w (element t of 8) as its 16 bits.
+__device__ __forceinline__ uint16_t piece_bits(const uint4 w, int t) {
+  const uint32_t x = (t >> 1) == 0 ? w.x : (t >> 1) == 1 ? w.y : (t >> 1) == 2 ? w.z : w.w;
+  return (uint16_t)((t & 1) ? (x >> 16) : (x & 0xffffu));
+}
+
 // One chunk's k, q, v (bf16) and g, β in the registers of the 128 threads that
 // prepare chunks, between their global loads and their shared-memory stores.
 struct TcStage {
@@ -154,12 +177,15 @@ struct TcStage {
       int j, cv;
       chunk_piece(ptid + e * 128, j, cv);
       *reinterpret_cast<uint4*>(sm + set + TcSmem::VS + (j * VP + cv * 8) * 2) = v[e];
-      const uint32_t w[4] = {k[e].x, k[e].y, k[e].z, k[e].w};
+      // k_j[i], i = 8 cv + t', at K^T row i, column j; lane group g of the warp
+      // stores t' = t + 2 g (mod 8) at step t, so each store reaches distinct banks
+      const int rot = (ptid >> 3) & 3;
+      const uint4 kr = rot_words(k[e], rot);
+      const uint32_t base = tc::kmaj_off(cv * 8, j, TC_C);
 #pragma unroll
-      for (int t = 0; t < 8; ++t) {   // k_j[i], i = 8 cv + t, at K^T row i, column j
-        const uint16_t x = (uint16_t)((t & 1) ? (w[t >> 1] >> 16) : (w[t >> 1] & 0xffffu));
-        *reinterpret_cast<uint16_t*>(sm + set + TcSmem::KT + tc::kmaj_off(cv * 8 + t, j, TC_C)) = x;
-      }
+      for (int t = 0; t < 8; ++t)
+        *reinterpret_cast<uint16_t*>(sm + set + TcSmem::KT + base + ((t + 2 * rot) & 7) * 16) =
+            piece_bits(kr, t);
     }
   }
 };
@@ -752,14 +778,15 @@ prefill_kda_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* __
       *reinterpret_cast<uint4*>(sm + KdaSmem::KBHI + okq) = hv;
       *reinterpret_cast<uint4*>(sm + KdaSmem::KBLO + okq) = lv;
       split8(kt, hv, lv);
-      const uint32_t hw4[4] = {hv.x, hv.y, hv.z, hv.w}, lw4[4] = {lv.x, lv.y, lv.z, lv.w};
+      // k̃_j[c] at row c = 8 cv + t', column j, t' = t + 2 g (mod 8) for lane group g
+      const int rot = (tid >> 3) & 3;
+      const uint4 th = rot_words(hv, rot), tl = rot_words(lv, rot);
+      const uint32_t base = tc::kmaj_off(cv * 8, j, TC_C);
 #pragma unroll
-      for (int t = 0; t < 8; ++t) {   // k̃_j[c] at row c, column j
-        const uint32_t off = tc::kmaj_off(cv * 8 + t, j, TC_C);
-        *reinterpret_cast<uint16_t*>(sm + KdaSmem::KTHI + off) =
-            (uint16_t)((t & 1) ? (hw4[t >> 1] >> 16) : (hw4[t >> 1] & 0xffffu));
-        *reinterpret_cast<uint16_t*>(sm + KdaSmem::KTLO + off) =
-            (uint16_t)((t & 1) ? (lw4[t >> 1] >> 16) : (lw4[t >> 1] & 0xffffu));
+      for (int t = 0; t < 8; ++t) {
+        const uint32_t off = base + ((t + 2 * rot) & 7) * 16;
+        *reinterpret_cast<uint16_t*>(sm + KdaSmem::KTHI + off) = piece_bits(th, t);
+        *reinterpret_cast<uint16_t*>(sm + KdaSmem::KTLO + off) = piece_bits(tl, t);
       }
     }
     tc::fence_smem_to_async();   // S̄ terms and the decayed operands, for the tensor cores
@@ -1091,29 +1118,6 @@ struct RwStage {
     }
   }
 };
-
-// The four 32-bit words of a piece rotated by `rot` (word i <- word i + rot,
-// mod 4), so that element t of the result is element t + 2 rot (mod 8).
-__device__ __forceinline__ uint4 rot_words(const uint4 w, int rot) {
-  uint32_t a0 = w.x, a1 = w.y, a2 = w.z, a3 = w.w;
-  if (rot & 1) {
-    const uint32_t t = a0;
-    a0 = a1; a1 = a2; a2 = a3; a3 = t;
-  }
-  if (rot & 2) {
-    uint32_t t = a0;
-    a0 = a2; a2 = t;
-    t = a1;
-    a1 = a3; a3 = t;
-  }
-  return make_uint4(a0, a1, a2, a3);
-}
-
-// A bf16 value of piece word w (element t of 8) as its 16 bits.
-__device__ __forceinline__ uint16_t piece_bits(const uint4 w, int t) {
-  const uint32_t x = (t >> 1) == 0 ? w.x : (t >> 1) == 1 ? w.y : (t >> 1) == 2 ? w.z : w.w;
-  return (uint16_t)((t & 1) ? (x >> 16) : (x & 0xffffu));
-}
 
 __global__ void __launch_bounds__(TC_THREADS, 1)
 prefill_rwkv6_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* __restrict__ r_in,
