@@ -773,11 +773,11 @@ def prefill_mma_flops(op, d, C=PREFILL_C):
     S̄[K;Q]^T in two terms (N=2C), D2 the rank-C rewrite in two terms (N=d, K=C),
     D3 the outputs' log terms in three (N=C, K=C); KDA the same with three terms
     each.  RWKV6 at d = 64 stacks two slot-heads in each M = 128 MMA and forms
-    both heads' blocks of every product: D0 [r̂;0]k̄^T and D1 S̄r̂^T in three terms
-    (N=2C, K=d), D3 VA^T in two (N=2C, K=C), D2 Vk̃ in two (N=2d, K=C), over 2C
+    both heads' blocks of every product: [r̂;0][k̄;S̄]^T in three terms (N=2C+2d,
+    K=d), [A;*]V^T in two (N=2d, K=C), D2 Vk̃ in two (N=2d, K=C), over 2C
     token·heads."""
     if op == 2:
-        mac = 3 * 128 * 2 * C * d * 2 + 2 * 128 * 2 * C * C + 2 * 128 * 2 * d * C
+        mac = 3 * 128 * (2 * C + 2 * d) * d + 2 * 128 * 2 * d * C + 2 * 128 * 2 * d * C
         return 2 * mac / (2 * C)
     terms = {0: (1, 2, 2, 3), 1: (3, 3, 3, 3)}[op]
     mac = (terms[0] * 128 * C * d + terms[1] * 128 * 2 * C * d + terms[2] * 128 * d * C

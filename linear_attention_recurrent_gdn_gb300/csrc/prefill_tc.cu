@@ -1018,28 +1018,32 @@ prefill_kda_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* __
 // head e sit at rows 64 e + v, its tokens at rows 32 e + j of the token-row
 // operands, its key channels at rows 64 e + c of k̃; each product is formed for
 // both heads at once and only head e's block of it is read:
-//   D0 [128 x 64]  = [r̂; 0] k̄^T    pair coefficients (rows 32 e + j, columns 32 e + s)
-//   D1 [128 x 64]  = S̄ r̂^T         rows 64 e + v, columns 32 e + j
-//   D3 [128 x 64]  = V A^T           the outputs' log terms, the same blocks
-//   D2 [128 x 128] = V k̃            rows 64 e + v, columns 64 e + c
-// S̄, r̂, k̄, k̃ and A are fp32, carried as hi + lo bf16 terms (three products
-// for S̄ r̂ and r̂ k̄, two with the exact bf16 V).  The factored pair products
+//   [D0 | Y] [128 x 192] = [r̂; 0] [k̄; S̄]^T, one N = 192 product:
+//       D0, columns 0-63: pair coefficients r̂_j·k̄_s (rows 32 e + j, columns 32 e + s);
+//       Y, columns 64-191: (S̄ r̂_j)[v] at row 32 e + j, column 64 + 64 e + v
+//   Y += A V^T                        the outputs' log terms, added onto Y
+//   D2 [128 x 128] = V k̃              rows 64 e + v, columns 64 e + c
+// (rows 64-127 of the first two pad the MMA's M and are not read).  S̄, r̂,
+// k̄, k̃ and A are fp32, carried as hi + lo bf16 terms (three products for
+// r̂ [k̄; S̄]^T, two with the exact bf16 V).  The factored pair products
 // stay finite while the chunk's log-decay stays above -60 in every channel,
 // as in KDA's kernel; a chunk below it forms A directly on the CUDA cores.
 constexpr int RW_D = 64;
-constexpr uint32_t RW_COLS = 512;   // TMEM: D0 [0, 64), D1 [64, 128), D3 [128, 192), D2 [256, 384)
+constexpr uint32_t RW_COLS = 512;   // TMEM: D0 [0, 64), Y [64, 192), D2 [256, 384)
 constexpr int RW_LT = TC_C + 1;   // fp32 Λ, channel-major: column 64 e + c at col * RW_LT, token j at + j
 
 struct RwSmem {
-  static constexpr uint32_t SHI = 0;                          // S̄ hi [128 x 64] K-major
-  static constexpr uint32_t SLO = SHI + 128 * RW_D * 2;
-  static constexpr uint32_t RHI = SLO + 128 * RW_D * 2;       // [r̂ (64 rows: 32 e + j); 0 (64)] x 64
+  // [k̄; S̄] hi and lo, the B operand of the N = 192 product: k̄ rows 32 e + s,
+  // then S̄ rows 64 e + v, each K-major over the 64 key channels
+  static constexpr uint32_t KSHI = 0;
+  static constexpr uint32_t KSLO = KSHI + (64 + 128) * RW_D * 2;
+  static constexpr uint32_t KBHI = KSHI, SHI = KSHI + 64 * RW_D * 2;
+  static constexpr uint32_t KBLO = KSLO, SLO = KSLO + 64 * RW_D * 2;
+  static constexpr uint32_t RHI = KSLO + (64 + 128) * RW_D * 2;   // [r̂ (64 rows: 32 e + j); 0 (64)] x 64
   static constexpr uint32_t RLO = RHI + 128 * RW_D * 2;
-  static constexpr uint32_t KBHI = RLO + 128 * RW_D * 2;      // k̄ [64 rows (32 e + s)] x 64
-  static constexpr uint32_t KBLO = KBHI + 64 * RW_D * 2;
-  static constexpr uint32_t KTHI = KBLO + 64 * RW_D * 2;      // k̃ [128 rows (64 e + c)] x [32 tokens]
+  static constexpr uint32_t KTHI = RLO + 128 * RW_D * 2;      // k̃ [128 rows (64 e + c)] x [32 tokens], MN-major
   static constexpr uint32_t KTLO = KTHI + 128 * TC_C * 2;
-  static constexpr uint32_t VO = KTLO + 128 * TC_C * 2;       // V [128 rows (64 e + v)] x [32 tokens]
+  static constexpr uint32_t VO = KTLO + 128 * TC_C * 2;       // V [128 rows (64 e + v)] x [32 tokens], MN-major
   static constexpr uint32_t AHI = VO + 128 * TC_C * 2;        // A [64 rows (32 e + j)] x [32 (s)]
   static constexpr uint32_t ALO = AHI + 64 * TC_C * 2;
   static constexpr uint32_t LP = ALO + 64 * TC_C * 2;         // g, then Λ_j, fp32 [128][RW_LT]
@@ -1055,6 +1059,11 @@ struct RwSmem {
 };
 static_assert(RwSmem::BYTES <= 227 * 1024, "shared memory");
 static_assert(RwSmem::LP % 16 == 0 && RwSmem::BAR % 16 == 0, "16-byte aligned buffers");
+// The pair-coefficient product reads A as an M = 128 operand: its rows 64-127
+// are the next 4 KB (ALO, then the start of LP), whatever they hold; the
+// product's rows 64-127 are never read.
+static_assert(RwSmem::ALO == RwSmem::AHI + 64 * TC_C * 2 && RwSmem::LP == RwSmem::ALO + 64 * TC_C * 2 &&
+              RwSmem::LP + 64 * TC_C * 2 <= RwSmem::BYTES, "A's padding rows stay inside the block");
 
 // One chunk's r, k, v (bf16) and g of the CTA's two slot-heads, in registers
 // between the global loads and the shared-memory stores.  The two slot-heads'
@@ -1137,7 +1146,7 @@ prefill_rwkv6_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* 
   int32_t* ok_flag = reinterpret_cast<int32_t*>(sm + RwSmem::BAR + 20);
   const uint32_t sbase = smem_u32(sm);
   const uint32_t bar1 = sbase + RwSmem::BAR, bar2 = sbase + RwSmem::BAR + 8;
-  constexpr uint32_t K_D0 = 0, K_D1 = 64, K_D3 = 128, K_D2 = 256;   // TMEM columns
+  constexpr uint32_t K_D0 = 0, K_Y = 64, K_D2 = 256;   // TMEM columns
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int q4 = warp & 3, hw = warp >> 2;
@@ -1148,6 +1157,7 @@ prefill_rwkv6_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* 
   const bool two = sh0 + 1 < nH;
   const int she = sh0 + he;
   const bool mine = he == 0 || two;      // this thread's row belongs to a slot-head of the batch
+  const bool ovec = (reinterpret_cast<uintptr_t>(o) & 15u) == 0;
   auto state_of = [&](int sh) {
     const int row = sh / a.H, h = sh - row * a.H;
     return a.Sbar + ((size_t)a.items[row].slot * a.H + h) * RW_D * RW_D;
@@ -1245,12 +1255,10 @@ prefill_rwkv6_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* 
     }
     const bool direct = __syncthreads_or(tid >= 128 && !(lc >= KDA_FACTOR_FLOOR)) != 0;
     // ---- operands, 8 channels of one token of one slot-head per piece (r, k, v
-    //      from registers): r̂ and k̄ (hi, lo) as token rows; k̃ (hi, lo) and V
-    //      transposed, as channel and value rows; the bonus sums' partials.  A
-    //      transposed row's bank depends only on its channel within the piece and
-    //      the token's low bits, so the four lane groups of a warp (pieces cv ..
-    //      cv + 3) store channels t + 2 g (mod 8) at step t: 16 distinct banks.
-    const int rot = (tid >> 3) & 3;   // lane group g of the warp
+    //      from registers), one 16-byte store each: r̂ and k̄ (hi, lo) K-major as
+    //      token rows; k̃ (hi, lo) and V MN-major, whose core-matrix rows are a
+    //      token's eight channels (eight lanes of a warp fill one core matrix);
+    //      the bonus sums' partials.
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       int j, cv;
@@ -1292,37 +1300,26 @@ prefill_rwkv6_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* 
       *reinterpret_cast<uint4*>(sm + RwSmem::KBHI + otok) = hv;
       *reinterpret_cast<uint4*>(sm + RwSmem::KBLO + otok) = lv;
       split8(kt, hv, lv);
-      const uint4 kh = rot_words(hv, rot), kl = rot_words(lv, rot), vv = rot_words(st.v[e], rot);
-      const uint32_t ocol = tc::kmaj_off(col0, j, TC_C);   // + 16 per channel row
-#pragma unroll
-      for (int t = 0; t < 8; ++t) {   // channel col0 + t' of token j, t' = t + 2 rot (mod 8)
-        const uint32_t off = ocol + (uint32_t)(((t + 2 * rot) & 7) * 16);
-        *reinterpret_cast<uint16_t*>(sm + RwSmem::KTHI + off) = piece_bits(kh, t);
-        *reinterpret_cast<uint16_t*>(sm + RwSmem::KTLO + off) = piece_bits(kl, t);
-        *reinterpret_cast<uint16_t*>(sm + RwSmem::VO + off) = piece_bits(vv, t);
-      }
+      const uint32_t ocol = tc::mnmaj_off(col0, j, TC_C);   // rows col0 .. col0 + 7 of token j
+      *reinterpret_cast<uint4*>(sm + RwSmem::KTHI + ocol) = hv;
+      *reinterpret_cast<uint4*>(sm + RwSmem::KTLO + ocol) = lv;
+      *reinterpret_cast<uint4*>(sm + RwSmem::VO + ocol) = st.v[e];
     }
     tc::fence_smem_to_async();   // S̄ terms and the chunk's operands, for the tensor cores
     tc::fence_before_sync();
     __syncthreads();
-    // ---- D0 = [r̂; 0] k̄^T (fast chunks) and D1 = S̄ r̂^T, three terms each
+    // ---- [D0 | Y] = [r̂; 0] [k̄; S̄]^T, three terms (a direct chunk's k̄ is zero)
     if (tid == 0) {
       tc::fence_after_sync();
-      constexpr uint32_t id64 = tc::idesc_bf16_f32(128, 64);
-      const uint32_t sa[3] = {RwSmem::SHI, RwSmem::SLO, RwSmem::SHI};
+      constexpr uint32_t id192 = tc::idesc_bf16_f32(128, 192);
       const uint32_t ra[3] = {RwSmem::RHI, RwSmem::RLO, RwSmem::RHI};
-      const uint32_t rb[3] = {RwSmem::RHI, RwSmem::RHI, RwSmem::RLO};
-      const uint32_t kb3[3] = {RwSmem::KBHI, RwSmem::KBHI, RwSmem::KBLO};
+      const uint32_t kb3[3] = {RwSmem::KSHI, RwSmem::KSHI, RwSmem::KSLO};
 #pragma unroll
       for (int term = 0; term < 3; ++term)
 #pragma unroll
-        for (int kk = 0; kk < RW_D / 16; ++kk) {
-          if (!direct)
-            tc::mma_bf16(tm + K_D0, tc::kmaj_desc(sbase + ra[term], RW_D, kk),
-                         tc::kmaj_desc(sbase + kb3[term], RW_D, kk), id64, (term | kk) != 0);
-          tc::mma_bf16(tm + K_D1, tc::kmaj_desc(sbase + sa[term], RW_D, kk),
-                       tc::kmaj_desc(sbase + rb[term], RW_D, kk), id64, (term | kk) != 0);
-        }
+        for (int kk = 0; kk < RW_D / 16; ++kk)
+          tc::mma_bf16(tm + K_D0, tc::kmaj_desc(sbase + ra[term], RW_D, kk),
+                       tc::kmaj_desc(sbase + kb3[term], RW_D, kk), id192, (term | kk) != 0);
       tc::mma_commit(bar1);
     }
     // the bonus sums c_j, in a fixed order
@@ -1389,18 +1386,19 @@ prefill_rwkv6_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* 
     tc::fence_smem_to_async();   // A terms, for the tensor cores
     tc::fence_before_sync();
     __syncthreads();
-    // ---- D3 = V A^T and D2 = V k̃, two terms each (V is exact in bf16)
+    // ---- Y += [A; *] V^T and D2 = V k̃, two terms each (V is exact in bf16)
     if (tid == 0) {
       tc::fence_after_sync();
-      constexpr uint32_t id3 = tc::idesc_bf16_f32(128, 64), id2 = tc::idesc_bf16_f32(128, 128);
+      constexpr uint32_t idy = tc::idesc_bf16_f32(128, 128, false, true);   // V MN-major
+      constexpr uint32_t id2 = tc::idesc_bf16_f32(128, 128, true, true);    // V, k̃ MN-major
       const uint32_t ab[2] = {RwSmem::AHI, RwSmem::ALO};
       const uint32_t kb2[2] = {RwSmem::KTHI, RwSmem::KTLO};
 #pragma unroll
       for (int term = 0; term < 2; ++term)
 #pragma unroll
         for (int kk = 0; kk < TC_C / 16; ++kk) {
-          tc::mma_bf16(tm + K_D3, tc::kmaj_desc(sbase + RwSmem::VO, TC_C, kk),
-                       tc::kmaj_desc(sbase + ab[term], TC_C, kk), id3, (term | kk) != 0);
+          tc::mma_bf16(tm + K_Y, tc::kmaj_desc(sbase + ab[term], TC_C, kk),
+                       tc::kmaj_desc(sbase + RwSmem::VO, TC_C, kk), idy, 1u);
           tc::mma_bf16(tm + K_D2, tc::kmaj_desc(sbase + RwSmem::VO, TC_C, kk),
                        tc::kmaj_desc(sbase + kb2[term], TC_C, kk), id2, (term | kk) != 0);
         }
@@ -1414,17 +1412,14 @@ prefill_rwkv6_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* 
     }
     tc::fence_after_sync();
     // ---- S̄ <- S̄ Diag(e^{Λ_C}) + D2 (slot-head he's columns 64 he + c) and its
-    //      bf16 terms for the next chunk; the outputs of tokens 16 hw .. 16 hw + 15
-    //      of row r, o_j = scale (S̄ r̂_j + D3 + c_j v_j), from columns 32 he + j.
-    //      The three tensor-memory loads go out together.
+    //      bf16 terms for the next chunk, every thread for its row r; then the
+    //      outputs o_j = scale (Y_j + c_j v_j) of token j = lane of slot-head
+    //      e = q4 (warps q4 < 2), values 32 hw .. 32 hw + 31, from Y's row 32 e + j
+    //      (16-byte stores when o is 16-byte aligned: a token's 32 values are
+    //      contiguous).
     {
-      const bool outs = o != nullptr && mine;   // uniform over the warp
-      uint32_t x[32], x1[16], x3[16];
+      uint32_t x[32];
       tc::tmem_ld32(tlane + K_D2 + 64 * he + 32 * hw, x);
-      if (outs) {
-        tc::tmem_ld16(tlane + K_D1 + 32 * he + 16 * hw, x1);
-        tc::tmem_ld16(tlane + K_D3 + 32 * he + 16 * hw, x3);
-      }
       tc::tmem_wait_ld(x);
       const float* ec = Ec + 64 * he + 32 * hw;
 #pragma unroll
@@ -1437,32 +1432,50 @@ prefill_rwkv6_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* 
         *reinterpret_cast<uint4*>(sm + RwSmem::SHI + off) = hv;
         *reinterpret_cast<uint4*>(sm + RwSmem::SLO + off) = lv;
       }
-      if (outs) {
-        const uint4 va = *reinterpret_cast<const uint4*>(sm + RwSmem::VO + tc::kmaj_off(r, 16 * hw, TC_C));
-        const uint4 vb = *reinterpret_cast<const uint4*>(sm + RwSmem::VO + tc::kmaj_off(r, 16 * hw + 8, TC_C));
-        float vj[16];
-        {
+      if (q4 < 2 && o != nullptr && (q4 == 0 || two)) {   // uniform over the warp
+        const int j = lane;
+        uint32_t y[32];
+        tc::tmem_ld32(tlane + K_Y + 64 * q4 + 32 * hw, y);
+        float vj[32];   // v_j of values 32 hw .. 32 hw + 31: value rows 64 e + v of V
+#pragma unroll
+        for (int c8 = 0; c8 < 4; ++c8) {
           float t8[8];
-          unpack8(va, t8);
+          unpack8(*reinterpret_cast<const uint4*>(
+                      sm + RwSmem::VO + tc::mnmaj_off(64 * q4 + 32 * hw + 8 * c8, j, TC_C)),
+                  t8);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) vj[e] = t8[e];
-          unpack8(vb, t8);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) vj[8 + e] = t8[e];
+          for (int e = 0; e < 8; ++e) vj[8 * c8 + e] = t8[e];
         }
-        tc::tmem_wait_ld16(x1);   // (complete already: the wait above covers every load)
-        tc::tmem_wait_ld16(x3);
-        const float* cbh = Cb + TC_C * he + 16 * hw;
-        const size_t ostride = (size_t)nH * RW_D;
-        const size_t obase = ((size_t)(t0 + 16 * hw) * nH + she) * RW_D + vrow;
+        const float cb = Cb[TC_C * q4 + j];
+        tc::tmem_wait_ld(y);
+        if (j < Cc) {
+          float yo[32];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          if (16 * hw + e < Cc) {
-            const float yo =
-                scale * ((__uint_as_float(x1[e]) + __uint_as_float(x3[e])) + cbh[e] * vj[e]);
-            const size_t oi = obase + (size_t)e * ostride;
-            if (out_bf16) static_cast<uint16_t*>(o)[oi] = f2bf16(yo);
-            else static_cast<float*>(o)[oi] = yo;
+          for (int i = 0; i < 32; ++i) yo[i] = scale * (__uint_as_float(y[i]) + cb * vj[i]);
+          const size_t oi = ((size_t)(t0 + j) * nH + sh0 + q4) * RW_D + 32 * hw;
+          if (out_bf16) {
+            uint16_t* ob = static_cast<uint16_t*>(o) + oi;
+            if (ovec) {
+#pragma unroll
+              for (int c8 = 0; c8 < 4; ++c8)
+                reinterpret_cast<uint4*>(ob)[c8] =
+                    make_uint4(bf16x2(yo[8 * c8], yo[8 * c8 + 1]), bf16x2(yo[8 * c8 + 2], yo[8 * c8 + 3]),
+                               bf16x2(yo[8 * c8 + 4], yo[8 * c8 + 5]), bf16x2(yo[8 * c8 + 6], yo[8 * c8 + 7]));
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) ob[i] = f2bf16(yo[i]);
+            }
+          } else {
+            float* of = static_cast<float*>(o) + oi;
+            if (ovec) {
+#pragma unroll
+              for (int c4 = 0; c4 < 8; ++c4)
+                reinterpret_cast<float4*>(of)[c4] =
+                    make_float4(yo[4 * c4], yo[4 * c4 + 1], yo[4 * c4 + 2], yo[4 * c4 + 3]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) of[i] = yo[i];
+            }
           }
         }
       }

@@ -24,6 +24,15 @@ namespace tc {
 __host__ __device__ constexpr uint32_t kmaj_off(int r, int k, int K) {
   return (uint32_t)((((r >> 3) * (K >> 3)) + (k >> 3)) * 128 + (r & 7) * 16 + (k & 7) * 2);
 }
+// The same operand stored MN-major, no swizzle: the core matrix at the same
+// place holds eight K indices as 16-byte rows, each with eight consecutive
+// rows r of the operand, so a K index's eight values of r are one 16-byte
+// store.  The shared-memory descriptor is the same as for kmaj_off (leading
+// offset 128 bytes between core matrices along K, stride offset K / 8 * 128
+// between 8-row groups); the instruction descriptor marks the operand MN-major.
+__host__ __device__ constexpr uint32_t mnmaj_off(int r, int k, int K) {
+  return (uint32_t)((((r >> 3) * (K >> 3)) + (k >> 3)) * 128 + (k & 7) * 16 + (r & 7) * 2);
+}
 
 // Shared-memory matrix descriptor: start address, leading / stride byte
 // offsets (all in 16-byte units), descriptor version 1 (bits 46-47), no swizzle.
@@ -36,10 +45,12 @@ __device__ __forceinline__ uint64_t kmaj_desc(uint32_t base, int K, int kk) {
   return sdesc(base + (uint32_t)kk * 256u, 128u, (uint32_t)(K >> 3) * 128u);
 }
 
-// Instruction descriptor of kind::f16: bf16 A and B (both K-major), fp32 D, M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
-         ((uint32_t)(M >> 4) << 24);
+// Instruction descriptor of kind::f16: bf16 A and B, fp32 D, M x N; A and B
+// K-major unless a_mn / b_mn mark them MN-major (bits 15 and 16).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn = false,
+                                                      bool b_mn = false) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // Allocate ncols TMEM columns (a power of two >= 32); one whole warp executes

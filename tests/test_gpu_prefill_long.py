@@ -125,6 +125,41 @@ def test_rwkv6_tensor_core_prefill_slot_head_pairs(B, H, T):
     ctx.close()
 
 
+@pytest.mark.parametrize("out_bf16", [False, True])
+def test_rwkv6_tensor_core_prefill_unaligned_output(out_bf16):
+    """RWKV6's tensor-core prefill writes a token's 32 values per thread as
+    16-byte vectors when o is 16-byte aligned, and element by element when it
+    is only element-aligned (the boundary's rule).  An output buffer one
+    element past a 16-byte boundary gives bitwise the same outputs and state as
+    an aligned one, and both match the oracle."""
+    from linear_attention_recurrent_gdn_gb300 import deltalog as dl
+    B, H, d, M, T = 2, 3, 64, 8, 70
+    x, S0, bonus = make_case(gen.RWKV6, B, H, d, T, seed=5600 + int(out_bf16))
+    o_ref, _, S_snap = oracle_run(gen.RWKV6, x, S0, bonus, snap=[T - 1])
+    dev = {k_: (v_.cuda() if v_ is not None else None) for k_, v_ in x.items()}
+    slots = list(range(B))
+    dt = torch.bfloat16 if out_bf16 else torch.float32
+    numel = T * B * H * d
+    res = []
+    for shift in (0, 1):
+        ctx = dl.DeltaLog(gen.RWKV6, B, H, d, d, M, out_bf16=out_bf16)
+        ctx.set_state(slots, S0.cuda())
+        ctx.set_bonus(bonus.cuda())
+        buf = torch.full((numel + 16,), float("nan"), dtype=dt, device="cuda")
+        out = buf[shift:shift + numel].view(T, B, H, d)
+        assert (out.data_ptr() % 16 == 0) == (shift == 0)
+        ctx.prefill(slots, dev["q"], dev["k"], dev["v"], dev["g"], None, out=out)
+        S = ctx.read_state(slots).cpu().reshape(B * H, d, d).numpy()
+        res.append((out.float().cpu(), S))
+        assert torch.isnan(buf[:shift]).all() and torch.isnan(buf[shift + numel:]).all()
+        ctx.close()
+    assert torch.equal(res[0][0], res[1][0])
+    assert (res[0][1] == res[1][1]).all()
+    assert rel_err(res[1][1], S_snap[0]) <= STATE_TOL
+    tol = OUT_TOL_BF16 if out_bf16 else 1e-4
+    assert max_step_rel(res[1][0].reshape(T, B * H, d).numpy(), o_ref[:T]) <= tol
+
+
 @pytest.mark.parametrize("T", [33, 64, 97, 130])
 @pytest.mark.parametrize("op", [gen.GDN, gen.KDA])
 def test_tensor_core_prefill_chunk_counts(op, T):
