@@ -59,7 +59,7 @@ struct TcSmem {
   static constexpr uint32_t WLO = WHI + TC_D * TC_C * 2;   // W lo
   static constexpr uint32_t UHI = WLO + TC_D * TC_C * 2;   // U hi [v (128)] x [i (32)], K-major
   static constexpr uint32_t ULO = UHI + TC_D * TC_C * 2;   // U lo
-  // doubled: K^T (K as [i (128)] x [j (32)], K-major), A hi / lo ([j] x [i], K-major),
+  // doubled: K^T (K as [i (128)] x [j (32)], MN-major), A hi / lo ([j] x [i], K-major),
   // v_j[r] (bf16 rows of VP), A_kk (fp32 [32][AP]), Λ_j, e^{Λ_j}, e^{Λ_C-Λ_j}, β_j ([4][32])
   static constexpr uint32_t KT_SZ = TC_D * TC_C * 2, A_SZ = TC_C * TC_C * 2, VS_SZ = TC_C * VP * 2,
                             AKK_SZ = TC_C * AP * 4, SC_SZ = 4 * TC_C * 4;
@@ -101,29 +101,6 @@ __device__ __forceinline__ void chunk_piece(int idx, int& j, int& cv) {
   const int rest = idx >> 5;
   j = (idx & 7) + 8 * (rest & 3);
   cv = ((idx >> 3) & 3) + 4 * (rest >> 2);
-}
-
-// The four 32-bit words of a piece rotated by `rot` (word i <- word i + rot,
-// mod 4), so that element t of the result is element t + 2 rot (mod 8).
-__device__ __forceinline__ uint4 rot_words(const uint4 w, int rot) {
-  uint32_t a0 = w.x, a1 = w.y, a2 = w.z, a3 = w.w;
-  if (rot & 1) {
-    const uint32_t t = a0;
-    a0 = a1; a1 = a2; a2 = a3; a3 = t;
-  }
-  if (rot & 2) {
-    uint32_t t = a0;
-    a0 = a2; a2 = t;
-    t = a1;
-    a1 = a3; a3 = t;
-  }
-  return make_uint4(a0, a1, a2, a3);
-}
-
-// A bf16 value of piece word w (element t of 8) as its 16 bits.
-__device__ __forceinline__ uint16_t piece_bits(const uint4 w, int t) {
-  const uint32_t x = (t >> 1) == 0 ? w.x : (t >> 1) == 1 ? w.y : (t >> 1) == 2 ? w.z : w.w;
-  return (uint16_t)((t & 1) ? (x >> 16) : (x & 0xffffu));
 }
 
 // One chunk's k, q, v (bf16) and g, β in the registers of the 128 threads that
@@ -170,22 +147,15 @@ struct TcStage {
     }
   }
 
-  // k into the transposed K^T operand of set `set`, v into its VS
+  // k into the K^T operand of set `set` (MN-major: k_j[8 cv .. 8 cv + 7] is
+  // one 16-byte row of a core matrix), v into its VS
   __device__ __forceinline__ void store_rest(unsigned char* sm, uint32_t set, int ptid) const {
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       int j, cv;
       chunk_piece(ptid + e * 128, j, cv);
       *reinterpret_cast<uint4*>(sm + set + TcSmem::VS + (j * VP + cv * 8) * 2) = v[e];
-      // k_j[i], i = 8 cv + t', at K^T row i, column j; lane group g of the warp
-      // stores t' = t + 2 g (mod 8) at step t, so each store reaches distinct banks
-      const int rot = (ptid >> 3) & 3;
-      const uint4 kr = rot_words(k[e], rot);
-      const uint32_t base = tc::kmaj_off(cv * 8, j, TC_C);
-#pragma unroll
-      for (int t = 0; t < 8; ++t)
-        *reinterpret_cast<uint16_t*>(sm + set + TcSmem::KT + base + ((t + 2 * rot) & 7) * 16) =
-            piece_bits(kr, t);
+      *reinterpret_cast<uint4*>(sm + set + TcSmem::KT + tc::mnmaj_off(cv * 8, j, TC_C)) = k[e];
     }
   }
 };
@@ -437,7 +407,8 @@ prefill_gdn_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* __
     // ---- D2 = (W_hi + W_lo) K and D3 = U_hi A_hi^T + U_lo A_hi^T + U_hi A_lo^T
     if (tid == 0) {
       tc::fence_after_sync();
-      constexpr uint32_t id2 = tc::idesc_bf16_f32(128, 128), id3 = tc::idesc_bf16_f32(128, 32);
+      constexpr uint32_t id2 = tc::idesc_bf16_f32(128, 128, false, true);   // K^T MN-major
+      constexpr uint32_t id3 = tc::idesc_bf16_f32(128, 32);
       const uint32_t kt = sbase + set + TcSmem::KT;
       const uint32_t ahi = sbase + set + TcSmem::AHI, alo = sbase + set + TcSmem::ALO;
 #pragma unroll
@@ -582,7 +553,7 @@ struct KdaSmem {
   static constexpr uint32_t BLO = BHI + TC_D * TC_D * 2;
   static constexpr uint32_t KBHI = BLO + TC_D * TC_D * 2;   // k̄ hi [32 x 128] K-major
   static constexpr uint32_t KBLO = KBHI + TC_C * TC_D * 2;
-  static constexpr uint32_t KTHI = KBLO + TC_C * TC_D * 2;  // k̃ hi as [c (128)] x [j (32)]
+  static constexpr uint32_t KTHI = KBLO + TC_C * TC_D * 2;  // k̃ hi as [c (128)] x [j (32)], MN-major
   static constexpr uint32_t KTLO = KTHI + TC_D * TC_C * 2;
   static constexpr uint32_t UHI = KTLO + TC_D * TC_C * 2;   // U hi [v (128)] x [i (32)]
   static constexpr uint32_t ULO = UHI + TC_D * TC_C * 2;
@@ -778,16 +749,10 @@ prefill_kda_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* __
       *reinterpret_cast<uint4*>(sm + KdaSmem::KBHI + okq) = hv;
       *reinterpret_cast<uint4*>(sm + KdaSmem::KBLO + okq) = lv;
       split8(kt, hv, lv);
-      // k̃_j[c] at row c = 8 cv + t', column j, t' = t + 2 g (mod 8) for lane group g
-      const int rot = (tid >> 3) & 3;
-      const uint4 th = rot_words(hv, rot), tl = rot_words(lv, rot);
-      const uint32_t base = tc::kmaj_off(cv * 8, j, TC_C);
-#pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        const uint32_t off = base + ((t + 2 * rot) & 7) * 16;
-        *reinterpret_cast<uint16_t*>(sm + KdaSmem::KTHI + off) = piece_bits(th, t);
-        *reinterpret_cast<uint16_t*>(sm + KdaSmem::KTLO + off) = piece_bits(tl, t);
-      }
+      // k̃_j[8 cv .. 8 cv + 7]: one 16-byte row of a core matrix of the MN-major k̃
+      const uint32_t otc = tc::mnmaj_off(cv * 8, j, TC_C);
+      *reinterpret_cast<uint4*>(sm + KdaSmem::KTHI + otc) = hv;
+      *reinterpret_cast<uint4*>(sm + KdaSmem::KTLO + otc) = lv;
     }
     tc::fence_smem_to_async();   // S̄ terms and the decayed operands, for the tensor cores
     tc::fence_before_sync();
@@ -921,7 +886,8 @@ prefill_kda_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* __
     // ---- D2 = U k̃ and D3 = U A^T, three terms each
     if (tid == 0) {
       tc::fence_after_sync();
-      constexpr uint32_t id2 = tc::idesc_bf16_f32(128, 128), id3 = tc::idesc_bf16_f32(128, 32);
+      constexpr uint32_t id2 = tc::idesc_bf16_f32(128, 128, false, true);   // k̃ MN-major
+      constexpr uint32_t id3 = tc::idesc_bf16_f32(128, 32);
       const uint32_t ua[3] = {KdaSmem::UHI, KdaSmem::ULO, KdaSmem::UHI};
       const uint32_t kb[3] = {KdaSmem::KTHI, KdaSmem::KTHI, KdaSmem::KTLO};
       const uint32_t ab[3] = {KdaSmem::AHI, KdaSmem::AHI, KdaSmem::ALO};
