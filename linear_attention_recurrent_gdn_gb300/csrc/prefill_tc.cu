@@ -995,7 +995,7 @@ prefill_kda_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* __
 // stay finite while the chunk's log-decay stays above -60 in every channel,
 // as in KDA's kernel; a chunk below it forms A directly on the CUDA cores.
 constexpr int RW_D = 64;
-constexpr uint32_t RW_COLS = 512;   // TMEM: D0 [0, 64), Y [64, 192), D2 [256, 384)
+constexpr uint32_t RW_COLS = 512;   // TMEM: [D0 | Y] of even chunks [0, 192), of odd ones [192, 384), D2 [384, 512)
 constexpr int RW_LT = TC_C + 1;   // fp32 Λ, channel-major: column 64 e + c at col * RW_LT, token j at + j
 
 struct RwSmem {
@@ -1009,8 +1009,9 @@ struct RwSmem {
   static constexpr uint32_t RLO = RHI + 128 * RW_D * 2;
   static constexpr uint32_t KTHI = RLO + 128 * RW_D * 2;      // k̃ [128 rows (64 e + c)] x [32 tokens], MN-major
   static constexpr uint32_t KTLO = KTHI + 128 * TC_C * 2;
-  static constexpr uint32_t VO = KTLO + 128 * TC_C * 2;       // V [128 rows (64 e + v)] x [32 tokens], MN-major
-  static constexpr uint32_t AHI = VO + 128 * TC_C * 2;        // A [64 rows (32 e + j)] x [32 (s)]
+  static constexpr uint32_t VO = KTLO + 128 * TC_C * 2;       // V [128 rows (64 e + v)] x [32 tokens], MN-major,
+  static constexpr uint32_t VO_SZ = 128 * TC_C * 2;           //   two (even and odd chunks)
+  static constexpr uint32_t AHI = VO + 2 * VO_SZ;             // A [64 rows (32 e + j)] x [32 (s)]
   static constexpr uint32_t ALO = AHI + 64 * TC_C * 2;
   static constexpr uint32_t LP = ALO + 64 * TC_C * 2;         // g, then Λ_j, fp32 [128][RW_LT]
   static constexpr uint32_t ER = LP + 128 * RW_LT * 4;        // e^{Λ_{j-1}}, same layout
@@ -1019,8 +1020,8 @@ struct RwSmem {
   static constexpr uint32_t EC = HT + 128 * 4;                // e^{Λ_C} [128]
   static constexpr uint32_t UB = EC + 128 * 4;                // bonus u of both heads [128]
   static constexpr uint32_t CBP = UB + 128 * 4;               // c_j partials [2][32][8]
-  static constexpr uint32_t CB = CBP + 2 * TC_C * 8 * 4;      // c_j [2][32]
-  static constexpr uint32_t BAR = CB + 2 * TC_C * 4;          // 2 mbarriers, TMEM base, ok flag
+  static constexpr uint32_t CB = CBP + 2 * TC_C * 8 * 4;      // c_j [2][32], two (even and odd chunks)
+  static constexpr uint32_t BAR = CB + 2 * 2 * TC_C * 4;      // 2 mbarriers, TMEM base, ok flag
   static constexpr uint32_t BYTES = BAR + 32;
 };
 static_assert(RwSmem::BYTES <= 227 * 1024, "shared memory");
@@ -1107,12 +1108,11 @@ prefill_rwkv6_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* 
   float* Ec = reinterpret_cast<float*>(sm + RwSmem::EC);
   float* Ub = reinterpret_cast<float*>(sm + RwSmem::UB);
   float* Cbp = reinterpret_cast<float*>(sm + RwSmem::CBP);
-  float* Cb = reinterpret_cast<float*>(sm + RwSmem::CB);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + RwSmem::BAR + 16);
   int32_t* ok_flag = reinterpret_cast<int32_t*>(sm + RwSmem::BAR + 20);
   const uint32_t sbase = smem_u32(sm);
   const uint32_t bar1 = sbase + RwSmem::BAR, bar2 = sbase + RwSmem::BAR + 8;
-  constexpr uint32_t K_D0 = 0, K_Y = 64, K_D2 = 256;   // TMEM columns
+  constexpr uint32_t K_D0 = 0, K_Y = 64, K_SET = 192, K_D2 = 384;   // TMEM columns
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int q4 = warp & 3, hw = warp >> 2;
@@ -1123,7 +1123,6 @@ prefill_rwkv6_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* 
   const bool two = sh0 + 1 < nH;
   const int she = sh0 + he;
   const bool mine = he == 0 || two;      // this thread's row belongs to a slot-head of the batch
-  const bool ovec = (reinterpret_cast<uintptr_t>(o) & 15u) == 0;
   auto state_of = [&](int sh) {
     const int row = sh / a.H, h = sh - row * a.H;
     return a.Sbar + ((size_t)a.items[row].slot * a.H + h) * RW_D * RW_D;
@@ -1178,11 +1177,70 @@ prefill_rwkv6_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* 
   tc::fence_after_sync();
   const uint32_t tm = *tmem_slot;
   const uint32_t tlane = tm + ((uint32_t)(32 * q4) << 16);
+  const bool ovec = (reinterpret_cast<uintptr_t>(o) & 15u) == 0;
+  // The outputs o_j = scale (Y_j + c_j v_j) of a finished chunk (the TMEM, V
+  // and c_j sets bo) for token j = lane of slot-head e = q4 (warps q4 < 2),
+  // values 32 hw .. 32 hw + 31, from Y's row 32 e + j; 16-byte stores when o is
+  // 16-byte aligned (a token's 32 values are contiguous).  Chunk c - 1's run
+  // while chunk c's first MMA group does.
+  auto emit = [&](int bo, int t0o, int Cco) {
+    if (q4 < 2 && o != nullptr && (q4 == 0 || two)) {   // uniform over the warp
+      const int j = lane;
+      uint32_t y[32];
+      tc::tmem_ld32(tlane + K_SET * bo + K_Y + 64 * q4 + 32 * hw, y);
+      float vj[32];   // v_j of values 32 hw .. 32 hw + 31: value rows 64 e + v of V
+#pragma unroll
+      for (int c8 = 0; c8 < 4; ++c8) {
+        float t8[8];
+        unpack8(*reinterpret_cast<const uint4*>(sm + RwSmem::VO + RwSmem::VO_SZ * bo +
+                                                tc::mnmaj_off(64 * q4 + 32 * hw + 8 * c8, j, TC_C)),
+                t8);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) vj[8 * c8 + e] = t8[e];
+      }
+      const float cb = reinterpret_cast<const float*>(sm + RwSmem::CB)[2 * TC_C * bo + TC_C * q4 + j];
+      tc::tmem_wait_ld(y);
+      if (j < Cco) {
+        float yo[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) yo[i] = scale * (__uint_as_float(y[i]) + cb * vj[i]);
+        const size_t oi = ((size_t)(t0o + j) * nH + sh0 + q4) * RW_D + 32 * hw;
+        if (out_bf16) {
+          uint16_t* ob = static_cast<uint16_t*>(o) + oi;
+          if (ovec) {
+#pragma unroll
+            for (int c8 = 0; c8 < 4; ++c8)
+              reinterpret_cast<uint4*>(ob)[c8] =
+                  make_uint4(bf16x2(yo[8 * c8], yo[8 * c8 + 1]), bf16x2(yo[8 * c8 + 2], yo[8 * c8 + 3]),
+                             bf16x2(yo[8 * c8 + 4], yo[8 * c8 + 5]), bf16x2(yo[8 * c8 + 6], yo[8 * c8 + 7]));
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ob[i] = f2bf16(yo[i]);
+          }
+        } else {
+          float* of = static_cast<float*>(o) + oi;
+          if (ovec) {
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4)
+              reinterpret_cast<float4*>(of)[c4] =
+                  make_float4(yo[4 * c4], yo[4 * c4 + 1], yo[4 * c4 + 2], yo[4 * c4 + 3]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) of[i] = yo[i];
+          }
+        }
+      }
+    }
+  };
+  // Thread 64 (a warp without outputs) issues the MMAs and waits for them.
+  constexpr int MMA_TID = 64;
   bool ok = true;
   int chunk = 0;
   for (int t0 = 0; t0 < T && ok; t0 += TC_C, ++chunk) {
     const int Cc = (T - t0) < TC_C ? (T - t0) : TC_C;
     const uint32_t par = (uint32_t)chunk & 1u;
+    const int b = chunk & 1;
+    const uint32_t vo = RwSmem::VO + RwSmem::VO_SZ * b, tb = K_SET * b;
     // ---- stage g; Λ = inclusive scan of g down each of the 128 columns (64 e + c;
     //      padding tokens and a missing second slot-head have g = 0); the vote:
     //      does every column's chunk log-decay stay above the floor?
@@ -1269,13 +1327,13 @@ prefill_rwkv6_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* 
       const uint32_t ocol = tc::mnmaj_off(col0, j, TC_C);   // rows col0 .. col0 + 7 of token j
       *reinterpret_cast<uint4*>(sm + RwSmem::KTHI + ocol) = hv;
       *reinterpret_cast<uint4*>(sm + RwSmem::KTLO + ocol) = lv;
-      *reinterpret_cast<uint4*>(sm + RwSmem::VO + ocol) = st.v[e];
+      *reinterpret_cast<uint4*>(sm + vo + ocol) = st.v[e];
     }
     tc::fence_smem_to_async();   // S̄ terms and the chunk's operands, for the tensor cores
     tc::fence_before_sync();
     __syncthreads();
     // ---- [D0 | Y] = [r̂; 0] [k̄; S̄]^T, three terms (a direct chunk's k̄ is zero)
-    if (tid == 0) {
+    if (tid == MMA_TID) {
       tc::fence_after_sync();
       constexpr uint32_t id192 = tc::idesc_bf16_f32(128, 192);
       const uint32_t ra[3] = {RwSmem::RHI, RwSmem::RLO, RwSmem::RHI};
@@ -1284,14 +1342,17 @@ prefill_rwkv6_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* 
       for (int term = 0; term < 3; ++term)
 #pragma unroll
         for (int kk = 0; kk < RW_D / 16; ++kk)
-          tc::mma_bf16(tm + K_D0, tc::kmaj_desc(sbase + ra[term], RW_D, kk),
+          tc::mma_bf16(tm + tb + K_D0, tc::kmaj_desc(sbase + ra[term], RW_D, kk),
                        tc::kmaj_desc(sbase + kb3[term], RW_D, kk), id192, (term | kk) != 0);
       tc::mma_commit(bar1);
     }
-    // the bonus sums c_j, in a fixed order
-    if (tid < 2 * TC_C) {
-      const float* p = Cbp + tid * 8;
-      Cb[tid] = ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
+    if (chunk > 0) emit(b ^ 1, t0 - TC_C, TC_C);   // (only the last chunk is ragged)
+    // the bonus sums c_j (warps 3 and 7), in a fixed order
+    if (warp == 3 || warp == 7) {
+      const int i = (warp == 3 ? 0 : TC_C) + lane;
+      const float* p = Cbp + i * 8;
+      reinterpret_cast<float*>(sm + RwSmem::CB)[2 * TC_C * b + i] =
+          ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
     }
     auto put_a = [&](int row, int s, float av) {   // A's bf16 terms, row 32 e + j, column s
       const uint32_t hv = bf16x2(av, 0.f) & 0xffffu;
@@ -1322,7 +1383,7 @@ prefill_rwkv6_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* 
       const int Cn = (T - t0 - TC_C) < TC_C ? (T - t0 - TC_C) : TC_C;
       st.load(r_in, k_in, v_in, g, t0 + TC_C, Cn, (size_t)nH, sh0, two, tid);
     }
-    if (tid == 0 && !mbar_wait(bar1, par, status, DEV_TIMEOUT_MMA)) *ok_flag = -1;
+    if (tid == MMA_TID && !mbar_wait(bar1, par, status, DEV_TIMEOUT_MMA)) *ok_flag = -1;
     __syncthreads();
     if (*ok_flag != 1) {
       ok = false;
@@ -1334,7 +1395,7 @@ prefill_rwkv6_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* 
     //      the diagonal
     if (!direct && q4 < 2) {
       uint32_t x[16];
-      tc::tmem_ld16(tlane + K_D0 + 32 * q4 + 16 * hw, x);
+      tc::tmem_ld16(tlane + tb + K_D0 + 32 * q4 + 16 * hw, x);
       tc::tmem_wait_ld16(x);
       const int j = lane, s0 = 16 * hw;
       float w[16];
@@ -1353,7 +1414,7 @@ prefill_rwkv6_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* 
     tc::fence_before_sync();
     __syncthreads();
     // ---- Y += [A; *] V^T and D2 = V k̃, two terms each (V is exact in bf16)
-    if (tid == 0) {
+    if (tid == MMA_TID) {
       tc::fence_after_sync();
       constexpr uint32_t idy = tc::idesc_bf16_f32(128, 128, false, true);   // V MN-major
       constexpr uint32_t id2 = tc::idesc_bf16_f32(128, 128, true, true);    // V, k̃ MN-major
@@ -1363,14 +1424,14 @@ prefill_rwkv6_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* 
       for (int term = 0; term < 2; ++term)
 #pragma unroll
         for (int kk = 0; kk < TC_C / 16; ++kk) {
-          tc::mma_bf16(tm + K_Y, tc::kmaj_desc(sbase + ab[term], TC_C, kk),
-                       tc::kmaj_desc(sbase + RwSmem::VO, TC_C, kk), idy, 1u);
-          tc::mma_bf16(tm + K_D2, tc::kmaj_desc(sbase + RwSmem::VO, TC_C, kk),
+          tc::mma_bf16(tm + tb + K_Y, tc::kmaj_desc(sbase + ab[term], TC_C, kk),
+                       tc::kmaj_desc(sbase + vo, TC_C, kk), idy, 1u);
+          tc::mma_bf16(tm + K_D2, tc::kmaj_desc(sbase + vo, TC_C, kk),
                        tc::kmaj_desc(sbase + kb2[term], TC_C, kk), id2, (term | kk) != 0);
         }
       tc::mma_commit(bar2);
     }
-    if (tid == 0 && !mbar_wait(bar2, par, status, DEV_TIMEOUT_MMA)) *ok_flag = -2;
+    if (tid == MMA_TID && !mbar_wait(bar2, par, status, DEV_TIMEOUT_MMA)) *ok_flag = -2;
     __syncthreads();
     if (*ok_flag != 1) {
       ok = false;
@@ -1378,11 +1439,8 @@ prefill_rwkv6_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* 
     }
     tc::fence_after_sync();
     // ---- S̄ <- S̄ Diag(e^{Λ_C}) + D2 (slot-head he's columns 64 he + c) and its
-    //      bf16 terms for the next chunk, every thread for its row r; then the
-    //      outputs o_j = scale (Y_j + c_j v_j) of token j = lane of slot-head
-    //      e = q4 (warps q4 < 2), values 32 hw .. 32 hw + 31, from Y's row 32 e + j
-    //      (16-byte stores when o is 16-byte aligned: a token's 32 values are
-    //      contiguous).
+    //      bf16 terms for the next chunk, every thread for its row r (the
+    //      outputs follow under the next chunk's first MMA group)
     {
       uint32_t x[32];
       tc::tmem_ld32(tlane + K_D2 + 64 * he + 32 * hw, x);
@@ -1398,58 +1456,15 @@ prefill_rwkv6_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* 
         *reinterpret_cast<uint4*>(sm + RwSmem::SHI + off) = hv;
         *reinterpret_cast<uint4*>(sm + RwSmem::SLO + off) = lv;
       }
-      if (q4 < 2 && o != nullptr && (q4 == 0 || two)) {   // uniform over the warp
-        const int j = lane;
-        uint32_t y[32];
-        tc::tmem_ld32(tlane + K_Y + 64 * q4 + 32 * hw, y);
-        float vj[32];   // v_j of values 32 hw .. 32 hw + 31: value rows 64 e + v of V
-#pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8) {
-          float t8[8];
-          unpack8(*reinterpret_cast<const uint4*>(
-                      sm + RwSmem::VO + tc::mnmaj_off(64 * q4 + 32 * hw + 8 * c8, j, TC_C)),
-                  t8);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) vj[8 * c8 + e] = t8[e];
-        }
-        const float cb = Cb[TC_C * q4 + j];
-        tc::tmem_wait_ld(y);
-        if (j < Cc) {
-          float yo[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) yo[i] = scale * (__uint_as_float(y[i]) + cb * vj[i]);
-          const size_t oi = ((size_t)(t0 + j) * nH + sh0 + q4) * RW_D + 32 * hw;
-          if (out_bf16) {
-            uint16_t* ob = static_cast<uint16_t*>(o) + oi;
-            if (ovec) {
-#pragma unroll
-              for (int c8 = 0; c8 < 4; ++c8)
-                reinterpret_cast<uint4*>(ob)[c8] =
-                    make_uint4(bf16x2(yo[8 * c8], yo[8 * c8 + 1]), bf16x2(yo[8 * c8 + 2], yo[8 * c8 + 3]),
-                               bf16x2(yo[8 * c8 + 4], yo[8 * c8 + 5]), bf16x2(yo[8 * c8 + 6], yo[8 * c8 + 7]));
-            } else {
-#pragma unroll
-              for (int i = 0; i < 32; ++i) ob[i] = f2bf16(yo[i]);
-            }
-          } else {
-            float* of = static_cast<float*>(o) + oi;
-            if (ovec) {
-#pragma unroll
-              for (int c4 = 0; c4 < 8; ++c4)
-                reinterpret_cast<float4*>(of)[c4] =
-                    make_float4(yo[4 * c4], yo[4 * c4 + 1], yo[4 * c4 + 2], yo[4 * c4 + 3]);
-            } else {
-#pragma unroll
-              for (int i = 0; i < 32; ++i) of[i] = yo[i];
-            }
-          }
-        }
-      }
     }
     tc::fence_before_sync();
     __syncthreads();
   }
-  if (!ok && tid == 0) mbar_drain(*ok_flag == -1 ? bar1 : bar2, (uint32_t)chunk & 1u);
+  if (ok) {   // the last chunk's outputs
+    const int last = (T - 1) / TC_C;
+    emit(last & 1, TC_C * last, T - TC_C * last);
+  }
+  if (!ok && tid == MMA_TID) mbar_drain(*ok_flag == -1 ? bar1 : bar2, (uint32_t)chunk & 1u);
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) {
