@@ -1013,7 +1013,7 @@ struct RwSmem {
   static constexpr uint32_t VO_SZ = 128 * TC_C * 2;           //   two (even and odd chunks)
   static constexpr uint32_t AHI = VO + 2 * VO_SZ;             // A [64 rows (32 e + j)] x [32 (s)]
   static constexpr uint32_t ALO = AHI + 64 * TC_C * 2;
-  static constexpr uint32_t LP = ALO + 64 * TC_C * 2;         // g, then Λ_j, fp32 [128][RW_LT]
+  static constexpr uint32_t LP = ALO + 64 * TC_C * 2;         // g, then (direct chunks) Λ_j, fp32 [128][RW_LT]
   static constexpr uint32_t ER = LP + 128 * RW_LT * 4;        // e^{Λ_{j-1}}, same layout
   static constexpr uint32_t EB = ER + 128 * RW_LT * 4;        // e^{-Λ_j}, same layout
   static constexpr uint32_t HT = EB + 128 * RW_LT * 4;        // Λ_15 of each column [128]
@@ -1251,10 +1251,11 @@ prefill_rwkv6_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* 
     st.store_g(sm, tid);
     __syncthreads();
     float lc = 0.f;
+    const int cl = tid & 127, hf = tid >> 7;
+    float* col = Lp + cl * RW_LT + 16 * hf;
+    float lam[16];
+    float pre;
     {
-      const int cl = tid & 127, hf = tid >> 7;
-      float* col = Lp + cl * RW_LT + 16 * hf;
-      float lam[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         lc += col[j];
@@ -1262,14 +1263,13 @@ prefill_rwkv6_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* 
       }
       if (hf == 0) Ht[cl] = lc;
       __syncthreads();
-      const float pre = hf ? Ht[cl] : 0.f;   // Λ at the half's first token minus one
+      pre = hf ? Ht[cl] : 0.f;   // Λ at the half's first token minus one
       float* er = Er + cl * RW_LT + 16 * hf;
       float* eb = Eb + cl * RW_LT + 16 * hf;
       float prev = pre;
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const float l = pre + lam[j];
-        col[j] = l;
         er[j] = __expf(prev);   // Λ_{j-1} <= 0
         eb[j] = __expf(-l);     // <= e^{60} while the vote passes
         prev = l;
@@ -1278,6 +1278,11 @@ prefill_rwkv6_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* 
       if (hf) Ec[cl] = expf(lc);
     }
     const bool direct = __syncthreads_or(tid >= 128 && !(lc >= KDA_FACTOR_FLOOR)) != 0;
+    if (direct) {   // Λ itself, over the staged g, for the direct path's exponents
+#pragma unroll
+      for (int j = 0; j < 16; ++j) col[j] = pre + lam[j];
+      __syncthreads();
+    }
     // ---- operands, 8 channels of one token of one slot-head per piece (r, k, v
     //      from registers), one 16-byte store each: r̂ and k̄ (hi, lo) K-major as
     //      token rows; k̃ (hi, lo) and V MN-major, whose core-matrix rows are a
