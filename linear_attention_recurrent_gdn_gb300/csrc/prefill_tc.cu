@@ -1013,7 +1013,7 @@ struct RwSmem {
   static constexpr uint32_t VO_SZ = 128 * TC_C * 2;           //   two (even and odd chunks)
   static constexpr uint32_t AHI = VO + 2 * VO_SZ;             // A [64 rows (32 e + j)] x [32 (s)]
   static constexpr uint32_t ALO = AHI + 64 * TC_C * 2;
-  static constexpr uint32_t LP = ALO + 64 * TC_C * 2;         // g, then (direct chunks) Λ_j, fp32 [128][RW_LT]
+  static constexpr uint32_t LP = ALO + 64 * TC_C * 2;         // Λ_j of direct chunks, fp32 [128][RW_LT]
   static constexpr uint32_t ER = LP + 128 * RW_LT * 4;        // e^{Λ_{j-1}}, same layout
   static constexpr uint32_t EB = ER + 128 * RW_LT * 4;        // e^{-Λ_j}, same layout
   static constexpr uint32_t HT = EB + 128 * RW_LT * 4;        // Λ_15 of each column [128]
@@ -1033,13 +1033,16 @@ static_assert(RwSmem::ALO == RwSmem::AHI + 64 * TC_C * 2 && RwSmem::LP == RwSmem
               RwSmem::LP + 64 * TC_C * 2 <= RwSmem::BYTES, "A's padding rows stay inside the block");
 
 // One chunk's r, k, v (bf16) and g of the CTA's two slot-heads, in registers
-// between the global loads and the shared-memory stores.  The two slot-heads'
-// rows of a token are adjacent in the token-major inputs, so a token's 128
-// values (64 e + c) are one contiguous run; a second slot-head past the batch
-// (`two` false) loads zeros.
+// between the global loads and their use.  The two slot-heads' rows of a token
+// are adjacent in the token-major inputs, so a token's 128 values (64 e + c)
+// are one contiguous run; a second slot-head past the batch (`two` false)
+// loads zeros.  r, k, v come as pieces (8 channels of one token); g comes in
+// the scan's layout: thread (half hf, column cl = 64 e + c) holds g of tokens
+// 16 hf .. 16 hf + 15 of its column (for one token the 128 columns' loads are
+// one contiguous 512-byte run).
 struct RwStage {
   uint4 r[2], k[2], v[2];
-  float4 gv[4];
+  float gs[16];
 
   __device__ __forceinline__ void load(const uint16_t* __restrict__ rg, const uint16_t* __restrict__ kg,
                                        const uint16_t* __restrict__ vg, const float* __restrict__ gg,
@@ -1057,40 +1060,12 @@ struct RwStage {
         r[e] = k[e] = v[e] = make_uint4(0u, 0u, 0u, 0u);
       }
     }
+    const int cl = tid & 127, hf = tid >> 7;
+    const bool col_ok = two || cl < RW_D;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int idx = tid + e * TC_THREADS, j = idx >> 5, c4 = idx & 31;
-      gv[e] = (j < Cc && (two || c4 < 16))
-                  ? *reinterpret_cast<const float4*>(gg + ((size_t)(t0 + j) * nH + sh0) * RW_D + 4 * c4)
-                  : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-  }
-
-  // g channel-major (column 64 e + c, token j at column * RW_LT + j).  Lane
-  // group (lane / 8) of a warp starts at component lane / 8 of its quad, so
-  // that each store's 32 lanes reach 32 distinct banks.
-  __device__ __forceinline__ void store_g(unsigned char* sm, int tid) const {
-    float* Lp = reinterpret_cast<float*>(sm + RwSmem::LP);
-    const int rot = (tid >> 3) & 3;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int idx = tid + e * TC_THREADS, j = idx >> 5, c4 = idx & 31;
-      float x0 = gv[e].x, x1 = gv[e].y, x2 = gv[e].z, x3 = gv[e].w;   // rotated by rot
-      if (rot & 1) {
-        const float t = x0;
-        x0 = x1; x1 = x2; x2 = x3; x3 = t;
-      }
-      if (rot & 2) {
-        float t = x0;
-        x0 = x2; x2 = t;
-        t = x1;
-        x1 = x3; x3 = t;
-      }
-      float* col = Lp + 4 * c4 * RW_LT + j;
-      col[((0 + rot) & 3) * RW_LT] = x0;
-      col[((1 + rot) & 3) * RW_LT] = x1;
-      col[((2 + rot) & 3) * RW_LT] = x2;
-      col[((3 + rot) & 3) * RW_LT] = x3;
+    for (int j = 0; j < 16; ++j) {
+      const int jj = 16 * hf + j;
+      gs[j] = (jj < Cc && col_ok) ? gg[((size_t)(t0 + jj) * nH + sh0) * RW_D + cl] : 0.f;
     }
   }
 };
@@ -1241,15 +1216,13 @@ prefill_rwkv6_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* 
     const uint32_t par = (uint32_t)chunk & 1u;
     const int b = chunk & 1;
     const uint32_t vo = RwSmem::VO + RwSmem::VO_SZ * b, tb = K_SET * b;
-    // ---- stage g; Λ = inclusive scan of g down each of the 128 columns (64 e + c;
-    //      padding tokens and a missing second slot-head have g = 0); the vote:
-    //      does every column's chunk log-decay stay above the floor?
-    //      Thread (half hf, column cl) scans tokens 16 hf .. 16 hf + 15 of its
-    //      column, the second half then adds the first half's total, and each
-    //      thread forms its tokens' decay factors e^{Λ_{j-1}} (for r̂) and
-    //      e^{-Λ_j} (for k̄ and k̃; only used while the vote passes).
-    st.store_g(sm, tid);
-    __syncthreads();
+    // ---- Λ = inclusive scan of g down each of the 128 columns (64 e + c; padding
+    //      tokens and a missing second slot-head have g = 0); the vote: does every
+    //      column's chunk log-decay stay above the floor?  Thread (half hf, column
+    //      cl) scans tokens 16 hf .. 16 hf + 15 of its column from its registers,
+    //      the second half then adds the first half's total, and each thread forms
+    //      its tokens' decay factors e^{Λ_{j-1}} (for r̂) and e^{-Λ_j} (for k̄ and
+    //      k̃; only used while the vote passes).
     float lc = 0.f;
     const int cl = tid & 127, hf = tid >> 7;
     float* col = Lp + cl * RW_LT + 16 * hf;
@@ -1258,7 +1231,7 @@ prefill_rwkv6_tc_kernel(const __grid_constant__ SlotListArgs a, const uint16_t* 
     {
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
-        lc += col[j];
+        lc += st.gs[j];
         lam[j] = lc;
       }
       if (hf == 0) Ht[cl] = lc;
