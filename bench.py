@@ -691,6 +691,9 @@ def run_ours(args):
             result["workloads"][name] = measure_decode(WORKLOADS[name], args, dist, world, rank,
                                                        local, dev, stream)
         result["workloads"]["fork"] = measure_fork(args, dist, world, rank, local, dev, stream)
+        for name in PREFILL:   # chunked prefill of 512-token contexts at the decode shapes
+            result["workloads"][name] = measure_prefill(name, args, dist, world, rank, local,
+                                                        dev, stream)
 
     # ---- CPU baseline (rank 0, N = 1 only)
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -852,11 +855,22 @@ def timed_steps(one, args, dist, local, dev, stream):
 def run_prefill(args):
     """Chunked prefill: one bench step is one dl_prefill call that feeds all B
     slots a T-token context (inputs resident in HBM)."""
-    import torch
     rank, world, dist, local, dev, stream = gpu_setup()
+    result = measure_prefill(args.workload, args, dist, world, rank, local, dev, stream)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def measure_prefill(name, args, dist, world, rank, local, dev, stream):
+    """One prefill workload (a PREFILL name) in its own timed region; returns its
+    JSON object."""
+    import torch
     from linear_attention_recurrent_gdn_gb300 import deltalog as dl
     from linear_attention_recurrent_gdn_gb300 import inputs as gen
-    w = WORKLOADS[PREFILL[args.workload]]
+    w = WORKLOADS[PREFILL[name]]
     op, B, H, d, M = w["op"], args.B or w["B"], w["H"], w["d"], w["M"]
     T = args.tokens or w["tokens"]
     seed = w["seed"] + 7919 * rank
@@ -909,12 +923,10 @@ def run_prefill(args):
               "roofline": roofline,
               "clocks": clocks,
               "gpu_launches": args.steps * clocks.get("reps", 1) * ((B + 1023) // 1024)}
-    if rank == 0:
-        print(json.dumps(result), flush=True)
     ctx.close()
-    if dist is not None:
-        dist.destroy_process_group()
-    return 0
+    del x, out
+    torch.cuda.empty_cache()
+    return result
 
 
 def hbm_peak():
